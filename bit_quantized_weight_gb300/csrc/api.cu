@@ -1,0 +1,241 @@
+// api.cu -- the extern "C" entry points of libqgemv: argument validation,
+// kernel selection and launch on the caller's stream. Nothing here allocates
+// device memory; the only device state is the status word below.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "qgemv_internal.h"
+
+namespace qg {
+
+__device__ int g_status_word = 0;
+
+namespace {
+
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_starve{0};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int g_sm_count[kMaxDevices] = {0};
+int* g_status_ptr[kMaxDevices] = {nullptr};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int current_device()
+{
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return d;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+qg_status check_dense(const void* w0, const void* w1, const void* x, const void* y, const void* residual, int M,
+                      int N, int K)
+{
+    if (!w0 || !w1 || !x || !y) return QG_ERR_INVALID_ARG;
+    if (M < 1 || M > kMaxTokens || N < 1 || K < 32 || (K % 32) != 0) return QG_ERR_INVALID_ARG;
+    if (!aligned16(w0) || !aligned16(w1) || !aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)))
+        return QG_ERR_MISALIGNED;
+    return QG_OK;
+}
+
+}  // namespace
+
+DebugState debug_state() { return DebugState{g_wait_ns.load(), g_starve.load()}; }
+
+int sm_count(int device)
+{
+    if (device < 0) device = current_device();
+    if (device < 0 || device >= kMaxDevices) return 148;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_sm_count[device] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0) v = 148;
+        g_sm_count[device] = v;
+    }
+    return g_sm_count[device];
+}
+
+int* device_status_ptr()
+{
+    const int device = current_device();
+    if (device < 0 || device >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_status_ptr[device]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[device] = static_cast<int*>(p);
+    }
+    return g_status_ptr[device];
+}
+
+bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
+                    uint64_t inner_elems, uint64_t rows, uint32_t box_inner, uint32_t box_rows, bool swizzle128)
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    if (!g_encode) return false;
+    const cuuint64_t dims[2] = {inner_elems, rows};
+    const cuuint64_t strides[1] = {inner_elems * static_cast<uint64_t>(elem_bytes)};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace qg
+
+using namespace qg;
+
+extern "C" {
+
+qg_status qgemv_nvfp4(const uint8_t* codes, const uint8_t* scales, float global_scale, const void* x, void* y,
+                      qg_out y_dtype, const void* residual, int M, int N, int K, cudaStream_t stream)
+{
+    qg_status s = check_dense(codes, scales, x, y, residual, M, N, K);
+    if (s != QG_OK) return s;
+    if (y_dtype != QG_OUT_BF16 && y_dtype != QG_OUT_F32) return QG_ERR_INVALID_ARG;
+    const int f32 = y_dtype == QG_OUT_F32;
+    if (K % kChunkK == 0)
+        return launch_dense_nvfp4(codes, scales, global_scale, x, y, f32, residual, M, N, K, 0, stream);
+    return launch_simple(FMT_NVFP4, codes, nullptr, scales, nullptr, global_scale, x, y, f32, residual, M, N, K, 0,
+                         stream);
+}
+
+qg_status qgemv_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min, int bits,
+                    const void* x, void* y, qg_out y_dtype, const void* residual, int M, int N, int K,
+                    cudaStream_t stream)
+{
+    qg_status s = check_dense(q_lo, scale, x, y, residual, M, N, K);
+    if (s != QG_OK) return s;
+    if (!min) return QG_ERR_INVALID_ARG;
+    if (bits != 4 && bits != 5) return QG_ERR_INVALID_ARG;
+    if ((bits == 5) != (q_hi != nullptr)) return QG_ERR_INVALID_ARG;
+    if (!aligned16(min) || (q_hi && !aligned16(q_hi))) return QG_ERR_MISALIGNED;
+    if (y_dtype != QG_OUT_BF16 && y_dtype != QG_OUT_F32) return QG_ERR_INVALID_ARG;
+    const int f32 = y_dtype == QG_OUT_F32;
+    if (K % kChunkK == 0) return launch_dense_q45(q_lo, q_hi, scale, min, bits, x, y, f32, residual, M, N, K, stream);
+    return launch_simple(bits == 5 ? FMT_Q5 : FMT_Q4, q_lo, q_hi, scale, min, 1.f, x, y, f32, residual, M, N, K, 0,
+                         stream);
+}
+
+qg_status qgemv_swiglu_nvfp4(const uint8_t* codes, const uint8_t* scales, float global_scale, const void* x,
+                             void* y, int M, int N, int K, cudaStream_t stream)
+{
+    qg_status s = check_dense(codes, scales, x, y, nullptr, M, N, K);
+    if (s != QG_OK) return s;
+    if (N % 2 != 0) return QG_ERR_INVALID_ARG;
+    if (K % kChunkK == 0)
+        return launch_dense_nvfp4(codes, scales, global_scale, x, y, 0, nullptr, M, N, K, 1, stream);
+    return launch_simple(FMT_NVFP4, codes, nullptr, scales, nullptr, global_scale, x, y, 0, nullptr, M, N, K, 1,
+                         stream);
+}
+
+qg_status moe_route_topk(const float* logits, int M, int E, int topk, int32_t* topk_ids, float* topk_w,
+                         cudaStream_t stream)
+{
+    if (!logits || !topk_ids || !topk_w) return QG_ERR_INVALID_ARG;
+    if (M < 1 || M > kMaxTokens || topk < 1 || topk > 8 || E < topk || E > 1024) return QG_ERR_INVALID_ARG;
+    if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w)) return QG_ERR_MISALIGNED;
+    return launch_route(logits, M, E, topk, topk_ids, topk_w, stream);
+}
+
+qg_status moe_qgemv_nvfp4_workspace_size(int M, int topk, int H, int I, int E, size_t* bytes)
+{
+    if (!bytes) return QG_ERR_INVALID_ARG;
+    if (M < 1 || M > kMaxTokens || topk < 1 || topk > 8 || E < topk || H < 256 || I < 256 || H % 256 || I % 256)
+        return QG_ERR_INVALID_ARG;
+    *bytes = moe_workspace_bytes(M, topk, H, I, E);
+    return QG_OK;
+}
+
+qg_status moe_qgemv_nvfp4(const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_gscale,
+                          const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_gscale, const void* x,
+                          const int32_t* topk_ids, const float* topk_w, void* y, void* workspace,
+                          size_t workspace_bytes, int M, int H, int I, int E, int topk, cudaStream_t stream)
+{
+    if (!gu_codes || !gu_scales || !gu_gscale || !dn_codes || !dn_scales || !dn_gscale || !x || !topk_ids ||
+        !topk_w || !y)
+        return QG_ERR_INVALID_ARG;
+    size_t need = 0;
+    qg_status s = moe_qgemv_nvfp4_workspace_size(M, topk, H, I, E, &need);
+    if (s != QG_OK) return s;
+    const void* ptrs[] = {gu_codes, gu_scales, gu_gscale, dn_codes, dn_scales, dn_gscale, x, topk_ids, topk_w, y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return QG_ERR_MISALIGNED;
+    if (!workspace || workspace_bytes < need) return QG_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QG_ERR_MISALIGNED;
+    return launch_moe(gu_codes, gu_scales, gu_gscale, dn_codes, dn_scales, dn_gscale, x, topk_ids, topk_w, y,
+                      workspace, workspace_bytes, M, H, I, E, topk, stream);
+}
+
+qg_status qdequant_nvfp4(const uint8_t* codes, const uint8_t* scales, float global_scale, float* w, int N, int K,
+                         cudaStream_t stream)
+{
+    if (!codes || !scales || !w || N < 1 || K < 32 || K % 32) return QG_ERR_INVALID_ARG;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(w)) return QG_ERR_MISALIGNED;
+    return launch_dequant(FMT_NVFP4, codes, nullptr, scales, nullptr, global_scale, w, N, K, stream);
+}
+
+qg_status qdequant_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min, int bits,
+                       float* w, int N, int K, cudaStream_t stream)
+{
+    if (!q_lo || !scale || !min || !w || N < 1 || K < 32 || K % 32) return QG_ERR_INVALID_ARG;
+    if (bits != 4 && bits != 5) return QG_ERR_INVALID_ARG;
+    if ((bits == 5) != (q_hi != nullptr)) return QG_ERR_INVALID_ARG;
+    if (!aligned16(q_lo) || !aligned16(scale) || !aligned16(min) || !aligned16(w) || (q_hi && !aligned16(q_hi)))
+        return QG_ERR_MISALIGNED;
+    return launch_dequant(bits == 5 ? FMT_Q5 : FMT_Q4, q_lo, q_hi, scale, min, 1.f, w, N, K, stream);
+}
+
+qg_status qg_last_device_status(cudaStream_t stream)
+{
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return QG_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return QG_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return QG_ERR_CUDA;
+    return static_cast<qg_status>(v);
+}
+
+const char* qg_status_string(qg_status status)
+{
+    switch (status) {
+    case QG_OK: return "QG_OK";
+    case QG_ERR_INVALID_ARG: return "QG_ERR_INVALID_ARG";
+    case QG_ERR_UNSUPPORTED: return "QG_ERR_UNSUPPORTED";
+    case QG_ERR_MISALIGNED: return "QG_ERR_MISALIGNED";
+    case QG_ERR_WORKSPACE: return "QG_ERR_WORKSPACE";
+    case QG_ERR_CUDA: return "QG_ERR_CUDA";
+    case QG_ERR_DEVICE_TIMEOUT: return "QG_ERR_DEVICE_TIMEOUT";
+    }
+    return "QG_ERR_UNKNOWN";
+}
+
+qg_status qg_debug_set_wait(uint64_t limit_ns, int starve)
+{
+    g_wait_ns.store(limit_ns ? limit_ns : kDefaultWaitNs);
+    g_starve.store(starve ? 1 : 0);
+    return QG_OK;
+}
+
+}  // extern "C"

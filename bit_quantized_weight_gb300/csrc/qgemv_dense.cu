@@ -1,0 +1,730 @@
+// qgemv_dense.cu -- TMA-fed tensor-core GEMV for NVFP4 and Q4/Q5 weights,
+// M = 1..8 tokens, with fused residual-add and SwiGLU epilogues.
+//
+// Prior art on the pages: NInfer writes one fused matmul (+ residual add /
+// SwiGLU) kernel per weight format because decode is memory-bandwidth bound
+// (NInfer article, section 2 "自研 CUDA 算子 混合量化权重"); Decapybara's
+// mx_gemv.cu is an NVFP4 block mat-vec (Decapybara README, "Blackwell CUDA 内核
+// 套件"). Both target sm_120a; this kernel is designed for sm_103a:
+//
+//   * Each CTA owns a contiguous range of R output rows (R = ceil(N / #SMs),
+//     so every SM streams the same number of bytes) and walks K in 256-wide
+//     chunks. One warp issues 2-D TMA loads of the chunk's codes and scales
+//     into a ring of shared-memory stages (mbarrier full/empty pairs); eight
+//     consumer warps decode and multiply. Every weight byte crosses HBM once.
+//   * Codes arrive 128B-swizzled, so ldmatrix reads a 16-row x 64-k tile of
+//     4-bit codes per instruction without bank conflicts.
+//   * NVFP4 decode: cvt.rn.f16x2.e2m1x2 turns two codes into f16 exactly, and
+//     an f16 multiply by the E4M3 block scale (also converted exactly) is exact
+//     too: e2m1 * e4m3 has at most 6 significant bits and lies in
+//     [2^-10, 2688]. Q4/Q5 decode: q is placed in an f16 mantissa
+//     (1024 + q) and 1024 subtracted, exactly.
+//   * The products run on the tensor cores (mma.m16n8k16, f16 in, fp32
+//     accumulate), 16 weight rows x 8 token columns per MMA. Tokens beyond M
+//     are zero columns.
+//   * Activations are bf16; they enter the MMA as f16 after an exact
+//     power-of-two prescale chosen per (token, 256-k chunk) so that the chunk
+//     maximum lands in [2^14, 2^15). Every bf16 value within 2^31 of that
+//     maximum is then exact in f16. A chunk holding a smaller nonzero value is
+//     flagged and gets extra passes over residual terms (x - f16(x)) * 2^24, so
+//     the result is exact-product fp32 accumulation for every finite input.
+//   * Accumulation: each chunk's MMA partial (at most 16 chained MMAs) is
+//     scaled back by 2^-p and added to an fp32 accumulator; Q groups add
+//     scale * sum(q x) + min * sum(x) per group of 32.
+#include "common.cuh"
+
+#include <cuda_bf16.h>
+
+namespace qg {
+
+namespace {
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds8(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("{\n .reg .u8 b;\n ld.shared.u8 b, [%1];\n cvt.u32.u8 %0, b;\n}\n" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_128(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t bcast_lo(uint32_t h2) { return __byte_perm(h2, 0, 0x1010); }
+__device__ __forceinline__ uint32_t bcast_hi(uint32_t h2) { return __byte_perm(h2, 0, 0x3232); }
+
+// Power-of-two prescale exponent p for a chunk whose largest finite |x| has
+// bf16 magnitude bits `mag` (0 if every value is zero): max * 2^p in [2^14, 2^15).
+__device__ __forceinline__ int prescale_exponent(uint32_t mag)
+{
+    if (mag == 0) return 0;
+    uint32_t e = mag >> 7;
+    if (e > 0) return 141 - static_cast<int>(e);
+    // subnormal bf16: value = mag * 2^-133
+    int lg = 31 - __clz(static_cast<int>(mag));
+    return 147 - lg;
+}
+
+// Convert one token's 256-k chunk (8 values per lane) to prescaled f16.
+// Returns the f16 values packed in the format's pair order and reports
+// whether every value was represented exactly.
+template <int FMT>
+__device__ __forceinline__ uint4 convert_chunk8(const uint4 raw, int p, bool& exact, float& lane_sum)
+{
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    float v[8];
+    uint32_t h[8];
+    exact = true;
+    lane_sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = ldexp_exact(bf16_bits_to_f32(w[i] & 0xFFFFu), p);
+        v[2 * i + 1] = ldexp_exact(bf16_bits_to_f32(w[i] >> 16), p);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        __half hv = __float2half_rn(v[i]);
+        h[i] = __half_as_ushort(hv);
+        float back = __half2float(hv);
+        if (isfinite(v[i]) && back != v[i]) exact = false;
+        lane_sum += v[i];
+    }
+    uint4 out;
+    if (FMT == FMT_NVFP4) {
+        out.x = h[0] | (h[1] << 16);
+        out.y = h[2] | (h[3] << 16);
+        out.z = h[4] | (h[5] << 16);
+        out.w = h[6] | (h[7] << 16);
+    } else {
+        out.x = h[0] | (h[4] << 16);
+        out.y = h[1] | (h[5] << 16);
+        out.z = h[2] | (h[6] << 16);
+        out.w = h[3] | (h[7] << 16);
+    }
+    return out;
+}
+
+// Residual term `term` (>= 1) of 8 exact values already multiplied by 2^p:
+// r_0 = v, r_{t+1} = (r_t - f16(r_t)) * 2^24. Returns f16 pairs of r_term in
+// the format's pair order and whether anything is left after it.
+template <int FMT>
+__device__ __forceinline__ uint4 residual_term8(const uint4 raw, int p, int term, bool& more)
+{
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t h[8];
+    more = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
+        float r = ldexp_exact(bf16_bits_to_f32(bits), p);
+        if (!isfinite(r)) r = 0.f;  // non-finite values were carried by term 0
+        for (int t = 0; t < term; ++t) r = (r - __half2float(__float2half_rn(r))) * 16777216.0f;
+        __half hv = __float2half_rn(r);
+        h[i] = __half_as_ushort(hv);
+        if (r - __half2float(hv) != 0.f) more = true;
+    }
+    uint4 out;
+    if (FMT == FMT_NVFP4) {
+        out = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+    } else {
+        out = make_uint4(h[0] | (h[4] << 16), h[1] | (h[5] << 16), h[2] | (h[6] << 16), h[3] | (h[7] << 16));
+    }
+    return out;
+}
+
+struct TileAcc {
+    float v[2][4];  // [gate/up][element]
+};
+
+// One consumer warp's share of one pipeline stage for one 16-row tile: the
+// macro-steps (64 k each) of its slice, every residual term the chunk needs,
+// and the fold of the chunk partial into the fp32 accumulator.
+template <int FMT, int EPI>
+__device__ __forceinline__ void process_tile(const DenseArgs& a, uint32_t sb, uint32_t x_base, uint32_t sm_base,
+                                             const int* xexp, int jsub, int kglob, int ks0, int ti, int slice,
+                                             int S, int n_terms, int lane, TileAcc& acc)
+{
+    constexpr int NGU = (EPI == EPI_SWIGLU) ? 2 : 1;
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int M = a.M;
+
+    // Q: scale and min of the chunk's 8 groups for rows g and g+8.
+    uint4 qs_g = make_uint4(0, 0, 0, 0), qs_g8 = qs_g, qm_g = qs_g, qm_g8 = qs_g;
+    if (FMT != FMT_NVFP4) {
+        qs_g = lds128(sb + a.st.scales + (16 * ti + g) * 16);
+        qs_g8 = lds128(sb + a.st.scales + (16 * ti + g + 8) * 16);
+        qm_g = lds128(sb + a.st.mins + (16 * ti + g) * 16);
+        qm_g8 = lds128(sb + a.st.mins + (16 * ti + g + 8) * 16);
+    }
+    const int p0 = xexp[jsub * 8 + 2 * t];
+    const int p1 = xexp[jsub * 8 + 2 * t + 1];
+
+#pragma unroll 1
+    for (int term = 0; term < n_terms; ++term) {
+        float d[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[j][e] = 0.f;
+        bool more = false;
+#pragma unroll
+        for (int ms = 0; ms < 4; ++ms) {
+            if ((ms % S) != slice) continue;
+            // B operand (token g) for the two 32-k chunks of this macro-step.
+            uint4 bx[2];
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                const int kk = (kglob - ks0) + 64 * ms + 32 * ch + 8 * t;
+                bx[ch] = make_uint4(0, 0, 0, 0);
+                if (g < M) {
+                    if (term == 0) {
+                        bx[ch] = lds128(x_base + (g * a.x_pitch + kk) * 2);
+                    } else {
+                        const uint4 raw = ldg_nc_128(a.x + static_cast<size_t>(g) * a.K + ks0 + kk);
+                        bool m2;
+                        bx[ch] = residual_term8<FMT>(raw, xexp[jsub * 8 + g], term, m2);
+                        more |= m2;
+                    }
+                }
+            }
+            // ldmatrix addressing: lane l supplies row (l & 7) + 8 * ((l >> 3) & 1)
+            // of the tile and 16-byte chunk 2 * ms + (l >> 4); rows are 128 B,
+            // 128B-swizzled (chunk c of row r sits at chunk c ^ (r & 7)).
+            const int lr = (lane & 7) + 8 * ((lane >> 3) & 1);
+            const int lc = 2 * ms + (lane >> 4);
+            const uint32_t lofs = (16 * ti + lr) * 128 + ((lc ^ (lr & 7)) << 4);
+#pragma unroll
+            for (int gu = 0; gu < NGU; ++gu) {
+                uint32_t cr[4];
+                ldmatrix_x4(cr, sb + (gu ? a.st.codes2 : a.st.codes) + lofs);
+                // cr[0]: row g, chunk 2ms; cr[1]: row g+8, chunk 2ms;
+                // cr[2]: row g, chunk 2ms+1; cr[3]: row g+8, chunk 2ms+1.
+                // Each holds 8 codes for k = 32 * chunk + 8t .. 8t+7.
+                if (FMT == FMT_NVFP4) {
+                    const uint32_t sbase = sb + (gu ? a.st.scales2 : a.st.scales);
+                    const uint32_t sw_g = lds32(sbase + (16 * ti + g) * 16 + 4 * ms);
+                    const uint32_t sw_g8 = lds32(sbase + (16 * ti + g + 8) * 16 + 4 * ms);
+                    // 16-k blocks 4ms + (t>>1) (chunk 2ms) and 4ms + 2 + (t>>1) (chunk 2ms+1)
+                    const uint32_t sel = static_cast<uint32_t>((t >> 1) | (((t >> 1) + 2) << 4));
+                    const uint32_t sc_g = e4m3x2_to_f16x2(__byte_perm(sw_g, 0, sel));
+                    const uint32_t sc_g8 = e4m3x2_to_f16x2(__byte_perm(sw_g8, 0, sel));
+#pragma unroll
+                    for (int ch = 0; ch < 2; ++ch) {
+                        const uint32_t s_g = ch ? bcast_hi(sc_g) : bcast_lo(sc_g);
+                        const uint32_t s_g8 = ch ? bcast_hi(sc_g8) : bcast_lo(sc_g8);
+                        const uint32_t rg = cr[2 * ch], rg8 = cr[2 * ch + 1];
+                        uint32_t pg[4], pg8[4];
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            pg[b] = hmul2(e2m1x2_to_f16x2((rg >> (8 * b)) & 0xFFu), s_g);
+                            pg8[b] = hmul2(e2m1x2_to_f16x2((rg8 >> (8 * b)) & 0xFFu), s_g8);
+                        }
+                        const uint4 bb = bx[ch];
+                        const uint32_t A0[4] = {pg[0], pg8[0], pg[1], pg8[1]};
+                        mma_f16_16816(d[gu], A0, bb.x, bb.y);
+                        const uint32_t A1[4] = {pg[2], pg8[2], pg[3], pg8[3]};
+                        mma_f16_16816(d[gu], A1, bb.z, bb.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int ch = 0; ch < 2; ++ch) {
+                        const int grp = 2 * ms + ch;  // 32-k group index inside the chunk
+                        const uint32_t rg = cr[2 * ch], rg8 = cr[2 * ch + 1];
+                        uint32_t hg = 0, hg8 = 0;
+                        if (FMT == FMT_Q5) {
+                            const uint32_t h0 = lds8(sb + a.st.hi + (16 * ti + g) * 32 + 4 * grp + t);
+                            const uint32_t h1 = lds8(sb + a.st.hi + (16 * ti + g + 8) * 32 + 4 * grp + t);
+                            hg = (h0 << 4) | (h0 << 16);
+                            hg8 = (h1 << 4) | (h1 << 16);
+                        }
+                        uint32_t q0[4], q8[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            // f16 pair {q(8t+i), q(8t+i+4)} as 1024 + q, then minus 1024
+                            uint32_t u = ((rg >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+                            uint32_t u8 = ((rg8 >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+                            if (FMT == FMT_Q5) {
+                                u |= (hg >> i) & 0x00100010u;
+                                u8 |= (hg8 >> i) & 0x00100010u;
+                            }
+                            q0[i] = hsub2(u, 0x64006400u);
+                            q8[i] = hsub2(u8, 0x64006400u);
+                        }
+                        const uint4 bb = bx[ch];
+                        float dg[4] = {0.f, 0.f, 0.f, 0.f};
+                        const uint32_t A0[4] = {q0[0], q8[0], q0[1], q8[1]};
+                        mma_f16_16816(dg, A0, bb.x, bb.y);
+                        const uint32_t A1[4] = {q0[2], q8[2], q0[3], q8[3]};
+                        mma_f16_16816(dg, A1, bb.z, bb.w);
+                        const uint32_t sv_g = (&qs_g.x)[grp >> 1], sv_g8 = (&qs_g8.x)[grp >> 1];
+                        const int sh = (grp & 1) * 16;
+                        const float s0 = half_bits_to_f32((sv_g >> sh) & 0xFFFFu);
+                        const float s8 = half_bits_to_f32((sv_g8 >> sh) & 0xFFFFu);
+                        d[0][0] = fmaf(s0, dg[0], d[0][0]);
+                        d[0][1] = fmaf(s0, dg[1], d[0][1]);
+                        d[0][2] = fmaf(s8, dg[2], d[0][2]);
+                        d[0][3] = fmaf(s8, dg[3], d[0][3]);
+                        if (term == 0) {
+                            // min * sum(x) over the group, with the exact prescaled sums
+                            const uint32_t mv_g = (&qm_g.x)[grp >> 1], mv_g8 = (&qm_g8.x)[grp >> 1];
+                            const float m0 = half_bits_to_f32((mv_g >> sh) & 0xFFFFu);
+                            const float m8 = half_bits_to_f32((mv_g8 >> sh) & 0xFFFFu);
+                            const uint2 sx = lds64(sm_base + a.smem_sum + ((jsub * 8 + grp) * 8 + 2 * t) * 4);
+                            const float S0 = __uint_as_float(sx.x), S1 = __uint_as_float(sx.y);
+                            d[0][0] = fmaf(m0, S0, d[0][0]);
+                            d[0][1] = fmaf(m0, S1, d[0][1]);
+                            d[0][2] = fmaf(m8, S0, d[0][2]);
+                            d[0][3] = fmaf(m8, S1, d[0][3]);
+                        }
+                    }
+                }
+            }
+        }
+        // fold the chunk partial: value = d * 2^-(p + 24 term) per token column
+        const int e0 = p0 + 24 * term, e1 = p1 + 24 * term;
+#pragma unroll
+        for (int gu = 0; gu < NGU; ++gu) {
+            acc.v[gu][0] += ldexp_exact(d[gu][0], -e0);
+            acc.v[gu][1] += ldexp_exact(d[gu][1], -e1);
+            acc.v[gu][2] += ldexp_exact(d[gu][2], -e0);
+            acc.v[gu][3] += ldexp_exact(d[gu][3], -e1);
+        }
+        if (term > 0 && !__any_sync(0xffffffffu, more)) break;
+    }
+}
+
+template <int FMT, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    dense_kernel(const __grid_constant__ DenseArgs a, const __grid_constant__ CUtensorMap tm0,
+                 const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm2,
+                 const __grid_constant__ CUtensorMap tm3)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int NGU = (EPI == EPI_SWIGLU) ? 2 : 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int row0 = blockIdx.x * a.rows_per_cta;
+    const int rows = min(a.rows_per_cta, a.n_out - row0);
+    const int n_chunks = a.K / kChunkK;
+
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.smem_bar);
+    uint64_t* empty = full + kMaxStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kMaxStages);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.n_stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ producer
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            prefetch_tensormap(&tm0);
+            prefetch_tensormap(&tm1);
+            if (FMT != FMT_NVFP4) prefetch_tensormap(&tm2);
+            if (FMT == FMT_Q5) prefetch_tensormap(&tm3);
+            int issued = 0;
+            for (int c = 0; c < n_chunks; ++c) {
+                const int slot = c % a.n_stages;
+                if (c >= a.n_stages) {
+                    if (!mbar_wait_bounded(&empty[slot], ((c / a.n_stages) - 1) & 1, a.wait_ns, a.status)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
+                if (*abort_flag || a.starve) break;
+                mbar_arrive_expect_tx(&full[slot], a.st.tx_bytes);
+                uint8_t* sb = smem + a.smem_ring + slot * a.st.bytes;
+                const int kb = c * kChunkK;
+                tma_load_2d(sb + a.st.codes, &tm0, kb / 2, row0, &full[slot]);
+                if (FMT == FMT_NVFP4) {
+                    tma_load_2d(sb + a.st.scales, &tm1, kb / 16, row0, &full[slot]);
+                    if (EPI == EPI_SWIGLU) {
+                        tma_load_2d(sb + a.st.codes2, &tm0, kb / 2, row0 + a.up_row_offset, &full[slot]);
+                        tma_load_2d(sb + a.st.scales2, &tm1, kb / 16, row0 + a.up_row_offset, &full[slot]);
+                    }
+                } else {
+                    tma_load_2d(sb + a.st.scales, &tm1, kb / 32, row0, &full[slot]);
+                    tma_load_2d(sb + a.st.mins, &tm2, kb / 32, row0, &full[slot]);
+                    if (FMT == FMT_Q5) tma_load_2d(sb + a.st.hi, &tm3, kb / 8, row0, &full[slot]);
+                }
+                issued = c + 1;
+            }
+            // No copy may still be landing in shared memory when the CTA exits.
+            for (int c = max(0, issued - a.n_stages); c < issued; ++c)
+                mbar_wait_bounded(&full[c % a.n_stages], (c / a.n_stages) & 1, a.wait_ns, a.status);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers
+    const int g = lane >> 2;  // MMA group: weight row g / g+8, token g
+    const int t = lane & 3;   // thread in group
+    const int T = (rows + 15) >> 4;
+    const int Tp = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16;
+    const int S = Tp >= 8 ? 1 : min(4, kConsumerWarps / Tp);
+    int my_tiles[2] = {-1, -1};
+    int slice = 0;
+    if (Tp == 16) {
+        my_tiles[0] = warp < T ? warp : -1;
+        my_tiles[1] = warp + 8 < T ? warp + 8 : -1;
+    } else {
+        slice = warp / Tp;
+        const int ti = warp % Tp;
+        if (slice < S && ti < T) my_tiles[0] = ti;
+    }
+
+    const uint32_t sm_base = smem_u32(smem);
+    const uint32_t x_base = sm_base + a.smem_x;
+    int* xexp = reinterpret_cast<int*>(smem + a.smem_exp);            // [nsub][8]
+    uint8_t* xflag = smem + a.smem_flag;                                // [nsub][8]
+    float* xsum = reinterpret_cast<float*>(smem + a.smem_sum);        // [groups][8]
+    const int M = a.M;
+
+    TileAcc acc[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[i].v[j][e] = 0.f;
+
+    bool aborted = false;
+    int ks0 = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+        const int kglob = c * kChunkK;
+        // ---------------- activation super-chunk conversion
+        if (kglob == ks0 + (c == 0 ? 0 : a.ksc) || c == 0) {
+            if (c != 0) ks0 += a.ksc;
+            const int len = min(a.ksc, a.K - ks0);
+            const int nsub = len / kChunkK;
+            named_barrier_sync(1, 32 * kConsumerWarps);
+            for (int it = warp; it < nsub * kMaxTokens; it += kConsumerWarps) {
+                const int m = it % kMaxTokens;
+                const int j = it / kMaxTokens;
+                if (m >= M) {
+                    if (lane == 0) {
+                        xexp[j * 8 + m] = 0;
+                        xflag[j * 8 + m] = 0;
+                    }
+                    if (FMT != FMT_NVFP4 && (lane & 3) == 0) xsum[(j * 8 + (lane >> 2)) * 8 + m] = 0.f;
+                    continue;
+                }
+                const uint4 raw = ldg_nc_128(a.x + static_cast<size_t>(m) * a.K + ks0 + j * kChunkK + lane * 8);
+                uint32_t mag = 0;
+                const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t lo = wv[i] & 0x7FFFu, hi = (wv[i] >> 16) & 0x7FFFu;
+                    if (lo < 0x7F80u) mag = max(mag, lo);
+                    if (hi < 0x7F80u) mag = max(mag, hi);
+                }
+                mag = __reduce_max_sync(0xffffffffu, mag);
+                const int p = prescale_exponent(mag);
+                bool exact;
+                float ls;
+                const uint4 hv = convert_chunk8<FMT>(raw, p, exact, ls);
+                const uint32_t dst = x_base + (static_cast<uint32_t>(m) * a.x_pitch + j * kChunkK + lane * 8) * 2;
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(hv.x), "r"(hv.y), "r"(hv.z),
+                             "r"(hv.w));
+                const bool any_inexact = __any_sync(0xffffffffu, !exact);
+                if (lane == 0) {
+                    xexp[j * 8 + m] = p;
+                    xflag[j * 8 + m] = any_inexact ? 1 : 0;
+                }
+                if (FMT != FMT_NVFP4) {
+                    ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+                    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+                    if ((lane & 3) == 0) xsum[(j * 8 + (lane >> 2)) * 8 + m] = ls;
+                }
+            }
+            named_barrier_sync(1, 32 * kConsumerWarps);
+        }
+
+        const int slot = c % a.n_stages;
+        if (!aborted && *abort_flag) aborted = true;
+        if (!aborted) {
+            if (!mbar_wait_bounded(&full[slot], (c / a.n_stages) & 1, a.wait_ns, a.status)) {
+                aborted = true;
+                *abort_flag = 1;
+            }
+        }
+        if (!aborted) {
+            const uint32_t sb = sm_base + a.smem_ring + slot * a.st.bytes;
+            const int jsub = (kglob - ks0) / kChunkK;
+            const uint64_t flags8 = *reinterpret_cast<const uint64_t*>(xflag + jsub * 8);
+            const int n_terms = flags8 ? 12 : 1;
+            if (my_tiles[0] >= 0)
+                process_tile<FMT, EPI>(a, sb, x_base, sm_base, xexp, jsub, kglob, ks0, my_tiles[0], slice, S,
+                                       n_terms, lane, acc[0]);
+            if (my_tiles[1] >= 0)
+                process_tile<FMT, EPI>(a, sb, x_base, sm_base, xexp, jsub, kglob, ks0, my_tiles[1], slice, S,
+                                       n_terms, lane, acc[1]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+
+    // ---------------- cross-slice reduction (fixed order) and epilogue
+    float* red = reinterpret_cast<float*>(smem + a.smem_red);
+    if (S > 1) {
+        named_barrier_sync(1, 32 * kConsumerWarps);
+        if (slice > 0 && my_tiles[0] >= 0) {
+#pragma unroll
+            for (int gu = 0; gu < NGU; ++gu)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    red[(((slice * Tp + my_tiles[0]) * 2 + gu) * 32 + lane) * 4 + e] = acc[0].v[gu][e];
+        }
+        named_barrier_sync(1, 32 * kConsumerWarps);
+        if (slice == 0 && my_tiles[0] >= 0) {
+            for (int s = 1; s < S; ++s)
+#pragma unroll
+                for (int gu = 0; gu < NGU; ++gu)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        acc[0].v[gu][e] += red[(((s * Tp + my_tiles[0]) * 2 + gu) * 32 + lane) * 4 + e];
+        }
+    }
+    if (slice != 0 || aborted) return;
+
+#pragma unroll
+    for (int ti_i = 0; ti_i < 2; ++ti_i) {
+        const int ti = my_tiles[ti_i];
+        if (ti < 0) continue;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = 16 * ti + g + ((e & 2) ? 8 : 0);
+            const int tok = 2 * t + (e & 1);
+            if (r >= rows || tok >= M) continue;
+            const int n = row0 + r;
+            float v = acc[ti_i].v[0][e] * a.g;
+            if (EPI == EPI_SWIGLU) {
+                const float u = acc[ti_i].v[1][e] * a.g;
+                v = (v / (1.0f + expf(-v))) * u;
+            }
+            if (EPI == EPI_RESID) v += bf16_bits_to_f32(a.residual[static_cast<size_t>(tok) * a.n_out + n]);
+            if (a.out_f32) {
+                reinterpret_cast<float*>(a.y)[static_cast<size_t>(tok) * a.n_out + n] = v;
+            } else {
+                reinterpret_cast<uint16_t*>(a.y)[static_cast<size_t>(tok) * a.n_out + n] = f32_to_bf16_bits_rn(v);
+            }
+        }
+    }
+}
+
+constexpr uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+template <int FMT, int EPI>
+qg_status launch_dense_impl(const CUtensorMap* maps, const uint16_t* x, void* y, int out_f32,
+                            const uint16_t* residual, int M, int n_out, int up_offset, int K, float g,
+                            int rows_per_cta, cudaStream_t stream)
+{
+    DenseArgs a{};
+    a.x = x;
+    a.y = y;
+    a.residual = residual;
+    a.M = M;
+    a.K = K;
+    a.n_out = n_out;
+    a.rows_per_cta = rows_per_cta;
+    a.up_row_offset = up_offset;
+    a.out_f32 = out_f32;
+    a.g = g;
+    a.status = device_status_ptr();
+    if (!a.status) return QG_ERR_CUDA;
+    const DebugState dbg = debug_state();
+    a.wait_ns = dbg.wait_ns;
+    a.starve = dbg.starve;
+
+    // activation super-chunk: M token rows of (ksc + 32) f16 within 64 KB
+    constexpr uint32_t kXBudget = 64 * 1024;
+    int ksc = (static_cast<int>(kXBudget / (2u * M)) - 32) / kChunkK * kChunkK;
+    ksc = min(ksc, K);
+    a.ksc = ksc;
+    a.x_pitch = ksc + 32;
+    const int nsub = ksc / kChunkK;
+
+    const int R = rows_per_cta;
+    const int R16 = (R + 15) / 16 * 16;  // regions cover whole 16-row tiles
+    StageLayout st{};
+    uint32_t off = 0;
+    st.codes = off;
+    off = align_up(off + R16 * 128, 1024);
+    if (EPI == EPI_SWIGLU) {
+        st.codes2 = off;
+        off = align_up(off + R16 * 128, 1024);
+    }
+    st.scales = off;
+    off = align_up(off + R16 * 16, 128);
+    if (EPI == EPI_SWIGLU) {
+        st.scales2 = off;
+        off = align_up(off + R16 * 16, 128);
+    }
+    if (FMT != FMT_NVFP4) {
+        st.mins = off;
+        off = align_up(off + R16 * 16, 128);
+    }
+    if (FMT == FMT_Q5) {
+        st.hi = off;
+        off = align_up(off + R16 * 32, 128);
+    }
+    st.bytes = align_up(off, 1024);
+    uint32_t tx = R * 128 + R * 16;
+    if (EPI == EPI_SWIGLU) tx *= 2;
+    if (FMT != FMT_NVFP4) tx += R * 16;
+    if (FMT == FMT_Q5) tx += R * 32;
+    st.tx_bytes = tx;
+    a.st = st;
+
+    // shared memory plan
+    uint32_t so = 0;
+    const uint32_t x_bytes = align_up(static_cast<uint32_t>(M) * a.x_pitch * 2, 128);
+    const uint32_t exp_bytes = align_up(nsub * 8 * 4, 128);
+    const uint32_t flag_bytes = align_up(nsub * 8, 128);
+    const uint32_t sum_bytes = FMT == FMT_NVFP4 ? 0 : align_up(nsub * 8 * 8 * 4, 128);
+    const uint32_t red_bytes = 8 * 2 * 32 * 4 * 4;
+    const uint32_t bar_bytes = 2 * kMaxStages * 8 + 16;
+    const uint32_t fixed = x_bytes + exp_bytes + flag_bytes + sum_bytes + red_bytes + bar_bytes;
+    const uint32_t smem_max = 227 * 1024;
+    if (fixed + st.bytes > smem_max) return QG_ERR_UNSUPPORTED;
+    int n_stages = static_cast<int>((smem_max - fixed) / st.bytes);
+    n_stages = min(n_stages, kMaxStages);
+    n_stages = min(n_stages, K / kChunkK);
+    if (n_stages < 2 && K / kChunkK >= 2) return QG_ERR_UNSUPPORTED;
+    a.n_stages = max(n_stages, 1);
+    a.smem_ring = so;
+    so += a.n_stages * st.bytes;
+    a.smem_x = so;
+    so += x_bytes;
+    a.smem_exp = so;
+    so += exp_bytes;
+    a.smem_flag = so;
+    so += flag_bytes;
+    a.smem_sum = so;
+    so += sum_bytes;
+    a.smem_red = so;
+    so += red_bytes;
+    a.smem_bar = so;
+    so += bar_bytes;
+
+    auto kern = dense_kernel<FMT, EPI>;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+            return QG_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    const int grid = (n_out + R - 1) / R;
+    kern<<<grid, kThreads, so, stream>>>(a, maps[0], maps[1], maps[2], maps[3]);
+    return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+int choose_rows_per_cta(int n_out, int factor)
+{
+    const int sms = sm_count(-1);
+    int R = (n_out + sms - 1) / sms;
+    R = max(R, 16);
+    R = min(R, kMaxRowsPerCta / factor);
+    return R;
+}
+
+}  // namespace
+
+qg_status launch_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
+                             int out_f32, const void* residual, int M, int N, int K, int swiglu,
+                             cudaStream_t stream)
+{
+    const int n_out = swiglu ? N / 2 : N;
+    const int R = choose_rows_per_cta(n_out, 1);
+    CUtensorMap maps[4];
+    memset(maps, 0, sizeof(maps));
+    if (!encode_tmap_2d(&maps[0], codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, R, true)) return QG_ERR_CUDA;
+    if (!encode_tmap_2d(&maps[1], scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 16, N, 16, R, false))
+        return QG_ERR_CUDA;
+    maps[2] = maps[1];
+    maps[3] = maps[1];
+    const uint16_t* xx = static_cast<const uint16_t*>(x);
+    const uint16_t* rr = static_cast<const uint16_t*>(residual);
+    if (swiglu)
+        return launch_dense_impl<FMT_NVFP4, EPI_SWIGLU>(maps, xx, y, 0, nullptr, M, n_out, n_out, K, g, R, stream);
+    if (residual)
+        return launch_dense_impl<FMT_NVFP4, EPI_RESID>(maps, xx, y, out_f32, rr, M, n_out, 0, K, g, R, stream);
+    return launch_dense_impl<FMT_NVFP4, EPI_NONE>(maps, xx, y, out_f32, nullptr, M, n_out, 0, K, g, R, stream);
+}
+
+qg_status launch_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min,
+                           int bits, const void* x, void* y, int out_f32, const void* residual, int M,
+                           int N, int K, cudaStream_t stream)
+{
+    const int R = choose_rows_per_cta(N, 1);
+    CUtensorMap maps[4];
+    memset(maps, 0, sizeof(maps));
+    if (!encode_tmap_2d(&maps[0], q_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, R, true)) return QG_ERR_CUDA;
+    if (!encode_tmap_2d(&maps[1], scale, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, N, 8, R, false))
+        return QG_ERR_CUDA;
+    if (!encode_tmap_2d(&maps[2], min, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, N, 8, R, false))
+        return QG_ERR_CUDA;
+    if (bits == 5) {
+        if (!encode_tmap_2d(&maps[3], q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 8, N, 32, R, false))
+            return QG_ERR_CUDA;
+    } else {
+        maps[3] = maps[2];
+    }
+    const uint16_t* xx = static_cast<const uint16_t*>(x);
+    const uint16_t* rr = static_cast<const uint16_t*>(residual);
+    if (bits == 5) {
+        if (residual)
+            return launch_dense_impl<FMT_Q5, EPI_RESID>(maps, xx, y, out_f32, rr, M, N, 0, K, 1.f, R, stream);
+        return launch_dense_impl<FMT_Q5, EPI_NONE>(maps, xx, y, out_f32, nullptr, M, N, 0, K, 1.f, R, stream);
+    }
+    if (residual)
+        return launch_dense_impl<FMT_Q4, EPI_RESID>(maps, xx, y, out_f32, rr, M, N, 0, K, 1.f, R, stream);
+    return launch_dense_impl<FMT_Q4, EPI_NONE>(maps, xx, y, out_f32, nullptr, M, N, 0, K, 1.f, R, stream);
+}
+
+}  // namespace qg

@@ -1,0 +1,92 @@
+// qgemv_internal.h -- types shared by the host launchers and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "qgemv.h"
+
+namespace qg {
+
+enum Fmt : int { FMT_NVFP4 = 0, FMT_Q4 = 1, FMT_Q5 = 2 };
+enum Epi : int { EPI_NONE = 0, EPI_RESID = 1, EPI_SWIGLU = 2 };
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one weight-streaming warp
+constexpr int kChunkK = 256;                          // k per pipeline stage
+constexpr int kMaxTokens = 8;                         // MMA n dimension
+constexpr int kMaxRowsPerCta = 256;                   // TMA box limit
+constexpr int kMaxStages = 32;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;    // 2 s
+
+// Per-stage shared-memory layout (byte offsets inside one stage buffer).
+struct StageLayout {
+    uint32_t codes;      // NVFP4 codes / Q q_lo: rows x 128 B, 128B-swizzled (gate rows for SwiGLU)
+    uint32_t codes2;     // SwiGLU up rows (same shape)
+    uint32_t scales;     // NVFP4 scales rows x 16 B; Q scale rows x 16 B (8 x fp16)
+    uint32_t scales2;    // SwiGLU up-row scales
+    uint32_t mins;       // Q min rows x 16 B
+    uint32_t hi;         // Q5 high plane rows x 32 B
+    uint32_t bytes;      // total stage size (multiple of 1024)
+    uint32_t tx_bytes;   // bytes the TMA writes per stage
+};
+
+struct DenseArgs {
+    const uint16_t* x;         // bf16 [M][K]
+    void* y;                   // [M][n_out]
+    const uint16_t* residual;  // bf16 [M][n_out] or nullptr
+    int M;
+    int K;
+    int n_out;                 // output columns (logical rows)
+    int rows_per_cta;          // R (box rows)
+    int up_row_offset;         // SwiGLU: first up row (= n_out)
+    int out_f32;
+    float g;
+    int n_stages;
+    int ksc;                   // k per activation super-chunk
+    int x_pitch;               // f16 elements per token row of the activation buffer
+    uint32_t smem_ring;        // offsets in dynamic shared memory
+    uint32_t smem_x;
+    uint32_t smem_exp;
+    uint32_t smem_flag;
+    uint32_t smem_sum;
+    uint32_t smem_red;
+    uint32_t smem_bar;
+    StageLayout st;
+    uint64_t wait_ns;
+    int starve;
+    int* status;               // device status word
+};
+
+// Host-side helpers implemented in api.cu.
+struct DebugState {
+    uint64_t wait_ns;
+    int starve;
+};
+DebugState debug_state();
+int* device_status_ptr();  // address of the status word on the current device
+int sm_count(int device);
+bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
+                    uint64_t inner_elems, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+                    bool swizzle128);
+
+qg_status launch_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
+                             int out_f32, const void* residual, int M, int N, int K, int swiglu,
+                             cudaStream_t stream);
+qg_status launch_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min,
+                           int bits, const void* x, void* y, int out_f32, const void* residual, int M,
+                           int N, int K, cudaStream_t stream);
+qg_status launch_simple(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
+                        const void* mins, float g, const void* x, void* y, int out_f32,
+                        const void* residual, int M, int N, int K, int swiglu, cudaStream_t stream);
+qg_status launch_dequant(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
+                         const void* mins, float g, float* w, int N, int K, cudaStream_t stream);
+qg_status launch_route(const float* logits, int M, int E, int topk, int32_t* ids, float* w,
+                       cudaStream_t stream);
+qg_status launch_moe(const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_g,
+                     const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_g, const void* x,
+                     const int32_t* ids, const float* tw, void* y, void* ws, size_t ws_bytes, int M,
+                     int H, int I, int E, int topk, cudaStream_t stream);
+size_t moe_workspace_bytes(int M, int topk, int H, int I, int E);
+
+}  // namespace qg

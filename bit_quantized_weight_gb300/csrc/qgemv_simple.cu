@@ -1,0 +1,155 @@
+// qgemv_simple.cu -- exact CUDA-core GEMV for shapes the TMA kernel does not
+// take (K not a multiple of 256), and the dequantisation export kernels.
+//
+// One warp per output row (per gate/up row pair for SwiGLU), lanes striding
+// over k, fp32 accumulation of exact products, a butterfly reduction across
+// the warp. Slow, simple and exact for every finite input.
+#include "common.cuh"
+
+#include <cuda_bf16.h>
+
+namespace qg {
+namespace {
+
+__device__ __forceinline__ float e2m1_value(uint32_t code)
+{
+    // f16 of the E2M1 code via the hardware conversion, then to fp32 (exact)
+    const uint32_t h2 = e2m1x2_to_f16x2(code & 0xFu);
+    return half_bits_to_f32(h2 & 0xFFFFu);
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t code)
+{
+    const uint32_t h2 = e4m3x2_to_f16x2(code & 0xFFu);
+    return half_bits_to_f32(h2 & 0xFFFFu);
+}
+
+// Weight w[n][k] in fp32: NVFP4 w = e2m1 * e4m3 (exact; g applied by the
+// caller); Q w = fmaf(scale, q, min).
+__device__ __forceinline__ float weight_at(int fmt, const uint8_t* codes, const uint8_t* q_hi,
+                                           const void* scales, const void* mins, int K, int n, int k)
+{
+    const uint8_t b = codes[static_cast<size_t>(n) * (K / 2) + k / 2];
+    const uint32_t nib = (k & 1) ? (b >> 4) : (b & 0xFu);
+    if (fmt == FMT_NVFP4) {
+        const uint8_t s = static_cast<const uint8_t*>(scales)[static_cast<size_t>(n) * (K / 16) + k / 16];
+        return e2m1_value(nib) * e4m3_value(s);
+    }
+    uint32_t q = nib;
+    if (fmt == FMT_Q5) q |= ((q_hi[static_cast<size_t>(n) * (K / 8) + k / 8] >> (k & 7)) & 1u) << 4;
+    const size_t gi = static_cast<size_t>(n) * (K / 32) + k / 32;
+    const float s = half_bits_to_f32(static_cast<const uint16_t*>(scales)[gi]);
+    const float m = half_bits_to_f32(static_cast<const uint16_t*>(mins)[gi]);
+    return fmaf(s, static_cast<float>(q), m);
+}
+
+__global__ void simple_kernel(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
+                              const void* mins, float g, const uint16_t* x, void* y, int out_f32,
+                              const uint16_t* residual, int M, int n_out, int K, int swiglu)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= n_out) return;
+    const int n = warp;
+    float acc[2][kMaxTokens];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int m = 0; m < kMaxTokens; ++m) acc[j][m] = 0.f;
+    for (int k = lane; k < K; k += 32) {
+        const float w0 = weight_at(fmt, codes, q_hi, scales, mins, K, n, k);
+        const float w1 = swiglu ? weight_at(fmt, codes, q_hi, scales, mins, K, n + n_out, k) : 0.f;
+#pragma unroll
+        for (int m = 0; m < kMaxTokens; ++m) {
+            if (m < M) {
+                const float xv = bf16_bits_to_f32(x[static_cast<size_t>(m) * K + k]);
+                acc[0][m] = fmaf(w0, xv, acc[0][m]);
+                if (swiglu) acc[1][m] = fmaf(w1, xv, acc[1][m]);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int m = 0; m < kMaxTokens; ++m)
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[j][m] += __shfl_xor_sync(0xffffffffu, acc[j][m], o);
+    if (lane != 0) return;
+    for (int m = 0; m < M; ++m) {
+        float v = acc[0][m] * g;
+        if (swiglu) {
+            const float u = acc[1][m] * g;
+            v = (v / (1.0f + expf(-v))) * u;
+        }
+        if (residual) v += bf16_bits_to_f32(residual[static_cast<size_t>(m) * n_out + n]);
+        if (out_f32)
+            static_cast<float*>(y)[static_cast<size_t>(m) * n_out + n] = v;
+        else
+            static_cast<uint16_t*>(y)[static_cast<size_t>(m) * n_out + n] = f32_to_bf16_bits_rn(v);
+    }
+}
+
+// Dequantise with the same device decode as the tensor-core kernel:
+// NVFP4: f16(e2m1) * f16(e4m3) (exact f16 product) -> fp32, times g.
+// Q: q through the 1024 + q f16 mantissa, then fmaf(scale, q, min).
+__global__ void dequant_kernel(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
+                               const void* mins, float g, float* w, int N, int K)
+{
+    const size_t pair = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t total_pairs = static_cast<size_t>(N) * (K / 2);
+    if (pair >= total_pairs) return;
+    const int n = static_cast<int>(pair / (K / 2));
+    const int k = static_cast<int>(pair % (K / 2)) * 2;
+    const uint32_t b = codes[pair];
+    float w0, w1;
+    if (fmt == FMT_NVFP4) {
+        const uint32_t s = static_cast<const uint8_t*>(scales)[static_cast<size_t>(n) * (K / 16) + k / 16];
+        const uint32_t sc = e4m3x2_to_f16x2(s | (s << 8));
+        const uint32_t p = hmul2(e2m1x2_to_f16x2(b), sc);
+        w0 = half_bits_to_f32(p & 0xFFFFu) * g;
+        w1 = half_bits_to_f32(p >> 16) * g;
+    } else {
+        uint32_t u = (b & 0xFu) | ((b >> 4) << 16) | 0x64006400u;
+        if (fmt == FMT_Q5) {
+            const uint32_t hb = q_hi[static_cast<size_t>(n) * (K / 8) + k / 8] >> (k & 7);
+            u |= ((hb & 1u) << 4) | (((hb >> 1) & 1u) << 20);
+        }
+        const uint32_t q = hsub2(u, 0x64006400u);
+        const size_t gi = static_cast<size_t>(n) * (K / 32) + k / 32;
+        const float s = half_bits_to_f32(static_cast<const uint16_t*>(scales)[gi]);
+        const float m = half_bits_to_f32(static_cast<const uint16_t*>(mins)[gi]);
+        w0 = fmaf(s, half_bits_to_f32(q & 0xFFFFu), m);
+        w1 = fmaf(s, half_bits_to_f32(q >> 16), m);
+    }
+    w[static_cast<size_t>(n) * K + k] = w0;
+    w[static_cast<size_t>(n) * K + k + 1] = w1;
+}
+
+}  // namespace
+
+qg_status launch_simple(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
+                        const void* mins, float g, const void* x, void* y, int out_f32,
+                        const void* residual, int M, int N, int K, int swiglu, cudaStream_t stream)
+{
+    const int n_out = swiglu ? N / 2 : N;
+    const int threads = 256;
+    const long long blocks = (static_cast<long long>(n_out) * 32 + threads - 1) / threads;
+    simple_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        fmt, codes, q_hi, scales, mins, g, static_cast<const uint16_t*>(x), y, out_f32,
+        static_cast<const uint16_t*>(residual), M, n_out, K, swiglu);
+    return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+qg_status launch_dequant(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
+                         const void* mins, float g, float* w, int N, int K, cudaStream_t stream)
+{
+    const size_t pairs = static_cast<size_t>(N) * (K / 2);
+    const int threads = 256;
+    const size_t blocks = (pairs + threads - 1) / threads;
+    if (blocks > 0x7FFFFFFFull) return QG_ERR_UNSUPPORTED;
+    dequant_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(fmt, codes, q_hi, scales, mins, g, w, N,
+                                                                           K);
+    return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+}  // namespace qg

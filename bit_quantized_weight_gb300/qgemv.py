@@ -1,0 +1,177 @@
+"""ctypes binding of libqgemv (argument marshalling only).
+
+The functions keep the C names. Tensor arguments are torch tensors on the
+current CUDA device in the layouts of include/qgemv.h; the call is enqueued on
+torch.cuda.current_stream(). A missing library raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+QG_OK = 0
+QG_ERR_INVALID_ARG = 1
+QG_ERR_UNSUPPORTED = 2
+QG_ERR_MISALIGNED = 3
+QG_ERR_WORKSPACE = 4
+QG_ERR_CUDA = 5
+QG_ERR_DEVICE_TIMEOUT = 6
+QG_OUT_BF16 = 0
+QG_OUT_F32 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libqgemv.so")
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+
+class QGemvError(RuntimeError):
+    def __init__(self, name, status):
+        super().__init__(f"{name} failed: {qg_status_string(status)} ({status})")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """Load libqgemv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"libqgemv.so not found at {_LIB_PATH}; build it with "
+                "`python bit_quantized_weight_gb300/build.py` (needs nvcc)")
+        L = ctypes.CDLL(_LIB_PATH)
+        L.qgemv_nvfp4.argtypes = [_P, _P, _F, _P, _P, _I, _P, _I, _I, _I, _P]
+        L.qgemv_q45.argtypes = [_P, _P, _P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _P]
+        L.qgemv_swiglu_nvfp4.argtypes = [_P, _P, _F, _P, _P, _I, _I, _I, _P]
+        L.moe_route_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P]
+        L.moe_qgemv_nvfp4_workspace_size.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_qgemv_nvfp4.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                      _I, _I, _I, _I, _I, _P]
+        L.qdequant_nvfp4.argtypes = [_P, _P, _F, _P, _I, _I, _P]
+        L.qdequant_q45.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _P]
+        L.qg_last_device_status.argtypes = [_P]
+        L.qg_status_string.argtypes = [_I]
+        L.qg_status_string.restype = ctypes.c_char_p
+        L.qg_debug_set_wait.argtypes = [ctypes.c_uint64, _I]
+        for name in ("qgemv_nvfp4", "qgemv_q45", "qgemv_swiglu_nvfp4", "moe_route_topk",
+                     "moe_qgemv_nvfp4_workspace_size", "moe_qgemv_nvfp4", "qdequant_nvfp4",
+                     "qdequant_q45", "qg_last_device_status", "qg_debug_set_wait"):
+            getattr(L, name).restype = _I
+        _lib = L
+    return _lib
+
+
+def qg_status_string(status: int) -> str:
+    return lib().qg_status_string(int(status)).decode()
+
+
+def _check(name, status):
+    if status != QG_OK:
+        raise QGemvError(name, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def qgemv_nvfp4(codes, scales, g, x, y, residual=None, stream=None):
+    """y[M][N] (bf16 or fp32 tensor) = NVFP4 W[N][K] @ x[M][K] (+ residual)."""
+    import torch
+    _cuda(codes, scales, x, y, residual)
+    M, K = x.shape
+    N = codes.shape[0]
+    out = QG_OUT_F32 if y.dtype == torch.float32 else QG_OUT_BF16
+    _check("qgemv_nvfp4", lib().qgemv_nvfp4(_ptr(codes), _ptr(scales), float(g), _ptr(x), _ptr(y), out,
+                                            _ptr(residual), M, N, K, _stream(stream)))
+    return y
+
+
+def qgemv_q45(q_lo, q_hi, scale, mn, bits, x, y, residual=None, stream=None):
+    import torch
+    _cuda(q_lo, q_hi, scale, mn, x, y, residual)
+    M, K = x.shape
+    N = q_lo.shape[0]
+    out = QG_OUT_F32 if y.dtype == torch.float32 else QG_OUT_BF16
+    _check("qgemv_q45", lib().qgemv_q45(_ptr(q_lo), _ptr(q_hi), _ptr(scale), _ptr(mn), int(bits), _ptr(x),
+                                        _ptr(y), out, _ptr(residual), M, N, K, _stream(stream)))
+    return y
+
+
+def qgemv_swiglu_nvfp4(codes, scales, g, x, y, stream=None):
+    _cuda(codes, scales, x, y)
+    M, K = x.shape
+    N = codes.shape[0]
+    _check("qgemv_swiglu_nvfp4", lib().qgemv_swiglu_nvfp4(_ptr(codes), _ptr(scales), float(g), _ptr(x),
+                                                          _ptr(y), M, N, K, _stream(stream)))
+    return y
+
+
+def moe_route_topk(logits, topk, ids, w, stream=None):
+    _cuda(logits, ids, w)
+    M, E = logits.shape
+    _check("moe_route_topk", lib().moe_route_topk(_ptr(logits), M, E, int(topk), _ptr(ids), _ptr(w),
+                                                  _stream(stream)))
+    return ids, w
+
+
+def moe_qgemv_nvfp4_workspace_size(M, topk, H, I, E) -> int:
+    b = ctypes.c_size_t(0)
+    _check("moe_qgemv_nvfp4_workspace_size",
+           lib().moe_qgemv_nvfp4_workspace_size(M, topk, H, I, E, ctypes.byref(b)))
+    return b.value
+
+
+def moe_qgemv_nvfp4(gu_codes, gu_scales, gu_g, dn_codes, dn_scales, dn_g, x, ids, w, y, workspace,
+                    stream=None):
+    _cuda(gu_codes, gu_scales, gu_g, dn_codes, dn_scales, dn_g, x, ids, w, y, workspace)
+    E, two_i, hh = gu_codes.shape
+    M, H = x.shape
+    topk = ids.shape[1]
+    _check("moe_qgemv_nvfp4", lib().moe_qgemv_nvfp4(
+        _ptr(gu_codes), _ptr(gu_scales), _ptr(gu_g), _ptr(dn_codes), _ptr(dn_scales), _ptr(dn_g), _ptr(x),
+        _ptr(ids), _ptr(w), _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        M, H, two_i // 2, E, topk, _stream(stream)))
+    return y
+
+
+def qdequant_nvfp4(codes, scales, g, w, stream=None):
+    _cuda(codes, scales, w)
+    N, K = w.shape
+    _check("qdequant_nvfp4", lib().qdequant_nvfp4(_ptr(codes), _ptr(scales), float(g), _ptr(w), N, K,
+                                                  _stream(stream)))
+    return w
+
+
+def qdequant_q45(q_lo, q_hi, scale, mn, bits, w, stream=None):
+    _cuda(q_lo, q_hi, scale, mn, w)
+    N, K = w.shape
+    _check("qdequant_q45", lib().qdequant_q45(_ptr(q_lo), _ptr(q_hi), _ptr(scale), _ptr(mn), int(bits),
+                                              _ptr(w), N, K, _stream(stream)))
+    return w
+
+
+def qg_last_device_status(stream=None) -> int:
+    return lib().qg_last_device_status(_stream(stream))
+
+
+def qg_debug_set_wait(limit_ns: int = 0, starve: bool = False) -> None:
+    _check("qg_debug_set_wait", lib().qg_debug_set_wait(int(limit_ns), int(bool(starve))))

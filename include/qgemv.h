@@ -1,0 +1,184 @@
+/*
+ * qgemv.h -- C ABI of libqgemv: decode-step GEMV / skinny GEMM (M = 1..8
+ * tokens) over low-bit block-scaled weights on one NVIDIA GB300 (sm_103a).
+ *
+ * What the pages say this is: single-GPU decode is memory-bandwidth bound and
+ * engines write one native fused kernel per weight format -- matmul, residual
+ * add and SwiGLU done in "one read, one write" -- with NVFP4 artefacts and a
+ * groupwise-int Q4/Q5 recipe (NInfer article, section 2 "自研 CUDA 算子
+ * 混合量化权重"); an "NVFP4 / MXFP8 block matvec" kernel and a "Top-8 gating
+ * and softmax" MoE router (Decapybara README, "Blackwell CUDA 内核套件",
+ * mx_gemv.cu and moe.cu); 1..8 concurrent decode lanes batched into one step
+ * (NInfer article, section 1 "单卡专用架构"). The pages print no bit layout;
+ * the layouts below are this library's contract.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major,
+ *     16-byte aligned (else QG_ERR_MISALIGNED). The library allocates no
+ *     device memory per call; it owns one 4-byte device status word.
+ *   - Work is enqueued on `stream` (0 = legacy default stream) and the call
+ *     returns without synchronising. Inputs must stay valid and unmodified,
+ *     and outputs untouched by others, until the stream work completes.
+ *     Outputs must not alias inputs, except `residual` == `y` (in place).
+ *   - Arguments are validated before anything is launched; a rejected call
+ *     launches nothing. A launch failure returns QG_ERR_CUDA and leaves the
+ *     CUDA error retrievable with cudaGetLastError().
+ *   - Activations x and residuals are bf16 [M][K] / [M][N]; M in [1, 8]
+ *     (the 1..8 decode lanes); K % 32 == 0 and K >= 32; N >= 1.
+ *   - Weights are read once per call; accumulation is fp32.
+ *
+ * Weight formats
+ *   NVFP4: codes u8[N][K/2], two FP4 E2M1 codes per byte, the low nibble
+ *          holding the even k; scales u8[N][K/16], one FP8 E4M3 (OCP "FN"
+ *          variant) per 16 consecutive k; one fp32 per-tensor scale g.
+ *          w[n][k] = e2m1(code) * e4m3(scale[n][k/16]) * g.
+ *   Q4/Q5: q_lo u8[N][K/2] (low 4 bits of the unsigned code, low nibble =
+ *          even k); Q5 adds q_hi u8[N][K/8] holding the 5th bit of k as bit
+ *          k%8 of byte k/8; scale and min are fp16 [N][K/32].
+ *          w[n][k] = scale[n][k/32] * q + min[n][k/32].
+ *
+ * Output accuracy: for every output element, with B = 1e-4 * sum_k |w x| +
+ * 1e-6, an fp32 output lies within B of the exact sum, and a bf16 output is
+ * the round-to-nearest-even of a value within B of it. Dequantised weights
+ * (qdequant_*) are bit-exact fp32 roundings of the exact weight values.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define QG_API __attribute__((visibility("default")))
+#else
+#define QG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QG_OK = 0,
+    QG_ERR_INVALID_ARG = 1,    /* a size, pointer or enum is out of range   */
+    QG_ERR_UNSUPPORTED = 2,    /* valid request this build does not serve    */
+    QG_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned           */
+    QG_ERR_WORKSPACE = 4,      /* MoE workspace missing or too small         */
+    QG_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed       */
+    QG_ERR_DEVICE_TIMEOUT = 6  /* a bounded device-side wait ran out         */
+} qg_status;
+
+typedef enum { QG_OUT_BF16 = 0, QG_OUT_F32 = 1 } qg_out;
+
+/*
+ * y[m][n] = g * sum_k e2m1(code[n][k]) * e4m3(scale[n][k/16]) * x[m][k]
+ *           (+ residual[m][n])
+ * NVFP4 dense GEMV with an optional fused residual add (NInfer article,
+ * section 2: fused matmul + residual add per weight format).
+ *   codes    u8[N][K/2]     scales u8[N][K/16]     global_scale g (by value)
+ *   x        bf16[M][K]     y bf16 or fp32 [M][N] per y_dtype
+ *   residual bf16[M][N] or NULL (added in fp32 before the output rounding)
+ */
+QG_API qg_status qgemv_nvfp4(const uint8_t* codes, const uint8_t* scales, float global_scale,
+                      const void* x, void* y, qg_out y_dtype, const void* residual,
+                      int M, int N, int K, cudaStream_t stream);
+
+/*
+ * y[m][n] = sum_k (scale[n][k/32] * q[n][k] + min[n][k/32]) * x[m][k]
+ *           (+ residual[m][n])
+ * Groupwise-int Q4/Q5 GEMV (NInfer article, section 2: the groupwise-int
+ * recipe puts Q/K projections in Q4 and gate/V in Q5).
+ *   q_lo u8[N][K/2]; q_hi u8[N][K/8] for bits == 5, must be NULL for bits == 4
+ *   scale, min fp16[N][K/32]; bits in {4, 5}; x, y, y_dtype, residual as above.
+ */
+QG_API qg_status qgemv_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min,
+                    int bits, const void* x, void* y, qg_out y_dtype, const void* residual,
+                    int M, int N, int K, cudaStream_t stream);
+
+/*
+ * SwiGLU-fused NVFP4 gate/up projection (NInfer article, section 2: fused
+ * SwiGLU). The N = 2I weight rows are the gate rows [0, I) followed by the up
+ * rows [I, 2I); with a = gate row i and b = up row i,
+ *   y[m][i] = bf16_rne( silu(a . x[m]) * (b . x[m]) ),  silu(v) = v / (1 + e^-v).
+ *   codes u8[N][K/2], scales u8[N][K/16], g by value, x bf16[M][K],
+ *   y bf16[M][N/2]; N must be even.
+ */
+QG_API qg_status qgemv_swiglu_nvfp4(const uint8_t* codes, const uint8_t* scales, float global_scale,
+                             const void* x, void* y, int M, int N, int K, cudaStream_t stream);
+
+/*
+ * MoE router (Decapybara README, moe.cu: "Top-8 gating and softmax"):
+ * p = softmax(logits[m]); the topk largest p in descending order, ties to the
+ * lower expert id; w = p_top / sum(p_top).
+ *   logits fp32[M][E]; topk_ids int32[M][topk] out; topk_w fp32[M][topk] out;
+ *   1 <= topk <= 8, topk <= E <= 1024, M in [1, 8].
+ */
+QG_API qg_status moe_route_topk(const float* logits, int M, int E, int topk, int32_t* topk_ids,
+                         float* topk_w, cudaStream_t stream);
+
+/* Bytes of device workspace moe_qgemv_nvfp4 needs for these sizes. */
+QG_API qg_status moe_qgemv_nvfp4_workspace_size(int M, int topk, int H, int I, int E, size_t* bytes);
+
+/*
+ * Expert-gathered MoE FFN over NVFP4 experts (35B-A3B-class decode layer;
+ * NInfer article, section 2, and Decapybara README, moe.cu). For each token m
+ * and slot i < topk with e = topk_ids[m][i]:
+ *   h[m][i] = bf16_rne( silu(G_e x[m]) * (U_e x[m]) )      (length I)
+ *   y[m]    = bf16_rne( sum_{i ascending} topk_w[m][i] * g_dn[e] * D_e h[m][i] )
+ * where gate/up rows of expert e are rows [0, I) and [I, 2I) of
+ * gu_codes[e] (scaled by gu_gscale[e]) and D_e is dn_codes[e] (scaled by
+ * dn_gscale[e]). Each active expert's weights are read once for all of its
+ * tokens; the combine is deterministic (fixed slot order, no atomics).
+ *   gu_codes u8[E][2I][H/2], gu_scales u8[E][2I][H/16], gu_gscale fp32[E] (device)
+ *   dn_codes u8[E][H][I/2],  dn_scales u8[E][H][I/16],  dn_gscale fp32[E] (device)
+ *   x bf16[M][H]; topk_ids int32[M][topk]; topk_w fp32[M][topk]; y bf16[M][H]
+ *   workspace: caller-owned device memory of at least
+ *   moe_qgemv_nvfp4_workspace_size() bytes, 256-byte aligned. It starts with
+ *   h as bf16[M][topk][I]; the rest is private scratch.
+ * Expert ids outside [0, E) are not checked on the host (they are device
+ * data); such a slot contributes nothing and records QG_ERR_INVALID_ARG in the
+ * device status word (see qg_last_device_status).
+ * H % 256 == 0, I % 256 == 0, 1 <= topk <= 8, M in [1, 8].
+ */
+QG_API qg_status moe_qgemv_nvfp4(const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_gscale,
+                          const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_gscale,
+                          const void* x, const int32_t* topk_ids, const float* topk_w, void* y,
+                          void* workspace, size_t workspace_bytes, int M, int H, int I, int E,
+                          int topk, cudaStream_t stream);
+
+/*
+ * Dequantise to fp32 w[N][K] with the same device decode the GEMV kernels
+ * use (test hook for the bit-exact check). NVFP4: w = fp32(e2m1 * e4m3) * g,
+ * one rounding. Q4/Q5: w = fmaf(scale, q, min), one rounding.
+ */
+QG_API qg_status qdequant_nvfp4(const uint8_t* codes, const uint8_t* scales, float global_scale,
+                         float* w, int N, int K, cudaStream_t stream);
+QG_API qg_status qdequant_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min,
+                       int bits, float* w, int N, int K, cudaStream_t stream);
+
+/*
+ * Synchronise `stream`, then return and clear the device status word:
+ * QG_OK, QG_ERR_DEVICE_TIMEOUT when a bounded device-side wait gave up (the
+ * kernel stopped early; its outputs are undefined), or QG_ERR_INVALID_ARG for
+ * out-of-range device data (MoE expert ids).
+ */
+QG_API qg_status qg_last_device_status(cudaStream_t stream);
+
+/* Static, NUL-terminated name of a status code. */
+QG_API const char* qg_status_string(qg_status status);
+
+/*
+ * Fault-injection hook for testing the bounded-wait path. Sets the time
+ * limit (ns) of every device-side wait for subsequent launches on this host
+ * thread's process (0 restores the default of two seconds). With
+ * starve != 0, the weight-streaming warps of the dense kernels issue no copies, so
+ * the consumer waits run out and the kernels return early with
+ * QG_ERR_DEVICE_TIMEOUT recorded. Not for production use.
+ */
+QG_API qg_status qg_debug_set_wait(uint64_t limit_ns, int starve);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QGEMV_H */

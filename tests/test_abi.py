@@ -1,0 +1,132 @@
+"""The C-ABI library: it builds, loads, exports every declared symbol, and
+rejects bad arguments with the documented status before launching anything
+(no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from bit_quantized_weight_gb300 import build as B
+    if B.needs_build():
+        B.build()
+    import bit_quantized_weight_gb300 as q
+    return q.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*QG_API\s+(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("qgemv_nvfp4", "qgemv_q45", "qgemv_swiglu_nvfp4", "moe_qgemv_nvfp4",
+              "moe_qgemv_nvfp4_workspace_size", "moe_route_topk", "qdequant_nvfp4", "qdequant_q45",
+              "qg_last_device_status", "qg_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in include/qgemv.h but not exported"
+
+
+def test_library_hides_cuda_runtime_symbols(L):
+    for name in ("cudaMalloc", "cudaLaunchKernel", "cudaStreamSynchronize"):
+        with pytest.raises(AttributeError):
+            getattr(L, name)
+
+
+def test_status_strings(L):
+    import bit_quantized_weight_gb300 as q
+    assert q.qg_status_string(0) == "QG_OK"
+    assert q.qg_status_string(q.QG_ERR_DEVICE_TIMEOUT) == "QG_ERR_DEVICE_TIMEOUT"
+    assert q.qg_status_string(99) == "QG_ERR_UNKNOWN"
+
+
+A = 0x100000  # fake, 16-byte-aligned addresses: validation never dereferences
+
+
+def _no_visible_gpu():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except Exception:
+        return True
+
+
+# These calls pass fake device addresses and must be rejected before any
+# launch; they only run where no GPU is visible, so a regression that let one
+# through could never touch a device. (The GPU suite repeats the rejections
+# with real, deliberately misaligned allocations.)
+fake_ptr = pytest.mark.skipif(not _no_visible_gpu(), reason="fake-pointer validation runs without a GPU")
+
+
+@pytest.mark.parametrize("M,N,K,want", [
+    (0, 16, 256, 1), (9, 16, 256, 1), (1, 0, 256, 1), (1, 16, 0, 1), (1, 16, 48, 1), (1, 16, 16, 1),
+])
+@fake_ptr
+def test_dense_rejects_bad_sizes(L, M, N, K, want):
+    assert L.qgemv_nvfp4(A, A, 1.0, A, A, 0, None, M, N, K, None) == want
+    assert L.qgemv_swiglu_nvfp4(A, A, 1.0, A, A, M, 2 * N, K, None) == want
+    assert L.qgemv_q45(A, None, A, A, 4, A, A, 0, None, M, N, K, None) == want
+
+
+@fake_ptr
+def test_dense_rejects_null_and_misaligned(L):
+    assert L.qgemv_nvfp4(None, A, 1.0, A, A, 0, None, 1, 16, 256, None) == 1
+    assert L.qgemv_nvfp4(A, A, 1.0, A + 8, A, 0, None, 1, 16, 256, None) == 3
+    assert L.qgemv_nvfp4(A, A, 1.0, A, A + 2, 0, None, 1, 16, 256, None) == 3
+    assert L.qgemv_nvfp4(A, A, 1.0, A, A, 0, A + 4, 1, 16, 256, None) == 3
+    assert L.qgemv_nvfp4(A, A, 1.0, A, A, 7, None, 1, 16, 256, None) == 1      # bad y dtype
+    assert L.qgemv_swiglu_nvfp4(A, A, 1.0, A, A, 1, 15, 256, None) == 1        # odd N
+
+
+@fake_ptr
+def test_q45_rejects_bad_bits_and_planes(L):
+    assert L.qgemv_q45(A, None, A, A, 3, A, A, 0, None, 1, 16, 256, None) == 1
+    assert L.qgemv_q45(A, None, A, A, 5, A, A, 0, None, 1, 16, 256, None) == 1  # Q5 needs q_hi
+    assert L.qgemv_q45(A, A, A, A, 4, A, A, 0, None, 1, 16, 256, None) == 1     # Q4 takes none
+    assert L.qgemv_q45(A, A, A, None, 5, A, A, 0, None, 1, 16, 256, None) == 1
+    assert L.qgemv_q45(A, A + 1, A, A, 5, A, A, 0, None, 1, 16, 256, None) == 3
+
+
+@fake_ptr
+def test_router_and_moe_validation(L):
+    assert L.moe_route_topk(A, 8, 128, 9, A, A, None) == 1
+    assert L.moe_route_topk(A, 8, 4, 8, A, A, None) == 1
+    assert L.moe_route_topk(A, 0, 128, 8, A, A, None) == 1
+    assert L.moe_route_topk(A + 4, 8, 128, 8, A, A, None) == 3
+    sz = ctypes.c_size_t(0)
+    assert L.moe_qgemv_nvfp4_workspace_size(8, 8, 2048, 768, 128, ctypes.byref(sz)) == 0
+    assert sz.value > 8 * 8 * 768 * 2
+    assert L.moe_qgemv_nvfp4_workspace_size(8, 8, 2000, 768, 128, ctypes.byref(sz)) == 1
+    args = [A] * 10
+    # workspace too small / missing
+    assert L.moe_qgemv_nvfp4(*args, A, 16, 8, 2048, 768, 128, 8, None) == 4
+    assert L.moe_qgemv_nvfp4(*args, None, 1 << 30, 8, 2048, 768, 128, 8, None) == 4
+    assert L.moe_qgemv_nvfp4(*args, A + 16, 1 << 30, 8, 2048, 768, 128, 8, None) == 3
+    assert L.moe_qgemv_nvfp4(*args, A, 1 << 30, 8, 2048, 768, 128, 9, None) == 1
+
+
+@fake_ptr
+def test_dequant_validation(L):
+    assert L.qdequant_nvfp4(A, A, 1.0, A, 0, 256, None) == 1
+    assert L.qdequant_nvfp4(A, A, 1.0, A + 4, 16, 256, None) == 3
+    assert L.qdequant_q45(A, None, A, A, 5, A, 16, 256, None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import bit_quantized_weight_gb300.qgemv as qm
+    monkeypatch.setattr(qm, "_lib", None)
+    monkeypatch.setattr(qm, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not found"):
+        qm.lib()
