@@ -132,7 +132,8 @@ def nvfp4_weights(seed: int, name: str, N: int, K: int, g: float = 1.0) -> dict:
     codes = rng_for(seed, name + ".codes").integers(0, 256, size=(N, K // 2), dtype=np.uint8)
     u = rng_for(seed, name + ".scales").uniform(-4.0, 2.0, size=(N, K // 16))
     scales = _to_e4m3_bits(np.exp2(u))
-    return {"codes": codes, "scales": scales, "g": float(g), "N": N, "K": K}
+    # the per-tensor scale is an FP32 value: store exactly what the kernel gets
+    return {"codes": codes, "scales": scales, "g": float(np.float32(g)), "N": N, "K": K}
 
 
 def q45_weights(seed: int, name: str, N: int, K: int, bits: int) -> dict:

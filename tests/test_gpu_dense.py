@@ -59,7 +59,7 @@ def test_dequant_nvfp4_bit_exact(g):
     w["codes"][:, :128] = (np.arange(128)[None, :] * 2 + np.arange(N)[:, None]) % 256
     d = nvfp4_dev(w)
     out = torch.empty((N, K), dtype=torch.float32, device="cuda")
-    q.qdequant_nvfp4(d["codes"], d["scales"], g, out)
+    q.qdequant_nvfp4(d["codes"], d["scales"], w["g"], out)
     ref = O.dequant_nvfp4(w).astype(np.float32)          # RNE fp64 -> fp32
     assert same_f32_bits(out.cpu().numpy(), ref)
 
