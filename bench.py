@@ -1,0 +1,549 @@
+#!/usr/bin/env python
+"""Benchmark of the quantised decode GEMV hot path on GB300.
+
+One step = one pass of a decode layer's projections through libqgemv on one
+batch of M tokens:
+  dense (default): 27B-class layer, NVFP4 -- QKV 7168x5120, O 5120x6144,
+                   gate+up 34816x5120 with the SwiGLU epilogue, down 5120x17408
+                   with the residual epilogue; every projection reads its own
+                   bf16 N(0, 1) activations;
+  q45:             the same shapes under the mixed Q4/Q5 recipe;
+  tiny:            one NVFP4 256x512 GEMV.
+Metric: effective weight-bytes GB/s (weight bytes per step / step time).
+
+Timing: W untimed warm-up steps, then exactly K steps captured in one CUDA
+graph and bracketed by CUDA events on the launching stream (barrier +
+synchronize on both sides, max over ranks). Each step reads a different copy
+of the layer's weights from a rotation whose total exceeds L2 several times,
+so every step streams its weights from HBM. Per-kernel durations come from
+events recorded between the kernels inside the graph.
+
+e2e: the same metric through the public Python API with pinned host buffers:
+every step copies its activations host->device, runs the projections, and
+copies the outputs device->host, all inside the timed region.
+
+--impl reference: the fp64 CPU oracle (the checker, not a product path) timed
+on the host cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized decode GEMV effective HBM GB/s (% of GB300 peak) and µs/call, M=1–8"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["dense", "q45", "tiny"], default="dense")
+    ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ environment
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.strip().split(",") for r in self.f.read().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for i, nm in enumerate(names):
+                    if r[5 + i].strip().lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("qgemv_dense.cu", "common.cuh", "qgemv_internal.h"):
+        with open(os.path.join(ROOT, "bit_quantized_weight_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag):
+    """DRAM bytes per launch of `kernel_tag` from the committed ncu summary,
+    or None if there is none or the kernel sources changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[kernel_tag]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ workloads
+class Workload:
+    """Host inputs, device weight copies and the per-step call sequence."""
+
+    def __init__(self, kind, M, copies_min_bytes):
+        import numpy as np
+        import torch
+        import synth
+        self.kind, self.M = kind, M
+        self.np, self.torch = np, torch
+        dev = torch.device("cuda", torch.cuda.current_device())
+        self.dev = dev
+        # -------- host inputs
+        self.projs = []  # (name, N, K, epi, host weights)
+        if kind == "dense":
+            for name, N, K, epi in synth.dense_layer_shapes():
+                self.projs.append((name, N, K, epi, synth.nvfp4_weights(1, f"dense.{name}", N, K)))
+        elif kind == "tiny":
+            c = synth.TINY
+            self.projs.append(("tiny", c.N, c.K, "none", synth.nvfp4_weights(0, "tiny.w", c.N, c.K)))
+        else:
+            for name, N, K, bits in synth.Q45_RECIPE:
+                epi = "residual" if name == "down" else "none"
+                self.projs.append((name, N, K, epi, synth.q45_weights(3, f"q45.{name}", N, K, bits)))
+        self.weight_bytes = sum(self._wbytes(w) for *_, w in self.projs)
+        # -------- activation inputs, packed in one buffer (one H2D copy per step)
+        self.in_layout, off = {}, 0
+        for name, N, K, epi, _ in self.projs:
+            self.in_layout[f"x.{name}"] = (off, (M, K))
+            off += M * K
+            if epi == "residual":
+                self.in_layout[f"r.{name}"] = (off, (M, N))
+                off += M * N
+        self.in_elems = off
+        host_in = np.zeros(off, np.uint16)
+        for key, (o, shp) in self.in_layout.items():
+            host_in[o:o + shp[0] * shp[1]] = synth.bf16_normal(2, f"bench.{kind}.{key}.M{M}", shp).ravel()
+        self.host_in = host_in
+        # -------- outputs packed in one buffer (one D2H copy per step)
+        self.out_layout, off = {}, 0
+        for name, N, K, epi, _ in self.projs:
+            n_out = N // 2 if epi == "swiglu" else N
+            self.out_layout[name] = (off, (M, n_out))
+            off += M * n_out
+        self.out_elems = off
+        # -------- device buffers
+        self.d_in = torch.from_numpy(host_in.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.d_out = torch.empty(self.out_elems, dtype=torch.bfloat16, device=dev)
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 * 2 ** 20)
+        self.l2_bytes = int(l2)
+        self.copies = max(2, math.ceil(copies_min_bytes * self.l2_bytes / max(self.weight_bytes, 1)))
+        self.dev_w = [[self._upload(w) for *_, w in self.projs]]
+        for _ in range(self.copies - 1):
+            self.dev_w.append([{k: (v.clone() if hasattr(v, "clone") else v) for k, v in d.items()}
+                               for d in self.dev_w[0]])
+
+    def _wbytes(self, w):
+        if "codes" in w:
+            return w["codes"].nbytes + w["scales"].nbytes
+        b = w["q_lo"].nbytes + w["scale"].nbytes + w["min"].nbytes
+        return b + (w["q_hi"].nbytes if w.get("q_hi") is not None else 0)
+
+    def _upload(self, w):
+        np, torch = self.np, self.torch
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
+        if "codes" in w:
+            return {"codes": t(w["codes"]), "scales": t(w["scales"]), "g": w["g"]}
+        return {"q_lo": t(w["q_lo"]), "q_hi": None if w.get("q_hi") is None else t(w["q_hi"]),
+                "scale": t(w["scale"].view(np.int16)).view(torch.float16),
+                "min": t(w["min"].view(np.int16)).view(torch.float16), "bits": w["bits"]}
+
+    def view_in(self, key):
+        o, shp = self.in_layout[key]
+        return self.d_in[o:o + shp[0] * shp[1]].view(shp)
+
+    def view_out(self, name):
+        o, shp = self.out_layout[name]
+        return self.d_out[o:o + shp[0] * shp[1]].view(shp)
+
+    def kernel_names(self):
+        return [p[0] for p in self.projs]
+
+    def call(self, idx, copy):
+        """Enqueue call idx of the step on the current stream."""
+        import bit_quantized_weight_gb300 as q
+        name, N, K, epi, _ = self.projs[idx]
+        w = self.dev_w[copy % self.copies][idx]
+        y = self.view_out(name)
+        x = self.view_in(f"x.{name}")
+        r = self.view_in(f"r.{name}") if epi == "residual" else None
+        if "codes" in w:
+            if epi == "swiglu":
+                q.qgemv_swiglu_nvfp4(w["codes"], w["scales"], w["g"], x, y)
+            else:
+                q.qgemv_nvfp4(w["codes"], w["scales"], w["g"], x, y, residual=r)
+        else:
+            q.qgemv_q45(w["q_lo"], w["q_hi"], w["scale"], w["min"], w["bits"], x, y, residual=r)
+
+    def step(self, copy, events=None):
+        """Enqueue one step on the current stream; events[i] is recorded
+        before call i and events[-1] after the last call."""
+        for i in range(len(self.projs)):
+            if events is not None:
+                events[i].record()
+            self.call(i, copy)
+        if events is not None:
+            events[-1].record()
+
+    def launches_per_step(self):
+        return len(self.projs)
+
+    def alg_bytes(self, idx):
+        """Algorithmic bytes of call idx: weights + activations in + outputs."""
+        name, N, K, epi, w = self.projs[idx]
+        n_out = N // 2 if epi == "swiglu" else N
+        b = self._wbytes(w) + 2 * self.M * K + 2 * self.M * n_out
+        if epi == "residual":
+            b += 2 * self.M * n_out
+        return b
+
+    def describe(self):
+        if self.kind == "dense":
+            return ("dense 27B-class decode layer, NVFP4: QKV 7168x5120, O 5120x6144, "
+                    f"gate+up 34816x5120 + SwiGLU, down 5120x17408 + residual, M={self.M}")
+        if self.kind == "q45":
+            return ("mixed Q4/Q5 groupwise-int layer on the 27B-class shapes (QK Q4, V Q5, O Q4, "
+                    f"gate Q5, up Q4, down Q4 + residual), M={self.M}")
+        return f"tiny NVFP4 GEMV 256x512, M={self.M}"
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_step_sample(wl_projs, M, frac, threads):
+    """Run the fp64 oracle on every `1/frac`-th output row of each projection;
+    returns (seconds, weight bytes processed)."""
+    import numpy as np
+    import oracle as O
+    import synth
+    t_total, bytes_done = 0.0, 0
+    for name, N, K, epi, w in wl_projs:
+        rows = np.arange(0, N, frac)
+        x = synth.bf16_normal(2, f"oracle.{name}.M{M}", (M, K))
+        if "codes" in w:
+            ws = {"codes": w["codes"][rows], "scales": w["scales"][rows], "g": w["g"]}
+            t0 = time.perf_counter()
+            O.gemv_nvfp4(ws, x, threads=threads)
+            t_total += time.perf_counter() - t0
+            bytes_done += ws["codes"].nbytes + ws["scales"].nbytes
+        else:
+            ws = {"q_lo": w["q_lo"][rows], "q_hi": None if w.get("q_hi") is None else w["q_hi"][rows],
+                  "scale": w["scale"][rows], "min": w["min"][rows], "bits": w["bits"]}
+            t0 = time.perf_counter()
+            O.gemv_q45(ws, x, threads=threads)
+            t_total += time.perf_counter() - t0
+            bytes_done += sum(a.nbytes for a in (ws["q_lo"], ws["scale"], ws["min"]) if a is not None)
+            if ws["q_hi"] is not None:
+                bytes_done += ws["q_hi"].nbytes
+    return t_total, bytes_done
+
+
+def host_projs(kind):
+    import synth
+    out = []
+    if kind == "dense":
+        for name, N, K, epi in synth.dense_layer_shapes():
+            out.append((name, N, K, epi, synth.nvfp4_weights(1, f"dense.{name}", N, K)))
+    elif kind == "tiny":
+        c = synth.TINY
+        out.append(("tiny", c.N, c.K, "none", synth.nvfp4_weights(0, "tiny.w", c.N, c.K)))
+    else:
+        for name, N, K, bits in synth.Q45_RECIPE:
+            out.append((name, N, K, "none", synth.q45_weights(3, f"q45.{name}", N, K, bits)))
+    return out
+
+
+def cpu_baseline(kind, M, budget_s=12.0):
+    """Oracle throughput on this host's cores over a bounded row sample."""
+    import oracle as O
+    threads = O.default_threads()
+    projs = host_projs(kind)
+    frac = 64
+    t, b = oracle_step_sample(projs, M, frac, threads)
+    if t < budget_s / 4 and frac > 1:                 # grow the sample toward the budget
+        frac = max(1, int(frac * t / (budget_s / 2))) if t > 0 else 1
+        t, b = oracle_step_sample(projs, M, frac, threads)
+    return {"value": b / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"every {frac}th output row of each projection of one step (M={M}), "
+                      f"{b / 1e6:.1f} MB of weights in {t:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle as O
+    threads = O.default_threads()
+    projs = host_projs(args.workload)
+    frac = 64
+    for _ in range(args.warmup):
+        oracle_step_sample(projs, args.M, frac * 4, threads)
+    tt, bb = 0.0, 0
+    for _ in range(args.steps):
+        t, b = oracle_step_sample(projs, args.M, frac, threads)
+        tt += t
+        bb += b
+    v = bb / tt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{args.workload} (oracle over a row sample)", "M": args.M},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"every {frac}th output row of each projection per step"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    import torch
+    import bit_quantized_weight_gb300 as q
+    torch.cuda.set_device(local)
+    if args.workload == "tiny":
+        args.M = 1
+    wl = Workload(args.workload, args.M, copies_min_bytes=4)
+    stream = torch.cuda.Stream()
+    n_calls = wl.launches_per_step()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):                 # eager warm-up
+            wl.step(i)
+    stream.synchronize()
+    assert q.qg_last_device_status(stream) == q.QG_OK
+
+    # ---- capture K steps (and a warm-up graph of W steps) with in-graph events
+    def make_events(n):
+        try:
+            return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
+        except (TypeError, RuntimeError):
+            return None
+
+    ev_steps = [make_events(n_calls + 1) for _ in range(args.steps)]
+    per_kernel = ev_steps[0] is not None
+    g_warm, g_main = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_warm, stream=stream):
+        for i in range(args.warmup):
+            wl.step(i)
+    with torch.cuda.graph(g_main, stream=stream):
+        for i in range(args.steps):
+            wl.step(args.warmup + i, ev_steps[i] if per_kernel else None)
+    g_warm.replay()
+    stream.synchronize()
+
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)                                  # let the sampler take its first reading
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        g_main.replay()
+        t1.record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    ms = max_over_ranks(ms, world)
+    st = q.qg_last_device_status(stream)
+    if st != q.QG_OK:
+        raise RuntimeError(f"device status {q.qg_status_string(st)} after the timed region")
+
+    value = wl.weight_bytes * args.steps * world / (ms * 1e-3) / 1e9
+    ms_per_step = ms / args.steps
+
+    # ---- per-kernel durations (in-graph events) and the dominant kernel's roofline
+    us_per_call, dom = {}, None
+    if per_kernel:
+        names = wl.kernel_names()
+        sums = [0.0] * n_calls
+        for evs in ev_steps:
+            for i in range(n_calls):
+                sums[i] += evs[i].elapsed_time(evs[i + 1])
+        for i, nm in enumerate(names):
+            us_per_call[nm] = sums[i] / args.steps * 1e3
+        dom = max(range(n_calls), key=lambda i: sums[i])
+    else:
+        # no in-graph events: time the largest call alone, K launches in one graph
+        dom = max(range(n_calls), key=lambda i: wl.alg_bytes(i))
+        g_dom = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_dom, stream=stream):
+            for i in range(args.steps):
+                wl.call(dom, i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g_dom.replay()
+            e1.record(stream)
+        stream.synchronize()
+        us_per_call[wl.kernel_names()[dom]] = e0.elapsed_time(e1) / args.steps * 1e3
+    peak, peak_kind = measured_peaks()
+    dom_name = wl.kernel_names()[dom]
+    dom_us = us_per_call[dom_name]
+    achieved = wl.alg_bytes(dom) / (dom_us * 1e-6) / 1e9
+    traffic = profiled_traffic(f"{args.workload}.{dom_name}.M{args.M}")
+    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s", "traffic": traffic,
+                "alg_bytes_per_launch": wl.alg_bytes(dom), "us_per_launch": dom_us}
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_in = torch.from_numpy(wl.host_in.view("int16")).view(torch.bfloat16).pin_memory()
+        h_out = torch.empty(wl.out_elems, dtype=torch.bfloat16).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                wl.d_in.copy_(h_in, non_blocking=True)
+                wl.step(i)
+                h_out.copy_(wl.d_out, non_blocking=True)
+            stream.synchronize()
+            barrier(world)
+            e0.record(stream)
+            for i in range(args.steps):
+                wl.d_in.copy_(h_in, non_blocking=True)
+                wl.step(i)
+                h_out.copy_(wl.d_out, non_blocking=True)
+            e1.record(stream)
+        stream.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1), world)
+        e2e = {"value": wl.weight_bytes * args.steps * world / (ems * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": wl.in_elems * 2, "d2h_bytes_per_step": wl.out_elems * 2,
+               "ms_per_step": ems / args.steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload, args.M)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16 MMA of exact decoded weights, f32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": wl.describe(), "M": args.M, "weight_bytes_per_step": wl.weight_bytes,
+                       "l2": f"weights rotate over {wl.copies} copies of the layer "
+                             f"({wl.copies * wl.weight_bytes / 1e6:.0f} MB vs {wl.l2_bytes / 1e6:.0f} MB L2)",
+                       "parallelism": "one independent replica per GPU" if world > 1 else "single GPU",
+                       "graph": "K steps captured in one CUDA graph"},
+            "frac_of_8tbs": value / world / NOMINAL_HBM_GBS,
+            "frac_of_measured_hbm": value / world / peak,
+            "us_per_call": us_per_call,
+            "roofline": roofline,
+            "gpu_launches": n_calls * args.steps,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -100,91 +100,63 @@ __device__ __forceinline__ int prescale_exponent(uint32_t mag)
     return 147 - lg;
 }
 
-// Convert one token's 256-k chunk (8 values per lane) to prescaled f16.
-// Returns the f16 values packed in the format's pair order and reports
-// whether every value was represented exactly.
+// Pack 8 16-bit values in the format's pair order: natural k order for
+// NVFP4 ({k, k+1} pairs, matching the e2m1x2 decode), {k, k+4} pairs for Q
+// (matching the 1024 + q mantissa decode).
 template <int FMT>
-__device__ __forceinline__ uint4 convert_chunk8(const uint4 raw, int p, bool& exact, float& lane_sum)
+__device__ __forceinline__ uint4 pack_pairs(const uint32_t (&h)[8])
 {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-    float v[8];
-    uint32_t h[8];
-    exact = true;
-    lane_sum = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        v[2 * i] = ldexp_exact(bf16_bits_to_f32(w[i] & 0xFFFFu), p);
-        v[2 * i + 1] = ldexp_exact(bf16_bits_to_f32(w[i] >> 16), p);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        __half hv = __float2half_rn(v[i]);
-        h[i] = __half_as_ushort(hv);
-        float back = __half2float(hv);
-        if (isfinite(v[i]) && back != v[i]) exact = false;
-        lane_sum += v[i];
-    }
-    uint4 out;
-    if (FMT == FMT_NVFP4) {
-        out.x = h[0] | (h[1] << 16);
-        out.y = h[2] | (h[3] << 16);
-        out.z = h[4] | (h[5] << 16);
-        out.w = h[6] | (h[7] << 16);
-    } else {
-        out.x = h[0] | (h[4] << 16);
-        out.y = h[1] | (h[5] << 16);
-        out.z = h[2] | (h[6] << 16);
-        out.w = h[3] | (h[7] << 16);
-    }
-    return out;
+    if (FMT == FMT_NVFP4)
+        return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+    return make_uint4(h[0] | (h[4] << 16), h[1] | (h[5] << 16), h[2] | (h[6] << 16), h[3] | (h[7] << 16));
 }
 
-// Residual term `term` (>= 1) of 8 exact values already multiplied by 2^p:
-// r_0 = v, r_{t+1} = (r_t - f16(r_t)) * 2^24. Returns f16 pairs of r_term in
-// the format's pair order and whether anything is left after it.
-template <int FMT>
-__device__ __forceinline__ uint4 residual_term8(const uint4 raw, int p, int term, bool& more)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t h[8];
-    more = false;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
-        float r = ldexp_exact(bf16_bits_to_f32(bits), p);
-        if (!isfinite(r)) r = 0.f;  // non-finite values were carried by term 0
-        for (int t = 0; t < term; ++t) r = (r - __half2float(__float2half_rn(r))) * 16777216.0f;
-        __half hv = __float2half_rn(r);
-        h[i] = __half_as_ushort(hv);
-        if (r - __half2float(hv) != 0.f) more = true;
-    }
-    uint4 out;
-    if (FMT == FMT_NVFP4) {
-        out = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-    } else {
-        out = make_uint4(h[0] | (h[4] << 16), h[1] | (h[5] << 16), h[2] | (h[6] << 16), h[3] | (h[7] << 16));
-    }
-    return out;
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Exact f16x2 -> bf16x2 for values with at most 8 significant bits in the
+// bf16 normal range (the decoded weights): through fp32, both steps exact.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h2)
+{
+    const float lo = half_bits_to_f32(h2 & 0xFFFFu), hi = half_bits_to_f32(h2 >> 16);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
 
 struct TileAcc {
     float v[2][4];  // [gate/up][element]
 };
 
-// One consumer warp's share of one pipeline stage for one 16-row tile: the
-// macro-steps (64 k each) of its slice, every residual term the chunk needs,
-// and the fold of the chunk partial into the fp32 accumulator.
-template <int FMT, int EPI>
-__device__ __forceinline__ void process_tile(const DenseArgs& a, uint32_t sb, uint32_t x_base, uint32_t sm_base,
-                                             const int* xexp, int jsub, int kglob, int ks0, int ti, int slice,
-                                             int S, int n_terms, int lane, TileAcc& acc)
+// One consumer warp's work on one pipeline stage (256 k) for one 16-row tile.
+// BF = false: f16 MMA on the prescaled activations (every value of the chunk
+// exact in f16). BF = true: bf16 MMA on the raw bf16 activations, used for a
+// chunk whose values do not all fit one f16 exponent window; the decoded
+// weights are exact in bf16 as well, so the products stay exact.
+template <int FMT, int EPI, bool BF>
+__device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint32_t xb, uint32_t sm_base, int jsub,
+                                           int kk0, int ti, int lane, const int* xexp, TileAcc& acc)
 {
     constexpr int NGU = (EPI == EPI_SWIGLU) ? 2 : 1;
     const int g = lane >> 2;
     const int t = lane & 3;
     const int M = a.M;
+    const int p0 = xexp[jsub * 8 + 2 * t];
+    const int p1 = xexp[jsub * 8 + 2 * t + 1];
 
-    // Q: scale and min of the chunk's 8 groups for rows g and g+8.
     uint4 qs_g = make_uint4(0, 0, 0, 0), qs_g8 = qs_g, qm_g = qs_g, qm_g8 = qs_g;
     if (FMT != FMT_NVFP4) {
         qs_g = lds128(sb + a.st.scales + (16 * ti + g) * 16);
@@ -192,140 +164,136 @@ __device__ __forceinline__ void process_tile(const DenseArgs& a, uint32_t sb, ui
         qm_g = lds128(sb + a.st.mins + (16 * ti + g) * 16);
         qm_g8 = lds128(sb + a.st.mins + (16 * ti + g + 8) * 16);
     }
-    const int p0 = xexp[jsub * 8 + 2 * t];
-    const int p1 = xexp[jsub * 8 + 2 * t + 1];
-
-#pragma unroll 1
-    for (int term = 0; term < n_terms; ++term) {
-        float d[2][4];
+    // two independent accumulator chains per gate/up tile (one per 32-k chunk)
+    float d[2][2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) d[j][e] = 0.f;
-        bool more = false;
+            for (int e = 0; e < 4; ++e) d[i][j][e] = 0.f;
+
+    const int lr = (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
-        for (int ms = 0; ms < 4; ++ms) {
-            if ((ms % S) != slice) continue;
-            // B operand (token g) for the two 32-k chunks of this macro-step.
-            uint4 bx[2];
+    for (int ms = 0; ms < 4; ++ms) {
+        uint4 bx[2];
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                const int kk = (kglob - ks0) + 64 * ms + 32 * ch + 8 * t;
-                bx[ch] = make_uint4(0, 0, 0, 0);
-                if (g < M) {
-                    if (term == 0) {
-                        bx[ch] = lds128(x_base + (g * a.x_pitch + kk) * 2);
-                    } else {
-                        const uint4 raw = ldg_nc_128(a.x + static_cast<size_t>(g) * a.K + ks0 + kk);
-                        bool m2;
-                        bx[ch] = residual_term8<FMT>(raw, xexp[jsub * 8 + g], term, m2);
-                        more |= m2;
-                    }
-                }
-            }
-            // ldmatrix addressing: lane l supplies row (l & 7) + 8 * ((l >> 3) & 1)
-            // of the tile and 16-byte chunk 2 * ms + (l >> 4); rows are 128 B,
-            // 128B-swizzled (chunk c of row r sits at chunk c ^ (r & 7)).
-            const int lr = (lane & 7) + 8 * ((lane >> 3) & 1);
-            const int lc = 2 * ms + (lane >> 4);
-            const uint32_t lofs = (16 * ti + lr) * 128 + ((lc ^ (lr & 7)) << 4);
-#pragma unroll
-            for (int gu = 0; gu < NGU; ++gu) {
-                uint32_t cr[4];
-                ldmatrix_x4(cr, sb + (gu ? a.st.codes2 : a.st.codes) + lofs);
-                // cr[0]: row g, chunk 2ms; cr[1]: row g+8, chunk 2ms;
-                // cr[2]: row g, chunk 2ms+1; cr[3]: row g+8, chunk 2ms+1.
-                // Each holds 8 codes for k = 32 * chunk + 8t .. 8t+7.
-                if (FMT == FMT_NVFP4) {
-                    const uint32_t sbase = sb + (gu ? a.st.scales2 : a.st.scales);
-                    const uint32_t sw_g = lds32(sbase + (16 * ti + g) * 16 + 4 * ms);
-                    const uint32_t sw_g8 = lds32(sbase + (16 * ti + g + 8) * 16 + 4 * ms);
-                    // 16-k blocks 4ms + (t>>1) (chunk 2ms) and 4ms + 2 + (t>>1) (chunk 2ms+1)
-                    const uint32_t sel = static_cast<uint32_t>((t >> 1) | (((t >> 1) + 2) << 4));
-                    const uint32_t sc_g = e4m3x2_to_f16x2(__byte_perm(sw_g, 0, sel));
-                    const uint32_t sc_g8 = e4m3x2_to_f16x2(__byte_perm(sw_g8, 0, sel));
-#pragma unroll
-                    for (int ch = 0; ch < 2; ++ch) {
-                        const uint32_t s_g = ch ? bcast_hi(sc_g) : bcast_lo(sc_g);
-                        const uint32_t s_g8 = ch ? bcast_hi(sc_g8) : bcast_lo(sc_g8);
-                        const uint32_t rg = cr[2 * ch], rg8 = cr[2 * ch + 1];
-                        uint32_t pg[4], pg8[4];
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) {
-                            pg[b] = hmul2(e2m1x2_to_f16x2((rg >> (8 * b)) & 0xFFu), s_g);
-                            pg8[b] = hmul2(e2m1x2_to_f16x2((rg8 >> (8 * b)) & 0xFFu), s_g8);
-                        }
-                        const uint4 bb = bx[ch];
-                        const uint32_t A0[4] = {pg[0], pg8[0], pg[1], pg8[1]};
-                        mma_f16_16816(d[gu], A0, bb.x, bb.y);
-                        const uint32_t A1[4] = {pg[2], pg8[2], pg[3], pg8[3]};
-                        mma_f16_16816(d[gu], A1, bb.z, bb.w);
-                    }
-                } else {
-#pragma unroll
-                    for (int ch = 0; ch < 2; ++ch) {
-                        const int grp = 2 * ms + ch;  // 32-k group index inside the chunk
-                        const uint32_t rg = cr[2 * ch], rg8 = cr[2 * ch + 1];
-                        uint32_t hg = 0, hg8 = 0;
-                        if (FMT == FMT_Q5) {
-                            const uint32_t h0 = lds8(sb + a.st.hi + (16 * ti + g) * 32 + 4 * grp + t);
-                            const uint32_t h1 = lds8(sb + a.st.hi + (16 * ti + g + 8) * 32 + 4 * grp + t);
-                            hg = (h0 << 4) | (h0 << 16);
-                            hg8 = (h1 << 4) | (h1 << 16);
-                        }
-                        uint32_t q0[4], q8[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            // f16 pair {q(8t+i), q(8t+i+4)} as 1024 + q, then minus 1024
-                            uint32_t u = ((rg >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
-                            uint32_t u8 = ((rg8 >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
-                            if (FMT == FMT_Q5) {
-                                u |= (hg >> i) & 0x00100010u;
-                                u8 |= (hg8 >> i) & 0x00100010u;
-                            }
-                            q0[i] = hsub2(u, 0x64006400u);
-                            q8[i] = hsub2(u8, 0x64006400u);
-                        }
-                        const uint4 bb = bx[ch];
-                        float dg[4] = {0.f, 0.f, 0.f, 0.f};
-                        const uint32_t A0[4] = {q0[0], q8[0], q0[1], q8[1]};
-                        mma_f16_16816(dg, A0, bb.x, bb.y);
-                        const uint32_t A1[4] = {q0[2], q8[2], q0[3], q8[3]};
-                        mma_f16_16816(dg, A1, bb.z, bb.w);
-                        const uint32_t sv_g = (&qs_g.x)[grp >> 1], sv_g8 = (&qs_g8.x)[grp >> 1];
-                        const int sh = (grp & 1) * 16;
-                        const float s0 = half_bits_to_f32((sv_g >> sh) & 0xFFFFu);
-                        const float s8 = half_bits_to_f32((sv_g8 >> sh) & 0xFFFFu);
-                        d[0][0] = fmaf(s0, dg[0], d[0][0]);
-                        d[0][1] = fmaf(s0, dg[1], d[0][1]);
-                        d[0][2] = fmaf(s8, dg[2], d[0][2]);
-                        d[0][3] = fmaf(s8, dg[3], d[0][3]);
-                        if (term == 0) {
-                            // min * sum(x) over the group, with the exact prescaled sums
-                            const uint32_t mv_g = (&qm_g.x)[grp >> 1], mv_g8 = (&qm_g8.x)[grp >> 1];
-                            const float m0 = half_bits_to_f32((mv_g >> sh) & 0xFFFFu);
-                            const float m8 = half_bits_to_f32((mv_g8 >> sh) & 0xFFFFu);
-                            const uint2 sx = lds64(sm_base + a.smem_sum + ((jsub * 8 + grp) * 8 + 2 * t) * 4);
-                            const float S0 = __uint_as_float(sx.x), S1 = __uint_as_float(sx.y);
-                            d[0][0] = fmaf(m0, S0, d[0][0]);
-                            d[0][1] = fmaf(m0, S1, d[0][1]);
-                            d[0][2] = fmaf(m8, S0, d[0][2]);
-                            d[0][3] = fmaf(m8, S1, d[0][3]);
-                        }
-                    }
-                }
-            }
+        for (int ch = 0; ch < 2; ++ch) {
+            const int kk = kk0 + 64 * ms + 32 * ch + 8 * t;
+            bx[ch] = g < M ? lds128(xb + (g * a.x_pitch + kk) * 2) : make_uint4(0, 0, 0, 0);
         }
-        // fold the chunk partial: value = d * 2^-(p + 24 term) per token column
-        const int e0 = p0 + 24 * term, e1 = p1 + 24 * term;
+        // ldmatrix: lane l supplies row (l & 7) + 8 * ((l >> 3) & 1) of the tile and
+        // 16-byte chunk 2 * ms + (l >> 4); chunk c of row r sits at c ^ (r & 7).
+        const int lc = 2 * ms + (lane >> 4);
+        const uint32_t lofs = (16 * ti + lr) * 128 + ((lc ^ (lr & 7)) << 4);
 #pragma unroll
         for (int gu = 0; gu < NGU; ++gu) {
-            acc.v[gu][0] += ldexp_exact(d[gu][0], -e0);
-            acc.v[gu][1] += ldexp_exact(d[gu][1], -e1);
-            acc.v[gu][2] += ldexp_exact(d[gu][2], -e0);
-            acc.v[gu][3] += ldexp_exact(d[gu][3], -e1);
+            uint32_t cr[4];
+            ldmatrix_x4(cr, sb + (gu ? a.st.codes2 : a.st.codes) + lofs);
+            // cr[0]: row g chunk 2ms; cr[1]: row g+8 chunk 2ms; cr[2], cr[3]: chunk 2ms+1.
+            // Each register holds the 8 codes of k = 32 * chunk + 8t .. 8t+7.
+            if (FMT == FMT_NVFP4) {
+                const uint32_t sbase = sb + (gu ? a.st.scales2 : a.st.scales);
+                const uint32_t sw_g = lds32(sbase + (16 * ti + g) * 16 + 4 * ms);
+                const uint32_t sw_g8 = lds32(sbase + (16 * ti + g + 8) * 16 + 4 * ms);
+                // 16-k blocks 4ms + (t>>1) (chunk 2ms) and 4ms + 2 + (t>>1) (chunk 2ms+1)
+                const uint32_t sel = static_cast<uint32_t>((t >> 1) | (((t >> 1) + 2) << 4));
+                const uint32_t sc_g = e4m3x2_to_f16x2(__byte_perm(sw_g, 0, sel));
+                const uint32_t sc_g8 = e4m3x2_to_f16x2(__byte_perm(sw_g8, 0, sel));
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    const uint32_t s_g = ch ? bcast_hi(sc_g) : bcast_lo(sc_g);
+                    const uint32_t s_g8 = ch ? bcast_hi(sc_g8) : bcast_lo(sc_g8);
+                    const uint32_t rg = cr[2 * ch], rg8 = cr[2 * ch + 1];
+                    uint32_t pg[4], pg8[4];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        pg[b] = hmul2(e2m1x2_to_f16x2((rg >> (8 * b)) & 0xFFu), s_g);
+                        pg8[b] = hmul2(e2m1x2_to_f16x2((rg8 >> (8 * b)) & 0xFFu), s_g8);
+                        if (BF) {
+                            pg[b] = f16x2_to_bf16x2(pg[b]);
+                            pg8[b] = f16x2_to_bf16x2(pg8[b]);
+                        }
+                    }
+                    const uint4 bb = bx[ch];
+                    const uint32_t A0[4] = {pg[0], pg8[0], pg[1], pg8[1]};
+                    const uint32_t A1[4] = {pg[2], pg8[2], pg[3], pg8[3]};
+                    if (BF) {
+                        mma_bf16_16816(d[gu][ch], A0, bb.x, bb.y);
+                        mma_bf16_16816(d[gu][ch], A1, bb.z, bb.w);
+                    } else {
+                        mma_f16_16816(d[gu][ch], A0, bb.x, bb.y);
+                        mma_f16_16816(d[gu][ch], A1, bb.z, bb.w);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    const int grp = 2 * ms + ch;  // 32-k group inside the chunk
+                    const uint32_t rg = cr[2 * ch], rg8 = cr[2 * ch + 1];
+                    uint32_t hg = 0, hg8 = 0;
+                    if (FMT == FMT_Q5) {
+                        const uint32_t h0 = lds8(sb + a.st.hi + (16 * ti + g) * 32 + 4 * grp + t);
+                        const uint32_t h1 = lds8(sb + a.st.hi + (16 * ti + g + 8) * 32 + 4 * grp + t);
+                        hg = (h0 << 4) | (h0 << 16);
+                        hg8 = (h1 << 4) | (h1 << 16);
+                    }
+                    // pair {q(8t+i), q(8t+i+4)}: f16 1024 + q (or bf16 128 + q), minus the offset
+                    constexpr uint32_t kMagic = BF ? 0x43004300u : 0x64006400u;
+                    uint32_t q0[4], q8[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t u = ((rg >> (4 * i)) & 0x000F000Fu) | kMagic;
+                        uint32_t u8 = ((rg8 >> (4 * i)) & 0x000F000Fu) | kMagic;
+                        if (FMT == FMT_Q5) {
+                            u |= (hg >> i) & 0x00100010u;
+                            u8 |= (hg8 >> i) & 0x00100010u;
+                        }
+                        q0[i] = BF ? bsub2(u, kMagic) : hsub2(u, kMagic);
+                        q8[i] = BF ? bsub2(u8, kMagic) : hsub2(u8, kMagic);
+                    }
+                    const uint4 bb = bx[ch];
+                    float dg[4] = {0.f, 0.f, 0.f, 0.f};
+                    const uint32_t A0[4] = {q0[0], q8[0], q0[1], q8[1]};
+                    const uint32_t A1[4] = {q0[2], q8[2], q0[3], q8[3]};
+                    if (BF) {
+                        mma_bf16_16816(dg, A0, bb.x, bb.y);
+                        mma_bf16_16816(dg, A1, bb.z, bb.w);
+                    } else {
+                        mma_f16_16816(dg, A0, bb.x, bb.y);
+                        mma_f16_16816(dg, A1, bb.z, bb.w);
+                    }
+                    const uint32_t sv_g = (&qs_g.x)[grp >> 1], sv_g8 = (&qs_g8.x)[grp >> 1];
+                    const uint32_t mv_g = (&qm_g.x)[grp >> 1], mv_g8 = (&qm_g8.x)[grp >> 1];
+                    const int sh = (grp & 1) * 16;
+                    const float s0 = half_bits_to_f32((sv_g >> sh) & 0xFFFFu);
+                    const float s8 = half_bits_to_f32((sv_g8 >> sh) & 0xFFFFu);
+                    const float m0 = half_bits_to_f32((mv_g >> sh) & 0xFFFFu);
+                    const float m8 = half_bits_to_f32((mv_g8 >> sh) & 0xFFFFu);
+                    // exact prescaled group sums of x for tokens 2t, 2t+1
+                    const uint2 sx = lds64(sm_base + a.smem_sum + ((jsub * 8 + grp) * 8 + 2 * t) * 4);
+                    float S0 = __uint_as_float(sx.x), S1 = __uint_as_float(sx.y);
+                    if (BF) {  // the bf16 pass works on unscaled activations
+                        S0 = ldexp_exact(S0, -p0);
+                        S1 = ldexp_exact(S1, -p1);
+                    }
+                    float* dd = d[0][ch];
+                    dd[0] = fmaf(m0, S0, fmaf(s0, dg[0], dd[0]));
+                    dd[1] = fmaf(m0, S1, fmaf(s0, dg[1], dd[1]));
+                    dd[2] = fmaf(m8, S0, fmaf(s8, dg[2], dd[2]));
+                    dd[3] = fmaf(m8, S1, fmaf(s8, dg[3], dd[3]));
+                }
+            }
         }
-        if (term > 0 && !__any_sync(0xffffffffu, more)) break;
+    }
+    // fold the chunk partial into the accumulator: value = d * 2^-p per token column
+    const int e0 = BF ? 0 : p0, e1 = BF ? 0 : p1;
+#pragma unroll
+    for (int gu = 0; gu < NGU; ++gu) {
+        acc.v[gu][0] += ldexp_exact(d[gu][0][0] + d[gu][1][0], -e0);
+        acc.v[gu][1] += ldexp_exact(d[gu][0][1] + d[gu][1][1], -e1);
+        acc.v[gu][2] += ldexp_exact(d[gu][0][2] + d[gu][1][2], -e0);
+        acc.v[gu][3] += ldexp_exact(d[gu][0][3] + d[gu][1][3], -e1);
     }
 }
 
@@ -400,11 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ consumers
-    const int g = lane >> 2;  // MMA group: weight row g / g+8, token g
-    const int t = lane & 3;   // thread in group
+    // Warp w works on tile (w % Tp) for the stages c with c % S == w / Tp; the
+    // S slices of a tile are summed in a fixed order at the end.
     const int T = (rows + 15) >> 4;
     const int Tp = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16;
-    const int S = Tp >= 8 ? 1 : min(4, kConsumerWarps / Tp);
+    const int S = Tp >= 8 ? 1 : kConsumerWarps / Tp;
     int my_tiles[2] = {-1, -1};
     int slice = 0;
     if (Tp == 16) {
@@ -413,15 +381,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         slice = warp / Tp;
         const int ti = warp % Tp;
-        if (slice < S && ti < T) my_tiles[0] = ti;
+        if (ti < T) my_tiles[0] = ti;
     }
 
     const uint32_t sm_base = smem_u32(smem);
     const uint32_t x_base = sm_base + a.smem_x;
+    const uint32_t xraw_base = sm_base + a.smem_xraw;
     int* xexp = reinterpret_cast<int*>(smem + a.smem_exp);            // [nsub][8]
     uint8_t* xflag = smem + a.smem_flag;                                // [nsub][8]
-    float* xsum = reinterpret_cast<float*>(smem + a.smem_sum);        // [groups][8]
+    float* xsum = reinterpret_cast<float*>(smem + a.smem_sum);        // [nsub * 8 groups][8]
     const int M = a.M;
+    const int ctid = threadIdx.x;                                       // 0 .. 255 among consumers
+
+    // entries of tokens >= M stay zero for the whole kernel
+    {
+        const int nsub_max = a.ksc / kChunkK;
+        for (int i = ctid; i < nsub_max * 8; i += 32 * kConsumerWarps) {
+            xexp[i] = 0;
+            xflag[i] = 0;
+        }
+        if (FMT != FMT_NVFP4)
+            for (int i = ctid; i < nsub_max * 64; i += 32 * kConsumerWarps) xsum[i] = 0.f;
+    }
 
     TileAcc acc[2];
 #pragma unroll
@@ -432,52 +413,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 4; ++e) acc[i].v[j][e] = 0.f;
 
     bool aborted = false;
-    int ks0 = 0;
+    int ks0 = -a.ksc;
     for (int c = 0; c < n_chunks; ++c) {
         const int kglob = c * kChunkK;
-        // ---------------- activation super-chunk conversion
-        if (kglob == ks0 + (c == 0 ? 0 : a.ksc) || c == 0) {
-            if (c != 0) ks0 += a.ksc;
+        // ---------------- activation super-chunk: prescale, convert, flag
+        if (kglob == ks0 + a.ksc) {
+            ks0 += a.ksc;
             const int len = min(a.ksc, a.K - ks0);
             const int nsub = len / kChunkK;
+            const int n_items = nsub * M;
             named_barrier_sync(1, 32 * kConsumerWarps);
-            for (int it = warp; it < nsub * kMaxTokens; it += kConsumerWarps) {
-                const int m = it % kMaxTokens;
-                const int j = it / kMaxTokens;
-                if (m >= M) {
-                    if (lane == 0) {
-                        xexp[j * 8 + m] = 0;
-                        xflag[j * 8 + m] = 0;
-                    }
-                    if (FMT != FMT_NVFP4 && (lane & 3) == 0) xsum[(j * 8 + (lane >> 2)) * 8 + m] = 0.f;
-                    continue;
-                }
-                const uint4 raw = ldg_nc_128(a.x + static_cast<size_t>(m) * a.K + ks0 + j * kChunkK + lane * 8);
-                uint32_t mag = 0;
-                const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+            for (int base = warp; base < n_items; base += 4 * kConsumerWarps) {
+                uint4 raw[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint32_t lo = wv[i] & 0x7FFFu, hi = (wv[i] >> 16) & 0x7FFFu;
-                    if (lo < 0x7F80u) mag = max(mag, lo);
-                    if (hi < 0x7F80u) mag = max(mag, hi);
+                for (int u = 0; u < 4; ++u) {
+                    const int it = base + u * kConsumerWarps;
+                    raw[u] = make_uint4(0, 0, 0, 0);
+                    if (it < n_items) {
+                        const int m = it % M, j = it / M;
+                        raw[u] = ldg_nc_128(a.x + static_cast<size_t>(m) * a.K + ks0 + j * kChunkK + lane * 8);
+                    }
                 }
-                mag = __reduce_max_sync(0xffffffffu, mag);
-                const int p = prescale_exponent(mag);
-                bool exact;
-                float ls;
-                const uint4 hv = convert_chunk8<FMT>(raw, p, exact, ls);
-                const uint32_t dst = x_base + (static_cast<uint32_t>(m) * a.x_pitch + j * kChunkK + lane * 8) * 2;
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(hv.x), "r"(hv.y), "r"(hv.z),
-                             "r"(hv.w));
-                const bool any_inexact = __any_sync(0xffffffffu, !exact);
-                if (lane == 0) {
-                    xexp[j * 8 + m] = p;
-                    xflag[j * 8 + m] = any_inexact ? 1 : 0;
-                }
-                if (FMT != FMT_NVFP4) {
-                    ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-                    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-                    if ((lane & 3) == 0) xsum[(j * 8 + (lane >> 2)) * 8 + m] = ls;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int it = base + u * kConsumerWarps;
+                    if (it >= n_items) break;
+                    const int m = it % M, j = it / M;
+                    const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+                    uint32_t hbits[8];
+                    uint32_t mag = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        hbits[i] = (i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu);
+                        const uint32_t mg = hbits[i] & 0x7FFFu;
+                        if (mg < 0x7F80u) mag = max(mag, mg);
+                    }
+                    mag = __reduce_max_sync(0xffffffffu, mag);
+                    const int p = prescale_exponent(mag);
+                    uint32_t h[8];
+                    bool exact = true;
+                    float ls = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float v = ldexp_exact(bf16_bits_to_f32(hbits[i]), p);
+                        const __half hv = __float2half_rn(v);
+                        h[i] = __half_as_ushort(hv);
+                        if (isfinite(v) && __half2float(hv) != v) exact = false;
+                        ls += v;
+                    }
+                    const uint32_t off = (static_cast<uint32_t>(m) * a.x_pitch + j * kChunkK + lane * 8) * 2;
+                    const uint4 hv = pack_pairs<FMT>(h);
+                    const uint4 rv = pack_pairs<FMT>(hbits);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(x_base + off), "r"(hv.x), "r"(hv.y),
+                                 "r"(hv.z), "r"(hv.w));
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(xraw_base + off), "r"(rv.x),
+                                 "r"(rv.y), "r"(rv.z), "r"(rv.w));
+                    const bool any_inexact = __any_sync(0xffffffffu, !exact);
+                    if (lane == 0) {
+                        xexp[j * 8 + m] = p;
+                        xflag[j * 8 + m] = any_inexact ? 1 : 0;
+                    }
+                    if (FMT != FMT_NVFP4) {
+                        ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+                        ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+                        if ((lane & 3) == 0) xsum[(j * 8 + (lane >> 2)) * 8 + m] = ls;
+                    }
                 }
             }
             named_barrier_sync(1, 32 * kConsumerWarps);
@@ -491,17 +491,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *abort_flag = 1;
             }
         }
-        if (!aborted) {
+        if (!aborted && (c % S) == slice) {
             const uint32_t sb = sm_base + a.smem_ring + slot * a.st.bytes;
             const int jsub = (kglob - ks0) / kChunkK;
             const uint64_t flags8 = *reinterpret_cast<const uint64_t*>(xflag + jsub * 8);
-            const int n_terms = flags8 ? 12 : 1;
-            if (my_tiles[0] >= 0)
-                process_tile<FMT, EPI>(a, sb, x_base, sm_base, xexp, jsub, kglob, ks0, my_tiles[0], slice, S,
-                                       n_terms, lane, acc[0]);
-            if (my_tiles[1] >= 0)
-                process_tile<FMT, EPI>(a, sb, x_base, sm_base, xexp, jsub, kglob, ks0, my_tiles[1], slice, S,
-                                       n_terms, lane, acc[1]);
+            const int kk0 = kglob - ks0;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                if (my_tiles[i] < 0) continue;
+                if (flags8)
+                    tile_stage<FMT, EPI, true>(a, sb, xraw_base, sm_base, jsub, kk0, my_tiles[i], lane, xexp, acc[i]);
+                else
+                    tile_stage<FMT, EPI, false>(a, sb, x_base, sm_base, jsub, kk0, my_tiles[i], lane, xexp, acc[i]);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
@@ -530,9 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (slice != 0 || aborted) return;
 
+    const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int ti_i = 0; ti_i < 2; ++ti_i) {
-        const int ti = my_tiles[ti_i];
+    for (int i = 0; i < 2; ++i) {
+        const int ti = my_tiles[i];
         if (ti < 0) continue;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -540,9 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tok = 2 * t + (e & 1);
             if (r >= rows || tok >= M) continue;
             const int n = row0 + r;
-            float v = acc[ti_i].v[0][e] * a.g;
+            float v = acc[i].v[0][e] * a.g;
             if (EPI == EPI_SWIGLU) {
-                const float u = acc[ti_i].v[1][e] * a.g;
+                const float u = acc[i].v[1][e] * a.g;
                 v = (v / (1.0f + expf(-v))) * u;
             }
             if (EPI == EPI_RESID) v += bf16_bits_to_f32(a.residual[static_cast<size_t>(tok) * a.n_out + n]);
@@ -580,8 +583,9 @@ qg_status launch_dense_impl(const CUtensorMap* maps, const uint16_t* x, void* y,
     a.starve = dbg.starve;
 
     // activation super-chunk: M token rows of (ksc + 32) f16 within 64 KB
-    constexpr uint32_t kXBudget = 64 * 1024;
-    int ksc = (static_cast<int>(kXBudget / (2u * M)) - 32) / kChunkK * kChunkK;
+    // f16 (prescaled) and raw bf16 copies of M token rows of (ksc + 32) values
+    constexpr uint32_t kXBudget = 80 * 1024;
+    int ksc = (static_cast<int>(kXBudget / (4u * M)) - 32) / kChunkK * kChunkK;
     ksc = min(ksc, K);
     a.ksc = ksc;
     a.x_pitch = ksc + 32;
@@ -627,7 +631,7 @@ qg_status launch_dense_impl(const CUtensorMap* maps, const uint16_t* x, void* y,
     const uint32_t sum_bytes = FMT == FMT_NVFP4 ? 0 : align_up(nsub * 8 * 8 * 4, 128);
     const uint32_t red_bytes = 8 * 2 * 32 * 4 * 4;
     const uint32_t bar_bytes = 2 * kMaxStages * 8 + 16;
-    const uint32_t fixed = x_bytes + exp_bytes + flag_bytes + sum_bytes + red_bytes + bar_bytes;
+    const uint32_t fixed = 2 * x_bytes + exp_bytes + flag_bytes + sum_bytes + red_bytes + bar_bytes;
     const uint32_t smem_max = 227 * 1024;
     if (fixed + st.bytes > smem_max) return QG_ERR_UNSUPPORTED;
     int n_stages = static_cast<int>((smem_max - fixed) / st.bytes);
@@ -638,6 +642,8 @@ qg_status launch_dense_impl(const CUtensorMap* maps, const uint16_t* x, void* y,
     a.smem_ring = so;
     so += a.n_stages * st.bytes;
     a.smem_x = so;
+    so += x_bytes;
+    a.smem_xraw = so;
     so += x_bytes;
     a.smem_exp = so;
     so += exp_bytes;

@@ -47,6 +47,7 @@ struct DenseArgs {
     int x_pitch;               // f16 elements per token row of the activation buffer
     uint32_t smem_ring;        // offsets in dynamic shared memory
     uint32_t smem_x;
+    uint32_t smem_xraw;
     uint32_t smem_exp;
     uint32_t smem_flag;
     uint32_t smem_sum;
