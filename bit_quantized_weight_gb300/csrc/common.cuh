@@ -110,6 +110,17 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low8)
     return r;
 }
 
+// The four codes bytes of a register, each as two E2M1 codes -> f16x2
+// (low nibble -> low half), exact.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&out)[4])
+{
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+        : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+        : "r"(w));
+}
+
 // Two E4M3 codes (low byte -> low half) to f16x2, exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes)
 {

@@ -164,14 +164,15 @@ __device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint
         qm_g = lds128(sb + a.st.mins + (16 * ti + g) * 16);
         qm_g8 = lds128(sb + a.st.mins + (16 * ti + g + 8) * 16);
     }
-    // two independent accumulator chains per gate/up tile (one per 32-k chunk)
+    // four independent accumulator chains per gate/up tile (chunk x MMA half)
     float d[2][2][4];
+    float d2[2][2][4];
 #pragma unroll
     for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) d[i][j][e] = 0.f;
+            for (int e = 0; e < 4; ++e) d[i][j][e] = d2[i][j][e] = 0.f;
 
     const int lr = (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
@@ -196,20 +197,20 @@ __device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint
                 const uint32_t sbase = sb + (gu ? a.st.scales2 : a.st.scales);
                 const uint32_t sw_g = lds32(sbase + (16 * ti + g) * 16 + 4 * ms);
                 const uint32_t sw_g8 = lds32(sbase + (16 * ti + g + 8) * 16 + 4 * ms);
-                // 16-k blocks 4ms + (t>>1) (chunk 2ms) and 4ms + 2 + (t>>1) (chunk 2ms+1)
-                const uint32_t sel = static_cast<uint32_t>((t >> 1) | (((t >> 1) + 2) << 4));
-                const uint32_t sc_g = e4m3x2_to_f16x2(__byte_perm(sw_g, 0, sel));
-                const uint32_t sc_g8 = e4m3x2_to_f16x2(__byte_perm(sw_g8, 0, sel));
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
-                    const uint32_t s_g = ch ? bcast_hi(sc_g) : bcast_lo(sc_g);
-                    const uint32_t s_g8 = ch ? bcast_hi(sc_g8) : bcast_lo(sc_g8);
-                    const uint32_t rg = cr[2 * ch], rg8 = cr[2 * ch + 1];
+                    // 16-k block 4ms + 2ch + (t>>1): its E4M3 byte duplicated, then
+                    // converted, gives the scale already broadcast to both halves.
+                    const uint32_t sel = static_cast<uint32_t>((2 * ch + (t >> 1)) * 0x11);
+                    const uint32_t s_g = e4m3x2_to_f16x2(__byte_perm(sw_g, 0, sel));
+                    const uint32_t s_g8 = e4m3x2_to_f16x2(__byte_perm(sw_g8, 0, sel));
                     uint32_t pg[4], pg8[4];
+                    e2m1x8_to_f16x2x4(cr[2 * ch], pg);
+                    e2m1x8_to_f16x2x4(cr[2 * ch + 1], pg8);
 #pragma unroll
                     for (int b = 0; b < 4; ++b) {
-                        pg[b] = hmul2(e2m1x2_to_f16x2((rg >> (8 * b)) & 0xFFu), s_g);
-                        pg8[b] = hmul2(e2m1x2_to_f16x2((rg8 >> (8 * b)) & 0xFFu), s_g8);
+                        pg[b] = hmul2(pg[b], s_g);
+                        pg8[b] = hmul2(pg8[b], s_g8);
                         if (BF) {
                             pg[b] = f16x2_to_bf16x2(pg[b]);
                             pg8[b] = f16x2_to_bf16x2(pg8[b]);
@@ -220,10 +221,10 @@ __device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint
                     const uint32_t A1[4] = {pg[2], pg8[2], pg[3], pg8[3]};
                     if (BF) {
                         mma_bf16_16816(d[gu][ch], A0, bb.x, bb.y);
-                        mma_bf16_16816(d[gu][ch], A1, bb.z, bb.w);
+                        mma_bf16_16816(d2[gu][ch], A1, bb.z, bb.w);
                     } else {
                         mma_f16_16816(d[gu][ch], A0, bb.x, bb.y);
-                        mma_f16_16816(d[gu][ch], A1, bb.z, bb.w);
+                        mma_f16_16816(d2[gu][ch], A1, bb.z, bb.w);
                     }
                 }
             } else {
@@ -290,10 +291,11 @@ __device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint
     const int e0 = BF ? 0 : p0, e1 = BF ? 0 : p1;
 #pragma unroll
     for (int gu = 0; gu < NGU; ++gu) {
-        acc.v[gu][0] += ldexp_exact(d[gu][0][0] + d[gu][1][0], -e0);
-        acc.v[gu][1] += ldexp_exact(d[gu][0][1] + d[gu][1][1], -e1);
-        acc.v[gu][2] += ldexp_exact(d[gu][0][2] + d[gu][1][2], -e0);
-        acc.v[gu][3] += ldexp_exact(d[gu][0][3] + d[gu][1][3], -e1);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float part = (d[gu][0][e] + d2[gu][0][e]) + (d[gu][1][e] + d2[gu][1][e]);
+            acc.v[gu][e] += ldexp_exact(part, (e & 1) ? -e1 : -e0);
+        }
     }
 }
 
@@ -316,10 +318,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* empty = full + kMaxStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kMaxStages);
 
+    // Let the next kernel on the stream be scheduled as soon as SMs free up
+    // (programmatic dependent launch); it waits for this grid before it reads
+    // anything this grid writes.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // Each stage is consumed by exactly one warp per 16-row tile.
+    const int n_tiles = (rows + 15) >> 4;
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.n_stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], n_tiles);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -372,17 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S slices of a tile are summed in a fixed order at the end.
     const int T = (rows + 15) >> 4;
     const int Tp = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16;
-    const int S = Tp >= 8 ? 1 : kConsumerWarps / Tp;
-    int my_tiles[2] = {-1, -1};
-    int slice = 0;
-    if (Tp == 16) {
-        my_tiles[0] = warp < T ? warp : -1;
-        my_tiles[1] = warp + 8 < T ? warp + 8 : -1;
-    } else {
-        slice = warp / Tp;
-        const int ti = warp % Tp;
-        if (ti < T) my_tiles[0] = ti;
-    }
+    const int S = kConsumerWarps / Tp;
+    // consecutive warps (on different schedulers) take the slices of one tile
+    const int slice = warp % S;
+    const int my_tile = (warp / S) < T ? (warp / S) : -1;
 
     const uint32_t sm_base = smem_u32(smem);
     const uint32_t x_base = sm_base + a.smem_x;
@@ -391,7 +393,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* xflag = smem + a.smem_flag;                                // [nsub][8]
     float* xsum = reinterpret_cast<float*>(smem + a.smem_sum);        // [nsub * 8 groups][8]
     const int M = a.M;
-    const int ctid = threadIdx.x;                                       // 0 .. 255 among consumers
+    const int ctid = threadIdx.x;                                       // 0 .. 511 among consumers
+
+    // The activations (and residual) may come from the previous kernel on the
+    // stream: wait for it before touching them. Weight streaming above does
+    // not depend on it and is already running.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    {
+        const int lines_per_row = (min(a.ksc, a.K) * 2) >> 7;  // 128-byte lines
+        for (int i = ctid; i < a.M * lines_per_row; i += 32 * kConsumerWarps) {
+            const uint16_t* p = a.x + static_cast<size_t>(i / lines_per_row) * a.K + (i % lines_per_row) * 64;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+        }
+    }
 
     // entries of tokens >= M stay zero for the whole kernel
     {
@@ -404,13 +418,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = ctid; i < nsub_max * 64; i += 32 * kConsumerWarps) xsum[i] = 0.f;
     }
 
-    TileAcc acc[2];
+    TileAcc acc;
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[i].v[j][e] = 0.f;
+        for (int e = 0; e < 4; ++e) acc.v[j][e] = 0.f;
 
     bool aborted = false;
     int ks0 = -a.ksc;
@@ -423,10 +435,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nsub = len / kChunkK;
             const int n_items = nsub * M;
             named_barrier_sync(1, 32 * kConsumerWarps);
-            for (int base = warp; base < n_items; base += 4 * kConsumerWarps) {
-                uint4 raw[4];
+            for (int base = warp; base < n_items; base += 2 * kConsumerWarps) {
+                uint4 raw[2];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < 2; ++u) {
                     const int it = base + u * kConsumerWarps;
                     raw[u] = make_uint4(0, 0, 0, 0);
                     if (it < n_items) {
@@ -435,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < 2; ++u) {
                     const int it = base + u * kConsumerWarps;
                     if (it >= n_items) break;
                     const int m = it % M, j = it / M;
@@ -484,6 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         const int slot = c % a.n_stages;
+        const bool mine = (c % S) == slice && my_tile >= 0;
+        if (!mine) continue;
         if (!aborted && *abort_flag) aborted = true;
         if (!aborted) {
             if (!mbar_wait_bounded(&full[slot], (c / a.n_stages) & 1, a.wait_ns, a.status)) {
@@ -491,18 +505,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *abort_flag = 1;
             }
         }
-        if (!aborted && (c % S) == slice) {
+        if (!aborted) {
             const uint32_t sb = sm_base + a.smem_ring + slot * a.st.bytes;
             const int jsub = (kglob - ks0) / kChunkK;
             const uint64_t flags8 = *reinterpret_cast<const uint64_t*>(xflag + jsub * 8);
             const int kk0 = kglob - ks0;
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                if (my_tiles[i] < 0) continue;
+            if (my_tile >= 0) {
                 if (flags8)
-                    tile_stage<FMT, EPI, true>(a, sb, xraw_base, sm_base, jsub, kk0, my_tiles[i], lane, xexp, acc[i]);
+                    tile_stage<FMT, EPI, true>(a, sb, xraw_base, sm_base, jsub, kk0, my_tile, lane, xexp, acc);
                 else
-                    tile_stage<FMT, EPI, false>(a, sb, x_base, sm_base, jsub, kk0, my_tiles[i], lane, xexp, acc[i]);
+                    tile_stage<FMT, EPI, false>(a, sb, x_base, sm_base, jsub, kk0, my_tile, lane, xexp, acc);
             }
         }
         __syncwarp();
@@ -513,47 +525,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* red = reinterpret_cast<float*>(smem + a.smem_red);
     if (S > 1) {
         named_barrier_sync(1, 32 * kConsumerWarps);
-        if (slice > 0 && my_tiles[0] >= 0) {
+        if (slice > 0 && my_tile >= 0) {
 #pragma unroll
             for (int gu = 0; gu < NGU; ++gu)
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    red[(((slice * Tp + my_tiles[0]) * 2 + gu) * 32 + lane) * 4 + e] = acc[0].v[gu][e];
+                    red[(((slice * Tp + my_tile) * 2 + gu) * 32 + lane) * 4 + e] = acc.v[gu][e];
         }
         named_barrier_sync(1, 32 * kConsumerWarps);
-        if (slice == 0 && my_tiles[0] >= 0) {
+        if (slice == 0 && my_tile >= 0) {
             for (int s = 1; s < S; ++s)
 #pragma unroll
                 for (int gu = 0; gu < NGU; ++gu)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        acc[0].v[gu][e] += red[(((s * Tp + my_tiles[0]) * 2 + gu) * 32 + lane) * 4 + e];
+                        acc.v[gu][e] += red[(((s * Tp + my_tile) * 2 + gu) * 32 + lane) * 4 + e];
         }
     }
-    if (slice != 0 || aborted) return;
+    if (slice != 0 || aborted || my_tile < 0) return;
 
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int ti = my_tiles[i];
-        if (ti < 0) continue;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int r = 16 * ti + g + ((e & 2) ? 8 : 0);
-            const int tok = 2 * t + (e & 1);
-            if (r >= rows || tok >= M) continue;
-            const int n = row0 + r;
-            float v = acc[i].v[0][e] * a.g;
-            if (EPI == EPI_SWIGLU) {
-                const float u = acc[i].v[1][e] * a.g;
-                v = (v / (1.0f + expf(-v))) * u;
-            }
-            if (EPI == EPI_RESID) v += bf16_bits_to_f32(a.residual[static_cast<size_t>(tok) * a.n_out + n]);
-            if (a.out_f32) {
-                reinterpret_cast<float*>(a.y)[static_cast<size_t>(tok) * a.n_out + n] = v;
-            } else {
-                reinterpret_cast<uint16_t*>(a.y)[static_cast<size_t>(tok) * a.n_out + n] = f32_to_bf16_bits_rn(v);
-            }
+    for (int e = 0; e < 4; ++e) {
+        const int r = 16 * my_tile + g + ((e & 2) ? 8 : 0);
+        const int tok = 2 * t + (e & 1);
+        if (r >= rows || tok >= M) continue;
+        const int n = row0 + r;
+        float v = acc.v[0][e] * a.g;
+        if (EPI == EPI_SWIGLU) {
+            const float u = acc.v[1][e] * a.g;
+            v = (v / (1.0f + expf(-v))) * u;
+        }
+        if (EPI == EPI_RESID) v += bf16_bits_to_f32(a.residual[static_cast<size_t>(tok) * a.n_out + n]);
+        if (a.out_f32) {
+            reinterpret_cast<float*>(a.y)[static_cast<size_t>(tok) * a.n_out + n] = v;
+        } else {
+            reinterpret_cast<uint16_t*>(a.y)[static_cast<size_t>(tok) * a.n_out + n] = f32_to_bf16_bits_rn(v);
         }
     }
 }
@@ -629,7 +636,7 @@ qg_status launch_dense_impl(const CUtensorMap* maps, const uint16_t* x, void* y,
     const uint32_t exp_bytes = align_up(nsub * 8 * 4, 128);
     const uint32_t flag_bytes = align_up(nsub * 8, 128);
     const uint32_t sum_bytes = FMT == FMT_NVFP4 ? 0 : align_up(nsub * 8 * 8 * 4, 128);
-    const uint32_t red_bytes = 8 * 2 * 32 * 4 * 4;
+    const uint32_t red_bytes = kConsumerWarps * 2 * 32 * 4 * 4;
     const uint32_t bar_bytes = 2 * kMaxStages * 8 + 16;
     const uint32_t fixed = 2 * x_bytes + exp_bytes + flag_bytes + sum_bytes + red_bytes + bar_bytes;
     const uint32_t smem_max = 227 * 1024;
@@ -666,7 +673,17 @@ qg_status launch_dense_impl(const CUtensorMap* maps, const uint16_t* x, void* y,
         attr_set[dev] = true;
     }
     const int grid = (n_out + R - 1) / R;
-    kern<<<grid, kThreads, so, stream>>>(a, maps[0], maps[1], maps[2], maps[3]);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = so;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, a, maps[0], maps[1], maps[2], maps[3]) != cudaSuccess) return QG_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 

@@ -11,7 +11,7 @@ namespace qg {
 enum Fmt : int { FMT_NVFP4 = 0, FMT_Q4 = 1, FMT_Q5 = 2 };
 enum Epi : int { EPI_NONE = 0, EPI_RESID = 1, EPI_SWIGLU = 2 };
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one weight-streaming warp
 constexpr int kChunkK = 256;                          // k per pipeline stage
 constexpr int kMaxTokens = 8;                         // MMA n dimension
