@@ -52,7 +52,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["dense", "q45", "tiny"], default="dense")
+    ap.add_argument("--workload", choices=["dense", "q45", "tiny", "moe"], default="dense")
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -302,6 +302,87 @@ class Workload:
         return f"tiny NVFP4 GEMV 256x512, M={self.M}"
 
 
+class MoeWorkload:
+    """35B-A3B-class MoE decode layer: device router (softmax, top-8,
+    renormalise) then the expert-gathered NVFP4 gate/up + SwiGLU, down and
+    weighted combine. Weight bytes per step = the distinct experts the router
+    picks x the bytes of one expert."""
+
+    def __init__(self, M, copies_min_bytes):
+        import numpy as np
+        import torch
+        import synth
+        import bit_quantized_weight_gb300 as q
+        c = synth.MOE35B
+        self.M, self.E, self.H, self.I, self.topk = M, c.experts, c.hidden, c.inter, c.topk
+        dev = torch.device("cuda", torch.cuda.current_device())
+        E, H, I = self.E, self.H, self.I
+        gu = synth.nvfp4_weights(4, "moe.gu", E * 2 * I, H)
+        dn = synth.nvfp4_weights(4, "moe.dn", E * H, I)
+        self.expert_bytes = (gu["codes"].nbytes + gu["scales"].nbytes + dn["codes"].nbytes
+                             + dn["scales"].nbytes) // E
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        base = {"gc": up(gu["codes"]).view(E, 2 * I, H // 2), "gs": up(gu["scales"]).view(E, 2 * I, H // 16),
+                "dc": up(dn["codes"]).view(E, H, I // 2), "ds": up(dn["scales"]).view(E, H, I // 16)}
+        self.gg = torch.ones(E, dtype=torch.float32, device=dev)
+        self.dg = torch.ones(E, dtype=torch.float32, device=dev)
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 * 2 ** 20)
+        self.l2_bytes = int(l2)
+        total = self.expert_bytes * E
+        self.copies = max(2, math.ceil(copies_min_bytes * self.l2_bytes / total))
+        self.w = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(self.copies - 1)]
+        # activations and router logits, packed for one H2D copy per step
+        x = synth.bf16_normal(4, "moe.x", (M, H))
+        lg = synth.router_logits(4, "moe.logits", M, E)
+        self.host_in = np.concatenate([x.view(np.uint16).ravel(), lg.view(np.uint16).ravel()])
+        self.in_elems = self.host_in.size
+        self.d_in = torch.from_numpy(self.host_in.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.x = self.d_in[: M * H].view(M, H)
+        self.logits = self.d_in[M * H:].view(torch.float32).view(M, E)
+        self.ids = torch.empty((M, self.topk), dtype=torch.int32, device=dev)
+        self.tw = torch.empty((M, self.topk), dtype=torch.float32, device=dev)
+        self.d_out = torch.empty(M * H, dtype=torch.bfloat16, device=dev)
+        self.out_elems = M * H
+        self.ws = torch.empty(q.moe_qgemv_nvfp4_workspace_size(M, self.topk, H, I, E), dtype=torch.uint8, device=dev)
+        q.moe_route_topk(self.logits, self.topk, self.ids, self.tw)
+        torch.cuda.synchronize()
+        self.n_active = int(np.unique(self.ids.cpu().numpy()).size)
+        self.weight_bytes = self.n_active * self.expert_bytes
+        self.projs = [("router",), ("moe",)]
+
+    def kernel_names(self):
+        return ["router", "moe"]
+
+    def launches_per_step(self):
+        return 5  # router, grouping, gate/up + SwiGLU, down, combine
+
+    def call(self, idx, copy):
+        import bit_quantized_weight_gb300 as q
+        w = self.w[copy % self.copies]
+        if idx == 0:
+            q.moe_route_topk(self.logits, self.topk, self.ids, self.tw)
+        else:
+            q.moe_qgemv_nvfp4(w["gc"], w["gs"], self.gg, w["dc"], w["ds"], self.dg, self.x, self.ids, self.tw,
+                              self.d_out.view(self.M, self.H), self.ws)
+
+    def step(self, copy, events=None):
+        for i in range(2):
+            if events is not None:
+                events[i].record()
+            self.call(i, copy)
+        if events is not None:
+            events[-1].record()
+
+    def alg_bytes(self, idx):
+        if idx == 0:
+            return self.M * self.E * 4 + self.M * self.topk * 8
+        return self.weight_bytes + 2 * self.M * self.H * 2
+
+    def describe(self):
+        return (f"MoE decode layer (35B-A3B-class): hidden {self.H}, {self.E} experts, intermediate {self.I}, "
+                f"top-{self.topk}, M={self.M}; {self.n_active} distinct experts active")
+
+
 # ------------------------------------------------------------------ CPU oracle
 def oracle_step_sample(wl_projs, M, frac, threads):
     """Run the fp64 oracle on every `1/frac`-th output row of each projection;
@@ -403,9 +484,13 @@ def main():
     torch.cuda.set_device(local)
     if args.workload == "tiny":
         args.M = 1
-    wl = Workload(args.workload, args.M, copies_min_bytes=4)
+    if args.workload == "moe":
+        args.M = 8
+        wl = MoeWorkload(args.M, copies_min_bytes=4)
+    else:
+        wl = Workload(args.workload, args.M, copies_min_bytes=4)
     stream = torch.cuda.Stream()
-    n_calls = wl.launches_per_step()
+    n_calls = len(wl.kernel_names())
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):                 # eager warm-up
@@ -516,7 +601,7 @@ def main():
                "ms_per_step": ems / args.steps}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload != "moe":
         cpu = cpu_baseline(args.workload, args.M)
 
     if rank == 0:
@@ -534,7 +619,7 @@ def main():
             "frac_of_measured_hbm": value / world / peak,
             "us_per_call": us_per_call,
             "roofline": roofline,
-            "gpu_launches": n_calls * args.steps,
+            "gpu_launches": wl.launches_per_step() * args.steps,
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,

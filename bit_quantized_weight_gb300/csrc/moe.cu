@@ -71,21 +71,210 @@ qg_status launch_route(const float* logits, int M, int E, int topk, int32_t* ids
     return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
+namespace {
+
+constexpr int kMaxPairs = kMaxTokens * 8;
+
+struct MoeLayout {
+    size_t h, yslot, ctrl, g_gu, g_dn, u_gu, u_dn, total;
+    int r_gu, r_dn, units_gu_max, units_dn_max;
+};
+
+size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Rows per unit: the gate/up launch walks (expert, 32-row block) units and the
+// down launch (expert, 128-row block) units (smaller blocks where H or I
+// need them), so the ~50 active experts spread evenly over the SMs.
+MoeLayout moe_layout(int M, int topk, int H, int I)
+{
+    MoeLayout L{};
+    const size_t P = static_cast<size_t>(M) * topk;
+    L.r_gu = 32;
+    L.r_dn = (H % 128 == 0) ? 128 : 64;
+    L.units_gu_max = kMaxPairs * (I / L.r_gu);
+    L.units_dn_max = kMaxPairs * (H / L.r_dn);
+    size_t o = 0;
+    L.h = o;
+    o += up256(P * I * 2);
+    L.yslot = o;
+    o += up256(P * H * 4);
+    L.ctrl = o;
+    o += 256;
+    L.g_gu = o;
+    o += up256(sizeof(GroupDesc) * kMaxPairs);
+    L.g_dn = o;
+    o += up256(sizeof(GroupDesc) * kMaxPairs);
+    L.u_gu = o;
+    o += up256(sizeof(UnitDesc) * L.units_gu_max);
+    L.u_dn = o;
+    o += up256(sizeof(UnitDesc) * L.units_dn_max);
+    L.total = o;
+    return L;
+}
+
+// Groups the (token, slot) pairs by expert and writes the unit lists.
+// Gate/up: one group per active expert; its 8 columns are the 8 token rows of
+// x (shared by every expert, xkey 0) and column m writes h row m * topk + i of
+// the slot that routed token m there. Down: the pairs of an expert, at most 8
+// per group; column j reads h row x_row[j] and writes slot row out_row[j].
+// A token listing one expert twice reuses the first slot's h row.
+__global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int I, int H, int r_gu, int r_dn,
+                                 GroupDesc* g_gu, GroupDesc* g_dn, UnitDesc* u_gu, UnitDesc* u_dn, int* ctrl,
+                                 int* status)
+{
+    __shared__ int s_pair_e[kMaxPairs];
+    __shared__ int s_order[kMaxPairs];
+    __shared__ int s_n_gu, s_n_dn;
+    __shared__ int s_gu_of_dn[kMaxPairs];  // gate/up group of each down group
+    const int P = M * topk;
+    if (threadIdx.x == 0) {
+        int nv = 0;
+        for (int p = 0; p < P; ++p) {
+            const int e = ids[p];
+            if (e < 0 || e >= E) {
+                atomicCAS(status, 0, QG_ERR_INVALID_ARG);
+                s_pair_e[p] = -1;
+                continue;
+            }
+            s_pair_e[p] = e;
+            // insertion into order sorted by (expert, pair)
+            int j = nv++;
+            while (j > 0 && (s_pair_e[s_order[j - 1]] > e)) {
+                s_order[j] = s_order[j - 1];
+                --j;
+            }
+            s_order[j] = p;
+        }
+        int n_gu = 0, n_dn = 0;
+        int i = 0;
+        while (i < nv) {
+            const int e = s_pair_e[s_order[i]];
+            int iend = i;
+            while (iend < nv && s_pair_e[s_order[iend]] == e) ++iend;
+            GroupDesc gg;
+            gg.ntok = M;
+            gg.e = e;
+            gg.xkey = 0;
+            for (int j = 0; j < 8; ++j) {
+                gg.x_row[j] = j < M ? j : 0;
+                gg.out_row[j] = -1;
+            }
+            int first_of_tok[kMaxTokens];
+            for (int m = 0; m < kMaxTokens; ++m) first_of_tok[m] = -1;
+            for (int q = i; q < iend; ++q) {
+                const int p = s_order[q];
+                const int m = p / topk;
+                if (first_of_tok[m] < 0) {
+                    first_of_tok[m] = p;
+                    gg.out_row[m] = p;
+                }
+            }
+            g_gu[n_gu] = gg;
+            // down groups: chunks of at most 8 pairs
+            for (int q = i; q < iend; q += 8) {
+                GroupDesc gd;
+                gd.ntok = min(8, iend - q);
+                gd.e = e;
+                gd.xkey = 1 + n_dn;
+                for (int j = 0; j < 8; ++j) {
+                    if (j < gd.ntok) {
+                        const int p = s_order[q + j];
+                        gd.out_row[j] = p;
+                        gd.x_row[j] = first_of_tok[p / topk];
+                    } else {
+                        gd.out_row[j] = -1;
+                        gd.x_row[j] = 0;
+                    }
+                }
+                s_gu_of_dn[n_dn] = n_gu;
+                g_dn[n_dn++] = gd;
+            }
+            ++n_gu;
+            i = iend;
+        }
+        s_n_gu = n_gu;
+        s_n_dn = n_dn;
+    }
+    __syncthreads();
+    const int per_gu = I / r_gu, per_dn = H / r_dn;
+    const int n_gu = s_n_gu * per_gu, n_dn = s_n_dn * per_dn;
+    for (int u = threadIdx.x; u < n_gu; u += blockDim.x) {
+        const int gi = u / per_gu, rb = u % per_gu;
+        UnitDesc d;
+        d.grp = gi;
+        d.w_row0 = g_gu[gi].e * 2 * I + rb * r_gu;
+        d.rows = r_gu;
+        d.out_col0 = rb * r_gu;
+        u_gu[u] = d;
+    }
+    for (int u = threadIdx.x; u < n_dn; u += blockDim.x) {
+        const int gi = u / per_dn, rb = u % per_dn;
+        UnitDesc d;
+        d.grp = gi;
+        d.w_row0 = g_dn[gi].e * H + rb * r_dn;
+        d.rows = r_dn;
+        d.out_col0 = rb * r_dn;
+        u_dn[u] = d;
+    }
+    if (threadIdx.x == 0) {
+        ctrl[0] = n_gu;
+        ctrl[1] = n_dn;
+    }
+}
+
+// y[m][j] = bf16_rne( sum_{i ascending} w[m][i] * yslot[m * topk + i][j] ), fp32.
+__global__ void moe_combine_kernel(const float* yslot, const int32_t* ids, const float* w, uint16_t* y, int M,
+                                   int topk, int H, int E)
+{
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= M * H) return;
+    const int m = idx / H, j = idx % H;
+    float acc = 0.f;
+    for (int i = 0; i < topk; ++i) {
+        const int e = ids[m * topk + i];
+        if (e < 0 || e >= E) continue;
+        acc = fmaf(w[m * topk + i], yslot[static_cast<size_t>(m * topk + i) * H + j], acc);
+    }
+    y[idx] = f32_to_bf16_bits_rn(acc);
+}
+
+}  // namespace
+
 size_t moe_workspace_bytes(int M, int topk, int H, int I, int E)
 {
     (void)E;
-    const size_t pairs = static_cast<size_t>(M) * topk;
-    size_t b = (pairs * I * 2 + 255) / 256 * 256;  // h, bf16 [M][topk][I]
-    b += (pairs * H * 4 + 255) / 256 * 256;        // per-slot down outputs, fp32
-    b += 64 * 1024;                                // expert lists and work units
-    return b;
+    return moe_layout(M, topk, H, I).total;
 }
 
-qg_status launch_moe(const uint8_t*, const uint8_t*, const float*, const uint8_t*, const uint8_t*, const float*,
-                     const void*, const int32_t*, const float*, void*, void*, size_t, int, int, int, int, int,
-                     cudaStream_t)
+qg_status launch_moe(const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_g, const uint8_t* dn_codes,
+                     const uint8_t* dn_scales, const float* dn_g, const void* x, const int32_t* ids, const float* tw,
+                     void* y, void* ws, size_t ws_bytes, int M, int H, int I, int E, int topk, cudaStream_t stream)
 {
-    return QG_ERR_UNSUPPORTED;
+    const MoeLayout L = moe_layout(M, topk, H, I);
+    if (ws_bytes < L.total) return QG_ERR_WORKSPACE;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    uint16_t* h = reinterpret_cast<uint16_t*>(w + L.h);
+    float* yslot = reinterpret_cast<float*>(w + L.yslot);
+    int* ctrl = reinterpret_cast<int*>(w + L.ctrl);
+    GroupDesc* g_gu = reinterpret_cast<GroupDesc*>(w + L.g_gu);
+    GroupDesc* g_dn = reinterpret_cast<GroupDesc*>(w + L.g_dn);
+    UnitDesc* u_gu = reinterpret_cast<UnitDesc*>(w + L.u_gu);
+    UnitDesc* u_dn = reinterpret_cast<UnitDesc*>(w + L.u_dn);
+    int* status = device_status_ptr();
+    if (!status) return QG_ERR_CUDA;
+
+    moe_group_kernel<<<1, 256, 0, stream>>>(ids, M, topk, E, I, H, L.r_gu, L.r_dn, g_gu, g_dn, u_gu, u_dn, ctrl,
+                                            status);
+    if (cudaPeekAtLastError() != cudaSuccess) return QG_ERR_CUDA;
+    qg_status s = launch_grouped_nvfp4(gu_codes, gu_scales, E * 2 * I, H, 1, I, x, M, h, I, 0, g_gu, u_gu, ctrl + 0,
+                                       gu_g, L.r_gu, stream);
+    if (s != QG_OK) return s;
+    s = launch_grouped_nvfp4(dn_codes, dn_scales, E * H, I, 0, 0, h, 8, yslot, H, 1, g_dn, u_dn, ctrl + 1, dn_g,
+                             L.r_dn, stream);
+    if (s != QG_OK) return s;
+    const int n = M * H;
+    moe_combine_kernel<<<(n + 255) / 256, 256, 0, stream>>>(yslot, ids, tw, static_cast<uint16_t*>(y), M, topk, H, E);
+    return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
 }  // namespace qg

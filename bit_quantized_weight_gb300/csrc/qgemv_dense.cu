@@ -148,12 +148,11 @@ struct TileAcc {
 // weights are exact in bf16 as well, so the products stay exact.
 template <int FMT, int EPI, bool BF>
 __device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint32_t xb, uint32_t sm_base, int jsub,
-                                           int kk0, int ti, int lane, const int* xexp, TileAcc& acc)
+                                           int kk0, int ti, int lane, const int* xexp, int ntok, TileAcc& acc)
 {
     constexpr int NGU = (EPI == EPI_SWIGLU) ? 2 : 1;
     const int g = lane >> 2;
     const int t = lane & 3;
-    const int M = a.M;
     const int p0 = xexp[jsub * 8 + 2 * t];
     const int p1 = xexp[jsub * 8 + 2 * t + 1];
 
@@ -181,7 +180,7 @@ __device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
             const int kk = kk0 + 64 * ms + 32 * ch + 8 * t;
-            bx[ch] = g < M ? lds128(xb + (g * a.x_pitch + kk) * 2) : make_uint4(0, 0, 0, 0);
+            bx[ch] = g < ntok ? lds128(xb + (g * a.x_pitch + kk) * 2) : make_uint4(0, 0, 0, 0);
         }
         // ldmatrix: lane l supplies row (l & 7) + 8 * ((l >> 3) & 1) of the tile and
         // 16-byte chunk 2 * ms + (l >> 4); chunk c of row r sits at c ^ (r & 7).
@@ -299,19 +298,60 @@ __device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint
     }
 }
 
+// Unit of work: rows [w_row0, w_row0 + rows) of the weight tensor (gate rows
+// for SwiGLU; the up rows follow at + up_row_offset) against one group of
+// activation rows, written to output columns out_col0 + r.
+struct Unit {
+    int w_row0;
+    int rows;
+    int out_col0;
+    int grp;
+};
+
+__device__ __forceinline__ Unit load_unit(const DenseArgs& a, int u)
+{
+    Unit un;
+    if (a.units == nullptr) {
+        un.w_row0 = u * a.rows_per_cta;
+        un.rows = min(a.rows_per_cta, a.n_out - un.w_row0);
+        un.out_col0 = un.w_row0;
+        un.grp = 0;
+    } else {
+        const UnitDesc d = a.units[u];
+        un.w_row0 = d.w_row0;
+        un.rows = d.rows;
+        un.out_col0 = d.out_col0;
+        un.grp = d.grp;
+    }
+    return un;
+}
+
+// Units of this CTA: dense launches own exactly one (blockIdx.x); grouped
+// launches split the device-side unit list into contiguous ranges so that
+// consecutive units mostly share their group (and its converted activations).
+__device__ __forceinline__ void unit_range(const DenseArgs& a, int& u_begin, int& u_end)
+{
+    if (a.units == nullptr) {
+        u_begin = blockIdx.x;
+        u_end = blockIdx.x + 1;
+    } else {
+        const int n = *a.n_units;
+        u_begin = static_cast<int>((static_cast<long long>(n) * blockIdx.x) / gridDim.x);
+        u_end = static_cast<int>((static_cast<long long>(n) * (blockIdx.x + 1)) / gridDim.x);
+    }
+}
+
 template <int FMT, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-    dense_kernel(const __grid_constant__ DenseArgs a, const __grid_constant__ CUtensorMap tm0,
-                 const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm2,
-                 const __grid_constant__ CUtensorMap tm3)
+    gemv_kernel(const __grid_constant__ DenseArgs a, const __grid_constant__ CUtensorMap tm0,
+                const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm2,
+                const __grid_constant__ CUtensorMap tm3)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int NGU = (EPI == EPI_SWIGLU) ? 2 : 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int row0 = blockIdx.x * a.rows_per_cta;
-    const int rows = min(a.rows_per_cta, a.n_out - row0);
     const int n_chunks = a.K / kChunkK;
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.smem_bar);
@@ -323,17 +363,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // anything this grid writes.
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // Each stage is consumed by exactly one warp per 16-row tile.
-    const int n_tiles = (rows + 15) >> 4;
+    // Every stage is consumed by one warp per 16-row tile of a full unit.
+    const int T = (a.rows_per_cta + 15) >> 4;
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.n_stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], n_tiles);
+            mbar_init(&empty[s], T);
         }
         *abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
+
+    // Grouped launches read their unit list from the previous kernel's output.
+    if (a.units != nullptr) asm volatile("griddepcontrol.wait;" ::: "memory");
+    int u_begin, u_end;
+    unit_range(a, u_begin, u_end);
 
     // ------------------------------------------------------------ producer
     if (warp == kConsumerWarps) {
@@ -342,47 +387,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&tm1);
             if (FMT != FMT_NVFP4) prefetch_tensormap(&tm2);
             if (FMT == FMT_Q5) prefetch_tensormap(&tm3);
-            int issued = 0;
-            for (int c = 0; c < n_chunks; ++c) {
-                const int slot = c % a.n_stages;
-                if (c >= a.n_stages) {
-                    if (!mbar_wait_bounded(&empty[slot], ((c / a.n_stages) - 1) & 1, a.wait_ns, a.status)) {
-                        *abort_flag = 1;
+            int gc = 0;  // global stage counter across units
+            bool stop = false;
+            for (int u = u_begin; u < u_end && !stop; ++u) {
+                const Unit un = load_unit(a, u);
+                for (int c = 0; c < n_chunks; ++c, ++gc) {
+                    const int slot = gc % a.n_stages;
+                    if (gc >= a.n_stages) {
+                        if (!mbar_wait_bounded(&empty[slot], ((gc / a.n_stages) - 1) & 1, a.wait_ns, a.status)) {
+                            *abort_flag = 1;
+                            stop = true;
+                            break;
+                        }
+                    }
+                    if (*abort_flag || a.starve) {
+                        stop = true;
                         break;
                     }
-                }
-                if (*abort_flag || a.starve) break;
-                mbar_arrive_expect_tx(&full[slot], a.st.tx_bytes);
-                uint8_t* sb = smem + a.smem_ring + slot * a.st.bytes;
-                const int kb = c * kChunkK;
-                tma_load_2d(sb + a.st.codes, &tm0, kb / 2, row0, &full[slot]);
-                if (FMT == FMT_NVFP4) {
-                    tma_load_2d(sb + a.st.scales, &tm1, kb / 16, row0, &full[slot]);
-                    if (EPI == EPI_SWIGLU) {
-                        tma_load_2d(sb + a.st.codes2, &tm0, kb / 2, row0 + a.up_row_offset, &full[slot]);
-                        tma_load_2d(sb + a.st.scales2, &tm1, kb / 16, row0 + a.up_row_offset, &full[slot]);
+                    mbar_arrive_expect_tx(&full[slot], a.st.tx_bytes);
+                    uint8_t* sb = smem + a.smem_ring + slot * a.st.bytes;
+                    const int kb = c * kChunkK;
+                    tma_load_2d(sb + a.st.codes, &tm0, kb / 2, un.w_row0, &full[slot]);
+                    if (FMT == FMT_NVFP4) {
+                        tma_load_2d(sb + a.st.scales, &tm1, kb / 16, un.w_row0, &full[slot]);
+                        if (EPI == EPI_SWIGLU) {
+                            tma_load_2d(sb + a.st.codes2, &tm0, kb / 2, un.w_row0 + a.up_row_offset, &full[slot]);
+                            tma_load_2d(sb + a.st.scales2, &tm1, kb / 16, un.w_row0 + a.up_row_offset, &full[slot]);
+                        }
+                    } else {
+                        tma_load_2d(sb + a.st.scales, &tm1, kb / 32, un.w_row0, &full[slot]);
+                        tma_load_2d(sb + a.st.mins, &tm2, kb / 32, un.w_row0, &full[slot]);
+                        if (FMT == FMT_Q5) tma_load_2d(sb + a.st.hi, &tm3, kb / 8, un.w_row0, &full[slot]);
                     }
-                } else {
-                    tma_load_2d(sb + a.st.scales, &tm1, kb / 32, row0, &full[slot]);
-                    tma_load_2d(sb + a.st.mins, &tm2, kb / 32, row0, &full[slot]);
-                    if (FMT == FMT_Q5) tma_load_2d(sb + a.st.hi, &tm3, kb / 8, row0, &full[slot]);
                 }
-                issued = c + 1;
             }
             // No copy may still be landing in shared memory when the CTA exits.
-            for (int c = max(0, issued - a.n_stages); c < issued; ++c)
+            for (int c = max(0, gc - a.n_stages); c < gc; ++c)
                 mbar_wait_bounded(&full[c % a.n_stages], (c / a.n_stages) & 1, a.wait_ns, a.status);
         }
         return;
     }
 
     // ------------------------------------------------------------ consumers
-    // Warp w works on tile (w % Tp) for the stages c with c % S == w / Tp; the
-    // S slices of a tile are summed in a fixed order at the end.
-    const int T = (rows + 15) >> 4;
+    // Warps w = S * tile + slice: the S slices of a tile take the stages
+    // c with c % S == slice (consecutive warps sit on different schedulers);
+    // slices are summed in a fixed order at the end of each unit.
     const int Tp = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16;
     const int S = kConsumerWarps / Tp;
-    // consecutive warps (on different schedulers) take the slices of one tile
     const int slice = warp % S;
     const int my_tile = (warp / S) < T ? (warp / S) : -1;
 
@@ -392,205 +443,205 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* xexp = reinterpret_cast<int*>(smem + a.smem_exp);            // [nsub][8]
     uint8_t* xflag = smem + a.smem_flag;                                // [nsub][8]
     float* xsum = reinterpret_cast<float*>(smem + a.smem_sum);        // [nsub * 8 groups][8]
-    const int M = a.M;
+    float* red = reinterpret_cast<float*>(smem + a.smem_red);
     const int ctid = threadIdx.x;                                       // 0 .. 511 among consumers
 
-    // The activations (and residual) may come from the previous kernel on the
+    // Activations (and residuals) may come from the previous kernel on the
     // stream: wait for it before touching them. Weight streaming above does
     // not depend on it and is already running.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    {
-        const int lines_per_row = (min(a.ksc, a.K) * 2) >> 7;  // 128-byte lines
-        for (int i = ctid; i < a.M * lines_per_row; i += 32 * kConsumerWarps) {
-            const uint16_t* p = a.x + static_cast<size_t>(i / lines_per_row) * a.K + (i % lines_per_row) * 64;
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-        }
-    }
-
-    // entries of tokens >= M stay zero for the whole kernel
-    {
-        const int nsub_max = a.ksc / kChunkK;
-        for (int i = ctid; i < nsub_max * 8; i += 32 * kConsumerWarps) {
-            xexp[i] = 0;
-            xflag[i] = 0;
-        }
-        if (FMT != FMT_NVFP4)
-            for (int i = ctid; i < nsub_max * 64; i += 32 * kConsumerWarps) xsum[i] = 0.f;
-    }
-
-    TileAcc acc;
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc.v[j][e] = 0.f;
 
     bool aborted = false;
-    int ks0 = -a.ksc;
-    for (int c = 0; c < n_chunks; ++c) {
-        const int kglob = c * kChunkK;
-        // ---------------- activation super-chunk: prescale, convert, flag
-        if (kglob == ks0 + a.ksc) {
-            ks0 += a.ksc;
-            const int len = min(a.ksc, a.K - ks0);
-            const int nsub = len / kChunkK;
-            const int n_items = nsub * M;
-            named_barrier_sync(1, 32 * kConsumerWarps);
-            for (int base = warp; base < n_items; base += 2 * kConsumerWarps) {
-                uint4 raw[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int it = base + u * kConsumerWarps;
-                    raw[u] = make_uint4(0, 0, 0, 0);
-                    if (it < n_items) {
-                        const int m = it % M, j = it / M;
-                        raw[u] = ldg_nc_128(a.x + static_cast<size_t>(m) * a.K + ks0 + j * kChunkK + lane * 8);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int it = base + u * kConsumerWarps;
-                    if (it >= n_items) break;
-                    const int m = it % M, j = it / M;
-                    const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-                    uint32_t hbits[8];
-                    uint32_t mag = 0;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        hbits[i] = (i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu);
-                        const uint32_t mg = hbits[i] & 0x7FFFu;
-                        if (mg < 0x7F80u) mag = max(mag, mg);
-                    }
-                    mag = __reduce_max_sync(0xffffffffu, mag);
-                    const int p = prescale_exponent(mag);
-                    uint32_t h[8];
-                    bool exact = true;
-                    float ls = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float v = ldexp_exact(bf16_bits_to_f32(hbits[i]), p);
-                        const __half hv = __float2half_rn(v);
-                        h[i] = __half_as_ushort(hv);
-                        if (isfinite(v) && __half2float(hv) != v) exact = false;
-                        ls += v;
-                    }
-                    const uint32_t off = (static_cast<uint32_t>(m) * a.x_pitch + j * kChunkK + lane * 8) * 2;
-                    const uint4 hv = pack_pairs<FMT>(h);
-                    const uint4 rv = pack_pairs<FMT>(hbits);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(x_base + off), "r"(hv.x), "r"(hv.y),
-                                 "r"(hv.z), "r"(hv.w));
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(xraw_base + off), "r"(rv.x),
-                                 "r"(rv.y), "r"(rv.z), "r"(rv.w));
-                    const bool any_inexact = __any_sync(0xffffffffu, !exact);
-                    if (lane == 0) {
-                        xexp[j * 8 + m] = p;
-                        xflag[j * 8 + m] = any_inexact ? 1 : 0;
-                    }
-                    if (FMT != FMT_NVFP4) {
-                        ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-                        ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-                        if ((lane & 3) == 0) xsum[(j * 8 + (lane >> 2)) * 8 + m] = ls;
-                    }
-                }
-            }
-            named_barrier_sync(1, 32 * kConsumerWarps);
+    int gc = 0;
+    int conv_key = -1;     // activation rows (group xkey) the buffer holds
+    int conv_ks0 = -1;     // and the super-chunk start
+    for (int u = u_begin; u < u_end; ++u) {
+        const Unit un = load_unit(a, u);
+        // ---------------- group info of this unit
+        int ntok, xkey;
+        float gsc;
+        if (a.units == nullptr) {
+            ntok = a.M;
+            gsc = a.g;
+            xkey = 0;
+        } else {
+            ntok = a.groups[un.grp].ntok;
+            gsc = a.gscales[a.groups[un.grp].e];
+            xkey = a.groups[un.grp].xkey;
         }
+        TileAcc acc;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc.v[j][e] = 0.f;
 
-        const int slot = c % a.n_stages;
-        const bool mine = (c % S) == slice && my_tile >= 0;
-        if (!mine) continue;
-        if (!aborted && *abort_flag) aborted = true;
-        if (!aborted) {
-            if (!mbar_wait_bounded(&full[slot], (c / a.n_stages) & 1, a.wait_ns, a.status)) {
-                aborted = true;
-                *abort_flag = 1;
+        for (int c = 0; c < n_chunks; ++c, ++gc) {
+            const int kglob = c * kChunkK;
+            const int ks0 = (kglob / a.ksc) * a.ksc;
+            // ---------------- activation super-chunk: prescale, convert, flag
+            if (ks0 != conv_ks0 || xkey != conv_key) {
+                const int len = min(a.ksc, a.K - ks0);
+                const int nsub = len / kChunkK;
+                const int n_items = nsub * ntok;
+                named_barrier_sync(1, 32 * kConsumerWarps);
+                // columns >= ntok read zero exponents / flags / sums
+                for (int i = ctid; i < nsub * 8; i += 32 * kConsumerWarps) {
+                    if ((i & 7) >= ntok) {
+                        xexp[i] = 0;
+                        xflag[i] = 0;
+                    }
+                }
+                if (FMT != FMT_NVFP4)
+                    for (int i = ctid; i < nsub * 64; i += 32 * kConsumerWarps)
+                        if ((i & 7) >= ntok) xsum[i] = 0.f;
+                for (int base = warp; base < n_items; base += 2 * kConsumerWarps) {
+                    uint4 raw[2];
+#pragma unroll
+                    for (int uu = 0; uu < 2; ++uu) {
+                        const int it = base + uu * kConsumerWarps;
+                        raw[uu] = make_uint4(0, 0, 0, 0);
+                        if (it < n_items) {
+                            const int m = it % ntok, j = it / ntok;
+                            const int xr = a.units == nullptr ? m : a.groups[un.grp].x_row[m];
+                            raw[uu] = ldg_nc_128(a.x + static_cast<size_t>(xr) * a.K + ks0 + j * kChunkK + lane * 8);
+                        }
+                    }
+#pragma unroll
+                    for (int uu = 0; uu < 2; ++uu) {
+                        const int it = base + uu * kConsumerWarps;
+                        if (it >= n_items) break;
+                        const int m = it % ntok, j = it / ntok;
+                        const uint32_t wv[4] = {raw[uu].x, raw[uu].y, raw[uu].z, raw[uu].w};
+                        uint32_t hbits[8];
+                        uint32_t mag = 0;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            hbits[i] = (i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu);
+                            const uint32_t mg = hbits[i] & 0x7FFFu;
+                            if (mg < 0x7F80u) mag = max(mag, mg);
+                        }
+                        mag = __reduce_max_sync(0xffffffffu, mag);
+                        const int p = prescale_exponent(mag);
+                        uint32_t h[8];
+                        bool exact = true;
+                        float ls = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float v = ldexp_exact(bf16_bits_to_f32(hbits[i]), p);
+                            const __half hv = __float2half_rn(v);
+                            h[i] = __half_as_ushort(hv);
+                            if (isfinite(v) && __half2float(hv) != v) exact = false;
+                            ls += v;
+                        }
+                        const uint32_t off = (static_cast<uint32_t>(m) * a.x_pitch + j * kChunkK + lane * 8) * 2;
+                        const uint4 hv = pack_pairs<FMT>(h);
+                        const uint4 rv = pack_pairs<FMT>(hbits);
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(x_base + off), "r"(hv.x),
+                                     "r"(hv.y), "r"(hv.z), "r"(hv.w));
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(xraw_base + off), "r"(rv.x),
+                                     "r"(rv.y), "r"(rv.z), "r"(rv.w));
+                        const bool any_inexact = __any_sync(0xffffffffu, !exact);
+                        if (lane == 0) {
+                            xexp[j * 8 + m] = p;
+                            xflag[j * 8 + m] = any_inexact ? 1 : 0;
+                        }
+                        if (FMT != FMT_NVFP4) {
+                            ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+                            ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+                            if ((lane & 3) == 0) xsum[(j * 8 + (lane >> 2)) * 8 + m] = ls;
+                        }
+                    }
+                }
+                named_barrier_sync(1, 32 * kConsumerWarps);
+                conv_ks0 = ks0;
+                conv_key = xkey;
             }
-        }
-        if (!aborted) {
-            const uint32_t sb = sm_base + a.smem_ring + slot * a.st.bytes;
-            const int jsub = (kglob - ks0) / kChunkK;
-            const uint64_t flags8 = *reinterpret_cast<const uint64_t*>(xflag + jsub * 8);
-            const int kk0 = kglob - ks0;
-            if (my_tile >= 0) {
+
+            const int slot = gc % a.n_stages;
+            if ((c % S) != slice || my_tile < 0) continue;
+            if (!aborted && *abort_flag) aborted = true;
+            if (!aborted) {
+                if (!mbar_wait_bounded(&full[slot], (gc / a.n_stages) & 1, a.wait_ns, a.status)) {
+                    aborted = true;
+                    *abort_flag = 1;
+                }
+            }
+            if (!aborted && 16 * my_tile < un.rows) {
+                const uint32_t sb = sm_base + a.smem_ring + slot * a.st.bytes;
+                const int jsub = (kglob - ks0) / kChunkK;
+                const uint64_t flags8 = *reinterpret_cast<const uint64_t*>(xflag + jsub * 8);
+                const int kk0 = kglob - ks0;
                 if (flags8)
-                    tile_stage<FMT, EPI, true>(a, sb, xraw_base, sm_base, jsub, kk0, my_tile, lane, xexp, acc);
+                    tile_stage<FMT, EPI, true>(a, sb, xraw_base, sm_base, jsub, kk0, my_tile, lane, xexp, ntok, acc);
                 else
-                    tile_stage<FMT, EPI, false>(a, sb, x_base, sm_base, jsub, kk0, my_tile, lane, xexp, acc);
+                    tile_stage<FMT, EPI, false>(a, sb, x_base, sm_base, jsub, kk0, my_tile, lane, xexp, ntok, acc);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-    }
 
-    // ---------------- cross-slice reduction (fixed order) and epilogue
-    float* red = reinterpret_cast<float*>(smem + a.smem_red);
-    if (S > 1) {
-        named_barrier_sync(1, 32 * kConsumerWarps);
-        if (slice > 0 && my_tile >= 0) {
-#pragma unroll
-            for (int gu = 0; gu < NGU; ++gu)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    red[(((slice * Tp + my_tile) * 2 + gu) * 32 + lane) * 4 + e] = acc.v[gu][e];
-        }
-        named_barrier_sync(1, 32 * kConsumerWarps);
-        if (slice == 0 && my_tile >= 0) {
-            for (int s = 1; s < S; ++s)
+        // ---------------- cross-slice reduction (fixed order) and epilogue
+        if (S > 1) {
+            named_barrier_sync(1, 32 * kConsumerWarps);
+            if (slice > 0 && my_tile >= 0) {
 #pragma unroll
                 for (int gu = 0; gu < NGU; ++gu)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        acc.v[gu][e] += red[(((s * Tp + my_tile) * 2 + gu) * 32 + lane) * 4 + e];
-        }
-    }
-    if (slice != 0 || aborted || my_tile < 0) return;
-
-    const int g = lane >> 2, t = lane & 3;
+                        red[(((slice * Tp + my_tile) * 2 + gu) * 32 + lane) * 4 + e] = acc.v[gu][e];
+            }
+            named_barrier_sync(1, 32 * kConsumerWarps);
+            if (slice == 0 && my_tile >= 0) {
+                for (int s = 1; s < S; ++s)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int r = 16 * my_tile + g + ((e & 2) ? 8 : 0);
-        const int tok = 2 * t + (e & 1);
-        if (r >= rows || tok >= M) continue;
-        const int n = row0 + r;
-        float v = acc.v[0][e] * a.g;
-        if (EPI == EPI_SWIGLU) {
-            const float u = acc.v[1][e] * a.g;
-            v = (v / (1.0f + expf(-v))) * u;
+                    for (int gu = 0; gu < NGU; ++gu)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            acc.v[gu][e] += red[(((s * Tp + my_tile) * 2 + gu) * 32 + lane) * 4 + e];
+            }
         }
-        if (EPI == EPI_RESID) v += bf16_bits_to_f32(a.residual[static_cast<size_t>(tok) * a.n_out + n]);
-        if (a.out_f32) {
-            reinterpret_cast<float*>(a.y)[static_cast<size_t>(tok) * a.n_out + n] = v;
-        } else {
-            reinterpret_cast<uint16_t*>(a.y)[static_cast<size_t>(tok) * a.n_out + n] = f32_to_bf16_bits_rn(v);
+        if (slice == 0 && !aborted && my_tile >= 0) {
+            const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = 16 * my_tile + g + ((e & 2) ? 8 : 0);
+                const int col = 2 * t + (e & 1);
+                if (r >= un.rows || col >= ntok) continue;
+                const int orow = a.units == nullptr ? col : a.groups[un.grp].out_row[col];
+                if (orow < 0) continue;
+                const size_t o = static_cast<size_t>(orow) * a.out_pitch + un.out_col0 + r;
+                float v = acc.v[0][e] * gsc;
+                if (EPI == EPI_SWIGLU) {
+                    const float uv = acc.v[1][e] * gsc;
+                    v = (v / (1.0f + expf(-v))) * uv;
+                }
+                if (EPI == EPI_RESID) v += bf16_bits_to_f32(a.residual[o]);
+                if (a.out_f32)
+                    reinterpret_cast<float*>(a.y)[o] = v;
+                else
+                    reinterpret_cast<uint16_t*>(a.y)[o] = f32_to_bf16_bits_rn(v);
+            }
         }
     }
 }
 
 constexpr uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
+// Fills in the launch-time fields of `a` (status word, debug limits, shared
+// memory plan) and launches `grid` CTAs with programmatic dependent launch.
 template <int FMT, int EPI>
-qg_status launch_dense_impl(const CUtensorMap* maps, const uint16_t* x, void* y, int out_f32,
-                            const uint16_t* residual, int M, int n_out, int up_offset, int K, float g,
-                            int rows_per_cta, cudaStream_t stream)
+qg_status launch_gemv_impl(const CUtensorMap* maps, DenseArgs a, int grid, cudaStream_t stream)
 {
-    DenseArgs a{};
-    a.x = x;
-    a.y = y;
-    a.residual = residual;
-    a.M = M;
-    a.K = K;
-    a.n_out = n_out;
-    a.rows_per_cta = rows_per_cta;
-    a.up_row_offset = up_offset;
-    a.out_f32 = out_f32;
-    a.g = g;
+    const int M = a.M;
+    const int K = a.K;
     a.status = device_status_ptr();
     if (!a.status) return QG_ERR_CUDA;
     const DebugState dbg = debug_state();
     a.wait_ns = dbg.wait_ns;
     a.starve = dbg.starve;
 
-    // activation super-chunk: M token rows of (ksc + 32) f16 within 64 KB
-    // f16 (prescaled) and raw bf16 copies of M token rows of (ksc + 32) values
+    // activation super-chunk: f16 (prescaled) and raw bf16 copies of M token
+    // rows of (ksc + 32) values
     constexpr uint32_t kXBudget = 80 * 1024;
     int ksc = (static_cast<int>(kXBudget / (4u * M)) - 32) / kChunkK * kChunkK;
     ksc = min(ksc, K);
@@ -598,7 +649,7 @@ qg_status launch_dense_impl(const CUtensorMap* maps, const uint16_t* x, void* y,
     a.x_pitch = ksc + 32;
     const int nsub = ksc / kChunkK;
 
-    const int R = rows_per_cta;
+    const int R = a.rows_per_cta;
     const int R16 = (R + 15) / 16 * 16;  // regions cover whole 16-row tiles
     StageLayout st{};
     uint32_t off = 0;
@@ -663,7 +714,7 @@ qg_status launch_dense_impl(const CUtensorMap* maps, const uint16_t* x, void* y,
     a.smem_bar = so;
     so += bar_bytes;
 
-    auto kern = dense_kernel<FMT, EPI>;
+    auto kern = gemv_kernel<FMT, EPI>;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
@@ -672,7 +723,6 @@ qg_status launch_dense_impl(const CUtensorMap* maps, const uint16_t* x, void* y,
             return QG_ERR_CUDA;
         attr_set[dev] = true;
     }
-    const int grid = (n_out + R - 1) / R;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -696,6 +746,24 @@ int choose_rows_per_cta(int n_out, int factor)
     return R;
 }
 
+DenseArgs dense_args(const void* x, void* y, int out_f32, const void* residual, int M, int n_out, int up_offset,
+                     int K, float g, int R)
+{
+    DenseArgs a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.y = y;
+    a.residual = static_cast<const uint16_t*>(residual);
+    a.M = M;
+    a.K = K;
+    a.n_out = n_out;
+    a.out_pitch = n_out;
+    a.rows_per_cta = R;
+    a.up_row_offset = up_offset;
+    a.out_f32 = out_f32;
+    a.g = g;
+    return a;
+}
+
 }  // namespace
 
 qg_status launch_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
@@ -711,13 +779,15 @@ qg_status launch_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float 
         return QG_ERR_CUDA;
     maps[2] = maps[1];
     maps[3] = maps[1];
-    const uint16_t* xx = static_cast<const uint16_t*>(x);
-    const uint16_t* rr = static_cast<const uint16_t*>(residual);
+    const int grid = (n_out + R - 1) / R;
     if (swiglu)
-        return launch_dense_impl<FMT_NVFP4, EPI_SWIGLU>(maps, xx, y, 0, nullptr, M, n_out, n_out, K, g, R, stream);
+        return launch_gemv_impl<FMT_NVFP4, EPI_SWIGLU>(maps, dense_args(x, y, 0, nullptr, M, n_out, n_out, K, g, R),
+                                                       grid, stream);
     if (residual)
-        return launch_dense_impl<FMT_NVFP4, EPI_RESID>(maps, xx, y, out_f32, rr, M, n_out, 0, K, g, R, stream);
-    return launch_dense_impl<FMT_NVFP4, EPI_NONE>(maps, xx, y, out_f32, nullptr, M, n_out, 0, K, g, R, stream);
+        return launch_gemv_impl<FMT_NVFP4, EPI_RESID>(maps, dense_args(x, y, out_f32, residual, M, n_out, 0, K, g, R),
+                                                      grid, stream);
+    return launch_gemv_impl<FMT_NVFP4, EPI_NONE>(maps, dense_args(x, y, out_f32, nullptr, M, n_out, 0, K, g, R), grid,
+                                                 stream);
 }
 
 qg_status launch_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min,
@@ -738,16 +808,39 @@ qg_status launch_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void*
     } else {
         maps[3] = maps[2];
     }
-    const uint16_t* xx = static_cast<const uint16_t*>(x);
-    const uint16_t* rr = static_cast<const uint16_t*>(residual);
+    const int grid = (N + R - 1) / R;
+    const DenseArgs a = dense_args(x, y, out_f32, residual, M, N, 0, K, 1.f, R);
     if (bits == 5) {
-        if (residual)
-            return launch_dense_impl<FMT_Q5, EPI_RESID>(maps, xx, y, out_f32, rr, M, N, 0, K, 1.f, R, stream);
-        return launch_dense_impl<FMT_Q5, EPI_NONE>(maps, xx, y, out_f32, nullptr, M, N, 0, K, 1.f, R, stream);
+        if (residual) return launch_gemv_impl<FMT_Q5, EPI_RESID>(maps, a, grid, stream);
+        return launch_gemv_impl<FMT_Q5, EPI_NONE>(maps, a, grid, stream);
     }
-    if (residual)
-        return launch_dense_impl<FMT_Q4, EPI_RESID>(maps, xx, y, out_f32, rr, M, N, 0, K, 1.f, R, stream);
-    return launch_dense_impl<FMT_Q4, EPI_NONE>(maps, xx, y, out_f32, nullptr, M, N, 0, K, 1.f, R, stream);
+    if (residual) return launch_gemv_impl<FMT_Q4, EPI_RESID>(maps, a, grid, stream);
+    return launch_gemv_impl<FMT_Q4, EPI_NONE>(maps, a, grid, stream);
+}
+
+qg_status launch_grouped_nvfp4(const uint8_t* codes, const uint8_t* scales, int total_rows, int K, int swiglu,
+                               int up_offset, const void* x, int max_cols, void* y, int out_pitch, int out_f32,
+                               const GroupDesc* groups, const UnitDesc* units, const int* n_units,
+                               const float* gscales, int rows_per_unit, cudaStream_t stream)
+{
+    const int R = rows_per_unit;
+    CUtensorMap maps[4];
+    memset(maps, 0, sizeof(maps));
+    if (!encode_tmap_2d(&maps[0], codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, total_rows, 128, R, true))
+        return QG_ERR_CUDA;
+    if (!encode_tmap_2d(&maps[1], scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 16, total_rows, 16, R, false))
+        return QG_ERR_CUDA;
+    maps[2] = maps[1];
+    maps[3] = maps[1];
+    DenseArgs a = dense_args(x, y, out_f32, nullptr, max_cols, 0, up_offset, K, 1.f, R);
+    a.out_pitch = out_pitch;
+    a.groups = groups;
+    a.units = units;
+    a.n_units = n_units;
+    a.gscales = gscales;
+    const int grid = sm_count(-1);
+    if (swiglu) return launch_gemv_impl<FMT_NVFP4, EPI_SWIGLU>(maps, a, grid, stream);
+    return launch_gemv_impl<FMT_NVFP4, EPI_NONE>(maps, a, grid, stream);
 }
 
 }  // namespace qg

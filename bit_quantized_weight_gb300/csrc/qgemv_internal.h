@@ -31,17 +31,40 @@ struct StageLayout {
     uint32_t tx_bytes;   // bytes the TMA writes per stage
 };
 
+// A group shares one set of activation rows (the MMA's 8 token columns):
+// column j reads activation row x_row[j] and writes output row out_row[j]
+// (-1: not stored). Grouped launches (MoE) take their units from device memory.
+struct GroupDesc {
+    int ntok;        // columns in use (the rest are zero)
+    int e;           // expert id (per-expert global scale)
+    int xkey;        // groups with equal xkey read the same activation rows
+    int x_row[8];
+    int out_row[8];
+};
+
+struct UnitDesc {
+    int grp;         // index into the group array
+    int w_row0;      // first weight row (gate row for SwiGLU)
+    int rows;        // rows in this unit (<= rows_per_cta)
+    int out_col0;    // first output column
+};
+
 struct DenseArgs {
-    const uint16_t* x;         // bf16 [M][K]
-    void* y;                   // [M][n_out]
-    const uint16_t* residual;  // bf16 [M][n_out] or nullptr
-    int M;
+    const uint16_t* x;         // bf16 activations, rows of K values
+    void* y;                   // output rows of out_pitch values
+    const uint16_t* residual;  // bf16, same layout as y, or nullptr
+    int M;                     // dense: tokens; grouped: max columns per group
     int K;
-    int n_out;                 // output columns (logical rows)
+    int n_out;                 // dense: output columns (logical rows)
+    int out_pitch;             // elements per output row
     int rows_per_cta;          // R (box rows)
-    int up_row_offset;         // SwiGLU: first up row (= n_out)
+    int up_row_offset;         // SwiGLU: up row = gate row + this
     int out_f32;
     float g;
+    const GroupDesc* groups;   // grouped mode (nullptr for dense)
+    const UnitDesc* units;
+    const int* n_units;
+    const float* gscales;      // per-expert global scale (grouped mode)
     int n_stages;
     int ksc;                   // k per activation super-chunk
     int x_pitch;               // f16 elements per token row of the activation buffer
@@ -77,6 +100,10 @@ qg_status launch_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float 
 qg_status launch_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min,
                            int bits, const void* x, void* y, int out_f32, const void* residual, int M,
                            int N, int K, cudaStream_t stream);
+qg_status launch_grouped_nvfp4(const uint8_t* codes, const uint8_t* scales, int total_rows, int K, int swiglu,
+                               int up_offset, const void* x, int max_cols, void* y, int out_pitch, int out_f32,
+                               const GroupDesc* groups, const UnitDesc* units, const int* n_units,
+                               const float* gscales, int rows_per_unit, cudaStream_t stream);
 qg_status launch_simple(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
                         const void* mins, float g, const void* x, void* y, int out_f32,
                         const void* residual, int M, int N, int K, int swiglu, cudaStream_t stream);

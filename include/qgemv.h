@@ -135,7 +135,9 @@ QG_API qg_status moe_qgemv_nvfp4_workspace_size(int M, int topk, int H, int I, i
  *   x bf16[M][H]; topk_ids int32[M][topk]; topk_w fp32[M][topk]; y bf16[M][H]
  *   workspace: caller-owned device memory of at least
  *   moe_qgemv_nvfp4_workspace_size() bytes, 256-byte aligned. It starts with
- *   h as bf16[M][topk][I]; the rest is private scratch.
+ *   h as bf16[M][topk][I] (a slot that repeats an expert of the same token,
+ *   or names an invalid one, leaves its row unwritten); the rest is private
+ *   scratch.
  * Expert ids outside [0, E) are not checked on the host (they are device
  * data); such a slot contributes nothing and records QG_ERR_INVALID_ARG in the
  * device status word (see qg_last_device_status).
