@@ -54,6 +54,7 @@ def lib():
         L.moe_qgemv_nvfp4_workspace_size.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_qgemv_nvfp4.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                       _I, _I, _I, _I, _I, _P]
+        L.moe_qgemv_nvfp4_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]
         L.qdequant_nvfp4.argtypes = [_P, _P, _F, _P, _I, _I, _P]
         L.qdequant_q45.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _P]
         L.qg_last_device_status.argtypes = [_P]
@@ -61,7 +62,8 @@ def lib():
         L.qg_status_string.restype = ctypes.c_char_p
         L.qg_debug_set_wait.argtypes = [ctypes.c_uint64, _I]
         for name in ("qgemv_nvfp4", "qgemv_q45", "qgemv_swiglu_nvfp4", "moe_route_topk",
-                     "moe_qgemv_nvfp4_workspace_size", "moe_qgemv_nvfp4", "qdequant_nvfp4",
+                     "moe_qgemv_nvfp4_workspace_size", "moe_qgemv_nvfp4", "moe_qgemv_nvfp4_noalloc",
+                     "qdequant_nvfp4",
                      "qdequant_q45", "qg_last_device_status", "qg_debug_set_wait"):
             getattr(L, name).restype = _I
         _lib = L
@@ -150,6 +152,19 @@ def moe_qgemv_nvfp4(gu_codes, gu_scales, gu_g, dn_codes, dn_scales, dn_g, x, ids
         _ptr(gu_codes), _ptr(gu_scales), _ptr(gu_g), _ptr(dn_codes), _ptr(dn_scales), _ptr(dn_g), _ptr(x),
         _ptr(ids), _ptr(w), _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
         M, H, two_i // 2, E, topk, _stream(stream)))
+    return y
+
+
+def moe_qgemv_nvfp4_noalloc(gu_codes, gu_scales, gu_g, dn_codes, dn_scales, dn_g, x, ids, w, y, stream=None):
+    """moe_qgemv_nvfp4 for callers that cannot allocate: the library's own
+    fixed 4 MiB device scratch replaces the workspace (see include/qgemv.h)."""
+    _cuda(gu_codes, gu_scales, gu_g, dn_codes, dn_scales, dn_g, x, ids, w, y)
+    E, two_i, hh = gu_codes.shape
+    M, H = x.shape
+    topk = ids.shape[1]
+    _check("moe_qgemv_nvfp4_noalloc", lib().moe_qgemv_nvfp4_noalloc(
+        _ptr(gu_codes), _ptr(gu_scales), _ptr(gu_g), _ptr(dn_codes), _ptr(dn_scales), _ptr(dn_g), _ptr(x),
+        _ptr(ids), _ptr(w), _ptr(y), M, H, two_i // 2, E, topk, _stream(stream)))
     return y
 
 

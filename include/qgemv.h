@@ -150,6 +150,30 @@ QG_API qg_status moe_qgemv_nvfp4(const uint8_t* gu_codes, const uint8_t* gu_scal
                           int topk, cudaStream_t stream);
 
 /*
+ * moe_qgemv_nvfp4 without a workspace argument, for callers that cannot
+ * allocate device memory: a plugin whose host framework owns all device
+ * memory and offers no allocator, or a latency-critical decode loop that may
+ * not call cudaMalloc. The pages have no counterpart; this is a library
+ * convenience. Arguments and results are those of moe_qgemv_nvfp4.
+ *   - The scratch is a fixed 4 MiB device array inside the library image
+ *     (every GPU that loads the library holds it until exit). Sizes whose
+ *     moe_qgemv_nvfp4_workspace_size() exceeds 4 MiB return QG_ERR_WORKSPACE
+ *     (at M = 8 and top-8, H = 4096 with I = 2048 still fits).
+ *   - The first call on a device looks up the array's device address; make
+ *     that first call before any stream capture on that device.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero). Calls that overlap on the GPU
+ *     -- on different streams, or from several host threads -- race; order
+ *     them on one stream.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating routine.
+ */
+QG_API qg_status moe_qgemv_nvfp4_noalloc(const uint8_t* gu_codes, const uint8_t* gu_scales,
+                                         const float* gu_gscale, const uint8_t* dn_codes,
+                                         const uint8_t* dn_scales, const float* dn_gscale, const void* x,
+                                         const int32_t* topk_ids, const float* topk_w, void* y, int M, int H,
+                                         int I, int E, int topk, cudaStream_t stream);
+
+/*
  * Dequantise to fp32 w[N][K] with the same device decode the GEMV kernels
  * use (test hook for the bit-exact check). NVFP4: w = fp32(e2m1 * e4m3) * g,
  * one rounding. Q4/Q5: w = fmaf(scale, q, min), one rounding.
