@@ -106,6 +106,19 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtyp
 
 using namespace qg;
 
+namespace {
+
+// NVFP4 with K a multiple of 256: the tcgen05 kernel, else the mma.sync one.
+qg_status dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y, int f32,
+                      const void* residual, int M, int N, int K, int swiglu, cudaStream_t stream)
+{
+    const qg_status s = launch_tc_dense_nvfp4(codes, scales, g, x, y, f32, residual, M, N, K, swiglu, stream);
+    if (s != QG_ERR_UNSUPPORTED) return s;
+    return launch_dense_nvfp4(codes, scales, g, x, y, f32, residual, M, N, K, swiglu, stream);
+}
+
+}  // namespace
+
 extern "C" {
 
 qg_status qgemv_nvfp4(const uint8_t* codes, const uint8_t* scales, float global_scale, const void* x, void* y,
@@ -116,7 +129,7 @@ qg_status qgemv_nvfp4(const uint8_t* codes, const uint8_t* scales, float global_
     if (y_dtype != QG_OUT_BF16 && y_dtype != QG_OUT_F32) return QG_ERR_INVALID_ARG;
     const int f32 = y_dtype == QG_OUT_F32;
     if (K % kChunkK == 0)
-        return launch_dense_nvfp4(codes, scales, global_scale, x, y, f32, residual, M, N, K, 0, stream);
+        return dense_nvfp4(codes, scales, global_scale, x, y, f32, residual, M, N, K, 0, stream);
     return launch_simple(FMT_NVFP4, codes, nullptr, scales, nullptr, global_scale, x, y, f32, residual, M, N, K, 0,
                          stream);
 }
@@ -145,7 +158,7 @@ qg_status qgemv_swiglu_nvfp4(const uint8_t* codes, const uint8_t* scales, float 
     if (s != QG_OK) return s;
     if (N % 2 != 0) return QG_ERR_INVALID_ARG;
     if (K % kChunkK == 0)
-        return launch_dense_nvfp4(codes, scales, global_scale, x, y, 0, nullptr, M, N, K, 1, stream);
+        return dense_nvfp4(codes, scales, global_scale, x, y, 0, nullptr, M, N, K, 1, stream);
     return launch_simple(FMT_NVFP4, codes, nullptr, scales, nullptr, global_scale, x, y, 0, nullptr, M, N, K, 1,
                          stream);
 }

@@ -69,6 +69,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` while the phase
+// is incomplete; it wakes when the phase completes, so waiting costs no issue
+// slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// One lane of the warp is elected (true for exactly one active lane).
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile("{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.u32 %0, 1, 0, P;\n}\n" : "=r"(pred));
+    return pred != 0;
+}
+
+// Warp index the compiler can treat as uniform across the warp.
+__device__ __forceinline__ int warp_index_uniform()
+{
+    return __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
+}
+
 // Wait for the phase with the given parity to complete, for at most
 // limit_ns nanoseconds. Returns false (and records a device timeout) when the
 // limit runs out; the caller then stops issuing work and returns.
@@ -174,6 +202,62 @@ __device__ __forceinline__ float ldexp_exact(float v, int e)
     const int e1 = e / 2;
     const int e2 = e - e1;
     return v * __int_as_float((127 + e1) << 23) * __int_as_float((127 + e2) << 23);
+}
+
+// ----------------------------------------------------------------- loads
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_128(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// ----------------------------------------------------------------- activation prescale
+// Power-of-two prescale exponent p for a chunk whose largest finite |x| has
+// bf16 magnitude bits `mag` (0 if every value is zero): max * 2^p in [2^14, 2^15).
+__device__ __forceinline__ int prescale_exponent(uint32_t mag)
+{
+    if (mag == 0) return 0;
+    uint32_t e = mag >> 7;
+    if (e > 0) return 141 - static_cast<int>(e);
+    // subnormal bf16: value = mag * 2^-133
+    int lg = 31 - __clz(static_cast<int>(mag));
+    return 147 - lg;
+}
+
+// Exact f16x2 -> bf16x2 for values with at most 8 significant bits in the
+// bf16 normal range (the decoded weights): through fp32, both steps exact.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h2)
+{
+    const float lo = half_bits_to_f32(h2 & 0xFFFFu), hi = half_bits_to_f32(h2 >> 16);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 // ----------------------------------------------------------------- MMA

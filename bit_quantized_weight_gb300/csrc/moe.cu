@@ -238,6 +238,20 @@ __global__ void moe_combine_kernel(const float* yslot, const int32_t* ids, const
     y[idx] = f32_to_bf16_bits_rn(acc);
 }
 
+// Expert-gathered NVFP4 GEMV: the tcgen05 kernel, else the mma.sync one.
+qg_status grouped_nvfp4(const uint8_t* codes, const uint8_t* scales, int total_rows, int K, int swiglu, int up_offset,
+                        const void* x, int max_cols, void* y, int out_pitch, int out_f32, const GroupDesc* groups,
+                        const UnitDesc* units, const int* n_units, const float* gscales, int rows_per_unit,
+                        cudaStream_t stream)
+{
+    const qg_status s = launch_tc_grouped_nvfp4(codes, scales, total_rows, K, swiglu, up_offset, x, max_cols, y,
+                                                out_pitch, out_f32, groups, units, n_units, gscales, rows_per_unit,
+                                                stream);
+    if (s != QG_ERR_UNSUPPORTED) return s;
+    return launch_grouped_nvfp4(codes, scales, total_rows, K, swiglu, up_offset, x, max_cols, y, out_pitch, out_f32,
+                                groups, units, n_units, gscales, rows_per_unit, stream);
+}
+
 }  // namespace
 
 size_t moe_workspace_bytes(int M, int topk, int H, int I, int E)
@@ -266,10 +280,10 @@ qg_status launch_moe(const uint8_t* gu_codes, const uint8_t* gu_scales, const fl
     moe_group_kernel<<<1, 256, 0, stream>>>(ids, M, topk, E, I, H, L.r_gu, L.r_dn, g_gu, g_dn, u_gu, u_dn, ctrl,
                                             status);
     if (cudaPeekAtLastError() != cudaSuccess) return QG_ERR_CUDA;
-    qg_status s = launch_grouped_nvfp4(gu_codes, gu_scales, E * 2 * I, H, 1, I, x, M, h, I, 0, g_gu, u_gu, ctrl + 0,
+    qg_status s = grouped_nvfp4(gu_codes, gu_scales, E * 2 * I, H, 1, I, x, M, h, I, 0, g_gu, u_gu, ctrl + 0,
                                        gu_g, L.r_gu, stream);
     if (s != QG_OK) return s;
-    s = launch_grouped_nvfp4(dn_codes, dn_scales, E * H, I, 0, 0, h, 8, yslot, H, 1, g_dn, u_dn, ctrl + 1, dn_g,
+    s = grouped_nvfp4(dn_codes, dn_scales, E * H, I, 0, 0, h, 8, yslot, H, 1, g_dn, u_dn, ctrl + 1, dn_g,
                              L.r_dn, stream);
     if (s != QG_OK) return s;
     const int n = M * H;

@@ -46,29 +46,6 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr)
                  : "r"(addr));
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr)
-{
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ uint2 lds64(uint32_t addr)
-{
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-    return v;
-}
-
 __device__ __forceinline__ uint32_t lds8(uint32_t addr)
 {
     uint32_t v;
@@ -76,29 +53,8 @@ __device__ __forceinline__ uint32_t lds8(uint32_t addr)
     return v;
 }
 
-__device__ __forceinline__ uint4 ldg_nc_128(const void* p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ uint32_t bcast_lo(uint32_t h2) { return __byte_perm(h2, 0, 0x1010); }
 __device__ __forceinline__ uint32_t bcast_hi(uint32_t h2) { return __byte_perm(h2, 0, 0x3232); }
-
-// Power-of-two prescale exponent p for a chunk whose largest finite |x| has
-// bf16 magnitude bits `mag` (0 if every value is zero): max * 2^p in [2^14, 2^15).
-__device__ __forceinline__ int prescale_exponent(uint32_t mag)
-{
-    if (mag == 0) return 0;
-    uint32_t e = mag >> 7;
-    if (e > 0) return 141 - static_cast<int>(e);
-    // subnormal bf16: value = mag * 2^-133
-    int lg = 31 - __clz(static_cast<int>(mag));
-    return 147 - lg;
-}
 
 // Pack 8 16-bit values in the format's pair order: natural k order for
 // NVFP4 ({k, k+1} pairs, matching the e2m1x2 decode), {k, k+4} pairs for Q
@@ -118,16 +74,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Exact f16x2 -> bf16x2 for values with at most 8 significant bits in the
-// bf16 normal range (the decoded weights): through fp32, both steps exact.
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h2)
-{
-    const float lo = half_bits_to_f32(h2 & 0xFFFFu), hi = half_bits_to_f32(h2 >> 16);
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
 }
 
 __device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b)

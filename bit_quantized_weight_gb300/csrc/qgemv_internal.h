@@ -97,6 +97,15 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtyp
 qg_status launch_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
                              int out_f32, const void* residual, int M, int N, int K, int swiglu,
                              cudaStream_t stream);
+// tcgen05 kernels (NVFP4): QG_ERR_UNSUPPORTED when a shape does not fit their
+// shared-memory plan; the callers then use the mma.sync kernels above.
+qg_status launch_tc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
+                                int out_f32, const void* residual, int M, int N, int K, int swiglu,
+                                cudaStream_t stream);
+qg_status launch_tc_grouped_nvfp4(const uint8_t* codes, const uint8_t* scales, int total_rows, int K, int swiglu,
+                                  int up_offset, const void* x, int max_cols, void* y, int out_pitch, int out_f32,
+                                  const GroupDesc* groups, const UnitDesc* units, const int* n_units,
+                                  const float* gscales, int rows_per_unit, cudaStream_t stream);
 qg_status launch_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min,
                            int bits, const void* x, void* y, int out_f32, const void* residual, int M,
                            int N, int K, cudaStream_t stream);
