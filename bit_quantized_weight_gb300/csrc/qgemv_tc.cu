@@ -61,16 +61,17 @@ namespace qg {
 
 namespace {
 
-constexpr int kTcDecodeWarps = 8;                   // warps 0-7: quadrant w % 4, parity w / 4
+constexpr int kTcDecodeSets = 4;                    // decode warp sets; set s takes granules g % 4 == s
+constexpr int kTcDecodeWarps = 4 * kTcDecodeSets;   // warps 0-15: quadrant w % 4, set w / 4
 constexpr int kTcDecodeThreads = 32 * kTcDecodeWarps;
-constexpr int kTcFoldWarps = 8;                     // warps 8-15: quadrant w % 4, parity (w - 8) / 4
+constexpr int kTcFoldWarps = 8;                     // warps 16-23: quadrant w % 4, parity (w - 16) / 4
 constexpr int kTcFoldThreads = 32 * kTcFoldWarps;
-constexpr int kTcMmaWarp0 = 16;                     // warps 16, 17: MMA issue, parity w - 16
-constexpr int kTcTmaWarp = 18;
-constexpr int kTcThreads = 32 * 19;
+constexpr int kTcMmaWarp0 = kTcDecodeWarps + kTcFoldWarps;  // warps 24, 25: MMA issue, parity w - 24
+constexpr int kTcTmaWarp = kTcMmaWarp0 + 2;
+constexpr int kTcThreads = 32 * (kTcTmaWarp + 1);
 constexpr int kTcMaxStages = 24;
 constexpr int kTcCols = 512;                        // TMEM columns allocated (all of them)
-constexpr int kTcMaxBufs = 8;                       // TMEM buffers in rotation
+constexpr int kTcMaxBufs = 4;                       // TMEM buffers in rotation, one per decode set
 constexpr int kTcGran = 2;                          // 128-k granules per 256-k stage
 constexpr uint32_t kTcZeroPad = 256;                // zero bytes before and after the one-token B layout
 constexpr uint32_t kTcSmemMax = 227u * 1024u;
@@ -127,13 +128,12 @@ struct TcCfg {
     static constexpr int ACOLS = 64;                   // A columns per granule
     static constexpr int DREG = DEF ? 2 : 1;           // D regions per granule
     static constexpr int BUFC = ACOLS + DREG * N;      // TMEM columns per buffer
-    // An even number of buffers, so that buffer b only ever holds granules of
-    // parity b % 2: each mbarrier of a buffer then has one waiting warp per
-    // role, which consumes its phases in order (a parity wait for phase k is
-    // only sound once phase k - 1 has completed).
-    static constexpr int NB = ((kTcCols / BUFC) < kTcMaxBufs ? (kTcCols / BUFC) : kTcMaxBufs) & ~1;
-    static constexpr int NACC = DEF ? 4 : MT;          // fp32 accumulators per lane
-    static_assert(NB >= 2 && NB % 2 == 0, "an even number of TMEM buffers");
+    // One buffer per decode set: buffer b = granule % 4 then always belongs to
+    // the same decode set, fold parity and MMA warp, so each mbarrier of a
+    // buffer has one waiting warp per role, which consumes its phases in order
+    // (a parity wait for phase k is only sound once phase k - 1 has completed).
+    static constexpr int NB = kTcMaxBufs;
+    static_assert(NB * BUFC <= kTcCols && NB % kTcDecodeSets == 0, "buffers per decode set");
     static_assert(kTcGran == 2, "granule parity = granule index within the stage");
     static_assert(kTcGran * STEPS * 16 == kChunkK, "granules tile a stage");
 };
@@ -240,16 +240,19 @@ __device__ __forceinline__ uint32_t z_off_one(int cr, int lane8, int p)
 
 // ---------------------------------------------------------------- activations
 // Converts stages [c0, c0 + nst) of every phase for the current group into the
-// B layout: pass 1 finds each (stage, phase, token) chunk's prescale exponent
-// and whether f16 holds it exactly (and clears the one-token layout); pass 2
-// writes f16 (or, for a stage with an inexact chunk, the raw bf16 of every
-// chunk of that stage) and the fp32 factors 2^-exponent. Run by the decode
-// warps.
+// B layout, run by the decode warps. One pass over x: each warp puts several
+// chunks' loads in flight, then per (stage, phase, token) chunk finds the
+// prescale exponent and whether f16 holds the chunk exactly, and stores the
+// raw bf16 in the chunk's B slot. A second pass, in shared memory, turns each
+// chunk into f16 under its prescale -- or keeps the raw bf16 for every chunk
+// of a stage that has an inexact chunk -- and writes the fp32 factors
+// 2^-exponent.
 template <int MT>
 __device__ void tc_convert(const TcArgs& a, uint8_t* smem, int c0, int nst, int ntok, const int* xrow, int warp,
                            int lane)
 {
     constexpr bool DEF = (MT == 1);
+    constexpr int kBatch = 4;  // chunks whose loads are in flight together, per warp
     int* ex = reinterpret_cast<int*>(smem + a.smem_ex);
     uint8_t* fl = smem + a.smem_fl;
     int* fs = reinterpret_cast<int*>(smem + a.smem_fs);
@@ -257,112 +260,127 @@ __device__ void tc_convert(const TcArgs& a, uint8_t* smem, int c0, int nst, int 
     const uint32_t zb = smem_u32(smem + a.smem_z);
     const int PM = a.P * MT;
     const int items = nst * PM;
+    // chunk `it` = (stage cr, phase p, token m); this lane's 8 k of it
+    auto slot_of = [&](int it) -> uint32_t {
+        const int m = it % MT;
+        const int t = it / MT;
+        const int pp = t % a.P;
+        const int cr = t / a.P;
+        return DEF ? zb + z_off_one(cr, lane, pp) : zb + z_row_multi(cr, lane, PM, pp * MT + m) * 16u;
+    };
 
-    // factors of phases beyond P (one-token layout) stay zero
+    // factors of phases beyond P (one-token layout) stay zero, as do the
+    // one-token layout's padding rows
     for (int i = threadIdx.x; i < nst * a.PES; i += kTcDecodeThreads) pe[i] = 0.f;
-    if (DEF)
+    if (DEF) {
         for (uint32_t o = threadIdx.x * 16u; o < a.z_bytes; o += kTcDecodeThreads * 16u)
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(zb + o), "r"(0u) : "memory");
-    for (int pass = 0; pass < 2; ++pass) {
-        for (int it = warp; it < items; it += kTcDecodeWarps) {
-            const int m = it % MT;
-            const int t = it / MT;
-            const int p = t % a.P;
-            const int cr = t / a.P;
-            const int kc = p * a.Cp + c0 + cr;
-            uint4 raw = make_uint4(0, 0, 0, 0);
-            if (m < ntok && kc < a.C) {
-                const int xr = xrow ? xrow[m] : m;
-                raw = ldg_nc_128(a.x + static_cast<size_t>(xr) * a.K + static_cast<size_t>(kc) * kChunkK + lane * 8);
-            }
-            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-            uint32_t hb[8];
+        named_barrier_sync(1, kTcDecodeThreads);
+    }
+    for (int base = warp; base < items; base += kTcDecodeWarps * kBatch) {
+        uint4 raw[kBatch];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) hb[i] = (i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu);
-            if (pass == 0) {
-                uint32_t mag = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t mg = hb[i] & 0x7FFFu;
-                    if (mg < 0x7F80u) mag = max(mag, mg);
-                }
-                mag = __reduce_max_sync(0xffffffffu, mag);
-                // At most 126 so that 2^-e is a normal float; a chunk that
-                // would need more is flagged by the exactness test below.
-                const int e = min(prescale_exponent(mag), 126);
-                bool exact = true;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float v = ldexp_exact(bf16_bits_to_f32(hb[i]), e);
-                    if (isfinite(v) && __half2float(__float2half_rn(v)) != v) exact = false;
-                }
-                const bool inexact = __any_sync(0xffffffffu, !exact);
-                if (lane == 0) {
-                    ex[it] = e;
-                    fl[it] = inexact ? 1 : 0;
-                }
-            } else {
-                const bool stage_bf = __any_sync(0xffffffffu, lane < PM && fl[cr * PM + lane] != 0);
-                const int e = stage_bf ? 0 : ex[it];
-                uint32_t o[4];
-                if (stage_bf) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) o[i] = wv[i];
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float lo = ldexp_exact(bf16_bits_to_f32(hb[2 * i]), e);
-                        const float hi = ldexp_exact(bf16_bits_to_f32(hb[2 * i + 1]), e);
-                        o[i] = pack_f16x2(lo, hi);
-                    }
-                }
-                const uint32_t addr =
-                    DEF ? zb + z_off_one(cr, lane, p) : zb + z_row_multi(cr, lane, PM, p * MT + m) * 16u;
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o[0]), "r"(o[1]), "r"(o[2]),
-                             "r"(o[3])
-                             : "memory");
-                if (lane == 0) {
-                    pe[cr * a.PES + p * MT + m] = __int_as_float((127 - e) << 23);
-                    if (p == 0 && m == 0) fs[cr] = stage_bf ? 1 : 0;
+        for (int u = 0; u < kBatch; ++u) {
+            const int it = base + u * kTcDecodeWarps;
+            raw[u] = make_uint4(0, 0, 0, 0);
+            if (it < items) {
+                const int m = it % MT;
+                const int t = it / MT;
+                const int kc = (t % a.P) * a.Cp + c0 + t / a.P;
+                if (m < ntok && kc < a.C) {
+                    const int xr = xrow ? xrow[m] : m;
+                    raw[u] = ldg_nc_128(a.x + static_cast<size_t>(xr) * a.K + static_cast<size_t>(kc) * kChunkK +
+                                        lane * 8);
                 }
             }
         }
-        named_barrier_sync(1, kTcDecodeThreads);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int it = base + u * kTcDecodeWarps;
+            if (it >= items) break;
+            const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+            uint32_t mag = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t mg = ((i & 1) ? (wv[i >> 1] >> 16) : wv[i >> 1]) & 0x7FFFu;
+                if (mg < 0x7F80u) mag = max(mag, mg);
+            }
+            mag = __reduce_max_sync(0xffffffffu, mag);
+            // At most 126 so that 2^-e is a normal float; a chunk that would
+            // need more is flagged by the exactness test below.
+            const int e = min(prescale_exponent(mag), 126);
+            bool exact = true;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float v = ldexp_exact(bf16_bits_to_f32((i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu)), e);
+                if (isfinite(v) && __half2float(__float2half_rn(v)) != v) exact = false;
+            }
+            const bool inexact = __any_sync(0xffffffffu, !exact);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(slot_of(it)), "r"(wv[0]), "r"(wv[1]),
+                         "r"(wv[2]), "r"(wv[3])
+                         : "memory");
+            if (lane == 0) {
+                ex[it] = e;
+                fl[it] = inexact ? 1 : 0;
+            }
+        }
+    }
+    named_barrier_sync(1, kTcDecodeThreads);
+    for (int it = warp; it < items; it += kTcDecodeWarps) {
+        const int m = it % MT;
+        const int t = it / MT;
+        const int pp = t % a.P;
+        const int cr = t / a.P;
+        const bool stage_bf = __any_sync(0xffffffffu, lane < PM && fl[cr * PM + lane] != 0);
+        const int e = stage_bf ? 0 : ex[it];
+        if (!stage_bf) {
+            const uint32_t addr = slot_of(it);
+            const uint4 v = lds128(addr);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float lo = ldexp_exact(bf16_bits_to_f32(wv[i] & 0xFFFFu), e);
+                const float hi = ldexp_exact(bf16_bits_to_f32(wv[i] >> 16), e);
+                o[i] = pack_f16x2(lo, hi);
+            }
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o[0]), "r"(o[1]), "r"(o[2]),
+                         "r"(o[3])
+                         : "memory");
+        }
+        if (lane == 0) {
+            pe[cr * a.PES + pp * MT + m] = __int_as_float((127 - e) << 23);
+            if (pp == 0 && m == 0) fs[cr] = stage_bf ? 1 : 0;
+        }
     }
     fence_proxy_async_smem();
     named_barrier_sync(1, kTcDecodeThreads);
 }
 
 // ---------------------------------------------------------------- decode
-// One 128-k granule of this lane's row: codes as f16 (or bf16) into TMEM,
+// One 128-k granule of this lane's row: codes as f16 (BF: bf16) into TMEM,
 // multiplied by their block scales unless those come after the MMA.
-template <int MT, int EPI>
-__device__ __forceinline__ void tc_decode(const TcArgs& a, uint32_t stage, int gran, int r, int bx, bool live, bool bf,
+template <int MT, int EPI, bool BF>
+__device__ __forceinline__ void tc_decode(const TcArgs& a, uint32_t stage, int gran, int r, int bx, bool live,
                                           uint32_t taddr)
 {
     using Cfg = TcCfg<MT, EPI>;
     const uint32_t row = stage + static_cast<uint32_t>(bx * a.R8 + r) * 128u;
-    uint32_t sw[2] = {0u, 0u};
-    uint4 w[4];
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) w[cc] = make_uint4(0, 0, 0, 0);
-    if (live) {
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-            w[cc] = lds128(row + ((static_cast<uint32_t>(4 * gran + cc) ^ static_cast<uint32_t>(r & 7)) << 4));
-        if (!Cfg::DEF) {
-            const uint2 s = lds64(stage + a.scales_off + static_cast<uint32_t>(bx * a.R8 + r) * 16u + 8 * gran);
-            sw[0] = s.x;
-            sw[1] = s.y;
-        }
-    }
+    uint2 sw = make_uint2(0u, 0u);
+    if (live && !Cfg::DEF) sw = lds64(stage + a.scales_off + static_cast<uint32_t>(bx * a.R8 + r) * 16u + 8 * gran);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
+        uint4 w[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (live) {
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2)
+                w[c2] = lds128(row + ((static_cast<uint32_t>(4 * gran + 2 * half + c2) ^ static_cast<uint32_t>(r & 7))
+                                      << 4));
+        }
         uint32_t av[32];
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
-            const int cc = 2 * half + c2;
-            const uint32_t ws[4] = {w[cc].x, w[cc].y, w[cc].z, w[cc].w};
+            const uint32_t ws[4] = {w[c2].x, w[c2].y, w[c2].z, w[c2].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t o[4];
@@ -371,12 +389,12 @@ __device__ __forceinline__ void tc_decode(const TcArgs& a, uint32_t stage, int g
                     // block 2 c2 + q / 2 of this half: its E4M3 byte
                     // duplicated, then converted, is the scale in both halves
                     const uint32_t blk = static_cast<uint32_t>(2 * c2 + (q >> 1));
-                    const uint32_t s2 = e4m3x2_to_f16x2(__byte_perm(sw[half], 0, blk * 0x11u));
+                    const uint32_t s2 = e4m3x2_to_f16x2(__byte_perm(half ? sw.y : sw.x, 0, blk * 0x11u));
 #pragma unroll
                     for (int i = 0; i < 4; ++i) o[i] = hmul2(o[i], s2);
                 }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) av[c2 * 16 + q * 4 + i] = bf ? f16x2_to_bf16x2(o[i]) : o[i];
+                for (int i = 0; i < 4; ++i) av[c2 * 16 + q * 4 + i] = BF ? f16x2_to_bf16x2(o[i]) : o[i];
             }
         }
         tc_st_x32(taddr + 32u * half, av);
@@ -396,7 +414,8 @@ __device__ __forceinline__ float tc_pick(const uint32_t* v, int p, int m)
     return r;
 }
 
-template <int MT, int EPI>
+// NPC: one-token phase columns the fold accumulates (1, 2 or 4 >= P).
+template <int MT, int EPI, int NPC>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemv_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales)
@@ -584,7 +603,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else if (warp < kTcDecodeWarps) {
         // ------------------------------------------------------------ decode warps
-        const int par = warp >> 2;
+        const int dset = warp >> 2;
         // Activations may come from the previous kernel.
         asm volatile("griddepcontrol.wait;" ::: "memory");
         bool aborted = false;
@@ -619,13 +638,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     conv_c0 = c;
                     conv_key = xkey;
                 }
-                if (!aborted && !tc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
+                // this set's granule of the stage, if any
+                const bool mine = ((gi & 3) == dset) || (((gi + 1) & 3) == dset);
+                if (mine && !aborted && !tc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
                 const bool bf = fs[cr] != 0;
                 const bool live = valid && (p * a.Cp + c < a.C);
                 const uint32_t stage = ring + slot * a.stage_bytes;
-#pragma unroll
+#pragma unroll 1
                 for (int gr = 0; gr < kTcGran; ++gr, ++gi) {
-                    if ((gi & 1) != par || aborted) continue;
+                    if ((gi & 3) != dset || aborted) continue;
                     const int b = gi % NB;
                     // Buffer b is free once its previous use was read back.
                     if (gi >= NB && !tc_wait_warp(&d_free[b], ((gi / NB) - 1) & 1, a, abort_flag)) {
@@ -633,7 +654,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         continue;
                     }
                     tc_fence_after();
-                    tc_decode<MT, EPI>(a, stage, gr, r, bx, live, bf, tl + static_cast<uint32_t>(b * Cfg::BUFC));
+                    const uint32_t ta = tl + static_cast<uint32_t>(b * Cfg::BUFC);
+                    if (bf)
+                        tc_decode<MT, EPI, true>(a, stage, gr, r, bx, live, ta);
+                    else
+                        tc_decode<MT, EPI, false>(a, stage, gr, r, bx, live, ta);
                     tc_wait_st();
                     tc_fence_before();
                     __syncwarp();
@@ -664,15 +689,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ntok = a.groups[un.grp].ntok;
                 gsc = a.gscales[a.groups[un.grp].e];
             }
-            float acc[Cfg::NACC];
+            constexpr int NACC = Cfg::DEF ? NPC : MT;
+            float acc[NACC];
 #pragma unroll
-            for (int n = 0; n < Cfg::NACC; ++n) acc[n] = 0.f;
+            for (int n = 0; n < NACC; ++n) acc[n] = 0.f;
             int cr = 0;
             for (int c = 0; c < a.Cp; ++c) {
                 const uint32_t stage = ring + slot * a.stage_bytes;
                 const bool live = valid && (p * a.Cp + c < a.C);
                 const float* pe_stage = pe_all + cr * a.PES;
-#pragma unroll
+#pragma unroll 1
                 for (int gr = 0; gr < kTcGran; ++gr, ++gi) {
                     if ((gi & 1) != par || aborted) continue;
                     const int b = gi % NB;
@@ -693,7 +719,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&d_free[b]);
-                        float part[4] = {0.f, 0.f, 0.f, 0.f};
+                        float part[NPC];
+#pragma unroll
+                        for (int n = 0; n < NPC; ++n) part[n] = 0.f;
 #pragma unroll
                         for (int rg = 0; rg < 2; ++rg) {
                             const uint32_t s_lo = e4m3x2_to_f16x2((rg ? sw.y : sw.x) & 0xFFFFu);
@@ -703,12 +731,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                             for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
-                                for (int n = 0; n < 4; ++n)
+                                for (int n = 0; n < NPC; ++n)
                                     part[n] = fmaf(__uint_as_float(tc_after_wait(v[rg][4 * jj + n])), sc[jj], part[n]);
                         }
                         const float fe[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-                        for (int n = 0; n < 4; ++n) acc[n] = fmaf(part[n], fe[n], acc[n]);
+                        for (int n = 0; n < NPC; ++n) acc[n] = fmaf(part[n], fe[n], acc[n]);
                     } else {
                         uint32_t v[Cfg::W];
                         tc_ld<Cfg::W>(tb + Cfg::ACOLS, v);
@@ -735,8 +763,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (valid) {
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
-                    float v = acc[m];
-                    if constexpr (Cfg::DEF) v = p == 1 ? acc[1] : p == 2 ? acc[2] : p == 3 ? acc[3] : acc[0];
+                    float v = acc[Cfg::DEF ? 0 : m];
+                    if constexpr (Cfg::DEF) {
+#pragma unroll
+                        for (int n = 1; n < NPC; ++n)
+                            if (p == n) v = acc[n];
+                    }
                     red[(((par * a.P + p) * NGU + gu) * a.R + r) * MT + m] = v;
                 }
             }
@@ -805,7 +837,7 @@ ZPlan z_plan(int sc, int P, int MT, int N, int PES)
 
 // Completes the launch-time fields of `a` (status word, debug limits, stage
 // and shared-memory plan) and launches with programmatic dependent launch.
-template <int MT, int EPI>
+template <int MT, int EPI, int NPC>
 qg_status tc_launch(TcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, int grid, cudaStream_t stream)
 {
     using Cfg = TcCfg<MT, EPI>;
@@ -838,6 +870,11 @@ qg_status tc_launch(TcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
     if (fixed + 2 * a.stage_bytes > kTcSmemMax) return QG_ERR_UNSUPPORTED;
     int n_stages = static_cast<int>((kTcSmemMax - fixed) / a.stage_bytes);
     n_stages = std::min(n_stages, kTcMaxStages);
+    // An even ring: slot c % n_stages then always holds stages of the same
+    // parity, i.e. the same pair of decode sets waits on each slot's barrier,
+    // every phase in order.
+    n_stages &= ~1;
+    if (n_stages < 2) return QG_ERR_UNSUPPORTED;
     a.n_stages = n_stages;
 
     uint32_t so = 0;
@@ -860,7 +897,7 @@ qg_status tc_launch(TcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
     so = std::max(so, kTcSmemMin);
     if (so > kTcSmemMax) return QG_ERR_UNSUPPORTED;
 
-    auto kern = tc_gemv_kernel<MT, EPI>;
+    auto kern = tc_gemv_kernel<MT, EPI, NPC>;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
@@ -887,10 +924,14 @@ template <int EPI>
 qg_status tc_dispatch_mt(const TcArgs& a, const CUtensorMap& tmc, const CUtensorMap& tms, int grid,
                          cudaStream_t stream)
 {
-    if (a.M <= 1) return tc_launch<1, EPI>(a, tmc, tms, grid, stream);
-    if (a.M <= 2) return tc_launch<2, EPI>(a, tmc, tms, grid, stream);
-    if (a.M <= 4) return tc_launch<4, EPI>(a, tmc, tms, grid, stream);
-    return tc_launch<8, EPI>(a, tmc, tms, grid, stream);
+    if (a.M <= 1) {
+        if (a.P <= 1) return tc_launch<1, EPI, 1>(a, tmc, tms, grid, stream);
+        if (a.P <= 2) return tc_launch<1, EPI, 2>(a, tmc, tms, grid, stream);
+        return tc_launch<1, EPI, 4>(a, tmc, tms, grid, stream);
+    }
+    if (a.M <= 2) return tc_launch<2, EPI, 4>(a, tmc, tms, grid, stream);
+    if (a.M <= 4) return tc_launch<4, EPI, 4>(a, tmc, tms, grid, stream);
+    return tc_launch<8, EPI, 4>(a, tmc, tms, grid, stream);
 }
 
 // K phases for units of R rows: as many as the 128 TMEM lanes hold, at most
