@@ -64,10 +64,10 @@ namespace {
 constexpr int kTcDecodeSets = 4;                    // decode warp sets; set s takes granules g % 4 == s
 constexpr int kTcDecodeWarps = 4 * kTcDecodeSets;   // warps 0-15: quadrant w % 4, set w / 4
 constexpr int kTcDecodeThreads = 32 * kTcDecodeWarps;
-constexpr int kTcFoldWarps = 8;                     // warps 16-23: quadrant w % 4, parity (w - 16) / 4
+constexpr int kTcFoldWarps = 4;                     // warps 16-19: quadrant w % 4, every granule
 constexpr int kTcFoldThreads = 32 * kTcFoldWarps;
-constexpr int kTcMmaWarp0 = kTcDecodeWarps + kTcFoldWarps;  // warps 24, 25: MMA issue, parity w - 24
-constexpr int kTcTmaWarp = kTcMmaWarp0 + 2;
+constexpr int kTcMmaWarp0 = kTcDecodeWarps + kTcFoldWarps;  // warps 20-23: MMA issue for decode set w - 20
+constexpr int kTcTmaWarp = kTcMmaWarp0 + kTcDecodeSets;
 constexpr int kTcThreads = 32 * (kTcTmaWarp + 1);
 constexpr int kTcMaxStages = 24;
 constexpr int kTcCols = 512;                        // TMEM columns allocated (all of them)
@@ -240,20 +240,25 @@ __device__ __forceinline__ uint32_t z_off_one(int cr, int lane8, int p)
 
 // ---------------------------------------------------------------- activations
 // Converts stages [c0, c0 + nst) of every phase for the current group into the
-// B layout, run by the decode warps. One pass over x: each warp puts several
-// chunks' loads in flight, then per (stage, phase, token) chunk finds the
-// prescale exponent and whether f16 holds the chunk exactly, and stores the
-// raw bf16 in the chunk's B slot. A second pass, in shared memory, turns each
-// chunk into f16 under its prescale -- or keeps the raw bf16 for every chunk
-// of a stage that has an inexact chunk -- and writes the fp32 factors
-// 2^-exponent.
+// B layout, run by the decode warps. Per (stage, phase, token) chunk of 256
+// activations one warp (8 per lane, loads of several chunks in flight):
+//   * reduces the largest and the smallest nonzero bf16 exponent field over
+//     the chunk (finite values only); the prescale exponent e puts the
+//     largest magnitude in [2^14, 2^15) (at most 126, so 2^-e stays normal);
+//   * the chunk is exact in f16 under 2^e if its smallest nonzero value keeps
+//     all 8 significant bits at or above 2^-24, i.e. scaled exponent >= -17
+//     (a sufficient test; a chunk failing it is flagged);
+//   * writes v * 2^e as f16 (an exact multiply, then an exact conversion)
+//     and the factor 2^-e.
+// If any chunk was flagged, a second pass rewrites every chunk of the stages
+// that hold one as raw bf16 with factor 1 and marks those stages bf16.
 template <int MT>
 __device__ void tc_convert(const TcArgs& a, uint8_t* smem, int c0, int nst, int ntok, const int* xrow, int warp,
                            int lane)
 {
     constexpr bool DEF = (MT == 1);
     constexpr int kBatch = 4;  // chunks whose loads are in flight together, per warp
-    int* ex = reinterpret_cast<int*>(smem + a.smem_ex);
+    int* any_flag = reinterpret_cast<int*>(smem + a.smem_ex);
     uint8_t* fl = smem + a.smem_fl;
     int* fs = reinterpret_cast<int*>(smem + a.smem_fs);
     float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
@@ -268,90 +273,93 @@ __device__ void tc_convert(const TcArgs& a, uint8_t* smem, int c0, int nst, int 
         const int cr = t / a.P;
         return DEF ? zb + z_off_one(cr, lane, pp) : zb + z_row_multi(cr, lane, PM, pp * MT + m) * 16u;
     };
+    auto load = [&](int it) -> uint4 {
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (it < items) {
+            const int m = it % MT;
+            const int t = it / MT;
+            const int kc = (t % a.P) * a.Cp + c0 + t / a.P;
+            if (m < ntok && kc < a.C) {
+                const int xr = xrow ? xrow[m] : m;
+                raw = ldg_nc_128(a.x + static_cast<size_t>(xr) * a.K + static_cast<size_t>(kc) * kChunkK + lane * 8);
+            }
+        }
+        return raw;
+    };
 
     // factors of phases beyond P (one-token layout) stay zero, as do the
-    // one-token layout's padding rows
+    // one-token layout's padding rows; stages are f16 unless flagged
     for (int i = threadIdx.x; i < nst * a.PES; i += kTcDecodeThreads) pe[i] = 0.f;
-    if (DEF) {
+    for (int i = threadIdx.x; i < nst; i += kTcDecodeThreads) fs[i] = 0;
+    if (threadIdx.x == 0) *any_flag = 0;
+    if (DEF)
         for (uint32_t o = threadIdx.x * 16u; o < a.z_bytes; o += kTcDecodeThreads * 16u)
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(zb + o), "r"(0u) : "memory");
-        named_barrier_sync(1, kTcDecodeThreads);
-    }
+    named_barrier_sync(1, kTcDecodeThreads);
+
+    bool flagged = false;
     for (int base = warp; base < items; base += kTcDecodeWarps * kBatch) {
         uint4 raw[kBatch];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int it = base + u * kTcDecodeWarps;
-            raw[u] = make_uint4(0, 0, 0, 0);
-            if (it < items) {
-                const int m = it % MT;
-                const int t = it / MT;
-                const int kc = (t % a.P) * a.Cp + c0 + t / a.P;
-                if (m < ntok && kc < a.C) {
-                    const int xr = xrow ? xrow[m] : m;
-                    raw[u] = ldg_nc_128(a.x + static_cast<size_t>(xr) * a.K + static_cast<size_t>(kc) * kChunkK +
-                                        lane * 8);
-                }
-            }
-        }
+        for (int u = 0; u < kBatch; ++u) raw[u] = load(base + u * kTcDecodeWarps);
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int it = base + u * kTcDecodeWarps;
             if (it >= items) break;
             const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-            uint32_t mag = 0;
+            uint32_t emax = 0, emin = 255, magmax = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const uint32_t mg = ((i & 1) ? (wv[i >> 1] >> 16) : wv[i >> 1]) & 0x7FFFu;
-                if (mg < 0x7F80u) mag = max(mag, mg);
+                const uint32_t ef = mg >> 7;
+                if (ef != 255u) {
+                    emax = max(emax, ef);
+                    magmax = max(magmax, mg);
+                    if (mg != 0u) emin = min(emin, ef);
+                }
             }
-            mag = __reduce_max_sync(0xffffffffu, mag);
-            // At most 126 so that 2^-e is a normal float; a chunk that would
-            // need more is flagged by the exactness test below.
-            const int e = min(prescale_exponent(mag), 126);
-            bool exact = true;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float v = ldexp_exact(bf16_bits_to_f32((i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu)), e);
-                if (isfinite(v) && __half2float(__float2half_rn(v)) != v) exact = false;
-            }
-            const bool inexact = __any_sync(0xffffffffu, !exact);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(slot_of(it)), "r"(wv[0]), "r"(wv[1]),
-                         "r"(wv[2]), "r"(wv[3])
-                         : "memory");
-            if (lane == 0) {
-                ex[it] = e;
-                fl[it] = inexact ? 1 : 0;
-            }
-        }
-    }
-    named_barrier_sync(1, kTcDecodeThreads);
-    for (int it = warp; it < items; it += kTcDecodeWarps) {
-        const int m = it % MT;
-        const int t = it / MT;
-        const int pp = t % a.P;
-        const int cr = t / a.P;
-        const bool stage_bf = __any_sync(0xffffffffu, lane < PM && fl[cr * PM + lane] != 0);
-        const int e = stage_bf ? 0 : ex[it];
-        if (!stage_bf) {
-            const uint32_t addr = slot_of(it);
-            const uint4 v = lds128(addr);
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            emax = __reduce_max_sync(0xffffffffu, emax);
+            emin = __reduce_min_sync(0xffffffffu, emin);
+            // a subnormal largest value needs its full magnitude (rare)
+            if (emax == 0u) magmax = __reduce_max_sync(0xffffffffu, magmax);
+            const int e = min(emax != 0u ? 141 - static_cast<int>(emax) : prescale_exponent(magmax), 126);
+            const bool inexact = emin != 255u && static_cast<int>(emin) - 127 + e < -17;
+            const float sc = __int_as_float((127 + e) << 23);
             uint32_t o[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float lo = ldexp_exact(bf16_bits_to_f32(wv[i] & 0xFFFFu), e);
-                const float hi = ldexp_exact(bf16_bits_to_f32(wv[i] >> 16), e);
-                o[i] = pack_f16x2(lo, hi);
-            }
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o[0]), "r"(o[1]), "r"(o[2]),
-                         "r"(o[3])
+            for (int i = 0; i < 4; ++i)
+                o[i] = pack_f16x2(__uint_as_float(wv[i] << 16) * sc, __uint_as_float(wv[i] & 0xFFFF0000u) * sc);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(slot_of(it)), "r"(o[0]), "r"(o[1]),
+                         "r"(o[2]), "r"(o[3])
                          : "memory");
+            if (lane == 0) {
+                const int m = it % MT;
+                const int t = it / MT;
+                pe[(t / a.P) * a.PES + (t % a.P) * MT + m] = __int_as_float((127 - e) << 23);
+                fl[it] = inexact ? 1 : 0;
+            }
+            flagged |= inexact;
         }
-        if (lane == 0) {
-            pe[cr * a.PES + pp * MT + m] = __int_as_float((127 - e) << 23);
-            if (pp == 0 && m == 0) fs[cr] = stage_bf ? 1 : 0;
+    }
+    if (flagged && lane == 0) *any_flag = 1;
+    named_barrier_sync(1, kTcDecodeThreads);
+    if (*any_flag != 0) {
+        // Rare: stages holding a chunk that f16 cannot carry run in bf16.
+        for (int it = warp; it < items; it += kTcDecodeWarps) {
+            const int t = it / MT;
+            const int cr = t / a.P;
+            const bool stage_bf = __any_sync(0xffffffffu, lane < PM && fl[cr * PM + lane] != 0);
+            if (!stage_bf) continue;
+            const uint4 raw = load(it);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(slot_of(it)), "r"(raw.x), "r"(raw.y),
+                         "r"(raw.z), "r"(raw.w)
+                         : "memory");
+            if (lane == 0) {
+                pe[cr * a.PES + (t % a.P) * MT + it % MT] = 1.0f;
+                if (it % PM == 0) fs[cr] = 1;
+            }
         }
+        named_barrier_sync(1, kTcDecodeThreads);
     }
     fence_proxy_async_smem();
     named_barrier_sync(1, kTcDecodeThreads);
@@ -444,7 +452,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.n_stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kTcFoldWarps);
+            mbar_init(&empty[s], kTcFoldWarps * kTcGran);
         }
         for (int b = 0; b < NB; ++b) {
             mbar_init(&a_ready[b], 4);
@@ -539,9 +547,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else if (warp >= kTcMmaWarp0) {
         // ------------------------------------------------------------ MMA issue
-        // The whole warp runs the loop, so descriptors and TMEM addresses are
-        // warp-uniform; one elected lane issues the MMAs and the commit.
-        const int par = warp - kTcMmaWarp0;
+        // One MMA warp per decode set (on its own sub-partition), so each
+        // issues one granule every two stages. The whole warp runs the loop,
+        // so descriptors and TMEM addresses are warp-uniform; one elected
+        // lane issues the MMAs and the commit.
+        const int mset = warp - kTcMmaWarp0;
         const uint32_t zb = smem_u32(smem + a.smem_z);
         const int PM = a.P * MT;
         constexpr uint32_t idesc_h = tc_idesc_f16(128, Cfg::N, false);
@@ -552,7 +562,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int cr = 0;
             for (int c = 0; c < a.Cp && !stop; ++c) {
                 for (int gr = 0; gr < kTcGran; ++gr, ++gi) {
-                    if ((gi & 1) != par) continue;
+                    if ((gi & 3) != mset) continue;
                     const int b = gi % NB;
                     // "A written" also means the previous use's D was read back.
                     if (!tc_wait_warp(&a_ready[b], (gi / NB) & 1, a, abort_flag)) {
@@ -597,7 +607,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // last granule's commit arrives after all of them.
         if (lane == 0 && issued > 0) {
             int last = gi - 1;
-            while ((last & 1) != par) --last;
+            while ((last & 3) != mset) --last;
             mbar_wait_bounded(&mma_done[last % NB], (last / NB) & 1, a.wait_ns, a.status);
         }
         __syncwarp();
@@ -673,10 +683,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ fold warps
-        const int par = (warp - kTcDecodeWarps) >> 2;
         float* red = reinterpret_cast<float*>(smem + a.smem_red);
         const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
-        const int ftid = threadIdx.x - kTcDecodeThreads;  // 0 .. 255
+        const int ftid = threadIdx.x - kTcDecodeThreads;  // 0 .. 127
         // Residuals and the output buffer may belong to the previous kernel.
         asm volatile("griddepcontrol.wait;" ::: "memory");
         bool aborted = false;
@@ -700,7 +709,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const float* pe_stage = pe_all + cr * a.PES;
 #pragma unroll 1
                 for (int gr = 0; gr < kTcGran; ++gr, ++gi) {
-                    if ((gi & 1) != par || aborted) continue;
+                    if (aborted) continue;
                     const int b = gi % NB;
                     if (!tc_wait_warp(&mma_done[b], (gi / NB) & 1, a, abort_flag)) {
                         aborted = true;
@@ -769,7 +778,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         for (int n = 1; n < NPC; ++n)
                             if (p == n) v = acc[n];
                     }
-                    red[(((par * a.P + p) * NGU + gu) * a.R + r) * MT + m] = v;
+                    red[((p * NGU + gu) * a.R + r) * MT + m] = v;
                 }
             }
             named_barrier_sync(2, kTcFoldThreads);
@@ -784,9 +793,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int gg = 0; gg < NGU; ++gg) {
                         float s = 0.f;
-                        for (int fp = 0; fp < 2; ++fp)
-                            for (int pp = 0; pp < a.P; ++pp)
-                                s += red[(((fp * a.P + pp) * NGU + gg) * a.R + rr) * MT + m];
+                        for (int pp = 0; pp < a.P; ++pp) s += red[((pp * NGU + gg) * a.R + rr) * MT + m];
                         v[gg] = s * gsc;
                     }
                     float val = v[0];
@@ -855,7 +862,7 @@ qg_status tc_launch(TcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
     a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
     a.PES = Cfg::DEF ? 4 : a.P * MT;
 
-    const uint32_t red_bytes = align_up(2u * nbox * a.R * MT * 4u, 128);
+    const uint32_t red_bytes = align_up(nbox * a.R * MT * 4u, 128);
     const uint32_t bar_bytes = (2 * kTcMaxStages + 3 * kTcMaxBufs) * 8 + 16;
     // Keep at least ~96 KB (or 4 stages) of weights in flight; the
     // activations get the rest, as few super-chunks as possible.
