@@ -298,6 +298,76 @@ __device__ void tc_convert(const TcArgs& a, uint8_t* smem, int c0, int nst, int 
     named_barrier_sync(1, kTcDecodeThreads);
 
     bool flagged = false;
+    if (!DEF && items >= 4 * kTcDecodeWarps) {
+        // Several tokens, many chunks: a warp takes 8 consecutive chunks; lane l holds
+        // chunk l % 8 at k-groups l / 8 + 4 i (i < 8), so each reduction runs
+        // over four lanes and each store instruction writes 8 different
+        // B rows of one k-group -- 8 distinct bank groups.
+        const int cl = lane & 7;
+        const int kq = lane >> 3;
+        for (int g0 = warp * 8; g0 < items; g0 += kTcDecodeWarps * 8) {
+            const int it = g0 + cl;
+            const bool have = it < items;
+            int m = 0, pp = 0, cr = 0, kc = 0;
+            if (have) {
+                m = it % MT;
+                const int t = it / MT;
+                pp = t % a.P;
+                cr = t / a.P;
+                kc = pp * a.Cp + c0 + cr;
+            }
+            const bool src = have && m < ntok && kc < a.C;
+            const uint16_t* xs = a.x;
+            if (src) xs += static_cast<size_t>(xrow ? xrow[m] : m) * a.K + static_cast<size_t>(kc) * kChunkK;
+            uint4 raw[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) raw[i] = src ? ldg_nc_128(xs + (kq + 4 * i) * 8) : make_uint4(0, 0, 0, 0);
+            uint32_t emax = 0, emin = 255, magmax = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const uint32_t mg = ((h & 1) ? (wv[h >> 1] >> 16) : wv[h >> 1]) & 0x7FFFu;
+                    const uint32_t ef = mg >> 7;
+                    if (ef != 255u) {
+                        emax = max(emax, ef);
+                        magmax = max(magmax, mg);
+                        if (mg != 0u) emin = min(emin, ef);
+                    }
+                }
+            }
+#pragma unroll
+            for (int sh = 8; sh <= 16; sh <<= 1) {
+                emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, sh));
+                emin = min(emin, __shfl_xor_sync(0xffffffffu, emin, sh));
+                magmax = max(magmax, __shfl_xor_sync(0xffffffffu, magmax, sh));
+            }
+            const int e = min(emax != 0u ? 141 - static_cast<int>(emax) : prescale_exponent(magmax), 126);
+            const bool inexact = emin != 255u && static_cast<int>(emin) - 127 + e < -17;
+            const float sc = __int_as_float((127 + e) << 23);
+            if (have) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+                        o[w] = pack_f16x2(__uint_as_float(wv[w] << 16) * sc, __uint_as_float(wv[w] & 0xFFFF0000u) * sc);
+                    const uint32_t addr = zb + z_row_multi(cr, kq + 4 * i, PM, pp * MT + m) * 16u;
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o[0]), "r"(o[1]),
+                                 "r"(o[2]), "r"(o[3])
+                                 : "memory");
+                }
+                if (kq == 0) {
+                    pe[cr * a.PES + pp * MT + m] = __int_as_float((127 - e) << 23);
+                    fl[it] = inexact ? 1 : 0;
+                }
+            }
+            flagged |= have && inexact;
+        }
+        flagged = __any_sync(0xffffffffu, flagged);
+    } else {
     for (int base = warp; base < items; base += kTcDecodeWarps * kBatch) {
         uint4 raw[kBatch];
 #pragma unroll
@@ -340,6 +410,7 @@ __device__ void tc_convert(const TcArgs& a, uint8_t* smem, int c0, int nst, int 
             }
             flagged |= inexact;
         }
+    }
     }
     if (flagged && lane == 0) *any_flag = 1;
     named_barrier_sync(1, kTcDecodeThreads);
