@@ -149,15 +149,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def kernel_source_hash():
+# Kernel sources behind each workload's launches (NVFP4: the tcgen05 kernel;
+# Q4/Q5: the mma.sync kernel); a committed traffic figure is used only while
+# these files are unchanged.
+KERNEL_SOURCES = {
+    "nvfp4": ("qgemv_tc.cu", "tcgen05.cuh", "common.cuh", "qgemv_internal.h"),
+    "q45": ("qgemv_dense.cu", "common.cuh", "qgemv_internal.h"),
+    "moe": ("qgemv_tc.cu", "moe.cu", "tcgen05.cuh", "common.cuh", "qgemv_internal.h"),
+}
+
+
+def kernel_source_hash(family):
     h = hashlib.sha256()
-    for f in ("qgemv_dense.cu", "common.cuh", "qgemv_internal.h"):
+    for f in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, "bit_quantized_weight_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_tag):
+def profiled_traffic(kernel_tag, family):
     """DRAM bytes per launch of `kernel_tag` from the committed ncu summary,
     or None if there is none or the kernel sources changed since it was taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -165,7 +175,7 @@ def profiled_traffic(kernel_tag):
         with open(p) as f:
             d = json.load(f)
         e = d[kernel_tag]
-        if e.get("source_hash") != kernel_source_hash():
+        if e.get("source_hash") != kernel_source_hash(family):
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -586,7 +596,8 @@ def main():
     dom_name = wl.kernel_names()[dom]
     dom_us = dom_alone_us
     achieved = wl.alg_bytes(dom) / (dom_us * 1e-6) / 1e9
-    traffic = profiled_traffic(f"{args.workload}.{dom_name}.M{args.M}")
+    family = {"q45": "q45", "moe": "moe"}.get(args.workload, "nvfp4")
+    traffic = profiled_traffic(f"{args.workload}.{dom_name}.M{args.M}", family)
     roofline = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s", "traffic": traffic,
