@@ -1,0 +1,537 @@
+// qgemv_cc.cu -- NVFP4 decode GEMV for one token (M = 1) on the CUDA cores,
+// with fused residual-add and SwiGLU epilogues.
+//
+// What is computed follows the pages' NVFP4 format (NVIDIA NVFP4 blog, "How
+// NVFP4 works": E2M1 codes, one E4M3 scale per 16 values, one FP32 tensor
+// scale) and decode fusions (NInfer article, section 2). For one token the
+// dot products are a plain streaming reduction; the tensor cores would need
+// the weights padded into a GEMM, so here every weight is consumed by one
+// CUDA-core multiply-add instead:
+//
+//   * codes become f16 pairs with cvt.rn.f16x2.e2m1x2 (exact);
+//   * the activations sit in shared memory as f16 after an exact
+//     power-of-two prescale per 256-k chunk (the chunk maximum lands in
+//     [2^14, 2^15)); a chunk whose smallest nonzero value f16 cannot carry
+//     under that scale stays raw bf16 and takes the bf16 path below;
+//   * fma.rn.f32.f16 multiplies an f16 weight by an f16 activation into an
+//     fp32 accumulator: the product (at most 13 significant bits) is exact,
+//     one rounding per add. The 16 products of a block are summed, then
+//     scaled by the block's E4M3 scale times 2^-prescale (an exact fp32
+//     product) and added to the row's accumulator.
+//
+// Work split. As in the tensor-core kernel, a CTA owns units of R output
+// rows (gate and up rows of a SwiGLU pair both) and streams all of K for
+// them; K is cut into P phases so that P * (gate/up) * R rows -- up to 256 --
+// fill the CTA's 16 compute warps. One warp streams 256-k stages (codes
+// 128B-swizzled, scales) of every (phase, gate/up) box into a shared-memory
+// ring with 2-D TMA loads. A compute thread takes 4 consecutive rows of a box
+// and a 32-k (or 16-k) segment of the stage: it loads its activation segment
+// once and reuses it for the 4 rows; a warp's code loads are conflict-free
+// under the swizzle. Each thread keeps its rows' partial sums across the
+// stages of a unit; at the unit's end they are reduced over segments and
+// phases in a fixed order, and the epilogue applies g, SwiGLU or the
+// residual and rounds once.
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace qg {
+
+namespace {
+
+constexpr int kCcWarps = 16;                          // compute warps 0-15
+constexpr int kCcThreads = 32 * kCcWarps;
+constexpr int kCcTmaWarp = kCcWarps;                  // warp 16: TMA producer
+constexpr int kCcAllThreads = 32 * (kCcWarps + 1);
+constexpr int kCcMaxStages = 16;
+constexpr int kCcRows = 4;                            // rows per thread
+constexpr uint32_t kCcSmemMax = 227u * 1024u;
+
+struct CcArgs {
+    const uint16_t* x;         // bf16 activations, K values
+    void* y;
+    const uint16_t* residual;  // bf16 [n_out] or nullptr
+    int K;
+    int C;                     // K / 256
+    int n_out;
+    int R;                     // output rows per unit
+    int R8;                    // R rounded up to 8: row stride of a box in shared memory
+    int P;                     // K phases
+    int Cp;                    // stages per phase
+    int up_row_offset;         // SwiGLU: up row = gate row + this
+    int out_f32;
+    float g;
+    int n_units;
+    int n_stages;
+    uint32_t stage_bytes;
+    uint32_t scales_off;
+    uint32_t box_tx;
+    uint32_t smem_ring;
+    uint32_t smem_x;           // activations: C chunks of 256 f16 (or raw bf16)
+    uint32_t smem_pe;          // C floats: 2^-prescale of each chunk
+    uint32_t smem_fl;          // C bytes: 1 = chunk kept as raw bf16
+    uint32_t smem_red;         // partial sums: P * NGU * R8 rows x NSEG segments
+    uint32_t smem_bar;
+    uint64_t wait_ns;
+    int starve;
+    int* status;
+};
+
+__device__ __forceinline__ bool cc_wait_warp(uint64_t* bar, uint32_t parity, const CcArgs& a,
+                                             volatile int* abort_flag)
+{
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok) {
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+            if (mbar_try_wait_sleep(bar, parity, 20000u)) {
+                ok = true;
+                break;
+            }
+            if (*abort_flag) break;
+            if (global_timer_ns() - t0 > a.wait_ns) {
+                set_device_status(a.status, QG_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// acc + lo(w) * lo(x) and acc + hi(w) * hi(x): f16 (or bf16) operands, exact
+// product, fp32 accumulation.
+template <bool BF>
+__device__ __forceinline__ float fma2_mixed(uint32_t w, uint32_t x, float acc)
+{
+    float r;
+    if (BF)
+        asm("{\n .reg .b16 wl, wh, xl, xh;\n .reg .f32 t;\n mov.b32 {wl, wh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+            " fma.rn.f32.bf16 t, wl, xl, %3;\n fma.rn.f32.bf16 %0, wh, xh, t;\n}\n"
+            : "=f"(r)
+            : "r"(w), "r"(x), "f"(acc));
+    else
+        asm("{\n .reg .b16 wl, wh, xl, xh;\n .reg .f32 t;\n mov.b32 {wl, wh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+            " fma.rn.f32.f16 t, wl, xl, %3;\n fma.rn.f32.f16 %0, wh, xh, t;\n}\n"
+            : "=f"(r)
+            : "r"(w), "r"(x), "f"(acc));
+    return r;
+}
+
+// Converts the C chunks of x into shared memory (one warp per chunk, 8
+// values per lane): f16 under the chunk's exact prescale, or raw bf16 when
+// its smallest nonzero value would fall below f16's last bit (a sufficient
+// test of exactness: scaled exponent >= -17 keeps all 8 significant bits at
+// or above 2^-24). Within a chunk, 16-byte piece p of k segment s (NSEG
+// segments of KS values) sits at p * NSEG * 16 + s * 16, so the segments'
+// i-th pieces are contiguous and one load instruction of 8 threads with 8
+// segments touches 8 different bank groups.
+template <int NSEG>
+__device__ void cc_convert(const CcArgs& a, uint8_t* smem, int warp, int lane)
+{
+    constexpr int PPS = kChunkK / NSEG / 8;  // 16-byte pieces per segment
+    constexpr int kBatch = 4;
+    uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
+    float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
+    uint8_t* fl = smem + a.smem_fl;
+    for (int base = warp; base < a.C; base += kCcWarps * kBatch) {
+        uint4 raw[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int kc = base + u * kCcWarps;
+            raw[u] = kc < a.C ? ldg_nc_128(a.x + static_cast<size_t>(kc) * kChunkK + lane * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int kc = base + u * kCcWarps;
+            if (kc >= a.C) break;
+            const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+            uint32_t emax = 0, emin = 255, magmax = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t mg = ((i & 1) ? (wv[i >> 1] >> 16) : wv[i >> 1]) & 0x7FFFu;
+                const uint32_t ef = mg >> 7;
+                if (ef != 255u) {
+                    emax = max(emax, ef);
+                    magmax = max(magmax, mg);
+                    if (mg != 0u) emin = min(emin, ef);
+                }
+            }
+            emax = __reduce_max_sync(0xffffffffu, emax);
+            emin = __reduce_min_sync(0xffffffffu, emin);
+            if (emax == 0u) magmax = __reduce_max_sync(0xffffffffu, magmax);
+            const int e = min(emax != 0u ? 141 - static_cast<int>(emax) : prescale_exponent(magmax), 126);
+            const bool inexact = emin != 255u && static_cast<int>(emin) - 127 + e < -17;
+            uint32_t o[4];
+            if (inexact) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[i] = wv[i];
+            } else {
+                const float sc = __int_as_float((127 + e) << 23);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = pack_f16x2(__uint_as_float(wv[i] << 16) * sc, __uint_as_float(wv[i] & 0xFFFF0000u) * sc);
+            }
+            const int off = (lane % PPS) * NSEG * 4 + (lane / PPS) * 4;  // in 4-byte words
+            *reinterpret_cast<uint4*>(xs + kc * (kChunkK / 2) + off) = make_uint4(o[0], o[1], o[2], o[3]);
+            if (lane == 0) {
+                pe[kc] = inexact ? 1.0f : __int_as_float((127 - e) << 23);
+                fl[kc] = inexact ? 1 : 0;
+            }
+        }
+    }
+}
+
+// One thread's share of a stage: rows row0 .. row0 + 3 of box b2 (rows at
+// or past R read as zero codes), k segment `seg` (KS = 256 / NSEG values) of
+// chunk kc. The four rows' blocks are interleaved, two accumulators per row
+// and block, so that eight independent multiply-add chains are in flight.
+template <int NSEG, bool BF>
+__device__ __forceinline__ void cc_stage(const CcArgs& a, uint32_t stage, int b2, int row0, int seg,
+                                         const uint32_t* xw, float pe, float (&acc)[kCcRows])
+{
+    constexpr int KS = kChunkK / NSEG;  // 32 or 16 k
+    constexpr int NW = KS / 8;          // code words per row
+    constexpr int NB = NW / 2;          // 16-k blocks per row
+    uint32_t cw[kCcRows][NW];
+    float sc[kCcRows][NB];
+#pragma unroll
+    for (int i = 0; i < kCcRows; ++i) {
+        const int r = row0 + i;
+        const bool in = r < a.R;
+        const uint32_t rowb = stage + static_cast<uint32_t>(b2 * a.R8 + r) * 128u;
+        const uint32_t chunk = static_cast<uint32_t>((NW == 4 ? seg : seg >> 1) ^ (r & 7));
+        if constexpr (NW == 4) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (in) v = lds128(rowb + (chunk << 4));
+            cw[i][0] = v.x; cw[i][1] = v.y; cw[i][2] = v.z; cw[i][3] = v.w;
+        } else {
+            uint2 v = make_uint2(0, 0);
+            if (in) v = lds64(rowb + (chunk << 4) + static_cast<uint32_t>(seg & 1) * 8u);
+            cw[i][0] = v.x; cw[i][1] = v.y;
+        }
+        // the NB scale bytes of this segment, times 2^-prescale (exact)
+        const uint32_t sb = stage + a.scales_off + static_cast<uint32_t>(b2 * a.R8 + r) * 16u;
+        const uint32_t byte0 = static_cast<uint32_t>(seg * NB);
+        const uint32_t word = in ? lds32(sb + (byte0 & ~3u)) : 0u;
+        const uint32_t two = (word >> (8 * (byte0 & 3))) & (NB == 2 ? 0xFFFFu : 0xFFu);
+        const uint32_t h2 = e4m3x2_to_f16x2(two);
+        sc[i][0] = half_bits_to_f32(h2 & 0xFFFFu) * pe;
+        if constexpr (NB == 2) sc[i][1] = half_bits_to_f32(h2 >> 16) * pe;
+    }
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk) {
+        float s[kCcRows][2];
+#pragma unroll
+        for (int i = 0; i < kCcRows; ++i) s[i][0] = s[i][1] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int wd = 2 * blk + h;
+            uint32_t w[kCcRows][4];
+#pragma unroll
+            for (int i = 0; i < kCcRows; ++i) {
+                e2m1x8_to_f16x2x4(cw[i][wd], w[i]);
+                if (BF) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) w[i][j] = f16x2_to_bf16x2(w[i][j]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t xv = xw[wd * 4 + j];
+#pragma unroll
+                for (int i = 0; i < kCcRows; ++i) s[i][j & 1] = fma2_mixed<BF>(w[i][j], xv, s[i][j & 1]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kCcRows; ++i) acc[i] = fmaf(s[i][0] + s[i][1], sc[i][blk], acc[i]);
+    }
+}
+
+template <int EPI, int NSEG>
+__global__ void __launch_bounds__(kCcAllThreads, 1)
+    cc_gemv_kernel(const __grid_constant__ CcArgs a, const __grid_constant__ CUtensorMap tm_codes,
+                   const __grid_constant__ CUtensorMap tm_scales)
+{
+    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
+    constexpr int KS = kChunkK / NSEG;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = warp_index_uniform();
+    const int lane = threadIdx.x & 31;
+
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.smem_bar);
+    uint64_t* empty = full + kCcMaxStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCcMaxStages);
+
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.n_stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCcWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kCcTmaWarp) {
+        // ------------------------------------------------------------ producer
+        if (elect_one()) {
+            prefetch_tensormap(&tm_codes);
+            prefetch_tensormap(&tm_scales);
+        }
+        __syncwarp();
+        int slot = 0, lap = 0, issued = 0;
+        bool stop = false;
+        for (int u = blockIdx.x; u < a.n_units && !stop; u += gridDim.x) {
+            const int row0 = u * a.R;
+            for (int c = 0; c < a.Cp; ++c) {
+                if (lap > 0 && !cc_wait_warp(&empty[slot], (lap - 1) & 1, a, abort_flag)) {
+                    stop = true;
+                    break;
+                }
+                if (*abort_flag || a.starve) {
+                    stop = true;
+                    break;
+                }
+                int live = 0;
+                for (int pp = 0; pp < a.P; ++pp) live += (pp * a.Cp + c < a.C) ? 1 : 0;
+                uint8_t* sb = smem + a.smem_ring + slot * a.stage_bytes;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live * NGU) * a.box_tx);
+                    for (int pp = 0; pp < a.P; ++pp) {
+                        const int kc = pp * a.Cp + c;
+                        if (kc >= a.C) continue;
+#pragma unroll
+                        for (int gg = 0; gg < NGU; ++gg) {
+                            const int b2 = pp * NGU + gg;
+                            const int row = row0 + gg * a.up_row_offset;
+                            tma_load_2d(sb + b2 * a.R8 * 128, &tm_codes, kc * (kChunkK / 2), row, &full[slot]);
+                            tma_load_2d(sb + a.scales_off + b2 * a.R8 * 16, &tm_scales, kc * (kChunkK / 16), row,
+                                        &full[slot]);
+                        }
+                    }
+                }
+                __syncwarp();
+                ++issued;
+                if (++slot == a.n_stages) {
+                    slot = 0;
+                    ++lap;
+                }
+            }
+        }
+        if (lane == 0)
+            for (int g = max(0, issued - a.n_stages); g < issued; ++g)
+                mbar_wait_bounded(&full[g % a.n_stages], (g / a.n_stages) & 1, a.wait_ns, a.status);
+        __syncwarp();
+        return;
+    }
+
+    // ---------------------------------------------------------------- compute warps
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    cc_convert<NSEG>(a, smem, warp, lane);
+    named_barrier_sync(1, kCcThreads);
+
+    // this thread's rows and segment: item = (box, row group, segment)
+    const int rg_per_box = a.R8 / kCcRows;
+    const int item = threadIdx.x;
+    const int seg = item % NSEG;
+    const int bg = item / NSEG;
+    const int b2 = bg / rg_per_box;
+    const int row0 = (bg % rg_per_box) * kCcRows;
+    const bool active = b2 < a.P * NGU;
+    const int p = active ? b2 / NGU : 0;
+    const uint32_t* xs = reinterpret_cast<const uint32_t*>(smem + a.smem_x);
+    const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
+    const uint8_t* fl = smem + a.smem_fl;
+    float* red = reinterpret_cast<float*>(smem + a.smem_red);
+    const uint32_t ring = smem_u32(smem + a.smem_ring);
+
+    bool aborted = false;
+    int slot = 0, lap = 0;
+    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+        float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
+        for (int c = 0; c < a.Cp; ++c) {
+            if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
+            const int kc = p * a.Cp + c;
+            if (!aborted && active && kc < a.C) {
+                const uint32_t stage = ring + slot * a.stage_bytes;
+                uint32_t xw[KS / 2];
+                const uint32_t* xc = xs + kc * (kChunkK / 2) + seg * 4;
+#pragma unroll
+                for (int i = 0; i < KS / 8; ++i) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(xc + i * NSEG * 4);
+                    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
+                }
+                if (fl[kc] == 0)
+                    cc_stage<NSEG, false>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
+                else
+                    cc_stage<NSEG, true>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (++slot == a.n_stages) {
+                slot = 0;
+                ++lap;
+            }
+        }
+
+        // ---------------- fixed-order reduction over segments and phases, epilogue
+        if (active) {
+#pragma unroll
+            for (int i = 0; i < kCcRows; ++i) red[(b2 * a.R8 + row0 + i) * NSEG + seg] = acc[i];
+        }
+        named_barrier_sync(1, kCcThreads);
+        if (!aborted) {
+            const int r0 = u * a.R;
+            for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
+                if (r0 + r >= a.n_out) break;
+                float v[NGU];
+#pragma unroll
+                for (int gg = 0; gg < NGU; ++gg) {
+                    float s = 0.f;
+                    for (int pp = 0; pp < a.P; ++pp) {
+                        const float* rp = red + ((pp * NGU + gg) * a.R8 + r) * NSEG;
+#pragma unroll
+                        for (int sg = 0; sg < NSEG; ++sg) s += rp[sg];
+                    }
+                    v[gg] = s * a.g;
+                }
+                float val = v[0];
+                if (EPI == EPI_SWIGLU) val = (val / (1.0f + expf(-val))) * v[NGU - 1];
+                if (EPI == EPI_RESID) val += bf16_bits_to_f32(a.residual[r0 + r]);
+                if (a.out_f32)
+                    reinterpret_cast<float*>(a.y)[r0 + r] = val;
+                else
+                    reinterpret_cast<uint16_t*>(a.y)[r0 + r] = f32_to_bf16_bits_rn(val);
+            }
+        }
+        named_barrier_sync(1, kCcThreads);  // red is rewritten by the next unit
+    }
+}
+
+constexpr uint32_t align_up(uint32_t v, uint32_t al) { return (v + al - 1) / al * al; }
+
+template <int EPI, int NSEG>
+qg_status cc_launch(CcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, int grid, cudaStream_t stream)
+{
+    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
+    a.status = device_status_ptr();
+    if (!a.status) return QG_ERR_CUDA;
+    const DebugState dbg = debug_state();
+    a.wait_ns = dbg.wait_ns;
+    a.starve = dbg.starve;
+
+    const uint32_t nbox = static_cast<uint32_t>(a.P * NGU);
+    a.scales_off = nbox * a.R8 * 128u;
+    a.stage_bytes = align_up(a.scales_off + nbox * a.R8 * 16u, 1024);
+    a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
+    const uint32_t x_bytes = static_cast<uint32_t>(a.C) * kChunkK * 2u;
+    const uint32_t pe_bytes = align_up(static_cast<uint32_t>(a.C) * 4u, 16);
+    const uint32_t fl_bytes = align_up(static_cast<uint32_t>(a.C), 16);
+    const uint32_t red_bytes = align_up(nbox * a.R8 * NSEG * 4u, 128);
+    const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
+    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + red_bytes + bar_bytes;
+    if (fixed + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
+    a.n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / a.stage_bytes));
+
+    uint32_t so = 0;
+    a.smem_ring = so;
+    so += a.n_stages * a.stage_bytes;
+    a.smem_x = so;
+    so += x_bytes;
+    a.smem_pe = so;
+    so += pe_bytes;
+    a.smem_fl = so;
+    so += fl_bytes;
+    a.smem_red = so;
+    so += red_bytes;
+    a.smem_bar = so;
+    so += bar_bytes;
+    if (so > kCcSmemMax) return QG_ERR_UNSUPPORTED;
+
+    auto kern = cc_gemv_kernel<EPI, NSEG>;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCcSmemMax) != cudaSuccess)
+            return QG_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kCcAllThreads);
+    cfg.dynamicSmemBytes = so;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, a, tmc, tms) != cudaSuccess) return QG_ERR_CUDA;
+    return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+template <int EPI>
+qg_status cc_dispatch(const CcArgs& a, const CUtensorMap& tmc, const CUtensorMap& tms, int grid,
+                      cudaStream_t stream)
+{
+    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
+    // 8 segments of 32 k when the rows fill 16 warps that way, else 16 of 16 k
+    const int items8 = a.P * NGU * (a.R8 / kCcRows) * 8;
+    if (items8 > kCcThreads / 2) return cc_launch<EPI, 8>(a, tmc, tms, grid, stream);
+    return cc_launch<EPI, 16>(a, tmc, tms, grid, stream);
+}
+
+}  // namespace
+
+// One-token NVFP4 GEMV on the CUDA cores; QG_ERR_UNSUPPORTED for other M,
+// for K not a multiple of 256 or when x does not fit in shared memory.
+qg_status launch_cc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
+                                int out_f32, const void* residual, int M, int N, int K, int swiglu,
+                                cudaStream_t stream)
+{
+    if (M != 1 || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
+    const int ngu = swiglu ? 2 : 1;
+    const int n_out = swiglu ? N / 2 : N;
+    const int sms = sm_count(-1);
+    if (sms <= 0) return QG_ERR_CUDA;
+    // Smallest number of units per CTA whose rows fit the 256-row budget of
+    // one stage; R = ceil(n_out / (SMs * units)) gives every SM the same
+    // byte count.
+    int R = 1;
+    for (int U = 1;; ++U) {
+        R = (n_out + sms * U - 1) / (sms * U);
+        if (ngu * ((R + 7) / 8 * 8) <= 256) break;
+    }
+    R = std::max(R, 1);
+    CcArgs a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.y = y;
+    a.residual = static_cast<const uint16_t*>(residual);
+    a.K = K;
+    a.C = K / kChunkK;
+    a.n_out = n_out;
+    a.R = R;
+    a.R8 = (R + 7) / 8 * 8;
+    a.P = std::max(1, std::min(256 / (ngu * a.R8), a.C));
+    a.Cp = (a.C + a.P - 1) / a.P;
+    a.up_row_offset = swiglu ? n_out : 0;
+    a.out_f32 = swiglu ? 0 : out_f32;
+    a.g = g;
+    a.n_units = (n_out + R - 1) / R;
+    const int grid = std::min(sms, a.n_units);
+    CUtensorMap tmc, tms;
+    memset(&tmc, 0, sizeof(tmc));
+    memset(&tms, 0, sizeof(tms));
+    if (!encode_tmap_2d(&tmc, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, R, true) ||
+        !encode_tmap_2d(&tms, scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 16, N, 16, R, false))
+        return QG_ERR_CUDA;
+    if (swiglu) return cc_dispatch<EPI_SWIGLU>(a, tmc, tms, grid, stream);
+    if (residual) return cc_dispatch<EPI_RESID>(a, tmc, tms, grid, stream);
+    return cc_dispatch<EPI_NONE>(a, tmc, tms, grid, stream);
+}
+
+}  // namespace qg

@@ -97,6 +97,11 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtyp
 qg_status launch_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
                              int out_f32, const void* residual, int M, int N, int K, int swiglu,
                              cudaStream_t stream);
+// One-token NVFP4 GEMV on the CUDA cores (qgemv_cc.cu): QG_ERR_UNSUPPORTED
+// for M != 1 or when a shape does not fit its shared-memory plan.
+qg_status launch_cc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
+                                int out_f32, const void* residual, int M, int N, int K, int swiglu,
+                                cudaStream_t stream);
 // tcgen05 kernels (NVFP4): QG_ERR_UNSUPPORTED when a shape does not fit their
 // shared-memory plan; the callers then use the mma.sync kernels above.
 qg_status launch_tc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,

@@ -17,19 +17,23 @@
 // Pipeline. One warp streams, per 256-k chunk of every phase (a stage), the
 // codes (128B-swizzled) and scales of each (phase, gate/up) box into a ring of
 // shared-memory stages with 2-D TMA loads. A stage is worked on in two 128-k
-// granules, each passing through three roles, two warps per role taking
-// alternate granules:
-//   * decode warps (one per TMEM lane quadrant) turn codes into f16 with
-//     cvt.rn.f16x2.e2m1x2 (exact) and store them to a TMEM buffer with
-//     tcgen05.st: TMEM lane = the triple, 32-bit column = two consecutive k;
-//   * an MMA warp issues eight tcgen05.mma (M = 128, K = 16) per granule with
-//     the activations as the shared-memory B operand;
-//   * fold warps (one per quadrant) read D back with tcgen05.ld, free the
-//     buffer and accumulate in fp32; they own the per-unit reduction and
-//     epilogue, which thus overlaps the next unit.
+// granules; granule g belongs to decode set g % 4 and passes through three
+// roles:
+//   * the set's four decode warps (one per TMEM lane quadrant) turn codes
+//     into f16 with cvt.rn.f16x2.e2m1x2 (exact) and store them to the set's
+//     TMEM buffer with tcgen05.st: TMEM lane = the triple, 32-bit column =
+//     two consecutive k;
+//   * the set's MMA warp (one per set, each on its own SM sub-partition)
+//     issues eight tcgen05.mma (M = 128, K = 16) with the activations as the
+//     shared-memory B operand;
+//   * four fold warps (one per quadrant, every granule in order) read D back
+//     with tcgen05.ld, free the buffer and accumulate in fp32; they own the
+//     per-unit reduction and epilogue, which thus overlaps the next unit.
 // The roles meet only at per-buffer mbarriers ("A written", "MMA done", "D
-// read"), up to eight buffers rotate, and every synchronisation covers a whole
-// 128-k granule: an mbarrier round trip costs about as much as decoding 32 k.
+// read"), and every synchronisation covers a whole 128-k granule: an mbarrier
+// round trip costs about as much as decoding 32 k. Before the first stage
+// (and whenever the activations no longer fit in shared memory, per
+// super-chunk) the decode warps convert the activations into the B layout.
 //
 // The E4M3 block scale is applied in one of two exact ways:
 //   * one token (M = 1): after the MMA, in fp32. Four 16-k blocks share one
@@ -44,9 +48,10 @@
 //     cheaper than one fp32 multiply-add per block and token.
 // Activations enter the MMA as f16 after an exact power-of-two prescale per
 // (token, 256-k chunk) that puts the chunk maximum in [2^14, 2^15); a stage
-// where some chunk holds values that f16 cannot represent exactly under that
-// scale runs in bf16 on the raw activations instead (weights are exact in
-// both). Products are therefore exact and the accumulation is fp32.
+// where some chunk's smallest nonzero value lies too far below its maximum
+// for f16 to hold it exactly under that scale runs in bf16 on the raw
+// activations instead (weights are exact in both). Products are therefore
+// exact and the accumulation is fp32.
 //
 // Determinism: every sum runs in a fixed order (MMA chains, granules in k
 // order per fold warp, then fold warps and phases in index order). Results for
