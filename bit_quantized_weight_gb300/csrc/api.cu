@@ -149,7 +149,11 @@ qg_status qgemv_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale,
     if (!aligned16(min) || (q_hi && !aligned16(q_hi))) return QG_ERR_MISALIGNED;
     if (y_dtype != QG_OUT_BF16 && y_dtype != QG_OUT_F32) return QG_ERR_INVALID_ARG;
     const int f32 = y_dtype == QG_OUT_F32;
-    if (K % kChunkK == 0) return launch_dense_q45(q_lo, q_hi, scale, min, bits, x, y, f32, residual, M, N, K, stream);
+    if (K % kChunkK == 0) {
+        s = launch_cc_dense_q45(q_lo, q_hi, scale, min, bits, x, y, f32, residual, M, N, K, stream);
+        if (s != QG_ERR_UNSUPPORTED) return s;
+        return launch_dense_q45(q_lo, q_hi, scale, min, bits, x, y, f32, residual, M, N, K, stream);
+    }
     return launch_simple(bits == 5 ? FMT_Q5 : FMT_Q4, q_lo, q_hi, scale, min, 1.f, x, y, f32, residual, M, N, K, 0,
                          stream);
 }

@@ -73,6 +73,10 @@ struct CcArgs {
     uint32_t smem_fl;          // C bytes: 1 = chunk kept as raw bf16
     uint32_t smem_red;         // partial sums: P * NGU * R8 rows x NSEG segments
     uint32_t smem_bar;
+    // groupwise-int layouts only
+    uint32_t mins_off;         // min boxes inside a stage
+    uint32_t hi_off;           // Q5 high-bit boxes inside a stage
+    uint32_t smem_gx;          // C * NSEG floats: sum of x over each k segment
     uint64_t wait_ns;
     int starve;
     int* status;
@@ -411,6 +415,320 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------- groupwise int (Q4 / Q5)
+// Same plan for w = scale * q + min per group of 32 (NInfer article, section
+// 2: the groupwise-int recipe): per row and group, y += scale * sum(q x) +
+// min * sum(x). The codes enter the multiply-add as f16 subnormals: the f16
+// with bit pattern q is exactly q * 2^-24 (q < 32), so a masked nibble pair
+// is an f16 pair with no conversion at all, and the 2^24 moves into the
+// scale. Nibble k and nibble k + 4 of a 32-bit code word form one pair, so
+// the activations are stored paired the same way, (x_k, x_{k+4}). The sums
+// of x per segment come from the original bf16 values, in a fixed order.
+
+// Converts x as cc_convert does, with the (k, k+4) pairing, and writes the
+// fp32 sum of each segment's original values.
+template <int NSEG>
+__device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lane)
+{
+    constexpr int kBatch = 4;
+    constexpr int PPS = kChunkK / NSEG / 8;  // lanes (16-byte pieces) per segment
+    uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
+    float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
+    float* gx = reinterpret_cast<float*>(smem + a.smem_gx);
+    uint8_t* fl = smem + a.smem_fl;
+    for (int base = warp; base < a.C; base += kCcWarps * kBatch) {
+        uint4 raw[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int kc = base + u * kCcWarps;
+            raw[u] = kc < a.C ? ldg_nc_128(a.x + static_cast<size_t>(kc) * kChunkK + lane * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int kc = base + u * kCcWarps;
+            if (kc >= a.C) break;
+            const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+            uint32_t emax = 0, emin = 255, magmax = 0;
+            float sx = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t hb = (i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu);
+                sx += bf16_bits_to_f32(hb);
+                const uint32_t mg = hb & 0x7FFFu;
+                const uint32_t ef = mg >> 7;
+                if (ef != 255u) {
+                    emax = max(emax, ef);
+                    magmax = max(magmax, mg);
+                    if (mg != 0u) emin = min(emin, ef);
+                }
+            }
+#pragma unroll
+            for (int sh = 1; sh < PPS; sh <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, sh);
+            emax = __reduce_max_sync(0xffffffffu, emax);
+            emin = __reduce_min_sync(0xffffffffu, emin);
+            if (emax == 0u) magmax = __reduce_max_sync(0xffffffffu, magmax);
+            const int e = min(emax != 0u ? 141 - static_cast<int>(emax) : prescale_exponent(magmax), 126);
+            const bool inexact = emin != 255u && static_cast<int>(emin) - 127 + e < -17;
+            uint32_t o[4];
+            if (inexact) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[i] = wv[i];
+            } else {
+                const float sc = __int_as_float((127 + e) << 23);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = pack_f16x2(__uint_as_float(wv[i] << 16) * sc, __uint_as_float(wv[i] & 0xFFFF0000u) * sc);
+            }
+            // natural pairs (x0,x1)(x2,x3)(x4,x5)(x6,x7) -> (x0,x4)(x1,x5)(x2,x6)(x3,x7)
+            const uint32_t p0 = __byte_perm(o[0], o[2], 0x5410), p1 = __byte_perm(o[0], o[2], 0x7632);
+            const uint32_t p2 = __byte_perm(o[1], o[3], 0x5410), p3 = __byte_perm(o[1], o[3], 0x7632);
+            const int off = (lane % PPS) * NSEG * 4 + (lane / PPS) * 4;
+            *reinterpret_cast<uint4*>(xs + kc * (kChunkK / 2) + off) = make_uint4(p0, p1, p2, p3);
+            if (lane % PPS == 0) gx[kc * NSEG + lane / PPS] = sx;
+            if (lane == 0) {
+                pe[kc] = inexact ? 1.0f : __int_as_float((127 - e) << 23);
+                fl[kc] = inexact ? 1 : 0;
+            }
+        }
+    }
+}
+
+// Code word w (8 unsigned 4-bit codes) -> four f16 pairs of subnormals
+// (q_j, q_{j+4}) * 2^-24; Q5 ORs in the fifth bit (bit 4 of each half) from
+// hsp, the word's high bits spread as k0..k3 -> bits 4..7 and k4..k7 -> bits
+// 20..23.
+template <int BITS>
+__device__ __forceinline__ void q45_pairs(uint32_t w, uint32_t hsp, uint32_t (&z)[4])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        z[j] = (w >> (4 * j)) & 0x000F000Fu;
+        if (BITS == 5) z[j] |= (hsp >> j) & 0x00100010u;
+    }
+}
+
+// One thread's share of a stage (see cc_stage); `seg` covers one group
+// (NSEG = 8) or half of one (NSEG = 16). The bf16 path (a chunk kept raw)
+// widens the codes and activations to fp32.
+template <int NSEG, int BITS, bool BF>
+__device__ __forceinline__ void cc_stage_q45(const CcArgs& a, uint32_t stage, int b2, int row0, int seg,
+                                             const uint32_t* xw, float pe, float gxs, float (&acc)[kCcRows])
+{
+    constexpr int KS = kChunkK / NSEG;
+    constexpr int NW = KS / 8;
+    const int grp = NSEG == 8 ? seg : seg >> 1;
+#pragma unroll
+    for (int i = 0; i < kCcRows; ++i) {
+        const int r = row0 + i;
+        if (r >= a.R) break;
+        const uint32_t rowi = static_cast<uint32_t>(b2 * a.R8 + r);
+        const uint32_t chunk = static_cast<uint32_t>((NW == 4 ? seg : seg >> 1) ^ (r & 7));
+        uint32_t cw[NW];
+        if constexpr (NW == 4) {
+            const uint4 v = lds128(stage + rowi * 128u + (chunk << 4));
+            cw[0] = v.x; cw[1] = v.y; cw[2] = v.z; cw[3] = v.w;
+        } else {
+            const uint2 v = lds64(stage + rowi * 128u + (chunk << 4) + static_cast<uint32_t>(seg & 1) * 8u);
+            cw[0] = v.x; cw[1] = v.y;
+        }
+        uint32_t hb = 0;
+        if (BITS == 5) {
+            // 4 (NSEG = 8) or 2 bytes of high bits, one per 8 k
+            const uint32_t hw = lds32(stage + a.hi_off + rowi * 32u + static_cast<uint32_t>(seg * NW) / 4u * 4u);
+            hb = NW == 4 ? hw : (hw >> (8 * ((seg * NW) & 3)));
+        }
+        const uint32_t sw = lds32(stage + a.scales_off + rowi * 16u + static_cast<uint32_t>(grp * 2) / 4u * 4u);
+        const uint32_t mw = lds32(stage + a.mins_off + rowi * 16u + static_cast<uint32_t>(grp * 2) / 4u * 4u);
+        const float sc = half_bits_to_f32((sw >> (16 * (grp & 1))) & 0xFFFFu);
+        const float mn = half_bits_to_f32((mw >> (16 * (grp & 1))) & 0xFFFFu);
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int wd = 0; wd < NW; ++wd) {
+            uint32_t hsp = 0;
+            if (BITS == 5) {
+                const uint32_t h8 = (hb >> (8 * wd)) & 0xFFu;
+                hsp = ((h8 & 0x0Fu) << 4) | ((h8 & 0xF0u) << 16);
+            }
+            uint32_t z[4];
+            q45_pairs<BITS>(cw[wd], hsp, z);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (BF) {
+                    // raw bf16 activations: widen both sides to fp32
+                    const uint32_t xv = xw[wd * 4 + j];
+                    s0 = fmaf(static_cast<float>(z[j] & 0xFFFFu), __uint_as_float(xv << 16), s0);
+                    s1 = fmaf(static_cast<float>(z[j] >> 16), __uint_as_float(xv & 0xFFFF0000u), s1);
+                } else if (j & 1) {
+                    s1 = fma2_mixed<false>(z[j], xw[wd * 4 + j], s1);
+                } else {
+                    s0 = fma2_mixed<false>(z[j], xw[wd * 4 + j], s0);
+                }
+            }
+        }
+        // subnormal codes carry 2^-24 (not on the bf16 path)
+        const float sq = (s0 + s1) * (BF ? 1.0f : 16777216.0f);
+        acc[i] = fmaf(sq * sc, pe, acc[i]);
+        acc[i] = fmaf(mn, gxs, acc[i]);
+    }
+}
+
+template <int BITS, int EPI, int NSEG>
+__global__ void __launch_bounds__(kCcAllThreads, 1)
+    cc_q45_kernel(const __grid_constant__ CcArgs a, const __grid_constant__ CUtensorMap tm_codes,
+                  const __grid_constant__ CUtensorMap tm_scales, const __grid_constant__ CUtensorMap tm_mins,
+                  const __grid_constant__ CUtensorMap tm_hi)
+{
+    constexpr int KS = kChunkK / NSEG;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = warp_index_uniform();
+    const int lane = threadIdx.x & 31;
+
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.smem_bar);
+    uint64_t* empty = full + kCcMaxStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCcMaxStages);
+
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.n_stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCcWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kCcTmaWarp) {
+        // ------------------------------------------------------------ producer
+        if (elect_one()) {
+            prefetch_tensormap(&tm_codes);
+            prefetch_tensormap(&tm_scales);
+            prefetch_tensormap(&tm_mins);
+            if (BITS == 5) prefetch_tensormap(&tm_hi);
+        }
+        __syncwarp();
+        int slot = 0, lap = 0, issued = 0;
+        bool stop = false;
+        for (int u = blockIdx.x; u < a.n_units && !stop; u += gridDim.x) {
+            const int row = u * a.R;
+            for (int c = 0; c < a.Cp; ++c) {
+                if (lap > 0 && !cc_wait_warp(&empty[slot], (lap - 1) & 1, a, abort_flag)) {
+                    stop = true;
+                    break;
+                }
+                if (*abort_flag || a.starve) {
+                    stop = true;
+                    break;
+                }
+                int live = 0;
+                for (int pp = 0; pp < a.P; ++pp) live += (pp * a.Cp + c < a.C) ? 1 : 0;
+                uint8_t* sb = smem + a.smem_ring + slot * a.stage_bytes;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live) * a.box_tx);
+                    for (int pp = 0; pp < a.P; ++pp) {
+                        const int kc = pp * a.Cp + c;
+                        if (kc >= a.C) continue;
+                        tma_load_2d(sb + pp * a.R8 * 128, &tm_codes, kc * (kChunkK / 2), row, &full[slot]);
+                        tma_load_2d(sb + a.scales_off + pp * a.R8 * 16, &tm_scales, kc * (kChunkK / 32), row,
+                                    &full[slot]);
+                        tma_load_2d(sb + a.mins_off + pp * a.R8 * 16, &tm_mins, kc * (kChunkK / 32), row, &full[slot]);
+                        if (BITS == 5)
+                            tma_load_2d(sb + a.hi_off + pp * a.R8 * 32, &tm_hi, kc * (kChunkK / 8), row, &full[slot]);
+                    }
+                }
+                __syncwarp();
+                ++issued;
+                if (++slot == a.n_stages) {
+                    slot = 0;
+                    ++lap;
+                }
+            }
+        }
+        if (lane == 0)
+            for (int g = max(0, issued - a.n_stages); g < issued; ++g)
+                mbar_wait_bounded(&full[g % a.n_stages], (g / a.n_stages) & 1, a.wait_ns, a.status);
+        __syncwarp();
+        return;
+    }
+
+    // ---------------------------------------------------------------- compute warps
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    cc_convert_q45<NSEG>(a, smem, warp, lane);
+    named_barrier_sync(1, kCcThreads);
+
+    const int rg_per_box = a.R8 / kCcRows;
+    const int item = threadIdx.x;
+    const int seg = item % NSEG;
+    const int bg = item / NSEG;
+    const int b2 = bg / rg_per_box;
+    const int row0 = (bg % rg_per_box) * kCcRows;
+    const bool active = b2 < a.P;
+    const int p = active ? b2 : 0;
+    const uint32_t* xs = reinterpret_cast<const uint32_t*>(smem + a.smem_x);
+    const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
+    const float* gx = reinterpret_cast<const float*>(smem + a.smem_gx);
+    const uint8_t* fl = smem + a.smem_fl;
+    float* red = reinterpret_cast<float*>(smem + a.smem_red);
+    const uint32_t ring = smem_u32(smem + a.smem_ring);
+
+    bool aborted = false;
+    int slot = 0, lap = 0;
+    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+        float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
+        for (int c = 0; c < a.Cp; ++c) {
+            if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
+            const int kc = p * a.Cp + c;
+            if (!aborted && active && kc < a.C) {
+                const uint32_t stage = ring + slot * a.stage_bytes;
+                uint32_t xw[KS / 2];
+                const uint32_t* xc = xs + kc * (kChunkK / 2) + seg * 4;
+#pragma unroll
+                for (int i = 0; i < KS / 8; ++i) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(xc + i * NSEG * 4);
+                    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
+                }
+                const float gxs = gx[kc * NSEG + seg];
+                if (fl[kc] == 0)
+                    cc_stage_q45<NSEG, BITS, false>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                else
+                    cc_stage_q45<NSEG, BITS, true>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (++slot == a.n_stages) {
+                slot = 0;
+                ++lap;
+            }
+        }
+
+        // ---------------- fixed-order reduction over segments and phases, epilogue
+        if (active) {
+#pragma unroll
+            for (int i = 0; i < kCcRows; ++i) red[(b2 * a.R8 + row0 + i) * NSEG + seg] = acc[i];
+        }
+        named_barrier_sync(1, kCcThreads);
+        if (!aborted) {
+            const int r0 = u * a.R;
+            for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
+                if (r0 + r >= a.n_out) break;
+                float s = 0.f;
+                for (int pp = 0; pp < a.P; ++pp) {
+                    const float* rp = red + (pp * a.R8 + r) * NSEG;
+#pragma unroll
+                    for (int sg = 0; sg < NSEG; ++sg) s += rp[sg];
+                }
+                float val = s;
+                if (EPI == EPI_RESID) val += bf16_bits_to_f32(a.residual[r0 + r]);
+                if (a.out_f32)
+                    reinterpret_cast<float*>(a.y)[r0 + r] = val;
+                else
+                    reinterpret_cast<uint16_t*>(a.y)[r0 + r] = f32_to_bf16_bits_rn(val);
+            }
+        }
+        named_barrier_sync(1, kCcThreads);
+    }
+}
+
 constexpr uint32_t align_up(uint32_t v, uint32_t al) { return (v + al - 1) / al * al; }
 
 template <int EPI, int NSEG>
@@ -485,6 +803,79 @@ qg_status cc_dispatch(const CcArgs& a, const CUtensorMap& tmc, const CUtensorMap
     return cc_launch<EPI, 16>(a, tmc, tms, grid, stream);
 }
 
+template <int BITS, int EPI, int NSEG>
+qg_status cc_q45_launch(CcArgs a, const CUtensorMap (&maps)[4], int grid, cudaStream_t stream)
+{
+    a.status = device_status_ptr();
+    if (!a.status) return QG_ERR_CUDA;
+    const DebugState dbg = debug_state();
+    a.wait_ns = dbg.wait_ns;
+    a.starve = dbg.starve;
+
+    const uint32_t nbox = static_cast<uint32_t>(a.P);
+    a.scales_off = nbox * a.R8 * 128u;
+    a.mins_off = a.scales_off + nbox * a.R8 * 16u;
+    a.hi_off = a.mins_off + nbox * a.R8 * 16u;
+    a.stage_bytes = align_up(a.hi_off + (BITS == 5 ? nbox * a.R8 * 32u : 0u), 1024);
+    a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (BITS == 5 ? 32u : 0u));
+    const uint32_t x_bytes = static_cast<uint32_t>(a.C) * kChunkK * 2u;
+    const uint32_t pe_bytes = align_up(static_cast<uint32_t>(a.C) * 4u, 16);
+    const uint32_t gx_bytes = align_up(static_cast<uint32_t>(a.C * NSEG) * 4u, 16);
+    const uint32_t fl_bytes = align_up(static_cast<uint32_t>(a.C), 16);
+    const uint32_t red_bytes = align_up(nbox * a.R8 * NSEG * 4u, 128);
+    const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
+    const uint32_t fixed = x_bytes + pe_bytes + gx_bytes + fl_bytes + red_bytes + bar_bytes;
+    if (fixed + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
+    a.n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / a.stage_bytes));
+
+    uint32_t so = 0;
+    a.smem_ring = so;
+    so += a.n_stages * a.stage_bytes;
+    a.smem_x = so;
+    so += x_bytes;
+    a.smem_pe = so;
+    so += pe_bytes;
+    a.smem_gx = so;
+    so += gx_bytes;
+    a.smem_fl = so;
+    so += fl_bytes;
+    a.smem_red = so;
+    so += red_bytes;
+    a.smem_bar = so;
+    so += bar_bytes;
+    if (so > kCcSmemMax) return QG_ERR_UNSUPPORTED;
+
+    auto kern = cc_q45_kernel<BITS, EPI, NSEG>;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCcSmemMax) != cudaSuccess)
+            return QG_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kCcAllThreads);
+    cfg.dynamicSmemBytes = so;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, a, maps[0], maps[1], maps[2], maps[3]) != cudaSuccess) return QG_ERR_CUDA;
+    return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+template <int BITS, int EPI>
+qg_status cc_q45_dispatch(const CcArgs& a, const CUtensorMap (&maps)[4], int grid, cudaStream_t stream)
+{
+    const int items8 = a.P * (a.R8 / kCcRows) * 8;
+    if (items8 > kCcThreads / 2) return cc_q45_launch<BITS, EPI, 8>(a, maps, grid, stream);
+    return cc_q45_launch<BITS, EPI, 16>(a, maps, grid, stream);
+}
+
 }  // namespace
 
 // One-token NVFP4 GEMV on the CUDA cores; QG_ERR_UNSUPPORTED for other M,
@@ -532,6 +923,57 @@ qg_status launch_cc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, flo
     if (swiglu) return cc_dispatch<EPI_SWIGLU>(a, tmc, tms, grid, stream);
     if (residual) return cc_dispatch<EPI_RESID>(a, tmc, tms, grid, stream);
     return cc_dispatch<EPI_NONE>(a, tmc, tms, grid, stream);
+}
+
+}  // namespace qg
+
+namespace qg {
+
+// One-token Q4/Q5 GEMV on the CUDA cores; QG_ERR_UNSUPPORTED for other M,
+// for K not a multiple of 256 or when x does not fit in shared memory.
+qg_status launch_cc_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min, int bits,
+                              const void* x, void* y, int out_f32, const void* residual, int M, int N, int K,
+                              cudaStream_t stream)
+{
+    if (M != 1 || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
+    const int sms = sm_count(-1);
+    if (sms <= 0) return QG_ERR_CUDA;
+    int R = 1;
+    for (int U = 1;; ++U) {
+        R = (N + sms * U - 1) / (sms * U);
+        if ((R + 7) / 8 * 8 <= 256) break;
+    }
+    R = std::max(R, 1);
+    CcArgs a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.y = y;
+    a.residual = static_cast<const uint16_t*>(residual);
+    a.K = K;
+    a.C = K / kChunkK;
+    a.n_out = N;
+    a.R = R;
+    a.R8 = (R + 7) / 8 * 8;
+    a.P = std::max(1, std::min(256 / a.R8, a.C));
+    a.Cp = (a.C + a.P - 1) / a.P;
+    a.out_f32 = out_f32;
+    a.g = 1.f;
+    a.n_units = (N + R - 1) / R;
+    const int grid = std::min(sms, a.n_units);
+    CUtensorMap maps[4];
+    memset(maps, 0, sizeof(maps));
+    if (!encode_tmap_2d(&maps[0], q_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, R, true) ||
+        !encode_tmap_2d(&maps[1], scale, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, N, 8, R, false) ||
+        !encode_tmap_2d(&maps[2], min, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, N, 8, R, false))
+        return QG_ERR_CUDA;
+    if (bits == 5) {
+        if (!encode_tmap_2d(&maps[3], q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 8, N, 32, R, false))
+            return QG_ERR_CUDA;
+        if (residual) return cc_q45_dispatch<5, EPI_RESID>(a, maps, grid, stream);
+        return cc_q45_dispatch<5, EPI_NONE>(a, maps, grid, stream);
+    }
+    maps[3] = maps[2];
+    if (residual) return cc_q45_dispatch<4, EPI_RESID>(a, maps, grid, stream);
+    return cc_q45_dispatch<4, EPI_NONE>(a, maps, grid, stream);
 }
 
 }  // namespace qg

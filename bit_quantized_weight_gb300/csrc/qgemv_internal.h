@@ -102,6 +102,9 @@ qg_status launch_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float 
 qg_status launch_cc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
                                 int out_f32, const void* residual, int M, int N, int K, int swiglu,
                                 cudaStream_t stream);
+qg_status launch_cc_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min, int bits,
+                              const void* x, void* y, int out_f32, const void* residual, int M, int N, int K,
+                              cudaStream_t stream);
 // tcgen05 kernels (NVFP4): QG_ERR_UNSUPPORTED when a shape does not fit their
 // shared-memory plan; the callers then use the mma.sync kernels above.
 qg_status launch_tc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
