@@ -149,14 +149,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-# Kernel sources behind each workload's launches (NVFP4: the tcgen05 kernel;
-# Q4/Q5: the mma.sync kernel); a committed traffic figure is used only while
-# these files are unchanged.
+# Kernel sources behind each workload's launches (one token: the CUDA-core
+# kernels; NVFP4 with more tokens and the MoE: the tcgen05 kernel; Q4/Q5 with
+# more tokens: the mma.sync kernel); a committed traffic figure is used only
+# while these files are unchanged.
 KERNEL_SOURCES = {
-    "nvfp4": ("qgemv_tc.cu", "tcgen05.cuh", "common.cuh", "qgemv_internal.h"),
-    "q45": ("qgemv_dense.cu", "common.cuh", "qgemv_internal.h"),
+    "cc": ("qgemv_cc.cu", "common.cuh", "qgemv_internal.h"),
+    "tc": ("qgemv_tc.cu", "tcgen05.cuh", "common.cuh", "qgemv_internal.h"),
+    "mma": ("qgemv_dense.cu", "common.cuh", "qgemv_internal.h"),
     "moe": ("qgemv_tc.cu", "moe.cu", "tcgen05.cuh", "common.cuh", "qgemv_internal.h"),
 }
+
+
+def kernel_family(workload, M):
+    if workload == "moe":
+        return "moe"
+    if M == 1:
+        return "cc"
+    return "mma" if workload == "q45" else "tc"
 
 
 def kernel_source_hash(family):
@@ -596,8 +606,7 @@ def main():
     dom_name = wl.kernel_names()[dom]
     dom_us = dom_alone_us
     achieved = wl.alg_bytes(dom) / (dom_us * 1e-6) / 1e9
-    family = {"q45": "q45", "moe": "moe"}.get(args.workload, "nvfp4")
-    traffic = profiled_traffic(f"{args.workload}.{dom_name}.M{args.M}", family)
+    traffic = profiled_traffic(f"{args.workload}.{dom_name}.M{args.M}", kernel_family(args.workload, args.M))
     roofline = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s", "traffic": traffic,
