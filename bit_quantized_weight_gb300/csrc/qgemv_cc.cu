@@ -71,7 +71,7 @@ struct CcArgs {
     uint32_t smem_x;           // activations: C chunks of 256 f16 (or raw bf16)
     uint32_t smem_pe;          // C floats: 2^-prescale of each chunk
     uint32_t smem_fl;          // C bytes: 1 = chunk kept as raw bf16
-    uint32_t smem_red;         // partial sums: P * NGU * R8 rows x NSEG segments
+    uint32_t smem_red;         // partial sums: P * NGU * R8 rows
     uint32_t smem_bar;
     // groupwise-int layouts only
     uint32_t mins_off;         // min boxes inside a stage
@@ -381,10 +381,15 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
             }
         }
 
-        // ---------------- fixed-order reduction over segments and phases, epilogue
-        if (active) {
+        // ---------------- fixed-order reduction over segments (a butterfly
+        // across the segment lanes of the warp) and phases, epilogue
 #pragma unroll
-            for (int i = 0; i < kCcRows; ++i) red[(b2 * a.R8 + row0 + i) * NSEG + seg] = acc[i];
+        for (int i = 0; i < kCcRows; ++i)
+#pragma unroll
+            for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+        if (active && seg == 0) {
+#pragma unroll
+            for (int i = 0; i < kCcRows; ++i) red[b2 * a.R8 + row0 + i] = acc[i];
         }
         named_barrier_sync(1, kCcThreads);
         if (!aborted) {
@@ -395,11 +400,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
 #pragma unroll
                 for (int gg = 0; gg < NGU; ++gg) {
                     float s = 0.f;
-                    for (int pp = 0; pp < a.P; ++pp) {
-                        const float* rp = red + ((pp * NGU + gg) * a.R8 + r) * NSEG;
-#pragma unroll
-                        for (int sg = 0; sg < NSEG; ++sg) s += rp[sg];
-                    }
+                    for (int pp = 0; pp < a.P; ++pp) s += red[(pp * NGU + gg) * a.R8 + r];
                     v[gg] = s * a.g;
                 }
                 float val = v[0];
@@ -701,10 +702,15 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
             }
         }
 
-        // ---------------- fixed-order reduction over segments and phases, epilogue
-        if (active) {
+        // ---------------- fixed-order reduction over segments (a butterfly
+        // across the segment lanes of the warp) and phases, epilogue
 #pragma unroll
-            for (int i = 0; i < kCcRows; ++i) red[(b2 * a.R8 + row0 + i) * NSEG + seg] = acc[i];
+        for (int i = 0; i < kCcRows; ++i)
+#pragma unroll
+            for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+        if (active && seg == 0) {
+#pragma unroll
+            for (int i = 0; i < kCcRows; ++i) red[b2 * a.R8 + row0 + i] = acc[i];
         }
         named_barrier_sync(1, kCcThreads);
         if (!aborted) {
@@ -712,11 +718,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
             for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
                 if (r0 + r >= a.n_out) break;
                 float s = 0.f;
-                for (int pp = 0; pp < a.P; ++pp) {
-                    const float* rp = red + (pp * a.R8 + r) * NSEG;
-#pragma unroll
-                    for (int sg = 0; sg < NSEG; ++sg) s += rp[sg];
-                }
+                for (int pp = 0; pp < a.P; ++pp) s += red[pp * a.R8 + r];
                 float val = s;
                 if (EPI == EPI_RESID) val += bf16_bits_to_f32(a.residual[r0 + r]);
                 if (a.out_f32)
@@ -748,7 +750,7 @@ qg_status cc_launch(CcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
     const uint32_t x_bytes = static_cast<uint32_t>(a.C) * kChunkK * 2u;
     const uint32_t pe_bytes = align_up(static_cast<uint32_t>(a.C) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(a.C), 16);
-    const uint32_t red_bytes = align_up(nbox * a.R8 * NSEG * 4u, 128);
+    const uint32_t red_bytes = align_up(nbox * a.R8 * 4u, 128);
     const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
     const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
@@ -822,7 +824,7 @@ qg_status cc_q45_launch(CcArgs a, const CUtensorMap (&maps)[4], int grid, cudaSt
     const uint32_t pe_bytes = align_up(static_cast<uint32_t>(a.C) * 4u, 16);
     const uint32_t gx_bytes = align_up(static_cast<uint32_t>(a.C * NSEG) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(a.C), 16);
-    const uint32_t red_bytes = align_up(nbox * a.R8 * NSEG * 4u, 128);
+    const uint32_t red_bytes = align_up(nbox * a.R8 * 4u, 128);
     const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
     const uint32_t fixed = x_bytes + pe_bytes + gx_bytes + fl_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
