@@ -17,19 +17,23 @@ __global__ void route_kernel(const float* logits, int M, int E, int topk, int32_
     const int lane = threadIdx.x;
     if (m >= M) return;
     const float* l = logits + static_cast<size_t>(m) * E;
-    uint32_t taken[32];  // bit i of taken[j]: expert lane + 32 * (32 * j + i)... kept per lane
+    // E <= 1024: this lane's logits (experts lane + 32 j) stay in registers,
+    // and bit j of `taken` marks expert lane + 32 j as already selected
+    float v[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) taken[j] = 0;
+    for (int j = 0; j < 32; ++j) v[j] = lane + 32 * j < E ? l[lane + 32 * j] : 0.f;
+    uint32_t taken = 0;
     float sel_l[8];
     int sel_id[8];
     for (int i = 0; i < topk; ++i) {
         float best = -INFINITY;
         int best_id = 0x7FFFFFFF;
-        for (int e = lane, j = 0; e < E; e += 32, ++j) {
-            if ((taken[j >> 5] >> (j & 31)) & 1u) continue;
-            const float v = l[e];
-            if (v > best || (v == best && e < best_id)) {
-                best = v;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int e = lane + 32 * j;
+            if (e >= E || ((taken >> j) & 1u)) continue;
+            if (v[j] > best || (v[j] == best && e < best_id)) {
+                best = v[j];
                 best_id = e;
             }
         }
@@ -42,10 +46,7 @@ __global__ void route_kernel(const float* logits, int M, int E, int topk, int32_
                 best_id = oid;
             }
         }
-        if ((best_id & 31) == lane) {
-            const int j = best_id >> 5;
-            taken[j >> 5] |= 1u << (j & 31);
-        }
+        if ((best_id & 31) == lane) taken |= 1u << (best_id >> 5);
         sel_l[i] = best;
         sel_id[i] = best_id;
     }
@@ -123,82 +124,114 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
                                  int* status)
 {
     __shared__ int s_pair_e[kMaxPairs];
-    __shared__ int s_order[kMaxPairs];
-    __shared__ int s_n_gu, s_n_dn;
-    __shared__ int s_gu_of_dn[kMaxPairs];  // gate/up group of each down group
+    __shared__ int s_order[kMaxPairs];    // valid pairs sorted by (expert, pair)
+    __shared__ int s_gu_at[kMaxPairs];    // gate/up group of sorted position i
+    __shared__ int s_run0[kMaxPairs];     // first sorted position of that group's expert run
+    __shared__ int s_dn_start[kMaxPairs]; // sorted position starting each down group
+    __shared__ int s_nv, s_n_gu, s_n_dn;
     const int P = M * topk;
-    if (threadIdx.x == 0) {
-        int nv = 0;
-        for (int p = 0; p < P; ++p) {
-            const int e = ids[p];
-            if (e < 0 || e >= E) {
-                atomicCAS(status, 0, QG_ERR_INVALID_ARG);
-                s_pair_e[p] = -1;
-                continue;
-            }
+    const int tid = threadIdx.x;
+    for (int p = tid; p < P; p += blockDim.x) {
+        const int e = ids[p];
+        if (e < 0 || e >= E) {
+            atomicCAS(status, 0, QG_ERR_INVALID_ARG);
+            s_pair_e[p] = -1;
+        } else {
             s_pair_e[p] = e;
-            // insertion into order sorted by (expert, pair)
-            int j = nv++;
-            while (j > 0 && (s_pair_e[s_order[j - 1]] > e)) {
-                s_order[j] = s_order[j - 1];
-                --j;
-            }
-            s_order[j] = p;
         }
-        int n_gu = 0, n_dn = 0;
-        int i = 0;
-        while (i < nv) {
+    }
+    __syncthreads();
+    // rank of each valid pair in (expert, pair) order: one thread per pair
+    for (int p = tid; p < P; p += blockDim.x) {
+        const int e = s_pair_e[p];
+        if (e < 0) continue;
+        int r = 0;
+        for (int q = 0; q < P; ++q) {
+            const int f = s_pair_e[q];
+            r += (f >= 0 && (f < e || (f == e && q < p))) ? 1 : 0;
+        }
+        s_order[r] = p;
+    }
+    if (tid == 0) {
+        int nv = 0;
+        for (int p = 0; p < P; ++p) nv += s_pair_e[p] >= 0 ? 1 : 0;
+        s_nv = nv;
+    }
+    __syncthreads();
+    // group boundaries along the sorted pairs (at most 64: one thread scans)
+    if (tid == 0) {
+        const int nv = s_nv;
+        int n_gu = 0, n_dn = 0, run0 = 0;
+        for (int i = 0; i < nv; ++i) {
             const int e = s_pair_e[s_order[i]];
-            int iend = i;
-            while (iend < nv && s_pair_e[s_order[iend]] == e) ++iend;
-            GroupDesc gg;
-            gg.ntok = M;
-            gg.e = e;
-            gg.xkey = 0;
-            for (int j = 0; j < 8; ++j) {
-                gg.x_row[j] = j < M ? j : 0;
-                gg.out_row[j] = -1;
+            if (i == 0 || e != s_pair_e[s_order[i - 1]]) {
+                run0 = i;
+                ++n_gu;
             }
-            int first_of_tok[kMaxTokens];
-            for (int m = 0; m < kMaxTokens; ++m) first_of_tok[m] = -1;
-            for (int q = i; q < iend; ++q) {
-                const int p = s_order[q];
-                const int m = p / topk;
-                if (first_of_tok[m] < 0) {
-                    first_of_tok[m] = p;
-                    gg.out_row[m] = p;
-                }
-            }
-            g_gu[n_gu] = gg;
-            // down groups: chunks of at most 8 pairs
-            for (int q = i; q < iend; q += 8) {
-                GroupDesc gd;
-                gd.ntok = min(8, iend - q);
-                gd.e = e;
-                gd.xkey = 1 + n_dn;
-                for (int j = 0; j < 8; ++j) {
-                    if (j < gd.ntok) {
-                        const int p = s_order[q + j];
-                        gd.out_row[j] = p;
-                        gd.x_row[j] = first_of_tok[p / topk];
-                    } else {
-                        gd.out_row[j] = -1;
-                        gd.x_row[j] = 0;
-                    }
-                }
-                s_gu_of_dn[n_dn] = n_gu;
-                g_dn[n_dn++] = gd;
-            }
-            ++n_gu;
-            i = iend;
+            s_gu_at[i] = n_gu - 1;
+            s_run0[i] = run0;
+            if ((i - run0) % 8 == 0) s_dn_start[n_dn++] = i;
         }
         s_n_gu = n_gu;
         s_n_dn = n_dn;
     }
     __syncthreads();
+    const int nv = s_nv;
+    // one gate/up group per expert run: all M token rows of x, the first
+    // slot of each token writes its h row
+    for (int i = tid; i < nv; i += blockDim.x) {
+        if (s_run0[i] != i) continue;
+        const int e = s_pair_e[s_order[i]];
+        GroupDesc gg;
+        gg.ntok = M;
+        gg.e = e;
+        gg.xkey = 0;
+        for (int j = 0; j < 8; ++j) {
+            gg.x_row[j] = j < M ? j : 0;
+            gg.out_row[j] = -1;
+        }
+        for (int q = i; q < nv && s_pair_e[s_order[q]] == e; ++q) {
+            const int p = s_order[q];
+            const int m = p / topk;
+            if (gg.out_row[m] < 0) gg.out_row[m] = p;
+        }
+        g_gu[s_gu_at[i]] = gg;
+    }
+    // down groups: chunks of at most 8 pairs of one run; a pair reads the h
+    // row its token's first slot for that expert wrote
+    for (int d = tid; d < s_n_dn; d += blockDim.x) {
+        const int i0 = s_dn_start[d];
+        const int e = s_pair_e[s_order[i0]];
+        const int run0 = s_run0[i0];
+        int iend = i0;
+        while (iend < nv && iend - i0 < 8 && s_pair_e[s_order[iend]] == e) ++iend;
+        GroupDesc gd;
+        gd.ntok = iend - i0;
+        gd.e = e;
+        gd.xkey = 1 + d;
+        for (int j = 0; j < 8; ++j) {
+            if (j < gd.ntok) {
+                const int p = s_order[i0 + j];
+                const int m = p / topk;
+                int first = p;
+                for (int q = run0; q < i0 + j; ++q)
+                    if (s_order[q] / topk == m) {
+                        first = s_order[q];
+                        break;
+                    }
+                gd.out_row[j] = p;
+                gd.x_row[j] = first;
+            } else {
+                gd.out_row[j] = -1;
+                gd.x_row[j] = 0;
+            }
+        }
+        g_dn[d] = gd;
+    }
+    __syncthreads();
     const int per_gu = I / r_gu, per_dn = H / r_dn;
     const int n_gu = s_n_gu * per_gu, n_dn = s_n_dn * per_dn;
-    for (int u = threadIdx.x; u < n_gu; u += blockDim.x) {
+    for (int u = tid; u < n_gu; u += blockDim.x) {
         const int gi = u / per_gu, rb = u % per_gu;
         UnitDesc d;
         d.grp = gi;
@@ -207,7 +240,7 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
         d.out_col0 = rb * r_gu;
         u_gu[u] = d;
     }
-    for (int u = threadIdx.x; u < n_dn; u += blockDim.x) {
+    for (int u = tid; u < n_dn; u += blockDim.x) {
         const int gi = u / per_dn, rb = u % per_dn;
         UnitDesc d;
         d.grp = gi;
@@ -216,7 +249,7 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
         d.out_col0 = rb * r_dn;
         u_dn[u] = d;
     }
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         ctrl[0] = n_gu;
         ctrl[1] = n_dn;
     }
