@@ -94,7 +94,7 @@ SHAPES = [
     # (M, N, K): ragged row counts, single-tile and multi-tile CTAs, several chunks
     (1, 1, 256), (1, 15, 512), (1, 17, 768), (2, 300, 1024), (3, 1000, 1280), (4, 4099, 512),
     (5, 2048, 2304), (6, 333, 4608), (7, 160, 256), (8, 1024, 1536), (8, 7001, 512),
-    (1, 5000, 2048), (8, 64, 9216),
+    (1, 5000, 2048), (8, 64, 9216), (1, 40000, 256),
     # K % 256 != 0 takes the exact CUDA-core kernel
     (1, 40, 32), (3, 77, 96), (8, 33, 800),
 ]
@@ -133,7 +133,8 @@ def test_nvfp4_residual_in_place():
     check_out(y, yref, a, "in-place residual")
 
 
-@pytest.mark.parametrize("M,I,K", [(1, 256, 512), (1, 300, 1024), (4, 1000, 768), (8, 64, 2048), (3, 50, 96)])
+@pytest.mark.parametrize("M,I,K", [(1, 256, 512), (1, 300, 1024), (4, 1000, 768), (8, 64, 2048), (3, 50, 96),
+                                   (1, 20000, 256)])
 def test_swiglu(M, I, K):
     w = synth.nvfp4_weights(15, f"sw{I}", 2 * I, K, g=1.25)
     x = synth.bf16_normal(16, "swx", (M, K))
@@ -150,7 +151,8 @@ def test_swiglu(M, I, K):
 
 # ---------------------------------------------------------------- Q4 / Q5
 @pytest.mark.parametrize("bits", [4, 5])
-@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (3, 1000, 1024), (8, 4099, 768), (2, 17, 256), (5, 70, 96)])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (3, 1000, 1024), (8, 4099, 768), (2, 17, 256), (5, 70, 96),
+                                   (1, 4099, 768), (1, 17, 256), (1, 1000, 4608), (1, 40000, 256)])
 def test_q45(bits, M, N, K):
     w = synth.q45_weights(17, f"q{bits}.{N}.{K}", N, K, bits)
     x = synth.bf16_normal(18, f"qx{K}", (M, K))
@@ -164,8 +166,9 @@ def test_q45(bits, M, N, K):
         check_out(y, yref, a, f"Q{bits} M={M} N={N} K={K}")
 
 
-def test_q45_residual():
-    M, N, K = 4, 640, 1024
+@pytest.mark.parametrize("M", [1, 4])
+def test_q45_residual(M):
+    N, K = 640, 1024
     w = synth.q45_weights(19, "qres", N, K, 5)
     x = synth.bf16_normal(20, "qresx", (M, K))
     r = synth.bf16_normal(21, "qresr", (M, N))
@@ -202,8 +205,9 @@ def test_nvfp4_wide_dynamic_range_activations(M):
 
 
 @pytest.mark.parametrize("bits", [4, 5])
-def test_q45_wide_dynamic_range_activations(bits):
-    M, N, K = 2, 200, 512
+@pytest.mark.parametrize("M", [1, 2])
+def test_q45_wide_dynamic_range_activations(bits, M):
+    N, K = 200, 512
     w = synth.q45_weights(24, "qwide", N, K, bits)
     x = wide_range_x(M, K, 25)
     yref, a = O.gemv_q45(w, x)
@@ -222,6 +226,9 @@ def test_zero_and_tiny_activations():
     x[1] = (x[1] & 0x807F) | (0x01 << 7)              # exponent field 1: |x| ~ 2^-126
     yref, a = O.gemv_nvfp4(w, x)
     check_out(run_nvfp4(w, x, torch.float32), yref, a, "zero/tiny fp32")
+    for m in range(2):                                  # one token at a time
+        yref1, a1 = O.gemv_nvfp4(w, x[m:m + 1])
+        check_out(run_nvfp4(w, x[m:m + 1], torch.float32), yref1, a1, f"zero/tiny fp32 row {m}")
 
 
 def test_non_finite_activations_propagate():
@@ -233,6 +240,8 @@ def test_non_finite_activations_propagate():
     y = run_nvfp4(w, x, torch.float32).cpu().numpy()
     assert not np.isfinite(y[0]).any() or np.isinf(y[0]).any()
     assert np.isnan(y[1]).all()
+    y1 = run_nvfp4(w, x[1:2], torch.float32).cpu().numpy()   # one token
+    assert np.isnan(y1).all()
 
 
 # ---------------------------------------------------------------- config 1 at full size
@@ -259,11 +268,12 @@ def test_dense_layer_full_size(M):
     assert d27.hidden == 5120
 
 
-def test_mixed_q45_layer_full_size():
-    M = 8
+@pytest.mark.parametrize("M", [1, 8])
+def test_mixed_q45_layer_full_size(M):
     for name, N, K, bits in synth.Q45_RECIPE:
         w = synth.q45_weights(3, f"q45.{name}", N, K, bits)
-        x = synth.bf16_normal(3, f"q45.{name}.x", (M, K))
+        x = synth.bf16_normal(3, f"q45.{name}.x", (M, K)) if M == 8 else \
+            synth.bf16_normal(3, f"q45.{name}.x", (8, K))[:1]
         yref, a = O.gemv_q45(w, x)
         d = q45_dev(w)
         y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
