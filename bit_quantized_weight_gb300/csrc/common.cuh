@@ -83,18 +83,6 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return ok != 0;
 }
 
-// Release store / acquire load of a shared-memory word at CTA scope.
-__device__ __forceinline__ void st_release_cta(uint32_t addr, int v)
-{
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ int ld_acquire_cta(uint32_t addr)
-{
-    int v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
 
 // One lane of the warp is elected (true for exactly one active lane).
 __device__ __forceinline__ bool elect_one()

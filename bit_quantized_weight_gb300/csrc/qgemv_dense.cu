@@ -53,9 +53,6 @@ __device__ __forceinline__ uint32_t lds8(uint32_t addr)
     return v;
 }
 
-__device__ __forceinline__ uint32_t bcast_lo(uint32_t h2) { return __byte_perm(h2, 0, 0x1010); }
-__device__ __forceinline__ uint32_t bcast_hi(uint32_t h2) { return __byte_perm(h2, 0, 0x3232); }
-
 // Pack 8 16-bit values in the format's pair order: natural k order for
 // NVFP4 ({k, k+1} pairs, matching the e2m1x2 decode), {k, k+4} pairs for Q
 // (matching the 1024 + q mantissa decode).
