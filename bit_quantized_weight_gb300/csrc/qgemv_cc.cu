@@ -187,10 +187,37 @@ __device__ void cc_convert(const CcArgs& a, uint8_t* smem, int warp, int lane)
     }
 }
 
-// One thread's share of a stage: rows row0 .. row0 + 3 of box b2 (rows at
-// or past R read as zero codes), k segment `seg` (KS = 256 / NSEG values) of
-// chunk kc. The four rows' blocks are interleaved, two accumulators per row
-// and block, so that eight independent multiply-add chains are in flight.
+// Zeroes the padding rows R .. R8 - 1 of every box region in every ring
+// slot (a TMA box holds R rows and never writes them), so that they read as
+// zero codes and scales; run by the compute threads, concurrently with the
+// first copies (which touch other bytes), before their first barrier.
+// Regions: (offset of box 0, bytes per row).
+__device__ void cc_zero_padding(const CcArgs& a, uint8_t* smem, int nbox, const uint32_t (&roff)[4],
+                                const uint32_t (&rbytes)[4], int nreg)
+{
+    const int pad = a.R8 - a.R;
+    if (pad == 0) return;
+    for (int reg = 0; reg < nreg; ++reg) {
+        const int pieces = static_cast<int>(rbytes[reg] / 16u);  // 16-byte pieces per row
+        const int per_slot = nbox * pad * pieces;
+        for (int t = threadIdx.x; t < a.n_stages * per_slot; t += kCcThreads) {
+            const int slot = t / per_slot;
+            const int rem = t % per_slot;
+            const int b = rem / (pad * pieces);
+            const int rr = a.R + (rem / pieces) % pad;
+            const int pc = rem % pieces;
+            uint8_t* dst = smem + a.smem_ring + slot * a.stage_bytes + roff[reg] +
+                           (static_cast<uint32_t>(b * a.R8 + rr) * rbytes[reg]) + pc * 16;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+// One thread's share of a stage: rows row0 .. row0 + 3 of box b2 (padding
+// rows at or past R hold zero codes and scales), k segment `seg` (KS = 256 /
+// NSEG values) of chunk kc. The four rows' blocks are interleaved, one chain
+// of pair products per (row, block), so eight independent multiply-add chains
+// are in flight.
 template <int NSEG, bool BF>
 __device__ __forceinline__ void cc_stage(const CcArgs& a, uint32_t stage, int b2, int row0, int seg,
                                          const uint32_t* xw, float pe, float (&acc)[kCcRows])
@@ -203,32 +230,30 @@ __device__ __forceinline__ void cc_stage(const CcArgs& a, uint32_t stage, int b2
 #pragma unroll
     for (int i = 0; i < kCcRows; ++i) {
         const int r = row0 + i;
-        const bool in = r < a.R;
         const uint32_t rowb = stage + static_cast<uint32_t>(b2 * a.R8 + r) * 128u;
         const uint32_t chunk = static_cast<uint32_t>((NW == 4 ? seg : seg >> 1) ^ (r & 7));
         if constexpr (NW == 4) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (in) v = lds128(rowb + (chunk << 4));
+            const uint4 v = lds128(rowb + (chunk << 4));
             cw[i][0] = v.x; cw[i][1] = v.y; cw[i][2] = v.z; cw[i][3] = v.w;
         } else {
-            uint2 v = make_uint2(0, 0);
-            if (in) v = lds64(rowb + (chunk << 4) + static_cast<uint32_t>(seg & 1) * 8u);
+            const uint2 v = lds64(rowb + (chunk << 4) + static_cast<uint32_t>(seg & 1) * 8u);
             cw[i][0] = v.x; cw[i][1] = v.y;
         }
-        // the NB scale bytes of this segment, times 2^-prescale (exact)
+        // the NB scale bytes of this segment
         const uint32_t sb = stage + a.scales_off + static_cast<uint32_t>(b2 * a.R8 + r) * 16u;
         const uint32_t byte0 = static_cast<uint32_t>(seg * NB);
-        const uint32_t word = in ? lds32(sb + (byte0 & ~3u)) : 0u;
+        const uint32_t word = lds32(sb + (byte0 & ~3u));
         const uint32_t two = (word >> (8 * (byte0 & 3))) & (NB == 2 ? 0xFFFFu : 0xFFu);
         const uint32_t h2 = e4m3x2_to_f16x2(two);
-        sc[i][0] = half_bits_to_f32(h2 & 0xFFFFu) * pe;
-        if constexpr (NB == 2) sc[i][1] = half_bits_to_f32(h2 >> 16) * pe;
+        sc[i][0] = half_bits_to_f32(h2 & 0xFFFFu);
+        if constexpr (NB == 2) sc[i][1] = half_bits_to_f32(h2 >> 16);
     }
+    float u[kCcRows];
 #pragma unroll
     for (int blk = 0; blk < NB; ++blk) {
-        float s[kCcRows][2];
+        float s[kCcRows];
 #pragma unroll
-        for (int i = 0; i < kCcRows; ++i) s[i][0] = s[i][1] = 0.f;
+        for (int i = 0; i < kCcRows; ++i) s[i] = 0.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int wd = 2 * blk + h;
@@ -245,12 +270,15 @@ __device__ __forceinline__ void cc_stage(const CcArgs& a, uint32_t stage, int b2
             for (int j = 0; j < 4; ++j) {
                 const uint32_t xv = xw[wd * 4 + j];
 #pragma unroll
-                for (int i = 0; i < kCcRows; ++i) s[i][j & 1] = fma2_mixed<BF>(w[i][j], xv, s[i][j & 1]);
+                for (int i = 0; i < kCcRows; ++i) s[i] = fma2_mixed<BF>(w[i][j], xv, s[i]);
             }
         }
+        // scale the block sums exactly by the E4M3 scale, then by 2^-prescale
 #pragma unroll
-        for (int i = 0; i < kCcRows; ++i) acc[i] = fmaf(s[i][0] + s[i][1], sc[i][blk], acc[i]);
+        for (int i = 0; i < kCcRows; ++i) u[i] = blk == 0 ? s[i] * sc[i][0] : fmaf(s[i], sc[i][blk], u[i]);
     }
+#pragma unroll
+    for (int i = 0; i < kCcRows; ++i) acc[i] = fmaf(u[i], pe, acc[i]);
 }
 
 template <int EPI, int NSEG>
@@ -333,6 +361,10 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     }
 
     // ---------------------------------------------------------------- compute warps
+    {
+        const uint32_t roff[4] = {0u, a.scales_off, 0u, 0u}, rbytes[4] = {128u, 16u, 0u, 0u};
+        cc_zero_padding(a, smem, a.P * NGU, roff, rbytes, 2);
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     cc_convert<NSEG>(a, smem, warp, lane);
     named_barrier_sync(1, kCcThreads);
@@ -520,8 +552,7 @@ __device__ __forceinline__ void cc_stage_q45(const CcArgs& a, uint32_t stage, in
     const int grp = NSEG == 8 ? seg : seg >> 1;
 #pragma unroll
     for (int i = 0; i < kCcRows; ++i) {
-        const int r = row0 + i;
-        if (r >= a.R) break;
+        const int r = row0 + i;  // padding rows (r >= R) read as zeros
         const uint32_t rowi = static_cast<uint32_t>(b2 * a.R8 + r);
         const uint32_t chunk = static_cast<uint32_t>((NW == 4 ? seg : seg >> 1) ^ (r & 7));
         uint32_t cw[NW];
@@ -653,6 +684,10 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     }
 
     // ---------------------------------------------------------------- compute warps
+    {
+        const uint32_t roff[4] = {0u, a.scales_off, a.mins_off, a.hi_off}, rbytes[4] = {128u, 16u, 16u, 32u};
+        cc_zero_padding(a, smem, a.P, roff, rbytes, BITS == 5 ? 4 : 3);
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     cc_convert_q45<NSEG>(a, smem, warp, lane);
     named_barrier_sync(1, kCcThreads);
