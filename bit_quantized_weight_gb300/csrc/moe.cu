@@ -21,7 +21,10 @@ __global__ void route_kernel(const float* logits, int M, int E, int topk, int32_
     // and bit j of `taken` marks expert lane + 32 j as already selected
     float v[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = lane + 32 * j < E ? l[lane + 32 * j] : 0.f;
+    for (int j = 0; j < 32; ++j) {
+        if (32 * j >= E) break;
+        v[j] = lane + 32 * j < E ? l[lane + 32 * j] : 0.f;
+    }
     uint32_t taken = 0;
     float sel_l[8];
     int sel_id[8];
@@ -30,6 +33,7 @@ __global__ void route_kernel(const float* logits, int M, int E, int topk, int32_
         int best_id = 0x7FFFFFFF;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
+            if (32 * j >= E) break;  // the same for every lane
             const int e = lane + 32 * j;
             if (e >= E || ((taken >> j) & 1u)) continue;
             if (v[j] > best || (v[j] == best && e < best_id)) {
@@ -128,6 +132,7 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
     __shared__ int s_gu_at[kMaxPairs];    // gate/up group of sorted position i
     __shared__ int s_run0[kMaxPairs];     // first sorted position of that group's expert run
     __shared__ int s_dn_start[kMaxPairs]; // sorted position starting each down group
+    __shared__ int s_gu_e[kMaxPairs], s_dn_e[kMaxPairs];  // expert of each group
     __shared__ int s_nv, s_n_gu, s_n_dn;
     const int P = M * topk;
     const int tid = threadIdx.x;
@@ -158,22 +163,46 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
         s_nv = nv;
     }
     __syncthreads();
-    // group boundaries along the sorted pairs (at most 64: one thread scans)
-    if (tid == 0) {
+    // group boundaries along the sorted pairs (at most 64 positions: the
+    // first two warps, one position per lane, ballots for the prefix counts)
+    if (tid < 64) {
         const int nv = s_nv;
-        int n_gu = 0, n_dn = 0, run0 = 0;
-        for (int i = 0; i < nv; ++i) {
-            const int e = s_pair_e[s_order[i]];
-            if (i == 0 || e != s_pair_e[s_order[i - 1]]) {
-                run0 = i;
-                ++n_gu;
+        const int i = tid;
+        const bool in = i < nv;
+        const int e = in ? s_pair_e[s_order[i]] : -1;
+        const bool run_start = in && (i == 0 || e != s_pair_e[s_order[i - 1]]);
+        // start of this position's run: the last run start at or before i
+        int run0 = 0;
+        for (int j = i; j >= 0 && in; --j)
+            if (j == 0 || s_pair_e[s_order[j]] != s_pair_e[s_order[j - 1]]) {
+                run0 = j;
+                break;
             }
-            s_gu_at[i] = n_gu - 1;
-            s_run0[i] = run0;
-            if ((i - run0) % 8 == 0) s_dn_start[n_dn++] = i;
+        const bool dn_start = in && ((i - run0) % 8 == 0);
+        const unsigned lanes_below = (1u << (tid & 31)) - 1u;
+        const unsigned rs = __ballot_sync(0xffffffffu, run_start), ds = __ballot_sync(0xffffffffu, dn_start);
+        s_run0[i] = run0;
+        // runs started at or before i, and down groups started before i, in this warp
+        const int my_gu = __popc(rs & lanes_below) + (run_start ? 1 : 0);
+        const int my_dn = __popc(ds & lanes_below);
+        // positions 32..63 add the first warp's totals
+        __shared__ int s_part[2][2];
+        if ((tid & 31) == 31) {
+            s_part[tid >> 5][0] = __popc(rs);
+            s_part[tid >> 5][1] = __popc(ds);
         }
-        s_n_gu = n_gu;
-        s_n_dn = n_dn;
+        asm volatile("bar.sync 3, 64;" ::: "memory");
+        const int base_gu = tid >= 32 ? s_part[0][0] : 0, base_dn = tid >= 32 ? s_part[0][1] : 0;
+        if (in) {
+            s_gu_at[i] = base_gu + my_gu - 1;
+            if (dn_start) s_dn_start[base_dn + my_dn] = i;
+            if (run_start) s_gu_e[base_gu + my_gu - 1] = e;
+            if (dn_start) s_dn_e[base_dn + my_dn] = e;
+        }
+        if (tid == 0) {
+            s_n_gu = s_part[0][0] + s_part[1][0];
+            s_n_dn = s_part[0][1] + s_part[1][1];
+        }
     }
     __syncthreads();
     const int nv = s_nv;
@@ -235,7 +264,7 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
         const int gi = u / per_gu, rb = u % per_gu;
         UnitDesc d;
         d.grp = gi;
-        d.w_row0 = g_gu[gi].e * 2 * I + rb * r_gu;
+        d.w_row0 = s_gu_e[gi] * 2 * I + rb * r_gu;
         d.rows = r_gu;
         d.out_col0 = rb * r_gu;
         u_gu[u] = d;
@@ -244,7 +273,7 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
         const int gi = u / per_dn, rb = u % per_dn;
         UnitDesc d;
         d.grp = gi;
-        d.w_row0 = g_dn[gi].e * H + rb * r_dn;
+        d.w_row0 = s_dn_e[gi] * H + rb * r_dn;
         d.rows = r_dn;
         d.out_col0 = rb * r_dn;
         u_dn[u] = d;
