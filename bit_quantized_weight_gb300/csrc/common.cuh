@@ -251,6 +251,33 @@ __device__ __forceinline__ int prescale_exponent(uint32_t mag)
     return 147 - lg;
 }
 
+// Range of bf16 magnitudes (15-bit patterns) over 32-bit words of two bf16
+// values each, both halves at once with 16-bit SIMD min/max: mx2 collects
+// the largest magnitude with non-finite ones counted as the largest finite
+// (0x7F7F), mn2 the smallest magnitude minus one (zero wraps to 0xFFFF and
+// drops out). A chunk holding inf or NaN thus takes the prescale of 0x7F7F,
+// which its other values do not survive exactly, so it is flagged and runs on
+// raw bf16 (still exact); a borrow from the low into the high half can only
+// lower the minimum, which makes the exactness test stricter, never looser.
+__device__ __forceinline__ void bf16_range_acc(uint32_t w, uint32_t& mx2, uint32_t& mn2)
+{
+    const uint32_t m = w & 0x7FFF7FFFu;
+    mx2 = __vmaxu2(mx2, __vminu2(m, 0x7F7F7F7Fu));
+    mn2 = __vminu2(mn2, m - 0x00010001u);
+}
+
+// Exponent fields of the largest magnitude and of the smallest nonzero one
+// (255 when there is none), and the largest magnitude itself, from the
+// accumulators of bf16_range_acc.
+__device__ __forceinline__ void bf16_range_fin(uint32_t mx2, uint32_t mn2, uint32_t& emax, uint32_t& emin,
+                                               uint32_t& magmax)
+{
+    magmax = max(mx2 & 0xFFFFu, mx2 >> 16);
+    const uint32_t mn = min(mn2 & 0xFFFFu, mn2 >> 16) + 1u;  // 0x10000: no nonzero value
+    emax = magmax >> 7;
+    emin = mn > 0x7FFFu ? 255u : min(mn >> 7, 255u);
+}
+
 // Exact f16x2 -> bf16x2 for values with at most 8 significant bits in the
 // bf16 normal range (the decoded weights): through fp32, both steps exact.
 __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h2)

@@ -151,17 +151,11 @@ __device__ void cc_convert(const CcArgs& a, uint8_t* smem, int warp, int lane)
             const int kc = base + u * kCcWarps;
             if (kc >= a.C) break;
             const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-            uint32_t emax = 0, emin = 255, magmax = 0;
+            uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t mg = ((i & 1) ? (wv[i >> 1] >> 16) : wv[i >> 1]) & 0x7FFFu;
-                const uint32_t ef = mg >> 7;
-                if (ef != 255u) {
-                    emax = max(emax, ef);
-                    magmax = max(magmax, mg);
-                    if (mg != 0u) emin = min(emin, ef);
-                }
-            }
+            for (int i = 0; i < 4; ++i) bf16_range_acc(wv[i], mx2, mn2);
+            uint32_t emax, emin, magmax;
+            bf16_range_fin(mx2, mn2, emax, emin, magmax);
             emax = __reduce_max_sync(0xffffffffu, emax);
             emin = __reduce_min_sync(0xffffffffu, emin);
             if (emax == 0u) magmax = __reduce_max_sync(0xffffffffu, magmax);
@@ -481,20 +475,14 @@ __device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lan
             const int kc = base + u * kCcWarps;
             if (kc >= a.C) break;
             const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-            uint32_t emax = 0, emin = 255, magmax = 0;
             float sx = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t hb = (i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu);
-                sx += bf16_bits_to_f32(hb);
-                const uint32_t mg = hb & 0x7FFFu;
-                const uint32_t ef = mg >> 7;
-                if (ef != 255u) {
-                    emax = max(emax, ef);
-                    magmax = max(magmax, mg);
-                    if (mg != 0u) emin = min(emin, ef);
-                }
-            }
+            for (int i = 0; i < 8; ++i) sx += bf16_bits_to_f32((i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu));
+            uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) bf16_range_acc(wv[i], mx2, mn2);
+            uint32_t emax, emin, magmax;
+            bf16_range_fin(mx2, mn2, emax, emin, magmax);
 #pragma unroll
             for (int sh = 1; sh < PPS; sh <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, sh);
             emax = __reduce_max_sync(0xffffffffu, emax);

@@ -327,21 +327,16 @@ __device__ void tc_convert(const TcArgs& a, uint8_t* smem, int c0, int nst, int 
             uint4 raw[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) raw[i] = src ? ldg_nc_128(xs + (kq + 4 * i) * 8) : make_uint4(0, 0, 0, 0);
-            uint32_t emax = 0, emin = 255, magmax = 0;
+            uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                    const uint32_t mg = ((h & 1) ? (wv[h >> 1] >> 16) : wv[h >> 1]) & 0x7FFFu;
-                    const uint32_t ef = mg >> 7;
-                    if (ef != 255u) {
-                        emax = max(emax, ef);
-                        magmax = max(magmax, mg);
-                        if (mg != 0u) emin = min(emin, ef);
-                    }
-                }
+                bf16_range_acc(raw[i].x, mx2, mn2);
+                bf16_range_acc(raw[i].y, mx2, mn2);
+                bf16_range_acc(raw[i].z, mx2, mn2);
+                bf16_range_acc(raw[i].w, mx2, mn2);
             }
+            uint32_t emax, emin, magmax;
+            bf16_range_fin(mx2, mn2, emax, emin, magmax);
 #pragma unroll
             for (int sh = 8; sh <= 16; sh <<= 1) {
                 emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, sh));
@@ -382,17 +377,11 @@ __device__ void tc_convert(const TcArgs& a, uint8_t* smem, int c0, int nst, int 
             const int it = base + u * kTcDecodeWarps;
             if (it >= items) break;
             const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-            uint32_t emax = 0, emin = 255, magmax = 0;
+            uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t mg = ((i & 1) ? (wv[i >> 1] >> 16) : wv[i >> 1]) & 0x7FFFu;
-                const uint32_t ef = mg >> 7;
-                if (ef != 255u) {
-                    emax = max(emax, ef);
-                    magmax = max(magmax, mg);
-                    if (mg != 0u) emin = min(emin, ef);
-                }
-            }
+            for (int i = 0; i < 4; ++i) bf16_range_acc(wv[i], mx2, mn2);
+            uint32_t emax, emin, magmax;
+            bf16_range_fin(mx2, mn2, emax, emin, magmax);
             emax = __reduce_max_sync(0xffffffffu, emax);
             emin = __reduce_min_sync(0xffffffffu, emin);
             // a subnormal largest value needs its full magnitude (rare)
