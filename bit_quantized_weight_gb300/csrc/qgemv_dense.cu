@@ -456,24 +456,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int m = it % ntok, j = it / ntok;
                         const uint32_t wv[4] = {raw[uu].x, raw[uu].y, raw[uu].z, raw[uu].w};
                         uint32_t hbits[8];
-                        uint32_t mag = 0;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            hbits[i] = (i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu);
-                            const uint32_t mg = hbits[i] & 0x7FFFu;
-                            if (mg < 0x7F80u) mag = max(mag, mg);
-                        }
+                        for (int i = 0; i < 8; ++i) hbits[i] = (i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu);
+                        // prescale from the largest magnitude (at most 126, so 2^p
+                        // is a normal float); exact in f16 if the smallest
+                        // nonzero value keeps its 8 bits at or above 2^-24
+                        uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu, emax, emin, mag;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) bf16_range_acc(wv[i], mx2, mn2);
+                        bf16_range_fin(mx2, mn2, emax, emin, mag);
                         mag = __reduce_max_sync(0xffffffffu, mag);
-                        const int p = prescale_exponent(mag);
+                        emin = __reduce_min_sync(0xffffffffu, emin);
+                        const int p = min(prescale_exponent(mag), 126);
+                        const bool exact = emin == 255u || static_cast<int>(emin) - 127 + p >= -17;
+                        const float sp = __int_as_float((127 + p) << 23);
                         uint32_t h[8];
-                        bool exact = true;
                         float ls = 0.f;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
-                            const float v = ldexp_exact(bf16_bits_to_f32(hbits[i]), p);
-                            const __half hv = __float2half_rn(v);
-                            h[i] = __half_as_ushort(hv);
-                            if (isfinite(v) && __half2float(hv) != v) exact = false;
+                            const float v = bf16_bits_to_f32(hbits[i]) * sp;
+                            h[i] = __half_as_ushort(__float2half_rn(v));
                             ls += v;
                         }
                         const uint32_t off = (static_cast<uint32_t>(m) * a.x_pitch + j * kChunkK + lane * 8) * 2;
