@@ -240,6 +240,7 @@ class Workload:
         # -------- device buffers
         self.d_in = torch.from_numpy(host_in.view(np.int16)).view(torch.bfloat16).to(dev)
         self.d_out = torch.empty(self.out_elems, dtype=torch.bfloat16, device=dev)
+        self._views = {}
         l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 * 2 ** 20)
         self.l2_bytes = int(l2)
         self.copies = max(2, math.ceil(copies_min_bytes * self.l2_bytes / max(self.weight_bytes, 1)))
@@ -264,12 +265,19 @@ class Workload:
                 "min": t(w["min"].view(np.int16)).view(torch.float16), "bits": w["bits"]}
 
     def view_in(self, key):
-        o, shp = self.in_layout[key]
-        return self.d_in[o:o + shp[0] * shp[1]].view(shp)
+        # views are made once: a caller holds its tensors, it does not re-slice
+        v = self._views.get(("in", key))
+        if v is None:
+            o, shp = self.in_layout[key]
+            v = self._views[("in", key)] = self.d_in[o:o + shp[0] * shp[1]].view(shp)
+        return v
 
     def view_out(self, name):
-        o, shp = self.out_layout[name]
-        return self.d_out[o:o + shp[0] * shp[1]].view(shp)
+        v = self._views.get(("out", name))
+        if v is None:
+            o, shp = self.out_layout[name]
+            v = self._views[("out", name)] = self.d_out[o:o + shp[0] * shp[1]].view(shp)
+        return v
 
     def kernel_names(self):
         return [p[0] for p in self.projs]

@@ -80,13 +80,26 @@ def _check(name, status):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # ctypes converts a Python int for a c_void_p argument
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream=None):
+_raw_stream = None
+
+
+def _stream(stream=None, like=None):
+    """The stream handle: `stream`'s, else the current stream of the device
+    of tensor `like` (else of the current device)."""
+    global _raw_stream
+    if stream is not None:
+        return stream.cuda_stream
     import torch
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if _raw_stream is None:
+        _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None) or False
+    if _raw_stream:
+        dev = like.get_device() if like is not None else torch.cuda.current_device()
+        return _raw_stream(dev)
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _cuda(*ts):
@@ -103,7 +116,7 @@ def qgemv_nvfp4(codes, scales, g, x, y, residual=None, stream=None):
     N = codes.shape[0]
     out = QG_OUT_F32 if y.dtype == torch.float32 else QG_OUT_BF16
     _check("qgemv_nvfp4", lib().qgemv_nvfp4(_ptr(codes), _ptr(scales), float(g), _ptr(x), _ptr(y), out,
-                                            _ptr(residual), M, N, K, _stream(stream)))
+                                            _ptr(residual), M, N, K, _stream(stream, y)))
     return y
 
 
@@ -114,7 +127,7 @@ def qgemv_q45(q_lo, q_hi, scale, mn, bits, x, y, residual=None, stream=None):
     N = q_lo.shape[0]
     out = QG_OUT_F32 if y.dtype == torch.float32 else QG_OUT_BF16
     _check("qgemv_q45", lib().qgemv_q45(_ptr(q_lo), _ptr(q_hi), _ptr(scale), _ptr(mn), int(bits), _ptr(x),
-                                        _ptr(y), out, _ptr(residual), M, N, K, _stream(stream)))
+                                        _ptr(y), out, _ptr(residual), M, N, K, _stream(stream, y)))
     return y
 
 
@@ -123,7 +136,7 @@ def qgemv_swiglu_nvfp4(codes, scales, g, x, y, stream=None):
     M, K = x.shape
     N = codes.shape[0]
     _check("qgemv_swiglu_nvfp4", lib().qgemv_swiglu_nvfp4(_ptr(codes), _ptr(scales), float(g), _ptr(x),
-                                                          _ptr(y), M, N, K, _stream(stream)))
+                                                          _ptr(y), M, N, K, _stream(stream, y)))
     return y
 
 
