@@ -87,15 +87,16 @@ struct MoeLayout {
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
-// Rows per unit: the gate/up launch walks (expert, 32-row block) units and the
-// down launch (expert, 128-row block) units (smaller blocks where H or I
-// need them), so the ~50 active experts spread evenly over the SMs.
+// Rows per unit: the gate/up launch walks (expert, 64-row block) units (64
+// gate plus 64 up rows fill one 128-lane accumulator) and the down launch
+// (expert, 128-row block) units, so the ~50 active experts spread evenly over
+// the SMs. H and I are multiples of 256, so both divide evenly.
 MoeLayout moe_layout(int M, int topk, int H, int I)
 {
     MoeLayout L{};
     const size_t P = static_cast<size_t>(M) * topk;
-    L.r_gu = 32;
-    L.r_dn = (H % 128 == 0) ? 128 : 64;
+    L.r_gu = 64;
+    L.r_dn = 128;
     L.units_gu_max = kMaxPairs * (I / L.r_gu);
     L.units_dn_max = kMaxPairs * (H / L.r_dn);
     size_t o = 0;

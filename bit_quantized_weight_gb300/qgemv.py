@@ -144,7 +144,7 @@ def moe_route_topk(logits, topk, ids, w, stream=None):
     _cuda(logits, ids, w)
     M, E = logits.shape
     _check("moe_route_topk", lib().moe_route_topk(_ptr(logits), M, E, int(topk), _ptr(ids), _ptr(w),
-                                                  _stream(stream)))
+                                                  _stream(stream, logits)))
     return ids, w
 
 
@@ -164,7 +164,7 @@ def moe_qgemv_nvfp4(gu_codes, gu_scales, gu_g, dn_codes, dn_scales, dn_g, x, ids
     _check("moe_qgemv_nvfp4", lib().moe_qgemv_nvfp4(
         _ptr(gu_codes), _ptr(gu_scales), _ptr(gu_g), _ptr(dn_codes), _ptr(dn_scales), _ptr(dn_g), _ptr(x),
         _ptr(ids), _ptr(w), _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        M, H, two_i // 2, E, topk, _stream(stream)))
+        M, H, two_i // 2, E, topk, _stream(stream, y)))
     return y
 
 
@@ -177,7 +177,7 @@ def moe_qgemv_nvfp4_noalloc(gu_codes, gu_scales, gu_g, dn_codes, dn_scales, dn_g
     topk = ids.shape[1]
     _check("moe_qgemv_nvfp4_noalloc", lib().moe_qgemv_nvfp4_noalloc(
         _ptr(gu_codes), _ptr(gu_scales), _ptr(gu_g), _ptr(dn_codes), _ptr(dn_scales), _ptr(dn_g), _ptr(x),
-        _ptr(ids), _ptr(w), _ptr(y), M, H, two_i // 2, E, topk, _stream(stream)))
+        _ptr(ids), _ptr(w), _ptr(y), M, H, two_i // 2, E, topk, _stream(stream, y)))
     return y
 
 
@@ -185,7 +185,7 @@ def qdequant_nvfp4(codes, scales, g, w, stream=None):
     _cuda(codes, scales, w)
     N, K = w.shape
     _check("qdequant_nvfp4", lib().qdequant_nvfp4(_ptr(codes), _ptr(scales), float(g), _ptr(w), N, K,
-                                                  _stream(stream)))
+                                                  _stream(stream, w)))
     return w
 
 
@@ -193,7 +193,7 @@ def qdequant_q45(q_lo, q_hi, scale, mn, bits, w, stream=None):
     _cuda(q_lo, q_hi, scale, mn, w)
     N, K = w.shape
     _check("qdequant_q45", lib().qdequant_q45(_ptr(q_lo), _ptr(q_hi), _ptr(scale), _ptr(mn), int(bits),
-                                              _ptr(w), N, K, _stream(stream)))
+                                              _ptr(w), N, K, _stream(stream, w)))
     return w
 
 
