@@ -130,12 +130,14 @@ __device__ __forceinline__ float fma2_mixed(uint32_t w, uint32_t x, float acc)
 // or above 2^-24). Within a chunk, 16-byte piece p of k segment s (NSEG
 // segments of KS values) sits at p * NSEG * 16 + s * 16, so the segments'
 // i-th pieces are contiguous and one load instruction of 8 threads with 8
-// segments touches 8 different bank groups.
+// segments touches 8 different bank groups. A chunk kept raw sets *any_bf.
+// Each warp issues the loads of up to kBatch chunks before converting, so K
+// up to 80 chunks costs one round trip to memory.
 template <int NSEG>
-__device__ void cc_convert(const CcArgs& a, uint8_t* smem, int warp, int lane)
+__device__ void cc_convert(const CcArgs& a, uint8_t* smem, int warp, int lane, volatile int* any_bf)
 {
     constexpr int PPS = kChunkK / NSEG / 8;  // 16-byte pieces per segment
-    constexpr int kBatch = 4;
+    constexpr int kBatch = 5;
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
     float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
     uint8_t* fl = smem + a.smem_fl;
@@ -176,6 +178,7 @@ __device__ void cc_convert(const CcArgs& a, uint8_t* smem, int warp, int lane)
             if (lane == 0) {
                 pe[kc] = inexact ? 1.0f : __int_as_float((127 - e) << 23);
                 fl[kc] = inexact ? 1 : 0;
+                if (inexact) *any_bf = 1;
             }
         }
     }
@@ -275,13 +278,101 @@ __device__ __forceinline__ void cc_stage(const CcArgs& a, uint32_t stage, int b2
     for (int i = 0; i < kCcRows; ++i) acc[i] = fmaf(u[i], pe, acc[i]);
 }
 
+// The compute warps' unit loop. MIXED: some chunk of x stayed raw bf16, so
+// each stage picks the f16 or the bf16 stage code; otherwise the loop holds
+// the f16 stage code alone.
+template <int EPI, int NSEG, bool MIXED>
+__device__ __forceinline__ void cc_units(const CcArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                         volatile int* abort_flag, int lane)
+{
+    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
+    constexpr int KS = kChunkK / NSEG;
+    // this thread's rows and segment: item = (box, row group, segment); the
+    // row groups cover rows 0 .. R rounded up to 4
+    const int rg_per_box = (a.R + kCcRows - 1) / kCcRows;
+    const int item = threadIdx.x;
+    const int seg = item % NSEG;
+    const int bg = item / NSEG;
+    const int b2 = bg / rg_per_box;
+    const int row0 = (bg % rg_per_box) * kCcRows;
+    const bool active = b2 < a.P * NGU;
+    const int p = active ? b2 / NGU : 0;
+    const uint32_t* xs = reinterpret_cast<const uint32_t*>(smem + a.smem_x);
+    const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
+    const uint8_t* fl = smem + a.smem_fl;
+    float* red = reinterpret_cast<float*>(smem + a.smem_red);
+    const uint32_t ring = smem_u32(smem + a.smem_ring);
+
+    bool aborted = false;
+    int slot = 0, lap = 0;
+    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+        float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
+        for (int c = 0; c < a.Cp; ++c) {
+            if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
+            const int kc = p * a.Cp + c;
+            if (!aborted && active && kc < a.C) {
+                const uint32_t stage = ring + slot * a.stage_bytes;
+                uint32_t xw[KS / 2];
+                const uint32_t* xc = xs + kc * (kChunkK / 2) + seg * 4;
+#pragma unroll
+                for (int i = 0; i < KS / 8; ++i) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(xc + i * NSEG * 4);
+                    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
+                }
+                if (!MIXED || fl[kc] == 0)
+                    cc_stage<NSEG, false>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
+                else
+                    cc_stage<NSEG, true>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (++slot == a.n_stages) {
+                slot = 0;
+                ++lap;
+            }
+        }
+
+        // ---------------- fixed-order reduction over segments (a butterfly
+        // across the segment lanes of the warp) and phases, epilogue
+#pragma unroll
+        for (int i = 0; i < kCcRows; ++i)
+#pragma unroll
+            for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+        if (active && seg == 0) {
+#pragma unroll
+            for (int i = 0; i < kCcRows; ++i) red[b2 * a.R8 + row0 + i] = acc[i];
+        }
+        named_barrier_sync(1, kCcThreads);
+        if (!aborted) {
+            const int r0 = u * a.R;
+            for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
+                if (r0 + r >= a.n_out) break;
+                float v[NGU];
+#pragma unroll
+                for (int gg = 0; gg < NGU; ++gg) {
+                    float s = 0.f;
+                    for (int pp = 0; pp < a.P; ++pp) s += red[(pp * NGU + gg) * a.R8 + r];
+                    v[gg] = s * a.g;
+                }
+                float val = v[0];
+                if (EPI == EPI_SWIGLU) val = (val / (1.0f + expf(-val))) * v[NGU - 1];
+                if (EPI == EPI_RESID) val += bf16_bits_to_f32(a.residual[r0 + r]);
+                if (a.out_f32)
+                    reinterpret_cast<float*>(a.y)[r0 + r] = val;
+                else
+                    reinterpret_cast<uint16_t*>(a.y)[r0 + r] = f32_to_bf16_bits_rn(val);
+            }
+        }
+        named_barrier_sync(1, kCcThreads);  // red is rewritten by the next unit
+    }
+}
+
 template <int EPI, int NSEG>
 __global__ void __launch_bounds__(kCcAllThreads, 1)
     cc_gemv_kernel(const __grid_constant__ CcArgs a, const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales)
 {
     constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
-    constexpr int KS = kChunkK / NSEG;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = warp_index_uniform();
     const int lane = threadIdx.x & 31;
@@ -289,6 +380,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.smem_bar);
     uint64_t* empty = full + kCcMaxStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCcMaxStages);
+    volatile int* any_bf = abort_flag + 1;  // some chunk of x kept raw bf16
 
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
@@ -297,6 +389,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
             mbar_init(&empty[s], kCcWarps);
         }
         *abort_flag = 0;
+        *any_bf = 0;
         fence_barrier_init();
     }
     __syncthreads();
@@ -360,86 +453,12 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
         cc_zero_padding(a, smem, a.P * NGU, roff, rbytes, 2);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    cc_convert<NSEG>(a, smem, warp, lane);
+    cc_convert<NSEG>(a, smem, warp, lane, any_bf);
     named_barrier_sync(1, kCcThreads);
-
-    // this thread's rows and segment: item = (box, row group, segment)
-    const int rg_per_box = a.R8 / kCcRows;
-    const int item = threadIdx.x;
-    const int seg = item % NSEG;
-    const int bg = item / NSEG;
-    const int b2 = bg / rg_per_box;
-    const int row0 = (bg % rg_per_box) * kCcRows;
-    const bool active = b2 < a.P * NGU;
-    const int p = active ? b2 / NGU : 0;
-    const uint32_t* xs = reinterpret_cast<const uint32_t*>(smem + a.smem_x);
-    const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
-    const uint8_t* fl = smem + a.smem_fl;
-    float* red = reinterpret_cast<float*>(smem + a.smem_red);
-    const uint32_t ring = smem_u32(smem + a.smem_ring);
-
-    bool aborted = false;
-    int slot = 0, lap = 0;
-    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
-        float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
-        for (int c = 0; c < a.Cp; ++c) {
-            if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
-            const int kc = p * a.Cp + c;
-            if (!aborted && active && kc < a.C) {
-                const uint32_t stage = ring + slot * a.stage_bytes;
-                uint32_t xw[KS / 2];
-                const uint32_t* xc = xs + kc * (kChunkK / 2) + seg * 4;
-#pragma unroll
-                for (int i = 0; i < KS / 8; ++i) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(xc + i * NSEG * 4);
-                    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
-                }
-                if (fl[kc] == 0)
-                    cc_stage<NSEG, false>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
-                else
-                    cc_stage<NSEG, true>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-            if (++slot == a.n_stages) {
-                slot = 0;
-                ++lap;
-            }
-        }
-
-        // ---------------- fixed-order reduction over segments (a butterfly
-        // across the segment lanes of the warp) and phases, epilogue
-#pragma unroll
-        for (int i = 0; i < kCcRows; ++i)
-#pragma unroll
-            for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
-        if (active && seg == 0) {
-#pragma unroll
-            for (int i = 0; i < kCcRows; ++i) red[b2 * a.R8 + row0 + i] = acc[i];
-        }
-        named_barrier_sync(1, kCcThreads);
-        if (!aborted) {
-            const int r0 = u * a.R;
-            for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
-                if (r0 + r >= a.n_out) break;
-                float v[NGU];
-#pragma unroll
-                for (int gg = 0; gg < NGU; ++gg) {
-                    float s = 0.f;
-                    for (int pp = 0; pp < a.P; ++pp) s += red[(pp * NGU + gg) * a.R8 + r];
-                    v[gg] = s * a.g;
-                }
-                float val = v[0];
-                if (EPI == EPI_SWIGLU) val = (val / (1.0f + expf(-val))) * v[NGU - 1];
-                if (EPI == EPI_RESID) val += bf16_bits_to_f32(a.residual[r0 + r]);
-                if (a.out_f32)
-                    reinterpret_cast<float*>(a.y)[r0 + r] = val;
-                else
-                    reinterpret_cast<uint16_t*>(a.y)[r0 + r] = f32_to_bf16_bits_rn(val);
-            }
-        }
-        named_barrier_sync(1, kCcThreads);  // red is rewritten by the next unit
-    }
+    if (*any_bf)
+        cc_units<EPI, NSEG, true>(a, smem, full, empty, abort_flag, lane);
+    else
+        cc_units<EPI, NSEG, false>(a, smem, full, empty, abort_flag, lane);
 }
 
 // ---------------------------------------------------------------- groupwise int (Q4 / Q5)
@@ -455,9 +474,9 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
 // Converts x as cc_convert does, with the (k, k+4) pairing, and writes the
 // fp32 sum of each segment's original values.
 template <int NSEG>
-__device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lane)
+__device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lane, volatile int* any_bf)
 {
-    constexpr int kBatch = 4;
+    constexpr int kBatch = 5;
     constexpr int PPS = kChunkK / NSEG / 8;  // lanes (16-byte pieces) per segment
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
     float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
@@ -509,6 +528,7 @@ __device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lan
             if (lane == 0) {
                 pe[kc] = inexact ? 1.0f : __int_as_float((127 - e) << 23);
                 fl[kc] = inexact ? 1 : 0;
+                if (inexact) *any_bf = 1;
             }
         }
     }
@@ -592,13 +612,95 @@ __device__ __forceinline__ void cc_stage_q45(const CcArgs& a, uint32_t stage, in
     }
 }
 
+// The compute warps' unit loop of the groupwise-int kernel (MIXED as in
+// cc_units).
+template <int BITS, int EPI, int NSEG, bool MIXED>
+__device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                             volatile int* abort_flag, int lane)
+{
+    constexpr int KS = kChunkK / NSEG;
+    // item = (box, row group, segment); the row groups cover rows 0 .. R
+    // rounded up to 4
+    const int rg_per_box = (a.R + kCcRows - 1) / kCcRows;
+    const int item = threadIdx.x;
+    const int seg = item % NSEG;
+    const int bg = item / NSEG;
+    const int b2 = bg / rg_per_box;
+    const int row0 = (bg % rg_per_box) * kCcRows;
+    const bool active = b2 < a.P;
+    const int p = active ? b2 : 0;
+    const uint32_t* xs = reinterpret_cast<const uint32_t*>(smem + a.smem_x);
+    const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
+    const float* gx = reinterpret_cast<const float*>(smem + a.smem_gx);
+    const uint8_t* fl = smem + a.smem_fl;
+    float* red = reinterpret_cast<float*>(smem + a.smem_red);
+    const uint32_t ring = smem_u32(smem + a.smem_ring);
+
+    bool aborted = false;
+    int slot = 0, lap = 0;
+    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+        float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
+        for (int c = 0; c < a.Cp; ++c) {
+            if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
+            const int kc = p * a.Cp + c;
+            if (!aborted && active && kc < a.C) {
+                const uint32_t stage = ring + slot * a.stage_bytes;
+                uint32_t xw[KS / 2];
+                const uint32_t* xc = xs + kc * (kChunkK / 2) + seg * 4;
+#pragma unroll
+                for (int i = 0; i < KS / 8; ++i) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(xc + i * NSEG * 4);
+                    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
+                }
+                const float gxs = gx[kc * NSEG + seg];
+                if (!MIXED || fl[kc] == 0)
+                    cc_stage_q45<NSEG, BITS, false>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                else
+                    cc_stage_q45<NSEG, BITS, true>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (++slot == a.n_stages) {
+                slot = 0;
+                ++lap;
+            }
+        }
+
+        // ---------------- fixed-order reduction over segments (a butterfly
+        // across the segment lanes of the warp) and phases, epilogue
+#pragma unroll
+        for (int i = 0; i < kCcRows; ++i)
+#pragma unroll
+            for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+        if (active && seg == 0) {
+#pragma unroll
+            for (int i = 0; i < kCcRows; ++i) red[b2 * a.R8 + row0 + i] = acc[i];
+        }
+        named_barrier_sync(1, kCcThreads);
+        if (!aborted) {
+            const int r0 = u * a.R;
+            for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
+                if (r0 + r >= a.n_out) break;
+                float s = 0.f;
+                for (int pp = 0; pp < a.P; ++pp) s += red[pp * a.R8 + r];
+                float val = s;
+                if (EPI == EPI_RESID) val += bf16_bits_to_f32(a.residual[r0 + r]);
+                if (a.out_f32)
+                    reinterpret_cast<float*>(a.y)[r0 + r] = val;
+                else
+                    reinterpret_cast<uint16_t*>(a.y)[r0 + r] = f32_to_bf16_bits_rn(val);
+            }
+        }
+        named_barrier_sync(1, kCcThreads);
+    }
+}
+
 template <int BITS, int EPI, int NSEG>
 __global__ void __launch_bounds__(kCcAllThreads, 1)
     cc_q45_kernel(const __grid_constant__ CcArgs a, const __grid_constant__ CUtensorMap tm_codes,
                   const __grid_constant__ CUtensorMap tm_scales, const __grid_constant__ CUtensorMap tm_mins,
                   const __grid_constant__ CUtensorMap tm_hi)
 {
-    constexpr int KS = kChunkK / NSEG;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = warp_index_uniform();
     const int lane = threadIdx.x & 31;
@@ -606,6 +708,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.smem_bar);
     uint64_t* empty = full + kCcMaxStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCcMaxStages);
+    volatile int* any_bf = abort_flag + 1;  // some chunk of x kept raw bf16
 
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
@@ -614,6 +717,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
             mbar_init(&empty[s], kCcWarps);
         }
         *abort_flag = 0;
+        *any_bf = 0;
         fence_barrier_init();
     }
     __syncthreads();
@@ -677,82 +781,14 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
         cc_zero_padding(a, smem, a.P, roff, rbytes, BITS == 5 ? 4 : 3);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    cc_convert_q45<NSEG>(a, smem, warp, lane);
+    cc_convert_q45<NSEG>(a, smem, warp, lane, any_bf);
     named_barrier_sync(1, kCcThreads);
-
-    const int rg_per_box = a.R8 / kCcRows;
-    const int item = threadIdx.x;
-    const int seg = item % NSEG;
-    const int bg = item / NSEG;
-    const int b2 = bg / rg_per_box;
-    const int row0 = (bg % rg_per_box) * kCcRows;
-    const bool active = b2 < a.P;
-    const int p = active ? b2 : 0;
-    const uint32_t* xs = reinterpret_cast<const uint32_t*>(smem + a.smem_x);
-    const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
-    const float* gx = reinterpret_cast<const float*>(smem + a.smem_gx);
-    const uint8_t* fl = smem + a.smem_fl;
-    float* red = reinterpret_cast<float*>(smem + a.smem_red);
-    const uint32_t ring = smem_u32(smem + a.smem_ring);
-
-    bool aborted = false;
-    int slot = 0, lap = 0;
-    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
-        float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
-        for (int c = 0; c < a.Cp; ++c) {
-            if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
-            const int kc = p * a.Cp + c;
-            if (!aborted && active && kc < a.C) {
-                const uint32_t stage = ring + slot * a.stage_bytes;
-                uint32_t xw[KS / 2];
-                const uint32_t* xc = xs + kc * (kChunkK / 2) + seg * 4;
-#pragma unroll
-                for (int i = 0; i < KS / 8; ++i) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(xc + i * NSEG * 4);
-                    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
-                }
-                const float gxs = gx[kc * NSEG + seg];
-                if (fl[kc] == 0)
-                    cc_stage_q45<NSEG, BITS, false>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
-                else
-                    cc_stage_q45<NSEG, BITS, true>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-            if (++slot == a.n_stages) {
-                slot = 0;
-                ++lap;
-            }
-        }
-
-        // ---------------- fixed-order reduction over segments (a butterfly
-        // across the segment lanes of the warp) and phases, epilogue
-#pragma unroll
-        for (int i = 0; i < kCcRows; ++i)
-#pragma unroll
-            for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
-        if (active && seg == 0) {
-#pragma unroll
-            for (int i = 0; i < kCcRows; ++i) red[b2 * a.R8 + row0 + i] = acc[i];
-        }
-        named_barrier_sync(1, kCcThreads);
-        if (!aborted) {
-            const int r0 = u * a.R;
-            for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
-                if (r0 + r >= a.n_out) break;
-                float s = 0.f;
-                for (int pp = 0; pp < a.P; ++pp) s += red[pp * a.R8 + r];
-                float val = s;
-                if (EPI == EPI_RESID) val += bf16_bits_to_f32(a.residual[r0 + r]);
-                if (a.out_f32)
-                    reinterpret_cast<float*>(a.y)[r0 + r] = val;
-                else
-                    reinterpret_cast<uint16_t*>(a.y)[r0 + r] = f32_to_bf16_bits_rn(val);
-            }
-        }
-        named_barrier_sync(1, kCcThreads);
-    }
+    if (*any_bf)
+        cc_q45_units<BITS, EPI, NSEG, true>(a, smem, full, empty, abort_flag, lane);
+    else
+        cc_q45_units<BITS, EPI, NSEG, false>(a, smem, full, empty, abort_flag, lane);
 }
+
 
 constexpr uint32_t align_up(uint32_t v, uint32_t al) { return (v + al - 1) / al * al; }
 
@@ -823,7 +859,7 @@ qg_status cc_dispatch(const CcArgs& a, const CUtensorMap& tmc, const CUtensorMap
 {
     constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
     // 8 segments of 32 k when the rows fill 16 warps that way, else 16 of 16 k
-    const int items8 = a.P * NGU * (a.R8 / kCcRows) * 8;
+    const int items8 = a.P * NGU * ((a.R + kCcRows - 1) / kCcRows) * 8;
     if (items8 > kCcThreads / 2) return cc_launch<EPI, 8>(a, tmc, tms, grid, stream);
     return cc_launch<EPI, 16>(a, tmc, tms, grid, stream);
 }
@@ -896,7 +932,7 @@ qg_status cc_q45_launch(CcArgs a, const CUtensorMap (&maps)[4], int grid, cudaSt
 template <int BITS, int EPI>
 qg_status cc_q45_dispatch(const CcArgs& a, const CUtensorMap (&maps)[4], int grid, cudaStream_t stream)
 {
-    const int items8 = a.P * (a.R8 / kCcRows) * 8;
+    const int items8 = a.P * ((a.R + kCcRows - 1) / kCcRows) * 8;
     if (items8 > kCcThreads / 2) return cc_q45_launch<BITS, EPI, 8>(a, maps, grid, stream);
     return cc_q45_launch<BITS, EPI, 16>(a, maps, grid, stream);
 }
