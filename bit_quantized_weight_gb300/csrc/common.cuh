@@ -222,6 +222,20 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ uint32_t lds16(uint32_t addr)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds8(uint32_t addr)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint2 lds64(uint32_t addr)
 {
     uint2 v;

@@ -237,10 +237,8 @@ __device__ __forceinline__ void cc_stage(const CcArgs& a, uint32_t stage, int b2
             cw[i][0] = v.x; cw[i][1] = v.y;
         }
         // the NB scale bytes of this segment
-        const uint32_t sb = stage + a.scales_off + static_cast<uint32_t>(b2 * a.R8 + r) * 16u;
-        const uint32_t byte0 = static_cast<uint32_t>(seg * NB);
-        const uint32_t word = lds32(sb + (byte0 & ~3u));
-        const uint32_t two = (word >> (8 * (byte0 & 3))) & (NB == 2 ? 0xFFFFu : 0xFFu);
+        const uint32_t sb = stage + a.scales_off + static_cast<uint32_t>((b2 * a.R8 + r) * 16 + seg * NB);
+        const uint32_t two = NB == 2 ? lds16(sb) : lds8(sb);
         const uint32_t h2 = e4m3x2_to_f16x2(two);
         sc[i][0] = half_bits_to_f32(h2 & 0xFFFFu);
         if constexpr (NB == 2) sc[i][1] = half_bits_to_f32(h2 >> 16);
@@ -283,7 +281,7 @@ __device__ __forceinline__ void cc_stage(const CcArgs& a, uint32_t stage, int b2
 // the f16 stage code alone.
 template <int EPI, int NSEG, bool MIXED>
 __device__ __forceinline__ void cc_units(const CcArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                                         volatile int* abort_flag, int lane)
+                                         volatile int* abort_flag)
 {
     constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
     constexpr int KS = kChunkK / NSEG;
@@ -302,6 +300,10 @@ __device__ __forceinline__ void cc_units(const CcArgs& a, uint8_t* smem, uint64_
     const uint8_t* fl = smem + a.smem_fl;
     float* red = reinterpret_cast<float*>(smem + a.smem_red);
     const uint32_t ring = smem_u32(smem + a.smem_ring);
+    // this thread computes chunks kc0 .. kc0 + n_mine - 1 of every unit
+    const int kc0 = p * a.Cp;
+    const int n_mine = active ? max(0, min(a.Cp, a.C - kc0)) : 0;
+    const uint32_t x0 = smem_u32(xs + kc0 * (kChunkK / 2) + seg * 4);
 
     bool aborted = false;
     int slot = 0, lap = 0;
@@ -309,23 +311,22 @@ __device__ __forceinline__ void cc_units(const CcArgs& a, uint8_t* smem, uint64_
         float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
         for (int c = 0; c < a.Cp; ++c) {
             if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
-            const int kc = p * a.Cp + c;
-            if (!aborted && active && kc < a.C) {
+            if (!aborted && c < n_mine) {
                 const uint32_t stage = ring + slot * a.stage_bytes;
                 uint32_t xw[KS / 2];
-                const uint32_t* xc = xs + kc * (kChunkK / 2) + seg * 4;
+                const uint32_t xc = x0 + static_cast<uint32_t>(c) * (kChunkK * 2u);
 #pragma unroll
                 for (int i = 0; i < KS / 8; ++i) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(xc + i * NSEG * 4);
+                    const uint4 v = lds128(xc + i * NSEG * 16);
                     xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
                 }
-                if (!MIXED || fl[kc] == 0)
-                    cc_stage<NSEG, false>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
+                if (!MIXED || fl[kc0 + c] == 0)
+                    cc_stage<NSEG, false>(a, stage, b2, row0, seg, xw, pe_all[kc0 + c], acc);
                 else
-                    cc_stage<NSEG, true>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
+                    cc_stage<NSEG, true>(a, stage, b2, row0, seg, xw, pe_all[kc0 + c], acc);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
+            // every compute thread arrives: its own reads of the slot are done
+            mbar_arrive(&empty[slot]);
             if (++slot == a.n_stages) {
                 slot = 0;
                 ++lap;
@@ -386,7 +387,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.n_stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kCcWarps);
+            mbar_init(&empty[s], kCcThreads);
         }
         *abort_flag = 0;
         *any_bf = 0;
@@ -456,9 +457,9 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     cc_convert<NSEG>(a, smem, warp, lane, any_bf);
     named_barrier_sync(1, kCcThreads);
     if (*any_bf)
-        cc_units<EPI, NSEG, true>(a, smem, full, empty, abort_flag, lane);
+        cc_units<EPI, NSEG, true>(a, smem, full, empty, abort_flag);
     else
-        cc_units<EPI, NSEG, false>(a, smem, full, empty, abort_flag, lane);
+        cc_units<EPI, NSEG, false>(a, smem, full, empty, abort_flag);
 }
 
 // ---------------------------------------------------------------- groupwise int (Q4 / Q5)
@@ -574,13 +575,11 @@ __device__ __forceinline__ void cc_stage_q45(const CcArgs& a, uint32_t stage, in
         uint32_t hb = 0;
         if (BITS == 5) {
             // 4 (NSEG = 8) or 2 bytes of high bits, one per 8 k
-            const uint32_t hw = lds32(stage + a.hi_off + rowi * 32u + static_cast<uint32_t>(seg * NW) / 4u * 4u);
-            hb = NW == 4 ? hw : (hw >> (8 * ((seg * NW) & 3)));
+            const uint32_t ha = stage + a.hi_off + rowi * 32u + static_cast<uint32_t>(seg * NW);
+            hb = NW == 4 ? lds32(ha) : lds16(ha);
         }
-        const uint32_t sw = lds32(stage + a.scales_off + rowi * 16u + static_cast<uint32_t>(grp * 2) / 4u * 4u);
-        const uint32_t mw = lds32(stage + a.mins_off + rowi * 16u + static_cast<uint32_t>(grp * 2) / 4u * 4u);
-        const float sc = half_bits_to_f32((sw >> (16 * (grp & 1))) & 0xFFFFu);
-        const float mn = half_bits_to_f32((mw >> (16 * (grp & 1))) & 0xFFFFu);
+        const float sc = half_bits_to_f32(lds16(stage + a.scales_off + rowi * 16u + static_cast<uint32_t>(grp * 2)));
+        const float mn = half_bits_to_f32(lds16(stage + a.mins_off + rowi * 16u + static_cast<uint32_t>(grp * 2)));
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int wd = 0; wd < NW; ++wd) {
@@ -616,7 +615,7 @@ __device__ __forceinline__ void cc_stage_q45(const CcArgs& a, uint32_t stage, in
 // cc_units).
 template <int BITS, int EPI, int NSEG, bool MIXED>
 __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                                             volatile int* abort_flag, int lane)
+                                             volatile int* abort_flag)
 {
     constexpr int KS = kChunkK / NSEG;
     // item = (box, row group, segment); the row groups cover rows 0 .. R
@@ -635,6 +634,10 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
     const uint8_t* fl = smem + a.smem_fl;
     float* red = reinterpret_cast<float*>(smem + a.smem_red);
     const uint32_t ring = smem_u32(smem + a.smem_ring);
+    // this thread computes chunks kc0 .. kc0 + n_mine - 1 of every unit
+    const int kc0 = p * a.Cp;
+    const int n_mine = active ? max(0, min(a.Cp, a.C - kc0)) : 0;
+    const uint32_t x0 = smem_u32(xs + kc0 * (kChunkK / 2) + seg * 4);
 
     bool aborted = false;
     int slot = 0, lap = 0;
@@ -642,14 +645,14 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
         float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
         for (int c = 0; c < a.Cp; ++c) {
             if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
-            const int kc = p * a.Cp + c;
-            if (!aborted && active && kc < a.C) {
+            if (!aborted && c < n_mine) {
+                const int kc = kc0 + c;
                 const uint32_t stage = ring + slot * a.stage_bytes;
                 uint32_t xw[KS / 2];
-                const uint32_t* xc = xs + kc * (kChunkK / 2) + seg * 4;
+                const uint32_t xc = x0 + static_cast<uint32_t>(c) * (kChunkK * 2u);
 #pragma unroll
                 for (int i = 0; i < KS / 8; ++i) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(xc + i * NSEG * 4);
+                    const uint4 v = lds128(xc + i * NSEG * 16);
                     xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
                 }
                 const float gxs = gx[kc * NSEG + seg];
@@ -658,8 +661,8 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
                 else
                     cc_stage_q45<NSEG, BITS, true>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
+            // every compute thread arrives: its own reads of the slot are done
+            mbar_arrive(&empty[slot]);
             if (++slot == a.n_stages) {
                 slot = 0;
                 ++lap;
@@ -714,7 +717,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.n_stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kCcWarps);
+            mbar_init(&empty[s], kCcThreads);
         }
         *abort_flag = 0;
         *any_bf = 0;
@@ -784,9 +787,9 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     cc_convert_q45<NSEG>(a, smem, warp, lane, any_bf);
     named_barrier_sync(1, kCcThreads);
     if (*any_bf)
-        cc_q45_units<BITS, EPI, NSEG, true>(a, smem, full, empty, abort_flag, lane);
+        cc_q45_units<BITS, EPI, NSEG, true>(a, smem, full, empty, abort_flag);
     else
-        cc_q45_units<BITS, EPI, NSEG, false>(a, smem, full, empty, abort_flag, lane);
+        cc_q45_units<BITS, EPI, NSEG, false>(a, smem, full, empty, abort_flag);
 }
 
 
