@@ -21,13 +21,14 @@
 //
 // Work split. As in the tensor-core kernel, a CTA owns units of R output
 // rows (gate and up rows of a SwiGLU pair both) and streams all of K for
-// them; K is cut into P phases so that P * (gate/up) * R rows -- up to 256 --
-// fill the CTA's 16 compute warps. One warp streams 256-k stages (codes
-// 128B-swizzled, scales) of every (phase, gate/up) box into a shared-memory
-// ring with 2-D TMA loads. A compute thread takes 4 consecutive rows of a box
-// and a 32-k (or 16-k) segment of the stage: it loads its activation segment
-// once and reuses it for the 4 rows; a warp's code loads are conflict-free
-// under the swizzle. Each thread keeps its rows' partial sums across the
+// them; the 256-k chunks of K are dealt to P phases (phase p takes chunks p,
+// p + P, ...) so that P * (gate/up) * R rows -- up to 256 -- fill the CTA's
+// 16 compute warps, and the P boxes of one stage are adjacent in memory. One
+// warp streams the stages (codes 128B-swizzled, scales) of every (phase,
+// gate/up) box into a shared-memory ring with 2-D TMA loads. A compute
+// thread takes 4 consecutive rows of a box and a 32-k (or 16-k) segment of
+// the stage: it loads its activation segment once and reuses it for the 4
+// rows; a warp's code loads are conflict-free under the swizzle. Each thread keeps its rows' partial sums across the
 // stages of a unit; at the unit's end they are reduced over segments and
 // phases in a fixed order, and the epilogue applies g, SwiGLU or the
 // residual and rounds once.
@@ -45,6 +46,10 @@ constexpr int kCcThreads = 32 * kCcWarps;
 constexpr int kCcTmaWarp = kCcWarps;                  // warp 16: TMA producer
 constexpr int kCcAllThreads = 32 * (kCcWarps + 1);
 constexpr int kCcMaxStages = 16;
+// Stages the producer issues before the activations are converted; the rest
+// wait, so that the activation loads and the first stage are not queued
+// behind the whole ring's weight traffic.
+constexpr int kCcLeadStages = 4;
 constexpr int kCcRows = 4;                            // rows per thread
 constexpr uint32_t kCcSmemMax = 227u * 1024u;
 
@@ -300,10 +305,11 @@ __device__ __forceinline__ void cc_units(const CcArgs& a, uint8_t* smem, uint64_
     const uint8_t* fl = smem + a.smem_fl;
     float* red = reinterpret_cast<float*>(smem + a.smem_red);
     const uint32_t ring = smem_u32(smem + a.smem_ring);
-    // this thread computes chunks kc0 .. kc0 + n_mine - 1 of every unit
-    const int kc0 = p * a.Cp;
-    const int n_mine = active ? max(0, min(a.Cp, a.C - kc0)) : 0;
-    const uint32_t x0 = smem_u32(xs + kc0 * (kChunkK / 2) + seg * 4);
+    // phase p takes chunks p, p + P, p + 2P, ... (the P boxes of a stage are
+    // adjacent in k): n_mine of them in every unit
+    const int n_mine = active ? max(0, (a.C - p + a.P - 1) / a.P) : 0;
+    const uint32_t x0 = smem_u32(xs + p * (kChunkK / 2) + seg * 4);
+    const uint32_t x_step = static_cast<uint32_t>(a.P) * (kChunkK * 2u);
 
     bool aborted = false;
     int slot = 0, lap = 0;
@@ -314,16 +320,17 @@ __device__ __forceinline__ void cc_units(const CcArgs& a, uint8_t* smem, uint64_
             if (!aborted && c < n_mine) {
                 const uint32_t stage = ring + slot * a.stage_bytes;
                 uint32_t xw[KS / 2];
-                const uint32_t xc = x0 + static_cast<uint32_t>(c) * (kChunkK * 2u);
+                const uint32_t xc = x0 + static_cast<uint32_t>(c) * x_step;
 #pragma unroll
                 for (int i = 0; i < KS / 8; ++i) {
                     const uint4 v = lds128(xc + i * NSEG * 16);
                     xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
                 }
-                if (!MIXED || fl[kc0 + c] == 0)
-                    cc_stage<NSEG, false>(a, stage, b2, row0, seg, xw, pe_all[kc0 + c], acc);
+                const int kc = c * a.P + p;
+                if (!MIXED || fl[kc] == 0)
+                    cc_stage<NSEG, false>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
                 else
-                    cc_stage<NSEG, true>(a, stage, b2, row0, seg, xw, pe_all[kc0 + c], acc);
+                    cc_stage<NSEG, true>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
             }
             // every compute thread arrives: its own reads of the slot are done
             mbar_arrive(&empty[slot]);
@@ -380,7 +387,8 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.smem_bar);
     uint64_t* empty = full + kCcMaxStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCcMaxStages);
+    uint64_t* xready = empty + kCcMaxStages;  // x converted
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(xready + 1);
     volatile int* any_bf = abort_flag + 1;  // some chunk of x kept raw bf16
 
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -389,6 +397,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCcThreads);
         }
+        mbar_init(xready, 1);
         *abort_flag = 0;
         *any_bf = 0;
         fence_barrier_init();
@@ -411,17 +420,21 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
                     stop = true;
                     break;
                 }
+                if (issued == kCcLeadStages && !cc_wait_warp(xready, 0, a, abort_flag)) {
+                    stop = true;
+                    break;
+                }
                 if (*abort_flag || a.starve) {
                     stop = true;
                     break;
                 }
                 int live = 0;
-                for (int pp = 0; pp < a.P; ++pp) live += (pp * a.Cp + c < a.C) ? 1 : 0;
+                for (int pp = 0; pp < a.P; ++pp) live += (c * a.P + pp < a.C) ? 1 : 0;
                 uint8_t* sb = smem + a.smem_ring + slot * a.stage_bytes;
                 if (elect_one()) {
                     mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live * NGU) * a.box_tx);
                     for (int pp = 0; pp < a.P; ++pp) {
-                        const int kc = pp * a.Cp + c;
+                        const int kc = c * a.P + pp;
                         if (kc >= a.C) continue;
 #pragma unroll
                         for (int gg = 0; gg < NGU; ++gg) {
@@ -456,6 +469,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     cc_convert<NSEG>(a, smem, warp, lane, any_bf);
     named_barrier_sync(1, kCcThreads);
+    if (threadIdx.x == 0) mbar_arrive(xready);
     if (*any_bf)
         cc_units<EPI, NSEG, true>(a, smem, full, empty, abort_flag);
     else
@@ -634,10 +648,11 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
     const uint8_t* fl = smem + a.smem_fl;
     float* red = reinterpret_cast<float*>(smem + a.smem_red);
     const uint32_t ring = smem_u32(smem + a.smem_ring);
-    // this thread computes chunks kc0 .. kc0 + n_mine - 1 of every unit
-    const int kc0 = p * a.Cp;
-    const int n_mine = active ? max(0, min(a.Cp, a.C - kc0)) : 0;
-    const uint32_t x0 = smem_u32(xs + kc0 * (kChunkK / 2) + seg * 4);
+    // phase p takes chunks p, p + P, p + 2P, ... (the P boxes of a stage are
+    // adjacent in k): n_mine of them in every unit
+    const int n_mine = active ? max(0, (a.C - p + a.P - 1) / a.P) : 0;
+    const uint32_t x0 = smem_u32(xs + p * (kChunkK / 2) + seg * 4);
+    const uint32_t x_step = static_cast<uint32_t>(a.P) * (kChunkK * 2u);
 
     bool aborted = false;
     int slot = 0, lap = 0;
@@ -646,10 +661,10 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
         for (int c = 0; c < a.Cp; ++c) {
             if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
             if (!aborted && c < n_mine) {
-                const int kc = kc0 + c;
+                const int kc = c * a.P + p;
                 const uint32_t stage = ring + slot * a.stage_bytes;
                 uint32_t xw[KS / 2];
-                const uint32_t xc = x0 + static_cast<uint32_t>(c) * (kChunkK * 2u);
+                const uint32_t xc = x0 + static_cast<uint32_t>(c) * x_step;
 #pragma unroll
                 for (int i = 0; i < KS / 8; ++i) {
                     const uint4 v = lds128(xc + i * NSEG * 16);
@@ -710,7 +725,8 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.smem_bar);
     uint64_t* empty = full + kCcMaxStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCcMaxStages);
+    uint64_t* xready = empty + kCcMaxStages;  // x converted
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(xready + 1);
     volatile int* any_bf = abort_flag + 1;  // some chunk of x kept raw bf16
 
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -719,6 +735,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCcThreads);
         }
+        mbar_init(xready, 1);
         *abort_flag = 0;
         *any_bf = 0;
         fence_barrier_init();
@@ -743,17 +760,21 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
                     stop = true;
                     break;
                 }
+                if (issued == kCcLeadStages && !cc_wait_warp(xready, 0, a, abort_flag)) {
+                    stop = true;
+                    break;
+                }
                 if (*abort_flag || a.starve) {
                     stop = true;
                     break;
                 }
                 int live = 0;
-                for (int pp = 0; pp < a.P; ++pp) live += (pp * a.Cp + c < a.C) ? 1 : 0;
+                for (int pp = 0; pp < a.P; ++pp) live += (c * a.P + pp < a.C) ? 1 : 0;
                 uint8_t* sb = smem + a.smem_ring + slot * a.stage_bytes;
                 if (elect_one()) {
                     mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live) * a.box_tx);
                     for (int pp = 0; pp < a.P; ++pp) {
-                        const int kc = pp * a.Cp + c;
+                        const int kc = c * a.P + pp;
                         if (kc >= a.C) continue;
                         tma_load_2d(sb + pp * a.R8 * 128, &tm_codes, kc * (kChunkK / 2), row, &full[slot]);
                         tma_load_2d(sb + a.scales_off + pp * a.R8 * 16, &tm_scales, kc * (kChunkK / 32), row,
@@ -786,6 +807,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     cc_convert_q45<NSEG>(a, smem, warp, lane, any_bf);
     named_barrier_sync(1, kCcThreads);
+    if (threadIdx.x == 0) mbar_arrive(xready);
     if (*any_bf)
         cc_q45_units<BITS, EPI, NSEG, true>(a, smem, full, empty, abort_flag);
     else
@@ -813,7 +835,7 @@ qg_status cc_launch(CcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
     const uint32_t pe_bytes = align_up(static_cast<uint32_t>(a.C) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(a.C), 16);
     const uint32_t red_bytes = align_up(nbox * a.R8 * 4u, 128);
-    const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
+    const uint32_t bar_bytes = (2 * kCcMaxStages + 1) * 8 + 16;
     const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
     a.n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / a.stage_bytes));
@@ -887,7 +909,7 @@ qg_status cc_q45_launch(CcArgs a, const CUtensorMap (&maps)[4], int grid, cudaSt
     const uint32_t gx_bytes = align_up(static_cast<uint32_t>(a.C * NSEG) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(a.C), 16);
     const uint32_t red_bytes = align_up(nbox * a.R8 * 4u, 128);
-    const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
+    const uint32_t bar_bytes = (2 * kCcMaxStages + 1) * 8 + 16;
     const uint32_t fixed = x_bytes + pe_bytes + gx_bytes + fl_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
     a.n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / a.stage_bytes));
