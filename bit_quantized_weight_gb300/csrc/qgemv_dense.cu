@@ -84,12 +84,12 @@ struct TileAcc {
     float v[2][4];  // [gate/up][element]
 };
 
-// One consumer warp's work on one pipeline stage (256 k) for one 16-row tile.
-// BF = false: f16 MMA on the prescaled activations (every value of the chunk
+// One consumer warp's work on one pipeline stage (256 k) for one 16-row tile
+// of NVFP4 weights. BF = false: f16 MMA on the prescaled activations (every value of the chunk
 // exact in f16). BF = true: bf16 MMA on the raw bf16 activations, used for a
 // chunk whose values do not all fit one f16 exponent window; the decoded
 // weights are exact in bf16 as well, so the products stay exact.
-template <int FMT, int EPI, bool BF>
+template <int EPI, bool BF>
 __device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint32_t xb, uint32_t sm_base, int jsub,
                                            int kk0, int ti, int lane, const int* xexp, int ntok, TileAcc& acc)
 {
@@ -99,13 +99,6 @@ __device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint
     const int p0 = xexp[jsub * 8 + 2 * t];
     const int p1 = xexp[jsub * 8 + 2 * t + 1];
 
-    uint4 qs_g = make_uint4(0, 0, 0, 0), qs_g8 = qs_g, qm_g = qs_g, qm_g8 = qs_g;
-    if (FMT != FMT_NVFP4) {
-        qs_g = lds128(sb + a.st.scales + (16 * ti + g) * 16);
-        qs_g8 = lds128(sb + a.st.scales + (16 * ti + g + 8) * 16);
-        qm_g = lds128(sb + a.st.mins + (16 * ti + g) * 16);
-        qm_g8 = lds128(sb + a.st.mins + (16 * ti + g + 8) * 16);
-    }
     // four independent accumulator chains per gate/up tile (chunk x MMA half)
     float d[2][2][4];
     float d2[2][2][4];
@@ -135,7 +128,7 @@ __device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint
             ldmatrix_x4(cr, sb + (gu ? a.st.codes2 : a.st.codes) + lofs);
             // cr[0]: row g chunk 2ms; cr[1]: row g+8 chunk 2ms; cr[2], cr[3]: chunk 2ms+1.
             // Each register holds the 8 codes of k = 32 * chunk + 8t .. 8t+7.
-            if (FMT == FMT_NVFP4) {
+            {
                 const uint32_t sbase = sb + (gu ? a.st.scales2 : a.st.scales);
                 const uint32_t sw_g = lds32(sbase + (16 * ti + g) * 16 + 4 * ms);
                 const uint32_t sw_g8 = lds32(sbase + (16 * ti + g + 8) * 16 + 4 * ms);
@@ -169,63 +162,6 @@ __device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint
                         mma_f16_16816(d2[gu][ch], A1, bb.z, bb.w);
                     }
                 }
-            } else {
-#pragma unroll
-                for (int ch = 0; ch < 2; ++ch) {
-                    const int grp = 2 * ms + ch;  // 32-k group inside the chunk
-                    const uint32_t rg = cr[2 * ch], rg8 = cr[2 * ch + 1];
-                    uint32_t hg = 0, hg8 = 0;
-                    if (FMT == FMT_Q5) {
-                        const uint32_t h0 = lds8(sb + a.st.hi + (16 * ti + g) * 32 + 4 * grp + t);
-                        const uint32_t h1 = lds8(sb + a.st.hi + (16 * ti + g + 8) * 32 + 4 * grp + t);
-                        hg = (h0 << 4) | (h0 << 16);
-                        hg8 = (h1 << 4) | (h1 << 16);
-                    }
-                    // pair {q(8t+i), q(8t+i+4)}: f16 1024 + q (or bf16 128 + q), minus the offset
-                    constexpr uint32_t kMagic = BF ? 0x43004300u : 0x64006400u;
-                    uint32_t q0[4], q8[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t u = ((rg >> (4 * i)) & 0x000F000Fu) | kMagic;
-                        uint32_t u8 = ((rg8 >> (4 * i)) & 0x000F000Fu) | kMagic;
-                        if (FMT == FMT_Q5) {
-                            u |= (hg >> i) & 0x00100010u;
-                            u8 |= (hg8 >> i) & 0x00100010u;
-                        }
-                        q0[i] = BF ? bsub2(u, kMagic) : hsub2(u, kMagic);
-                        q8[i] = BF ? bsub2(u8, kMagic) : hsub2(u8, kMagic);
-                    }
-                    const uint4 bb = bx[ch];
-                    float dg[4] = {0.f, 0.f, 0.f, 0.f};
-                    const uint32_t A0[4] = {q0[0], q8[0], q0[1], q8[1]};
-                    const uint32_t A1[4] = {q0[2], q8[2], q0[3], q8[3]};
-                    if (BF) {
-                        mma_bf16_16816(dg, A0, bb.x, bb.y);
-                        mma_bf16_16816(dg, A1, bb.z, bb.w);
-                    } else {
-                        mma_f16_16816(dg, A0, bb.x, bb.y);
-                        mma_f16_16816(dg, A1, bb.z, bb.w);
-                    }
-                    const uint32_t sv_g = (&qs_g.x)[grp >> 1], sv_g8 = (&qs_g8.x)[grp >> 1];
-                    const uint32_t mv_g = (&qm_g.x)[grp >> 1], mv_g8 = (&qm_g8.x)[grp >> 1];
-                    const int sh = (grp & 1) * 16;
-                    const float s0 = half_bits_to_f32((sv_g >> sh) & 0xFFFFu);
-                    const float s8 = half_bits_to_f32((sv_g8 >> sh) & 0xFFFFu);
-                    const float m0 = half_bits_to_f32((mv_g >> sh) & 0xFFFFu);
-                    const float m8 = half_bits_to_f32((mv_g8 >> sh) & 0xFFFFu);
-                    // exact prescaled group sums of x for tokens 2t, 2t+1
-                    const uint2 sx = lds64(sm_base + a.smem_sum + ((jsub * 8 + grp) * 8 + 2 * t) * 4);
-                    float S0 = __uint_as_float(sx.x), S1 = __uint_as_float(sx.y);
-                    if (BF) {  // the bf16 pass works on unscaled activations
-                        S0 = ldexp_exact(S0, -p0);
-                        S1 = ldexp_exact(S1, -p1);
-                    }
-                    float* dd = d[0][ch];
-                    dd[0] = fmaf(m0, S0, fmaf(s0, dg[0], dd[0]));
-                    dd[1] = fmaf(m0, S1, fmaf(s0, dg[1], dd[1]));
-                    dd[2] = fmaf(m8, S0, fmaf(s8, dg[2], dd[2]));
-                    dd[3] = fmaf(m8, S1, fmaf(s8, dg[3], dd[3]));
-                }
             }
         }
     }
@@ -239,6 +175,100 @@ __device__ __forceinline__ void tile_stage(const DenseArgs& a, uint32_t sb, uint
             acc.v[gu][e] += ldexp_exact(part, (e & 1) ? -e1 : -e0);
         }
     }
+}
+
+// One consumer warp's work on one pipeline stage (256 k) for one 16-row tile
+// of Q4/Q5 weights. The codes are small integers, exact in bf16, so the MMAs
+// run in bf16 on the raw bf16 activations the stage carries (no prescale):
+// per 32-k group, sum(q x) from the codes and sum(x) from an MMA of all-ones
+// rows, which lands in the same fragment layout; then
+// y += scale * sum(q x) + min * sum(x).
+template <int FMT>
+__device__ __forceinline__ void tile_stage_q(const DenseArgs& a, uint32_t sb, int ti, int lane, int ntok,
+                                             TileAcc& acc)
+{
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const uint4 qs_g = lds128(sb + a.st.scales + (16 * ti + g) * 16);
+    const uint4 qs_g8 = lds128(sb + a.st.scales + (16 * ti + g + 8) * 16);
+    const uint4 qm_g = lds128(sb + a.st.mins + (16 * ti + g) * 16);
+    const uint4 qm_g8 = lds128(sb + a.st.mins + (16 * ti + g + 8) * 16);
+    constexpr uint32_t kOnes = 0x3F803F80u;  // bf16 pair (1, 1)
+    const uint32_t ones[4] = {kOnes, kOnes, kOnes, kOnes};
+    float d[2][4];
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[ch][e] = 0.f;
+
+    const int lr = (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+    for (int ms = 0; ms < 4; ++ms) {
+        // token g's 8 activations at k = 64 ms + 32 ch + 8 t, as the pairs
+        // (k, k+4) (k+1, k+5) (k+2, k+6) (k+3, k+7) the code decode produces
+        uint4 bx[2];
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+            const uint4 v = g < ntok ? lds128(sb + a.st.x + g * 512 + (64 * ms + 32 * ch + 8 * t) * 2)
+                                     : make_uint4(0, 0, 0, 0);
+            bx[ch] = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
+                                __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
+        }
+        const int lc = 2 * ms + (lane >> 4);
+        const uint32_t lofs = (16 * ti + lr) * 128 + ((lc ^ (lr & 7)) << 4);
+        uint32_t cr[4];
+        ldmatrix_x4(cr, sb + a.st.codes + lofs);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+            const int grp = 2 * ms + ch;  // 32-k group inside the chunk
+            const uint32_t rg = cr[2 * ch], rg8 = cr[2 * ch + 1];
+            uint32_t hg = 0, hg8 = 0;
+            if (FMT == FMT_Q5) {
+                const uint32_t h0 = lds8(sb + a.st.hi + (16 * ti + g) * 32 + 4 * grp + t);
+                const uint32_t h1 = lds8(sb + a.st.hi + (16 * ti + g + 8) * 32 + 4 * grp + t);
+                hg = (h0 << 4) | (h0 << 16);
+                hg8 = (h1 << 4) | (h1 << 16);
+            }
+            // pair {q(8t+i), q(8t+i+4)}: bf16 128 + q, minus 128
+            constexpr uint32_t kMagic = 0x43004300u;
+            uint32_t q0[4], q8[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t u = ((rg >> (4 * i)) & 0x000F000Fu) | kMagic;
+                uint32_t u8 = ((rg8 >> (4 * i)) & 0x000F000Fu) | kMagic;
+                if (FMT == FMT_Q5) {
+                    u |= (hg >> i) & 0x00100010u;
+                    u8 |= (hg8 >> i) & 0x00100010u;
+                }
+                q0[i] = bsub2(u, kMagic);
+                q8[i] = bsub2(u8, kMagic);
+            }
+            const uint4 bb = bx[ch];
+            const uint32_t A0[4] = {q0[0], q8[0], q0[1], q8[1]};
+            const uint32_t A1[4] = {q0[2], q8[2], q0[3], q8[3]};
+            float dg[4] = {0.f, 0.f, 0.f, 0.f};
+            float ds[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_bf16_16816(dg, A0, bb.x, bb.y);
+            mma_bf16_16816(dg, A1, bb.z, bb.w);
+            mma_bf16_16816(ds, ones, bb.x, bb.y);
+            mma_bf16_16816(ds, ones, bb.z, bb.w);
+            const uint32_t sv_g = (&qs_g.x)[grp >> 1], sv_g8 = (&qs_g8.x)[grp >> 1];
+            const uint32_t mv_g = (&qm_g.x)[grp >> 1], mv_g8 = (&qm_g8.x)[grp >> 1];
+            const int sh = (grp & 1) * 16;
+            const float s0 = half_bits_to_f32((sv_g >> sh) & 0xFFFFu);
+            const float s8 = half_bits_to_f32((sv_g8 >> sh) & 0xFFFFu);
+            const float m0 = half_bits_to_f32((mv_g >> sh) & 0xFFFFu);
+            const float m8 = half_bits_to_f32((mv_g8 >> sh) & 0xFFFFu);
+            // ds[e]: sum of x over the group for token column 2t + (e & 1)
+            float* dd = d[ch];
+            dd[0] = fmaf(m0, ds[0], fmaf(s0, dg[0], dd[0]));
+            dd[1] = fmaf(m0, ds[1], fmaf(s0, dg[1], dd[1]));
+            dd[2] = fmaf(m8, ds[2], fmaf(s8, dg[2], dd[2]));
+            dd[3] = fmaf(m8, ds[3], fmaf(s8, dg[3], dd[3]));
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc.v[0][e] += d[0][e] + d[1][e];
 }
 
 // Unit of work: rows [w_row0, w_row0 + rows) of the weight tensor (gate rows
@@ -288,7 +318,7 @@ template <int FMT, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const __grid_constant__ DenseArgs a, const __grid_constant__ CUtensorMap tm0,
                 const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm2,
-                const __grid_constant__ CUtensorMap tm3)
+                const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tmx)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int NGU = (EPI == EPI_SWIGLU) ? 2 : 1;
@@ -330,12 +360,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&tm1);
             if (FMT != FMT_NVFP4) prefetch_tensormap(&tm2);
             if (FMT == FMT_Q5) prefetch_tensormap(&tm3);
+            if (FMT != FMT_NVFP4) prefetch_tensormap(&tmx);
             int gc = 0;  // global stage counter across units
             bool stop = false;
+            // Q4/Q5 stages carry their activations, which may come from the
+            // previous kernel: weight copies start at once, the activation
+            // copies of the stages issued so far follow the dependency wait
+            // (before the first wait for a free slot, so no stage is left
+            // without its activations).
+            bool x_ready = FMT == FMT_NVFP4;
+            auto x_backfill = [&]() {
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                for (int s = max(0, gc - a.n_stages); s < gc; ++s)
+                    tma_load_2d(smem + a.smem_ring + (s % a.n_stages) * a.st.bytes + a.st.x, &tmx,
+                                (s % n_chunks) * kChunkK, 0, &full[s % a.n_stages]);
+                x_ready = true;
+            };
             for (int u = u_begin; u < u_end && !stop; ++u) {
                 const Unit un = load_unit(a, u);
                 for (int c = 0; c < n_chunks; ++c, ++gc) {
                     const int slot = gc % a.n_stages;
+                    if (gc >= a.n_stages && !x_ready) x_backfill();
                     if (gc >= a.n_stages) {
                         if (!mbar_wait_bounded(&empty[slot], ((gc / a.n_stages) - 1) & 1, a.wait_ns, a.status)) {
                             *abort_flag = 1;
@@ -361,9 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_2d(sb + a.st.scales, &tm1, kb / 32, un.w_row0, &full[slot]);
                         tma_load_2d(sb + a.st.mins, &tm2, kb / 32, un.w_row0, &full[slot]);
                         if (FMT == FMT_Q5) tma_load_2d(sb + a.st.hi, &tm3, kb / 8, un.w_row0, &full[slot]);
+                        if (x_ready) tma_load_2d(sb + a.st.x, &tmx, kb, 0, &full[slot]);
                     }
                 }
             }
+            if (!x_ready) x_backfill();
             // No copy may still be landing in shared memory when the CTA exits.
             for (int c = max(0, gc - a.n_stages); c < gc; ++c)
                 mbar_wait_bounded(&full[c % a.n_stages], (c / a.n_stages) & 1, a.wait_ns, a.status);
@@ -422,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kglob = c * kChunkK;
             const int ks0 = (kglob / a.ksc) * a.ksc;
             // ---------------- activation super-chunk: prescale, convert, flag
-            if (ks0 != conv_ks0 || xkey != conv_key) {
+            if (FMT == FMT_NVFP4 && (ks0 != conv_ks0 || xkey != conv_key)) {
                 const int len = min(a.ksc, a.K - ks0);
                 const int nsub = len / kChunkK;
                 const int n_items = nsub * ntok;
@@ -513,13 +560,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!aborted && 16 * my_tile < un.rows) {
                 const uint32_t sb = sm_base + a.smem_ring + slot * a.st.bytes;
-                const int jsub = (kglob - ks0) / kChunkK;
-                const uint64_t flags8 = *reinterpret_cast<const uint64_t*>(xflag + jsub * 8);
-                const int kk0 = kglob - ks0;
-                if (flags8)
-                    tile_stage<FMT, EPI, true>(a, sb, xraw_base, sm_base, jsub, kk0, my_tile, lane, xexp, ntok, acc);
-                else
-                    tile_stage<FMT, EPI, false>(a, sb, x_base, sm_base, jsub, kk0, my_tile, lane, xexp, ntok, acc);
+                if constexpr (FMT == FMT_NVFP4) {
+                    const int jsub = (kglob - ks0) / kChunkK;
+                    const uint64_t flags8 = *reinterpret_cast<const uint64_t*>(xflag + jsub * 8);
+                    const int kk0 = kglob - ks0;
+                    if (flags8)
+                        tile_stage<EPI, true>(a, sb, xraw_base, sm_base, jsub, kk0, my_tile, lane, xexp, ntok, acc);
+                    else
+                        tile_stage<EPI, false>(a, sb, x_base, sm_base, jsub, kk0, my_tile, lane, xexp, ntok, acc);
+                } else {
+                    tile_stage_q<FMT>(a, sb, my_tile, lane, ntok, acc);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
@@ -585,14 +636,15 @@ qg_status launch_gemv_impl(const CUtensorMap* maps, DenseArgs a, int grid, cudaS
     a.wait_ns = dbg.wait_ns;
     a.starve = dbg.starve;
 
-    // activation super-chunk: f16 (prescaled) and raw bf16 copies of M token
-    // rows of (ksc + 32) values
+    // NVFP4: activation super-chunk, f16 (prescaled) and raw bf16 copies of M
+    // token rows of (ksc + 32) values. Q4/Q5: the activations travel with
+    // each stage instead.
     constexpr uint32_t kXBudget = 80 * 1024;
     int ksc = (static_cast<int>(kXBudget / (4u * M)) - 32) / kChunkK * kChunkK;
     ksc = min(ksc, K);
     a.ksc = ksc;
-    a.x_pitch = ksc + 32;
-    const int nsub = ksc / kChunkK;
+    a.x_pitch = FMT == FMT_NVFP4 ? ksc + 32 : 0;
+    const int nsub = FMT == FMT_NVFP4 ? ksc / kChunkK : 0;
 
     const int R = a.rows_per_cta;
     const int R16 = (R + 15) / 16 * 16;  // regions cover whole 16-row tiles
@@ -618,10 +670,14 @@ qg_status launch_gemv_impl(const CUtensorMap* maps, DenseArgs a, int grid, cudaS
         st.hi = off;
         off = align_up(off + R16 * 32, 128);
     }
+    if (FMT != FMT_NVFP4) {
+        st.x = off;
+        off = align_up(off + static_cast<uint32_t>(M) * kChunkK * 2, 128);
+    }
     st.bytes = align_up(off, 1024);
     uint32_t tx = R * 128 + R * 16;
     if (EPI == EPI_SWIGLU) tx *= 2;
-    if (FMT != FMT_NVFP4) tx += R * 16;
+    if (FMT != FMT_NVFP4) tx += R * 16 + M * kChunkK * 2;
     if (FMT == FMT_Q5) tx += R * 32;
     st.tx_bytes = tx;
     a.st = st;
@@ -631,7 +687,7 @@ qg_status launch_gemv_impl(const CUtensorMap* maps, DenseArgs a, int grid, cudaS
     const uint32_t x_bytes = align_up(static_cast<uint32_t>(M) * a.x_pitch * 2, 128);
     const uint32_t exp_bytes = align_up(nsub * 8 * 4, 128);
     const uint32_t flag_bytes = align_up(nsub * 8, 128);
-    const uint32_t sum_bytes = FMT == FMT_NVFP4 ? 0 : align_up(nsub * 8 * 8 * 4, 128);
+    const uint32_t sum_bytes = 0;
     const uint32_t red_bytes = kConsumerWarps * 2 * 32 * 4 * 4;
     const uint32_t bar_bytes = 2 * kMaxStages * 8 + 16;
     const uint32_t fixed = 2 * x_bytes + exp_bytes + flag_bytes + sum_bytes + red_bytes + bar_bytes;
@@ -678,7 +734,8 @@ qg_status launch_gemv_impl(const CUtensorMap* maps, DenseArgs a, int grid, cudaS
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, a, maps[0], maps[1], maps[2], maps[3]) != cudaSuccess) return QG_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, a, maps[0], maps[1], maps[2], maps[3], maps[4]) != cudaSuccess)
+        return QG_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
@@ -717,13 +774,14 @@ qg_status launch_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float 
 {
     const int n_out = swiglu ? N / 2 : N;
     const int R = choose_rows_per_cta(n_out, 1);
-    CUtensorMap maps[4];
+    CUtensorMap maps[5];
     memset(maps, 0, sizeof(maps));
     if (!encode_tmap_2d(&maps[0], codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, R, true)) return QG_ERR_CUDA;
     if (!encode_tmap_2d(&maps[1], scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 16, N, 16, R, false))
         return QG_ERR_CUDA;
     maps[2] = maps[1];
     maps[3] = maps[1];
+    maps[4] = maps[1];
     const int grid = (n_out + R - 1) / R;
     if (swiglu)
         return launch_gemv_impl<FMT_NVFP4, EPI_SWIGLU>(maps, dense_args(x, y, 0, nullptr, M, n_out, n_out, K, g, R),
@@ -740,7 +798,7 @@ qg_status launch_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void*
                            int N, int K, cudaStream_t stream)
 {
     const int R = choose_rows_per_cta(N, 1);
-    CUtensorMap maps[4];
+    CUtensorMap maps[5];
     memset(maps, 0, sizeof(maps));
     if (!encode_tmap_2d(&maps[0], q_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, R, true)) return QG_ERR_CUDA;
     if (!encode_tmap_2d(&maps[1], scale, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, N, 8, R, false))
@@ -753,6 +811,8 @@ qg_status launch_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void*
     } else {
         maps[3] = maps[2];
     }
+    // the M activation rows, one 256-k chunk per stage
+    if (!encode_tmap_2d(&maps[4], x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K, M, kChunkK, M, false)) return QG_ERR_CUDA;
     const int grid = (N + R - 1) / R;
     const DenseArgs a = dense_args(x, y, out_f32, residual, M, N, 0, K, 1.f, R);
     if (bits == 5) {
@@ -769,7 +829,7 @@ qg_status launch_grouped_nvfp4(const uint8_t* codes, const uint8_t* scales, int 
                                const float* gscales, int rows_per_unit, cudaStream_t stream)
 {
     const int R = rows_per_unit;
-    CUtensorMap maps[4];
+    CUtensorMap maps[5];
     memset(maps, 0, sizeof(maps));
     if (!encode_tmap_2d(&maps[0], codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, total_rows, 128, R, true))
         return QG_ERR_CUDA;
@@ -777,6 +837,7 @@ qg_status launch_grouped_nvfp4(const uint8_t* codes, const uint8_t* scales, int 
         return QG_ERR_CUDA;
     maps[2] = maps[1];
     maps[3] = maps[1];
+    maps[4] = maps[1];
     DenseArgs a = dense_args(x, y, out_f32, nullptr, max_cols, 0, up_offset, K, 1.f, R);
     a.out_pitch = out_pitch;
     a.groups = groups;

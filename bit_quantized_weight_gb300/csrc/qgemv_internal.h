@@ -27,6 +27,7 @@ struct StageLayout {
     uint32_t scales2;    // SwiGLU up-row scales
     uint32_t mins;       // Q min rows x 16 B
     uint32_t hi;         // Q5 high plane rows x 32 B
+    uint32_t x;          // Q4/Q5: the stage's raw bf16 activations, M rows x 512 B
     uint32_t bytes;      // total stage size (multiple of 1024)
     uint32_t tx_bytes;   // bytes the TMA writes per stage
 };
