@@ -497,6 +497,40 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------ main
+def read_probe_bandwidth(torch, q, stream, peak, nbytes=2 << 30, reps=10):
+    """Read-only HBM bandwidth of the library's streaming-read probe (128-bit
+    loads from every SM over a 2 GiB buffer, far larger than L2): median of
+    `reps` single launches timed with events on the launching stream."""
+    buf = torch.empty(nbytes // 4, dtype=torch.int32, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    times = []
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            q.read_probe(buf, sink, stream=stream)
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            q.read_probe(buf, sink, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+    t = sorted(times)[len(times) // 2]
+    del buf
+    gbs = nbytes / (t * 1e-3) / 1e9
+    return {"value": gbs, "unit": "GB/s", "bytes": nbytes, "frac_of_measured_copy": gbs / peak,
+            "what": "library streaming-read probe (qg_read_probe), median of 10 launches"}
+
+
+def arithmetic(workload, M):
+    if workload in ("dense", "tiny") and M == 1:
+        return "f16 x f16 -> f32 FMA on CUDA cores (exact decoded weights, prescaled activations)"
+    if workload == "q45" and M == 1:
+        return "f16 x f16 -> f32 FMA on CUDA cores (codes as exact f16, prescaled activations)"
+    if workload == "q45":
+        return "bf16 mma.sync, f32 accumulate (codes exact in bf16, raw bf16 activations)"
+    return "f16 tcgen05 MMA, f32 accumulate (exact decoded weights, prescaled activations)"
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_setup(args.gpus)
@@ -646,6 +680,8 @@ def main():
                "h2d_bytes_per_step": wl.in_elems * 2, "d2h_bytes_per_step": wl.out_elems * 2,
                "ms_per_step": ems / args.steps}
 
+    probe = read_probe_bandwidth(torch, q, stream, peak) if rank == 0 else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload != "moe":
         cpu = cpu_baseline(args.workload, args.M)
@@ -654,7 +690,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16 MMA of exact decoded weights, f32 accumulate",
+            "scaling": "weak", "vs_baseline": None, "dtype": arithmetic(args.workload, args.M),
             "data": "synthetic",
             "config": {"workload": wl.describe(), "M": args.M, "weight_bytes_per_step": wl.weight_bytes,
                        "l2": f"weights rotate over {wl.copies} copies of the layer "
@@ -666,6 +702,7 @@ def main():
             "frac_of_measured_hbm": value / world / peak,
             "us_per_call": us_per_call,
             "roofline": roofline,
+            "read_probe": probe,
             "gpu_launches": wl.launches_per_step() * args.steps,
             "clocks": clk,
             "e2e": e2e,

@@ -227,6 +227,14 @@ qg_status qdequant_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* sca
     return launch_dequant(bits == 5 ? FMT_Q5 : FMT_Q4, q_lo, q_hi, scale, min, 1.f, w, N, K, stream);
 }
 
+qg_status qg_read_probe(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t stream)
+{
+    if (!sink || bytes % 16 || (!buf && bytes)) return QG_ERR_INVALID_ARG;
+    if (bytes == 0) return QG_OK;
+    if (!aligned16(buf) || (reinterpret_cast<uintptr_t>(sink) & 3u)) return QG_ERR_MISALIGNED;
+    return launch_read_probe(buf, bytes, sink, stream);
+}
+
 qg_status qg_last_device_status(cudaStream_t stream)
 {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return QG_ERR_CUDA;

@@ -125,6 +125,7 @@ qg_status launch_grouped_nvfp4(const uint8_t* codes, const uint8_t* scales, int 
 qg_status launch_simple(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
                         const void* mins, float g, const void* x, void* y, int out_f32,
                         const void* residual, int M, int N, int K, int swiglu, cudaStream_t stream);
+qg_status launch_read_probe(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t stream);
 qg_status launch_dequant(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
                          const void* mins, float g, float* w, int N, int K, cudaStream_t stream);
 qg_status launch_route(const float* logits, int M, int E, int topk, int32_t* ids, float* w,

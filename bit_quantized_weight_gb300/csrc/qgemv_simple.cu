@@ -6,6 +6,8 @@
 // the warp. Slow, simple and exact for every finite input.
 #include "common.cuh"
 
+#include <algorithm>
+
 #include <cuda_bf16.h>
 
 namespace qg {
@@ -137,6 +139,51 @@ qg_status launch_simple(int fmt, const uint8_t* codes, const uint8_t* q_hi, cons
     simple_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         fmt, codes, q_hi, scales, mins, g, static_cast<const uint16_t*>(x), y, out_f32,
         static_cast<const uint16_t*>(residual), M, n_out, K, swiglu);
+    return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+// Streaming-read probe: every thread keeps kProbeUnroll 128-bit loads in
+// flight over a grid-stride walk of the buffer and XORs the words it reads;
+// the warps' results are XORed into *sink.
+namespace {
+
+constexpr int kProbeUnroll = 8;
+constexpr int kProbeThreads = 512;
+
+__global__ void __launch_bounds__(kProbeThreads) read_probe_kernel(const uint4* __restrict__ p, size_t n16,
+                                                                   uint32_t* sink)
+{
+    const size_t stride = static_cast<size_t>(gridDim.x) * kProbeThreads;
+    size_t i = static_cast<size_t>(blockIdx.x) * kProbeThreads + threadIdx.x;
+    uint32_t acc = 0;
+    for (; i + (kProbeUnroll - 1) * stride < n16; i += kProbeUnroll * stride) {
+        uint4 v[kProbeUnroll];
+#pragma unroll
+        for (int u = 0; u < kProbeUnroll; ++u) v[u] = ldg_nc_128(p + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < kProbeUnroll; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+    }
+    for (; i < n16; i += stride) {
+        const uint4 v = ldg_nc_128(p + i);
+        acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+    acc = __reduce_xor_sync(0xffffffffu, acc);
+    if ((threadIdx.x & 31) == 0) atomicXor(sink, acc);
+}
+
+}  // namespace
+
+qg_status launch_read_probe(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t stream)
+{
+    const size_t n16 = bytes / 16;
+    if (n16 == 0) return QG_OK;
+    const int sms = sm_count(-1);
+    if (sms <= 0) return QG_ERR_CUDA;
+    // four resident CTAs per SM, fewer for small buffers
+    const size_t per_cta = static_cast<size_t>(kProbeThreads) * kProbeUnroll;
+    const size_t blocks = std::min<size_t>(static_cast<size_t>(4) * sms, (n16 + per_cta - 1) / per_cta);
+    read_probe_kernel<<<static_cast<unsigned>(blocks), kProbeThreads, 0, stream>>>(
+        static_cast<const uint4*>(buf), n16, sink);
     return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 

@@ -58,6 +58,7 @@ def lib():
         L.qdequant_nvfp4.argtypes = [_P, _P, _F, _P, _I, _I, _P]
         L.qdequant_q45.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _P]
         L.qg_last_device_status.argtypes = [_P]
+        L.qg_read_probe.argtypes = [_P, ctypes.c_size_t, _P, _P]
         L.qg_status_string.argtypes = [_I]
         L.qg_status_string.restype = ctypes.c_char_p
         L.qg_debug_set_wait.argtypes = [ctypes.c_uint64, _I]
@@ -195,6 +196,15 @@ def qdequant_q45(q_lo, q_hi, scale, mn, bits, w, stream=None):
     _check("qdequant_q45", lib().qdequant_q45(_ptr(q_lo), _ptr(q_hi), _ptr(scale), _ptr(mn), int(bits),
                                               _ptr(w), N, K, _stream(stream, w)))
     return w
+
+
+def read_probe(buf, sink, stream=None):
+    """XOR every 32-bit word of the CUDA tensor `buf` into the one-word
+    int32 CUDA tensor `sink` with 128-bit streaming loads (see qg_read_probe)."""
+    _cuda(buf, sink)
+    _check("qg_read_probe", lib().qg_read_probe(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
+                                                _stream(stream, buf)))
+    return sink
 
 
 def qg_last_device_status(stream=None) -> int:

@@ -184,6 +184,22 @@ QG_API qg_status qdequant_q45(const uint8_t* q_lo, const uint8_t* q_hi, const vo
                        int bits, float* w, int N, int K, cudaStream_t stream);
 
 /*
+ * Streaming-read probe for the measurement of a GEMV against the memory
+ * roofline: reads the `bytes` of device buffer `buf` once, with 128-bit
+ * non-coherent loads from every SM, and XORs all its 32-bit words into the
+ * device word *sink (caller-owned, not cleared: afterwards *sink equals its
+ * old value XOR the buffer's words), so the loads cannot be elided and the
+ * result can be checked. Timing it with events gives the read-only HBM
+ * bandwidth a weight-streaming kernel can reach, next to the copy bandwidth.
+ *   buf: 16-byte aligned, bytes a multiple of 16 (0 launches nothing, and
+ *   buf may then be null);
+ *   sink: 4-byte aligned.
+ * QG_ERR_INVALID_ARG for a null pointer or a ragged size, QG_ERR_MISALIGNED
+ * for misaligned pointers; asynchronous on `stream`.
+ */
+QG_API qg_status qg_read_probe(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t stream);
+
+/*
  * Synchronise `stream`, then return and clear the device status word:
  * QG_OK, QG_ERR_DEVICE_TIMEOUT when a bounded device-side wait gave up (the
  * kernel stopped early; its outputs are undefined), or QG_ERR_INVALID_ARG for
