@@ -13,6 +13,7 @@ namespace {
 // p_i / sum_{top} p_j for p = softmax(l) because the full denominator cancels.
 __global__ void route_kernel(const float* logits, int M, int E, int topk, int32_t* ids, float* w)
 {
+    pdl_enter();
     const int m = blockIdx.x;
     const int lane = threadIdx.x;
     if (m >= M) return;
@@ -72,7 +73,8 @@ __global__ void route_kernel(const float* logits, int M, int E, int topk, int32_
 
 qg_status launch_route(const float* logits, int M, int E, int topk, int32_t* ids, float* w, cudaStream_t stream)
 {
-    route_kernel<<<M, 32, 0, stream>>>(logits, M, E, topk, ids, w);
+    if (launch_pdl(route_kernel, dim3(M), dim3(32), 0, stream, logits, M, E, topk, ids, w) != cudaSuccess)
+        return QG_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
@@ -135,6 +137,7 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
     __shared__ int s_dn_start[kMaxPairs]; // sorted position starting each down group
     __shared__ int s_gu_e[kMaxPairs], s_dn_e[kMaxPairs];  // expert of each group
     __shared__ int s_nv, s_n_gu, s_n_dn;
+    pdl_enter();
     const int P = M * topk;
     const int tid = threadIdx.x;
     for (int p = tid; p < P; p += blockDim.x) {
@@ -289,6 +292,7 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
 __global__ void moe_combine_kernel(const float* yslot, const int32_t* ids, const float* w, uint16_t* y, int M,
                                    int topk, int H, int E)
 {
+    pdl_enter();
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= M * H) return;
     const int m = idx / H, j = idx % H;
@@ -340,9 +344,9 @@ qg_status launch_moe(const uint8_t* gu_codes, const uint8_t* gu_scales, const fl
     int* status = device_status_ptr();
     if (!status) return QG_ERR_CUDA;
 
-    moe_group_kernel<<<1, 256, 0, stream>>>(ids, M, topk, E, I, H, L.r_gu, L.r_dn, g_gu, g_dn, u_gu, u_dn, ctrl,
-                                            status);
-    if (cudaPeekAtLastError() != cudaSuccess) return QG_ERR_CUDA;
+    if (launch_pdl(moe_group_kernel, dim3(1), dim3(256), 0, stream, ids, M, topk, E, I, H, L.r_gu, L.r_dn, g_gu,
+                   g_dn, u_gu, u_dn, ctrl, status) != cudaSuccess)
+        return QG_ERR_CUDA;
     qg_status s = grouped_nvfp4(gu_codes, gu_scales, E * 2 * I, H, 1, I, x, M, h, I, 0, g_gu, u_gu, ctrl + 0,
                                        gu_g, L.r_gu, stream);
     if (s != QG_OK) return s;
@@ -350,7 +354,9 @@ qg_status launch_moe(const uint8_t* gu_codes, const uint8_t* gu_scales, const fl
                              L.r_dn, stream);
     if (s != QG_OK) return s;
     const int n = M * H;
-    moe_combine_kernel<<<(n + 255) / 256, 256, 0, stream>>>(yslot, ids, tw, static_cast<uint16_t*>(y), M, topk, H, E);
+    if (launch_pdl(moe_combine_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, yslot, ids, tw,
+                   static_cast<uint16_t*>(y), M, topk, H, E) != cudaSuccess)
+        return QG_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
