@@ -56,6 +56,7 @@ def parse_args():
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-read-probe", action="store_true")
     return ap.parse_args()
 
 
@@ -633,7 +634,9 @@ def main():
     g_dom = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_dom, stream=stream):
         for i in range(args.steps):
-            wl.call(dom, i)
+            # copies the timed step did not just touch (small weights would
+            # otherwise still sit in L2)
+            wl.call(dom, i + args.steps)
     with torch.cuda.stream(stream):
         g_dom.replay()
     stream.synchronize()
@@ -680,7 +683,7 @@ def main():
                "h2d_bytes_per_step": wl.in_elems * 2, "d2h_bytes_per_step": wl.out_elems * 2,
                "ms_per_step": ems / args.steps}
 
-    probe = read_probe_bandwidth(torch, q, stream, peak) if rank == 0 else None
+    probe = read_probe_bandwidth(torch, q, stream, peak) if rank == 0 and not args.no_read_probe else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload != "moe":

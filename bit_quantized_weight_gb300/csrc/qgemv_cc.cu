@@ -46,10 +46,10 @@ constexpr int kCcThreads = 32 * kCcWarps;
 constexpr int kCcTmaWarp = kCcWarps;                  // warp 16: TMA producer
 constexpr int kCcAllThreads = 32 * (kCcWarps + 1);
 constexpr int kCcMaxStages = 16;
-// Stages the producer issues before the activations are converted; the rest
-// wait, so that the activation loads and the first stage are not queued
-// behind the whole ring's weight traffic.
-constexpr int kCcLeadStages = 4;
+// Stages the producer issues before it waits for the previous kernel to
+// complete: CTAs that start early (their SM freed first) then cannot queue a
+// whole ring of weight traffic ahead of the CTAs that start late.
+constexpr int kCcLeadStages = 1;
 constexpr int kCcRows = 4;                            // rows per thread
 constexpr uint32_t kCcSmemMax = 227u * 1024u;
 
@@ -311,6 +311,11 @@ __device__ __forceinline__ void cc_units(const CcArgs& a, uint8_t* smem, uint64_
     const uint32_t x0 = smem_u32(xs + p * (kChunkK / 2) + seg * 4);
     const uint32_t x_step = static_cast<uint32_t>(a.P) * (kChunkK * 2u);
 
+    // residual of the first unit's rows, read now rather than in the epilogue
+    float res_first = 0.f;
+    if (EPI == EPI_RESID && threadIdx.x < a.R && blockIdx.x * a.R + static_cast<int>(threadIdx.x) < a.n_out)
+        res_first = bf16_bits_to_f32(a.residual[blockIdx.x * a.R + threadIdx.x]);
+
     bool aborted = false;
     int slot = 0, lap = 0;
     for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
@@ -364,7 +369,10 @@ __device__ __forceinline__ void cc_units(const CcArgs& a, uint8_t* smem, uint64_
                 }
                 float val = v[0];
                 if (EPI == EPI_SWIGLU) val = (val / (1.0f + expf(-val))) * v[NGU - 1];
-                if (EPI == EPI_RESID) val += bf16_bits_to_f32(a.residual[r0 + r]);
+                if (EPI == EPI_RESID)
+                    val += u == static_cast<int>(blockIdx.x) && r == static_cast<int>(threadIdx.x)
+                               ? res_first
+                               : bf16_bits_to_f32(a.residual[r0 + r]);
                 if (a.out_f32)
                     reinterpret_cast<float*>(a.y)[r0 + r] = val;
                 else
@@ -387,8 +395,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.smem_bar);
     uint64_t* empty = full + kCcMaxStages;
-    uint64_t* xready = empty + kCcMaxStages;  // x converted
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(xready + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCcMaxStages);
     volatile int* any_bf = abort_flag + 1;  // some chunk of x kept raw bf16
 
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -397,7 +404,6 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCcThreads);
         }
-        mbar_init(xready, 1);
         *abort_flag = 0;
         *any_bf = 0;
         fence_barrier_init();
@@ -420,10 +426,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
                     stop = true;
                     break;
                 }
-                if (issued == kCcLeadStages && !cc_wait_warp(xready, 0, a, abort_flag)) {
-                    stop = true;
-                    break;
-                }
+                if (issued == kCcLeadStages) asm volatile("griddepcontrol.wait;" ::: "memory");
                 if (*abort_flag || a.starve) {
                     stop = true;
                     break;
@@ -469,7 +472,6 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     cc_convert<NSEG>(a, smem, warp, lane, any_bf);
     named_barrier_sync(1, kCcThreads);
-    if (threadIdx.x == 0) mbar_arrive(xready);
     if (*any_bf)
         cc_units<EPI, NSEG, true>(a, smem, full, empty, abort_flag);
     else
@@ -654,6 +656,11 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
     const uint32_t x0 = smem_u32(xs + p * (kChunkK / 2) + seg * 4);
     const uint32_t x_step = static_cast<uint32_t>(a.P) * (kChunkK * 2u);
 
+    // residual of the first unit's rows, read now rather than in the epilogue
+    float res_first = 0.f;
+    if (EPI == EPI_RESID && threadIdx.x < a.R && blockIdx.x * a.R + static_cast<int>(threadIdx.x) < a.n_out)
+        res_first = bf16_bits_to_f32(a.residual[blockIdx.x * a.R + threadIdx.x]);
+
     bool aborted = false;
     int slot = 0, lap = 0;
     for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
@@ -702,7 +709,10 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
                 float s = 0.f;
                 for (int pp = 0; pp < a.P; ++pp) s += red[pp * a.R8 + r];
                 float val = s;
-                if (EPI == EPI_RESID) val += bf16_bits_to_f32(a.residual[r0 + r]);
+                if (EPI == EPI_RESID)
+                    val += u == static_cast<int>(blockIdx.x) && r == static_cast<int>(threadIdx.x)
+                               ? res_first
+                               : bf16_bits_to_f32(a.residual[r0 + r]);
                 if (a.out_f32)
                     reinterpret_cast<float*>(a.y)[r0 + r] = val;
                 else
@@ -725,8 +735,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.smem_bar);
     uint64_t* empty = full + kCcMaxStages;
-    uint64_t* xready = empty + kCcMaxStages;  // x converted
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(xready + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCcMaxStages);
     volatile int* any_bf = abort_flag + 1;  // some chunk of x kept raw bf16
 
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -735,7 +744,6 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCcThreads);
         }
-        mbar_init(xready, 1);
         *abort_flag = 0;
         *any_bf = 0;
         fence_barrier_init();
@@ -760,10 +768,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
                     stop = true;
                     break;
                 }
-                if (issued == kCcLeadStages && !cc_wait_warp(xready, 0, a, abort_flag)) {
-                    stop = true;
-                    break;
-                }
+                if (issued == kCcLeadStages) asm volatile("griddepcontrol.wait;" ::: "memory");
                 if (*abort_flag || a.starve) {
                     stop = true;
                     break;
@@ -807,7 +812,6 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     cc_convert_q45<NSEG>(a, smem, warp, lane, any_bf);
     named_barrier_sync(1, kCcThreads);
-    if (threadIdx.x == 0) mbar_arrive(xready);
     if (*any_bf)
         cc_q45_units<BITS, EPI, NSEG, true>(a, smem, full, empty, abort_flag);
     else
@@ -835,7 +839,7 @@ qg_status cc_launch(CcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
     const uint32_t pe_bytes = align_up(static_cast<uint32_t>(a.C) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(a.C), 16);
     const uint32_t red_bytes = align_up(nbox * a.R8 * 4u, 128);
-    const uint32_t bar_bytes = (2 * kCcMaxStages + 1) * 8 + 16;
+    const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
     const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
     a.n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / a.stage_bytes));
@@ -909,7 +913,7 @@ qg_status cc_q45_launch(CcArgs a, const CUtensorMap (&maps)[4], int grid, cudaSt
     const uint32_t gx_bytes = align_up(static_cast<uint32_t>(a.C * NSEG) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(a.C), 16);
     const uint32_t red_bytes = align_up(nbox * a.R8 * 4u, 128);
-    const uint32_t bar_bytes = (2 * kCcMaxStages + 1) * 8 + 16;
+    const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
     const uint32_t fixed = x_bytes + pe_bytes + gx_bytes + fl_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
     a.n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / a.stage_bytes));
