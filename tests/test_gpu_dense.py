@@ -166,7 +166,7 @@ def test_q45(bits, M, N, K):
         check_out(y, yref, a, f"Q{bits} M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 8])
 def test_q45_residual(M):
     N, K = 640, 1024
     w = synth.q45_weights(19, "qres", N, K, 5)
@@ -178,6 +178,43 @@ def test_q45_residual(M):
     q.qgemv_q45(d["q_lo"], d["q_hi"], d["scale"], d["min"], 5, to_dev(x), y, residual=to_dev(r))
     torch.cuda.synchronize()
     check_out(y, yref, a, "Q5 residual")
+
+
+@pytest.mark.parametrize("bits", [4, 5])
+@pytest.mark.parametrize("M", [3, 8])
+def test_q45_long_k(bits, M):
+    """K = 17408 (68 stages): the stage ring wraps many times, and the
+    activation copies of the first ring's stages are issued after the
+    weight copies."""
+    N, K = 200, 17408
+    w = synth.q45_weights(26, f"qlong{bits}", N, K, bits)
+    x = synth.bf16_normal(27, "qlongx", (M, K))
+    yref, a = O.gemv_q45(w, x)
+    d = q45_dev(w)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    q.qgemv_q45(d["q_lo"], d["q_hi"], d["scale"], d["min"], bits, to_dev(x), y)
+    torch.cuda.synchronize()
+    check_out(y, yref, a, f"Q{bits} long K M={M}")
+
+
+def test_q45_deterministic_and_row_independent():
+    """Q4/Q5 with 2..8 tokens: repeated calls are bit-identical and a token's
+    result does not depend on the other tokens of the call."""
+    M, N, K = 8, 700, 2048
+    w = synth.q45_weights(33, "qdet", N, K, 5)
+    x = synth.bf16_normal(34, "qdetx", (M, K))
+    d = q45_dev(w)
+
+    def run(xb):
+        y = torch.empty((xb.shape[0], N), dtype=torch.float32, device="cuda")
+        q.qgemv_q45(d["q_lo"], d["q_hi"], d["scale"], d["min"], 5, to_dev(xb), y)
+        torch.cuda.synchronize()
+        return y.cpu().numpy()
+    y1, y2 = run(x), run(x)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32)), "two runs differ"
+    for m in (0, 6):
+        ym = run(np.stack([x[m], x[(m + 5) % M]]))
+        assert np.array_equal(ym[0].view(np.uint32), y1[m].view(np.uint32)), f"row {m}: M=2 call != M=8 call"
 
 
 # ---------------------------------------------------------------- activations
@@ -205,7 +242,7 @@ def test_nvfp4_wide_dynamic_range_activations(M):
 
 
 @pytest.mark.parametrize("bits", [4, 5])
-@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("M", [1, 2, 8])
 def test_q45_wide_dynamic_range_activations(bits, M):
     N, K = 200, 512
     w = synth.q45_weights(24, "qwide", N, K, bits)
