@@ -95,6 +95,8 @@ SHAPES = [
     (1, 1, 256), (1, 15, 512), (1, 17, 768), (2, 300, 1024), (3, 1000, 1280), (4, 4099, 512),
     (5, 2048, 2304), (6, 333, 4608), (7, 160, 256), (8, 1024, 1536), (8, 7001, 512),
     (1, 5000, 2048), (8, 64, 9216), (1, 40000, 256),
+    # two tokens: many units, few rows, long K
+    (2, 40000, 256), (2, 5000, 2048), (2, 17, 768), (2, 513, 17408),
     # K % 256 != 0 takes the exact CUDA-core kernel
     (1, 40, 32), (3, 77, 96), (8, 33, 800),
 ]
@@ -110,7 +112,7 @@ def test_nvfp4_shapes(M, N, K, out):
     check_out(run_nvfp4(w, x, dt), yref, a, f"nvfp4 M={M} N={N} K={K} {out}")
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 513, 1024), (8, 200, 768), (2, 96, 32 * 7)])
+@pytest.mark.parametrize("M,N,K", [(1, 513, 1024), (8, 200, 768), (2, 96, 32 * 7), (2, 513, 1024)])
 def test_nvfp4_residual(M, N, K):
     w = synth.nvfp4_weights(9, "res", N, K)
     x = synth.bf16_normal(10, "resx", (M, K))
@@ -134,7 +136,7 @@ def test_nvfp4_residual_in_place():
 
 
 @pytest.mark.parametrize("M,I,K", [(1, 256, 512), (1, 300, 1024), (4, 1000, 768), (8, 64, 2048), (3, 50, 96),
-                                   (1, 20000, 256)])
+                                   (1, 20000, 256), (2, 300, 1024), (2, 20000, 256)])
 def test_swiglu(M, I, K):
     w = synth.nvfp4_weights(15, f"sw{I}", 2 * I, K, g=1.25)
     x = synth.bf16_normal(16, "swx", (M, K))
@@ -231,7 +233,7 @@ def wide_range_x(M, K, seed):
     return T.from_numpy(v.astype(np.float32)).to(T.bfloat16).view(T.int16).numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("M", [1, 3, 8])
+@pytest.mark.parametrize("M", [1, 2, 3, 8])
 def test_nvfp4_wide_dynamic_range_activations(M):
     N, K = 300, 1024
     w = synth.nvfp4_weights(22, "wide", N, K)
@@ -282,7 +284,7 @@ def test_non_finite_activations_propagate():
 
 
 # ---------------------------------------------------------------- config 1 at full size
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 2, 8])
 def test_dense_layer_full_size(M):
     d27 = synth.DENSE27B
     for name, N, K, epi in synth.dense_layer_shapes():
