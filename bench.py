@@ -466,8 +466,17 @@ def cpu_baseline(kind, M, budget_s=12.0):
     if t < budget_s / 4 and frac > 1:                 # grow the sample toward the budget
         frac = max(1, int(frac * t / (budget_s / 2))) if t > 0 else 1
         t, b = oracle_step_sample(projs, M, frac, threads)
+    passes = 1
+    if frac == 1 and t < budget_s / 2:                # a whole step is short: repeat it
+        passes = max(1, min(5000, int(budget_s / max(t, 1e-4))))
+        tt, bb = 0.0, 0
+        for _ in range(passes):
+            t1, b1 = oracle_step_sample(projs, M, frac, threads)
+            tt += t1
+            bb += b1
+        t, b = tt, bb
     return {"value": b / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"every {frac}th output row of each projection of one step (M={M}), "
+            "sample": f"every {frac}th output row of each projection of one step (M={M}), {passes} pass(es), "
                       f"{b / 1e6:.1f} MB of weights in {t:.1f} s"}
 
 
