@@ -8,8 +8,14 @@ batch of M tokens:
                    with the residual epilogue; every projection reads its own
                    bf16 N(0, 1) activations;
   q45:             the same shapes under the mixed Q4/Q5 recipe;
-  tiny:            one NVFP4 256x512 GEMV.
+  tiny:            one NVFP4 256x512 GEMV;
+  moe:             35B-A3B-class MoE layer at M = 8 (device router, then the
+                   expert-gathered gate/up + SwiGLU, down and combine).
 Metric: effective weight-bytes GB/s (weight bytes per step / step time).
+The JSON line is the selected workload (default: dense, M = 1); its "sweep"
+array holds the same measurements for every other configuration (dense at
+M = 2, 4, 8; Q4/Q5 at M = 1, 8; tiny; MoE), each with its roofline and its
+oracle baseline (--no-sweep skips them).
 
 Timing: W untimed warm-up steps, then exactly K steps captured in one CUDA
 graph and bracketed by CUDA events on the launching stream (barrier +
@@ -22,8 +28,9 @@ e2e: the same metric through the public Python API with pinned host buffers:
 every step copies its activations host->device, runs the projections, and
 copies the outputs device->host, all inside the timed region.
 
---impl reference: the fp64 CPU oracle (the checker, not a product path) timed
-on the host cores over a bounded sample of the same workload.
+cpu_baseline: the fp64 oracle on the host cores over whole steps of the same
+workload (repeated to about 12 s; 4 s in the sweep), and with one thread.
+--impl reference: the same oracle as the reference arm, K whole steps.
 """
 from __future__ import annotations
 
@@ -57,6 +64,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-read-probe", action="store_true")
+    ap.add_argument("--sweep", dest="sweep", action="store_true", default=True,
+                    help="also measure every other configuration (default)")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     return ap.parse_args()
 
 
@@ -322,13 +332,7 @@ class Workload:
         return b
 
     def describe(self):
-        if self.kind == "dense":
-            return ("dense 27B-class decode layer, NVFP4: QKV 7168x5120, O 5120x6144, "
-                    f"gate+up 34816x5120 + SwiGLU, down 5120x17408 + residual, M={self.M}")
-        if self.kind == "q45":
-            return ("mixed Q4/Q5 groupwise-int layer on the 27B-class shapes (QK Q4, V Q5, O Q4, "
-                    f"gate Q5, up Q4, down Q4 + residual), M={self.M}")
-        return f"tiny NVFP4 GEMV 256x512, M={self.M}"
+        return WORKLOAD_NAMES[self.kind](self.M)
 
 
 class MoeWorkload:
@@ -408,14 +412,13 @@ class MoeWorkload:
         return self.weight_bytes + 2 * self.M * self.H * 2
 
     def describe(self):
-        return (f"MoE decode layer (35B-A3B-class): hidden {self.H}, {self.E} experts, intermediate {self.I}, "
-                f"top-{self.topk}, M={self.M}; {self.n_active} distinct experts active")
+        return WORKLOAD_NAMES["moe"](self.M) + f"; {self.n_active} distinct experts active"
 
 
 # ------------------------------------------------------------------ CPU oracle
 def oracle_step_sample(wl_projs, M, frac, threads):
-    """Run the fp64 oracle on every `1/frac`-th output row of each projection;
-    returns (seconds, weight bytes processed)."""
+    """Run the fp64 oracle on every `frac`-th output row of each projection
+    (frac = 1: the whole step); returns (seconds, weight bytes processed)."""
     import numpy as np
     import oracle as O
     import synth
@@ -424,19 +427,20 @@ def oracle_step_sample(wl_projs, M, frac, threads):
         rows = np.arange(0, N, frac)
         x = synth.bf16_normal(2, f"oracle.{name}.M{M}", (M, K))
         if "codes" in w:
-            ws = {"codes": w["codes"][rows], "scales": w["scales"][rows], "g": w["g"]}
+            ws = w if frac == 1 else {"codes": w["codes"][rows], "scales": w["scales"][rows], "g": w["g"]}
             t0 = time.perf_counter()
             O.gemv_nvfp4(ws, x, threads=threads)
             t_total += time.perf_counter() - t0
             bytes_done += ws["codes"].nbytes + ws["scales"].nbytes
         else:
-            ws = {"q_lo": w["q_lo"][rows], "q_hi": None if w.get("q_hi") is None else w["q_hi"][rows],
-                  "scale": w["scale"][rows], "min": w["min"][rows], "bits": w["bits"]}
+            ws = w if frac == 1 else {
+                "q_lo": w["q_lo"][rows], "q_hi": None if w.get("q_hi") is None else w["q_hi"][rows],
+                "scale": w["scale"][rows], "min": w["min"][rows], "bits": w["bits"]}
             t0 = time.perf_counter()
             O.gemv_q45(ws, x, threads=threads)
             t_total += time.perf_counter() - t0
-            bytes_done += sum(a.nbytes for a in (ws["q_lo"], ws["scale"], ws["min"]) if a is not None)
-            if ws["q_hi"] is not None:
+            bytes_done += sum(a.nbytes for a in (ws["q_lo"], ws["scale"], ws["min"]))
+            if ws.get("q_hi") is not None:
                 bytes_done += ws["q_hi"].nbytes
     return t_total, bytes_done
 
@@ -456,54 +460,133 @@ def host_projs(kind):
     return out
 
 
-def cpu_baseline(kind, M, budget_s=12.0):
-    """Oracle throughput on this host's cores over a bounded row sample."""
+class OracleMoe:
+    """The MoE step on the oracle: the same seeded experts and routing as the
+    GPU workload, gate/up + SwiGLU for every (token, slot), then the down
+    projections combined in slot order. Weight bytes per step = distinct
+    experts x bytes per expert (the metric's definition)."""
+
+    def __init__(self, M):
+        import numpy as np
+        import oracle as O
+        import synth
+        c = synth.MOE35B
+        E, H, I = c.experts, c.hidden, c.inter
+        gu = synth.nvfp4_weights(4, "moe.gu", E * 2 * I, H)
+        dn = synth.nvfp4_weights(4, "moe.dn", E * H, I)
+        self.expert_bytes = (gu["codes"].nbytes + gu["scales"].nbytes + dn["codes"].nbytes
+                             + dn["scales"].nbytes) // E
+        self.gu = {"codes": gu["codes"].reshape(E, 2 * I, H // 2), "scales": gu["scales"].reshape(E, 2 * I, H // 16),
+                   "g": np.ones(E)}
+        self.dn = {"codes": dn["codes"].reshape(E, H, I // 2), "scales": dn["scales"].reshape(E, H, I // 16),
+                   "g": np.ones(E)}
+        self.x = synth.bf16_normal(4, "moe.x", (M, H))
+        lg = synth.router_logits(4, "moe.logits", M, E)
+        self.ids, self.w = O.route_topk(lg, c.topk)
+        self.n_active = int(np.unique(self.ids).size)
+        self.step_bytes = self.n_active * self.expert_bytes
+
+    def step(self, threads):
+        import oracle as O
+        t0 = time.perf_counter()
+        _, _, _, _, h = O.moe_gate_up(self.gu, self.x, self.ids, threads=threads)
+        O.moe_down(self.dn, O.bf16_array(h), self.ids, self.w, threads=threads)
+        return time.perf_counter() - t0, self.step_bytes
+
+
+def oracle_runner(kind, M):
+    """A callable (threads, frac) -> (seconds, weight bytes) for one oracle
+    step of the workload (frac > 1: every frac-th output row only; the MoE
+    step is always whole), the workload's name and its weight bytes per step."""
+    if kind == "moe":
+        om = OracleMoe(M)
+        name = WORKLOAD_NAMES["moe"](M) + f"; {om.n_active} distinct experts active"
+        return (lambda threads, frac: om.step(threads)), name, om.step_bytes
+    projs = host_projs(kind)
+    wb = 0
+    for *_, w in projs:
+        wb += sum(w[k].nbytes for k in ("codes", "scales", "q_lo", "q_hi", "scale", "min")
+                  if w.get(k) is not None and hasattr(w[k], "nbytes"))
+    return (lambda threads, frac: oracle_step_sample(projs, M, frac, threads)), WORKLOAD_NAMES[kind](M), wb
+
+
+def cpu_baseline(kind, M, budget_s=12.0, single_thread_budget_s=6.0):
+    """Oracle throughput on this host's cores: whole steps of the workload,
+    repeated until about budget_s of CPU work (a row sample only if one step
+    alone exceeds the budget), plus the same with one thread."""
     import oracle as O
     threads = O.default_threads()
-    projs = host_projs(kind)
-    frac = 64
-    t, b = oracle_step_sample(projs, M, frac, threads)
-    if t < budget_s / 4 and frac > 1:                 # grow the sample toward the budget
-        frac = max(1, int(frac * t / (budget_s / 2))) if t > 0 else 1
-        t, b = oracle_step_sample(projs, M, frac, threads)
-    passes = 1
-    if frac == 1 and t < budget_s / 2:                # a whole step is short: repeat it
-        passes = max(1, min(5000, int(budget_s / max(t, 1e-4))))
-        tt, bb = 0.0, 0
-        for _ in range(passes):
-            t1, b1 = oracle_step_sample(projs, M, frac, threads)
-            tt += t1
-            bb += b1
-        t, b = tt, bb
-    return {"value": b / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"every {frac}th output row of each projection of one step (M={M}), {passes} pass(es), "
-                      f"{b / 1e6:.1f} MB of weights in {t:.1f} s"}
+    run, _, _ = oracle_runner(kind, M)
+
+    def timed(nthreads, budget):
+        t, b = run(nthreads, 1)
+        frac, passes = 1, 1
+        if t > budget and kind != "moe":               # one whole step is too long: sample rows
+            frac = max(2, int(math.ceil(t / budget)))
+            t, b = run(nthreads, frac)
+        elif t < budget / 2:                           # a whole step is short: repeat it
+            passes = max(1, min(5000, int(budget / max(t, 1e-4))))
+            for _ in range(passes - 1):
+                t1, b1 = run(nthreads, 1)
+                t += t1
+                b += b1
+        return b / t / 1e9, frac, passes, t, b
+
+    v, frac, passes, t, b = timed(threads, budget_s)
+    v1, frac1, passes1, t1, b1 = timed(1, single_thread_budget_s)
+    what = "whole steps" if frac == 1 else f"every {frac}th output row of each projection"
+    return {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{what} of the workload (M={M}), {passes} pass(es), {b / 1e6:.1f} MB of weights in {t:.1f} s",
+            "single_thread": {"value": v1, "unit": "GB/s", "cores": 1,
+                              "sample": f"{'whole steps' if frac1 == 1 else f'every {frac1}th row'}, "
+                                        f"{passes1} pass(es), {b1 / 1e6:.1f} MB in {t1:.1f} s"}}
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle (the method's plain definition)
+    timed on the host cores, W untimed then K timed whole steps of the same
+    workload as the GPU arm (rows sampled only if K whole steps would take
+    more than about two minutes)."""
     if rank != 0:
         return
     import oracle as O
     threads = O.default_threads()
-    projs = host_projs(args.workload)
-    frac = 64
+    kind = args.workload
+    M = 8 if kind == "moe" else (1 if kind == "tiny" else args.M)
+    run, name, step_bytes = oracle_runner(kind, M)
+    t1, _ = run(threads, 1)
+    frac = 1
+    if kind != "moe" and t1 * (args.steps + args.warmup) > 120.0:
+        frac = max(2, int(math.ceil(t1 * (args.steps + args.warmup) / 120.0)))
     for _ in range(args.warmup):
-        oracle_step_sample(projs, args.M, frac * 4, threads)
+        run(threads, frac)
     tt, bb = 0.0, 0
     for _ in range(args.steps):
-        t, b = oracle_step_sample(projs, args.M, frac, threads)
+        t, b = run(threads, frac)
         tt += t
         bb += b
     v = bb / tt / 1e9
+    sample = ("whole steps of the workload" if frac == 1 else
+              f"every {frac}th output row of each projection per step")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"{args.workload} (oracle over a row sample)", "M": args.M},
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": f"every {frac}th output row of each projection per step"},
+            "config": {"workload": name, "M": M, "weight_bytes_per_step": step_bytes, "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+WORKLOAD_NAMES = {
+    "dense": lambda M: ("dense 27B-class decode layer, NVFP4: QKV 7168x5120, O 5120x6144, "
+                        f"gate+up 34816x5120 + SwiGLU, down 5120x17408 + residual, M={M}"),
+    "q45": lambda M: ("mixed Q4/Q5 groupwise-int layer on the 27B-class shapes (QK Q4, V Q5, O Q4, "
+                      f"gate Q5, up Q4, down Q4 + residual), M={M}"),
+    "tiny": lambda M: f"tiny NVFP4 GEMV 256x512, M={M}",
+    "moe": lambda M: (f"MoE decode layer (35B-A3B-class): hidden 2048, 128 experts, intermediate 768, "
+                      f"top-8, M={M}"),
+}
 
 
 # ------------------------------------------------------------------ main
@@ -541,27 +624,16 @@ def arithmetic(workload, M):
     return "f16 tcgen05 MMA, f32 accumulate (exact decoded weights, prescaled activations)"
 
 
-def main():
-    args = parse_args()
-    rank, world, local = dist_setup(args.gpus)
-    if args.impl == "reference":
-        run_reference(args, rank, world)
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return
-    assert args.warmup >= 3, "at least 3 warm-up steps"
+def measure(args, kind, M, world, rank, stream, cpu=True, e2e=True):
+    """Time one workload: K steps in one CUDA graph (the headline), per-kernel
+    durations, the dominant kernel alone for the roofline, the end-to-end
+    loop through the Python API, and the oracle beside it."""
     import torch
     import bit_quantized_weight_gb300 as q
-    torch.cuda.set_device(local)
-    if args.workload == "tiny":
-        args.M = 1
-    if args.workload == "moe":
-        args.M = 8
-        wl = MoeWorkload(args.M, copies_min_bytes=4)
+    if kind == "moe":
+        wl = MoeWorkload(M, copies_min_bytes=4)
     else:
-        wl = Workload(args.workload, args.M, copies_min_bytes=4)
-    stream = torch.cuda.Stream()
+        wl = Workload(kind, M, copies_min_bytes=4)
     n_calls = len(wl.kernel_names())
 
     with torch.cuda.stream(stream):
@@ -570,7 +642,6 @@ def main():
     stream.synchronize()
     assert q.qg_last_device_status(stream) == q.QG_OK
 
-    # ---- capture K steps (and a warm-up graph of W steps) with in-graph events
     def make_events(n):
         try:
             return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
@@ -598,7 +669,7 @@ def main():
     stream.synchronize()
 
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(torch.cuda.current_device())
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
@@ -655,12 +726,11 @@ def main():
         g_dom.replay()
         e1.record(stream)
     stream.synchronize()
-    dom_alone_us = e0.elapsed_time(e1) / args.steps * 1e3
+    dom_us = e0.elapsed_time(e1) / args.steps * 1e3
     peak, peak_kind = measured_peaks()
     dom_name = wl.kernel_names()[dom]
-    dom_us = dom_alone_us
     achieved = wl.alg_bytes(dom) / (dom_us * 1e-6) / 1e9
-    traffic = profiled_traffic(f"{args.workload}.{dom_name}.M{args.M}", kernel_family(args.workload, args.M))
+    traffic = profiled_traffic(f"{kind}.{dom_name}.M{M}", kernel_family(kind, M))
     roofline = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s", "traffic": traffic,
@@ -668,8 +738,8 @@ def main():
                 "timing": "the kernel alone, K launches in one CUDA graph, events on its stream"}
 
     # ---- end to end through the public API with pinned host buffers
-    e2e = None
-    if not args.no_e2e:
+    e2e_line = None
+    if e2e:
         h_in = torch.from_numpy(wl.host_in.view("int16")).view(torch.bfloat16).pin_memory()
         h_out = torch.empty(wl.out_elems, dtype=torch.bfloat16).pin_memory()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -688,37 +758,87 @@ def main():
             e1.record(stream)
         stream.synchronize()
         ems = max_over_ranks(e0.elapsed_time(e1), world)
-        e2e = {"value": wl.weight_bytes * args.steps * world / (ems * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": wl.in_elems * 2, "d2h_bytes_per_step": wl.out_elems * 2,
-               "ms_per_step": ems / args.steps}
+        e2e_line = {"value": wl.weight_bytes * args.steps * world / (ems * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": wl.in_elems * 2, "d2h_bytes_per_step": wl.out_elems * 2,
+                    "ms_per_step": ems / args.steps}
 
+    cpu_line = cpu_baseline(kind, M, **({} if args.sweep_entry_budget is None else
+                                        {"budget_s": args.sweep_entry_budget,
+                                         "single_thread_budget_s": args.sweep_entry_budget / 2})) \
+        if (cpu and rank == 0 and world == 1) else None
+    out = {"workload": wl.describe(), "kind": kind, "M": M, "value": value, "unit": "GB/s",
+           "ms_per_step": ms_per_step, "weight_bytes_per_step": wl.weight_bytes,
+           "frac_of_measured_hbm": value / world / peak, "frac_of_8tbs": value / world / NOMINAL_HBM_GBS,
+           "us_per_call": us_per_call, "roofline": roofline, "e2e": e2e_line, "cpu_baseline": cpu_line,
+           "clocks": clk, "gpu_launches": wl.launches_per_step() * args.steps,
+           "dtype": arithmetic(kind, M), "l2": f"weights rotate over {wl.copies} copies "
+           f"({wl.copies * wl.weight_bytes / 1e6:.0f} MB vs {wl.l2_bytes / 1e6:.0f} MB L2)"}
+    del wl, g_warm, g_main, g_ev, g_dom
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+# Every configuration besides the headline one, measured in the same run.
+SWEEP = [("dense", 2), ("dense", 4), ("dense", 8), ("q45", 1), ("q45", 8), ("tiny", 1), ("moe", 8)]
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    import torch
+    import bit_quantized_weight_gb300 as q
+    torch.cuda.set_device(local)
+    if args.workload == "tiny":
+        args.M = 1
+    if args.workload == "moe":
+        args.M = 8
+    stream = torch.cuda.Stream()
+    args.sweep_entry_budget = None
+    head = measure(args, args.workload, args.M, world, rank, stream, cpu=not args.no_cpu_baseline,
+                   e2e=not args.no_e2e)
+    peak, _ = measured_peaks()
     probe = read_probe_bandwidth(torch, q, stream, peak) if rank == 0 and not args.no_read_probe else None
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload != "moe":
-        cpu = cpu_baseline(args.workload, args.M)
+    sweep = []
+    if args.sweep and world == 1:
+        args.sweep_entry_budget = 4.0
+        for kind, M in SWEEP:
+            if (kind, M) == (args.workload, args.M):
+                continue
+            try:
+                sweep.append(measure(args, kind, M, world, rank, stream, cpu=not args.no_cpu_baseline))
+            except Exception as ex:                  # one configuration failing must not hide the rest
+                sweep.append({"kind": kind, "M": M, "error": f"{type(ex).__name__}: {ex}"})
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": arithmetic(args.workload, args.M),
+            "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
             "data": "synthetic",
-            "config": {"workload": wl.describe(), "M": args.M, "weight_bytes_per_step": wl.weight_bytes,
-                       "l2": f"weights rotate over {wl.copies} copies of the layer "
-                             f"({wl.copies * wl.weight_bytes / 1e6:.0f} MB vs {wl.l2_bytes / 1e6:.0f} MB L2)",
+            "config": {"workload": head["workload"], "M": args.M,
+                       "weight_bytes_per_step": head["weight_bytes_per_step"], "l2": head["l2"],
                        "parallelism": "one independent replica per GPU" if world > 1 else "single GPU",
                        "graph": "K steps captured in one CUDA graph (kernels only); us_per_call from a "
                                 "second graph with events between the calls (which serialise them)"},
-            "frac_of_8tbs": value / world / NOMINAL_HBM_GBS,
-            "frac_of_measured_hbm": value / world / peak,
-            "us_per_call": us_per_call,
-            "roofline": roofline,
+            "frac_of_8tbs": head["frac_of_8tbs"],
+            "frac_of_measured_hbm": head["frac_of_measured_hbm"],
+            "us_per_call": head["us_per_call"],
+            "roofline": head["roofline"],
             "read_probe": probe,
-            "gpu_launches": wl.launches_per_step() * args.steps,
-            "clocks": clk,
-            "e2e": e2e,
-            "cpu_baseline": cpu,
+            "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"],
+            "e2e": head["e2e"],
+            "cpu_baseline": head["cpu_baseline"],
+            "sweep": sweep,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

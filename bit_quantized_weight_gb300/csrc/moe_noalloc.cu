@@ -29,7 +29,12 @@ void* g_scratch_ptr[kMaxDevices] = {nullptr};
 
 // Device address of the scratch array on the current device. In host code
 // the array's name is only a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress, once per device, with that device current. With lazy
+// module loading (the CUDA default) that first lookup is also what makes the
+// driver load the library's device code, and with it reserve the 4 MiB, on
+// that device. The cached address is only valid while the device's primary
+// context lives: after cudaDeviceReset the library must not be called again
+// on that device in the same process.
 void* scratch_on_current_device()
 {
     int device = -1;
@@ -52,9 +57,17 @@ extern "C" qg_status moe_qgemv_nvfp4_noalloc(const uint8_t* gu_codes, const uint
                                               const int32_t* topk_ids, const float* topk_w, void* y, int M, int H,
                                               int I, int E, int topk, cudaStream_t stream)
 {
+    // Same checks, in the same order, as moe_qgemv_nvfp4: pointers and sizes
+    // first, so a call is rejected before anything touches CUDA.
+    if (!gu_codes || !gu_scales || !gu_gscale || !dn_codes || !dn_scales || !dn_gscale || !x || !topk_ids ||
+        !topk_w || !y)
+        return QG_ERR_INVALID_ARG;
     size_t need = 0;
     const qg_status s = moe_qgemv_nvfp4_workspace_size(M, topk, H, I, E, &need);
     if (s != QG_OK) return s;
+    const void* ptrs[] = {gu_codes, gu_scales, gu_gscale, dn_codes, dn_scales, dn_gscale, x, topk_ids, topk_w, y};
+    for (const void* p : ptrs)
+        if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return QG_ERR_MISALIGNED;
     if (need > qg::kNoAllocScratchBytes) return QG_ERR_WORKSPACE;
     void* scratch = qg::scratch_on_current_device();
     if (!scratch) return QG_ERR_CUDA;

@@ -23,6 +23,9 @@
  *   - Arguments are validated before anything is launched; a rejected call
  *     launches nothing. A launch failure returns QG_ERR_CUDA and leaves the
  *     CUDA error retrievable with cudaGetLastError().
+ *   - The library caches per-device state (the status word's address,
+ *     kernel attributes) for the life of the process; after cudaDeviceReset
+ *     it must not be called again on that device.
  *   - Activations x and residuals are bf16 [M][K] / [M][N]; M in [1, 8]
  *     (the 1..8 decode lanes); K % 32 == 0 and K >= 32; N >= 1.
  *   - Weights are read once per call; accumulation is fp32.
@@ -155,12 +158,19 @@ QG_API qg_status moe_qgemv_nvfp4(const uint8_t* gu_codes, const uint8_t* gu_scal
  * memory and offers no allocator, or a latency-critical decode loop that may
  * not call cudaMalloc. The pages have no counterpart; this is a library
  * convenience. Arguments and results are those of moe_qgemv_nvfp4.
- *   - The scratch is a fixed 4 MiB device array inside the library image
- *     (every GPU that loads the library holds it until exit). Sizes whose
+ *   - The scratch is a fixed 4 MiB device array inside the library image;
+ *     once loaded on a GPU it stays there until the process exits. Sizes whose
  *     moe_qgemv_nvfp4_workspace_size() exceeds 4 MiB return QG_ERR_WORKSPACE
- *     (at M = 8 and top-8, H = 4096 with I = 2048 still fits).
+ *     (at M = 8 and top-8, H = 4096 with I = 2048 still fits). Arguments are
+ *     checked as moe_qgemv_nvfp4 checks them, before the size limit.
  *   - The first call on a device looks up the array's device address; make
- *     that first call before any stream capture on that device.
+ *     that first call before any stream capture on that device. Under lazy
+ *     module loading (the CUDA default) that first call is also when the
+ *     driver loads the library's device code on that device and reserves the
+ *     4 MiB, so it can fail with QG_ERR_CUDA if device memory is exhausted;
+ *     later calls reserve nothing.
+ *   - The address is cached per device for the life of the process: do not
+ *     call this after cudaDeviceReset on that device.
  *   - All calls share the one array and it keeps the last call's contents
  *     (nothing in it needs to start at zero). Calls that overlap on the GPU
  *     -- on different streams, or from several host threads -- race; order

@@ -69,3 +69,39 @@ def same_f32_bits(a, b) -> bool:
     both_nan = np.isnan(a) & np.isnan(b)
     eq = (a.view(np.uint32) == b.view(np.uint32)) | ((a == 0) & (b == 0)) | both_nan
     return bool(eq.all())
+
+
+def q_split_ratio(w: dict, x_bits, B, chain: int):
+    """A-priori error bound of the groupwise-int split, relative to B.
+
+    The Q kernels compute each group's contribution as scale*sum(q x) +
+    min*sum(x) in fp32. With d the longest sequential chain of fp32 roundings
+    an output element meets (`chain`), the error is at most d * 2^-24 * T,
+    T = sum_g (|scale_g| sum_{k in g} |q_k x_k| + |min_g| sum_{k in g} |x_k|),
+    which can exceed the stated bound B when scale*q and min cancel inside
+    the groups. Returns the largest d * 2^-24 * T / B over the outputs.
+    """
+    x = O.bf16_array(np.asarray(x_bits, np.uint16))          # [M][K]
+    lo = np.asarray(w["q_lo"], np.uint8)
+    q = np.empty((lo.shape[0], lo.shape[1] * 2), np.float64)
+    q[:, 0::2] = lo & 0xF
+    q[:, 1::2] = lo >> 4
+    if w.get("q_hi") is not None:
+        hi = np.unpackbits(np.asarray(w["q_hi"], np.uint8), axis=1, bitorder="little")
+        q += 16.0 * hi
+    s = np.abs(O.f16_array(w["scale"]))                     # [N][K/32]
+    mn = np.abs(O.f16_array(w["min"]))
+    N, K = q.shape
+    G = K // 32
+    ax = np.abs(x).reshape(x.shape[0], G, 32)                # [M][G][32]
+    qx = np.einsum("ngk,mgk->mng", q.reshape(N, G, 32), ax)  # sum_k |q x| per group
+    sx = ax.sum(axis=2)                                      # [M][G]
+    T = np.einsum("ng,mng->mn", s, qx) + np.einsum("ng,mg->mn", mn, sx)
+    return float(np.max(chain * 2.0 ** -24 * T / B))
+
+
+def q_chain(K: int) -> int:
+    """Longest fp32 rounding chain of the groupwise-int kernels for K: up to
+    32 products in a group, two accumulations per group along K, and the
+    cross-lane, cross-warp and phase reductions."""
+    return 32 + 2 * (K // 32) + 32

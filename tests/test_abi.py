@@ -118,6 +118,19 @@ def test_router_and_moe_validation(L):
 
 
 @fake_ptr
+def test_noalloc_moe_validation(L):
+    args = [A] * 10
+    # the same argument checks as the workspace entry point, in the same order
+    assert L.moe_qgemv_nvfp4_noalloc(None, *args[1:], 8, 2048, 768, 128, 8, None) == 1
+    assert L.moe_qgemv_nvfp4_noalloc(*args, 8, 2048, 768, 128, 9, None) == 1
+    assert L.moe_qgemv_nvfp4_noalloc(A + 8, *args[1:], 8, 2048, 768, 128, 8, None) == 3
+    # misaligned and too large: the pointer check comes first
+    assert L.moe_qgemv_nvfp4_noalloc(A + 8, *args[1:], 8, 16384, 8192, 64, 8, None) == 3
+    # H = 16384, I = 8192 at M = 8, top-8 needs far more than the 4 MiB scratch
+    assert L.moe_qgemv_nvfp4_noalloc(*args, 8, 16384, 8192, 64, 8, None) == 4
+
+
+@fake_ptr
 def test_dequant_validation(L):
     assert L.qdequant_nvfp4(A, A, 1.0, A, 0, 256, None) == 1
     assert L.qdequant_nvfp4(A, A, 1.0, A + 4, 16, 256, None) == 3

@@ -284,7 +284,7 @@ def test_non_finite_activations_propagate():
 
 
 # ---------------------------------------------------------------- config 1 at full size
-@pytest.mark.parametrize("M", [1, 2, 8])
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
 def test_dense_layer_full_size(M):
     d27 = synth.DENSE27B
     for name, N, K, epi in synth.dense_layer_shapes():
@@ -370,19 +370,50 @@ def test_rejects_misaligned_device_pointers():
     assert L.qgemv_nvfp4(p, p, 1.0, p, p, 0, None, 0, 16, 256, None) == q.QG_ERR_INVALID_ARG
 
 
-def test_bounded_wait_reports_timeout_and_recovers():
-    N, K = 512, 1024
-    w = synth.nvfp4_weights(34, "starve", N, K)
-    x = synth.bf16_normal(35, "starvex", (1, K))
+def _nvfp4_call(M, N, K, seed):
+    w = synth.nvfp4_weights(seed, f"starve{M}", N, K)
+    x = synth.bf16_normal(seed + 1, f"starvex{M}", (M, K))
     d = nvfp4_dev(w)
-    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    xd = to_dev(x)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+
+    def call():
+        q.qgemv_nvfp4(d["codes"], d["scales"], 1.0, xd, y)
+    ref = O.gemv_nvfp4(w, x)
+    return call, y, ref
+
+
+def _q5_call(M, N, K, seed):
+    w = synth.q45_weights(seed, f"starveq{M}", N, K, 5)
+    x = synth.bf16_normal(seed + 1, f"starveqx{M}", (M, K))
+    d = q45_dev(w)
+    xd = to_dev(x)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+
+    def call():
+        q.qgemv_q45(d["q_lo"], d["q_hi"], d["scale"], d["min"], 5, xd, y)
+    ref = O.gemv_q45(w, x)
+    return call, y, ref
+
+
+# One case per pipelined kernel: the one-token CUDA-core NVFP4 and Q5
+# kernels, the tcgen05 kernel (NVFP4, 8 tokens) and the mma.sync
+# groupwise-int kernel (Q5, 8 tokens).
+STARVE_CASES = [("nvfp4", 1), ("nvfp4", 8), ("q5", 1), ("q5", 8)]
+
+
+@pytest.mark.parametrize("fmt,M", STARVE_CASES)
+def test_bounded_wait_reports_timeout_and_recovers(fmt, M):
+    N, K = 512, 1024
+    call, y, (yref, a) = (_nvfp4_call if fmt == "nvfp4" else _q5_call)(M, N, K, 34 + M)
     assert q.qg_last_device_status() == q.QG_OK
-    q.qg_debug_set_wait(20_000_000, True)             # 20 ms, producer issues nothing
+    q.qg_debug_set_wait(20_000_000, True)             # 20 ms, the weight stream issues nothing
     try:
-        q.qgemv_nvfp4(d["codes"], d["scales"], 1.0, to_dev(x), y)
+        call()
         assert q.qg_last_device_status() == q.QG_ERR_DEVICE_TIMEOUT
     finally:
         q.qg_debug_set_wait(0, False)
-    yref, a = O.gemv_nvfp4(w, x)
-    check_out(run_nvfp4(w, x, torch.float32), yref, a, "after timeout")
+    call()                                            # a clean call right after
+    torch.cuda.synchronize()
     assert q.qg_last_device_status() == q.QG_OK
+    check_out(y, yref, a, f"{fmt} M={M} after timeout")

@@ -156,3 +156,24 @@ def test_moe_duplicate_and_invalid_expert_ids():
     assert q.qg_last_device_status() == q.QG_ERR_INVALID_ARG
     check_moe(gu, dn, x, ids, w, y, h, valid=valid)
     assert q.qg_last_device_status() == q.QG_OK
+
+
+def test_moe_bounded_wait_reports_timeout_and_recovers():
+    """The grouped expert kernels' waits run out when the weight stream
+    issues nothing; the call reports QG_ERR_DEVICE_TIMEOUT and a clean call
+    right after matches the oracle."""
+    M, E, H, I, topk = 4, 6, 256, 512, 2
+    gu, dn, x = make_moe(12, E, H, I, M)
+    r = np.random.default_rng(13)
+    ids = np.stack([r.choice(E, topk, replace=False) for _ in range(M)]).astype(np.int32)
+    w = r.uniform(0.05, 1.0, (M, topk)).astype(np.float32).astype(np.float64)
+    assert q.qg_last_device_status() == q.QG_OK
+    q.qg_debug_set_wait(20_000_000, True)
+    try:
+        run_moe(gu, dn, x, ids, w)
+        assert q.qg_last_device_status() == q.QG_ERR_DEVICE_TIMEOUT
+    finally:
+        q.qg_debug_set_wait(0, False)
+    y, h = run_moe(gu, dn, x, ids, w)
+    assert q.qg_last_device_status() == q.QG_OK
+    check_moe(gu, dn, x, ids, w, y, h)
