@@ -1,0 +1,407 @@
+// cc_core.cuh -- the one-token CUDA-core GEMV's shared device code: its
+// argument block, bounded waits, the exact activation conversion into
+// shared memory and the per-stage dot-product code for NVFP4 and Q4/Q5.
+// Included by the standalone one-token kernels (qgemv_cc.cu) and by the
+// chained-layer kernel (qgemv_chain.cu); qgemv_cc.cu describes what they
+// compute.
+#pragma once
+
+#include "common.cuh"
+
+namespace qg {
+
+namespace {
+
+constexpr int kCcWarps = 16;                          // compute warps 0-15
+constexpr int kCcThreads = 32 * kCcWarps;
+constexpr int kCcTmaWarp = kCcWarps;                  // warp 16: TMA producer
+constexpr int kCcAllThreads = 32 * (kCcWarps + 1);
+constexpr int kCcMaxStages = 16;
+// Stages the producer issues before it waits for the previous kernel to
+// complete: CTAs that start early (their SM freed first) then cannot queue a
+// whole ring of weight traffic ahead of the CTAs that start late.
+constexpr int kCcLeadStages = 1;
+constexpr int kCcRows = 4;                            // rows per thread
+constexpr uint32_t kCcSmemMax = 227u * 1024u;
+
+struct CcArgs {
+    const uint16_t* x;         // bf16 activations, K values
+    void* y;
+    const uint16_t* residual;  // bf16 [n_out] or nullptr
+    int K;
+    int C;                     // K / 256
+    int n_out;
+    int R;                     // output rows per unit
+    int R8;                    // R rounded up to 8: row stride of a box in shared memory
+    int P;                     // K phases
+    int Cp;                    // stages per phase
+    int up_row_offset;         // SwiGLU: up row = gate row + this
+    int out_f32;
+    float g;
+    int n_units;
+    int n_stages;
+    uint32_t stage_bytes;
+    uint32_t scales_off;
+    uint32_t box_tx;
+    uint32_t smem_ring;
+    uint32_t smem_x;           // activations: C chunks of 256 f16 (or raw bf16)
+    uint32_t smem_pe;          // C floats: 2^-prescale of each chunk
+    uint32_t smem_fl;          // C bytes: 1 = chunk kept as raw bf16
+    uint32_t smem_red;         // partial sums: P * NGU * R8 rows
+    uint32_t smem_bar;
+    // groupwise-int layouts only
+    uint32_t mins_off;         // min boxes inside a stage
+    uint32_t hi_off;           // Q5 high-bit boxes inside a stage
+    uint32_t smem_gx;          // C * NSEG floats: sum of x over each k segment
+    uint64_t wait_ns;
+    int starve;
+    int* status;
+};
+
+__device__ __forceinline__ bool cc_wait_warp(uint64_t* bar, uint32_t parity, const CcArgs& a,
+                                             volatile int* abort_flag)
+{
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok) {
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+            if (mbar_try_wait_sleep(bar, parity, 20000u)) {
+                ok = true;
+                break;
+            }
+            if (*abort_flag) break;
+            if (global_timer_ns() - t0 > a.wait_ns) {
+                set_device_status(a.status, QG_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// acc + lo(w) * lo(x) and acc + hi(w) * hi(x): f16 (or bf16) operands, exact
+// product, fp32 accumulation.
+template <bool BF>
+__device__ __forceinline__ float fma2_mixed(uint32_t w, uint32_t x, float acc)
+{
+    float r;
+    if (BF)
+        asm("{\n .reg .b16 wl, wh, xl, xh;\n .reg .f32 t;\n mov.b32 {wl, wh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+            " fma.rn.f32.bf16 t, wl, xl, %3;\n fma.rn.f32.bf16 %0, wh, xh, t;\n}\n"
+            : "=f"(r)
+            : "r"(w), "r"(x), "f"(acc));
+    else
+        asm("{\n .reg .b16 wl, wh, xl, xh;\n .reg .f32 t;\n mov.b32 {wl, wh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+            " fma.rn.f32.f16 t, wl, xl, %3;\n fma.rn.f32.f16 %0, wh, xh, t;\n}\n"
+            : "=f"(r)
+            : "r"(w), "r"(x), "f"(acc));
+    return r;
+}
+
+// Converts the C chunks of x into shared memory (one warp per chunk, 8
+// values per lane): f16 under the chunk's exact prescale, or raw bf16 when
+// its smallest nonzero value would fall below f16's last bit (a sufficient
+// test of exactness: scaled exponent >= -17 keeps all 8 significant bits at
+// or above 2^-24). Within a chunk, 16-byte piece p of k segment s (NSEG
+// segments of KS values) sits at p * NSEG * 16 + s * 16, so the segments'
+// i-th pieces are contiguous and one load instruction of 8 threads with 8
+// segments touches 8 different bank groups. A chunk kept raw sets *any_bf.
+// Each warp issues the loads of up to kBatch chunks before converting, so K
+// up to 80 chunks costs one round trip to memory. CG: load through L2 only
+// (x may have been written earlier in the same kernel by other CTAs).
+template <int NSEG, bool CG = false>
+__device__ void cc_convert(const CcArgs& a, uint8_t* smem, int warp, int lane, volatile int* any_bf)
+{
+    constexpr int PPS = kChunkK / NSEG / 8;  // 16-byte pieces per segment
+    constexpr int kBatch = 5;
+    uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
+    float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
+    uint8_t* fl = smem + a.smem_fl;
+    for (int base = warp; base < a.C; base += kCcWarps * kBatch) {
+        uint4 raw[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int kc = base + u * kCcWarps;
+            raw[u] = kc < a.C ? ldg_128<CG>(a.x + static_cast<size_t>(kc) * kChunkK + lane * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int kc = base + u * kCcWarps;
+            if (kc >= a.C) break;
+            const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+            uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) bf16_range_acc(wv[i], mx2, mn2);
+            uint32_t emax, emin, magmax;
+            bf16_range_fin(mx2, mn2, emax, emin, magmax);
+            emax = __reduce_max_sync(0xffffffffu, emax);
+            emin = __reduce_min_sync(0xffffffffu, emin);
+            if (emax == 0u) magmax = __reduce_max_sync(0xffffffffu, magmax);
+            const int e = min(emax != 0u ? 141 - static_cast<int>(emax) : prescale_exponent(magmax), 126);
+            const bool inexact = emin != 255u && static_cast<int>(emin) - 127 + e < -17;
+            uint32_t o[4];
+            if (inexact) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[i] = wv[i];
+            } else {
+                const float sc = __int_as_float((127 + e) << 23);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = pack_f16x2(__uint_as_float(wv[i] << 16) * sc, __uint_as_float(wv[i] & 0xFFFF0000u) * sc);
+            }
+            const int off = (lane % PPS) * NSEG * 4 + (lane / PPS) * 4;  // in 4-byte words
+            *reinterpret_cast<uint4*>(xs + kc * (kChunkK / 2) + off) = make_uint4(o[0], o[1], o[2], o[3]);
+            if (lane == 0) {
+                pe[kc] = inexact ? 1.0f : __int_as_float((127 - e) << 23);
+                fl[kc] = inexact ? 1 : 0;
+                if (inexact) *any_bf = 1;
+            }
+        }
+    }
+}
+
+// Zeroes the padding rows R .. R8 - 1 of every box region in every ring
+// slot (a TMA box holds R rows and never writes them), so that they read as
+// zero codes and scales; run by the compute threads, concurrently with the
+// first copies (which touch other bytes), before their first barrier.
+// Regions: (offset of box 0, bytes per row).
+__device__ void cc_zero_padding(const CcArgs& a, uint8_t* smem, int nbox, const uint32_t (&roff)[4],
+                                const uint32_t (&rbytes)[4], int nreg)
+{
+    const int pad = a.R8 - a.R;
+    if (pad == 0) return;
+    for (int reg = 0; reg < nreg; ++reg) {
+        const int pieces = static_cast<int>(rbytes[reg] / 16u);  // 16-byte pieces per row
+        const int per_slot = nbox * pad * pieces;
+        for (int t = threadIdx.x; t < a.n_stages * per_slot; t += kCcThreads) {
+            const int slot = t / per_slot;
+            const int rem = t % per_slot;
+            const int b = rem / (pad * pieces);
+            const int rr = a.R + (rem / pieces) % pad;
+            const int pc = rem % pieces;
+            uint8_t* dst = smem + a.smem_ring + slot * a.stage_bytes + roff[reg] +
+                           (static_cast<uint32_t>(b * a.R8 + rr) * rbytes[reg]) + pc * 16;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+// One thread's share of a stage: rows row0 .. row0 + 3 of box b2 (padding
+// rows at or past R hold zero codes and scales), k segment `seg` (KS = 256 /
+// NSEG values) of chunk kc. The four rows' blocks are interleaved, one chain
+// of pair products per (row, block), so eight independent multiply-add chains
+// are in flight.
+template <int NSEG, bool BF>
+__device__ __forceinline__ void cc_stage(const CcArgs& a, uint32_t stage, int b2, int row0, int seg,
+                                         const uint32_t* xw, float pe, float (&acc)[kCcRows])
+{
+    constexpr int KS = kChunkK / NSEG;  // 32 or 16 k
+    constexpr int NW = KS / 8;          // code words per row
+    constexpr int NB = NW / 2;          // 16-k blocks per row
+    uint32_t cw[kCcRows][NW];
+    float sc[kCcRows][NB];
+#pragma unroll
+    for (int i = 0; i < kCcRows; ++i) {
+        const int r = row0 + i;
+        const uint32_t rowb = stage + static_cast<uint32_t>(b2 * a.R8 + r) * 128u;
+        const uint32_t chunk = static_cast<uint32_t>((NW == 4 ? seg : seg >> 1) ^ (r & 7));
+        if constexpr (NW == 4) {
+            const uint4 v = lds128(rowb + (chunk << 4));
+            cw[i][0] = v.x; cw[i][1] = v.y; cw[i][2] = v.z; cw[i][3] = v.w;
+        } else {
+            const uint2 v = lds64(rowb + (chunk << 4) + static_cast<uint32_t>(seg & 1) * 8u);
+            cw[i][0] = v.x; cw[i][1] = v.y;
+        }
+        // the NB scale bytes of this segment
+        const uint32_t sb = stage + a.scales_off + static_cast<uint32_t>((b2 * a.R8 + r) * 16 + seg * NB);
+        const uint32_t two = NB == 2 ? lds16(sb) : lds8(sb);
+        const uint32_t h2 = e4m3x2_to_f16x2(two);
+        sc[i][0] = half_bits_to_f32(h2 & 0xFFFFu);
+        if constexpr (NB == 2) sc[i][1] = half_bits_to_f32(h2 >> 16);
+    }
+    float u[kCcRows];
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk) {
+        float s[kCcRows];
+#pragma unroll
+        for (int i = 0; i < kCcRows; ++i) s[i] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int wd = 2 * blk + h;
+            uint32_t w[kCcRows][4];
+#pragma unroll
+            for (int i = 0; i < kCcRows; ++i) {
+                e2m1x8_to_f16x2x4(cw[i][wd], w[i]);
+                if (BF) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) w[i][j] = f16x2_to_bf16x2(w[i][j]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t xv = xw[wd * 4 + j];
+#pragma unroll
+                for (int i = 0; i < kCcRows; ++i) s[i] = fma2_mixed<BF>(w[i][j], xv, s[i]);
+            }
+        }
+        // scale the block sums exactly by the E4M3 scale, then by 2^-prescale
+#pragma unroll
+        for (int i = 0; i < kCcRows; ++i) u[i] = blk == 0 ? s[i] * sc[i][0] : fmaf(s[i], sc[i][blk], u[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < kCcRows; ++i) acc[i] = fmaf(u[i], pe, acc[i]);
+}
+
+// ---------------------------------------------------------------- groupwise int (Q4 / Q5)
+// Same plan for w = scale * q + min per group of 32 (NInfer article, section
+// 2: the groupwise-int recipe): per row and group, y += scale * sum(q x) +
+// min * sum(x). The codes enter the multiply-add as f16 subnormals: the f16
+// with bit pattern q is exactly q * 2^-24 (q < 32), so a masked nibble pair
+// is an f16 pair with no conversion at all, and the 2^24 moves into the
+// scale. Nibble k and nibble k + 4 of a 32-bit code word form one pair, so
+// the activations are stored paired the same way, (x_k, x_{k+4}). The sums
+// of x per segment come from the original bf16 values, in a fixed order.
+
+// Converts x as cc_convert does, with the (k, k+4) pairing, and writes the
+// fp32 sum of each segment's original values.
+template <int NSEG, bool CG = false>
+__device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lane, volatile int* any_bf)
+{
+    constexpr int kBatch = 5;
+    constexpr int PPS = kChunkK / NSEG / 8;  // lanes (16-byte pieces) per segment
+    uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
+    float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
+    float* gx = reinterpret_cast<float*>(smem + a.smem_gx);
+    uint8_t* fl = smem + a.smem_fl;
+    for (int base = warp; base < a.C; base += kCcWarps * kBatch) {
+        uint4 raw[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int kc = base + u * kCcWarps;
+            raw[u] = kc < a.C ? ldg_128<CG>(a.x + static_cast<size_t>(kc) * kChunkK + lane * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int kc = base + u * kCcWarps;
+            if (kc >= a.C) break;
+            const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+            float sx = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sx += bf16_bits_to_f32((i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu));
+            uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) bf16_range_acc(wv[i], mx2, mn2);
+            uint32_t emax, emin, magmax;
+            bf16_range_fin(mx2, mn2, emax, emin, magmax);
+#pragma unroll
+            for (int sh = 1; sh < PPS; sh <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, sh);
+            emax = __reduce_max_sync(0xffffffffu, emax);
+            emin = __reduce_min_sync(0xffffffffu, emin);
+            if (emax == 0u) magmax = __reduce_max_sync(0xffffffffu, magmax);
+            const int e = min(emax != 0u ? 141 - static_cast<int>(emax) : prescale_exponent(magmax), 126);
+            const bool inexact = emin != 255u && static_cast<int>(emin) - 127 + e < -17;
+            uint32_t o[4];
+            if (inexact) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[i] = wv[i];
+            } else {
+                const float sc = __int_as_float((127 + e) << 23);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = pack_f16x2(__uint_as_float(wv[i] << 16) * sc, __uint_as_float(wv[i] & 0xFFFF0000u) * sc);
+            }
+            // natural pairs (x0,x1)(x2,x3)(x4,x5)(x6,x7) -> (x0,x4)(x1,x5)(x2,x6)(x3,x7)
+            const uint32_t p0 = __byte_perm(o[0], o[2], 0x5410), p1 = __byte_perm(o[0], o[2], 0x7632);
+            const uint32_t p2 = __byte_perm(o[1], o[3], 0x5410), p3 = __byte_perm(o[1], o[3], 0x7632);
+            const int off = (lane % PPS) * NSEG * 4 + (lane / PPS) * 4;
+            *reinterpret_cast<uint4*>(xs + kc * (kChunkK / 2) + off) = make_uint4(p0, p1, p2, p3);
+            if (lane % PPS == 0) gx[kc * NSEG + lane / PPS] = sx;
+            if (lane == 0) {
+                pe[kc] = inexact ? 1.0f : __int_as_float((127 - e) << 23);
+                fl[kc] = inexact ? 1 : 0;
+                if (inexact) *any_bf = 1;
+            }
+        }
+    }
+}
+
+// Code word w (8 unsigned 4-bit codes) -> four f16 pairs of subnormals
+// (q_j, q_{j+4}) * 2^-24; Q5 ORs in the fifth bit (bit 4 of each half) from
+// hsp, the word's high bits spread as k0..k3 -> bits 4..7 and k4..k7 -> bits
+// 20..23.
+template <int BITS>
+__device__ __forceinline__ void q45_pairs(uint32_t w, uint32_t hsp, uint32_t (&z)[4])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        z[j] = (w >> (4 * j)) & 0x000F000Fu;
+        if (BITS == 5) z[j] |= (hsp >> j) & 0x00100010u;
+    }
+}
+
+// One thread's share of a stage (see cc_stage); `seg` covers one group
+// (NSEG = 8) or half of one (NSEG = 16). The bf16 path (a chunk kept raw)
+// widens the codes and activations to fp32.
+template <int NSEG, int BITS, bool BF>
+__device__ __forceinline__ void cc_stage_q45(const CcArgs& a, uint32_t stage, int b2, int row0, int seg,
+                                             const uint32_t* xw, float pe, float gxs, float (&acc)[kCcRows])
+{
+    constexpr int KS = kChunkK / NSEG;
+    constexpr int NW = KS / 8;
+    const int grp = NSEG == 8 ? seg : seg >> 1;
+#pragma unroll
+    for (int i = 0; i < kCcRows; ++i) {
+        const int r = row0 + i;  // padding rows (r >= R) read as zeros
+        const uint32_t rowi = static_cast<uint32_t>(b2 * a.R8 + r);
+        const uint32_t chunk = static_cast<uint32_t>((NW == 4 ? seg : seg >> 1) ^ (r & 7));
+        uint32_t cw[NW];
+        if constexpr (NW == 4) {
+            const uint4 v = lds128(stage + rowi * 128u + (chunk << 4));
+            cw[0] = v.x; cw[1] = v.y; cw[2] = v.z; cw[3] = v.w;
+        } else {
+            const uint2 v = lds64(stage + rowi * 128u + (chunk << 4) + static_cast<uint32_t>(seg & 1) * 8u);
+            cw[0] = v.x; cw[1] = v.y;
+        }
+        uint32_t hb = 0;
+        if (BITS == 5) {
+            // 4 (NSEG = 8) or 2 bytes of high bits, one per 8 k
+            const uint32_t ha = stage + a.hi_off + rowi * 32u + static_cast<uint32_t>(seg * NW);
+            hb = NW == 4 ? lds32(ha) : lds16(ha);
+        }
+        const float sc = half_bits_to_f32(lds16(stage + a.scales_off + rowi * 16u + static_cast<uint32_t>(grp * 2)));
+        const float mn = half_bits_to_f32(lds16(stage + a.mins_off + rowi * 16u + static_cast<uint32_t>(grp * 2)));
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int wd = 0; wd < NW; ++wd) {
+            uint32_t hsp = 0;
+            if (BITS == 5) {
+                const uint32_t h8 = (hb >> (8 * wd)) & 0xFFu;
+                hsp = ((h8 & 0x0Fu) << 4) | ((h8 & 0xF0u) << 16);
+            }
+            uint32_t z[4];
+            q45_pairs<BITS>(cw[wd], hsp, z);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (BF) {
+                    // raw bf16 activations: widen both sides to fp32
+                    const uint32_t xv = xw[wd * 4 + j];
+                    s0 = fmaf(static_cast<float>(z[j] & 0xFFFFu), __uint_as_float(xv << 16), s0);
+                    s1 = fmaf(static_cast<float>(z[j] >> 16), __uint_as_float(xv & 0xFFFF0000u), s1);
+                } else if (j & 1) {
+                    s1 = fma2_mixed<false>(z[j], xw[wd * 4 + j], s1);
+                } else {
+                    s0 = fma2_mixed<false>(z[j], xw[wd * 4 + j], s0);
+                }
+            }
+        }
+        // subnormal codes carry 2^-24 (not on the bf16 path)
+        const float sq = (s0 + s1) * (BF ? 1.0f : 16777216.0f);
+        acc[i] = fmaf(sq * sc, pe, acc[i]);
+        acc[i] = fmaf(mn, gxs, acc[i]);
+    }
+}
+
+}  // namespace
+
+}  // namespace qg

@@ -282,6 +282,31 @@ __device__ __forceinline__ uint4 ldg_nc_128(const void* p)
     return v;
 }
 
+// 128-bit global load cached in L2 only: coherent with stores other CTAs of
+// the same kernel made before a grid-wide barrier.
+__device__ __forceinline__ uint4 ldg_cg_128(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+template <bool CG>
+__device__ __forceinline__ uint4 ldg_128(const void* p)
+{
+    return CG ? ldg_cg_128(p) : ldg_nc_128(p);
+}
+
+__device__ __forceinline__ uint32_t ldg_cg_u16(const uint16_t* p)
+{
+    uint16_t v;
+    asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // ----------------------------------------------------------------- activation prescale
 // Power-of-two prescale exponent p for a chunk whose largest finite |x| has
 // bf16 magnitude bits `mag` (0 if every value is zero): max * 2^p in [2^14, 2^15).

@@ -258,16 +258,18 @@ def test_q45_edge_scales_and_mins(M, bits, mode, record_property):
     prior = q_split_ratio(w, x, B, q_chain(K))
     d = q45_dev(w)
     xd = to_dev(x)
-    seen = []
+    observed = None
     for dt in (torch.float32, torch.bfloat16):
         y = torch.empty((M, N), dtype=dt, device="cuda")
         q.qgemv_q45(d["q_lo"], d["q_hi"], d["scale"], d["min"], bits, xd, y)
         torch.cuda.synchronize()
-        seen.append(check_out(y, yref, a, f"Q{bits} {mode} M={M} {dt}"))
+        r = check_out(y, yref, a, f"Q{bits} {mode} M={M} {dt}")   # raises outside the bound
+        if dt == torch.float32:
+            observed = r              # |y - y_ref| / B of the unrounded output
     record_property("q_split_prior_ratio", prior)
-    record_property("observed_ratio", max(seen))
-    print(f"Q{bits} {mode} M={M}: a-priori split bound / B = {prior:.3g}, observed error / B = {max(seen):.3g}")
-    assert max(seen) <= 1.0
+    record_property("observed_ratio", observed)
+    print(f"Q{bits} {mode} M={M}: a-priori split bound / B = {prior:.3g}, observed fp32 error / B = {observed:.3g}")
+    assert observed <= 1.0 and prior <= 1.0
 
 
 @pytest.mark.parametrize("bits", [4, 5])
