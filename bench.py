@@ -67,6 +67,8 @@ def parse_args():
     ap.add_argument("--sweep", dest="sweep", action="store_true", default=True,
                     help="also measure every other configuration (default)")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--no-chain", dest="chain", action="store_false", default=True,
+                    help="one launch per projection instead of one qgemv_chain call per step")
     return ap.parse_args()
 
 
@@ -165,10 +167,11 @@ class ClockSampler:
 # more tokens: the mma.sync kernel); a committed traffic figure is used only
 # while these files are unchanged.
 KERNEL_SOURCES = {
-    "cc": ("qgemv_cc.cu", "common.cuh", "qgemv_internal.h"),
+    "cc": ("qgemv_cc.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
     "tc": ("qgemv_tc.cu", "tcgen05.cuh", "common.cuh", "qgemv_internal.h"),
     "mma": ("qgemv_dense.cu", "common.cuh", "qgemv_internal.h"),
     "moe": ("qgemv_tc.cu", "moe.cu", "tcgen05.cuh", "common.cuh", "qgemv_internal.h"),
+    "chain": ("qgemv_chain.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
 }
 
 
@@ -255,6 +258,7 @@ class Workload:
         l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 * 2 ** 20)
         self.l2_bytes = int(l2)
         self.copies = max(2, math.ceil(copies_min_bytes * self.l2_bytes / max(self.weight_bytes, 1)))
+        self.chains = []
         self.dev_w = [[self._upload(w) for *_, w in self.projs]]
         for _ in range(self.copies - 1):
             self.dev_w.append([{k: (v.clone() if hasattr(v, "clone") else v) for k, v in d.items()}
@@ -309,9 +313,31 @@ class Workload:
         else:
             q.qgemv_q45(w["q_lo"], w["q_hi"], w["scale"], w["min"], w["bits"], x, y, residual=r)
 
+    def build_chains(self):
+        """One prepared qgemv_chain call per weight copy: the layer's
+        projections as the library's single layer call."""
+        import bit_quantized_weight_gb300 as q
+        self.chains = []
+        for c in range(self.copies):
+            ops = []
+            for idx, (name, N, K, epi, _) in enumerate(self.projs):
+                w = self.dev_w[c][idx]
+                op = dict(w)
+                op.update({"x": self.view_in(f"x.{name}"), "y": self.view_out(name), "epilogue": epi})
+                if epi == "residual":
+                    op["residual"] = self.view_in(f"r.{name}")
+                if "codes" not in op and op.get("q_hi") is None:
+                    op.pop("q_hi", None)
+                ops.append(op)
+            self.chains.append(q.GemvChain(ops))
+
     def step(self, copy, events=None):
-        """Enqueue one step on the current stream; events[i] is recorded
-        before call i and events[-1] after the last call."""
+        """Enqueue one step on the current stream: one qgemv_chain call, or
+        (with events, or without chains) one call per projection with
+        events[i] recorded before call i and events[-1] after the last."""
+        if events is None and self.chains:
+            self.chains[copy % self.copies].run()
+            return
         for i in range(len(self.projs)):
             if events is not None:
                 events[i].record()
@@ -320,7 +346,7 @@ class Workload:
             events[-1].record()
 
     def launches_per_step(self):
-        return len(self.projs)
+        return 1 if (self.chains and self.M == 1) else len(self.projs)
 
     def alg_bytes(self, idx):
         """Algorithmic bytes of call idx: weights + activations in + outputs."""
@@ -634,6 +660,9 @@ def measure(args, kind, M, world, rank, stream, cpu=True, e2e=True):
         wl = MoeWorkload(M, copies_min_bytes=4)
     else:
         wl = Workload(kind, M, copies_min_bytes=4)
+        if args.chain and kind != "tiny":
+            wl.build_chains()
+    chained = bool(getattr(wl, "chains", None))
     n_calls = len(wl.kernel_names())
 
     with torch.cuda.stream(stream):
@@ -711,31 +740,56 @@ def measure(args, kind, M, world, rank, stream, cpu=True, e2e=True):
     # it alone (weights rotating over the same copies) in one graph, CUDA
     # events around the replay on the launching stream. Back to back, each
     # launch overlaps the previous one's tail exactly as inside the step.
-    g_dom = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_dom, stream=stream):
-        for i in range(args.steps):
-            # copies the timed step did not just touch (small weights would
-            # otherwise still sit in L2)
-            wl.call(dom, i + args.steps)
-    with torch.cuda.stream(stream):
-        g_dom.replay()
-    stream.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        g_dom.replay()
-        e1.record(stream)
-    stream.synchronize()
-    dom_us = e0.elapsed_time(e1) / args.steps * 1e3
+    def alone_us(idx):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(args.steps):
+                # copies the timed step did not just touch (small weights
+                # would otherwise still sit in L2)
+                wl.call(idx, i + args.steps)
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) / args.steps * 1e3
+
+    dom_us = alone_us(dom)
+    g_dom = None
+    sum_alone = None
+    if chained:
+        sum_alone = sum(dom_us if i == dom else alone_us(i) for i in range(n_calls))
     peak, peak_kind = measured_peaks()
     dom_name = wl.kernel_names()[dom]
     achieved = wl.alg_bytes(dom) / (dom_us * 1e-6) / 1e9
     traffic = profiled_traffic(f"{kind}.{dom_name}.M{M}", kernel_family(kind, M))
-    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6.8 TB/s", "traffic": traffic,
-                "alg_bytes_per_launch": wl.alg_bytes(dom), "us_per_launch": dom_us,
-                "timing": "the kernel alone, K launches in one CUDA graph, events on its stream"}
+    peak_src = (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s")
+    alone = {"kernel": dom_name, "achieved": achieved, "frac": achieved / peak, "alg_bytes_per_launch": wl.alg_bytes(dom),
+             "us_per_launch": dom_us, "traffic": traffic,
+             "timing": "the projection alone, K launches in one CUDA graph, events on its stream"}
+    if chained and M == 1:
+        # the step is one launch of the chained-layer kernel: it is the
+        # dominant (only) kernel, timed by the headline graph itself
+        step_bytes = sum(wl.alg_bytes(i) for i in range(n_calls))
+        ach = step_bytes / (ms_per_step * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "chain_kernel (whole layer, one launch)", "achieved": ach,
+                    "peak": peak, "unit": "GB/s", "frac": ach / peak, "peak_source": peak_src,
+                    "traffic": profiled_traffic(f"{kind}.chain.M{M}", "chain"),
+                    "alg_bytes_per_launch": step_bytes, "us_per_launch": ms_per_step * 1e3,
+                    "timing": "K launches in one CUDA graph (the headline region), events on its stream",
+                    "largest_projection_alone": alone}
+    else:
+        roofline = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "peak_source": peak_src, "traffic": traffic,
+                    "alg_bytes_per_launch": wl.alg_bytes(dom), "us_per_launch": dom_us,
+                    "timing": "the kernel alone, K launches in one CUDA graph, events on its stream"}
+    if chained:
+        roofline["projections_sum_alone_us"] = sum_alone
+        roofline["step_vs_sum_alone"] = ms_per_step * 1e3 / sum_alone
 
     # ---- end to end through the public API with pinned host buffers
     e2e_line = None
@@ -766,7 +820,7 @@ def measure(args, kind, M, world, rank, stream, cpu=True, e2e=True):
                                         {"budget_s": args.sweep_entry_budget,
                                          "single_thread_budget_s": args.sweep_entry_budget / 2})) \
         if (cpu and rank == 0 and world == 1) else None
-    out = {"workload": wl.describe(), "kind": kind, "M": M, "value": value, "unit": "GB/s",
+    out = {"workload": wl.describe(), "kind": kind, "M": M, "chained": chained, "value": value, "unit": "GB/s",
            "ms_per_step": ms_per_step, "weight_bytes_per_step": wl.weight_bytes,
            "frac_of_measured_hbm": value / world / peak, "frac_of_8tbs": value / world / NOMINAL_HBM_GBS,
            "us_per_call": us_per_call, "roofline": roofline, "e2e": e2e_line, "cpu_baseline": cpu_line,
@@ -827,6 +881,8 @@ def main():
             "config": {"workload": head["workload"], "M": args.M,
                        "weight_bytes_per_step": head["weight_bytes_per_step"], "l2": head["l2"],
                        "parallelism": "one independent replica per GPU" if world > 1 else "single GPU",
+                       "step": "one qgemv_chain call (the layer's projections; one persistent launch at M = 1)"
+                               if head["chained"] else "one library call per projection",
                        "graph": "K steps captured in one CUDA graph (kernels only); us_per_call from a "
                                 "second graph with events between the calls (which serialise them)"},
             "frac_of_8tbs": head["frac_of_8tbs"],

@@ -208,6 +208,51 @@ qg_status moe_qgemv_nvfp4(const uint8_t* gu_codes, const uint8_t* gu_scales, con
                       workspace, workspace_bytes, M, H, I, E, topk, stream);
 }
 
+qg_status qgemv_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, cudaStream_t stream)
+{
+    if (!ops || n_ops < 1 || n_ops > 8 || M < 1 || M > kMaxTokens) return QG_ERR_INVALID_ARG;
+    bool any_dep = false;
+    for (int o = 0; o < n_ops; ++o) {
+        const qg_gemv_op& g = ops[o];
+        if (g.format != QG_FMT_NVFP4 && g.format != QG_FMT_Q4 && g.format != QG_FMT_Q5) return QG_ERR_INVALID_ARG;
+        if (g.epilogue != QG_EPI_NONE && g.epilogue != QG_EPI_RESIDUAL && g.epilogue != QG_EPI_SWIGLU)
+            return QG_ERR_INVALID_ARG;
+        if (g.y_dtype != QG_OUT_BF16 && g.y_dtype != QG_OUT_F32) return QG_ERR_INVALID_ARG;
+        if ((g.epilogue == QG_EPI_RESIDUAL) != (g.residual != nullptr)) return QG_ERR_INVALID_ARG;
+        if (g.epilogue == QG_EPI_SWIGLU && (g.format != QG_FMT_NVFP4 || g.y_dtype != QG_OUT_BF16 || g.N % 2))
+            return QG_ERR_INVALID_ARG;
+        qg_status s = check_dense(g.codes, g.scales, g.x, g.y, g.residual, M, g.N, g.K);
+        if (s != QG_OK) return s;
+        if (g.format == QG_FMT_NVFP4) {
+            if (g.q_hi || g.mins) return QG_ERR_INVALID_ARG;
+        } else {
+            if (!g.mins || ((g.format == QG_FMT_Q5) != (g.q_hi != nullptr))) return QG_ERR_INVALID_ARG;
+            if (!aligned16(g.mins) || (g.q_hi && !aligned16(g.q_hi))) return QG_ERR_MISALIGNED;
+        }
+        any_dep = any_dep || (o > 0 && g.after_previous);
+    }
+    if (sync && !aligned16(sync)) return QG_ERR_MISALIGNED;
+    if (any_dep && !sync) return QG_ERR_INVALID_ARG;
+    qg_status s = launch_chain(ops, n_ops, M, sync, stream);
+    if (s != QG_ERR_UNSUPPORTED) return s;
+    // One launch per op, in stream order (which also orders dependent ops).
+    for (int o = 0; o < n_ops; ++o) {
+        const qg_gemv_op& g = ops[o];
+        const qg_out out = g.y_dtype == QG_OUT_F32 ? QG_OUT_F32 : QG_OUT_BF16;
+        if (g.format == QG_FMT_NVFP4 && g.epilogue == QG_EPI_SWIGLU)
+            s = qgemv_swiglu_nvfp4(g.codes, static_cast<const uint8_t*>(g.scales), g.global_scale, g.x, g.y, M,
+                                   g.N, g.K, stream);
+        else if (g.format == QG_FMT_NVFP4)
+            s = qgemv_nvfp4(g.codes, static_cast<const uint8_t*>(g.scales), g.global_scale, g.x, g.y, out,
+                            g.residual, M, g.N, g.K, stream);
+        else
+            s = qgemv_q45(g.codes, g.q_hi, g.scales, g.mins, g.format == QG_FMT_Q5 ? 5 : 4, g.x, g.y, out,
+                          g.residual, M, g.N, g.K, stream);
+        if (s != QG_OK) return s;
+    }
+    return QG_OK;
+}
+
 qg_status qdequant_nvfp4(const uint8_t* codes, const uint8_t* scales, float global_scale, float* w, int N, int K,
                          cudaStream_t stream)
 {

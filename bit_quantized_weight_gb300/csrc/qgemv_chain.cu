@@ -1,0 +1,621 @@
+// qgemv_chain.cu -- the one-token projections of a decode layer in one
+// persistent launch.
+//
+// Decode engines replay one fixed sequence of projections per layer (NInfer
+// article, section 1: one CUDA graph per batch size; Decapybara README,
+// "Blackwell CUDA 内核套件": a persistent single-launch decode loop,
+// megakernel.cu). Launched one by one, every projection pays its own start
+// (launch, barrier set-up, the first weight stage's latency, the wait for the
+// previous kernel) and its own tail (the slowest CTA, the epilogue), and on
+// one GB300 those fixed costs were about a fifth of a 27B-class layer.
+//
+// Here one CTA per SM walks the whole list. Its TMA warp streams the weights
+// of op after op into one shared-memory ring without stopping at an op
+// boundary (weights never depend on earlier outputs), so the next op's first
+// stages are already in flight while the compute warps finish the current op.
+// The compute warps run each op exactly as the one-token kernels of
+// qgemv_cc.cu do (same units, phases, exact activation conversion and
+// fixed-order reductions, so results are identical to separate calls): they
+// convert the op's activations into shared memory, stream its units and
+// write its outputs. An op that reads an earlier op's output first waits at a
+// grid-wide barrier (bounded, sense-reversing, on two caller-owned words),
+// and then reads activations and residuals through L2 only.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "cc_core.cuh"
+
+namespace qg {
+
+namespace {
+
+constexpr int kChainMaxOps = 8;
+constexpr int kChainNseg = 8;   // 32-k segments (always valid: at most 256 rows per stage)
+
+struct ChainOp {
+    CcArgs a;   // the op's plan, as the standalone one-token kernel would use it
+    int fmt;    // FMT_NVFP4, FMT_Q4, FMT_Q5
+    int epi;    // EPI_NONE, EPI_RESID, EPI_SWIGLU
+    int dep;    // grid-wide barrier before the op reads its inputs
+};
+
+struct ChainParams {
+    CUtensorMap map[kChainMaxOps][4];  // codes, scales, mins, Q5 high plane
+    ChainOp op[kChainMaxOps];
+    int n_ops;
+    int n_stages;
+    uint32_t slot_bytes;               // ring slot stride (the largest op's stage)
+    uint32_t smem_bar;
+    uint32_t* sync;                    // [0] arrivals, [1] generation; nullptr without barriers
+    uint64_t wait_ns;
+    int starve;
+    int* status;
+};
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid-wide barrier among the compute warps of all CTAs. Thread 0 of each CTA
+// arrives once all of its CTA's compute threads are here (their earlier
+// global writes ordered before the arrival); the last arrival resets the
+// count and advances the generation the others wait on. Bounded: on expiry
+// it records QG_ERR_DEVICE_TIMEOUT and sets the CTA's abort flag.
+__device__ void chain_grid_barrier(const ChainParams& p, volatile int* abort_flag)
+{
+    named_barrier_sync(1, kCcThreads);
+    if (threadIdx.x == 0 && !*abort_flag) {
+        uint32_t* count = p.sync;
+        uint32_t* gen = p.sync + 1;
+        __threadfence();
+        const uint32_t g0 = ld_acquire_u32(gen);
+        if (atomicAdd(count, 1u) == gridDim.x - 1) {
+            atomicExch(count, 0u);
+            __threadfence();
+            atomicAdd(gen, 1u);
+        } else {
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_u32(gen) == g0) {
+                __nanosleep(64);
+                if (global_timer_ns() - t0 > p.wait_ns) {
+                    set_device_status(p.status, QG_ERR_DEVICE_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+    }
+    named_barrier_sync(1, kCcThreads);
+}
+
+__device__ __forceinline__ void chain_store(const CcArgs& a, int idx, float val)
+{
+    if (a.out_f32)
+        reinterpret_cast<float*>(a.y)[idx] = val;
+    else
+        reinterpret_cast<uint16_t*>(a.y)[idx] = f32_to_bf16_bits_rn(val);
+}
+
+// The compute warps' unit loop of one NVFP4 op (cc_units of qgemv_cc.cu with
+// the ring position carried across ops and coherent residual loads).
+template <int EPI, bool MIXED>
+__device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, uint8_t* smem, uint32_t ring,
+                                                  uint32_t slot_bytes, int n_stages, uint64_t* full,
+                                                  uint64_t* empty, volatile int* abort_flag, bool& aborted,
+                                                  int& slot, int& lap)
+{
+    constexpr int NSEG = kChainNseg;
+    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
+    constexpr int KS = kChunkK / NSEG;
+    const int rg_per_box = (a.R + kCcRows - 1) / kCcRows;
+    const int item = threadIdx.x;
+    const int seg = item % NSEG;
+    const int bg = item / NSEG;
+    const int b2 = bg / rg_per_box;
+    const int row0 = (bg % rg_per_box) * kCcRows;
+    const bool active = b2 < a.P * NGU;
+    const int p = active ? b2 / NGU : 0;
+    const uint32_t* xs = reinterpret_cast<const uint32_t*>(smem + a.smem_x);
+    const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
+    const uint8_t* fl = smem + a.smem_fl;
+    float* red = reinterpret_cast<float*>(smem + a.smem_red);
+    const int n_mine = active ? max(0, (a.C - p + a.P - 1) / a.P) : 0;
+    const uint32_t x0 = smem_u32(xs + p * (kChunkK / 2) + seg * 4);
+    const uint32_t x_step = static_cast<uint32_t>(a.P) * (kChunkK * 2u);
+
+    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+        float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
+        // the unit's residuals, read while its stages stream
+        float res = 0.f;
+        const int r0 = u * a.R;
+        if (EPI == EPI_RESID && threadIdx.x < a.R && r0 + static_cast<int>(threadIdx.x) < a.n_out)
+            res = bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + threadIdx.x));
+        for (int c = 0; c < a.Cp; ++c) {
+            if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
+            if (!aborted && c < n_mine) {
+                const uint32_t stage = ring + slot * slot_bytes;
+                uint32_t xw[KS / 2];
+                const uint32_t xc = x0 + static_cast<uint32_t>(c) * x_step;
+#pragma unroll
+                for (int i = 0; i < KS / 8; ++i) {
+                    const uint4 v = lds128(xc + i * NSEG * 16);
+                    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
+                }
+                const int kc = c * a.P + p;
+                if (!MIXED || fl[kc] == 0)
+                    cc_stage<NSEG, false>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
+                else
+                    cc_stage<NSEG, true>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
+            }
+            mbar_arrive(&empty[slot]);
+            if (++slot == n_stages) {
+                slot = 0;
+                ++lap;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kCcRows; ++i)
+#pragma unroll
+            for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+        if (active && seg == 0) {
+#pragma unroll
+            for (int i = 0; i < kCcRows; ++i) red[b2 * a.R8 + row0 + i] = acc[i];
+        }
+        named_barrier_sync(1, kCcThreads);
+        if (!aborted) {
+            for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
+                if (r0 + r >= a.n_out) break;
+                float v[NGU];
+#pragma unroll
+                for (int gg = 0; gg < NGU; ++gg) {
+                    float s = 0.f;
+                    for (int pp = 0; pp < a.P; ++pp) s += red[(pp * NGU + gg) * a.R8 + r];
+                    v[gg] = s * a.g;
+                }
+                float val = v[0];
+                if (EPI == EPI_SWIGLU) val = (val / (1.0f + expf(-val))) * v[NGU - 1];
+                if (EPI == EPI_RESID)
+                    val += r == static_cast<int>(threadIdx.x) ? res
+                                                              : bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + r));
+                chain_store(a, r0 + r, val);
+            }
+        }
+        named_barrier_sync(1, kCcThreads);
+    }
+}
+
+// The unit loop of one groupwise-int op (cc_q45_units of qgemv_cc.cu, as above).
+template <int BITS, int EPI, bool MIXED>
+__device__ __forceinline__ void chain_units_q45(const CcArgs& a, uint8_t* smem, uint32_t ring, uint32_t slot_bytes,
+                                                int n_stages, uint64_t* full, uint64_t* empty,
+                                                volatile int* abort_flag, bool& aborted, int& slot, int& lap)
+{
+    constexpr int NSEG = kChainNseg;
+    constexpr int KS = kChunkK / NSEG;
+    const int rg_per_box = (a.R + kCcRows - 1) / kCcRows;
+    const int item = threadIdx.x;
+    const int seg = item % NSEG;
+    const int bg = item / NSEG;
+    const int b2 = bg / rg_per_box;
+    const int row0 = (bg % rg_per_box) * kCcRows;
+    const bool active = b2 < a.P;
+    const int p = active ? b2 : 0;
+    const uint32_t* xs = reinterpret_cast<const uint32_t*>(smem + a.smem_x);
+    const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
+    const float* gx = reinterpret_cast<const float*>(smem + a.smem_gx);
+    const uint8_t* fl = smem + a.smem_fl;
+    float* red = reinterpret_cast<float*>(smem + a.smem_red);
+    const int n_mine = active ? max(0, (a.C - p + a.P - 1) / a.P) : 0;
+    const uint32_t x0 = smem_u32(xs + p * (kChunkK / 2) + seg * 4);
+    const uint32_t x_step = static_cast<uint32_t>(a.P) * (kChunkK * 2u);
+
+    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+        float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
+        float res = 0.f;
+        const int r0 = u * a.R;
+        if (EPI == EPI_RESID && threadIdx.x < a.R && r0 + static_cast<int>(threadIdx.x) < a.n_out)
+            res = bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + threadIdx.x));
+        for (int c = 0; c < a.Cp; ++c) {
+            if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
+            if (!aborted && c < n_mine) {
+                const int kc = c * a.P + p;
+                const uint32_t stage = ring + slot * slot_bytes;
+                uint32_t xw[KS / 2];
+                const uint32_t xc = x0 + static_cast<uint32_t>(c) * x_step;
+#pragma unroll
+                for (int i = 0; i < KS / 8; ++i) {
+                    const uint4 v = lds128(xc + i * NSEG * 16);
+                    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
+                }
+                const float gxs = gx[kc * NSEG + seg];
+                if (!MIXED || fl[kc] == 0)
+                    cc_stage_q45<NSEG, BITS, false>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                else
+                    cc_stage_q45<NSEG, BITS, true>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+            }
+            mbar_arrive(&empty[slot]);
+            if (++slot == n_stages) {
+                slot = 0;
+                ++lap;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kCcRows; ++i)
+#pragma unroll
+            for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+        if (active && seg == 0) {
+#pragma unroll
+            for (int i = 0; i < kCcRows; ++i) red[b2 * a.R8 + row0 + i] = acc[i];
+        }
+        named_barrier_sync(1, kCcThreads);
+        if (!aborted) {
+            for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
+                if (r0 + r >= a.n_out) break;
+                float val = 0.f;
+                for (int pp = 0; pp < a.P; ++pp) val += red[pp * a.R8 + r];
+                if (EPI == EPI_RESID)
+                    val += r == static_cast<int>(threadIdx.x) ? res
+                                                              : bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + r));
+                chain_store(a, r0 + r, val);
+            }
+        }
+        named_barrier_sync(1, kCcThreads);
+    }
+}
+
+template <int EPI>
+__device__ __forceinline__ void chain_nvfp4(const CcArgs& a, bool mixed, uint8_t* smem, uint32_t ring,
+                                            uint32_t slot_bytes, int n_stages, uint64_t* full, uint64_t* empty,
+                                            volatile int* abort_flag, bool& aborted, int& slot, int& lap)
+{
+    if (mixed)
+        chain_units_nvfp4<EPI, true>(a, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted, slot,
+                                     lap);
+    else
+        chain_units_nvfp4<EPI, false>(a, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted, slot,
+                                      lap);
+}
+
+template <int BITS, int EPI>
+__device__ __forceinline__ void chain_q45(const CcArgs& a, bool mixed, uint8_t* smem, uint32_t ring,
+                                          uint32_t slot_bytes, int n_stages, uint64_t* full, uint64_t* empty,
+                                          volatile int* abort_flag, bool& aborted, int& slot, int& lap)
+{
+    if (mixed)
+        chain_units_q45<BITS, EPI, true>(a, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted,
+                                         slot, lap);
+    else
+        chain_units_q45<BITS, EPI, false>(a, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted,
+                                          slot, lap);
+}
+
+__global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_constant__ ChainParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = warp_index_uniform();
+    const int lane = threadIdx.x & 31;
+
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.smem_bar);
+    uint64_t* empty = full + kCcMaxStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCcMaxStages);
+    volatile int* any_bf = abort_flag + 1;
+
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.n_stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCcThreads);
+        }
+        *abort_flag = 0;
+        *any_bf = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const uint32_t ring = smem_u32(smem + p.op[0].a.smem_ring);
+
+    if (warp == kCcTmaWarp) {
+        // ------------------------------------------------------------ producer
+        if (elect_one()) {
+            for (int o = 0; o < p.n_ops; ++o) {
+                prefetch_tensormap(&p.map[o][0]);
+                prefetch_tensormap(&p.map[o][1]);
+                if (p.op[o].fmt != FMT_NVFP4) prefetch_tensormap(&p.map[o][2]);
+                if (p.op[o].fmt == FMT_Q5) prefetch_tensormap(&p.map[o][3]);
+            }
+        }
+        __syncwarp();
+        int slot = 0, lap = 0, issued = 0;
+        bool stop = false;
+        for (int o = 0; o < p.n_ops && !stop; ++o) {
+            const CcArgs& a = p.op[o].a;
+            const int fmt = p.op[o].fmt;
+            const int ngu = p.op[o].epi == EPI_SWIGLU ? 2 : 1;
+            for (int u = blockIdx.x; u < a.n_units && !stop; u += gridDim.x) {
+                const int row0 = u * a.R;
+                for (int c = 0; c < a.Cp; ++c) {
+                    if (lap > 0 && !cc_wait_warp(&empty[slot], (lap - 1) & 1, a, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    if (*abort_flag || p.starve) {
+                        stop = true;
+                        break;
+                    }
+                    int live = 0;
+                    for (int pp = 0; pp < a.P; ++pp) live += (c * a.P + pp < a.C) ? 1 : 0;
+                    uint8_t* sb = smem + a.smem_ring + slot * p.slot_bytes;
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live * ngu) * a.box_tx);
+                        for (int pp = 0; pp < a.P; ++pp) {
+                            const int kc = c * a.P + pp;
+                            if (kc >= a.C) continue;
+                            if (fmt == FMT_NVFP4) {
+                                for (int gg = 0; gg < ngu; ++gg) {
+                                    const int b2 = pp * ngu + gg;
+                                    const int row = row0 + gg * a.up_row_offset;
+                                    tma_load_2d(sb + b2 * a.R8 * 128, &p.map[o][0], kc * (kChunkK / 2), row,
+                                                &full[slot]);
+                                    tma_load_2d(sb + a.scales_off + b2 * a.R8 * 16, &p.map[o][1],
+                                                kc * (kChunkK / 16), row, &full[slot]);
+                                }
+                            } else {
+                                tma_load_2d(sb + pp * a.R8 * 128, &p.map[o][0], kc * (kChunkK / 2), row0,
+                                            &full[slot]);
+                                tma_load_2d(sb + a.scales_off + pp * a.R8 * 16, &p.map[o][1], kc * (kChunkK / 32),
+                                            row0, &full[slot]);
+                                tma_load_2d(sb + a.mins_off + pp * a.R8 * 16, &p.map[o][2], kc * (kChunkK / 32),
+                                            row0, &full[slot]);
+                                if (fmt == FMT_Q5)
+                                    tma_load_2d(sb + a.hi_off + pp * a.R8 * 32, &p.map[o][3], kc * (kChunkK / 8),
+                                                row0, &full[slot]);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    ++issued;
+                    if (++slot == p.n_stages) {
+                        slot = 0;
+                        ++lap;
+                    }
+                }
+            }
+        }
+        // No copy may still be landing in shared memory when the CTA exits.
+        if (lane == 0)
+            for (int g = max(0, issued - p.n_stages); g < issued; ++g)
+                mbar_wait_bounded(&full[g % p.n_stages], (g / p.n_stages) & 1, p.wait_ns, p.status);
+        __syncwarp();
+        return;
+    }
+
+    // ---------------------------------------------------------------- compute warps
+    // The first op's inputs may come from the previous kernel on the stream.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    bool aborted = false;
+    int slot = 0, lap = 0;
+    for (int o = 0; o < p.n_ops; ++o) {
+        const ChainOp& op = p.op[o];
+        const CcArgs& a = op.a;
+        if (op.dep) chain_grid_barrier(p, abort_flag);
+        if (*abort_flag) aborted = true;
+        if (threadIdx.x == 0) *any_bf = 0;
+        named_barrier_sync(1, kCcThreads);
+        if (op.fmt == FMT_NVFP4)
+            cc_convert<kChainNseg, true>(a, smem, warp, lane, any_bf);
+        else
+            cc_convert_q45<kChainNseg, true>(a, smem, warp, lane, any_bf);
+        named_barrier_sync(1, kCcThreads);
+        const bool mixed = *any_bf != 0;
+        if (op.fmt == FMT_NVFP4) {
+            if (op.epi == EPI_SWIGLU)
+                chain_nvfp4<EPI_SWIGLU>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                        aborted, slot, lap);
+            else if (op.epi == EPI_RESID)
+                chain_nvfp4<EPI_RESID>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                       aborted, slot, lap);
+            else
+                chain_nvfp4<EPI_NONE>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                      aborted, slot, lap);
+        } else if (op.fmt == FMT_Q5) {
+            if (op.epi == EPI_RESID)
+                chain_q45<5, EPI_RESID>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                        aborted, slot, lap);
+            else
+                chain_q45<5, EPI_NONE>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                       aborted, slot, lap);
+        } else {
+            if (op.epi == EPI_RESID)
+                chain_q45<4, EPI_RESID>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                        aborted, slot, lap);
+            else
+                chain_q45<4, EPI_NONE>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                       aborted, slot, lap);
+        }
+    }
+}
+
+constexpr uint32_t align_up(uint32_t v, uint32_t al) { return (v + al - 1) / al * al; }
+
+// Units of R rows with the one-token kernels' rule: the smallest number of
+// units per CTA whose rows fit 256 per stage, R = ceil(rows / (SMs * units)).
+void cc_plan(CcArgs& a, int n_out, int ngu, int K, int sms)
+{
+    int R = 1;
+    for (int U = 1;; ++U) {
+        R = (n_out + sms * U - 1) / (sms * U);
+        if (ngu * ((R + 7) / 8 * 8) <= 256) break;
+    }
+    R = std::max(R, 1);
+    a.K = K;
+    a.C = K / kChunkK;
+    a.n_out = n_out;
+    a.R = R;
+    a.R8 = (R + 7) / 8 * 8;
+    a.P = std::max(1, std::min(256 / (ngu * a.R8), a.C));
+    a.Cp = (a.C + a.P - 1) / a.P;
+    a.n_units = (n_out + R - 1) / R;
+}
+
+}  // namespace
+
+// One persistent launch for a list of one-token projections;
+// QG_ERR_UNSUPPORTED when the list does not fit its plan (M != 1, K not a
+// multiple of 256, too many ops, or shared memory), so that the caller runs
+// the ops one by one instead.
+qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, cudaStream_t stream)
+{
+    if (M != 1 || n_ops < 1 || n_ops > kChainMaxOps) return QG_ERR_UNSUPPORTED;
+    const int sms = sm_count(-1);
+    if (sms <= 0) return QG_ERR_CUDA;
+    static ChainParams p;  // large: built here, copied into the launch's parameters
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    memset(&p, 0, sizeof(p));
+    p.n_ops = n_ops;
+    bool any_dep = false;
+    uint32_t slot_bytes = 0;
+    int c_max = 0, red_max = 0;
+    for (int o = 0; o < n_ops; ++o) {
+        const qg_gemv_op& g = ops[o];
+        if (g.K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
+        ChainOp& op = p.op[o];
+        op.fmt = g.format == QG_FMT_NVFP4 ? FMT_NVFP4 : g.format == QG_FMT_Q5 ? FMT_Q5 : FMT_Q4;
+        op.epi = g.epilogue == QG_EPI_SWIGLU ? EPI_SWIGLU : g.epilogue == QG_EPI_RESIDUAL ? EPI_RESID : EPI_NONE;
+        op.dep = o > 0 && g.after_previous ? 1 : 0;
+        any_dep = any_dep || op.dep;
+        const int ngu = op.epi == EPI_SWIGLU ? 2 : 1;
+        const int n_out = op.epi == EPI_SWIGLU ? g.N / 2 : g.N;
+        CcArgs& a = op.a;
+        cc_plan(a, n_out, ngu, g.K, sms);
+        a.x = static_cast<const uint16_t*>(g.x);
+        a.y = g.y;
+        a.residual = static_cast<const uint16_t*>(g.residual);
+        a.up_row_offset = op.epi == EPI_SWIGLU ? n_out : 0;
+        a.out_f32 = op.epi == EPI_SWIGLU ? 0 : (g.y_dtype == QG_OUT_F32 ? 1 : 0);
+        a.g = op.fmt == FMT_NVFP4 ? g.global_scale : 1.f;
+        const uint32_t nbox = static_cast<uint32_t>(a.P * ngu);
+        a.scales_off = nbox * a.R8 * 128u;
+        uint32_t st;
+        if (op.fmt == FMT_NVFP4) {
+            st = a.scales_off + nbox * a.R8 * 16u;
+            a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
+        } else {
+            a.mins_off = a.scales_off + nbox * a.R8 * 16u;
+            a.hi_off = a.mins_off + nbox * a.R8 * 16u;
+            st = a.hi_off + (op.fmt == FMT_Q5 ? nbox * a.R8 * 32u : 0u);
+            a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (op.fmt == FMT_Q5 ? 32u : 0u));
+        }
+        slot_bytes = std::max(slot_bytes, align_up(st, 1024));
+        c_max = std::max(c_max, a.C);
+        red_max = std::max(red_max, static_cast<int>(nbox) * a.R8);
+        // tensor maps: the standalone kernels' boxes
+        const int rows = g.N;
+        const int R = a.R;
+        if (!encode_tmap_2d(&p.map[o][0], g.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 2, rows, 128, R, true))
+            return QG_ERR_CUDA;
+        if (op.fmt == FMT_NVFP4) {
+            if (!encode_tmap_2d(&p.map[o][1], g.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 16, rows, 16, R,
+                                false))
+                return QG_ERR_CUDA;
+        } else {
+            if (!encode_tmap_2d(&p.map[o][1], g.scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8, R,
+                                false) ||
+                !encode_tmap_2d(&p.map[o][2], g.mins, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8, R,
+                                false))
+                return QG_ERR_CUDA;
+            if (op.fmt == FMT_Q5 &&
+                !encode_tmap_2d(&p.map[o][3], g.q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 8, rows, 32, R, false))
+                return QG_ERR_CUDA;
+        }
+    }
+    if (any_dep && !sync) return QG_ERR_INVALID_ARG;
+    // shared memory: ring | activations | 2^-prescale | flags | sums of x | partial sums | barriers
+    const uint32_t x_bytes = static_cast<uint32_t>(c_max) * kChunkK * 2u;
+    const uint32_t pe_bytes = align_up(static_cast<uint32_t>(c_max) * 4u, 16);
+    const uint32_t fl_bytes = align_up(static_cast<uint32_t>(c_max), 16);
+    const uint32_t gx_bytes = align_up(static_cast<uint32_t>(c_max * kChainNseg) * 4u, 16);
+    const uint32_t red_bytes = align_up(static_cast<uint32_t>(red_max) * 4u, 128);
+    const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
+    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + gx_bytes + red_bytes + bar_bytes;
+    if (fixed + 3 * slot_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
+    const int n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / slot_bytes));
+    uint32_t so = 0;
+    const uint32_t smem_ring = so;
+    so += n_stages * slot_bytes;
+    const uint32_t smem_x = so;
+    so += x_bytes;
+    const uint32_t smem_pe = so;
+    so += pe_bytes;
+    const uint32_t smem_fl = so;
+    so += fl_bytes;
+    const uint32_t smem_gx = so;
+    so += gx_bytes;
+    const uint32_t smem_red = so;
+    so += red_bytes;
+    const uint32_t smem_bar = so;
+    so += bar_bytes;
+    if (so > kCcSmemMax) return QG_ERR_UNSUPPORTED;
+
+    int* status = device_status_ptr();
+    if (!status) return QG_ERR_CUDA;
+    const DebugState dbg = debug_state();
+    p.n_stages = n_stages;
+    p.slot_bytes = slot_bytes;
+    p.smem_bar = smem_bar;
+    p.sync = sync;
+    p.wait_ns = dbg.wait_ns;
+    p.starve = dbg.starve;
+    p.status = status;
+    for (int o = 0; o < n_ops; ++o) {
+        CcArgs& a = p.op[o].a;
+        a.n_stages = n_stages;
+        a.stage_bytes = slot_bytes;
+        a.smem_ring = smem_ring;
+        a.smem_x = smem_x;
+        a.smem_pe = smem_pe;
+        a.smem_fl = smem_fl;
+        a.smem_gx = smem_gx;
+        a.smem_red = smem_red;
+        a.smem_bar = smem_bar;
+        a.wait_ns = dbg.wait_ns;
+        a.starve = dbg.starve;
+        a.status = status;
+    }
+
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCcSmemMax) !=
+            cudaSuccess)
+            return QG_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    // Every CTA must be resident for the grid-wide barrier: one CTA per SM
+    // (the shared memory allows no more), launched cooperatively when an op
+    // waits at the barrier; otherwise with programmatic dependent launch.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms);
+    cfg.blockDim = dim3(kCcAllThreads);
+    cfg.dynamicSmemBytes = so;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (any_dep) {
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+    } else {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, chain_kernel, p) != cudaSuccess) return QG_ERR_CUDA;
+    return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+}  // namespace qg

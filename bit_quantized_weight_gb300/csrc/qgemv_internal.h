@@ -135,5 +135,8 @@ qg_status launch_moe(const uint8_t* gu_codes, const uint8_t* gu_scales, const fl
                      const int32_t* ids, const float* tw, void* y, void* ws, size_t ws_bytes, int M,
                      int H, int I, int E, int topk, cudaStream_t stream);
 size_t moe_workspace_bytes(int M, int topk, int H, int I, int E);
+// One persistent launch for a list of one-token projections (qgemv_chain.cu);
+// QG_ERR_UNSUPPORTED when the list does not fit its plan.
+qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, cudaStream_t stream);
 
 }  // namespace qg

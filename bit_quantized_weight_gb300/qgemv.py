@@ -18,6 +18,12 @@ QG_ERR_CUDA = 5
 QG_ERR_DEVICE_TIMEOUT = 6
 QG_OUT_BF16 = 0
 QG_OUT_F32 = 1
+QG_FMT_NVFP4 = 0
+QG_FMT_Q4 = 1
+QG_FMT_Q5 = 2
+QG_EPI_NONE = 0
+QG_EPI_RESIDUAL = 1
+QG_EPI_SWIGLU = 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libqgemv.so")
@@ -26,6 +32,15 @@ _lib = None
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
+
+
+class QgGemvOp(ctypes.Structure):
+    """qg_gemv_op of include/qgemv.h."""
+    _fields_ = [("format", ctypes.c_int), ("epilogue", ctypes.c_int), ("y_dtype", ctypes.c_int),
+                ("after_previous", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int),
+                ("codes", ctypes.c_void_p), ("q_hi", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("mins", ctypes.c_void_p), ("global_scale", ctypes.c_float), ("x", ctypes.c_void_p),
+                ("residual", ctypes.c_void_p), ("y", ctypes.c_void_p)]
 
 
 class QGemvError(RuntimeError):
@@ -55,6 +70,7 @@ def lib():
         L.moe_qgemv_nvfp4.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                       _I, _I, _I, _I, _I, _P]
         L.moe_qgemv_nvfp4_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]
+        L.qgemv_chain.argtypes = [ctypes.POINTER(QgGemvOp), _I, _I, _P, _P]
         L.qdequant_nvfp4.argtypes = [_P, _P, _F, _P, _I, _I, _P]
         L.qdequant_q45.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _P]
         L.qg_last_device_status.argtypes = [_P]
@@ -64,7 +80,7 @@ def lib():
         L.qg_debug_set_wait.argtypes = [ctypes.c_uint64, _I]
         for name in ("qgemv_nvfp4", "qgemv_q45", "qgemv_swiglu_nvfp4", "moe_route_topk",
                      "moe_qgemv_nvfp4_workspace_size", "moe_qgemv_nvfp4", "moe_qgemv_nvfp4_noalloc",
-                     "qdequant_nvfp4",
+                     "qgemv_chain", "qdequant_nvfp4",
                      "qdequant_q45", "qg_last_device_status", "qg_debug_set_wait"):
             getattr(L, name).restype = _I
         _lib = L
@@ -180,6 +196,63 @@ def moe_qgemv_nvfp4_noalloc(gu_codes, gu_scales, gu_g, dn_codes, dn_scales, dn_g
         _ptr(gu_codes), _ptr(gu_scales), _ptr(gu_g), _ptr(dn_codes), _ptr(dn_scales), _ptr(dn_g), _ptr(x),
         _ptr(ids), _ptr(w), _ptr(y), M, H, two_i // 2, E, topk, _stream(stream, y)))
     return y
+
+
+_FORMATS = {"nvfp4": QG_FMT_NVFP4, "q4": QG_FMT_Q4, "q5": QG_FMT_Q5}
+_EPILOGUES = {"none": QG_EPI_NONE, "residual": QG_EPI_RESIDUAL, "swiglu": QG_EPI_SWIGLU}
+
+
+class GemvChain:
+    """A prepared qgemv_chain call: the op records are built once, so that
+    run() is one C call. Each op is a dict with the weight tensors of its
+    format (NVFP4: codes, scales, g; Q4/Q5: q_lo, q_hi (Q5), scale, min),
+    "x", "y", optionally "residual", "epilogue" ("none", "residual",
+    "swiglu") and "after_previous" (bool). The tensors must stay alive and
+    unchanged in place for as long as the chain is run."""
+
+    def __init__(self, ops, sync=None):
+        import torch
+        n = len(ops)
+        self.ops = (QgGemvOp * n)()
+        self.keep = []
+        M = None
+        for i, op in enumerate(ops):
+            x, y = op["x"], op["y"]
+            r = op.get("residual")
+            if "codes" in op:
+                fmt, codes, q_hi, scales, mins, g = QG_FMT_NVFP4, op["codes"], None, op["scales"], None, op["g"]
+            else:
+                fmt = QG_FMT_Q5 if op.get("q_hi") is not None else QG_FMT_Q4
+                codes, q_hi, scales, mins, g = op["q_lo"], op.get("q_hi"), op["scale"], op["min"], 1.0
+            _cuda(codes, q_hi, scales, mins, x, y, r)
+            epi = op.get("epilogue", "residual" if r is not None else "none")
+            rec = self.ops[i]
+            rec.format = fmt
+            rec.epilogue = _EPILOGUES[epi]
+            rec.y_dtype = QG_OUT_F32 if y.dtype == torch.float32 else QG_OUT_BF16
+            rec.after_previous = int(bool(op.get("after_previous", False)))
+            rec.N = codes.shape[0]
+            rec.K = x.shape[1]
+            rec.codes, rec.q_hi, rec.scales, rec.mins = _ptr(codes), _ptr(q_hi), _ptr(scales), _ptr(mins)
+            rec.global_scale = float(g)
+            rec.x, rec.residual, rec.y = _ptr(x), _ptr(r), _ptr(y)
+            self.keep.append(op)
+            if M is None:
+                M = x.shape[0]
+            elif x.shape[0] != M:
+                raise ValueError("every op of a chain takes the same number of tokens")
+        self.n, self.M = n, M
+        self.sync = sync
+        self.like = ops[0]["y"]
+
+    def run(self, stream=None):
+        _check("qgemv_chain", lib().qgemv_chain(self.ops, self.n, self.M, _ptr(self.sync),
+                                                _stream(stream, self.like)))
+
+
+def qgemv_chain(ops, sync=None, stream=None):
+    """Run a list of projections as one qgemv_chain call (see GemvChain)."""
+    GemvChain(ops, sync).run(stream)
 
 
 def qdequant_nvfp4(codes, scales, g, w, stream=None):

@@ -183,6 +183,70 @@ QG_API qg_status moe_qgemv_nvfp4_noalloc(const uint8_t* gu_codes, const uint8_t*
                                          const int32_t* topk_ids, const float* topk_w, void* y, int M, int H,
                                          int I, int E, int topk, cudaStream_t stream);
 
+/* Weight formats and epilogues of one projection in a chained call. */
+typedef enum { QG_FMT_NVFP4 = 0, QG_FMT_Q4 = 1, QG_FMT_Q5 = 2 } qg_format;
+typedef enum { QG_EPI_NONE = 0, QG_EPI_RESIDUAL = 1, QG_EPI_SWIGLU = 2 } qg_epilogue;
+
+/*
+ * One projection of qgemv_chain: the arguments of qgemv_nvfp4,
+ * qgemv_swiglu_nvfp4 or qgemv_q45 in one record (same layouts and rules).
+ *   format          qg_format
+ *   epilogue        QG_EPI_NONE, QG_EPI_RESIDUAL (residual != NULL) or
+ *                   QG_EPI_SWIGLU (NVFP4 only: N = 2I rows, gate then up,
+ *                   y bf16 [M][I])
+ *   y_dtype         qg_out; QG_OUT_BF16 for QG_EPI_SWIGLU
+ *   after_previous  nonzero if the op reads memory that an earlier op of the
+ *                   same call writes (its x or residual is an earlier y); the
+ *                   op then starts reading only once every earlier op of the
+ *                   call is complete. Without it the op may overlap earlier
+ *                   ops: it must then neither read nor write anything an
+ *                   earlier op of the call writes, nor write what one reads.
+ *   codes           NVFP4 codes or Q q_lo, u8[N][K/2]
+ *   q_hi            Q5 high-bit plane u8[N][K/8]; NULL for NVFP4 and Q4
+ *   scales          NVFP4 e4m3 u8[N][K/16], or Q fp16 [N][K/32]
+ *   mins            Q fp16 [N][K/32]; NULL for NVFP4
+ *   global_scale    NVFP4 tensor scale g (ignored for Q)
+ *   x, residual, y  as in the single-projection calls
+ */
+typedef struct {
+    int format;
+    int epilogue;
+    int y_dtype;
+    int after_previous;
+    int N;
+    int K;
+    const uint8_t* codes;
+    const uint8_t* q_hi;
+    const void* scales;
+    const void* mins;
+    float global_scale;
+    const void* x;
+    const void* residual;
+    void* y;
+} qg_gemv_op;
+
+/*
+ * The projections of a decode layer in order, as one call (NInfer article,
+ * section 1: a decode step is one fixed sequence replayed per batch size;
+ * Decapybara README, "Blackwell CUDA 内核套件": a persistent single-launch
+ * decode loop, megakernel.cu). Each op computes exactly what its
+ * single-projection call computes, with the same accuracy.
+ *   ops     host array of n_ops records, 1 <= n_ops <= 8 (read during the call)
+ *   M       tokens, 1..8, shared by every op
+ *   sync    two caller-owned device words (uint32_t[2], 16-byte aligned), zero
+ *           before their first use; the call leaves them zero again. Needed
+ *           (else QG_ERR_INVALID_ARG) when some op after the first has
+ *           after_previous set; may be NULL otherwise. Calls that overlap on
+ *           the GPU must use different words, and after a call that reported
+ *           QG_ERR_DEVICE_TIMEOUT the words must be zeroed again.
+ * With one token and K a multiple of 256 for every op, the list runs as one
+ * persistent kernel (one CTA per SM, launched cooperatively when an op waits
+ * for earlier ones): the weight stream runs on across op boundaries. Other
+ * lists run as one launch per op, in order, on `stream`.
+ * Every op is validated before anything is launched.
+ */
+QG_API qg_status qgemv_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, cudaStream_t stream);
+
 /*
  * Dequantise to fp32 w[N][K] with the same device decode the GEMV kernels
  * use (test hook for the bit-exact check). NVFP4: w = fp32(e2m1 * e4m3) * g,

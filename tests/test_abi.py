@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("qgemv_nvfp4", "qgemv_q45", "qgemv_swiglu_nvfp4", "moe_qgemv_nvfp4",
+    for n in ("qgemv_nvfp4", "qgemv_q45", "qgemv_swiglu_nvfp4", "moe_qgemv_nvfp4", "qgemv_chain",
               "moe_qgemv_nvfp4_workspace_size", "moe_route_topk", "qdequant_nvfp4", "qdequant_q45",
               "qg_last_device_status", "qg_status_string"):
         assert n in names
@@ -128,6 +128,71 @@ def test_noalloc_moe_validation(L):
     assert L.moe_qgemv_nvfp4_noalloc(A + 8, *args[1:], 8, 16384, 8192, 64, 8, None) == 3
     # H = 16384, I = 8192 at M = 8, top-8 needs far more than the 4 MiB scratch
     assert L.moe_qgemv_nvfp4_noalloc(*args, 8, 16384, 8192, 64, 8, None) == 4
+
+
+def _op(**kw):
+    import bit_quantized_weight_gb300 as q
+    rec = q.QgGemvOp()
+    base = dict(format=0, epilogue=0, y_dtype=0, after_previous=0, N=64, K=256, codes=A, q_hi=None, scales=A,
+                mins=None, global_scale=1.0, x=A, residual=None, y=A)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(rec, k, v)
+    return rec
+
+
+def _chain(L, recs, M=1, sync=None):
+    import bit_quantized_weight_gb300 as q
+    arr = (q.QgGemvOp * len(recs))(*recs)
+    return L.qgemv_chain(arr, len(recs), M, sync, None)
+
+
+@fake_ptr
+def test_chain_validation(L):
+    assert _chain(L, [_op(format=3)]) == 1
+    assert _chain(L, [_op(epilogue=5)]) == 1
+    assert _chain(L, [_op(y_dtype=2)]) == 1
+    assert _chain(L, [_op(epilogue=1)]) == 1                      # residual epilogue without residual
+    assert _chain(L, [_op(residual=A)]) == 1                      # residual without its epilogue
+    assert _chain(L, [_op(format=1, epilogue=2, mins=A)]) == 1   # SwiGLU is NVFP4 only
+    assert _chain(L, [_op(epilogue=2, N=63)]) == 1
+    assert _chain(L, [_op(epilogue=2, y_dtype=1)]) == 1
+    assert _chain(L, [_op(format=1)]) == 1                        # Q needs mins
+    assert _chain(L, [_op(format=2, mins=A)]) == 1                # Q5 needs q_hi
+    assert _chain(L, [_op(format=1, mins=A, q_hi=A)]) == 1        # Q4 takes none
+    assert _chain(L, [_op(mins=A)]) == 1                          # NVFP4 takes no mins
+    assert _chain(L, [_op(K=48)]) == 1
+    assert _chain(L, [_op(x=A + 8)]) == 3
+    assert _chain(L, [_op(format=1, mins=A + 4)]) == 3
+    assert _chain(L, [_op()], M=0) == 1
+    assert _chain(L, [_op()], M=9) == 1
+    assert L.qgemv_chain(None, 1, 1, None, None) == 1
+    assert _chain(L, [_op()] * 9) == 1
+    # a later op reading earlier outputs needs the sync words
+    assert _chain(L, [_op(), _op(after_previous=1)]) == 1
+    assert _chain(L, [_op(), _op(after_previous=1)], sync=A + 4) == 3
+
+
+def test_chain_record_layout_matches_the_header(tmp_path):
+    """The binding's qg_gemv_op has the C struct's size and field offsets."""
+    import shutil
+    import subprocess
+    import bit_quantized_weight_gb300 as q
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    fields = [f for f, _ in q.QgGemvOp._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "qgemv.h"\nint main(void){\n'
+                   '  printf("%zu", sizeof(qg_gemv_op));\n'
+                   + "".join(f'  printf(" %zu", offsetof(qg_gemv_op, {f}));\n' for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    cuda_inc = "/usr/local/cuda/include"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    want = [ctypes.sizeof(q.QgGemvOp)] + [getattr(q.QgGemvOp, f).offset for f in fields]
+    assert got == want
 
 
 @fake_ptr

@@ -1,0 +1,204 @@
+"""qgemv_chain: a decode layer's projections in one call (GPU).
+
+One token: the ops run in one persistent kernel; each op must give exactly
+what its single-projection call gives (same plan and arithmetic: bit for bit
+where the standalone kernel picks the same 32-k segments) and match the
+oracle within the stated bound. Ops flagged after_previous read earlier
+outputs of the same call through the grid-wide barrier; each such stage is
+checked against the oracle fed the GPU's own earlier output. More tokens run
+as one launch per op, identical to separate calls.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from checks import check_bf16, check_f32, gemv_bound, swiglu_bound
+from gpu_util import bits16, nvfp4_dev, q45_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+q = pytest.importorskip("bit_quantized_weight_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    q.qg_debug_set_wait(0, False)
+    yield
+    assert q.qg_last_device_status() == q.QG_OK
+
+
+def check_out(y, yref, a, what):
+    B = gemv_bound(a)
+    if y.dtype == torch.float32:
+        return check_f32(y.cpu().numpy(), yref, B, what)
+    return check_bf16(bits16(y), yref, B, what)
+
+
+def sync_words():
+    return torch.zeros(4, dtype=torch.int32, device="cuda")   # 16 bytes; the call uses two words
+
+
+def dense_layer_ops(M, seed=1):
+    """The 27B-class layer's four NVFP4 projections with independent inputs."""
+    ops, host = [], []
+    for name, N, K, epi in synth.dense_layer_shapes():
+        w = synth.nvfp4_weights(seed, f"dense.{name}", N, K)
+        x = synth.bf16_normal(seed, f"chain.{name}.x.M{M}", (M, K))
+        r = synth.bf16_normal(seed, f"chain.{name}.r.M{M}", (M, N)) if epi == "residual" else None
+        d = nvfp4_dev(w)
+        n_out = N // 2 if epi == "swiglu" else N
+        op = {"codes": d["codes"], "scales": d["scales"], "g": d["g"], "x": to_dev(x),
+              "y": torch.empty((M, n_out), dtype=torch.bfloat16, device="cuda"),
+              "epilogue": epi}
+        if r is not None:
+            op["residual"] = to_dev(r)
+        ops.append(op)
+        host.append((name, N, K, epi, w, x, r))
+    return ops, host
+
+
+def run_separately(ops):
+    outs = []
+    for op in ops:
+        y = torch.empty_like(op["y"])
+        if op.get("epilogue") == "swiglu":
+            q.qgemv_swiglu_nvfp4(op["codes"], op["scales"], op["g"], op["x"], y)
+        elif "codes" in op:
+            q.qgemv_nvfp4(op["codes"], op["scales"], op["g"], op["x"], y, residual=op.get("residual"))
+        else:
+            q.qgemv_q45(op["q_lo"], op.get("q_hi"), op["scale"], op["min"], 5 if op.get("q_hi") is not None else 4,
+                        op["x"], y, residual=op.get("residual"))
+        outs.append(y)
+    torch.cuda.synchronize()
+    return outs
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_chain_dense_layer_matches_separate_calls(M):
+    ops, host = dense_layer_ops(M)
+    q.qgemv_chain(ops)
+    torch.cuda.synchronize()
+    assert q.qg_last_device_status() == q.QG_OK
+    sep = run_separately(ops)
+    for op, ys, (name, N, K, epi, w, x, r) in zip(ops, sep, host):
+        assert torch.equal(op["y"].view(torch.int16), ys.view(torch.int16)), f"{name}: chain != separate call"
+        if M == 1:
+            if epi == "swiglu":
+                yref, a = O.gemv_nvfp4(w, x)
+                I = N // 2
+                B = swiglu_bound(yref[:, :I], yref[:, I:], gemv_bound(a[:, :I]), gemv_bound(a[:, I:]))
+                check_bf16(bits16(op["y"]), O.swiglu(yref[:, :I], yref[:, I:]), B, f"chain {name}")
+            else:
+                yref, a = O.gemv_nvfp4(w, x, residual=r)
+                check_out(op["y"], yref, a, f"chain {name}")
+
+
+def test_chain_dependent_ops_through_the_grid_barrier():
+    """o: y1 = W_o x (+ r); gate/up reads y1; down reads h with y1 as its
+    residual; a last projection reads the down output -- each op after the
+    first waits for the earlier ones inside the one launch."""
+    H, I = 1024, 2048
+    wo = synth.nvfp4_weights(70, "dep.o", H, 1536)
+    wgu = synth.nvfp4_weights(70, "dep.gu", 2 * I, H)
+    wdn = synth.nvfp4_weights(70, "dep.dn", H, I)
+    wl = synth.nvfp4_weights(70, "dep.last", 512, H)
+    x = synth.bf16_normal(71, "dep.x", (1, 1536))
+    r = synth.bf16_normal(71, "dep.r", (1, H))
+    D = {k: nvfp4_dev(w) for k, w in (("o", wo), ("gu", wgu), ("dn", wdn), ("last", wl))}
+    y1 = torch.empty((1, H), dtype=torch.bfloat16, device="cuda")
+    h = torch.empty((1, I), dtype=torch.bfloat16, device="cuda")
+    y2 = torch.empty((1, H), dtype=torch.bfloat16, device="cuda")
+    y3 = torch.empty((1, 512), dtype=torch.float32, device="cuda")
+    ops = [
+        {**D["o"], "x": to_dev(x), "y": y1, "residual": to_dev(r)},
+        {**D["gu"], "x": y1, "y": h, "epilogue": "swiglu", "after_previous": True},
+        {**D["dn"], "x": h, "y": y2, "residual": y1, "after_previous": True},
+        {**D["last"], "x": y2, "y": y3, "after_previous": True},
+    ]
+    sync = sync_words()
+    for rep in range(2):                    # the sync words are reusable
+        q.qgemv_chain(ops, sync=sync)
+        torch.cuda.synchronize()
+        assert q.qg_last_device_status() == q.QG_OK
+        assert int(sync[0].item()) == 0, "arrival count not reset"
+        assert int(sync[1].item()) == 3 * (rep + 1), "one generation per waiting op"
+    y1b, hb, y2b = bits16(y1), bits16(h), bits16(y2)
+    yref, a = O.gemv_nvfp4(wo, x, residual=r)
+    check_bf16(y1b, yref, gemv_bound(a), "dep o")
+    g_ref, ag = O.gemv_nvfp4(wgu, y1b)
+    B = swiglu_bound(g_ref[:, :I], g_ref[:, I:], gemv_bound(ag[:, :I]), gemv_bound(ag[:, I:]))
+    check_bf16(hb, O.swiglu(g_ref[:, :I], g_ref[:, I:]), B, "dep gate/up")
+    yref, a = O.gemv_nvfp4(wdn, hb, residual=y1b)
+    check_bf16(y2b, yref, gemv_bound(a), "dep down")
+    yref, a = O.gemv_nvfp4(wl, y2b)
+    check_f32(y3.cpu().numpy(), yref, gemv_bound(a), "dep last")
+
+
+def test_chain_q45_layer_full_size():
+    ops, host = [], []
+    for name, N, K, bits in synth.Q45_RECIPE:
+        w = synth.q45_weights(3, f"q45.{name}", N, K, bits)
+        x = synth.bf16_normal(72, f"chainq.{name}.x", (1, K))
+        r = synth.bf16_normal(72, f"chainq.{name}.r", (1, N)) if name == "down" else None
+        d = q45_dev(w)
+        op = {"q_lo": d["q_lo"], "q_hi": d["q_hi"], "scale": d["scale"], "min": d["min"], "x": to_dev(x),
+              "y": torch.empty((1, N), dtype=torch.bfloat16, device="cuda")}
+        if r is not None:
+            op["residual"] = to_dev(r)
+        ops.append(op)
+        host.append((name, w, x, r))
+    q.qgemv_chain(ops)
+    torch.cuda.synchronize()
+    assert q.qg_last_device_status() == q.QG_OK
+    for op, (name, w, x, r) in zip(ops, host):
+        yref, a = O.gemv_q45(w, x, residual=r)
+        check_out(op["y"], yref, a, f"chain Q {name}")
+
+
+def test_chain_mixed_formats_and_fp32_outputs():
+    """NVFP4 and Q4/Q5 ops in one launch, fp32 and bf16 outputs, ragged rows."""
+    specs = [("nvfp4", 1000, 768, torch.float32), ("q5", 333, 1024, torch.bfloat16),
+             ("q4", 2049, 512, torch.float32), ("nvfp4", 77, 2304, torch.bfloat16)]
+    ops, host = [], []
+    for i, (fmt, N, K, dt) in enumerate(specs):
+        x = synth.bf16_normal(73, f"mix.x{i}", (1, K))
+        if fmt == "nvfp4":
+            w = synth.nvfp4_weights(73, f"mix.w{i}", N, K, g=0.5)
+            d = nvfp4_dev(w)
+            op = {"codes": d["codes"], "scales": d["scales"], "g": d["g"]}
+        else:
+            w = synth.q45_weights(73, f"mix.w{i}", N, K, 5 if fmt == "q5" else 4)
+            d = q45_dev(w)
+            op = {"q_lo": d["q_lo"], "q_hi": d["q_hi"], "scale": d["scale"], "min": d["min"]}
+        op.update({"x": to_dev(x), "y": torch.empty((1, N), dtype=dt, device="cuda")})
+        ops.append(op)
+        host.append((fmt, w, x))
+    q.qgemv_chain(ops)
+    torch.cuda.synchronize()
+    assert q.qg_last_device_status() == q.QG_OK
+    for op, (fmt, w, x) in zip(ops, host):
+        yref, a = (O.gemv_nvfp4 if fmt == "nvfp4" else O.gemv_q45)(w, x)
+        check_out(op["y"], yref, a, f"chain mixed {fmt}")
+
+
+def test_chain_bounded_wait_reports_timeout_and_recovers():
+    ops, host = dense_layer_ops(1, seed=2)
+    ops = ops[:2]
+    assert q.qg_last_device_status() == q.QG_OK
+    q.qg_debug_set_wait(20_000_000, True)
+    try:
+        q.qgemv_chain(ops)
+        assert q.qg_last_device_status() == q.QG_ERR_DEVICE_TIMEOUT
+    finally:
+        q.qg_debug_set_wait(0, False)
+    q.qgemv_chain(ops)
+    torch.cuda.synchronize()
+    assert q.qg_last_device_status() == q.QG_OK
+    sep = run_separately(ops)
+    for op, ys in zip(ops, sep):
+        assert torch.equal(op["y"].view(torch.int16), ys.view(torch.int16))
