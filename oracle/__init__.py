@@ -39,6 +39,7 @@ def _configure(lib):
     lib.orc_gemv_q45.argtypes = [_P, _P, _P, _P, ctypes.c_int, _P, _P, _I64, _I64, _I64,
                                  _I64, _I64, _P, _P]
     lib.orc_swiglu.argtypes = [_P, _P, _I64, _P]
+    lib.orc_rmsnorm.argtypes = [_P, _P, _D, _I64, _I64, _P, _P, _P]
     lib.orc_round_bf16_array.argtypes = [_P, _I64, _P]
     lib.orc_bf16_bits_array.argtypes = [_P, _I64, _P]
     lib.orc_bf16_array.argtypes = [_P, _I64, _P]
@@ -167,6 +168,20 @@ def swiglu(gate, up) -> np.ndarray:
     out = np.empty(g.shape, np.float64)
     _load().orc_swiglu(_ptr(g), _ptr(u), g.size, _ptr(out))
     return out
+
+
+def rmsnorm(x, gamma, eps: float):
+    """RMSNorm of bf16 rows x[M][K] with bf16 weight gamma[K]: returns
+    (h bf16 bits [M][K], unrounded v [M][K], r [M])."""
+    xx = _c(x, np.uint16)
+    gg = _c(gamma, np.uint16)
+    M, K = xx.shape
+    assert gg.shape == (K,)
+    r = np.empty(M, np.float64)
+    v = np.empty((M, K), np.float64)
+    h = np.empty((M, K), np.uint16)
+    _load().orc_rmsnorm(_ptr(xx), _ptr(gg), float(eps), M, K, _ptr(r), _ptr(v), _ptr(h))
+    return h, v, r
 
 
 # ---------------------------------------------------------------- weights

@@ -20,6 +20,8 @@
  *     memory-bound mat-vec: NInfer article, section 2), with optional fused
  *     residual add and SwiGLU epilogues (same section: "矩阵乘、残差加、SwiGLU
  *     ... 一次读、一次写").
+ *   - RMSNorm ahead of a projection (same section: normalisation fused with
+ *     the matmul): r = 1/sqrt(mean(x^2) + eps), h = bf16(x * r * gamma).
  *   - MoE: softmax over expert logits, top-8, renormalised weights (Decapybara
  *     README, moe.cu "Top-8 门控和 softmax"); each selected expert runs
  *     gate/up + SwiGLU then down, and the outputs are summed with the weights.
@@ -238,6 +240,33 @@ double orc_silu(double v)
 void orc_swiglu(const double* gate, const double* up, int64_t n, double* out)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_silu(gate[i]) * up[i];
+}
+
+/* RMSNorm, the normalisation that decode engines fuse ahead of a projection
+ * (NInfer article, section 2: normalisation and matmul in one read and one
+ * write). For each token m, with a plain sequential fp64 sum in k order:
+ *   r_m   = 1 / sqrt( (sum_k x_mk^2) / K + eps )
+ *   v_mk  = x_mk * r_m * gamma_k
+ *   h_mk  = bf16_rne(v_mk)      -- the bf16 activation the projection reads
+ * The pages give no formula; this is the standard RMSNorm with a weight
+ * vector gamma, and h is a bf16 activation as between any two layers. */
+void orc_rmsnorm(const uint16_t* x, const uint16_t* gamma, double eps, int64_t M, int64_t K,
+                 double* r, double* v, uint16_t* h)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double xv = orc_bf16(x[m * K + k]);
+            ss += xv * xv;
+        }
+        const double rm = 1.0 / sqrt(ss / (double)K + eps);
+        r[m] = rm;
+        for (int64_t k = 0; k < K; ++k) {
+            const double vk = orc_bf16(x[m * K + k]) * rm * orc_bf16(gamma[k]);
+            v[m * K + k] = vk;
+            h[m * K + k] = (uint16_t)orc_bf16_bits(vk);
+        }
+    }
 }
 
 void orc_round_bf16_array(const double* v, int64_t n, double* out)

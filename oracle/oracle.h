@@ -39,6 +39,8 @@ void orc_gemv_q45(const uint8_t* q_lo, const uint8_t* q_hi, const uint16_t* scal
                   double* y, double* absacc);
 
 void orc_swiglu(const double* gate, const double* up, int64_t n, double* out);
+void orc_rmsnorm(const uint16_t* x, const uint16_t* gamma, double eps, int64_t M, int64_t K,
+                 double* r, double* v, uint16_t* h);
 void orc_round_bf16_array(const double* v, int64_t n, double* out);
 void orc_bf16_bits_array(const double* v, int64_t n, uint16_t* out);
 void orc_bf16_array(const uint16_t* bits, int64_t n, double* out);

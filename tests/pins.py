@@ -439,4 +439,46 @@ def pin_moe_slot_permutation():
     assert np.array_equal(y2, 2 * y)
 
 
+# ------------------------------------------------------------------ RMSNorm
+def pin_rmsnorm_hand():
+    """Two hand-worked cases (tests/golden/hand_rmsnorm.txt): mean of squares,
+    eps inside the root, gamma per element, bf16 rounding of the result."""
+    kv = read_kv("hand_rmsnorm.txt")
+    gamma = hexbytes(kv["gamma"], np.uint16)
+    for case in ("a", "b"):
+        x = hexbytes(kv["x" + case], np.uint16)[None, :]
+        h, v, r = O.rmsnorm(x, gamma, float(kv["eps" + case][0]))
+        assert r[0] == float(kv["r" + case][0]), (case, r[0])
+        assert np.array_equal(h[0], hexbytes(kv["h" + case], np.uint16)), (case, [hex(a) for a in h[0]])
+
+
+def pin_rmsnorm_invariants():
+    """Exact properties: a constant row normalises to +-1 (eps = 0); scaling x
+    by 2^j leaves h unchanged (eps = 0); doubling gamma doubles h exactly; a
+    zero row gives zeros; rows are independent."""
+    r = _rng(31)
+    K = 96
+    g1 = bf16_bits_of(np.ones(K))
+    for c in (0.75, -3.0, 2.0 ** -20):
+        x = bf16_bits_of(np.full((1, K), c))
+        h, v, rr = O.rmsnorm(x, g1, 0.0)
+        assert np.array_equal(O.bf16_array(h), np.full((1, K), math.copysign(1.0, c))), c
+    # values with at most 8 significant bits (exact in bf16)
+    x = bf16_bits_of(np.round(r.standard_normal((3, K)) * 64.0) / 64.0)
+    gamma = bf16_bits_of(np.round(r.uniform(0.5, 1.5, K) * 128.0) / 128.0)
+    h, v, rr = O.rmsnorm(x, gamma, 0.0)
+    for j in (-7, 5):
+        xs = bf16_bits_of(O.bf16_array(x) * 2.0 ** j)
+        hs, vs, _ = O.rmsnorm(xs, gamma, 0.0)
+        assert np.array_equal(hs, h) and np.array_equal(vs, v), j
+    h2, v2, _ = O.rmsnorm(x, bf16_bits_of(O.bf16_array(gamma) * 2.0), 0.0)
+    assert np.array_equal(O.bf16_array(h2), 2.0 * O.bf16_array(h))
+    hz, vz, rz = O.rmsnorm(np.zeros((1, K), np.uint16), gamma, 1e-6)
+    assert np.all(O.bf16_array(hz) == 0.0) and rz[0] == 1.0 / math.sqrt(1e-6)
+    for m in range(3):
+        hm, vm, _ = O.rmsnorm(x[m:m + 1], gamma, 0.25)
+        ha, va, _ = O.rmsnorm(x, gamma, 0.25)
+        assert np.array_equal(hm[0], ha[m]) and np.array_equal(vm[0], va[m])
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

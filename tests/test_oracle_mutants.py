@@ -50,6 +50,12 @@ MUTANTS = [
     ("moe_h_not_rounded", "h_bits[pr * I + i] = (uint16_t)orc_bf16_bits(orc_silu(gate[pr * I + i]) * up[pr * I + i]);",
      "h_bits[pr * I + i] = (uint16_t)orc_bf16_bits(orc_silu(gate[pr * I + i]) * up[pr * I + i] * 1.001);", 0),
     ("moe_weight_dropped", "acc += (use_abs ? fabs(ci) : ci) * d;", "acc += d;", 0),
+    ("rms_mean_not_divided", "1.0 / sqrt(ss / (double)K + eps)", "1.0 / sqrt(ss + eps)", 0),
+    ("rms_eps_dropped", "1.0 / sqrt(ss / (double)K + eps)", "1.0 / sqrt(ss / (double)K)", 0),
+    ("rms_no_root", "1.0 / sqrt(ss / (double)K + eps)", "1.0 / (ss / (double)K + eps)", 0),
+    ("rms_gamma_dropped", "orc_bf16(x[m * K + k]) * rm * orc_bf16(gamma[k]);", "orc_bf16(x[m * K + k]) * rm;", 0),
+    ("rms_gamma_reversed", "orc_bf16(x[m * K + k]) * rm * orc_bf16(gamma[k]);",
+     "orc_bf16(x[m * K + k]) * rm * orc_bf16(gamma[K - 1 - k]);", 0),
     ("moe_down_expert_index", "int64_t e = ids[m * topk + i];\n                const uint8_t* c = dn_codes",
      "int64_t e = ids[m * topk];\n                const uint8_t* c = dn_codes", 0),
 ]
