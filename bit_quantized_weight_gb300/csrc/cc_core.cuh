@@ -53,10 +53,30 @@ struct CcArgs {
     uint32_t mins_off;         // min boxes inside a stage
     uint32_t hi_off;           // Q5 high-bit boxes inside a stage
     uint32_t smem_gx;          // C * NSEG floats: sum of x over each k segment
+    // RMSNorm prologue (norm_w == nullptr: none): the projection reads
+    // h = bf16(x * r * gamma) with r = 1 / sqrt(mean(x^2) + eps)
+    const uint16_t* norm_w;    // gamma, bf16 [K]
+    float norm_eps;
+    uint32_t smem_ss;          // C floats: each chunk's sum of squares
     uint64_t wait_ns;
     int starve;
     int* status;
 };
+
+// Shared-memory geometry of a stage as plain values: a kernel that walks
+// several plans (the chained-layer kernel) keeps them in registers instead of
+// indexing its parameter block inside the stage loop.
+struct CcGeom {
+    int R8;
+    uint32_t scales_off;
+    uint32_t mins_off;
+    uint32_t hi_off;
+};
+
+__device__ __forceinline__ CcGeom cc_geom(const CcArgs& a)
+{
+    return CcGeom{a.R8, a.scales_off, a.mins_off, a.hi_off};
+}
 
 __device__ __forceinline__ bool cc_wait_warp(uint64_t* bar, uint32_t parity, const CcArgs& a,
                                              volatile int* abort_flag)
@@ -99,22 +119,57 @@ __device__ __forceinline__ float fma2_mixed(uint32_t w, uint32_t x, float acc)
     return r;
 }
 
-// Converts the C chunks of x into shared memory (one warp per chunk, 8
-// values per lane): f16 under the chunk's exact prescale, or raw bf16 when
-// its smallest nonzero value would fall below f16's last bit (a sufficient
-// test of exactness: scaled exponent >= -17 keeps all 8 significant bits at
-// or above 2^-24). Within a chunk, 16-byte piece p of k segment s (NSEG
-// segments of KS values) sits at p * NSEG * 16 + s * 16, so the segments'
-// i-th pieces are contiguous and one load instruction of 8 threads with 8
-// segments touches 8 different bank groups. A chunk kept raw sets *any_bf.
-// Each warp issues the loads of up to kBatch chunks before converting, so K
-// up to 80 chunks costs one round trip to memory. CG: load through L2 only
-// (x may have been written earlier in the same kernel by other CTAs).
-template <int NSEG, bool CG = false>
+// Where the activation conversion reads x: global memory through the
+// read-only path, global memory through L2 only (x written earlier in the
+// same kernel by other CTAs), or a raw copy already staged in the very
+// shared-memory buffer the conversion writes (chunk kc at byte kc * 512,
+// converted in place: each chunk is read whole by its warp before the warp
+// writes it).
+enum XSrc : int { XSRC_NC = 0, XSRC_CG = 1, XSRC_SMEM = 2 };
+
+template <int SRC>
+__device__ __forceinline__ uint4 cc_load_chunk(const CcArgs& a, const uint8_t* smem, int kc, int lane)
+{
+    if (SRC == XSRC_SMEM)
+        return lds128(smem_u32(smem + a.smem_x) + static_cast<uint32_t>(kc) * 512u + static_cast<uint32_t>(lane) * 16u);
+    return ldg_128<SRC == XSRC_CG>(a.x + static_cast<size_t>(kc) * kChunkK + lane * 8);
+}
+
+// The RMSNorm factor of the token (1 when there is no norm): chunk sums of
+// squares in shared memory (one warp per chunk), then added in k order by
+// every thread. Ends with a barrier of the compute threads.
+template <int SRC>
+__device__ float cc_norm_factor(const CcArgs& a, const uint8_t* smem, int warp, int lane)
+{
+    if (a.norm_w == nullptr) return 1.0f;
+    float* ss = reinterpret_cast<float*>(const_cast<uint8_t*>(smem) + a.smem_ss);
+    for (int kc = warp; kc < a.C; kc += kCcWarps) {
+        const float part = rms_chunk_ss(cc_load_chunk<SRC>(a, smem, kc, lane));
+        if (lane == 0) ss[kc] = part;
+    }
+    named_barrier_sync(1, kCcThreads);
+    float t = 0.f;
+    for (int kc = 0; kc < a.C; ++kc) t += ss[kc];
+    return rms_factor(t, a.K, a.norm_eps);
+}
+
+// Converts the C chunks of x (h with the RMSNorm prologue) into shared
+// memory (one warp per chunk, 8 values per lane): f16 under the chunk's exact
+// prescale, or raw bf16 when its smallest nonzero value would fall below
+// f16's last bit (a sufficient test of exactness: scaled exponent >= -17
+// keeps all 8 significant bits at or above 2^-24). Within a chunk, 16-byte
+// piece p of k segment s (NSEG segments of KS values) sits at
+// p * NSEG * 16 + s * 16, so the segments' i-th pieces are contiguous and one
+// load instruction of 8 threads with 8 segments touches 8 different bank
+// groups. A chunk kept raw sets *any_bf. Each warp issues the loads of up to
+// kBatch chunks before converting, so K up to 80 chunks costs one round trip
+// to memory.
+template <int NSEG, int SRC = XSRC_NC>
 __device__ void cc_convert(const CcArgs& a, uint8_t* smem, int warp, int lane, volatile int* any_bf)
 {
     constexpr int PPS = kChunkK / NSEG / 8;  // 16-byte pieces per segment
     constexpr int kBatch = 5;
+    const float rn = cc_norm_factor<SRC>(a, smem, warp, lane);
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
     float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
     uint8_t* fl = smem + a.smem_fl;
@@ -123,7 +178,14 @@ __device__ void cc_convert(const CcArgs& a, uint8_t* smem, int warp, int lane, v
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int kc = base + u * kCcWarps;
-            raw[u] = kc < a.C ? ldg_128<CG>(a.x + static_cast<size_t>(kc) * kChunkK + lane * 8) : make_uint4(0, 0, 0, 0);
+            raw[u] = kc < a.C ? cc_load_chunk<SRC>(a, smem, kc, lane) : make_uint4(0, 0, 0, 0);
+        }
+        if (a.norm_w != nullptr) {
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int kc = base + u * kCcWarps;
+                if (kc < a.C) raw[u] = rms_apply8(raw[u], ldg_nc_128(a.norm_w + kc * kChunkK + lane * 8), rn);
+            }
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
@@ -193,7 +255,7 @@ __device__ void cc_zero_padding(const CcArgs& a, uint8_t* smem, int nbox, const 
 // of pair products per (row, block), so eight independent multiply-add chains
 // are in flight.
 template <int NSEG, bool BF>
-__device__ __forceinline__ void cc_stage(const CcArgs& a, uint32_t stage, int b2, int row0, int seg,
+__device__ __forceinline__ void cc_stage(const CcGeom& a, uint32_t stage, int b2, int row0, int seg,
                                          const uint32_t* xw, float pe, float (&acc)[kCcRows])
 {
     constexpr int KS = kChunkK / NSEG;  // 32 or 16 k
@@ -263,13 +325,15 @@ __device__ __forceinline__ void cc_stage(const CcArgs& a, uint32_t stage, int b2
 // the activations are stored paired the same way, (x_k, x_{k+4}). The sums
 // of x per segment come from the original bf16 values, in a fixed order.
 
-// Converts x as cc_convert does, with the (k, k+4) pairing, and writes the
-// fp32 sum of each segment's original values.
-template <int NSEG, bool CG = false>
+// Converts x as cc_convert does (RMSNorm prologue included), with the
+// (k, k+4) pairing, and writes the fp32 sum of each segment's values (the
+// values the projection reads: x, or h with the prologue).
+template <int NSEG, int SRC = XSRC_NC>
 __device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lane, volatile int* any_bf)
 {
     constexpr int kBatch = 5;
     constexpr int PPS = kChunkK / NSEG / 8;  // lanes (16-byte pieces) per segment
+    const float rn = cc_norm_factor<SRC>(a, smem, warp, lane);
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
     float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
     float* gx = reinterpret_cast<float*>(smem + a.smem_gx);
@@ -279,7 +343,14 @@ __device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lan
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int kc = base + u * kCcWarps;
-            raw[u] = kc < a.C ? ldg_128<CG>(a.x + static_cast<size_t>(kc) * kChunkK + lane * 8) : make_uint4(0, 0, 0, 0);
+            raw[u] = kc < a.C ? cc_load_chunk<SRC>(a, smem, kc, lane) : make_uint4(0, 0, 0, 0);
+        }
+        if (a.norm_w != nullptr) {
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int kc = base + u * kCcWarps;
+                if (kc < a.C) raw[u] = rms_apply8(raw[u], ldg_nc_128(a.norm_w + kc * kChunkK + lane * 8), rn);
+            }
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
@@ -344,7 +415,7 @@ __device__ __forceinline__ void q45_pairs(uint32_t w, uint32_t hsp, uint32_t (&z
 // (NSEG = 8) or half of one (NSEG = 16). The bf16 path (a chunk kept raw)
 // widens the codes and activations to fp32.
 template <int NSEG, int BITS, bool BF>
-__device__ __forceinline__ void cc_stage_q45(const CcArgs& a, uint32_t stage, int b2, int row0, int seg,
+__device__ __forceinline__ void cc_stage_q45(const CcGeom& a, uint32_t stage, int b2, int row0, int seg,
                                              const uint32_t* xw, float pe, float gxs, float (&acc)[kCcRows])
 {
     constexpr int KS = kChunkK / NSEG;

@@ -155,6 +155,17 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// Plain bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global to shared memory, completing on the mbarrier.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -305,6 +316,50 @@ __device__ __forceinline__ uint32_t ldg_cg_u16(const uint16_t* p)
     uint16_t v;
     asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
     return v;
+}
+
+// ----------------------------------------------------------------- RMSNorm prologue
+// The normalisation fused ahead of a projection: for one token of K bf16
+// values, r = 1 / sqrt(sum(x^2) / K + eps) and h_k = bf16_rne(x_k * r * gamma_k);
+// the projection then reads h. Every kernel derives r in one fixed order, so
+// all CTAs of all kernels get the same bits: the squares of a 256-value chunk
+// held 8 values per lane (lane l: values 8l .. 8l+7) are summed in order per
+// lane, then by a butterfly over the warp; the chunks' sums are added in k
+// order.
+__device__ __forceinline__ float rms_chunk_ss(const uint4 raw)
+{
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+        s = fmaf(lo, lo, s);
+        s = fmaf(hi, hi, s);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    return s;
+}
+
+// r from the sum of squares (IEEE division and square root).
+__device__ __forceinline__ float rms_factor(float ss, int K, float eps)
+{
+    return 1.0f / sqrtf(__fdiv_rn(ss, static_cast<float>(K)) + eps);
+}
+
+// Eight bf16 activations (two per word) -> bf16(x * r * gamma), one rounding
+// of the fp32 product (x * r) * gamma.
+__device__ __forceinline__ uint4 rms_apply8(const uint4 x, const uint4 g, float r)
+{
+    const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, gw[4] = {g.x, g.y, g.z, g.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = (__uint_as_float(xw[i] << 16) * r) * __uint_as_float(gw[i] << 16);
+        const float hi = (__uint_as_float(xw[i] & 0xFFFF0000u) * r) * __uint_as_float(gw[i] & 0xFFFF0000u);
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[i]) : "f"(hi), "f"(lo));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // ----------------------------------------------------------------- activation prescale

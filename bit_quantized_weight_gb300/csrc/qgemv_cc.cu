@@ -93,9 +93,9 @@ __device__ __forceinline__ void cc_units(const CcArgs& a, uint8_t* smem, uint64_
                 }
                 const int kc = c * a.P + p;
                 if (!MIXED || fl[kc] == 0)
-                    cc_stage<NSEG, false>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
+                    cc_stage<NSEG, false>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], acc);
                 else
-                    cc_stage<NSEG, true>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
+                    cc_stage<NSEG, true>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], acc);
             }
             // every compute thread arrives: its own reads of the slot are done
             mbar_arrive(&empty[slot]);
@@ -290,9 +290,9 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
                 }
                 const float gxs = gx[kc * NSEG + seg];
                 if (!MIXED || fl[kc] == 0)
-                    cc_stage_q45<NSEG, BITS, false>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                    cc_stage_q45<NSEG, BITS, false>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
                 else
-                    cc_stage_q45<NSEG, BITS, true>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                    cc_stage_q45<NSEG, BITS, true>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
             }
             // every compute thread arrives: its own reads of the slot are done
             mbar_arrive(&empty[slot]);
@@ -449,9 +449,10 @@ qg_status cc_launch(CcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
     const uint32_t x_bytes = static_cast<uint32_t>(a.C) * kChunkK * 2u;
     const uint32_t pe_bytes = align_up(static_cast<uint32_t>(a.C) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(a.C), 16);
+    const uint32_t ss_bytes = a.norm_w ? align_up(static_cast<uint32_t>(a.C) * 4u, 16) : 0u;
     const uint32_t red_bytes = align_up(nbox * a.R8 * 4u, 128);
     const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
-    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + red_bytes + bar_bytes;
+    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + ss_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
     a.n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / a.stage_bytes));
 
@@ -464,6 +465,8 @@ qg_status cc_launch(CcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
     so += pe_bytes;
     a.smem_fl = so;
     so += fl_bytes;
+    a.smem_ss = so;
+    so += ss_bytes;
     a.smem_red = so;
     so += red_bytes;
     a.smem_bar = so;
@@ -523,9 +526,10 @@ qg_status cc_q45_launch(CcArgs a, const CUtensorMap (&maps)[4], int grid, cudaSt
     const uint32_t pe_bytes = align_up(static_cast<uint32_t>(a.C) * 4u, 16);
     const uint32_t gx_bytes = align_up(static_cast<uint32_t>(a.C * NSEG) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(a.C), 16);
+    const uint32_t ss_bytes = a.norm_w ? align_up(static_cast<uint32_t>(a.C) * 4u, 16) : 0u;
     const uint32_t red_bytes = align_up(nbox * a.R8 * 4u, 128);
     const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
-    const uint32_t fixed = x_bytes + pe_bytes + gx_bytes + fl_bytes + red_bytes + bar_bytes;
+    const uint32_t fixed = x_bytes + pe_bytes + gx_bytes + fl_bytes + ss_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
     a.n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / a.stage_bytes));
 
@@ -540,6 +544,8 @@ qg_status cc_q45_launch(CcArgs a, const CUtensorMap (&maps)[4], int grid, cudaSt
     so += gx_bytes;
     a.smem_fl = so;
     so += fl_bytes;
+    a.smem_ss = so;
+    so += ss_bytes;
     a.smem_red = so;
     so += red_bytes;
     a.smem_bar = so;

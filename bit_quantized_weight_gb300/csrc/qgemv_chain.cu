@@ -102,40 +102,47 @@ __device__ __forceinline__ void chain_store(const CcArgs& a, int idx, float val)
 }
 
 // The compute warps' unit loop of one NVFP4 op (cc_units of qgemv_cc.cu with
-// the ring position carried across ops and coherent residual loads).
-template <int EPI, bool MIXED>
-__device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, uint8_t* smem, uint32_t ring,
+// the ring position carried across ops, coherent residual loads, and the
+// epilogue chosen at run time: it only runs after a unit's stage loop, and one
+// loop copy for all epilogues keeps the kernel's code small).
+template <bool MIXED>
+__device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, int epi, uint8_t* smem, uint32_t ring,
                                                   uint32_t slot_bytes, int n_stages, uint64_t* full,
                                                   uint64_t* empty, volatile int* abort_flag, bool& aborted,
                                                   int& slot, int& lap)
 {
     constexpr int NSEG = kChainNseg;
-    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
     constexpr int KS = kChunkK / NSEG;
-    const int rg_per_box = (a.R + kCcRows - 1) / kCcRows;
+    const bool swiglu = epi == EPI_SWIGLU, resid = epi == EPI_RESID;
+    const int gsh = swiglu ? 1 : 0;   // log2 of the boxes per phase (gate and up rows)
+    // the op's plan in registers (the parameter block is indexed by op)
+    const CcGeom geom = cc_geom(a);
+    const int R = a.R, P = a.P, C = a.C, Cp = a.Cp, n_units = a.n_units, n_out = a.n_out;
+    const float gscale = a.g;
+    const int rg_per_box = (R + kCcRows - 1) / kCcRows;
     const int item = threadIdx.x;
     const int seg = item % NSEG;
     const int bg = item / NSEG;
     const int b2 = bg / rg_per_box;
     const int row0 = (bg % rg_per_box) * kCcRows;
-    const bool active = b2 < a.P * NGU;
-    const int p = active ? b2 / NGU : 0;
+    const bool active = b2 < (P << gsh);
+    const int p = active ? b2 >> gsh : 0;
     const uint32_t* xs = reinterpret_cast<const uint32_t*>(smem + a.smem_x);
     const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
     const uint8_t* fl = smem + a.smem_fl;
     float* red = reinterpret_cast<float*>(smem + a.smem_red);
-    const int n_mine = active ? max(0, (a.C - p + a.P - 1) / a.P) : 0;
+    const int n_mine = active ? max(0, (C - p + P - 1) / P) : 0;
     const uint32_t x0 = smem_u32(xs + p * (kChunkK / 2) + seg * 4);
-    const uint32_t x_step = static_cast<uint32_t>(a.P) * (kChunkK * 2u);
+    const uint32_t x_step = static_cast<uint32_t>(P) * (kChunkK * 2u);
 
-    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
         // the unit's residuals, read while its stages stream
         float res = 0.f;
-        const int r0 = u * a.R;
-        if (EPI == EPI_RESID && threadIdx.x < a.R && r0 + static_cast<int>(threadIdx.x) < a.n_out)
+        const int r0 = u * R;
+        if (resid && threadIdx.x < R && r0 + static_cast<int>(threadIdx.x) < n_out)
             res = bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + threadIdx.x));
-        for (int c = 0; c < a.Cp; ++c) {
+        for (int c = 0; c < Cp; ++c) {
             if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
             if (!aborted && c < n_mine) {
                 const uint32_t stage = ring + slot * slot_bytes;
@@ -146,11 +153,11 @@ __device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, uint8_t* smem
                     const uint4 v = lds128(xc + i * NSEG * 16);
                     xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
                 }
-                const int kc = c * a.P + p;
+                const int kc = c * P + p;
                 if (!MIXED || fl[kc] == 0)
-                    cc_stage<NSEG, false>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
+                    cc_stage<NSEG, false>(geom, stage, b2, row0, seg, xw, pe_all[kc], acc);
                 else
-                    cc_stage<NSEG, true>(a, stage, b2, row0, seg, xw, pe_all[kc], acc);
+                    cc_stage<NSEG, true>(geom, stage, b2, row0, seg, xw, pe_all[kc], acc);
             }
             mbar_arrive(&empty[slot]);
             if (++slot == n_stages) {
@@ -164,22 +171,22 @@ __device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, uint8_t* smem
             for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
         if (active && seg == 0) {
 #pragma unroll
-            for (int i = 0; i < kCcRows; ++i) red[b2 * a.R8 + row0 + i] = acc[i];
+            for (int i = 0; i < kCcRows; ++i) red[b2 * geom.R8 + row0 + i] = acc[i];
         }
         named_barrier_sync(1, kCcThreads);
         if (!aborted) {
-            for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
-                if (r0 + r >= a.n_out) break;
-                float v[NGU];
-#pragma unroll
-                for (int gg = 0; gg < NGU; ++gg) {
-                    float s = 0.f;
-                    for (int pp = 0; pp < a.P; ++pp) s += red[(pp * NGU + gg) * a.R8 + r];
-                    v[gg] = s * a.g;
+            for (int r = threadIdx.x; r < R; r += kCcThreads) {
+                if (r0 + r >= n_out) break;
+                float v0 = 0.f, v1 = 0.f;
+                for (int pp = 0; pp < P; ++pp) v0 += red[((pp << gsh)) * geom.R8 + r];
+                v0 *= gscale;
+                float val = v0;
+                if (swiglu) {
+                    for (int pp = 0; pp < P; ++pp) v1 += red[((pp << gsh) + 1) * geom.R8 + r];
+                    v1 *= gscale;
+                    val = (v0 / (1.0f + expf(-v0))) * v1;
                 }
-                float val = v[0];
-                if (EPI == EPI_SWIGLU) val = (val / (1.0f + expf(-val))) * v[NGU - 1];
-                if (EPI == EPI_RESID)
+                if (resid)
                     val += r == static_cast<int>(threadIdx.x) ? res
                                                               : bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + r));
                 chain_store(a, r0 + r, val);
@@ -197,33 +204,35 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, uint8_t* smem, 
 {
     constexpr int NSEG = kChainNseg;
     constexpr int KS = kChunkK / NSEG;
-    const int rg_per_box = (a.R + kCcRows - 1) / kCcRows;
+    const CcGeom geom = cc_geom(a);
+    const int R = a.R, P = a.P, C = a.C, Cp = a.Cp, n_units = a.n_units, n_out = a.n_out;
+    const int rg_per_box = (R + kCcRows - 1) / kCcRows;
     const int item = threadIdx.x;
     const int seg = item % NSEG;
     const int bg = item / NSEG;
     const int b2 = bg / rg_per_box;
     const int row0 = (bg % rg_per_box) * kCcRows;
-    const bool active = b2 < a.P;
+    const bool active = b2 < P;
     const int p = active ? b2 : 0;
     const uint32_t* xs = reinterpret_cast<const uint32_t*>(smem + a.smem_x);
     const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
     const float* gx = reinterpret_cast<const float*>(smem + a.smem_gx);
     const uint8_t* fl = smem + a.smem_fl;
     float* red = reinterpret_cast<float*>(smem + a.smem_red);
-    const int n_mine = active ? max(0, (a.C - p + a.P - 1) / a.P) : 0;
+    const int n_mine = active ? max(0, (C - p + P - 1) / P) : 0;
     const uint32_t x0 = smem_u32(xs + p * (kChunkK / 2) + seg * 4);
-    const uint32_t x_step = static_cast<uint32_t>(a.P) * (kChunkK * 2u);
+    const uint32_t x_step = static_cast<uint32_t>(P) * (kChunkK * 2u);
 
-    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
         float res = 0.f;
-        const int r0 = u * a.R;
-        if (EPI == EPI_RESID && threadIdx.x < a.R && r0 + static_cast<int>(threadIdx.x) < a.n_out)
+        const int r0 = u * R;
+        if (EPI == EPI_RESID && threadIdx.x < R && r0 + static_cast<int>(threadIdx.x) < n_out)
             res = bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + threadIdx.x));
-        for (int c = 0; c < a.Cp; ++c) {
+        for (int c = 0; c < Cp; ++c) {
             if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
             if (!aborted && c < n_mine) {
-                const int kc = c * a.P + p;
+                const int kc = c * P + p;
                 const uint32_t stage = ring + slot * slot_bytes;
                 uint32_t xw[KS / 2];
                 const uint32_t xc = x0 + static_cast<uint32_t>(c) * x_step;
@@ -234,9 +243,9 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, uint8_t* smem, 
                 }
                 const float gxs = gx[kc * NSEG + seg];
                 if (!MIXED || fl[kc] == 0)
-                    cc_stage_q45<NSEG, BITS, false>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                    cc_stage_q45<NSEG, BITS, false>(geom, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
                 else
-                    cc_stage_q45<NSEG, BITS, true>(a, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                    cc_stage_q45<NSEG, BITS, true>(geom, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
             }
             mbar_arrive(&empty[slot]);
             if (++slot == n_stages) {
@@ -250,14 +259,14 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, uint8_t* smem, 
             for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
         if (active && seg == 0) {
 #pragma unroll
-            for (int i = 0; i < kCcRows; ++i) red[b2 * a.R8 + row0 + i] = acc[i];
+            for (int i = 0; i < kCcRows; ++i) red[b2 * geom.R8 + row0 + i] = acc[i];
         }
         named_barrier_sync(1, kCcThreads);
         if (!aborted) {
-            for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
-                if (r0 + r >= a.n_out) break;
+            for (int r = threadIdx.x; r < R; r += kCcThreads) {
+                if (r0 + r >= n_out) break;
                 float val = 0.f;
-                for (int pp = 0; pp < a.P; ++pp) val += red[pp * a.R8 + r];
+                for (int pp = 0; pp < P; ++pp) val += red[pp * geom.R8 + r];
                 if (EPI == EPI_RESID)
                     val += r == static_cast<int>(threadIdx.x) ? res
                                                               : bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + r));
@@ -268,17 +277,16 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, uint8_t* smem, 
     }
 }
 
-template <int EPI>
-__device__ __forceinline__ void chain_nvfp4(const CcArgs& a, bool mixed, uint8_t* smem, uint32_t ring,
+__device__ __forceinline__ void chain_nvfp4(const CcArgs& a, int epi, bool mixed, uint8_t* smem, uint32_t ring,
                                             uint32_t slot_bytes, int n_stages, uint64_t* full, uint64_t* empty,
                                             volatile int* abort_flag, bool& aborted, int& slot, int& lap)
 {
     if (mixed)
-        chain_units_nvfp4<EPI, true>(a, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted, slot,
-                                     lap);
+        chain_units_nvfp4<true>(a, epi, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted, slot,
+                                lap);
     else
-        chain_units_nvfp4<EPI, false>(a, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted, slot,
-                                      lap);
+        chain_units_nvfp4<false>(a, epi, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted, slot,
+                                 lap);
 }
 
 template <int BITS, int EPI>
@@ -335,9 +343,12 @@ __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_co
             const CcArgs& a = p.op[o].a;
             const int fmt = p.op[o].fmt;
             const int ngu = p.op[o].epi == EPI_SWIGLU ? 2 : 1;
-            for (int u = blockIdx.x; u < a.n_units && !stop; u += gridDim.x) {
-                const int row0 = u * a.R;
-                for (int c = 0; c < a.Cp; ++c) {
+            const int P = a.P, C = a.C, Cp = a.Cp, R = a.R, n_units = a.n_units, up_off = a.up_row_offset;
+            const uint32_t box_bytes = static_cast<uint32_t>(a.R8) * 128u, sbox_bytes = static_cast<uint32_t>(a.R8) * 16u;
+            const uint32_t scales_off = a.scales_off, mins_off = a.mins_off, hi_off = a.hi_off, box_tx = a.box_tx;
+            for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+                const int row0 = u * R;
+                for (int c = 0; c < Cp; ++c) {
                     if (lap > 0 && !cc_wait_warp(&empty[slot], (lap - 1) & 1, a, abort_flag)) {
                         stop = true;
                         break;
@@ -347,32 +358,32 @@ __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_co
                         break;
                     }
                     int live = 0;
-                    for (int pp = 0; pp < a.P; ++pp) live += (c * a.P + pp < a.C) ? 1 : 0;
+                    for (int pp = 0; pp < P; ++pp) live += (c * P + pp < C) ? 1 : 0;
                     uint8_t* sb = smem + a.smem_ring + slot * p.slot_bytes;
                     if (elect_one()) {
-                        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live * ngu) * a.box_tx);
-                        for (int pp = 0; pp < a.P; ++pp) {
-                            const int kc = c * a.P + pp;
-                            if (kc >= a.C) continue;
+                        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live * ngu) * box_tx);
+                        for (int pp = 0; pp < P; ++pp) {
+                            const int kc = c * P + pp;
+                            if (kc >= C) continue;
                             if (fmt == FMT_NVFP4) {
                                 for (int gg = 0; gg < ngu; ++gg) {
                                     const int b2 = pp * ngu + gg;
-                                    const int row = row0 + gg * a.up_row_offset;
-                                    tma_load_2d(sb + b2 * a.R8 * 128, &p.map[o][0], kc * (kChunkK / 2), row,
+                                    const int row = row0 + gg * up_off;
+                                    tma_load_2d(sb + b2 * box_bytes, &p.map[o][0], kc * (kChunkK / 2), row,
                                                 &full[slot]);
-                                    tma_load_2d(sb + a.scales_off + b2 * a.R8 * 16, &p.map[o][1],
+                                    tma_load_2d(sb + scales_off + b2 * sbox_bytes, &p.map[o][1],
                                                 kc * (kChunkK / 16), row, &full[slot]);
                                 }
                             } else {
-                                tma_load_2d(sb + pp * a.R8 * 128, &p.map[o][0], kc * (kChunkK / 2), row0,
+                                tma_load_2d(sb + pp * box_bytes, &p.map[o][0], kc * (kChunkK / 2), row0,
                                             &full[slot]);
-                                tma_load_2d(sb + a.scales_off + pp * a.R8 * 16, &p.map[o][1], kc * (kChunkK / 32),
+                                tma_load_2d(sb + scales_off + pp * sbox_bytes, &p.map[o][1], kc * (kChunkK / 32),
                                             row0, &full[slot]);
-                                tma_load_2d(sb + a.mins_off + pp * a.R8 * 16, &p.map[o][2], kc * (kChunkK / 32),
+                                tma_load_2d(sb + mins_off + pp * sbox_bytes, &p.map[o][2], kc * (kChunkK / 32),
                                             row0, &full[slot]);
                                 if (fmt == FMT_Q5)
-                                    tma_load_2d(sb + a.hi_off + pp * a.R8 * 32, &p.map[o][3], kc * (kChunkK / 8),
-                                                row0, &full[slot]);
+                                    tma_load_2d(sb + hi_off + pp * 2u * sbox_bytes, &p.map[o][3],
+                                                kc * (kChunkK / 8), row0, &full[slot]);
                             }
                         }
                     }
@@ -405,22 +416,16 @@ __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_co
         if (*abort_flag) aborted = true;
         if (threadIdx.x == 0) *any_bf = 0;
         named_barrier_sync(1, kCcThreads);
+        // x through L2 only: an earlier op of this launch may have written it
         if (op.fmt == FMT_NVFP4)
-            cc_convert<kChainNseg, true>(a, smem, warp, lane, any_bf);
+            cc_convert<kChainNseg, XSRC_CG>(a, smem, warp, lane, any_bf);
         else
-            cc_convert_q45<kChainNseg, true>(a, smem, warp, lane, any_bf);
+            cc_convert_q45<kChainNseg, XSRC_CG>(a, smem, warp, lane, any_bf);
         named_barrier_sync(1, kCcThreads);
         const bool mixed = *any_bf != 0;
         if (op.fmt == FMT_NVFP4) {
-            if (op.epi == EPI_SWIGLU)
-                chain_nvfp4<EPI_SWIGLU>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                        aborted, slot, lap);
-            else if (op.epi == EPI_RESID)
-                chain_nvfp4<EPI_RESID>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                       aborted, slot, lap);
-            else
-                chain_nvfp4<EPI_NONE>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                      aborted, slot, lap);
+            chain_nvfp4(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag, aborted,
+                        slot, lap);
         } else if (op.fmt == FMT_Q5) {
             if (op.epi == EPI_RESID)
                 chain_q45<5, EPI_RESID>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
@@ -534,14 +539,18 @@ qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, 
         }
     }
     if (any_dep && !sync) return QG_ERR_INVALID_ARG;
-    // shared memory: ring | activations | 2^-prescale | flags | sums of x | partial sums | barriers
+    // shared memory: ring | activations | 2^-prescale | flags | sums of x |
+    // sums of squares | partial sums | barriers
     const uint32_t x_bytes = static_cast<uint32_t>(c_max) * kChunkK * 2u;
     const uint32_t pe_bytes = align_up(static_cast<uint32_t>(c_max) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(c_max), 16);
-    const uint32_t gx_bytes = align_up(static_cast<uint32_t>(c_max * kChainNseg) * 4u, 16);
+    bool any_q = false;
+    for (int o = 0; o < n_ops; ++o) any_q = any_q || p.op[o].fmt != FMT_NVFP4;
+    const uint32_t gx_bytes = any_q ? align_up(static_cast<uint32_t>(c_max * kChainNseg) * 4u, 16) : 0u;
+    const uint32_t ss_bytes = align_up(static_cast<uint32_t>(c_max) * 4u, 16);
     const uint32_t red_bytes = align_up(static_cast<uint32_t>(red_max) * 4u, 128);
     const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
-    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + gx_bytes + red_bytes + bar_bytes;
+    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + gx_bytes + ss_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * slot_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
     const int n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / slot_bytes));
     uint32_t so = 0;
@@ -555,6 +564,8 @@ qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, 
     so += fl_bytes;
     const uint32_t smem_gx = so;
     so += gx_bytes;
+    const uint32_t smem_ss = so;
+    so += ss_bytes;
     const uint32_t smem_red = so;
     so += red_bytes;
     const uint32_t smem_bar = so;
@@ -577,6 +588,7 @@ qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, 
         a.stage_bytes = slot_bytes;
         a.smem_ring = smem_ring;
         a.smem_x = smem_x;
+        a.smem_ss = smem_ss;
         a.smem_pe = smem_pe;
         a.smem_fl = smem_fl;
         a.smem_gx = smem_gx;
