@@ -138,16 +138,29 @@ __device__ __forceinline__ uint4 cc_load_chunk(const CcArgs& a, const uint8_t* s
 // The RMSNorm factor of the token (1 when there is no norm): chunk sums of
 // squares in shared memory (one warp per chunk), then added in k order by
 // every thread. Ends with a barrier of the compute threads.
-template <int SRC>
+// The warps converting: all 16 compute warps (barrier 1), a group of
+// converter warps (barrier 2), or one warp alone.
+template <int NW>
+__device__ __forceinline__ void cc_conv_sync()
+{
+    if (NW == 1)
+        __syncwarp();
+    else if (NW == kCcWarps)
+        named_barrier_sync(1, kCcThreads);
+    else
+        named_barrier_sync(2, 32 * NW);
+}
+
+template <int SRC, int NW = kCcWarps>
 __device__ float cc_norm_factor(const CcArgs& a, const uint8_t* smem, int warp, int lane)
 {
     if (a.norm_w == nullptr) return 1.0f;
     float* ss = reinterpret_cast<float*>(const_cast<uint8_t*>(smem) + a.smem_ss);
-    for (int kc = warp; kc < a.C; kc += kCcWarps) {
+    for (int kc = warp; kc < a.C; kc += NW) {
         const float part = rms_chunk_ss(cc_load_chunk<SRC>(a, smem, kc, lane));
         if (lane == 0) ss[kc] = part;
     }
-    named_barrier_sync(1, kCcThreads);
+    cc_conv_sync<NW>();
     float t = 0.f;
     for (int kc = 0; kc < a.C; ++kc) t += ss[kc];
     return rms_factor(t, a.K, a.norm_eps);
@@ -164,32 +177,32 @@ __device__ float cc_norm_factor(const CcArgs& a, const uint8_t* smem, int warp, 
 // groups. A chunk kept raw sets *any_bf. Each warp issues the loads of up to
 // kBatch chunks before converting, so K up to 80 chunks costs one round trip
 // to memory.
-template <int NSEG, int SRC = XSRC_NC>
+template <int NSEG, int SRC = XSRC_NC, int NW = kCcWarps>
 __device__ void cc_convert(const CcArgs& a, uint8_t* smem, int warp, int lane, volatile int* any_bf)
 {
     constexpr int PPS = kChunkK / NSEG / 8;  // 16-byte pieces per segment
-    constexpr int kBatch = 5;
-    const float rn = cc_norm_factor<SRC>(a, smem, warp, lane);
+    constexpr int kBatch = NW < kCcWarps ? 8 : 5;
+    const float rn = cc_norm_factor<SRC, NW>(a, smem, warp, lane);
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
     float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
     uint8_t* fl = smem + a.smem_fl;
-    for (int base = warp; base < a.C; base += kCcWarps * kBatch) {
+    for (int base = warp; base < a.C; base += NW * kBatch) {
         uint4 raw[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            const int kc = base + u * kCcWarps;
+            const int kc = base + u * NW;
             raw[u] = kc < a.C ? cc_load_chunk<SRC>(a, smem, kc, lane) : make_uint4(0, 0, 0, 0);
         }
         if (a.norm_w != nullptr) {
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
-                const int kc = base + u * kCcWarps;
+                const int kc = base + u * NW;
                 if (kc < a.C) raw[u] = rms_apply8(raw[u], ldg_nc_128(a.norm_w + kc * kChunkK + lane * 8), rn);
             }
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            const int kc = base + u * kCcWarps;
+            const int kc = base + u * NW;
             if (kc >= a.C) break;
             const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
             uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
@@ -328,33 +341,33 @@ __device__ __forceinline__ void cc_stage(const CcGeom& a, uint32_t stage, int b2
 // Converts x as cc_convert does (RMSNorm prologue included), with the
 // (k, k+4) pairing, and writes the fp32 sum of each segment's values (the
 // values the projection reads: x, or h with the prologue).
-template <int NSEG, int SRC = XSRC_NC>
+template <int NSEG, int SRC = XSRC_NC, int NW = kCcWarps>
 __device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lane, volatile int* any_bf)
 {
-    constexpr int kBatch = 5;
+    constexpr int kBatch = NW < kCcWarps ? 8 : 5;
     constexpr int PPS = kChunkK / NSEG / 8;  // lanes (16-byte pieces) per segment
-    const float rn = cc_norm_factor<SRC>(a, smem, warp, lane);
+    const float rn = cc_norm_factor<SRC, NW>(a, smem, warp, lane);
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
     float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
     float* gx = reinterpret_cast<float*>(smem + a.smem_gx);
     uint8_t* fl = smem + a.smem_fl;
-    for (int base = warp; base < a.C; base += kCcWarps * kBatch) {
+    for (int base = warp; base < a.C; base += NW * kBatch) {
         uint4 raw[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            const int kc = base + u * kCcWarps;
+            const int kc = base + u * NW;
             raw[u] = kc < a.C ? cc_load_chunk<SRC>(a, smem, kc, lane) : make_uint4(0, 0, 0, 0);
         }
         if (a.norm_w != nullptr) {
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
-                const int kc = base + u * kCcWarps;
+                const int kc = base + u * NW;
                 if (kc < a.C) raw[u] = rms_apply8(raw[u], ldg_nc_128(a.norm_w + kc * kChunkK + lane * 8), rn);
             }
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            const int kc = base + u * kCcWarps;
+            const int kc = base + u * NW;
             if (kc >= a.C) break;
             const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
             float sx = 0.f;
