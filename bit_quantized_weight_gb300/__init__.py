@@ -10,6 +10,6 @@ from .qgemv import (  # noqa: F401
     QG_ERR_CUDA, QG_ERR_DEVICE_TIMEOUT, QGemvError, lib, lib_path,
     qgemv_nvfp4, qgemv_q45, qgemv_swiglu_nvfp4, moe_route_topk, moe_qgemv_nvfp4, moe_qgemv_nvfp4_noalloc,
     moe_qgemv_nvfp4_workspace_size, qdequant_nvfp4, qdequant_q45, qg_last_device_status,
-    qg_status_string, qg_debug_set_wait, read_probe, GemvChain, qgemv_chain, QgGemvOp,
+    qg_status_string, qg_debug_set_wait, read_probe, GemvChain, qgemv_chain, QgGemvOp, qgemv_swiglu_q45,
     QG_FMT_NVFP4, QG_FMT_Q4, QG_FMT_Q5, QG_EPI_NONE, QG_EPI_RESIDUAL, QG_EPI_SWIGLU,
 )

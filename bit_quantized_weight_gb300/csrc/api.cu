@@ -120,6 +120,124 @@ qg_status dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, cons
     return launch_dense_nvfp4(codes, scales, g, x, y, f32, residual, M, N, K, swiglu, stream);
 }
 
+// Validation of one qg_gemv_op record (qgemv_chain, qgemv_swiglu_q45).
+qg_status check_op(const qg_gemv_op& g, int M)
+{
+    if (g.format != QG_FMT_NVFP4 && g.format != QG_FMT_Q4 && g.format != QG_FMT_Q5) return QG_ERR_INVALID_ARG;
+    if (g.epilogue != QG_EPI_NONE && g.epilogue != QG_EPI_RESIDUAL && g.epilogue != QG_EPI_SWIGLU)
+        return QG_ERR_INVALID_ARG;
+    if (g.y_dtype != QG_OUT_BF16 && g.y_dtype != QG_OUT_F32) return QG_ERR_INVALID_ARG;
+    if ((g.epilogue == QG_EPI_RESIDUAL) != (g.residual != nullptr)) return QG_ERR_INVALID_ARG;
+    const bool sep_up = g.up_codes != nullptr;
+    if (g.epilogue == QG_EPI_SWIGLU) {
+        if (g.y_dtype != QG_OUT_BF16) return QG_ERR_INVALID_ARG;
+        // NVFP4: gate and up rows in one matrix; groupwise int: a separate up matrix
+        if (g.format == QG_FMT_NVFP4 ? (sep_up || g.N % 2) : !sep_up) return QG_ERR_INVALID_ARG;
+    } else if (sep_up) {
+        return QG_ERR_INVALID_ARG;
+    }
+    qg_status s = check_dense(g.codes, g.scales, g.x, g.y, g.residual, M, g.N, g.K);
+    if (s != QG_OK) return s;
+    if (g.format == QG_FMT_NVFP4) {
+        if (g.q_hi || g.mins) return QG_ERR_INVALID_ARG;
+    } else {
+        if (!g.mins || ((g.format == QG_FMT_Q5) != (g.q_hi != nullptr))) return QG_ERR_INVALID_ARG;
+        if (!aligned16(g.mins) || (g.q_hi && !aligned16(g.q_hi))) return QG_ERR_MISALIGNED;
+    }
+    if (sep_up) {
+        if (g.up_format != QG_FMT_Q4 && g.up_format != QG_FMT_Q5) return QG_ERR_INVALID_ARG;
+        if (!g.up_scales || !g.up_mins || ((g.up_format == QG_FMT_Q5) != (g.up_q_hi != nullptr)))
+            return QG_ERR_INVALID_ARG;
+        if (!aligned16(g.up_codes) || !aligned16(g.up_scales) || !aligned16(g.up_mins) ||
+            (g.up_q_hi && !aligned16(g.up_q_hi)))
+            return QG_ERR_MISALIGNED;
+    } else if (g.up_q_hi || g.up_scales || g.up_mins) {
+        return QG_ERR_INVALID_ARG;
+    }
+    if (g.norm_weight && !aligned16(g.norm_weight)) return QG_ERR_MISALIGNED;
+    return QG_OK;
+}
+
+// The exact warp-per-row kernel for a record (any M and K).
+qg_status run_op_simple(const qg_gemv_op& g, int M, cudaStream_t stream)
+{
+    const bool swiglu = g.epilogue == QG_EPI_SWIGLU;
+    const bool sep_up = g.up_codes != nullptr;
+    SimpleArgs a{};
+    a.fmt = g.format == QG_FMT_NVFP4 ? FMT_NVFP4 : g.format == QG_FMT_Q5 ? FMT_Q5 : FMT_Q4;
+    a.codes = g.codes;
+    a.q_hi = g.q_hi;
+    a.scales = g.scales;
+    a.mins = g.mins;
+    a.g = g.format == QG_FMT_NVFP4 ? g.global_scale : 1.f;
+    if (sep_up) {
+        a.ufmt = g.up_format == QG_FMT_Q5 ? FMT_Q5 : FMT_Q4;
+        a.ucodes = g.up_codes;
+        a.uq_hi = g.up_q_hi;
+        a.uscales = g.up_scales;
+        a.umins = g.up_mins;
+        a.ug = 1.f;
+    }
+    a.x = static_cast<const uint16_t*>(g.x);
+    a.y = g.y;
+    a.out_f32 = g.y_dtype == QG_OUT_F32 && !swiglu;
+    a.residual = static_cast<const uint16_t*>(g.residual);
+    a.norm_w = static_cast<const uint16_t*>(g.norm_weight);
+    a.norm_eps = g.norm_eps;
+    a.M = M;
+    a.n_out = swiglu && !sep_up ? g.N / 2 : g.N;
+    a.K = g.K;
+    a.swiglu = swiglu ? 1 : 0;
+    return launch_simple_args(a, stream);
+}
+
+// One validated record on the kernel that serves it.
+qg_status run_op(const qg_gemv_op& g, int M, cudaStream_t stream)
+{
+    const int f32 = g.y_dtype == QG_OUT_F32;
+    const bool swiglu = g.epilogue == QG_EPI_SWIGLU;
+    const bool full_chunks = g.K % kChunkK == 0;
+    if (g.format == QG_FMT_NVFP4) {
+        const uint8_t* sc = static_cast<const uint8_t*>(g.scales);
+        if (!g.norm_weight) {
+            if (!full_chunks)
+                return launch_simple(FMT_NVFP4, g.codes, nullptr, sc, nullptr, g.global_scale, g.x, g.y,
+                                     swiglu ? 0 : f32, g.residual, M, g.N, g.K, swiglu ? 1 : 0, stream);
+            return dense_nvfp4(g.codes, sc, g.global_scale, g.x, g.y, swiglu ? 0 : f32, g.residual, M, g.N, g.K,
+                               swiglu ? 1 : 0, stream);
+        }
+        if (full_chunks) {
+            qg_status s = launch_cc_dense_nvfp4(g.codes, sc, g.global_scale, g.x, g.y, swiglu ? 0 : f32, g.residual,
+                                                M, g.N, g.K, swiglu ? 1 : 0, stream, g.norm_weight, g.norm_eps);
+            if (s != QG_ERR_UNSUPPORTED) return s;
+            s = launch_tc_dense_nvfp4(g.codes, sc, g.global_scale, g.x, g.y, swiglu ? 0 : f32, g.residual, M, g.N,
+                                      g.K, swiglu ? 1 : 0, stream, g.norm_weight, g.norm_eps);
+            if (s != QG_ERR_UNSUPPORTED) return s;
+        }
+        return run_op_simple(g, M, stream);
+    }
+    const int bits = g.format == QG_FMT_Q5 ? 5 : 4;
+    if (swiglu) {
+        if (full_chunks) {
+            const Q45Matrix gate{g.codes, g.q_hi, g.scales, g.mins, bits};
+            const Q45Matrix up{g.up_codes, g.up_q_hi, g.up_scales, g.up_mins, g.up_format == QG_FMT_Q5 ? 5 : 4};
+            const qg_status s = launch_cc_swiglu_q45(gate, up, g.x, g.y, M, g.N, g.K, stream, g.norm_weight,
+                                                     g.norm_eps);
+            if (s != QG_ERR_UNSUPPORTED) return s;
+        }
+        return run_op_simple(g, M, stream);
+    }
+    if (full_chunks) {
+        qg_status s = launch_cc_dense_q45(g.codes, g.q_hi, g.scales, g.mins, bits, g.x, g.y, f32, g.residual, M,
+                                          g.N, g.K, stream, g.norm_weight, g.norm_eps);
+        if (s != QG_ERR_UNSUPPORTED) return s;
+        if (!g.norm_weight)
+            return launch_dense_q45(g.codes, g.q_hi, g.scales, g.mins, bits, g.x, g.y, f32, g.residual, M, g.N,
+                                    g.K, stream);
+    }
+    return run_op_simple(g, M, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -213,23 +331,9 @@ qg_status qgemv_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, c
     if (!ops || n_ops < 1 || n_ops > 8 || M < 1 || M > kMaxTokens) return QG_ERR_INVALID_ARG;
     bool any_dep = false;
     for (int o = 0; o < n_ops; ++o) {
-        const qg_gemv_op& g = ops[o];
-        if (g.format != QG_FMT_NVFP4 && g.format != QG_FMT_Q4 && g.format != QG_FMT_Q5) return QG_ERR_INVALID_ARG;
-        if (g.epilogue != QG_EPI_NONE && g.epilogue != QG_EPI_RESIDUAL && g.epilogue != QG_EPI_SWIGLU)
-            return QG_ERR_INVALID_ARG;
-        if (g.y_dtype != QG_OUT_BF16 && g.y_dtype != QG_OUT_F32) return QG_ERR_INVALID_ARG;
-        if ((g.epilogue == QG_EPI_RESIDUAL) != (g.residual != nullptr)) return QG_ERR_INVALID_ARG;
-        if (g.epilogue == QG_EPI_SWIGLU && (g.format != QG_FMT_NVFP4 || g.y_dtype != QG_OUT_BF16 || g.N % 2))
-            return QG_ERR_INVALID_ARG;
-        qg_status s = check_dense(g.codes, g.scales, g.x, g.y, g.residual, M, g.N, g.K);
+        const qg_status s = check_op(ops[o], M);
         if (s != QG_OK) return s;
-        if (g.format == QG_FMT_NVFP4) {
-            if (g.q_hi || g.mins) return QG_ERR_INVALID_ARG;
-        } else {
-            if (!g.mins || ((g.format == QG_FMT_Q5) != (g.q_hi != nullptr))) return QG_ERR_INVALID_ARG;
-            if (!aligned16(g.mins) || (g.q_hi && !aligned16(g.q_hi))) return QG_ERR_MISALIGNED;
-        }
-        any_dep = any_dep || (o > 0 && g.after_previous);
+        any_dep = any_dep || (o > 0 && ops[o].after_previous);
     }
     if (sync && !aligned16(sync)) return QG_ERR_MISALIGNED;
     if (any_dep && !sync) return QG_ERR_INVALID_ARG;
@@ -237,20 +341,41 @@ qg_status qgemv_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, c
     if (s != QG_ERR_UNSUPPORTED) return s;
     // One launch per op, in stream order (which also orders dependent ops).
     for (int o = 0; o < n_ops; ++o) {
-        const qg_gemv_op& g = ops[o];
-        const qg_out out = g.y_dtype == QG_OUT_F32 ? QG_OUT_F32 : QG_OUT_BF16;
-        if (g.format == QG_FMT_NVFP4 && g.epilogue == QG_EPI_SWIGLU)
-            s = qgemv_swiglu_nvfp4(g.codes, static_cast<const uint8_t*>(g.scales), g.global_scale, g.x, g.y, M,
-                                   g.N, g.K, stream);
-        else if (g.format == QG_FMT_NVFP4)
-            s = qgemv_nvfp4(g.codes, static_cast<const uint8_t*>(g.scales), g.global_scale, g.x, g.y, out,
-                            g.residual, M, g.N, g.K, stream);
-        else
-            s = qgemv_q45(g.codes, g.q_hi, g.scales, g.mins, g.format == QG_FMT_Q5 ? 5 : 4, g.x, g.y, out,
-                          g.residual, M, g.N, g.K, stream);
+        s = run_op(ops[o], M, stream);
         if (s != QG_OK) return s;
     }
     return QG_OK;
+}
+
+qg_status qgemv_swiglu_q45(const uint8_t* gate_lo, const uint8_t* gate_hi, const void* gate_scale,
+                           const void* gate_min, int gate_bits, const uint8_t* up_lo, const uint8_t* up_hi,
+                           const void* up_scale, const void* up_min, int up_bits, const void* x,
+                           const void* norm_weight, float norm_eps, void* y, int M, int I, int K, cudaStream_t stream)
+{
+    if ((gate_bits != 4 && gate_bits != 5) || (up_bits != 4 && up_bits != 5)) return QG_ERR_INVALID_ARG;
+    qg_gemv_op g{};
+    g.format = gate_bits == 5 ? QG_FMT_Q5 : QG_FMT_Q4;
+    g.epilogue = QG_EPI_SWIGLU;
+    g.y_dtype = QG_OUT_BF16;
+    g.N = I;
+    g.K = K;
+    g.codes = gate_lo;
+    g.q_hi = gate_hi;
+    g.scales = gate_scale;
+    g.mins = gate_min;
+    g.global_scale = 1.f;
+    g.x = x;
+    g.y = y;
+    g.norm_weight = norm_weight;
+    g.norm_eps = norm_eps;
+    g.up_format = up_bits == 5 ? QG_FMT_Q5 : QG_FMT_Q4;
+    g.up_codes = up_lo;
+    g.up_q_hi = up_hi;
+    g.up_scales = up_scale;
+    g.up_mins = up_min;
+    const qg_status s = check_op(g, M);
+    if (s != QG_OK) return s;
+    return run_op(g, M, stream);
 }
 
 qg_status qdequant_nvfp4(const uint8_t* codes, const uint8_t* scales, float global_scale, float* w, int N, int K,

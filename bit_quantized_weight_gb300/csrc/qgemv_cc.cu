@@ -240,11 +240,14 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
 
 // The compute warps' unit loop of the groupwise-int kernel (MIXED as in
 // cc_units).
-template <int BITS, int EPI, int NSEG, bool MIXED>
+// SwiGLU (a separate up matrix of BITS_U-bit codes): each phase holds a gate
+// box (BITS) and an up box (BITS_U).
+template <int BITS, int EPI, int NSEG, bool MIXED, int BITS_U = BITS>
 __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                              volatile int* abort_flag)
 {
     constexpr int KS = kChunkK / NSEG;
+    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
     // item = (box, row group, segment); the row groups cover rows 0 .. R
     // rounded up to 4
     const int rg_per_box = (a.R + kCcRows - 1) / kCcRows;
@@ -253,8 +256,9 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
     const int bg = item / NSEG;
     const int b2 = bg / rg_per_box;
     const int row0 = (bg % rg_per_box) * kCcRows;
-    const bool active = b2 < a.P;
-    const int p = active ? b2 : 0;
+    const bool active = b2 < a.P * NGU;
+    const int p = active ? b2 / NGU : 0;
+    const bool up_box = NGU == 2 && (b2 & 1);
     const uint32_t* xs = reinterpret_cast<const uint32_t*>(smem + a.smem_x);
     const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
     const float* gx = reinterpret_cast<const float*>(smem + a.smem_gx);
@@ -289,10 +293,17 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
                     xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
                 }
                 const float gxs = gx[kc * NSEG + seg];
-                if (!MIXED || fl[kc] == 0)
-                    cc_stage_q45<NSEG, BITS, false>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
-                else
-                    cc_stage_q45<NSEG, BITS, true>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                if (up_box) {
+                    if (!MIXED || fl[kc] == 0)
+                        cc_stage_q45<NSEG, BITS_U, false>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                    else
+                        cc_stage_q45<NSEG, BITS_U, true>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                } else {
+                    if (!MIXED || fl[kc] == 0)
+                        cc_stage_q45<NSEG, BITS, false>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                    else
+                        cc_stage_q45<NSEG, BITS, true>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                }
             }
             // every compute thread arrives: its own reads of the slot are done
             mbar_arrive(&empty[slot]);
@@ -317,9 +328,15 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
             const int r0 = u * a.R;
             for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
                 if (r0 + r >= a.n_out) break;
-                float s = 0.f;
-                for (int pp = 0; pp < a.P; ++pp) s += red[pp * a.R8 + r];
-                float val = s;
+                float v[NGU];
+#pragma unroll
+                for (int gg = 0; gg < NGU; ++gg) {
+                    float s = 0.f;
+                    for (int pp = 0; pp < a.P; ++pp) s += red[(pp * NGU + gg) * a.R8 + r];
+                    v[gg] = s;
+                }
+                float val = v[0];
+                if (EPI == EPI_SWIGLU) val = (val / (1.0f + expf(-val))) * v[NGU - 1];
                 if (EPI == EPI_RESID)
                     val += u == static_cast<int>(blockIdx.x) && r == static_cast<int>(threadIdx.x)
                                ? res_first
@@ -334,12 +351,16 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
     }
 }
 
-template <int BITS, int EPI, int NSEG>
+// The groupwise-int maps of one matrix: codes (q_lo), scales, mins, Q5 plane.
+struct Q45Maps {
+    CUtensorMap m[2][4];  // [gate or only matrix, SwiGLU up matrix][codes, scales, mins, hi]
+};
+
+template <int BITS, int EPI, int NSEG, int BITS_U>
 __global__ void __launch_bounds__(kCcAllThreads, 1)
-    cc_q45_kernel(const __grid_constant__ CcArgs a, const __grid_constant__ CUtensorMap tm_codes,
-                  const __grid_constant__ CUtensorMap tm_scales, const __grid_constant__ CUtensorMap tm_mins,
-                  const __grid_constant__ CUtensorMap tm_hi)
+    cc_q45_kernel(const __grid_constant__ CcArgs a, const __grid_constant__ Q45Maps maps)
 {
+    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = warp_index_uniform();
     const int lane = threadIdx.x & 31;
@@ -364,10 +385,12 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     if (warp == kCcTmaWarp) {
         // ------------------------------------------------------------ producer
         if (elect_one()) {
-            prefetch_tensormap(&tm_codes);
-            prefetch_tensormap(&tm_scales);
-            prefetch_tensormap(&tm_mins);
-            if (BITS == 5) prefetch_tensormap(&tm_hi);
+            for (int gg = 0; gg < NGU; ++gg) {
+                prefetch_tensormap(&maps.m[gg][0]);
+                prefetch_tensormap(&maps.m[gg][1]);
+                prefetch_tensormap(&maps.m[gg][2]);
+                if ((gg ? BITS_U : BITS) == 5) prefetch_tensormap(&maps.m[gg][3]);
+            }
         }
         __syncwarp();
         int slot = 0, lap = 0, issued = 0;
@@ -392,12 +415,18 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
                     for (int pp = 0; pp < a.P; ++pp) {
                         const int kc = c * a.P + pp;
                         if (kc >= a.C) continue;
-                        tma_load_2d(sb + pp * a.R8 * 128, &tm_codes, kc * (kChunkK / 2), row, &full[slot]);
-                        tma_load_2d(sb + a.scales_off + pp * a.R8 * 16, &tm_scales, kc * (kChunkK / 32), row,
-                                    &full[slot]);
-                        tma_load_2d(sb + a.mins_off + pp * a.R8 * 16, &tm_mins, kc * (kChunkK / 32), row, &full[slot]);
-                        if (BITS == 5)
-                            tma_load_2d(sb + a.hi_off + pp * a.R8 * 32, &tm_hi, kc * (kChunkK / 8), row, &full[slot]);
+#pragma unroll
+                        for (int gg = 0; gg < NGU; ++gg) {
+                            const uint32_t bx = static_cast<uint32_t>(pp * NGU + gg) * a.R8;
+                            tma_load_2d(sb + bx * 128, &maps.m[gg][0], kc * (kChunkK / 2), row, &full[slot]);
+                            tma_load_2d(sb + a.scales_off + bx * 16, &maps.m[gg][1], kc * (kChunkK / 32), row,
+                                        &full[slot]);
+                            tma_load_2d(sb + a.mins_off + bx * 16, &maps.m[gg][2], kc * (kChunkK / 32), row,
+                                        &full[slot]);
+                            if ((gg ? BITS_U : BITS) == 5)
+                                tma_load_2d(sb + a.hi_off + bx * 32, &maps.m[gg][3], kc * (kChunkK / 8), row,
+                                            &full[slot]);
+                        }
                     }
                 }
                 __syncwarp();
@@ -418,15 +447,15 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
     // ---------------------------------------------------------------- compute warps
     {
         const uint32_t roff[4] = {0u, a.scales_off, a.mins_off, a.hi_off}, rbytes[4] = {128u, 16u, 16u, 32u};
-        cc_zero_padding(a, smem, a.P, roff, rbytes, BITS == 5 ? 4 : 3);
+        cc_zero_padding(a, smem, a.P * NGU, roff, rbytes, (BITS == 5 || BITS_U == 5) ? 4 : 3);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     cc_convert_q45<NSEG>(a, smem, warp, lane, any_bf);
     named_barrier_sync(1, kCcThreads);
     if (*any_bf)
-        cc_q45_units<BITS, EPI, NSEG, true>(a, smem, full, empty, abort_flag);
+        cc_q45_units<BITS, EPI, NSEG, true, BITS_U>(a, smem, full, empty, abort_flag);
     else
-        cc_q45_units<BITS, EPI, NSEG, false>(a, smem, full, empty, abort_flag);
+        cc_q45_units<BITS, EPI, NSEG, false, BITS_U>(a, smem, full, empty, abort_flag);
 }
 
 
@@ -507,21 +536,25 @@ qg_status cc_dispatch(const CcArgs& a, const CUtensorMap& tmc, const CUtensorMap
     return cc_launch<EPI, 16>(a, tmc, tms, grid, stream);
 }
 
-template <int BITS, int EPI, int NSEG>
-qg_status cc_q45_launch(CcArgs a, const CUtensorMap (&maps)[4], int grid, cudaStream_t stream)
+template <int BITS, int EPI, int NSEG, int BITS_U>
+qg_status cc_q45_launch(CcArgs a, const Q45Maps& maps, int grid, cudaStream_t stream)
 {
+    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
+    constexpr bool any5 = BITS == 5 || BITS_U == 5;
     a.status = device_status_ptr();
     if (!a.status) return QG_ERR_CUDA;
     const DebugState dbg = debug_state();
     a.wait_ns = dbg.wait_ns;
     a.starve = dbg.starve;
 
-    const uint32_t nbox = static_cast<uint32_t>(a.P);
+    const uint32_t nbox = static_cast<uint32_t>(a.P * NGU);
     a.scales_off = nbox * a.R8 * 128u;
     a.mins_off = a.scales_off + nbox * a.R8 * 16u;
     a.hi_off = a.mins_off + nbox * a.R8 * 16u;
-    a.stage_bytes = align_up(a.hi_off + (BITS == 5 ? nbox * a.R8 * 32u : 0u), 1024);
+    a.stage_bytes = align_up(a.hi_off + (any5 ? nbox * a.R8 * 32u : 0u), 1024);
+    // bytes one phase brings in (its gate box and, for SwiGLU, its up box)
     a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (BITS == 5 ? 32u : 0u));
+    if (NGU == 2) a.box_tx += static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (BITS_U == 5 ? 32u : 0u));
     const uint32_t x_bytes = static_cast<uint32_t>(a.C) * kChunkK * 2u;
     const uint32_t pe_bytes = align_up(static_cast<uint32_t>(a.C) * 4u, 16);
     const uint32_t gx_bytes = align_up(static_cast<uint32_t>(a.C * NSEG) * 4u, 16);
@@ -552,7 +585,7 @@ qg_status cc_q45_launch(CcArgs a, const CUtensorMap (&maps)[4], int grid, cudaSt
     so += bar_bytes;
     if (so > kCcSmemMax) return QG_ERR_UNSUPPORTED;
 
-    auto kern = cc_q45_kernel<BITS, EPI, NSEG>;
+    auto kern = cc_q45_kernel<BITS, EPI, NSEG, BITS_U>;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
@@ -571,16 +604,17 @@ qg_status cc_q45_launch(CcArgs a, const CUtensorMap (&maps)[4], int grid, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, a, maps[0], maps[1], maps[2], maps[3]) != cudaSuccess) return QG_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, a, maps) != cudaSuccess) return QG_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
-template <int BITS, int EPI>
-qg_status cc_q45_dispatch(const CcArgs& a, const CUtensorMap (&maps)[4], int grid, cudaStream_t stream)
+template <int BITS, int EPI, int BITS_U = BITS>
+qg_status cc_q45_dispatch(const CcArgs& a, const Q45Maps& maps, int grid, cudaStream_t stream)
 {
-    const int items8 = a.P * ((a.R + kCcRows - 1) / kCcRows) * 8;
-    if (items8 > kCcThreads / 2) return cc_q45_launch<BITS, EPI, 8>(a, maps, grid, stream);
-    return cc_q45_launch<BITS, EPI, 16>(a, maps, grid, stream);
+    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
+    const int items8 = a.P * NGU * ((a.R + kCcRows - 1) / kCcRows) * 8;
+    if (items8 > kCcThreads / 2) return cc_q45_launch<BITS, EPI, 8, BITS_U>(a, maps, grid, stream);
+    return cc_q45_launch<BITS, EPI, 16, BITS_U>(a, maps, grid, stream);
 }
 
 }  // namespace
@@ -589,7 +623,7 @@ qg_status cc_q45_dispatch(const CcArgs& a, const CUtensorMap (&maps)[4], int gri
 // for K not a multiple of 256 or when x does not fit in shared memory.
 qg_status launch_cc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
                                 int out_f32, const void* residual, int M, int N, int K, int swiglu,
-                                cudaStream_t stream)
+                                cudaStream_t stream, const void* norm_w, float norm_eps)
 {
     if (M != 1 || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
     const int ngu = swiglu ? 2 : 1;
@@ -609,6 +643,8 @@ qg_status launch_cc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, flo
     a.x = static_cast<const uint16_t*>(x);
     a.y = y;
     a.residual = static_cast<const uint16_t*>(residual);
+    a.norm_w = static_cast<const uint16_t*>(norm_w);
+    a.norm_eps = norm_eps;
     a.K = K;
     a.C = K / kChunkK;
     a.n_out = n_out;
@@ -632,55 +668,92 @@ qg_status launch_cc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, flo
     return cc_dispatch<EPI_NONE>(a, tmc, tms, grid, stream);
 }
 
-}  // namespace qg
+namespace {
 
-namespace qg {
-
-// One-token Q4/Q5 GEMV on the CUDA cores; QG_ERR_UNSUPPORTED for other M,
-// for K not a multiple of 256 or when x does not fit in shared memory.
-qg_status launch_cc_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min, int bits,
-                              const void* x, void* y, int out_f32, const void* residual, int M, int N, int K,
-                              cudaStream_t stream)
+// The groupwise-int plan for one token: units of R rows (per matrix) over all
+// of K, P phases so that P * ngu boxes of R8 rows fill at most 256 rows.
+CcArgs q45_plan(const void* x, void* y, int out_f32, const void* residual, int n_out, int ngu, int K,
+                const void* norm_w, float norm_eps)
 {
-    if (M != 1 || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
     const int sms = sm_count(-1);
-    if (sms <= 0) return QG_ERR_CUDA;
     int R = 1;
     for (int U = 1;; ++U) {
-        R = (N + sms * U - 1) / (sms * U);
-        if ((R + 7) / 8 * 8 <= 256) break;
+        R = (n_out + sms * U - 1) / (sms * U);
+        if (ngu * ((R + 7) / 8 * 8) <= 256) break;
     }
     R = std::max(R, 1);
     CcArgs a{};
     a.x = static_cast<const uint16_t*>(x);
     a.y = y;
     a.residual = static_cast<const uint16_t*>(residual);
+    a.norm_w = static_cast<const uint16_t*>(norm_w);
+    a.norm_eps = norm_eps;
     a.K = K;
     a.C = K / kChunkK;
-    a.n_out = N;
+    a.n_out = n_out;
     a.R = R;
     a.R8 = (R + 7) / 8 * 8;
-    a.P = std::max(1, std::min(256 / a.R8, a.C));
+    a.P = std::max(1, std::min(256 / (ngu * a.R8), a.C));
     a.Cp = (a.C + a.P - 1) / a.P;
     a.out_f32 = out_f32;
     a.g = 1.f;
-    a.n_units = (N + R - 1) / R;
-    const int grid = std::min(sms, a.n_units);
-    CUtensorMap maps[4];
-    memset(maps, 0, sizeof(maps));
-    if (!encode_tmap_2d(&maps[0], q_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, R, true) ||
-        !encode_tmap_2d(&maps[1], scale, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, N, 8, R, false) ||
-        !encode_tmap_2d(&maps[2], min, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, N, 8, R, false))
-        return QG_ERR_CUDA;
+    a.n_units = (n_out + R - 1) / R;
+    return a;
+}
+
+bool q45_maps(CUtensorMap (&m)[4], const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min,
+              int bits, int N, int K, int R)
+{
+    memset(m, 0, sizeof(m));
+    if (!encode_tmap_2d(&m[0], q_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, R, true) ||
+        !encode_tmap_2d(&m[1], scale, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, N, 8, R, false) ||
+        !encode_tmap_2d(&m[2], min, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, N, 8, R, false))
+        return false;
+    if (bits == 5) return encode_tmap_2d(&m[3], q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 8, N, 32, R, false);
+    m[3] = m[2];
+    return true;
+}
+
+}  // namespace
+
+// One-token Q4/Q5 GEMV on the CUDA cores; QG_ERR_UNSUPPORTED for other M,
+// for K not a multiple of 256 or when x does not fit in shared memory.
+qg_status launch_cc_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min, int bits,
+                              const void* x, void* y, int out_f32, const void* residual, int M, int N, int K,
+                              cudaStream_t stream, const void* norm_w, float norm_eps)
+{
+    if (M != 1 || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
+    if (sm_count(-1) <= 0) return QG_ERR_CUDA;
+    const CcArgs a = q45_plan(x, y, out_f32, residual, N, 1, K, norm_w, norm_eps);
+    const int grid = std::min(sm_count(-1), a.n_units);
+    Q45Maps maps;
+    if (!q45_maps(maps.m[0], q_lo, q_hi, scale, min, bits, N, K, a.R)) return QG_ERR_CUDA;
+    maps.m[1][0] = maps.m[1][1] = maps.m[1][2] = maps.m[1][3] = maps.m[0][0];
     if (bits == 5) {
-        if (!encode_tmap_2d(&maps[3], q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 8, N, 32, R, false))
-            return QG_ERR_CUDA;
         if (residual) return cc_q45_dispatch<5, EPI_RESID>(a, maps, grid, stream);
         return cc_q45_dispatch<5, EPI_NONE>(a, maps, grid, stream);
     }
-    maps[3] = maps[2];
     if (residual) return cc_q45_dispatch<4, EPI_RESID>(a, maps, grid, stream);
     return cc_q45_dispatch<4, EPI_NONE>(a, maps, grid, stream);
+}
+
+// One-token SwiGLU over separate groupwise-int gate and up matrices (I rows
+// each, gate_bits / up_bits wide), y bf16 [I]; QG_ERR_UNSUPPORTED as above.
+qg_status launch_cc_swiglu_q45(const Q45Matrix& gate, const Q45Matrix& up, const void* x, void* y, int M, int I,
+                               int K, cudaStream_t stream, const void* norm_w, float norm_eps)
+{
+    if (M != 1 || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
+    if (sm_count(-1) <= 0) return QG_ERR_CUDA;
+    const CcArgs a = q45_plan(x, y, 0, nullptr, I, 2, K, norm_w, norm_eps);
+    const int grid = std::min(sm_count(-1), a.n_units);
+    Q45Maps maps;
+    if (!q45_maps(maps.m[0], gate.q_lo, gate.q_hi, gate.scale, gate.min, gate.bits, I, K, a.R) ||
+        !q45_maps(maps.m[1], up.q_lo, up.q_hi, up.scale, up.min, up.bits, I, K, a.R))
+        return QG_ERR_CUDA;
+    if (gate.bits == 5 && up.bits == 4) return cc_q45_dispatch<5, EPI_SWIGLU, 4>(a, maps, grid, stream);
+    if (gate.bits == 5 && up.bits == 5) return cc_q45_dispatch<5, EPI_SWIGLU, 5>(a, maps, grid, stream);
+    if (gate.bits == 4 && up.bits == 5) return cc_q45_dispatch<4, EPI_SWIGLU, 5>(a, maps, grid, stream);
+    return cc_q45_dispatch<4, EPI_SWIGLU, 4>(a, maps, grid, stream);
 }
 
 }  // namespace qg

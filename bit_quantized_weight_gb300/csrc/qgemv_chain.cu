@@ -487,7 +487,7 @@ qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, 
     int c_max = 0, red_max = 0;
     for (int o = 0; o < n_ops; ++o) {
         const qg_gemv_op& g = ops[o];
-        if (g.K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
+        if (g.K % kChunkK != 0 || g.up_codes != nullptr) return QG_ERR_UNSUPPORTED;
         ChainOp& op = p.op[o];
         op.fmt = g.format == QG_FMT_NVFP4 ? FMT_NVFP4 : g.format == QG_FMT_Q5 ? FMT_Q5 : FMT_Q4;
         op.epi = g.epilogue == QG_EPI_SWIGLU ? EPI_SWIGLU : g.epilogue == QG_EPI_RESIDUAL ? EPI_RESID : EPI_NONE;
@@ -500,6 +500,8 @@ qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, 
         a.x = static_cast<const uint16_t*>(g.x);
         a.y = g.y;
         a.residual = static_cast<const uint16_t*>(g.residual);
+        a.norm_w = static_cast<const uint16_t*>(g.norm_weight);
+        a.norm_eps = g.norm_eps;
         a.up_row_offset = op.epi == EPI_SWIGLU ? n_out : 0;
         a.out_f32 = op.epi == EPI_SWIGLU ? 0 : (g.y_dtype == QG_OUT_F32 ? 1 : 0);
         a.g = op.fmt == FMT_NVFP4 ? g.global_scale : 1.f;

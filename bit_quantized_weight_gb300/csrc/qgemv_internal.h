@@ -83,6 +83,33 @@ struct DenseArgs {
     int* status;               // device status word
 };
 
+// The exact warp-per-row kernel (qgemv_simple.cu): any K, any M, every
+// epilogue, the RMSNorm prologue and SwiGLU with a separate up matrix.
+struct SimpleArgs {
+    int fmt;                   // FMT_NVFP4, FMT_Q4, FMT_Q5 (the gate matrix for SwiGLU)
+    const uint8_t* codes;
+    const uint8_t* q_hi;
+    const void* scales;
+    const void* mins;
+    float g;
+    int ufmt;                  // SwiGLU up matrix when ucodes != nullptr, else the up rows
+    const uint8_t* ucodes;     // follow the gate rows in the same matrix
+    const uint8_t* uq_hi;
+    const void* uscales;
+    const void* umins;
+    float ug;
+    const uint16_t* x;
+    void* y;
+    int out_f32;
+    const uint16_t* residual;
+    const uint16_t* norm_w;    // RMSNorm gamma (bf16 [K]) or nullptr
+    float norm_eps;
+    int M;
+    int n_out;
+    int K;
+    int swiglu;
+};
+
 // Host-side helpers implemented in api.cu.
 struct DebugState {
     uint64_t wait_ns;
@@ -98,19 +125,32 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtyp
 qg_status launch_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
                              int out_f32, const void* residual, int M, int N, int K, int swiglu,
                              cudaStream_t stream);
-// One-token NVFP4 GEMV on the CUDA cores (qgemv_cc.cu): QG_ERR_UNSUPPORTED
-// for M != 1 or when a shape does not fit its shared-memory plan.
+// One groupwise-int matrix: q_lo u8[rows][K/2], q_hi (Q5) u8[rows][K/8],
+// fp16 scale and min [rows][K/32].
+struct Q45Matrix {
+    const uint8_t* q_lo;
+    const uint8_t* q_hi;
+    const void* scale;
+    const void* min;
+    int bits;
+};
+
+// One-token kernels on the CUDA cores (qgemv_cc.cu): QG_ERR_UNSUPPORTED for
+// M != 1 or when a shape does not fit their shared-memory plan. norm_w: the
+// RMSNorm prologue's gamma (bf16 [K]) or nullptr.
 qg_status launch_cc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
                                 int out_f32, const void* residual, int M, int N, int K, int swiglu,
-                                cudaStream_t stream);
+                                cudaStream_t stream, const void* norm_w = nullptr, float norm_eps = 0.f);
 qg_status launch_cc_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min, int bits,
                               const void* x, void* y, int out_f32, const void* residual, int M, int N, int K,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const void* norm_w = nullptr, float norm_eps = 0.f);
+qg_status launch_cc_swiglu_q45(const Q45Matrix& gate, const Q45Matrix& up, const void* x, void* y, int M, int I,
+                               int K, cudaStream_t stream, const void* norm_w, float norm_eps);
 // tcgen05 kernels (NVFP4): QG_ERR_UNSUPPORTED when a shape does not fit their
 // shared-memory plan; the callers then use the mma.sync kernels above.
 qg_status launch_tc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
                                 int out_f32, const void* residual, int M, int N, int K, int swiglu,
-                                cudaStream_t stream);
+                                cudaStream_t stream, const void* norm_w = nullptr, float norm_eps = 0.f);
 qg_status launch_tc_grouped_nvfp4(const uint8_t* codes, const uint8_t* scales, int total_rows, int K, int swiglu,
                                   int up_offset, const void* x, int max_cols, void* y, int out_pitch, int out_f32,
                                   const GroupDesc* groups, const UnitDesc* units, const int* n_units,
@@ -125,6 +165,7 @@ qg_status launch_grouped_nvfp4(const uint8_t* codes, const uint8_t* scales, int 
 qg_status launch_simple(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
                         const void* mins, float g, const void* x, void* y, int out_f32,
                         const void* residual, int M, int N, int K, int swiglu, cudaStream_t stream);
+qg_status launch_simple_args(const SimpleArgs& a, cudaStream_t stream);
 qg_status launch_read_probe(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t stream);
 qg_status launch_dequant(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
                          const void* mins, float g, float* w, int N, int K, cudaStream_t stream);

@@ -45,28 +45,52 @@ __device__ __forceinline__ float weight_at(int fmt, const uint8_t* codes, const 
     return fmaf(s, static_cast<float>(q), m);
 }
 
-__global__ void simple_kernel(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
-                              const void* mins, float g, const uint16_t* x, void* y, int out_f32,
-                              const uint16_t* residual, int M, int n_out, int K, int swiglu)
+// One warp per output row (gate/up row pair for SwiGLU). With the RMSNorm
+// prologue, the CTA's first warps first derive each token's factor in the
+// shared fixed order (chunks of 256 values, 8 per lane, then k order) and
+// every k reads h = bf16((x * r) * gamma) instead of x.
+__global__ void simple_kernel(const SimpleArgs a)
 {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    __shared__ float s_r[kMaxTokens];
+    const int M = a.M, K = a.K, n_out = a.n_out;
     const int lane = threadIdx.x & 31;
+    if (a.norm_w != nullptr) {
+        const int w = threadIdx.x >> 5;
+        if (w < M) {
+            const uint16_t* xr = a.x + static_cast<size_t>(w) * K;
+            float t = 0.f;
+            for (int k0 = 0; k0 < K; k0 += kChunkK) {
+                const int k = k0 + lane * 8;
+                const uint4 raw = k < K ? ldg_nc_128(xr + k) : make_uint4(0, 0, 0, 0);
+                t += rms_chunk_ss(raw);
+            }
+            if (lane == 0) s_r[w] = rms_factor(t, K, a.norm_eps);
+        }
+        __syncthreads();
+    }
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (warp >= n_out) return;
     const int n = warp;
+    const bool sep_up = a.ucodes != nullptr;
     float acc[2][kMaxTokens];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int m = 0; m < kMaxTokens; ++m) acc[j][m] = 0.f;
     for (int k = lane; k < K; k += 32) {
-        const float w0 = weight_at(fmt, codes, q_hi, scales, mins, K, n, k);
-        const float w1 = swiglu ? weight_at(fmt, codes, q_hi, scales, mins, K, n + n_out, k) : 0.f;
+        const float w0 = weight_at(a.fmt, a.codes, a.q_hi, a.scales, a.mins, K, n, k);
+        float w1 = 0.f;
+        if (a.swiglu)
+            w1 = sep_up ? weight_at(a.ufmt, a.ucodes, a.uq_hi, a.uscales, a.umins, K, n, k)
+                        : weight_at(a.fmt, a.codes, a.q_hi, a.scales, a.mins, K, n + n_out, k);
+        const float gk = a.norm_w != nullptr ? bf16_bits_to_f32(a.norm_w[k]) : 0.f;
 #pragma unroll
         for (int m = 0; m < kMaxTokens; ++m) {
             if (m < M) {
-                const float xv = bf16_bits_to_f32(x[static_cast<size_t>(m) * K + k]);
+                float xv = bf16_bits_to_f32(a.x[static_cast<size_t>(m) * K + k]);
+                if (a.norm_w != nullptr) xv = __bfloat162float(__float2bfloat16_rn((xv * s_r[m]) * gk));
                 acc[0][m] = fmaf(w0, xv, acc[0][m]);
-                if (swiglu) acc[1][m] = fmaf(w1, xv, acc[1][m]);
+                if (a.swiglu) acc[1][m] = fmaf(w1, xv, acc[1][m]);
             }
         }
     }
@@ -78,16 +102,16 @@ __global__ void simple_kernel(int fmt, const uint8_t* codes, const uint8_t* q_hi
             for (int o = 16; o > 0; o >>= 1) acc[j][m] += __shfl_xor_sync(0xffffffffu, acc[j][m], o);
     if (lane != 0) return;
     for (int m = 0; m < M; ++m) {
-        float v = acc[0][m] * g;
-        if (swiglu) {
-            const float u = acc[1][m] * g;
+        float v = acc[0][m] * a.g;
+        if (a.swiglu) {
+            const float u = acc[1][m] * (sep_up ? a.ug : a.g);
             v = (v / (1.0f + expf(-v))) * u;
         }
-        if (residual) v += bf16_bits_to_f32(residual[static_cast<size_t>(m) * n_out + n]);
-        if (out_f32)
-            static_cast<float*>(y)[static_cast<size_t>(m) * n_out + n] = v;
+        if (a.residual) v += bf16_bits_to_f32(a.residual[static_cast<size_t>(m) * n_out + n]);
+        if (a.out_f32)
+            static_cast<float*>(a.y)[static_cast<size_t>(m) * n_out + n] = v;
         else
-            static_cast<uint16_t*>(y)[static_cast<size_t>(m) * n_out + n] = f32_to_bf16_bits_rn(v);
+            static_cast<uint16_t*>(a.y)[static_cast<size_t>(m) * n_out + n] = f32_to_bf16_bits_rn(v);
     }
 }
 
@@ -129,17 +153,34 @@ __global__ void dequant_kernel(int fmt, const uint8_t* codes, const uint8_t* q_h
 
 }  // namespace
 
+qg_status launch_simple_args(const SimpleArgs& a, cudaStream_t stream)
+{
+    const int threads = 256;  // 8 warps: one per token for the RMSNorm factors
+    const long long blocks = (static_cast<long long>(a.n_out) * 32 + threads - 1) / threads;
+    simple_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
+    return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
 qg_status launch_simple(int fmt, const uint8_t* codes, const uint8_t* q_hi, const void* scales,
                         const void* mins, float g, const void* x, void* y, int out_f32,
                         const void* residual, int M, int N, int K, int swiglu, cudaStream_t stream)
 {
-    const int n_out = swiglu ? N / 2 : N;
-    const int threads = 256;
-    const long long blocks = (static_cast<long long>(n_out) * 32 + threads - 1) / threads;
-    simple_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        fmt, codes, q_hi, scales, mins, g, static_cast<const uint16_t*>(x), y, out_f32,
-        static_cast<const uint16_t*>(residual), M, n_out, K, swiglu);
-    return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+    SimpleArgs a{};
+    a.fmt = fmt;
+    a.codes = codes;
+    a.q_hi = q_hi;
+    a.scales = scales;
+    a.mins = mins;
+    a.g = g;
+    a.x = static_cast<const uint16_t*>(x);
+    a.y = y;
+    a.out_f32 = out_f32;
+    a.residual = static_cast<const uint16_t*>(residual);
+    a.M = M;
+    a.n_out = swiglu ? N / 2 : N;
+    a.K = K;
+    a.swiglu = swiglu;
+    return launch_simple_args(a, stream);
 }
 
 // Streaming-read probe: every thread keeps kProbeUnroll 128-bit loads in

@@ -118,6 +118,11 @@ struct TcArgs {
     uint32_t smem_pe;          // 2^-exponent per (stage, phase, token), fp32, PES per stage
     uint32_t smem_red;
     uint32_t smem_bar;
+    // RMSNorm prologue (dense launches; norm_w == nullptr: none): the MMA
+    // reads h = bf16(x * r_m * gamma) with r_m = 1 / sqrt(mean(x_m^2) + eps)
+    const uint16_t* norm_w;
+    float norm_eps;
+    uint32_t smem_rms;         // M * C chunk sums of squares, then r_m [8]
     uint64_t wait_ns;
     int starve;
     int* status;
@@ -257,10 +262,32 @@ __device__ __forceinline__ uint32_t z_off_one(int cr, int lane8, int p)
 //     and the factor 2^-e.
 // If any chunk was flagged, a second pass rewrites every chunk of the stages
 // that hold one as raw bf16 with factor 1 and marks those stages bf16.
-template <int MT>
+// The RMSNorm factors r_m of the M tokens (dense launches), by the decode
+// warps: every (token, chunk) sum of squares in the order all kernels share
+// (8 values per lane, a warp butterfly), then each token's chunks in k order.
+__device__ void tc_norm_factors(const TcArgs& a, uint8_t* smem, int warp, int lane)
+{
+    float* part = reinterpret_cast<float*>(smem + a.smem_rms);
+    float* r = part + a.M * a.C;
+    for (int it = warp; it < a.M * a.C; it += kTcDecodeWarps) {
+        const int m = it / a.C, kc = it % a.C;
+        const float ss = rms_chunk_ss(ldg_nc_128(a.x + static_cast<size_t>(m) * a.K + kc * kChunkK + lane * 8));
+        if (lane == 0) part[it] = ss;
+    }
+    named_barrier_sync(1, kTcDecodeThreads);
+    if (threadIdx.x < static_cast<unsigned>(a.M)) {
+        float t = 0.f;
+        for (int kc = 0; kc < a.C; ++kc) t += part[threadIdx.x * a.C + kc];
+        r[threadIdx.x] = rms_factor(t, a.K, a.norm_eps);
+    }
+    named_barrier_sync(1, kTcDecodeThreads);
+}
+
+template <int MT, bool NORM>
 __device__ void tc_convert(const TcArgs& a, uint8_t* smem, int c0, int nst, int ntok, const int* xrow, int warp,
                            int lane)
 {
+    const float* rnorm = reinterpret_cast<const float*>(smem + a.smem_rms) + a.M * a.C;
     constexpr bool DEF = (MT == 1);
     constexpr int kBatch = 4;  // chunks whose loads are in flight together, per warp
     int* any_flag = reinterpret_cast<int*>(smem + a.smem_ex);
@@ -287,6 +314,9 @@ __device__ void tc_convert(const TcArgs& a, uint8_t* smem, int c0, int nst, int 
             if (m < ntok && kc < a.C) {
                 const int xr = xrow ? xrow[m] : m;
                 raw = ldg_nc_128(a.x + static_cast<size_t>(xr) * a.K + static_cast<size_t>(kc) * kChunkK + lane * 8);
+                if (NORM)
+                    raw = rms_apply8(raw, ldg_nc_128(a.norm_w + static_cast<size_t>(kc) * kChunkK + lane * 8),
+                                     rnorm[m]);
             }
         }
         return raw;
@@ -327,6 +357,11 @@ __device__ void tc_convert(const TcArgs& a, uint8_t* smem, int c0, int nst, int 
             uint4 raw[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) raw[i] = src ? ldg_nc_128(xs + (kq + 4 * i) * 8) : make_uint4(0, 0, 0, 0);
+            if (NORM && src) {
+                const uint16_t* gw = a.norm_w + static_cast<size_t>(kc) * kChunkK;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) raw[i] = rms_apply8(raw[i], ldg_nc_128(gw + (kq + 4 * i) * 8), rnorm[m]);
+            }
             uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -488,7 +523,8 @@ __device__ __forceinline__ float tc_pick(const uint32_t* v, int p, int m)
 }
 
 // NPC: one-token phase columns the fold accumulates (1, 2 or 4 >= P).
-template <int MT, int EPI, int NPC>
+// NORM: the RMSNorm prologue (dense launches).
+template <int MT, int EPI, int NPC, bool NORM>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemv_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales)
@@ -681,6 +717,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int dset = warp >> 2;
         // Activations may come from the previous kernel.
         asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (NORM) tc_norm_factors(a, smem, warp, lane);
         bool aborted = false;
         int slot = 0, lap = 0, gi = 0;
         int conv_key = -1, conv_c0 = -1;
@@ -709,7 +746,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 break;
                             }
                     named_barrier_sync(1, kTcDecodeThreads);
-                    tc_convert<MT>(a, smem, c, min(a.SC, a.Cp - c), ntok, xrow, warp, lane);
+                    tc_convert<MT, NORM>(a, smem, c, min(a.SC, a.Cp - c), ntok, xrow, warp, lane);
                     conv_c0 = c;
                     conv_key = xkey;
                 }
@@ -909,7 +946,7 @@ ZPlan z_plan(int sc, int P, int MT, int N, int PES)
 
 // Completes the launch-time fields of `a` (status word, debug limits, stage
 // and shared-memory plan) and launches with programmatic dependent launch.
-template <int MT, int EPI, int NPC>
+template <int MT, int EPI, int NPC, bool NORM = false>
 qg_status tc_launch(TcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, int grid, cudaStream_t stream)
 {
     using Cfg = TcCfg<MT, EPI>;
@@ -928,7 +965,8 @@ qg_status tc_launch(TcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
     a.PES = Cfg::DEF ? 4 : a.P * MT;
 
     const uint32_t red_bytes = align_up(nbox * a.R * MT * 4u, 128);
-    const uint32_t bar_bytes = (2 * kTcMaxStages + 3 * kTcMaxBufs) * 8 + 16;
+    const uint32_t rms_bytes = a.norm_w ? align_up(static_cast<uint32_t>(a.M * a.C + 8) * 4u, 16) : 0u;
+    const uint32_t bar_bytes = (2 * kTcMaxStages + 3 * kTcMaxBufs) * 8 + 16 + rms_bytes;
     // Keep at least ~96 KB (or 4 stages) of weights in flight; the
     // activations get the rest, as few super-chunks as possible.
     const uint32_t ring_min = std::max<uint32_t>(96u * 1024u, 4u * a.stage_bytes);
@@ -965,11 +1003,12 @@ qg_status tc_launch(TcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
     a.smem_red = so;
     so += red_bytes;
     a.smem_bar = so;
+    a.smem_rms = so + bar_bytes - rms_bytes;
     so += bar_bytes;
     so = std::max(so, kTcSmemMin);
     if (so > kTcSmemMax) return QG_ERR_UNSUPPORTED;
 
-    auto kern = tc_gemv_kernel<MT, EPI, NPC>;
+    auto kern = tc_gemv_kernel<MT, EPI, NPC, NORM>;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
@@ -996,6 +1035,13 @@ template <int EPI>
 qg_status tc_dispatch_mt(const TcArgs& a, const CUtensorMap& tmc, const CUtensorMap& tms, int grid,
                          cudaStream_t stream)
 {
+    if (a.norm_w != nullptr) {
+        // one token with the prologue runs on the CUDA-core kernel
+        if (a.M <= 1) return QG_ERR_UNSUPPORTED;
+        if (a.M <= 2) return tc_launch<2, EPI, 4, true>(a, tmc, tms, grid, stream);
+        if (a.M <= 4) return tc_launch<4, EPI, 4, true>(a, tmc, tms, grid, stream);
+        return tc_launch<8, EPI, 4, true>(a, tmc, tms, grid, stream);
+    }
     if (a.M <= 1) {
         if (a.P <= 1) return tc_launch<1, EPI, 1>(a, tmc, tms, grid, stream);
         if (a.P <= 2) return tc_launch<1, EPI, 2>(a, tmc, tms, grid, stream);
@@ -1029,7 +1075,7 @@ bool tc_maps(CUtensorMap* tmc, CUtensorMap* tms, const uint8_t* codes, const uin
 
 qg_status launch_tc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
                                 int out_f32, const void* residual, int M, int N, int K, int swiglu,
-                                cudaStream_t stream)
+                                cudaStream_t stream, const void* norm_w, float norm_eps)
 {
     const int ngu = swiglu ? 2 : 1;
     const int n_out = swiglu ? N / 2 : N;
@@ -1058,6 +1104,8 @@ qg_status launch_tc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, flo
     a.up_row_offset = swiglu ? n_out : 0;
     a.out_f32 = swiglu ? 0 : out_f32;
     a.g = g;
+    a.norm_w = static_cast<const uint16_t*>(norm_w);
+    a.norm_eps = norm_eps;
     a.n_units = (n_out + R - 1) / R;
     const int grid = std::min(sms, a.n_units);
     CUtensorMap tmc, tms;

@@ -40,7 +40,9 @@ class QgGemvOp(ctypes.Structure):
                 ("after_previous", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int),
                 ("codes", ctypes.c_void_p), ("q_hi", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("mins", ctypes.c_void_p), ("global_scale", ctypes.c_float), ("x", ctypes.c_void_p),
-                ("residual", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+                ("residual", ctypes.c_void_p), ("y", ctypes.c_void_p), ("norm_weight", ctypes.c_void_p),
+                ("norm_eps", ctypes.c_float), ("up_format", ctypes.c_int), ("up_codes", ctypes.c_void_p),
+                ("up_q_hi", ctypes.c_void_p), ("up_scales", ctypes.c_void_p), ("up_mins", ctypes.c_void_p)]
 
 
 class QGemvError(RuntimeError):
@@ -71,6 +73,7 @@ def lib():
                                       _I, _I, _I, _I, _I, _P]
         L.moe_qgemv_nvfp4_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]
         L.qgemv_chain.argtypes = [ctypes.POINTER(QgGemvOp), _I, _I, _P, _P]
+        L.qgemv_swiglu_q45.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _F, _P, _I, _I, _I, _P]
         L.qdequant_nvfp4.argtypes = [_P, _P, _F, _P, _I, _I, _P]
         L.qdequant_q45.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _P]
         L.qg_last_device_status.argtypes = [_P]
@@ -80,7 +83,7 @@ def lib():
         L.qg_debug_set_wait.argtypes = [ctypes.c_uint64, _I]
         for name in ("qgemv_nvfp4", "qgemv_q45", "qgemv_swiglu_nvfp4", "moe_route_topk",
                      "moe_qgemv_nvfp4_workspace_size", "moe_qgemv_nvfp4", "moe_qgemv_nvfp4_noalloc",
-                     "qgemv_chain", "qdequant_nvfp4",
+                     "qgemv_chain", "qgemv_swiglu_q45", "qdequant_nvfp4",
                      "qdequant_q45", "qg_last_device_status", "qg_debug_set_wait"):
             getattr(L, name).restype = _I
         _lib = L
@@ -211,6 +214,9 @@ class GemvChain:
     unchanged in place for as long as the chain is run."""
 
     def __init__(self, ops, sync=None):
+        """ops: dicts as above; optional "norm" (bf16 gamma [K] tensor) and
+        "norm_eps" select the RMSNorm prologue, and for groupwise-int SwiGLU
+        "up" is a dict with the up matrix's q_lo, q_hi, scale, min."""
         import torch
         n = len(ops)
         self.ops = (QgGemvOp * n)()
@@ -236,6 +242,16 @@ class GemvChain:
             rec.codes, rec.q_hi, rec.scales, rec.mins = _ptr(codes), _ptr(q_hi), _ptr(scales), _ptr(mins)
             rec.global_scale = float(g)
             rec.x, rec.residual, rec.y = _ptr(x), _ptr(r), _ptr(y)
+            nw = op.get("norm")
+            _cuda(nw)
+            rec.norm_weight = _ptr(nw)
+            rec.norm_eps = float(op.get("norm_eps", 1e-6))
+            up = op.get("up")
+            if up is not None:
+                _cuda(up["q_lo"], up.get("q_hi"), up["scale"], up["min"])
+                rec.up_format = QG_FMT_Q5 if up.get("q_hi") is not None else QG_FMT_Q4
+                rec.up_codes, rec.up_q_hi = _ptr(up["q_lo"]), _ptr(up.get("q_hi"))
+                rec.up_scales, rec.up_mins = _ptr(up["scale"]), _ptr(up["min"])
             self.keep.append(op)
             if M is None:
                 M = x.shape[0]
@@ -253,6 +269,23 @@ class GemvChain:
 def qgemv_chain(ops, sync=None, stream=None):
     """Run a list of projections as one qgemv_chain call (see GemvChain)."""
     GemvChain(ops, sync).run(stream)
+
+
+def qgemv_swiglu_q45(gate, up, x, y, norm=None, norm_eps=1e-6, stream=None):
+    """y[M][I] = bf16(silu(G h) * (U h)) over separate groupwise-int gate and
+    up matrices (dicts with q_lo, q_hi (Q5 only), scale, min); h = x, or the
+    RMSNorm of x with gamma `norm` (bf16 [K])."""
+    _cuda(gate["q_lo"], gate.get("q_hi"), gate["scale"], gate["min"], up["q_lo"], up.get("q_hi"), up["scale"],
+          up["min"], x, y, norm)
+    M, K = x.shape
+    I = gate["q_lo"].shape[0]
+    gb = 5 if gate.get("q_hi") is not None else 4
+    ub = 5 if up.get("q_hi") is not None else 4
+    _check("qgemv_swiglu_q45", lib().qgemv_swiglu_q45(
+        _ptr(gate["q_lo"]), _ptr(gate.get("q_hi")), _ptr(gate["scale"]), _ptr(gate["min"]), gb,
+        _ptr(up["q_lo"]), _ptr(up.get("q_hi")), _ptr(up["scale"]), _ptr(up["min"]), ub, _ptr(x), _ptr(norm),
+        float(norm_eps), _ptr(y), M, I, K, _stream(stream, y)))
+    return y
 
 
 def qdequant_nvfp4(codes, scales, g, w, stream=None):

@@ -192,8 +192,8 @@ typedef enum { QG_EPI_NONE = 0, QG_EPI_RESIDUAL = 1, QG_EPI_SWIGLU = 2 } qg_epil
  * qgemv_swiglu_nvfp4 or qgemv_q45 in one record (same layouts and rules).
  *   format          qg_format
  *   epilogue        QG_EPI_NONE, QG_EPI_RESIDUAL (residual != NULL) or
- *                   QG_EPI_SWIGLU (NVFP4 only: N = 2I rows, gate then up,
- *                   y bf16 [M][I])
+ *                   QG_EPI_SWIGLU (NVFP4: N = 2I rows, gate then up, y bf16
+ *                   [M][I]; groupwise-int: separate up matrix, see up_*)
  *   y_dtype         qg_out; QG_OUT_BF16 for QG_EPI_SWIGLU
  *   after_previous  nonzero if the op reads memory that an earlier op of the
  *                   same call writes (its x or residual is an earlier y); the
@@ -207,6 +207,19 @@ typedef enum { QG_EPI_NONE = 0, QG_EPI_RESIDUAL = 1, QG_EPI_SWIGLU = 2 } qg_epil
  *   mins            Q fp16 [N][K/32]; NULL for NVFP4
  *   global_scale    NVFP4 tensor scale g (ignored for Q)
  *   x, residual, y  as in the single-projection calls
+ *   norm_weight     RMSNorm prologue (NInfer article, section 2: the
+ *                   normalisation fused with the matmul, "one read, one
+ *                   write"): gamma, bf16 [K], or NULL for none. With it the
+ *                   projection reads, per token m, h = bf16_rne(x * r * gamma)
+ *                   with r = 1 / sqrt(sum_k x^2 / K + norm_eps), r computed in
+ *                   fp32 in one fixed order shared by every kernel.
+ *   norm_eps        the RMSNorm epsilon (ignored without norm_weight)
+ *   up_format       SwiGLU over separate groupwise-int gate and up matrices
+ *   up_codes ...    (NInfer article, section 2: gate in Q5, up in Q4): with
+ *                   QG_EPI_SWIGLU and a Q format, the record's own matrix holds
+ *                   the I gate rows (N = I), up_codes / up_q_hi / up_scales /
+ *                   up_mins the I up rows in up_format (QG_FMT_Q4 or Q5), and
+ *                   y is bf16 [M][I]. NULL / 0 otherwise.
  */
 typedef struct {
     int format;
@@ -223,6 +236,13 @@ typedef struct {
     const void* x;
     const void* residual;
     void* y;
+    const void* norm_weight;
+    float norm_eps;
+    int up_format;
+    const uint8_t* up_codes;
+    const uint8_t* up_q_hi;
+    const void* up_scales;
+    const void* up_mins;
 } qg_gemv_op;
 
 /*
@@ -234,18 +254,38 @@ typedef struct {
  *   ops     host array of n_ops records, 1 <= n_ops <= 8 (read during the call)
  *   M       tokens, 1..8, shared by every op
  *   sync    two caller-owned device words (uint32_t[2], 16-byte aligned), zero
- *           before their first use; the call leaves them zero again. Needed
+ *           before their first use; every call returns the first word to zero
+ *           (the second counts completed barriers), so they are reusable. Needed
  *           (else QG_ERR_INVALID_ARG) when some op after the first has
  *           after_previous set; may be NULL otherwise. Calls that overlap on
  *           the GPU must use different words, and after a call that reported
  *           QG_ERR_DEVICE_TIMEOUT the words must be zeroed again.
- * With one token and K a multiple of 256 for every op, the list runs as one
- * persistent kernel (one CTA per SM, launched cooperatively when an op waits
- * for earlier ones): the weight stream runs on across op boundaries. Other
- * lists run as one launch per op, in order, on `stream`.
+ * With one token, K a multiple of 256 for every op and no separate up
+ * matrix, the list runs as one persistent kernel (one CTA per SM, launched
+ * cooperatively when an op waits for earlier ones): the weight stream runs on
+ * across op boundaries. Other lists run as one launch per op, in order, on
+ * `stream`; a single record is thus also the way to call any projection with
+ * the RMSNorm prologue.
  * Every op is validated before anything is launched.
  */
 QG_API qg_status qgemv_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, cudaStream_t stream);
+
+/*
+ * SwiGLU over separate groupwise-int gate and up matrices, for the recipe
+ * that puts gate in Q5 and up in Q4 (NInfer article, section 2), with an
+ * optional fused RMSNorm prologue:
+ *   y[m][i] = bf16_rne( silu(gate_i . h_m) * (up_i . h_m) ),
+ *   h_m = x_m, or bf16(x_m * r_m * gamma) with norm_weight (see qg_gemv_op)
+ *   gate_lo u8[I][K/2], gate_hi u8[I][K/8] (gate_bits == 5, else NULL),
+ *   gate_scale, gate_min fp16 [I][K/32]; the same for up_*; bits in {4, 5}
+ *   x bf16 [M][K]; norm_weight bf16 [K] or NULL; y bf16 [M][I].
+ * Validation and errors as for qgemv_q45.
+ */
+QG_API qg_status qgemv_swiglu_q45(const uint8_t* gate_lo, const uint8_t* gate_hi, const void* gate_scale,
+                                  const void* gate_min, int gate_bits, const uint8_t* up_lo, const uint8_t* up_hi,
+                                  const void* up_scale, const void* up_min, int up_bits, const void* x,
+                                  const void* norm_weight, float norm_eps, void* y, int M, int I, int K,
+                                  cudaStream_t stream);
 
 /*
  * Dequantise to fp32 w[N][K] with the same device decode the GEMV kernels

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("qgemv_nvfp4", "qgemv_q45", "qgemv_swiglu_nvfp4", "moe_qgemv_nvfp4", "qgemv_chain",
+    for n in ("qgemv_nvfp4", "qgemv_q45", "qgemv_swiglu_nvfp4", "moe_qgemv_nvfp4", "qgemv_chain", "qgemv_swiglu_q45",
               "moe_qgemv_nvfp4_workspace_size", "moe_route_topk", "qdequant_nvfp4", "qdequant_q45",
               "qg_last_device_status", "qg_status_string"):
         assert n in names
@@ -171,6 +171,34 @@ def test_chain_validation(L):
     # a later op reading earlier outputs needs the sync words
     assert _chain(L, [_op(), _op(after_previous=1)]) == 1
     assert _chain(L, [_op(), _op(after_previous=1)], sync=A + 4) == 3
+    # RMSNorm weight alignment; separate up matrices only for groupwise-int SwiGLU
+    assert _chain(L, [_op(norm_weight=A + 2)]) == 3
+    q5 = dict(format=2, mins=A, q_hi=A)
+    assert _chain(L, [_op(up_codes=A, up_format=1, up_scales=A, up_mins=A)]) == 1        # no SwiGLU
+    assert _chain(L, [_op(epilogue=2, up_codes=A, up_format=1, up_scales=A, up_mins=A)]) == 1  # NVFP4
+    assert _chain(L, [_op(epilogue=2, **q5)]) == 1                                        # Q needs up
+    assert _chain(L, [_op(epilogue=2, up_codes=A, up_format=0, up_scales=A, up_mins=A, **q5)]) == 1
+    assert _chain(L, [_op(epilogue=2, up_codes=A, up_format=2, up_scales=A, up_mins=A, **q5)]) == 1  # Q5 up: plane
+    assert _chain(L, [_op(epilogue=2, up_codes=A, up_format=1, up_scales=A, up_mins=None, **q5)]) == 1
+    assert _chain(L, [_op(epilogue=2, up_codes=A + 4, up_format=1, up_scales=A, up_mins=A, **q5)]) == 3
+    assert _chain(L, [_op(up_scales=A)]) == 1                                             # stray up field
+
+
+@fake_ptr
+def test_swiglu_q45_validation(L):
+    args = dict(gate=(A, A, A, A, 5), up=(A, None, A, A, 4))
+    def call(gate=args["gate"], up=args["up"], x=A, nw=None, y=A, M=1, I=64, K=256):
+        return L.qgemv_swiglu_q45(*gate, *up, x, nw, 1e-6, y, M, I, K, None)
+    assert call(gate=(A, A, A, A, 3)) == 1
+    assert call(up=(A, None, A, A, 6)) == 1
+    assert call(gate=(A, None, A, A, 5)) == 1          # Q5 gate needs its plane
+    assert call(up=(A, A, A, A, 4)) == 1               # Q4 up takes none
+    assert call(M=0) == 1
+    assert call(M=9) == 1
+    assert call(K=48) == 1
+    assert call(x=A + 8) == 3
+    assert call(nw=A + 2) == 3
+    assert call(up=(A, None, A, A + 4, 4)) == 3
 
 
 def test_chain_record_layout_matches_the_header(tmp_path):
