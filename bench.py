@@ -59,7 +59,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["dense", "q45", "tiny", "moe"], default="dense")
+    ap.add_argument("--workload", choices=["dense", "q45", "q45ffn", "tiny", "moe"], default="dense")
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -167,6 +167,7 @@ class ClockSampler:
 # more tokens: the mma.sync kernel); a committed traffic figure is used only
 # while these files are unchanged.
 KERNEL_SOURCES = {
+    "simple": ("qgemv_simple.cu", "common.cuh", "qgemv_internal.h"),
     "cc": ("qgemv_cc.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
     "tc": ("qgemv_tc.cu", "tcgen05.cuh", "common.cuh", "qgemv_internal.h"),
     "mma": ("qgemv_dense.cu", "common.cuh", "qgemv_internal.h"),
@@ -178,6 +179,8 @@ KERNEL_SOURCES = {
 def kernel_family(workload, M):
     if workload == "moe":
         return "moe"
+    if workload == "q45ffn" and M > 1:
+        return "simple"
     if M == 1:
         return "cc"
     return "mma" if workload == "q45" else "tc"
@@ -226,6 +229,22 @@ class Workload:
         elif kind == "tiny":
             c = synth.TINY
             self.projs.append(("tiny", c.N, c.K, "none", synth.nvfp4_weights(0, "tiny.w", c.N, c.K)))
+        elif kind == "q45ffn":
+            # the recipe's layer with its FFN fused (Q5 gate + Q4 up, SwiGLU)
+            # and RMSNorm prologues ahead of QK, V and the FFN
+            W = {name: synth.q45_weights(3, f"q45.{name}", N, K, bits) for name, N, K, bits in synth.Q45_RECIPE}
+            sh = {name: (N, K) for name, N, K, bits in synth.Q45_RECIPE}
+            for name in ("qk", "v", "o"):
+                self.projs.append((name, *sh[name], "none", W[name]))
+            ffn = dict(W["gate"])
+            ffn["up"] = W["up"]
+            self.projs.append(("ffn", *sh["gate"], "swiglu", ffn))
+            self.projs.append(("down", *sh["down"], "residual", W["down"]))
+            H = synth.DENSE27B.hidden
+            r = np.random.default_rng(3)
+            gam = [np.round(r.uniform(0.5, 1.5, H) * 128.0) / 128.0 for _ in range(2)]
+            self.norms = [torch.from_numpy(g.astype(np.float32)).to(torch.bfloat16).to(dev) for g in gam]
+            self.norm_of = {"qk": 0, "v": 0, "ffn": 1}
         else:
             for name, N, K, bits in synth.Q45_RECIPE:
                 epi = "residual" if name == "down" else "none"
@@ -246,8 +265,8 @@ class Workload:
         self.host_in = host_in
         # -------- outputs packed in one buffer (one D2H copy per step)
         self.out_layout, off = {}, 0
-        for name, N, K, epi, _ in self.projs:
-            n_out = N // 2 if epi == "swiglu" else N
+        for name, N, K, epi, w in self.projs:
+            n_out = N // 2 if (epi == "swiglu" and "up" not in w) else N
             self.out_layout[name] = (off, (M, n_out))
             off += M * n_out
         self.out_elems = off
@@ -260,24 +279,31 @@ class Workload:
         self.copies = max(2, math.ceil(copies_min_bytes * self.l2_bytes / max(self.weight_bytes, 1)))
         self.chains = []
         self.dev_w = [[self._upload(w) for *_, w in self.projs]]
+
+        def clone(d):
+            return {k: (clone(v) if isinstance(v, dict) else v.clone() if hasattr(v, "clone") else v)
+                    for k, v in d.items()}
         for _ in range(self.copies - 1):
-            self.dev_w.append([{k: (v.clone() if hasattr(v, "clone") else v) for k, v in d.items()}
-                               for d in self.dev_w[0]])
+            self.dev_w.append([clone(d) for d in self.dev_w[0]])
 
     def _wbytes(self, w):
         if "codes" in w:
             return w["codes"].nbytes + w["scales"].nbytes
         b = w["q_lo"].nbytes + w["scale"].nbytes + w["min"].nbytes
-        return b + (w["q_hi"].nbytes if w.get("q_hi") is not None else 0)
+        b += w["q_hi"].nbytes if w.get("q_hi") is not None else 0
+        return b + (self._wbytes(w["up"]) if "up" in w else 0)
 
     def _upload(self, w):
         np, torch = self.np, self.torch
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
         if "codes" in w:
             return {"codes": t(w["codes"]), "scales": t(w["scales"]), "g": w["g"]}
-        return {"q_lo": t(w["q_lo"]), "q_hi": None if w.get("q_hi") is None else t(w["q_hi"]),
-                "scale": t(w["scale"].view(np.int16)).view(torch.float16),
-                "min": t(w["min"].view(np.int16)).view(torch.float16), "bits": w["bits"]}
+        d = {"q_lo": t(w["q_lo"]), "q_hi": None if w.get("q_hi") is None else t(w["q_hi"]),
+             "scale": t(w["scale"].view(np.int16)).view(torch.float16),
+             "min": t(w["min"].view(np.int16)).view(torch.float16), "bits": w["bits"]}
+        if "up" in w:
+            d["up"] = self._upload(w["up"])
+        return d
 
     def view_in(self, key):
         # views are made once: a caller holds its tensors, it does not re-slice
@@ -305,11 +331,16 @@ class Workload:
         y = self.view_out(name)
         x = self.view_in(f"x.{name}")
         r = self.view_in(f"r.{name}") if epi == "residual" else None
+        nw = self.norms[self.norm_of[name]] if name in getattr(self, "norm_of", {}) else None
         if "codes" in w:
             if epi == "swiglu":
                 q.qgemv_swiglu_nvfp4(w["codes"], w["scales"], w["g"], x, y)
             else:
                 q.qgemv_nvfp4(w["codes"], w["scales"], w["g"], x, y, residual=r)
+        elif "up" in w:
+            q.qgemv_swiglu_q45(w, w["up"], x, y, norm=nw)
+        elif nw is not None:
+            q.GemvChain([{**w, "x": x, "y": y, "norm": nw}]).run()
         else:
             q.qgemv_q45(w["q_lo"], w["q_hi"], w["scale"], w["min"], w["bits"], x, y, residual=r)
 
@@ -328,6 +359,8 @@ class Workload:
                     op["residual"] = self.view_in(f"r.{name}")
                 if "codes" not in op and op.get("q_hi") is None:
                     op.pop("q_hi", None)
+                if name in getattr(self, "norm_of", {}):
+                    op["norm"] = self.norms[self.norm_of[name]]
                 ops.append(op)
             self.chains.append(q.GemvChain(ops))
 
@@ -351,7 +384,7 @@ class Workload:
     def alg_bytes(self, idx):
         """Algorithmic bytes of call idx: weights + activations in + outputs."""
         name, N, K, epi, w = self.projs[idx]
-        n_out = N // 2 if epi == "swiglu" else N
+        n_out = N // 2 if (epi == "swiglu" and "up" not in w) else N
         b = self._wbytes(w) + 2 * self.M * K + 2 * self.M * n_out
         if epi == "residual":
             b += 2 * self.M * n_out
@@ -528,7 +561,7 @@ def oracle_runner(kind, M):
         om = OracleMoe(M)
         name = WORKLOAD_NAMES["moe"](M) + f"; {om.n_active} distinct experts active"
         return (lambda threads, frac: om.step(threads)), name, om.step_bytes
-    projs = host_projs(kind)
+    projs = host_projs("q45" if kind == "q45ffn" else kind)
     wb = 0
     for *_, w in projs:
         wb += sum(w[k].nbytes for k in ("codes", "scales", "q_lo", "q_hi", "scale", "min")
@@ -537,6 +570,8 @@ def oracle_runner(kind, M):
 
 
 def cpu_baseline(kind, M, budget_s=12.0, single_thread_budget_s=6.0):
+    # the fused-FFN layer streams the same weights through the same GEMV definition
+    # (its RMSNorm prologues cost O(K) each): the oracle runs the recipe's projections
     """Oracle throughput on this host's cores: whole steps of the workload,
     repeated until about budget_s of CPU work (a row sample only if one step
     alone exceeds the budget), plus the same with one thread."""
@@ -609,6 +644,9 @@ WORKLOAD_NAMES = {
                         f"gate+up 34816x5120 + SwiGLU, down 5120x17408 + residual, M={M}"),
     "q45": lambda M: ("mixed Q4/Q5 groupwise-int layer on the 27B-class shapes (QK Q4, V Q5, O Q4, "
                       f"gate Q5, up Q4, down Q4 + residual), M={M}"),
+    "q45ffn": lambda M: ("mixed Q4/Q5 groupwise-int layer on the 27B-class shapes with the FFN fused (Q5 gate + "
+                         "Q4 up, SwiGLU) and RMSNorm prologues on QK, V and the FFN; O Q4, down Q4 + residual, "
+                         f"M={M}"),
     "tiny": lambda M: f"tiny NVFP4 GEMV 256x512, M={M}",
     "moe": lambda M: (f"MoE decode layer (35B-A3B-class): hidden 2048, 128 experts, intermediate 768, "
                       f"top-8, M={M}"),
@@ -643,8 +681,10 @@ def read_probe_bandwidth(torch, q, stream, peak, nbytes=2 << 30, reps=10):
 def arithmetic(workload, M):
     if workload in ("dense", "tiny") and M == 1:
         return "f16 x f16 -> f32 FMA on CUDA cores (exact decoded weights, prescaled activations)"
-    if workload == "q45" and M == 1:
+    if workload in ("q45", "q45ffn") and M == 1:
         return "f16 x f16 -> f32 FMA on CUDA cores (codes as exact f16, prescaled activations)"
+    if workload == "q45ffn":
+        return "fp32 FMA on CUDA cores (exact fallback kernel for the normalised and fused ops), bf16 mma.sync for the rest"
     if workload == "q45":
         return "bf16 mma.sync, f32 accumulate (codes exact in bf16, raw bf16 activations)"
     return "f16 tcgen05 MMA, f32 accumulate (exact decoded weights, prescaled activations)"
@@ -834,7 +874,7 @@ def measure(args, kind, M, world, rank, stream, cpu=True, e2e=True):
 
 
 # Every configuration besides the headline one, measured in the same run.
-SWEEP = [("dense", 2), ("dense", 4), ("dense", 8), ("q45", 1), ("q45", 8), ("tiny", 1), ("moe", 8)]
+SWEEP = [("dense", 2), ("dense", 4), ("dense", 8), ("q45", 1), ("q45", 8), ("q45ffn", 1), ("tiny", 1), ("moe", 8)]
 
 
 def main():

@@ -177,28 +177,69 @@ __device__ float cc_norm_factor(const CcArgs& a, const uint8_t* smem, int warp, 
 // groups. A chunk kept raw sets *any_bf. Each warp issues the loads of up to
 // kBatch chunks before converting, so K up to 80 chunks costs one round trip
 // to memory.
+// Loads one batch of this warp's chunks (chunk base + u * NW) and, with the
+// RMSNorm prologue, their gamma pieces, all before any use (each load
+// followed by its use would serialise the round trips).
+template <int SRC, int NW, int B>
+__device__ __forceinline__ void cc_load_batch(const CcArgs& a, const uint8_t* smem, int base, int lane, uint4 (&raw)[B],
+                                              uint4 (&gam)[B])
+{
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+        const int kc = base + u * NW;
+        raw[u] = kc < a.C ? cc_load_chunk<SRC>(a, smem, kc, lane) : make_uint4(0, 0, 0, 0);
+    }
+    if (a.norm_w != nullptr) {
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int kc = base + u * NW;
+            gam[u] = kc < a.C ? ldg_nc_128(a.norm_w + kc * kChunkK + lane * 8) : make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+// The RMSNorm factor when every chunk of the warp fits one batch: the chunk
+// sums of squares come from the batch already loaded (same order as
+// cc_norm_factor), so x is read once.
+template <int NW, int B>
+__device__ __forceinline__ float cc_norm_factor_batch(const CcArgs& a, uint8_t* smem, int warp, int lane,
+                                                      const uint4 (&raw)[B])
+{
+    float* ss = reinterpret_cast<float*>(smem + a.smem_ss);
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+        const int kc = warp + u * NW;
+        if (kc < a.C) {
+            const float part = rms_chunk_ss(raw[u]);
+            if (lane == 0) ss[kc] = part;
+        }
+    }
+    cc_conv_sync<NW>();
+    float t = 0.f;
+    for (int kc = 0; kc < a.C; ++kc) t += ss[kc];
+    return rms_factor(t, a.K, a.norm_eps);
+}
+
 template <int NSEG, int SRC = XSRC_NC, int NW = kCcWarps>
 __device__ void cc_convert(const CcArgs& a, uint8_t* smem, int warp, int lane, volatile int* any_bf)
 {
     constexpr int PPS = kChunkK / NSEG / 8;  // 16-byte pieces per segment
     constexpr int kBatch = NW < kCcWarps ? 8 : 5;
-    const float rn = cc_norm_factor<SRC, NW>(a, smem, warp, lane);
+    const bool one_batch = a.C <= NW * kBatch;
+    float rn = 1.0f;
+    if (a.norm_w != nullptr && !one_batch) rn = cc_norm_factor<SRC, NW>(a, smem, warp, lane);
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
     float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
     uint8_t* fl = smem + a.smem_fl;
-    for (int base = warp; base < a.C; base += NW * kBatch) {
-        uint4 raw[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int kc = base + u * NW;
-            raw[u] = kc < a.C ? cc_load_chunk<SRC>(a, smem, kc, lane) : make_uint4(0, 0, 0, 0);
-        }
+    for (int base = warp; base < a.C || (a.norm_w != nullptr && one_batch && base == warp); base += NW * kBatch) {
+        uint4 raw[kBatch], gam[kBatch];
+        cc_load_batch<SRC, NW>(a, smem, base, lane, raw, gam);
         if (a.norm_w != nullptr) {
+            // every warp takes part in the factor's barrier, with or without chunks
+            if (one_batch) rn = cc_norm_factor_batch<NW>(a, smem, warp, lane, raw);
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int kc = base + u * NW;
-                if (kc < a.C) raw[u] = rms_apply8(raw[u], ldg_nc_128(a.norm_w + kc * kChunkK + lane * 8), rn);
-            }
+            for (int u = 0; u < kBatch; ++u)
+                if (base + u * NW < a.C) raw[u] = rms_apply8(raw[u], gam[u], rn);
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
@@ -346,24 +387,21 @@ __device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lan
 {
     constexpr int kBatch = NW < kCcWarps ? 8 : 5;
     constexpr int PPS = kChunkK / NSEG / 8;  // lanes (16-byte pieces) per segment
-    const float rn = cc_norm_factor<SRC, NW>(a, smem, warp, lane);
+    const bool one_batch = a.C <= NW * kBatch;
+    float rn = 1.0f;
+    if (a.norm_w != nullptr && !one_batch) rn = cc_norm_factor<SRC, NW>(a, smem, warp, lane);
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
     float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
     float* gx = reinterpret_cast<float*>(smem + a.smem_gx);
     uint8_t* fl = smem + a.smem_fl;
-    for (int base = warp; base < a.C; base += NW * kBatch) {
-        uint4 raw[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int kc = base + u * NW;
-            raw[u] = kc < a.C ? cc_load_chunk<SRC>(a, smem, kc, lane) : make_uint4(0, 0, 0, 0);
-        }
+    for (int base = warp; base < a.C || (a.norm_w != nullptr && one_batch && base == warp); base += NW * kBatch) {
+        uint4 raw[kBatch], gam[kBatch];
+        cc_load_batch<SRC, NW>(a, smem, base, lane, raw, gam);
         if (a.norm_w != nullptr) {
+            if (one_batch) rn = cc_norm_factor_batch<NW>(a, smem, warp, lane, raw);
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int kc = base + u * NW;
-                if (kc < a.C) raw[u] = rms_apply8(raw[u], ldg_nc_128(a.norm_w + kc * kChunkK + lane * 8), rn);
-            }
+            for (int u = 0; u < kBatch; ++u)
+                if (base + u * NW < a.C) raw[u] = rms_apply8(raw[u], gam[u], rn);
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {

@@ -35,13 +35,16 @@ constexpr int kChainNseg = 8;   // 32-k segments (always valid: at most 256 rows
 
 struct ChainOp {
     CcArgs a;   // the op's plan, as the standalone one-token kernel would use it
-    int fmt;    // FMT_NVFP4, FMT_Q4, FMT_Q5
+    int fmt;    // FMT_NVFP4, FMT_Q4, FMT_Q5 (the gate matrix of a SwiGLU)
     int epi;    // EPI_NONE, EPI_RESID, EPI_SWIGLU
     int dep;    // grid-wide barrier before the op reads its inputs
+    int ufmt;   // groupwise-int SwiGLU: the up matrix's format
 };
 
 struct ChainParams {
-    CUtensorMap map[kChainMaxOps][4];  // codes, scales, mins, Q5 high plane
+    // codes, scales, mins, Q5 high plane; then the same for a separate
+    // groupwise-int SwiGLU up matrix
+    CUtensorMap map[kChainMaxOps][8];
     ChainOp op[kChainMaxOps];
     int n_ops;
     int n_stages;
@@ -196,14 +199,18 @@ __device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, int epi, uint
     }
 }
 
-// The unit loop of one groupwise-int op (cc_q45_units of qgemv_cc.cu, as above).
-template <int BITS, int EPI, bool MIXED>
-__device__ __forceinline__ void chain_units_q45(const CcArgs& a, uint8_t* smem, uint32_t ring, uint32_t slot_bytes,
-                                                int n_stages, uint64_t* full, uint64_t* empty,
+// The unit loop of one groupwise-int op (cc_q45_units of qgemv_cc.cu, as
+// above): the epilogue at run time; SwiGLU reads a gate box (BITS) and an up
+// box (BITS_U) per phase.
+template <int BITS, int BITS_U, bool MIXED>
+__device__ __forceinline__ void chain_units_q45(const CcArgs& a, int epi, uint8_t* smem, uint32_t ring,
+                                                uint32_t slot_bytes, int n_stages, uint64_t* full, uint64_t* empty,
                                                 volatile int* abort_flag, bool& aborted, int& slot, int& lap)
 {
     constexpr int NSEG = kChainNseg;
     constexpr int KS = kChunkK / NSEG;
+    const bool swiglu = epi == EPI_SWIGLU, resid = epi == EPI_RESID;
+    const int gsh = swiglu ? 1 : 0;
     const CcGeom geom = cc_geom(a);
     const int R = a.R, P = a.P, C = a.C, Cp = a.Cp, n_units = a.n_units, n_out = a.n_out;
     const int rg_per_box = (R + kCcRows - 1) / kCcRows;
@@ -212,8 +219,9 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, uint8_t* smem, 
     const int bg = item / NSEG;
     const int b2 = bg / rg_per_box;
     const int row0 = (bg % rg_per_box) * kCcRows;
-    const bool active = b2 < P;
-    const int p = active ? b2 : 0;
+    const bool active = b2 < (P << gsh);
+    const int p = active ? b2 >> gsh : 0;
+    const bool up_box = swiglu && (b2 & 1);
     const uint32_t* xs = reinterpret_cast<const uint32_t*>(smem + a.smem_x);
     const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
     const float* gx = reinterpret_cast<const float*>(smem + a.smem_gx);
@@ -227,7 +235,7 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, uint8_t* smem, 
         float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
         float res = 0.f;
         const int r0 = u * R;
-        if (EPI == EPI_RESID && threadIdx.x < R && r0 + static_cast<int>(threadIdx.x) < n_out)
+        if (resid && threadIdx.x < R && r0 + static_cast<int>(threadIdx.x) < n_out)
             res = bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + threadIdx.x));
         for (int c = 0; c < Cp; ++c) {
             if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
@@ -242,10 +250,18 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, uint8_t* smem, 
                     xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
                 }
                 const float gxs = gx[kc * NSEG + seg];
-                if (!MIXED || fl[kc] == 0)
-                    cc_stage_q45<NSEG, BITS, false>(geom, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
-                else
-                    cc_stage_q45<NSEG, BITS, true>(geom, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                const bool bf = MIXED && fl[kc] != 0;
+                if (up_box) {
+                    if (bf)
+                        cc_stage_q45<NSEG, BITS_U, true>(geom, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                    else
+                        cc_stage_q45<NSEG, BITS_U, false>(geom, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                } else {
+                    if (bf)
+                        cc_stage_q45<NSEG, BITS, true>(geom, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                    else
+                        cc_stage_q45<NSEG, BITS, false>(geom, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                }
             }
             mbar_arrive(&empty[slot]);
             if (++slot == n_stages) {
@@ -266,8 +282,13 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, uint8_t* smem, 
             for (int r = threadIdx.x; r < R; r += kCcThreads) {
                 if (r0 + r >= n_out) break;
                 float val = 0.f;
-                for (int pp = 0; pp < P; ++pp) val += red[pp * geom.R8 + r];
-                if (EPI == EPI_RESID)
+                for (int pp = 0; pp < P; ++pp) val += red[(pp << gsh) * geom.R8 + r];
+                if (swiglu) {
+                    float v1 = 0.f;
+                    for (int pp = 0; pp < P; ++pp) v1 += red[((pp << gsh) + 1) * geom.R8 + r];
+                    val = (val / (1.0f + expf(-val))) * v1;
+                }
+                if (resid)
                     val += r == static_cast<int>(threadIdx.x) ? res
                                                               : bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + r));
                 chain_store(a, r0 + r, val);
@@ -289,17 +310,17 @@ __device__ __forceinline__ void chain_nvfp4(const CcArgs& a, int epi, bool mixed
                                  lap);
 }
 
-template <int BITS, int EPI>
-__device__ __forceinline__ void chain_q45(const CcArgs& a, bool mixed, uint8_t* smem, uint32_t ring,
+template <int BITS, int BITS_U>
+__device__ __forceinline__ void chain_q45(const CcArgs& a, int epi, bool mixed, uint8_t* smem, uint32_t ring,
                                           uint32_t slot_bytes, int n_stages, uint64_t* full, uint64_t* empty,
                                           volatile int* abort_flag, bool& aborted, int& slot, int& lap)
 {
     if (mixed)
-        chain_units_q45<BITS, EPI, true>(a, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted,
-                                         slot, lap);
+        chain_units_q45<BITS, BITS_U, true>(a, epi, smem, ring, slot_bytes, n_stages, full, empty, abort_flag,
+                                            aborted, slot, lap);
     else
-        chain_units_q45<BITS, EPI, false>(a, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted,
-                                          slot, lap);
+        chain_units_q45<BITS, BITS_U, false>(a, epi, smem, ring, slot_bytes, n_stages, full, empty, abort_flag,
+                                             aborted, slot, lap);
 }
 
 __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_constant__ ChainParams p)
@@ -334,6 +355,8 @@ __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_co
                 prefetch_tensormap(&p.map[o][1]);
                 if (p.op[o].fmt != FMT_NVFP4) prefetch_tensormap(&p.map[o][2]);
                 if (p.op[o].fmt == FMT_Q5) prefetch_tensormap(&p.map[o][3]);
+                if (p.op[o].fmt != FMT_NVFP4 && p.op[o].epi == EPI_SWIGLU)
+                    for (int i = 4; i < 8; ++i) prefetch_tensormap(&p.map[o][i]);
             }
         }
         __syncwarp();
@@ -361,7 +384,9 @@ __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_co
                     for (int pp = 0; pp < P; ++pp) live += (c * P + pp < C) ? 1 : 0;
                     uint8_t* sb = smem + a.smem_ring + slot * p.slot_bytes;
                     if (elect_one()) {
-                        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live * ngu) * box_tx);
+                        // NVFP4: box_tx per (phase, gate/up) box; groupwise int: per phase
+                        const uint32_t phase_tx = fmt == FMT_NVFP4 ? static_cast<uint32_t>(ngu) * box_tx : box_tx;
+                        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live) * phase_tx);
                         for (int pp = 0; pp < P; ++pp) {
                             const int kc = c * P + pp;
                             if (kc >= C) continue;
@@ -375,15 +400,19 @@ __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_co
                                                 kc * (kChunkK / 16), row, &full[slot]);
                                 }
                             } else {
-                                tma_load_2d(sb + pp * box_bytes, &p.map[o][0], kc * (kChunkK / 2), row0,
-                                            &full[slot]);
-                                tma_load_2d(sb + scales_off + pp * sbox_bytes, &p.map[o][1], kc * (kChunkK / 32),
-                                            row0, &full[slot]);
-                                tma_load_2d(sb + mins_off + pp * sbox_bytes, &p.map[o][2], kc * (kChunkK / 32),
-                                            row0, &full[slot]);
-                                if (fmt == FMT_Q5)
-                                    tma_load_2d(sb + hi_off + pp * 2u * sbox_bytes, &p.map[o][3],
-                                                kc * (kChunkK / 8), row0, &full[slot]);
+                                // gate (or only) box, then a SwiGLU's up box: same rows of two matrices
+                                for (int gg = 0; gg < ngu; ++gg) {
+                                    const uint32_t b2 = static_cast<uint32_t>(pp * ngu + gg);
+                                    const CUtensorMap* mp = &p.map[o][4 * gg];
+                                    tma_load_2d(sb + b2 * box_bytes, mp, kc * (kChunkK / 2), row0, &full[slot]);
+                                    tma_load_2d(sb + scales_off + b2 * sbox_bytes, mp + 1, kc * (kChunkK / 32),
+                                                row0, &full[slot]);
+                                    tma_load_2d(sb + mins_off + b2 * sbox_bytes, mp + 2, kc * (kChunkK / 32), row0,
+                                                &full[slot]);
+                                    if ((gg ? p.op[o].ufmt : fmt) == FMT_Q5)
+                                        tma_load_2d(sb + hi_off + b2 * 2u * sbox_bytes, mp + 3, kc * (kChunkK / 8),
+                                                    row0, &full[slot]);
+                                }
                             }
                         }
                     }
@@ -426,20 +455,21 @@ __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_co
         if (op.fmt == FMT_NVFP4) {
             chain_nvfp4(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag, aborted,
                         slot, lap);
-        } else if (op.fmt == FMT_Q5) {
-            if (op.epi == EPI_RESID)
-                chain_q45<5, EPI_RESID>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                        aborted, slot, lap);
-            else
-                chain_q45<5, EPI_NONE>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                       aborted, slot, lap);
         } else {
-            if (op.epi == EPI_RESID)
-                chain_q45<4, EPI_RESID>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                        aborted, slot, lap);
+            const bool b5 = op.fmt == FMT_Q5;
+            const bool u5 = op.epi == EPI_SWIGLU ? op.ufmt == FMT_Q5 : b5;
+            if (b5 && u5)
+                chain_q45<5, 5>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                aborted, slot, lap);
+            else if (b5)
+                chain_q45<5, 4>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                aborted, slot, lap);
+            else if (u5)
+                chain_q45<4, 5>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                aborted, slot, lap);
             else
-                chain_q45<4, EPI_NONE>(a, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                       aborted, slot, lap);
+                chain_q45<4, 4>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                aborted, slot, lap);
         }
     }
 }
@@ -487,14 +517,16 @@ qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, 
     int c_max = 0, red_max = 0;
     for (int o = 0; o < n_ops; ++o) {
         const qg_gemv_op& g = ops[o];
-        if (g.K % kChunkK != 0 || g.up_codes != nullptr) return QG_ERR_UNSUPPORTED;
+        if (g.K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
         ChainOp& op = p.op[o];
         op.fmt = g.format == QG_FMT_NVFP4 ? FMT_NVFP4 : g.format == QG_FMT_Q5 ? FMT_Q5 : FMT_Q4;
         op.epi = g.epilogue == QG_EPI_SWIGLU ? EPI_SWIGLU : g.epilogue == QG_EPI_RESIDUAL ? EPI_RESID : EPI_NONE;
         op.dep = o > 0 && g.after_previous ? 1 : 0;
         any_dep = any_dep || op.dep;
+        const bool sep_up = g.up_codes != nullptr;
+        op.ufmt = sep_up ? (g.up_format == QG_FMT_Q5 ? FMT_Q5 : FMT_Q4) : op.fmt;
         const int ngu = op.epi == EPI_SWIGLU ? 2 : 1;
-        const int n_out = op.epi == EPI_SWIGLU ? g.N / 2 : g.N;
+        const int n_out = op.epi == EPI_SWIGLU && !sep_up ? g.N / 2 : g.N;
         CcArgs& a = op.a;
         cc_plan(a, n_out, ngu, g.K, sms);
         a.x = static_cast<const uint16_t*>(g.x);
@@ -512,10 +544,13 @@ qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, 
             st = a.scales_off + nbox * a.R8 * 16u;
             a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
         } else {
+            const bool any5 = op.fmt == FMT_Q5 || op.ufmt == FMT_Q5;
             a.mins_off = a.scales_off + nbox * a.R8 * 16u;
             a.hi_off = a.mins_off + nbox * a.R8 * 16u;
-            st = a.hi_off + (op.fmt == FMT_Q5 ? nbox * a.R8 * 32u : 0u);
+            st = a.hi_off + (any5 ? nbox * a.R8 * 32u : 0u);
+            // bytes one phase brings in: its gate (or only) box and a SwiGLU's up box
             a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (op.fmt == FMT_Q5 ? 32u : 0u));
+            if (ngu == 2) a.box_tx += static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (op.ufmt == FMT_Q5 ? 32u : 0u));
         }
         slot_bytes = std::max(slot_bytes, align_up(st, 1024));
         c_max = std::max(c_max, a.C);
@@ -538,6 +573,18 @@ qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, 
             if (op.fmt == FMT_Q5 &&
                 !encode_tmap_2d(&p.map[o][3], g.q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 8, rows, 32, R, false))
                 return QG_ERR_CUDA;
+            if (sep_up) {
+                if (!encode_tmap_2d(&p.map[o][4], g.up_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 2, rows, 128,
+                                    R, true) ||
+                    !encode_tmap_2d(&p.map[o][5], g.up_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8,
+                                    R, false) ||
+                    !encode_tmap_2d(&p.map[o][6], g.up_mins, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8,
+                                    R, false))
+                    return QG_ERR_CUDA;
+                if (op.ufmt == FMT_Q5 && !encode_tmap_2d(&p.map[o][7], g.up_q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                                                         g.K / 8, rows, 32, R, false))
+                    return QG_ERR_CUDA;
+            }
         }
     }
     if (any_dep && !sync) return QG_ERR_INVALID_ARG;

@@ -359,8 +359,11 @@ __device__ void tc_convert(const TcArgs& a, uint8_t* smem, int c0, int nst, int 
             for (int i = 0; i < 8; ++i) raw[i] = src ? ldg_nc_128(xs + (kq + 4 * i) * 8) : make_uint4(0, 0, 0, 0);
             if (NORM && src) {
                 const uint16_t* gw = a.norm_w + static_cast<size_t>(kc) * kChunkK;
+                uint4 gam[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) raw[i] = rms_apply8(raw[i], ldg_nc_128(gw + (kq + 4 * i) * 8), rnorm[m]);
+                for (int i = 0; i < 8; ++i) gam[i] = ldg_nc_128(gw + (kq + 4 * i) * 8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) raw[i] = rms_apply8(raw[i], gam[i], rnorm[m]);
             }
             uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
 #pragma unroll

@@ -260,8 +260,8 @@ typedef struct {
  *           after_previous set; may be NULL otherwise. Calls that overlap on
  *           the GPU must use different words, and after a call that reported
  *           QG_ERR_DEVICE_TIMEOUT the words must be zeroed again.
- * With one token, K a multiple of 256 for every op and no separate up
- * matrix, the list runs as one persistent kernel (one CTA per SM, launched
+ * With one token and K a multiple of 256 for every op, the list runs as one
+ * persistent kernel (one CTA per SM, launched
  * cooperatively when an op waits for earlier ones): the weight stream runs on
  * across op boundaries. Other lists run as one launch per op, in order, on
  * `stream`; a single record is thus also the way to call any projection with
