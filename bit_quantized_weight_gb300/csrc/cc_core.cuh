@@ -381,66 +381,108 @@ __device__ __forceinline__ void cc_stage(const CcGeom& a, uint32_t stage, int b2
 
 // Converts x as cc_convert does (RMSNorm prologue included), with the
 // (k, k+4) pairing, and writes the fp32 sum of each segment's values (the
-// values the projection reads: x, or h with the prologue).
-template <int NSEG, int SRC = XSRC_NC, int NW = kCcWarps>
+// values the projection reads: x, or h with the prologue). MT tokens (rows
+// of x, K apart): token t's chunks at smem_x + t * C * 512, its factors at
+// pe[t * C + kc], its segment sums at gx[(t * C + kc) * NSEG + s]; a chunk
+// that one token cannot carry exactly in f16 stays raw bf16 for every token
+// (one flag per chunk), so a stage runs one arithmetic for all of them.
+template <int NSEG, int SRC = XSRC_NC, int NW = kCcWarps, int MT = 1>
 __device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lane, volatile int* any_bf)
 {
-    constexpr int kBatch = NW < kCcWarps ? 8 : 5;
+    constexpr int kBatch = MT == 2 ? 3 : (NW < kCcWarps ? 8 : 5);
     constexpr int PPS = kChunkK / NSEG / 8;  // lanes (16-byte pieces) per segment
-    const bool one_batch = a.C <= NW * kBatch;
-    float rn = 1.0f;
-    if (a.norm_w != nullptr && !one_batch) rn = cc_norm_factor<SRC, NW>(a, smem, warp, lane);
+    const bool one_batch = MT == 1 && a.C <= NW * kBatch;
+    float rn[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) rn[t] = 1.0f;
+    if (a.norm_w != nullptr && !one_batch) {
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            CcArgs at = a;
+            at.x = a.x + static_cast<size_t>(t) * a.K;
+            at.smem_ss = a.smem_ss + static_cast<uint32_t>(t * a.C) * 4u;
+            rn[t] = cc_norm_factor<SRC, NW>(at, smem, warp, lane);
+        }
+    }
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + a.smem_x);
     float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
     float* gx = reinterpret_cast<float*>(smem + a.smem_gx);
     uint8_t* fl = smem + a.smem_fl;
     for (int base = warp; base < a.C || (a.norm_w != nullptr && one_batch && base == warp); base += NW * kBatch) {
-        uint4 raw[kBatch], gam[kBatch];
-        cc_load_batch<SRC, NW>(a, smem, base, lane, raw, gam);
-        if (a.norm_w != nullptr) {
-            if (one_batch) rn = cc_norm_factor_batch<NW>(a, smem, warp, lane, raw);
+        uint4 raw[MT][kBatch], gam[kBatch];
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u)
-                if (base + u * NW < a.C) raw[u] = rms_apply8(raw[u], gam[u], rn);
+        for (int t = 0; t < MT; ++t) {
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int kc = base + u * NW;
+                raw[t][u] = kc < a.C ? (SRC == XSRC_SMEM && MT == 1
+                                            ? cc_load_chunk<SRC>(a, smem, kc, lane)
+                                            : ldg_128<SRC == XSRC_CG>(a.x + static_cast<size_t>(t) * a.K +
+                                                                      static_cast<size_t>(kc) * kChunkK + lane * 8))
+                                     : make_uint4(0, 0, 0, 0);
+            }
+        }
+        if (a.norm_w != nullptr) {
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int kc = base + u * NW;
+                gam[u] = kc < a.C ? ldg_nc_128(a.norm_w + kc * kChunkK + lane * 8) : make_uint4(0, 0, 0, 0);
+            }
+            if (one_batch) rn[0] = cc_norm_factor_batch<NW>(a, smem, warp, lane, raw[0]);
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u)
+                    if (base + u * NW < a.C) raw[t][u] = rms_apply8(raw[t][u], gam[u], rn[t]);
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int kc = base + u * NW;
             if (kc >= a.C) break;
-            const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-            float sx = 0.f;
+            int e[MT];
+            bool inexact = false;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) sx += bf16_bits_to_f32((i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu));
-            uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
+            for (int t = 0; t < MT; ++t) {
+                const uint32_t wv[4] = {raw[t][u].x, raw[t][u].y, raw[t][u].z, raw[t][u].w};
+                uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) bf16_range_acc(wv[i], mx2, mn2);
-            uint32_t emax, emin, magmax;
-            bf16_range_fin(mx2, mn2, emax, emin, magmax);
-#pragma unroll
-            for (int sh = 1; sh < PPS; sh <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, sh);
-            emax = __reduce_max_sync(0xffffffffu, emax);
-            emin = __reduce_min_sync(0xffffffffu, emin);
-            if (emax == 0u) magmax = __reduce_max_sync(0xffffffffu, magmax);
-            const int e = min(emax != 0u ? 141 - static_cast<int>(emax) : prescale_exponent(magmax), 126);
-            const bool inexact = emin != 255u && static_cast<int>(emin) - 127 + e < -17;
-            uint32_t o[4];
-            if (inexact) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) o[i] = wv[i];
-            } else {
-                const float sc = __int_as_float((127 + e) << 23);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    o[i] = pack_f16x2(__uint_as_float(wv[i] << 16) * sc, __uint_as_float(wv[i] & 0xFFFF0000u) * sc);
+                for (int i = 0; i < 4; ++i) bf16_range_acc(wv[i], mx2, mn2);
+                uint32_t emax, emin, magmax;
+                bf16_range_fin(mx2, mn2, emax, emin, magmax);
+                emax = __reduce_max_sync(0xffffffffu, emax);
+                emin = __reduce_min_sync(0xffffffffu, emin);
+                if (emax == 0u) magmax = __reduce_max_sync(0xffffffffu, magmax);
+                e[t] = min(emax != 0u ? 141 - static_cast<int>(emax) : prescale_exponent(magmax), 126);
+                inexact = inexact || (emin != 255u && static_cast<int>(emin) - 127 + e[t] < -17);
             }
-            // natural pairs (x0,x1)(x2,x3)(x4,x5)(x6,x7) -> (x0,x4)(x1,x5)(x2,x6)(x3,x7)
-            const uint32_t p0 = __byte_perm(o[0], o[2], 0x5410), p1 = __byte_perm(o[0], o[2], 0x7632);
-            const uint32_t p2 = __byte_perm(o[1], o[3], 0x5410), p3 = __byte_perm(o[1], o[3], 0x7632);
-            const int off = (lane % PPS) * NSEG * 4 + (lane / PPS) * 4;
-            *reinterpret_cast<uint4*>(xs + kc * (kChunkK / 2) + off) = make_uint4(p0, p1, p2, p3);
-            if (lane % PPS == 0) gx[kc * NSEG + lane / PPS] = sx;
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                const uint32_t wv[4] = {raw[t][u].x, raw[t][u].y, raw[t][u].z, raw[t][u].w};
+                float sx = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    sx += bf16_bits_to_f32((i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu));
+#pragma unroll
+                for (int sh = 1; sh < PPS; sh <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, sh);
+                uint32_t o[4];
+                if (inexact) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[i] = wv[i];
+                } else {
+                    const float sc = __int_as_float((127 + e[t]) << 23);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        o[i] = pack_f16x2(__uint_as_float(wv[i] << 16) * sc, __uint_as_float(wv[i] & 0xFFFF0000u) * sc);
+                }
+                // natural pairs (x0,x1)(x2,x3)(x4,x5)(x6,x7) -> (x0,x4)(x1,x5)(x2,x6)(x3,x7)
+                const uint32_t p0 = __byte_perm(o[0], o[2], 0x5410), p1 = __byte_perm(o[0], o[2], 0x7632);
+                const uint32_t p2 = __byte_perm(o[1], o[3], 0x5410), p3 = __byte_perm(o[1], o[3], 0x7632);
+                const int off = (lane % PPS) * NSEG * 4 + (lane / PPS) * 4;
+                *reinterpret_cast<uint4*>(xs + (t * a.C + kc) * (kChunkK / 2) + off) = make_uint4(p0, p1, p2, p3);
+                if (lane % PPS == 0) gx[(t * a.C + kc) * NSEG + lane / PPS] = sx;
+                if (lane == 0) pe[t * a.C + kc] = inexact ? 1.0f : __int_as_float((127 - e[t]) << 23);
+            }
             if (lane == 0) {
-                pe[kc] = inexact ? 1.0f : __int_as_float((127 - e) << 23);
                 fl[kc] = inexact ? 1 : 0;
                 if (inexact) *any_bf = 1;
             }
@@ -465,9 +507,14 @@ __device__ __forceinline__ void q45_pairs(uint32_t w, uint32_t hsp, uint32_t (&z
 // One thread's share of a stage (see cc_stage); `seg` covers one group
 // (NSEG = 8) or half of one (NSEG = 16). The bf16 path (a chunk kept raw)
 // widens the codes and activations to fp32.
-template <int NSEG, int BITS, bool BF>
+//
+// MT tokens (1 or 2) share each decoded code pair: token t's activation
+// words are xw[t * KS / 2 ...], its factors pe[t] and gxs[t], its sums
+// acc[i * MT + t].
+template <int NSEG, int BITS, bool BF, int MT = 1>
 __device__ __forceinline__ void cc_stage_q45(const CcGeom& a, uint32_t stage, int b2, int row0, int seg,
-                                             const uint32_t* xw, float pe, float gxs, float (&acc)[kCcRows])
+                                             const uint32_t* xw, const float* pe, const float* gxs,
+                                             float (&acc)[kCcRows * MT])
 {
     constexpr int KS = kChunkK / NSEG;
     constexpr int NW = KS / 8;
@@ -493,7 +540,9 @@ __device__ __forceinline__ void cc_stage_q45(const CcGeom& a, uint32_t stage, in
         }
         const float sc = half_bits_to_f32(lds16(stage + a.scales_off + rowi * 16u + static_cast<uint32_t>(grp * 2)));
         const float mn = half_bits_to_f32(lds16(stage + a.mins_off + rowi * 16u + static_cast<uint32_t>(grp * 2)));
-        float s0 = 0.f, s1 = 0.f;
+        float s0[MT], s1[MT];
+#pragma unroll
+        for (int t = 0; t < MT; ++t) s0[t] = s1[t] = 0.f;
 #pragma unroll
         for (int wd = 0; wd < NW; ++wd) {
             uint32_t hsp = 0;
@@ -505,22 +554,28 @@ __device__ __forceinline__ void cc_stage_q45(const CcGeom& a, uint32_t stage, in
             q45_pairs<BITS>(cw[wd], hsp, z);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (BF) {
-                    // raw bf16 activations: widen both sides to fp32
-                    const uint32_t xv = xw[wd * 4 + j];
-                    s0 = fmaf(static_cast<float>(z[j] & 0xFFFFu), __uint_as_float(xv << 16), s0);
-                    s1 = fmaf(static_cast<float>(z[j] >> 16), __uint_as_float(xv & 0xFFFF0000u), s1);
-                } else if (j & 1) {
-                    s1 = fma2_mixed<false>(z[j], xw[wd * 4 + j], s1);
-                } else {
-                    s0 = fma2_mixed<false>(z[j], xw[wd * 4 + j], s0);
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    const uint32_t xv = xw[t * (KS / 2) + wd * 4 + j];
+                    if (BF) {
+                        // raw bf16 activations: widen both sides to fp32
+                        s0[t] = fmaf(static_cast<float>(z[j] & 0xFFFFu), __uint_as_float(xv << 16), s0[t]);
+                        s1[t] = fmaf(static_cast<float>(z[j] >> 16), __uint_as_float(xv & 0xFFFF0000u), s1[t]);
+                    } else if (j & 1) {
+                        s1[t] = fma2_mixed<false>(z[j], xv, s1[t]);
+                    } else {
+                        s0[t] = fma2_mixed<false>(z[j], xv, s0[t]);
+                    }
                 }
             }
         }
-        // subnormal codes carry 2^-24 (not on the bf16 path)
-        const float sq = (s0 + s1) * (BF ? 1.0f : 16777216.0f);
-        acc[i] = fmaf(sq * sc, pe, acc[i]);
-        acc[i] = fmaf(mn, gxs, acc[i]);
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            // subnormal codes carry 2^-24 (not on the bf16 path)
+            const float sq = (s0[t] + s1[t]) * (BF ? 1.0f : 16777216.0f);
+            acc[i * MT + t] = fmaf(sq * sc, pe[t], acc[i * MT + t]);
+            acc[i * MT + t] = fmaf(mn, gxs[t], acc[i * MT + t]);
+        }
     }
 }
 

@@ -241,8 +241,10 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
 // The compute warps' unit loop of the groupwise-int kernel (MIXED as in
 // cc_units).
 // SwiGLU (a separate up matrix of BITS_U-bit codes): each phase holds a gate
-// box (BITS) and an up box (BITS_U).
-template <int BITS, int EPI, int NSEG, bool MIXED, int BITS_U = BITS>
+// box (BITS) and an up box (BITS_U). MT tokens (1 or 2) share every decoded
+// code: their activations, factors and sums are kept per token, their
+// outputs and residuals are rows of n_out values.
+template <int BITS, int EPI, int NSEG, bool MIXED, int BITS_U = BITS, int MT = 1>
 __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                              volatile int* abort_flag)
 {
@@ -270,39 +272,52 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
     const int n_mine = active ? max(0, (a.C - p + a.P - 1) / a.P) : 0;
     const uint32_t x0 = smem_u32(xs + p * (kChunkK / 2) + seg * 4);
     const uint32_t x_step = static_cast<uint32_t>(a.P) * (kChunkK * 2u);
+    const uint32_t x_tok = static_cast<uint32_t>(a.C) * (kChunkK * 2u);  // bytes per token's activations
 
     // residual of the first unit's rows, read now rather than in the epilogue
-    float res_first = 0.f;
-    if (EPI == EPI_RESID && threadIdx.x < a.R && blockIdx.x * a.R + static_cast<int>(threadIdx.x) < a.n_out)
-        res_first = bf16_bits_to_f32(a.residual[blockIdx.x * a.R + threadIdx.x]);
+    float res_first[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        res_first[t] = 0.f;
+        if (EPI == EPI_RESID && threadIdx.x < a.R && blockIdx.x * a.R + static_cast<int>(threadIdx.x) < a.n_out)
+            res_first[t] = bf16_bits_to_f32(a.residual[t * a.n_out + blockIdx.x * a.R + threadIdx.x]);
+    }
 
     bool aborted = false;
     int slot = 0, lap = 0;
     for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
-        float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
+        float acc[kCcRows * MT];
+#pragma unroll
+        for (int i = 0; i < kCcRows * MT; ++i) acc[i] = 0.f;
         for (int c = 0; c < a.Cp; ++c) {
             if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
             if (!aborted && c < n_mine) {
                 const int kc = c * a.P + p;
                 const uint32_t stage = ring + slot * a.stage_bytes;
-                uint32_t xw[KS / 2];
+                uint32_t xw[MT * (KS / 2)];
                 const uint32_t xc = x0 + static_cast<uint32_t>(c) * x_step;
+                float pe[MT], gxs[MT];
 #pragma unroll
-                for (int i = 0; i < KS / 8; ++i) {
-                    const uint4 v = lds128(xc + i * NSEG * 16);
-                    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
+                for (int t = 0; t < MT; ++t) {
+#pragma unroll
+                    for (int i = 0; i < KS / 8; ++i) {
+                        const uint4 v = lds128(xc + t * x_tok + i * NSEG * 16);
+                        uint32_t* d = xw + t * (KS / 2) + 4 * i;
+                        d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+                    }
+                    pe[t] = pe_all[t * a.C + kc];
+                    gxs[t] = gx[(t * a.C + kc) * NSEG + seg];
                 }
-                const float gxs = gx[kc * NSEG + seg];
                 if (up_box) {
                     if (!MIXED || fl[kc] == 0)
-                        cc_stage_q45<NSEG, BITS_U, false>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                        cc_stage_q45<NSEG, BITS_U, false, MT>(cc_geom(a), stage, b2, row0, seg, xw, pe, gxs, acc);
                     else
-                        cc_stage_q45<NSEG, BITS_U, true>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                        cc_stage_q45<NSEG, BITS_U, true, MT>(cc_geom(a), stage, b2, row0, seg, xw, pe, gxs, acc);
                 } else {
                     if (!MIXED || fl[kc] == 0)
-                        cc_stage_q45<NSEG, BITS, false>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                        cc_stage_q45<NSEG, BITS, false, MT>(cc_geom(a), stage, b2, row0, seg, xw, pe, gxs, acc);
                     else
-                        cc_stage_q45<NSEG, BITS, true>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                        cc_stage_q45<NSEG, BITS, true, MT>(cc_geom(a), stage, b2, row0, seg, xw, pe, gxs, acc);
                 }
             }
             // every compute thread arrives: its own reads of the slot are done
@@ -316,35 +331,41 @@ __device__ __forceinline__ void cc_q45_units(const CcArgs& a, uint8_t* smem, uin
         // ---------------- fixed-order reduction over segments (a butterfly
         // across the segment lanes of the warp) and phases, epilogue
 #pragma unroll
-        for (int i = 0; i < kCcRows; ++i)
+        for (int i = 0; i < kCcRows * MT; ++i)
 #pragma unroll
             for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
         if (active && seg == 0) {
 #pragma unroll
-            for (int i = 0; i < kCcRows; ++i) red[b2 * a.R8 + row0 + i] = acc[i];
+            for (int i = 0; i < kCcRows; ++i)
+#pragma unroll
+                for (int t = 0; t < MT; ++t) red[(b2 * a.R8 + row0 + i) * MT + t] = acc[i * MT + t];
         }
         named_barrier_sync(1, kCcThreads);
         if (!aborted) {
             const int r0 = u * a.R;
             for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
                 if (r0 + r >= a.n_out) break;
-                float v[NGU];
 #pragma unroll
-                for (int gg = 0; gg < NGU; ++gg) {
-                    float s = 0.f;
-                    for (int pp = 0; pp < a.P; ++pp) s += red[(pp * NGU + gg) * a.R8 + r];
-                    v[gg] = s;
+                for (int t = 0; t < MT; ++t) {
+                    float v[NGU];
+#pragma unroll
+                    for (int gg = 0; gg < NGU; ++gg) {
+                        float s = 0.f;
+                        for (int pp = 0; pp < a.P; ++pp) s += red[((pp * NGU + gg) * a.R8 + r) * MT + t];
+                        v[gg] = s;
+                    }
+                    float val = v[0];
+                    if (EPI == EPI_SWIGLU) val = (val / (1.0f + expf(-val))) * v[NGU - 1];
+                    const int o = t * a.n_out + r0 + r;
+                    if (EPI == EPI_RESID)
+                        val += u == static_cast<int>(blockIdx.x) && r == static_cast<int>(threadIdx.x)
+                                   ? res_first[t]
+                                   : bf16_bits_to_f32(a.residual[o]);
+                    if (a.out_f32)
+                        reinterpret_cast<float*>(a.y)[o] = val;
+                    else
+                        reinterpret_cast<uint16_t*>(a.y)[o] = f32_to_bf16_bits_rn(val);
                 }
-                float val = v[0];
-                if (EPI == EPI_SWIGLU) val = (val / (1.0f + expf(-val))) * v[NGU - 1];
-                if (EPI == EPI_RESID)
-                    val += u == static_cast<int>(blockIdx.x) && r == static_cast<int>(threadIdx.x)
-                               ? res_first
-                               : bf16_bits_to_f32(a.residual[r0 + r]);
-                if (a.out_f32)
-                    reinterpret_cast<float*>(a.y)[r0 + r] = val;
-                else
-                    reinterpret_cast<uint16_t*>(a.y)[r0 + r] = f32_to_bf16_bits_rn(val);
             }
         }
         named_barrier_sync(1, kCcThreads);
@@ -356,7 +377,7 @@ struct Q45Maps {
     CUtensorMap m[2][4];  // [gate or only matrix, SwiGLU up matrix][codes, scales, mins, hi]
 };
 
-template <int BITS, int EPI, int NSEG, int BITS_U>
+template <int BITS, int EPI, int NSEG, int BITS_U, int MT>
 __global__ void __launch_bounds__(kCcAllThreads, 1)
     cc_q45_kernel(const __grid_constant__ CcArgs a, const __grid_constant__ Q45Maps maps)
 {
@@ -450,12 +471,12 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
         cc_zero_padding(a, smem, a.P * NGU, roff, rbytes, (BITS == 5 || BITS_U == 5) ? 4 : 3);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    cc_convert_q45<NSEG>(a, smem, warp, lane, any_bf);
+    cc_convert_q45<NSEG, XSRC_NC, kCcWarps, MT>(a, smem, warp, lane, any_bf);
     named_barrier_sync(1, kCcThreads);
     if (*any_bf)
-        cc_q45_units<BITS, EPI, NSEG, true, BITS_U>(a, smem, full, empty, abort_flag);
+        cc_q45_units<BITS, EPI, NSEG, true, BITS_U, MT>(a, smem, full, empty, abort_flag);
     else
-        cc_q45_units<BITS, EPI, NSEG, false, BITS_U>(a, smem, full, empty, abort_flag);
+        cc_q45_units<BITS, EPI, NSEG, false, BITS_U, MT>(a, smem, full, empty, abort_flag);
 }
 
 
@@ -536,7 +557,7 @@ qg_status cc_dispatch(const CcArgs& a, const CUtensorMap& tmc, const CUtensorMap
     return cc_launch<EPI, 16>(a, tmc, tms, grid, stream);
 }
 
-template <int BITS, int EPI, int NSEG, int BITS_U>
+template <int BITS, int EPI, int NSEG, int BITS_U, int MT>
 qg_status cc_q45_launch(CcArgs a, const Q45Maps& maps, int grid, cudaStream_t stream)
 {
     constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
@@ -555,12 +576,12 @@ qg_status cc_q45_launch(CcArgs a, const Q45Maps& maps, int grid, cudaStream_t st
     // bytes one phase brings in (its gate box and, for SwiGLU, its up box)
     a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (BITS == 5 ? 32u : 0u));
     if (NGU == 2) a.box_tx += static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (BITS_U == 5 ? 32u : 0u));
-    const uint32_t x_bytes = static_cast<uint32_t>(a.C) * kChunkK * 2u;
-    const uint32_t pe_bytes = align_up(static_cast<uint32_t>(a.C) * 4u, 16);
-    const uint32_t gx_bytes = align_up(static_cast<uint32_t>(a.C * NSEG) * 4u, 16);
+    const uint32_t x_bytes = static_cast<uint32_t>(MT * a.C) * kChunkK * 2u;
+    const uint32_t pe_bytes = align_up(static_cast<uint32_t>(MT * a.C) * 4u, 16);
+    const uint32_t gx_bytes = align_up(static_cast<uint32_t>(MT * a.C * NSEG) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(a.C), 16);
-    const uint32_t ss_bytes = a.norm_w ? align_up(static_cast<uint32_t>(a.C) * 4u, 16) : 0u;
-    const uint32_t red_bytes = align_up(nbox * a.R8 * 4u, 128);
+    const uint32_t ss_bytes = a.norm_w ? align_up(static_cast<uint32_t>(MT * a.C) * 4u, 16) : 0u;
+    const uint32_t red_bytes = align_up(nbox * a.R8 * 4u * MT, 128);
     const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
     const uint32_t fixed = x_bytes + pe_bytes + gx_bytes + fl_bytes + ss_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
@@ -585,7 +606,7 @@ qg_status cc_q45_launch(CcArgs a, const Q45Maps& maps, int grid, cudaStream_t st
     so += bar_bytes;
     if (so > kCcSmemMax) return QG_ERR_UNSUPPORTED;
 
-    auto kern = cc_q45_kernel<BITS, EPI, NSEG, BITS_U>;
+    auto kern = cc_q45_kernel<BITS, EPI, NSEG, BITS_U, MT>;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
@@ -609,12 +630,16 @@ qg_status cc_q45_launch(CcArgs a, const Q45Maps& maps, int grid, cudaStream_t st
 }
 
 template <int BITS, int EPI, int BITS_U = BITS>
-qg_status cc_q45_dispatch(const CcArgs& a, const Q45Maps& maps, int grid, cudaStream_t stream)
+qg_status cc_q45_dispatch(const CcArgs& a, const Q45Maps& maps, int grid, cudaStream_t stream, int M)
 {
     constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
     const int items8 = a.P * NGU * ((a.R + kCcRows - 1) / kCcRows) * 8;
-    if (items8 > kCcThreads / 2) return cc_q45_launch<BITS, EPI, 8, BITS_U>(a, maps, grid, stream);
-    return cc_q45_launch<BITS, EPI, 16, BITS_U>(a, maps, grid, stream);
+    if (M == 2) {
+        if (items8 > kCcThreads / 2) return cc_q45_launch<BITS, EPI, 8, BITS_U, 2>(a, maps, grid, stream);
+        return cc_q45_launch<BITS, EPI, 16, BITS_U, 2>(a, maps, grid, stream);
+    }
+    if (items8 > kCcThreads / 2) return cc_q45_launch<BITS, EPI, 8, BITS_U, 1>(a, maps, grid, stream);
+    return cc_q45_launch<BITS, EPI, 16, BITS_U, 1>(a, maps, grid, stream);
 }
 
 }  // namespace
@@ -722,7 +747,7 @@ qg_status launch_cc_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const vo
                               const void* x, void* y, int out_f32, const void* residual, int M, int N, int K,
                               cudaStream_t stream, const void* norm_w, float norm_eps)
 {
-    if (M != 1 || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
+    if (M < 1 || M > 2 || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
     if (sm_count(-1) <= 0) return QG_ERR_CUDA;
     const CcArgs a = q45_plan(x, y, out_f32, residual, N, 1, K, norm_w, norm_eps);
     const int grid = std::min(sm_count(-1), a.n_units);
@@ -730,11 +755,11 @@ qg_status launch_cc_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const vo
     if (!q45_maps(maps.m[0], q_lo, q_hi, scale, min, bits, N, K, a.R)) return QG_ERR_CUDA;
     maps.m[1][0] = maps.m[1][1] = maps.m[1][2] = maps.m[1][3] = maps.m[0][0];
     if (bits == 5) {
-        if (residual) return cc_q45_dispatch<5, EPI_RESID>(a, maps, grid, stream);
-        return cc_q45_dispatch<5, EPI_NONE>(a, maps, grid, stream);
+        if (residual) return cc_q45_dispatch<5, EPI_RESID>(a, maps, grid, stream, M);
+        return cc_q45_dispatch<5, EPI_NONE>(a, maps, grid, stream, M);
     }
-    if (residual) return cc_q45_dispatch<4, EPI_RESID>(a, maps, grid, stream);
-    return cc_q45_dispatch<4, EPI_NONE>(a, maps, grid, stream);
+    if (residual) return cc_q45_dispatch<4, EPI_RESID>(a, maps, grid, stream, M);
+    return cc_q45_dispatch<4, EPI_NONE>(a, maps, grid, stream, M);
 }
 
 // One-token SwiGLU over separate groupwise-int gate and up matrices (I rows
@@ -742,7 +767,7 @@ qg_status launch_cc_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const vo
 qg_status launch_cc_swiglu_q45(const Q45Matrix& gate, const Q45Matrix& up, const void* x, void* y, int M, int I,
                                int K, cudaStream_t stream, const void* norm_w, float norm_eps)
 {
-    if (M != 1 || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
+    if (M < 1 || M > 2 || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
     if (sm_count(-1) <= 0) return QG_ERR_CUDA;
     const CcArgs a = q45_plan(x, y, 0, nullptr, I, 2, K, norm_w, norm_eps);
     const int grid = std::min(sm_count(-1), a.n_units);
@@ -750,10 +775,10 @@ qg_status launch_cc_swiglu_q45(const Q45Matrix& gate, const Q45Matrix& up, const
     if (!q45_maps(maps.m[0], gate.q_lo, gate.q_hi, gate.scale, gate.min, gate.bits, I, K, a.R) ||
         !q45_maps(maps.m[1], up.q_lo, up.q_hi, up.scale, up.min, up.bits, I, K, a.R))
         return QG_ERR_CUDA;
-    if (gate.bits == 5 && up.bits == 4) return cc_q45_dispatch<5, EPI_SWIGLU, 4>(a, maps, grid, stream);
-    if (gate.bits == 5 && up.bits == 5) return cc_q45_dispatch<5, EPI_SWIGLU, 5>(a, maps, grid, stream);
-    if (gate.bits == 4 && up.bits == 5) return cc_q45_dispatch<4, EPI_SWIGLU, 5>(a, maps, grid, stream);
-    return cc_q45_dispatch<4, EPI_SWIGLU, 4>(a, maps, grid, stream);
+    if (gate.bits == 5 && up.bits == 4) return cc_q45_dispatch<5, EPI_SWIGLU, 4>(a, maps, grid, stream, M);
+    if (gate.bits == 5 && up.bits == 5) return cc_q45_dispatch<5, EPI_SWIGLU, 5>(a, maps, grid, stream, M);
+    if (gate.bits == 4 && up.bits == 5) return cc_q45_dispatch<4, EPI_SWIGLU, 5>(a, maps, grid, stream, M);
+    return cc_q45_dispatch<4, EPI_SWIGLU, 4>(a, maps, grid, stream, M);
 }
 
 }  // namespace qg

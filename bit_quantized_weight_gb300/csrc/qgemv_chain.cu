@@ -250,17 +250,18 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, int epi, uint8_
                     xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
                 }
                 const float gxs = gx[kc * NSEG + seg];
+                const float pe = pe_all[kc];
                 const bool bf = MIXED && fl[kc] != 0;
                 if (up_box) {
                     if (bf)
-                        cc_stage_q45<NSEG, BITS_U, true>(geom, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                        cc_stage_q45<NSEG, BITS_U, true>(geom, stage, b2, row0, seg, xw, &pe, &gxs, acc);
                     else
-                        cc_stage_q45<NSEG, BITS_U, false>(geom, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                        cc_stage_q45<NSEG, BITS_U, false>(geom, stage, b2, row0, seg, xw, &pe, &gxs, acc);
                 } else {
                     if (bf)
-                        cc_stage_q45<NSEG, BITS, true>(geom, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                        cc_stage_q45<NSEG, BITS, true>(geom, stage, b2, row0, seg, xw, &pe, &gxs, acc);
                     else
-                        cc_stage_q45<NSEG, BITS, false>(geom, stage, b2, row0, seg, xw, pe_all[kc], gxs, acc);
+                        cc_stage_q45<NSEG, BITS, false>(geom, stage, b2, row0, seg, xw, &pe, &gxs, acc);
                 }
             }
             mbar_arrive(&empty[slot]);

@@ -168,7 +168,7 @@ def test_q45(bits, M, N, K):
         check_out(y, yref, a, f"Q{bits} M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("M", [1, 4, 8])
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
 def test_q45_residual(M):
     N, K = 640, 1024
     w = synth.q45_weights(19, "qres", N, K, 5)
@@ -183,7 +183,7 @@ def test_q45_residual(M):
 
 
 @pytest.mark.parametrize("bits", [4, 5])
-@pytest.mark.parametrize("M", [3, 8])
+@pytest.mark.parametrize("M", [2, 3, 8])
 def test_q45_long_k(bits, M):
     """K = 17408 (68 stages): the stage ring wraps many times, and the
     activation copies of the first ring's stages are issued after the
@@ -200,8 +200,10 @@ def test_q45_long_k(bits, M):
 
 
 def test_q45_deterministic_and_row_independent():
-    """Q4/Q5 with 2..8 tokens: repeated calls are bit-identical and a token's
-    result does not depend on the other tokens of the call."""
+    """Q4/Q5 with 3..8 tokens (one arithmetic for all of them): repeated
+    calls are bit-identical and a token's result does not depend on the other
+    tokens of the call. One and two tokens take the CUDA-core kernel, whose
+    two-token results equal one-token calls (checked separately)."""
     M, N, K = 8, 700, 2048
     w = synth.q45_weights(33, "qdet", N, K, 5)
     x = synth.bf16_normal(34, "qdetx", (M, K))
@@ -215,8 +217,8 @@ def test_q45_deterministic_and_row_independent():
     y1, y2 = run(x), run(x)
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32)), "two runs differ"
     for m in (0, 6):
-        ym = run(np.stack([x[m], x[(m + 5) % M]]))
-        assert np.array_equal(ym[0].view(np.uint32), y1[m].view(np.uint32)), f"row {m}: M=2 call != M=8 call"
+        ym = run(np.stack([x[m], x[(m + 5) % M], x[(m + 3) % M]]))
+        assert np.array_equal(ym[0].view(np.uint32), y1[m].view(np.uint32)), f"row {m}: M=3 call != M=8 call"
 
 
 # ---------------------------------------------------------------- activations
@@ -307,18 +309,43 @@ def test_dense_layer_full_size(M):
     assert d27.hidden == 5120
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 2, 8])
 def test_mixed_q45_layer_full_size(M):
     for name, N, K, bits in synth.Q45_RECIPE:
         w = synth.q45_weights(3, f"q45.{name}", N, K, bits)
-        x = synth.bf16_normal(3, f"q45.{name}.x", (M, K)) if M == 8 else \
-            synth.bf16_normal(3, f"q45.{name}.x", (8, K))[:1]
+        x = synth.bf16_normal(3, f"q45.{name}.x", (8, K))[:M]
         yref, a = O.gemv_q45(w, x)
         d = q45_dev(w)
         y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         q.qgemv_q45(d["q_lo"], d["q_hi"], d["scale"], d["min"], bits, to_dev(x), y)
         torch.cuda.synchronize()
         check_out(y, yref, a, f"Q{bits} {name}")
+
+
+@pytest.mark.parametrize("bits", [4, 5])
+@pytest.mark.parametrize("residual", [False, True])
+def test_q45_two_tokens_match_one_token_calls(bits, residual):
+    """The two-token groupwise-int kernel decodes each code once for both
+    tokens but keeps their prescales, sums and epilogues apart: with
+    activations that prescale exactly, each token equals its own one-token
+    call bit for bit."""
+    N, K = 3001, 2560
+    w = synth.q45_weights(40 + bits, f"q2tok{bits}", N, K, bits)
+    x = synth.bf16_normal(41, "q2tokx", (2, K))
+    r = synth.bf16_normal(42, "q2tokr", (2, N)) if residual else None
+    d = q45_dev(w)
+    xd = to_dev(x)
+    rd = to_dev(r) if residual else None
+    y2 = torch.empty((2, N), dtype=torch.float32, device="cuda")
+    q.qgemv_q45(d["q_lo"], d["q_hi"], d["scale"], d["min"], bits, xd, y2, residual=rd)
+    for t in range(2):
+        y1 = torch.empty((1, N), dtype=torch.float32, device="cuda")
+        q.qgemv_q45(d["q_lo"], d["q_hi"], d["scale"], d["min"], bits, xd[t:t + 1].clone(), y1,
+                    residual=None if rd is None else rd[t:t + 1].clone())
+        torch.cuda.synchronize()
+        assert torch.equal(y1[0], y2[t]), f"token {t}: two-token call != one-token call"
+    yref, a = O.gemv_q45(w, x, residual=r)
+    check_out(y2, yref, a, f"Q{bits} two tokens")
 
 
 # ---------------------------------------------------------------- properties
@@ -397,9 +424,9 @@ def _q5_call(M, N, K, seed):
 
 
 # One case per pipelined kernel: the one-token CUDA-core NVFP4 and Q5
-# kernels, the tcgen05 kernel (NVFP4, 8 tokens) and the mma.sync
-# groupwise-int kernel (Q5, 8 tokens).
-STARVE_CASES = [("nvfp4", 1), ("nvfp4", 8), ("q5", 1), ("q5", 8)]
+# kernels, the two-token Q5 variant, the tcgen05 kernel (NVFP4, 8 tokens)
+# and the mma.sync groupwise-int kernel (Q5, 8 tokens).
+STARVE_CASES = [("nvfp4", 1), ("nvfp4", 8), ("q5", 1), ("q5", 2), ("q5", 8)]
 
 
 @pytest.mark.parametrize("fmt,M", STARVE_CASES)

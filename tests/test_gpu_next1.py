@@ -187,7 +187,7 @@ def test_swiglu_q45(gbits, ubits, M, norm):
     check_bf16(bits16(y), href, B, f"swiglu Q{gbits}/Q{ubits} M={M} norm={norm}")
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 2, 8])
 def test_swiglu_q45_config_shapes(M):
     """The recipe's FFN at full size: gate Q5 + up Q4, I = 17408, K = 5120,
     with the RMSNorm prologue."""
