@@ -162,10 +162,11 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-# Kernel sources behind each workload's launches (one token: the CUDA-core
-# kernels; NVFP4 with more tokens and the MoE: the tcgen05 kernel; Q4/Q5 with
-# more tokens: the mma.sync kernel); a committed traffic figure is used only
-# while these files are unchanged.
+# Kernel sources behind each workload's launches (one or two tokens: the
+# CUDA-core kernels; NVFP4 with more tokens and the MoE: the tcgen05 kernel;
+# Q4/Q5 with more tokens: the mma.sync kernel, and the exact fallback kernel
+# for the normalised and fused groupwise-int ops); a committed traffic figure
+# is used only while these files are unchanged.
 KERNEL_SOURCES = {
     "simple": ("qgemv_simple.cu", "common.cuh", "qgemv_internal.h"),
     "cc": ("qgemv_cc.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
@@ -179,9 +180,9 @@ KERNEL_SOURCES = {
 def kernel_family(workload, M):
     if workload == "moe":
         return "moe"
-    if workload == "q45ffn" and M > 1:
+    if workload == "q45ffn" and M > 2:
         return "simple"
-    if M == 1:
+    if M <= 2:
         return "cc"
     return "mma" if workload == "q45" else "tc"
 
@@ -379,7 +380,7 @@ class Workload:
             events[-1].record()
 
     def launches_per_step(self):
-        return 1 if (self.chains and self.M == 1) else len(self.projs)
+        return 1 if (self.chains and self.M <= 2) else len(self.projs)
 
     def alg_bytes(self, idx):
         """Algorithmic bytes of call idx: weights + activations in + outputs."""
@@ -679,9 +680,9 @@ def read_probe_bandwidth(torch, q, stream, peak, nbytes=2 << 30, reps=10):
 
 
 def arithmetic(workload, M):
-    if workload in ("dense", "tiny") and M == 1:
+    if workload in ("dense", "tiny") and M <= 2:
         return "f16 x f16 -> f32 FMA on CUDA cores (exact decoded weights, prescaled activations)"
-    if workload in ("q45", "q45ffn") and M == 1:
+    if workload in ("q45", "q45ffn") and M <= 2:
         return "f16 x f16 -> f32 FMA on CUDA cores (codes as exact f16, prescaled activations)"
     if workload == "q45ffn":
         return "fp32 FMA on CUDA cores (exact fallback kernel for the normalised and fused ops), bf16 mma.sync for the rest"
@@ -811,7 +812,7 @@ def measure(args, kind, M, world, rank, stream, cpu=True, e2e=True):
     alone = {"kernel": dom_name, "achieved": achieved, "frac": achieved / peak, "alg_bytes_per_launch": wl.alg_bytes(dom),
              "us_per_launch": dom_us, "traffic": traffic,
              "timing": "the projection alone, K launches in one CUDA graph, events on its stream"}
-    if chained and M == 1:
+    if chained and M <= 2:
         # the step is one launch of the chained-layer kernel: it is the
         # dominant (only) kernel, timed by the headline graph itself
         step_bytes = sum(wl.alg_bytes(i) for i in range(n_calls))
@@ -921,7 +922,7 @@ def main():
             "config": {"workload": head["workload"], "M": args.M,
                        "weight_bytes_per_step": head["weight_bytes_per_step"], "l2": head["l2"],
                        "parallelism": "one independent replica per GPU" if world > 1 else "single GPU",
-                       "step": "one qgemv_chain call (the layer's projections; one persistent launch at M = 1)"
+                       "step": "one qgemv_chain call (the layer's projections; one persistent launch at M <= 2)"
                                if head["chained"] else "one library call per projection",
                        "graph": "K steps captured in one CUDA graph (kernels only); us_per_call from a "
                                 "second graph with events between the calls (which serialise them)"},

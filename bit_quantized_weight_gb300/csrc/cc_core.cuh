@@ -369,6 +369,78 @@ __device__ __forceinline__ void cc_stage(const CcGeom& a, uint32_t stage, int b2
     for (int i = 0; i < kCcRows; ++i) acc[i] = fmaf(u[i], pe, acc[i]);
 }
 
+// cc_stage for MT tokens: each decoded code pair feeds every token; token
+// t's activation pieces are read from shared memory at xc + t * x_tok as
+// the code words come (the same lds count as cc_stage, fewer live
+// registers), its factor is pe[t], its sums acc[i * MT + t].
+template <int NSEG, bool BF, int MT>
+__device__ __forceinline__ void cc_stage_mt(const CcGeom& a, uint32_t stage, int b2, int row0, int seg,
+                                            uint32_t xc, uint32_t x_tok, const float* pe,
+                                            float (&acc)[kCcRows * MT])
+{
+    constexpr int KS = kChunkK / NSEG;
+    constexpr int NW = KS / 8;
+    constexpr int NB = NW / 2;
+    uint32_t cw[kCcRows][NW];
+    float sc[kCcRows][NB];
+#pragma unroll
+    for (int i = 0; i < kCcRows; ++i) {
+        const int r = row0 + i;
+        const uint32_t rowb = stage + static_cast<uint32_t>(b2 * a.R8 + r) * 128u;
+        const uint32_t chunk = static_cast<uint32_t>((NW == 4 ? seg : seg >> 1) ^ (r & 7));
+        if constexpr (NW == 4) {
+            const uint4 v = lds128(rowb + (chunk << 4));
+            cw[i][0] = v.x; cw[i][1] = v.y; cw[i][2] = v.z; cw[i][3] = v.w;
+        } else {
+            const uint2 v = lds64(rowb + (chunk << 4) + static_cast<uint32_t>(seg & 1) * 8u);
+            cw[i][0] = v.x; cw[i][1] = v.y;
+        }
+        const uint32_t sb = stage + a.scales_off + static_cast<uint32_t>((b2 * a.R8 + r) * 16 + seg * NB);
+        const uint32_t two = NB == 2 ? lds16(sb) : lds8(sb);
+        const uint32_t h2 = e4m3x2_to_f16x2(two);
+        sc[i][0] = half_bits_to_f32(h2 & 0xFFFFu);
+        if constexpr (NB == 2) sc[i][1] = half_bits_to_f32(h2 >> 16);
+    }
+    float u[kCcRows * MT];
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk) {
+        float s[kCcRows * MT];
+#pragma unroll
+        for (int i = 0; i < kCcRows * MT; ++i) s[i] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int wd = 2 * blk + h;
+            uint32_t w[kCcRows][4];
+#pragma unroll
+            for (int i = 0; i < kCcRows; ++i) {
+                e2m1x8_to_f16x2x4(cw[i][wd], w[i]);
+                if (BF) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) w[i][j] = f16x2_to_bf16x2(w[i][j]);
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                const uint4 v = lds128(xc + t * x_tok + wd * NSEG * 16);
+                const uint32_t xv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int i = 0; i < kCcRows; ++i) s[i * MT + t] = fma2_mixed<BF>(w[i][j], xv[j], s[i * MT + t]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kCcRows; ++i)
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+                u[i * MT + t] = blk == 0 ? s[i * MT + t] * sc[i][0] : fmaf(s[i * MT + t], sc[i][blk], u[i * MT + t]);
+    }
+#pragma unroll
+    for (int i = 0; i < kCcRows; ++i)
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[i * MT + t] = fmaf(u[i * MT + t], pe[t], acc[i * MT + t]);
+}
+
 // ---------------------------------------------------------------- groupwise int (Q4 / Q5)
 // Same plan for w = scale * q + min per group of 32 (NInfer article, section
 // 2: the groupwise-int recipe): per row and group, y += scale * sum(q x) +
@@ -386,7 +458,9 @@ __device__ __forceinline__ void cc_stage(const CcGeom& a, uint32_t stage, int b2
 // pe[t * C + kc], its segment sums at gx[(t * C + kc) * NSEG + s]; a chunk
 // that one token cannot carry exactly in f16 stays raw bf16 for every token
 // (one flag per chunk), so a stage runs one arithmetic for all of them.
-template <int NSEG, int SRC = XSRC_NC, int NW = kCcWarps, int MT = 1>
+// Q45 = false gives the NVFP4 layout of the multi-token NVFP4 kernel:
+// natural pairs, no segment sums.
+template <int NSEG, int SRC = XSRC_NC, int NW = kCcWarps, int MT = 1, bool Q45 = true>
 __device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lane, volatile int* any_bf)
 {
     constexpr int kBatch = MT == 2 ? 3 : (NW < kCcWarps ? 8 : 5);
@@ -459,11 +533,13 @@ __device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lan
             for (int t = 0; t < MT; ++t) {
                 const uint32_t wv[4] = {raw[t][u].x, raw[t][u].y, raw[t][u].z, raw[t][u].w};
                 float sx = 0.f;
+                if constexpr (Q45) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    sx += bf16_bits_to_f32((i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu));
+                    for (int i = 0; i < 8; ++i)
+                        sx += bf16_bits_to_f32((i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu));
 #pragma unroll
-                for (int sh = 1; sh < PPS; sh <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, sh);
+                    for (int sh = 1; sh < PPS; sh <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, sh);
+                }
                 uint32_t o[4];
                 if (inexact) {
 #pragma unroll
@@ -474,12 +550,17 @@ __device__ void cc_convert_q45(const CcArgs& a, uint8_t* smem, int warp, int lan
                     for (int i = 0; i < 4; ++i)
                         o[i] = pack_f16x2(__uint_as_float(wv[i] << 16) * sc, __uint_as_float(wv[i] & 0xFFFF0000u) * sc);
                 }
-                // natural pairs (x0,x1)(x2,x3)(x4,x5)(x6,x7) -> (x0,x4)(x1,x5)(x2,x6)(x3,x7)
-                const uint32_t p0 = __byte_perm(o[0], o[2], 0x5410), p1 = __byte_perm(o[0], o[2], 0x7632);
-                const uint32_t p2 = __byte_perm(o[1], o[3], 0x5410), p3 = __byte_perm(o[1], o[3], 0x7632);
                 const int off = (lane % PPS) * NSEG * 4 + (lane / PPS) * 4;
-                *reinterpret_cast<uint4*>(xs + (t * a.C + kc) * (kChunkK / 2) + off) = make_uint4(p0, p1, p2, p3);
-                if (lane % PPS == 0) gx[(t * a.C + kc) * NSEG + lane / PPS] = sx;
+                uint32_t* dst = xs + (t * a.C + kc) * (kChunkK / 2) + off;
+                if constexpr (Q45) {
+                    // natural pairs (x0,x1)(x2,x3)(x4,x5)(x6,x7) -> (x0,x4)(x1,x5)(x2,x6)(x3,x7)
+                    const uint32_t p0 = __byte_perm(o[0], o[2], 0x5410), p1 = __byte_perm(o[0], o[2], 0x7632);
+                    const uint32_t p2 = __byte_perm(o[1], o[3], 0x5410), p3 = __byte_perm(o[1], o[3], 0x7632);
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(p0, p1, p2, p3);
+                    if (lane % PPS == 0) gx[(t * a.C + kc) * NSEG + lane / PPS] = sx;
+                } else {
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
                 if (lane == 0) pe[t * a.C + kc] = inexact ? 1.0f : __int_as_float((127 - e[t]) << 23);
             }
             if (lane == 0) {

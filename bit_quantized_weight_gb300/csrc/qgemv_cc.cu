@@ -43,8 +43,9 @@ namespace {
 
 // The compute warps' unit loop. MIXED: some chunk of x stayed raw bf16, so
 // each stage picks the f16 or the bf16 stage code; otherwise the loop holds
-// the f16 stage code alone.
-template <int EPI, int NSEG, bool MIXED>
+// the f16 stage code alone. MT tokens (1 or 2) share every decoded code;
+// token t's outputs and residuals start t * n_out into y and residual.
+template <int EPI, int NSEG, bool MIXED, int MT = 1>
 __device__ __forceinline__ void cc_units(const CcArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                          volatile int* abort_flag)
 {
@@ -70,32 +71,49 @@ __device__ __forceinline__ void cc_units(const CcArgs& a, uint8_t* smem, uint64_
     const int n_mine = active ? max(0, (a.C - p + a.P - 1) / a.P) : 0;
     const uint32_t x0 = smem_u32(xs + p * (kChunkK / 2) + seg * 4);
     const uint32_t x_step = static_cast<uint32_t>(a.P) * (kChunkK * 2u);
+    const uint32_t x_tok = static_cast<uint32_t>(a.C) * (kChunkK * 2u);  // bytes per token's activations
 
     // residual of the first unit's rows, read now rather than in the epilogue
-    float res_first = 0.f;
-    if (EPI == EPI_RESID && threadIdx.x < a.R && blockIdx.x * a.R + static_cast<int>(threadIdx.x) < a.n_out)
-        res_first = bf16_bits_to_f32(a.residual[blockIdx.x * a.R + threadIdx.x]);
+    float res_first[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        res_first[t] = 0.f;
+        if (EPI == EPI_RESID && threadIdx.x < a.R && blockIdx.x * a.R + static_cast<int>(threadIdx.x) < a.n_out)
+            res_first[t] = bf16_bits_to_f32(a.residual[t * a.n_out + blockIdx.x * a.R + threadIdx.x]);
+    }
 
     bool aborted = false;
     int slot = 0, lap = 0;
     for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
-        float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
+        float acc[kCcRows * MT];
+#pragma unroll
+        for (int i = 0; i < kCcRows * MT; ++i) acc[i] = 0.f;
         for (int c = 0; c < a.Cp; ++c) {
             if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
             if (!aborted && c < n_mine) {
                 const uint32_t stage = ring + slot * a.stage_bytes;
-                uint32_t xw[KS / 2];
                 const uint32_t xc = x0 + static_cast<uint32_t>(c) * x_step;
-#pragma unroll
-                for (int i = 0; i < KS / 8; ++i) {
-                    const uint4 v = lds128(xc + i * NSEG * 16);
-                    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
-                }
                 const int kc = c * a.P + p;
-                if (!MIXED || fl[kc] == 0)
-                    cc_stage<NSEG, false>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], acc);
-                else
-                    cc_stage<NSEG, true>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], acc);
+                if constexpr (MT == 1) {
+                    uint32_t xw[KS / 2];
+#pragma unroll
+                    for (int i = 0; i < KS / 8; ++i) {
+                        const uint4 v = lds128(xc + i * NSEG * 16);
+                        xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
+                    }
+                    if (!MIXED || fl[kc] == 0)
+                        cc_stage<NSEG, false>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], acc);
+                    else
+                        cc_stage<NSEG, true>(cc_geom(a), stage, b2, row0, seg, xw, pe_all[kc], acc);
+                } else {
+                    float pe[MT];
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) pe[t] = pe_all[t * a.C + kc];
+                    if (!MIXED || fl[kc] == 0)
+                        cc_stage_mt<NSEG, false, MT>(cc_geom(a), stage, b2, row0, seg, xc, x_tok, pe, acc);
+                    else
+                        cc_stage_mt<NSEG, true, MT>(cc_geom(a), stage, b2, row0, seg, xc, x_tok, pe, acc);
+                }
             }
             // every compute thread arrives: its own reads of the slot are done
             mbar_arrive(&empty[slot]);
@@ -108,42 +126,48 @@ __device__ __forceinline__ void cc_units(const CcArgs& a, uint8_t* smem, uint64_
         // ---------------- fixed-order reduction over segments (a butterfly
         // across the segment lanes of the warp) and phases, epilogue
 #pragma unroll
-        for (int i = 0; i < kCcRows; ++i)
+        for (int i = 0; i < kCcRows * MT; ++i)
 #pragma unroll
             for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
         if (active && seg == 0) {
 #pragma unroll
-            for (int i = 0; i < kCcRows; ++i) red[b2 * a.R8 + row0 + i] = acc[i];
+            for (int i = 0; i < kCcRows; ++i)
+#pragma unroll
+                for (int t = 0; t < MT; ++t) red[(b2 * a.R8 + row0 + i) * MT + t] = acc[i * MT + t];
         }
         named_barrier_sync(1, kCcThreads);
         if (!aborted) {
             const int r0 = u * a.R;
             for (int r = threadIdx.x; r < a.R; r += kCcThreads) {
                 if (r0 + r >= a.n_out) break;
-                float v[NGU];
 #pragma unroll
-                for (int gg = 0; gg < NGU; ++gg) {
-                    float s = 0.f;
-                    for (int pp = 0; pp < a.P; ++pp) s += red[(pp * NGU + gg) * a.R8 + r];
-                    v[gg] = s * a.g;
+                for (int t = 0; t < MT; ++t) {
+                    float v[NGU];
+#pragma unroll
+                    for (int gg = 0; gg < NGU; ++gg) {
+                        float s = 0.f;
+                        for (int pp = 0; pp < a.P; ++pp) s += red[((pp * NGU + gg) * a.R8 + r) * MT + t];
+                        v[gg] = s * a.g;
+                    }
+                    float val = v[0];
+                    if (EPI == EPI_SWIGLU) val = (val / (1.0f + expf(-val))) * v[NGU - 1];
+                    const int o = t * a.n_out + r0 + r;
+                    if (EPI == EPI_RESID)
+                        val += u == static_cast<int>(blockIdx.x) && r == static_cast<int>(threadIdx.x)
+                                   ? res_first[t]
+                                   : bf16_bits_to_f32(a.residual[o]);
+                    if (a.out_f32)
+                        reinterpret_cast<float*>(a.y)[o] = val;
+                    else
+                        reinterpret_cast<uint16_t*>(a.y)[o] = f32_to_bf16_bits_rn(val);
                 }
-                float val = v[0];
-                if (EPI == EPI_SWIGLU) val = (val / (1.0f + expf(-val))) * v[NGU - 1];
-                if (EPI == EPI_RESID)
-                    val += u == static_cast<int>(blockIdx.x) && r == static_cast<int>(threadIdx.x)
-                               ? res_first
-                               : bf16_bits_to_f32(a.residual[r0 + r]);
-                if (a.out_f32)
-                    reinterpret_cast<float*>(a.y)[r0 + r] = val;
-                else
-                    reinterpret_cast<uint16_t*>(a.y)[r0 + r] = f32_to_bf16_bits_rn(val);
             }
         }
         named_barrier_sync(1, kCcThreads);  // red is rewritten by the next unit
     }
 }
 
-template <int EPI, int NSEG>
+template <int EPI, int NSEG, int MT>
 __global__ void __launch_bounds__(kCcAllThreads, 1)
     cc_gemv_kernel(const __grid_constant__ CcArgs a, const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales)
@@ -230,12 +254,15 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
         cc_zero_padding(a, smem, a.P * NGU, roff, rbytes, 2);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    cc_convert<NSEG>(a, smem, warp, lane, any_bf);
+    if constexpr (MT == 1)
+        cc_convert<NSEG>(a, smem, warp, lane, any_bf);
+    else
+        cc_convert_q45<NSEG, XSRC_NC, kCcWarps, MT, false>(a, smem, warp, lane, any_bf);
     named_barrier_sync(1, kCcThreads);
     if (*any_bf)
-        cc_units<EPI, NSEG, true>(a, smem, full, empty, abort_flag);
+        cc_units<EPI, NSEG, true, MT>(a, smem, full, empty, abort_flag);
     else
-        cc_units<EPI, NSEG, false>(a, smem, full, empty, abort_flag);
+        cc_units<EPI, NSEG, false, MT>(a, smem, full, empty, abort_flag);
 }
 
 // The compute warps' unit loop of the groupwise-int kernel (MIXED as in
@@ -482,7 +509,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
 
 constexpr uint32_t align_up(uint32_t v, uint32_t al) { return (v + al - 1) / al * al; }
 
-template <int EPI, int NSEG>
+template <int EPI, int NSEG, int MT>
 qg_status cc_launch(CcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, int grid, cudaStream_t stream)
 {
     constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
@@ -496,11 +523,11 @@ qg_status cc_launch(CcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
     a.scales_off = nbox * a.R8 * 128u;
     a.stage_bytes = align_up(a.scales_off + nbox * a.R8 * 16u, 1024);
     a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
-    const uint32_t x_bytes = static_cast<uint32_t>(a.C) * kChunkK * 2u;
-    const uint32_t pe_bytes = align_up(static_cast<uint32_t>(a.C) * 4u, 16);
+    const uint32_t x_bytes = static_cast<uint32_t>(MT * a.C) * kChunkK * 2u;
+    const uint32_t pe_bytes = align_up(static_cast<uint32_t>(MT * a.C) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(a.C), 16);
-    const uint32_t ss_bytes = a.norm_w ? align_up(static_cast<uint32_t>(a.C) * 4u, 16) : 0u;
-    const uint32_t red_bytes = align_up(nbox * a.R8 * 4u, 128);
+    const uint32_t ss_bytes = a.norm_w ? align_up(static_cast<uint32_t>(MT * a.C) * 4u, 16) : 0u;
+    const uint32_t red_bytes = align_up(nbox * a.R8 * 4u * MT, 128);
     const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
     const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + ss_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
@@ -523,7 +550,7 @@ qg_status cc_launch(CcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
     so += bar_bytes;
     if (so > kCcSmemMax) return QG_ERR_UNSUPPORTED;
 
-    auto kern = cc_gemv_kernel<EPI, NSEG>;
+    auto kern = cc_gemv_kernel<EPI, NSEG, MT>;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
@@ -548,13 +575,17 @@ qg_status cc_launch(CcArgs a, const CUtensorMap& tmc, const CUtensorMap& tms, in
 
 template <int EPI>
 qg_status cc_dispatch(const CcArgs& a, const CUtensorMap& tmc, const CUtensorMap& tms, int grid,
-                      cudaStream_t stream)
+                      cudaStream_t stream, int M)
 {
     constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
     // 8 segments of 32 k when the rows fill 16 warps that way, else 16 of 16 k
     const int items8 = a.P * NGU * ((a.R + kCcRows - 1) / kCcRows) * 8;
-    if (items8 > kCcThreads / 2) return cc_launch<EPI, 8>(a, tmc, tms, grid, stream);
-    return cc_launch<EPI, 16>(a, tmc, tms, grid, stream);
+    if (M == 2) {
+        if (items8 > kCcThreads / 2) return cc_launch<EPI, 8, 2>(a, tmc, tms, grid, stream);
+        return cc_launch<EPI, 16, 2>(a, tmc, tms, grid, stream);
+    }
+    if (items8 > kCcThreads / 2) return cc_launch<EPI, 8, 1>(a, tmc, tms, grid, stream);
+    return cc_launch<EPI, 16, 1>(a, tmc, tms, grid, stream);
 }
 
 template <int BITS, int EPI, int NSEG, int BITS_U, int MT>
@@ -650,7 +681,7 @@ qg_status launch_cc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, flo
                                 int out_f32, const void* residual, int M, int N, int K, int swiglu,
                                 cudaStream_t stream, const void* norm_w, float norm_eps)
 {
-    if (M != 1 || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
+    if (M < 1 || M > 2 || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
     const int ngu = swiglu ? 2 : 1;
     const int n_out = swiglu ? N / 2 : N;
     const int sms = sm_count(-1);
@@ -688,9 +719,9 @@ qg_status launch_cc_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, flo
     if (!encode_tmap_2d(&tmc, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, R, true) ||
         !encode_tmap_2d(&tms, scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 16, N, 16, R, false))
         return QG_ERR_CUDA;
-    if (swiglu) return cc_dispatch<EPI_SWIGLU>(a, tmc, tms, grid, stream);
-    if (residual) return cc_dispatch<EPI_RESID>(a, tmc, tms, grid, stream);
-    return cc_dispatch<EPI_NONE>(a, tmc, tms, grid, stream);
+    if (swiglu) return cc_dispatch<EPI_SWIGLU>(a, tmc, tms, grid, stream, M);
+    if (residual) return cc_dispatch<EPI_RESID>(a, tmc, tms, grid, stream, M);
+    return cc_dispatch<EPI_NONE>(a, tmc, tms, grid, stream, M);
 }
 
 namespace {

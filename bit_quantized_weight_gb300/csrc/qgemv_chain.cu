@@ -1,5 +1,5 @@
-// qgemv_chain.cu -- the one-token projections of a decode layer in one
-// persistent launch.
+// qgemv_chain.cu -- the one- or two-token projections of a decode layer in
+// one persistent launch.
 //
 // Decode engines replay one fixed sequence of projections per layer (NInfer
 // article, section 1: one CUDA graph per batch size; Decapybara README,
@@ -13,7 +13,7 @@
 // of op after op into one shared-memory ring without stopping at an op
 // boundary (weights never depend on earlier outputs), so the next op's first
 // stages are already in flight while the compute warps finish the current op.
-// The compute warps run each op exactly as the one-token kernels of
+// The compute warps run each op exactly as the one- and two-token kernels of
 // qgemv_cc.cu do (same units, phases, exact activation conversion and
 // fixed-order reductions, so results are identical to separate calls): they
 // convert the op's activations into shared memory, stream its units and
@@ -34,7 +34,7 @@ constexpr int kChainMaxOps = 8;
 constexpr int kChainNseg = 8;   // 32-k segments (always valid: at most 256 rows per stage)
 
 struct ChainOp {
-    CcArgs a;   // the op's plan, as the standalone one-token kernel would use it
+    CcArgs a;   // the op's plan, as the standalone kernel would use it
     int fmt;    // FMT_NVFP4, FMT_Q4, FMT_Q5 (the gate matrix of a SwiGLU)
     int epi;    // EPI_NONE, EPI_RESID, EPI_SWIGLU
     int dep;    // grid-wide barrier before the op reads its inputs
@@ -108,7 +108,7 @@ __device__ __forceinline__ void chain_store(const CcArgs& a, int idx, float val)
 // the ring position carried across ops, coherent residual loads, and the
 // epilogue chosen at run time: it only runs after a unit's stage loop, and one
 // loop copy for all epilogues keeps the kernel's code small).
-template <bool MIXED>
+template <bool MIXED, int MT>
 __device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, int epi, uint8_t* smem, uint32_t ring,
                                                   uint32_t slot_bytes, int n_stages, uint64_t* full,
                                                   uint64_t* empty, volatile int* abort_flag, bool& aborted,
@@ -137,30 +137,46 @@ __device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, int epi, uint
     const int n_mine = active ? max(0, (C - p + P - 1) / P) : 0;
     const uint32_t x0 = smem_u32(xs + p * (kChunkK / 2) + seg * 4);
     const uint32_t x_step = static_cast<uint32_t>(P) * (kChunkK * 2u);
-
+    const uint32_t x_tok = static_cast<uint32_t>(C) * (kChunkK * 2u);
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
+        float acc[kCcRows * MT];
+#pragma unroll
+        for (int i = 0; i < kCcRows * MT; ++i) acc[i] = 0.f;
         // the unit's residuals, read while its stages stream
-        float res = 0.f;
+        float res[MT];
         const int r0 = u * R;
-        if (resid && threadIdx.x < R && r0 + static_cast<int>(threadIdx.x) < n_out)
-            res = bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + threadIdx.x));
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            res[t] = 0.f;
+            if (resid && threadIdx.x < R && r0 + static_cast<int>(threadIdx.x) < n_out)
+                res[t] = bf16_bits_to_f32(ldg_cg_u16(a.residual + t * n_out + r0 + threadIdx.x));
+        }
         for (int c = 0; c < Cp; ++c) {
             if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
             if (!aborted && c < n_mine) {
                 const uint32_t stage = ring + slot * slot_bytes;
-                uint32_t xw[KS / 2];
                 const uint32_t xc = x0 + static_cast<uint32_t>(c) * x_step;
-#pragma unroll
-                for (int i = 0; i < KS / 8; ++i) {
-                    const uint4 v = lds128(xc + i * NSEG * 16);
-                    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
-                }
                 const int kc = c * P + p;
-                if (!MIXED || fl[kc] == 0)
-                    cc_stage<NSEG, false>(geom, stage, b2, row0, seg, xw, pe_all[kc], acc);
-                else
-                    cc_stage<NSEG, true>(geom, stage, b2, row0, seg, xw, pe_all[kc], acc);
+                if constexpr (MT == 1) {
+                    uint32_t xw[KS / 2];
+#pragma unroll
+                    for (int i = 0; i < KS / 8; ++i) {
+                        const uint4 v = lds128(xc + i * NSEG * 16);
+                        xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
+                    }
+                    if (!MIXED || fl[kc] == 0)
+                        cc_stage<NSEG, false>(geom, stage, b2, row0, seg, xw, pe_all[kc], acc);
+                    else
+                        cc_stage<NSEG, true>(geom, stage, b2, row0, seg, xw, pe_all[kc], acc);
+                } else {
+                    float pe[MT];
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) pe[t] = pe_all[t * C + kc];
+                    if (!MIXED || fl[kc] == 0)
+                        cc_stage_mt<NSEG, false, MT>(geom, stage, b2, row0, seg, xc, x_tok, pe, acc);
+                    else
+                        cc_stage_mt<NSEG, true, MT>(geom, stage, b2, row0, seg, xc, x_tok, pe, acc);
+                }
             }
             mbar_arrive(&empty[slot]);
             if (++slot == n_stages) {
@@ -169,30 +185,36 @@ __device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, int epi, uint
             }
         }
 #pragma unroll
-        for (int i = 0; i < kCcRows; ++i)
+        for (int i = 0; i < kCcRows * MT; ++i)
 #pragma unroll
             for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
         if (active && seg == 0) {
 #pragma unroll
-            for (int i = 0; i < kCcRows; ++i) red[b2 * geom.R8 + row0 + i] = acc[i];
+            for (int i = 0; i < kCcRows; ++i)
+#pragma unroll
+                for (int t = 0; t < MT; ++t) red[(b2 * geom.R8 + row0 + i) * MT + t] = acc[i * MT + t];
         }
         named_barrier_sync(1, kCcThreads);
         if (!aborted) {
             for (int r = threadIdx.x; r < R; r += kCcThreads) {
                 if (r0 + r >= n_out) break;
-                float v0 = 0.f, v1 = 0.f;
-                for (int pp = 0; pp < P; ++pp) v0 += red[((pp << gsh)) * geom.R8 + r];
-                v0 *= gscale;
-                float val = v0;
-                if (swiglu) {
-                    for (int pp = 0; pp < P; ++pp) v1 += red[((pp << gsh) + 1) * geom.R8 + r];
-                    v1 *= gscale;
-                    val = (v0 / (1.0f + expf(-v0))) * v1;
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    float v0 = 0.f, v1 = 0.f;
+                    for (int pp = 0; pp < P; ++pp) v0 += red[((pp << gsh) * geom.R8 + r) * MT + t];
+                    v0 *= gscale;
+                    float val = v0;
+                    if (swiglu) {
+                        for (int pp = 0; pp < P; ++pp) v1 += red[(((pp << gsh) + 1) * geom.R8 + r) * MT + t];
+                        v1 *= gscale;
+                        val = (v0 / (1.0f + expf(-v0))) * v1;
+                    }
+                    const int o = t * n_out + r0 + r;
+                    if (resid)
+                        val += r == static_cast<int>(threadIdx.x) ? res[t]
+                                                                  : bf16_bits_to_f32(ldg_cg_u16(a.residual + o));
+                    chain_store(a, o, val);
                 }
-                if (resid)
-                    val += r == static_cast<int>(threadIdx.x) ? res
-                                                              : bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + r));
-                chain_store(a, r0 + r, val);
             }
         }
         named_barrier_sync(1, kCcThreads);
@@ -202,7 +224,7 @@ __device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, int epi, uint
 // The unit loop of one groupwise-int op (cc_q45_units of qgemv_cc.cu, as
 // above): the epilogue at run time; SwiGLU reads a gate box (BITS) and an up
 // box (BITS_U) per phase.
-template <int BITS, int BITS_U, bool MIXED>
+template <int BITS, int BITS_U, bool MIXED, int MT>
 __device__ __forceinline__ void chain_units_q45(const CcArgs& a, int epi, uint8_t* smem, uint32_t ring,
                                                 uint32_t slot_bytes, int n_stages, uint64_t* full, uint64_t* empty,
                                                 volatile int* abort_flag, bool& aborted, int& slot, int& lap)
@@ -230,38 +252,50 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, int epi, uint8_
     const int n_mine = active ? max(0, (C - p + P - 1) / P) : 0;
     const uint32_t x0 = smem_u32(xs + p * (kChunkK / 2) + seg * 4);
     const uint32_t x_step = static_cast<uint32_t>(P) * (kChunkK * 2u);
-
+    const uint32_t x_tok = static_cast<uint32_t>(C) * (kChunkK * 2u);
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        float acc[kCcRows] = {0.f, 0.f, 0.f, 0.f};
-        float res = 0.f;
+        float acc[kCcRows * MT];
+#pragma unroll
+        for (int i = 0; i < kCcRows * MT; ++i) acc[i] = 0.f;
+        // the unit's residuals, read while its stages stream
+        float res[MT];
         const int r0 = u * R;
-        if (resid && threadIdx.x < R && r0 + static_cast<int>(threadIdx.x) < n_out)
-            res = bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + threadIdx.x));
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            res[t] = 0.f;
+            if (resid && threadIdx.x < R && r0 + static_cast<int>(threadIdx.x) < n_out)
+                res[t] = bf16_bits_to_f32(ldg_cg_u16(a.residual + t * n_out + r0 + threadIdx.x));
+        }
         for (int c = 0; c < Cp; ++c) {
             if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
             if (!aborted && c < n_mine) {
                 const int kc = c * P + p;
                 const uint32_t stage = ring + slot * slot_bytes;
-                uint32_t xw[KS / 2];
+                uint32_t xw[MT * (KS / 2)];
                 const uint32_t xc = x0 + static_cast<uint32_t>(c) * x_step;
+                float pe[MT], gxs[MT];
 #pragma unroll
-                for (int i = 0; i < KS / 8; ++i) {
-                    const uint4 v = lds128(xc + i * NSEG * 16);
-                    xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
+                for (int t = 0; t < MT; ++t) {
+#pragma unroll
+                    for (int i = 0; i < KS / 8; ++i) {
+                        const uint4 v = lds128(xc + t * x_tok + i * NSEG * 16);
+                        uint32_t* d = xw + t * (KS / 2) + 4 * i;
+                        d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+                    }
+                    gxs[t] = gx[(t * C + kc) * NSEG + seg];
+                    pe[t] = pe_all[t * C + kc];
                 }
-                const float gxs = gx[kc * NSEG + seg];
-                const float pe = pe_all[kc];
                 const bool bf = MIXED && fl[kc] != 0;
                 if (up_box) {
                     if (bf)
-                        cc_stage_q45<NSEG, BITS_U, true>(geom, stage, b2, row0, seg, xw, &pe, &gxs, acc);
+                        cc_stage_q45<NSEG, BITS_U, true, MT>(geom, stage, b2, row0, seg, xw, pe, gxs, acc);
                     else
-                        cc_stage_q45<NSEG, BITS_U, false>(geom, stage, b2, row0, seg, xw, &pe, &gxs, acc);
+                        cc_stage_q45<NSEG, BITS_U, false, MT>(geom, stage, b2, row0, seg, xw, pe, gxs, acc);
                 } else {
                     if (bf)
-                        cc_stage_q45<NSEG, BITS, true>(geom, stage, b2, row0, seg, xw, &pe, &gxs, acc);
+                        cc_stage_q45<NSEG, BITS, true, MT>(geom, stage, b2, row0, seg, xw, pe, gxs, acc);
                     else
-                        cc_stage_q45<NSEG, BITS, false>(geom, stage, b2, row0, seg, xw, &pe, &gxs, acc);
+                        cc_stage_q45<NSEG, BITS, false, MT>(geom, stage, b2, row0, seg, xw, pe, gxs, acc);
                 }
             }
             mbar_arrive(&empty[slot]);
@@ -271,59 +305,69 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, int epi, uint8_
             }
         }
 #pragma unroll
-        for (int i = 0; i < kCcRows; ++i)
+        for (int i = 0; i < kCcRows * MT; ++i)
 #pragma unroll
             for (int off = NSEG / 2; off >= 1; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
         if (active && seg == 0) {
 #pragma unroll
-            for (int i = 0; i < kCcRows; ++i) red[b2 * geom.R8 + row0 + i] = acc[i];
+            for (int i = 0; i < kCcRows; ++i)
+#pragma unroll
+                for (int t = 0; t < MT; ++t) red[(b2 * geom.R8 + row0 + i) * MT + t] = acc[i * MT + t];
         }
         named_barrier_sync(1, kCcThreads);
         if (!aborted) {
             for (int r = threadIdx.x; r < R; r += kCcThreads) {
                 if (r0 + r >= n_out) break;
-                float val = 0.f;
-                for (int pp = 0; pp < P; ++pp) val += red[(pp << gsh) * geom.R8 + r];
-                if (swiglu) {
-                    float v1 = 0.f;
-                    for (int pp = 0; pp < P; ++pp) v1 += red[((pp << gsh) + 1) * geom.R8 + r];
-                    val = (val / (1.0f + expf(-val))) * v1;
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    float val = 0.f;
+                    for (int pp = 0; pp < P; ++pp) val += red[((pp << gsh) * geom.R8 + r) * MT + t];
+                    if (swiglu) {
+                        float v1 = 0.f;
+                        for (int pp = 0; pp < P; ++pp) v1 += red[(((pp << gsh) + 1) * geom.R8 + r) * MT + t];
+                        val = (val / (1.0f + expf(-val))) * v1;
+                    }
+                    const int o = t * n_out + r0 + r;
+                    if (resid)
+                        val += r == static_cast<int>(threadIdx.x) ? res[t]
+                                                                  : bf16_bits_to_f32(ldg_cg_u16(a.residual + o));
+                    chain_store(a, o, val);
                 }
-                if (resid)
-                    val += r == static_cast<int>(threadIdx.x) ? res
-                                                              : bf16_bits_to_f32(ldg_cg_u16(a.residual + r0 + r));
-                chain_store(a, r0 + r, val);
             }
         }
         named_barrier_sync(1, kCcThreads);
     }
 }
 
+template <int MT>
 __device__ __forceinline__ void chain_nvfp4(const CcArgs& a, int epi, bool mixed, uint8_t* smem, uint32_t ring,
                                             uint32_t slot_bytes, int n_stages, uint64_t* full, uint64_t* empty,
                                             volatile int* abort_flag, bool& aborted, int& slot, int& lap)
 {
     if (mixed)
-        chain_units_nvfp4<true>(a, epi, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted, slot,
+        chain_units_nvfp4<true, MT>(a, epi, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted, slot,
                                 lap);
     else
-        chain_units_nvfp4<false>(a, epi, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted, slot,
+        chain_units_nvfp4<false, MT>(a, epi, smem, ring, slot_bytes, n_stages, full, empty, abort_flag, aborted, slot,
                                  lap);
 }
 
-template <int BITS, int BITS_U>
+template <int BITS, int BITS_U, int MT>
 __device__ __forceinline__ void chain_q45(const CcArgs& a, int epi, bool mixed, uint8_t* smem, uint32_t ring,
                                           uint32_t slot_bytes, int n_stages, uint64_t* full, uint64_t* empty,
                                           volatile int* abort_flag, bool& aborted, int& slot, int& lap)
 {
     if (mixed)
-        chain_units_q45<BITS, BITS_U, true>(a, epi, smem, ring, slot_bytes, n_stages, full, empty, abort_flag,
+        chain_units_q45<BITS, BITS_U, true, MT>(a, epi, smem, ring, slot_bytes, n_stages, full, empty, abort_flag,
                                             aborted, slot, lap);
     else
-        chain_units_q45<BITS, BITS_U, false>(a, epi, smem, ring, slot_bytes, n_stages, full, empty, abort_flag,
+        chain_units_q45<BITS, BITS_U, false, MT>(a, epi, smem, ring, slot_bytes, n_stages, full, empty, abort_flag,
                                              aborted, slot, lap);
 }
 
+// MT tokens (1 or 2) per op: every op's activations, residuals and outputs
+// are MT rows (K, N or n_out apart), as in the one- and two-token kernels.
+template <int MT>
 __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_constant__ ChainParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -447,29 +491,33 @@ __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_co
         if (threadIdx.x == 0) *any_bf = 0;
         named_barrier_sync(1, kCcThreads);
         // x through L2 only: an earlier op of this launch may have written it
-        if (op.fmt == FMT_NVFP4)
-            cc_convert<kChainNseg, XSRC_CG>(a, smem, warp, lane, any_bf);
-        else
-            cc_convert_q45<kChainNseg, XSRC_CG>(a, smem, warp, lane, any_bf);
+        if (op.fmt == FMT_NVFP4) {
+            if constexpr (MT == 1)
+                cc_convert<kChainNseg, XSRC_CG>(a, smem, warp, lane, any_bf);
+            else
+                cc_convert_q45<kChainNseg, XSRC_CG, kCcWarps, MT, false>(a, smem, warp, lane, any_bf);
+        } else {
+            cc_convert_q45<kChainNseg, XSRC_CG, kCcWarps, MT>(a, smem, warp, lane, any_bf);
+        }
         named_barrier_sync(1, kCcThreads);
         const bool mixed = *any_bf != 0;
         if (op.fmt == FMT_NVFP4) {
-            chain_nvfp4(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag, aborted,
+            chain_nvfp4<MT>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag, aborted,
                         slot, lap);
         } else {
             const bool b5 = op.fmt == FMT_Q5;
             const bool u5 = op.epi == EPI_SWIGLU ? op.ufmt == FMT_Q5 : b5;
             if (b5 && u5)
-                chain_q45<5, 5>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                chain_q45<5, 5, MT>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
                                 aborted, slot, lap);
             else if (b5)
-                chain_q45<5, 4>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                chain_q45<5, 4, MT>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
                                 aborted, slot, lap);
             else if (u5)
-                chain_q45<4, 5>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                chain_q45<4, 5, MT>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
                                 aborted, slot, lap);
             else
-                chain_q45<4, 4>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                chain_q45<4, 4, MT>(a, op.epi, mixed, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
                                 aborted, slot, lap);
         }
     }
@@ -499,13 +547,13 @@ void cc_plan(CcArgs& a, int n_out, int ngu, int K, int sms)
 
 }  // namespace
 
-// One persistent launch for a list of one-token projections;
-// QG_ERR_UNSUPPORTED when the list does not fit its plan (M != 1, K not a
+// One persistent launch for a list of one- or two-token projections;
+// QG_ERR_UNSUPPORTED when the list does not fit its plan (M > 2, K not a
 // multiple of 256, too many ops, or shared memory), so that the caller runs
 // the ops one by one instead.
 qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, cudaStream_t stream)
 {
-    if (M != 1 || n_ops < 1 || n_ops > kChainMaxOps) return QG_ERR_UNSUPPORTED;
+    if (M < 1 || M > 2 || n_ops < 1 || n_ops > kChainMaxOps) return QG_ERR_UNSUPPORTED;
     const int sms = sm_count(-1);
     if (sms <= 0) return QG_ERR_CUDA;
     static ChainParams p;  // large: built here, copied into the launch's parameters
@@ -591,14 +639,14 @@ qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, 
     if (any_dep && !sync) return QG_ERR_INVALID_ARG;
     // shared memory: ring | activations | 2^-prescale | flags | sums of x |
     // sums of squares | partial sums | barriers
-    const uint32_t x_bytes = static_cast<uint32_t>(c_max) * kChunkK * 2u;
-    const uint32_t pe_bytes = align_up(static_cast<uint32_t>(c_max) * 4u, 16);
+    const uint32_t x_bytes = static_cast<uint32_t>(M * c_max) * kChunkK * 2u;
+    const uint32_t pe_bytes = align_up(static_cast<uint32_t>(M * c_max) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(c_max), 16);
     bool any_q = false;
     for (int o = 0; o < n_ops; ++o) any_q = any_q || p.op[o].fmt != FMT_NVFP4;
-    const uint32_t gx_bytes = any_q ? align_up(static_cast<uint32_t>(c_max * kChainNseg) * 4u, 16) : 0u;
-    const uint32_t ss_bytes = align_up(static_cast<uint32_t>(c_max) * 4u, 16);
-    const uint32_t red_bytes = align_up(static_cast<uint32_t>(red_max) * 4u, 128);
+    const uint32_t gx_bytes = any_q ? align_up(static_cast<uint32_t>(M * c_max * kChainNseg) * 4u, 16) : 0u;
+    const uint32_t ss_bytes = align_up(static_cast<uint32_t>(M * c_max) * 4u, 16);
+    const uint32_t red_bytes = align_up(static_cast<uint32_t>(M * red_max) * 4u, 128);
     const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
     const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + gx_bytes + ss_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * slot_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
@@ -649,14 +697,14 @@ qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, 
         a.status = status;
     }
 
-    static bool attr_set[64] = {false};
+    auto kern = M == 2 ? chain_kernel<2> : chain_kernel<1>;
+    static bool attr_set[2][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCcSmemMax) !=
-            cudaSuccess)
+    if (!attr_set[M - 1][dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCcSmemMax) != cudaSuccess)
             return QG_ERR_CUDA;
-        attr_set[dev] = true;
+        attr_set[M - 1][dev] = true;
     }
     // Every CTA must be resident for the grid-wide barrier: one CTA per SM
     // (the shared memory allows no more), launched cooperatively when an op
@@ -676,7 +724,7 @@ qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, 
     }
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, chain_kernel, p) != cudaSuccess) return QG_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return QG_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 

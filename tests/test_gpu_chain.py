@@ -1,9 +1,9 @@
 """qgemv_chain: a decode layer's projections in one call (GPU).
 
-One token: the ops run in one persistent kernel; each op must give exactly
-what its single-projection call gives (same plan and arithmetic: bit for bit
-where the standalone kernel picks the same 32-k segments) and match the
-oracle within the stated bound. Ops flagged after_previous read earlier
+One or two tokens: the ops run in one persistent kernel; each op must give
+exactly what its single-projection call gives (same plan and arithmetic: bit
+for bit where the standalone kernel picks the same 32-k segments) and match
+the oracle within the stated bound. Ops flagged after_previous read earlier
 outputs of the same call through the grid-wide barrier; each such stage is
 checked against the oracle fed the GPU's own earlier output. More tokens run
 as one launch per op, identical to separate calls.
@@ -78,7 +78,7 @@ def run_separately(ops):
     return outs
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 2, 4])
 def test_chain_dense_layer_matches_separate_calls(M):
     ops, host = dense_layer_ops(M)
     q.qgemv_chain(ops)
@@ -87,7 +87,7 @@ def test_chain_dense_layer_matches_separate_calls(M):
     sep = run_separately(ops)
     for op, ys, (name, N, K, epi, w, x, r) in zip(ops, sep, host):
         assert torch.equal(op["y"].view(torch.int16), ys.view(torch.int16)), f"{name}: chain != separate call"
-        if M == 1:
+        if M <= 2:
             if epi == "swiglu":
                 yref, a = O.gemv_nvfp4(w, x)
                 I = N // 2
@@ -98,7 +98,8 @@ def test_chain_dense_layer_matches_separate_calls(M):
                 check_out(op["y"], yref, a, f"chain {name}")
 
 
-def test_chain_dependent_ops_through_the_grid_barrier():
+@pytest.mark.parametrize("M", [1, 2])
+def test_chain_dependent_ops_through_the_grid_barrier(M):
     """o: y1 = W_o x (+ r); gate/up reads y1; down reads h with y1 as its
     residual; a last projection reads the down output -- each op after the
     first waits for the earlier ones inside the one launch."""
@@ -107,13 +108,13 @@ def test_chain_dependent_ops_through_the_grid_barrier():
     wgu = synth.nvfp4_weights(70, "dep.gu", 2 * I, H)
     wdn = synth.nvfp4_weights(70, "dep.dn", H, I)
     wl = synth.nvfp4_weights(70, "dep.last", 512, H)
-    x = synth.bf16_normal(71, "dep.x", (1, 1536))
-    r = synth.bf16_normal(71, "dep.r", (1, H))
+    x = synth.bf16_normal(71, "dep.x", (2, 1536))[:M]
+    r = synth.bf16_normal(71, "dep.r", (2, H))[:M]
     D = {k: nvfp4_dev(w) for k, w in (("o", wo), ("gu", wgu), ("dn", wdn), ("last", wl))}
-    y1 = torch.empty((1, H), dtype=torch.bfloat16, device="cuda")
-    h = torch.empty((1, I), dtype=torch.bfloat16, device="cuda")
-    y2 = torch.empty((1, H), dtype=torch.bfloat16, device="cuda")
-    y3 = torch.empty((1, 512), dtype=torch.float32, device="cuda")
+    y1 = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    h = torch.empty((M, I), dtype=torch.bfloat16, device="cuda")
+    y2 = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    y3 = torch.empty((M, 512), dtype=torch.float32, device="cuda")
     ops = [
         {**D["o"], "x": to_dev(x), "y": y1, "residual": to_dev(r)},
         {**D["gu"], "x": y1, "y": h, "epilogue": "swiglu", "after_previous": True},
@@ -139,15 +140,16 @@ def test_chain_dependent_ops_through_the_grid_barrier():
     check_f32(y3.cpu().numpy(), yref, gemv_bound(a), "dep last")
 
 
-def test_chain_q45_layer_full_size():
+@pytest.mark.parametrize("M", [1, 2])
+def test_chain_q45_layer_full_size(M):
     ops, host = [], []
     for name, N, K, bits in synth.Q45_RECIPE:
         w = synth.q45_weights(3, f"q45.{name}", N, K, bits)
-        x = synth.bf16_normal(72, f"chainq.{name}.x", (1, K))
-        r = synth.bf16_normal(72, f"chainq.{name}.r", (1, N)) if name == "down" else None
+        x = synth.bf16_normal(72, f"chainq.{name}.x", (2, K))[:M]
+        r = synth.bf16_normal(72, f"chainq.{name}.r", (2, N))[:M] if name == "down" else None
         d = q45_dev(w)
         op = {"q_lo": d["q_lo"], "q_hi": d["q_hi"], "scale": d["scale"], "min": d["min"], "x": to_dev(x),
-              "y": torch.empty((1, N), dtype=torch.bfloat16, device="cuda")}
+              "y": torch.empty((M, N), dtype=torch.bfloat16, device="cuda")}
         if r is not None:
             op["residual"] = to_dev(r)
         ops.append(op)
@@ -155,18 +157,21 @@ def test_chain_q45_layer_full_size():
     q.qgemv_chain(ops)
     torch.cuda.synchronize()
     assert q.qg_last_device_status() == q.QG_OK
-    for op, (name, w, x, r) in zip(ops, host):
+    sep = run_separately(ops)
+    for op, ys, (name, w, x, r) in zip(ops, sep, host):
+        assert torch.equal(op["y"].view(torch.int16), ys.view(torch.int16)), f"{name}: chain != separate call"
         yref, a = O.gemv_q45(w, x, residual=r)
         check_out(op["y"], yref, a, f"chain Q {name}")
 
 
-def test_chain_mixed_formats_and_fp32_outputs():
+@pytest.mark.parametrize("M", [1, 2])
+def test_chain_mixed_formats_and_fp32_outputs(M):
     """NVFP4 and Q4/Q5 ops in one launch, fp32 and bf16 outputs, ragged rows."""
     specs = [("nvfp4", 1000, 768, torch.float32), ("q5", 333, 1024, torch.bfloat16),
              ("q4", 2049, 512, torch.float32), ("nvfp4", 77, 2304, torch.bfloat16)]
     ops, host = [], []
     for i, (fmt, N, K, dt) in enumerate(specs):
-        x = synth.bf16_normal(73, f"mix.x{i}", (1, K))
+        x = synth.bf16_normal(73, f"mix.x{i}", (2, K))[:M]
         if fmt == "nvfp4":
             w = synth.nvfp4_weights(73, f"mix.w{i}", N, K, g=0.5)
             d = nvfp4_dev(w)
@@ -175,7 +180,7 @@ def test_chain_mixed_formats_and_fp32_outputs():
             w = synth.q45_weights(73, f"mix.w{i}", N, K, 5 if fmt == "q5" else 4)
             d = q45_dev(w)
             op = {"q_lo": d["q_lo"], "q_hi": d["q_hi"], "scale": d["scale"], "min": d["min"]}
-        op.update({"x": to_dev(x), "y": torch.empty((1, N), dtype=dt, device="cuda")})
+        op.update({"x": to_dev(x), "y": torch.empty((M, N), dtype=dt, device="cuda")})
         ops.append(op)
         host.append((fmt, w, x))
     q.qgemv_chain(ops)

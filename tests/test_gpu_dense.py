@@ -351,9 +351,10 @@ def test_q45_two_tokens_match_one_token_calls(bits, residual):
 # ---------------------------------------------------------------- properties
 def test_deterministic_and_row_independent():
     """Repeated calls are bit-identical; a token's result does not depend on
-    the other tokens of a 2..8-token call (same arithmetic for every such M);
-    the one-token kernel applies block scales after the MMA, so it is checked
-    against the oracle's bound instead of bit for bit."""
+    the other tokens of a 3..8-token call (same arithmetic for every such M);
+    the one- and two-token CUDA-core kernel applies block scales per 16-k
+    block instead, so it is checked against the oracle's bound, and its
+    two-token results against one-token calls bit for bit."""
     M, N, K = 8, 2000, 2048
     w = synth.nvfp4_weights(30, "det", N, K)
     x = synth.bf16_normal(31, "detx", (M, K))
@@ -361,14 +362,18 @@ def test_deterministic_and_row_independent():
     y2 = run_nvfp4(w, x, torch.float32).cpu().numpy()
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32)), "two runs differ"
     for m in (0, 5):
-        pair = np.stack([x[m], x[(m + 3) % M]])
-        ym = run_nvfp4(w, pair, torch.float32).cpu().numpy()
-        assert np.array_equal(ym[0].view(np.uint32), y1[m].view(np.uint32)), f"row {m}: M=2 call != M=8 call"
+        three = np.stack([x[m], x[(m + 3) % M], x[(m + 1) % M]])
+        ym = run_nvfp4(w, three, torch.float32).cpu().numpy()
+        assert np.array_equal(ym[0].view(np.uint32), y1[m].view(np.uint32)), f"row {m}: M=3 call != M=8 call"
         y_one = run_nvfp4(w, x[m:m + 1], torch.float32)
         y_one2 = run_nvfp4(w, x[m:m + 1], torch.float32)
         assert torch.equal(y_one, y_one2), "one-token runs differ"
         yref, a = O.gemv_nvfp4(w, x[m:m + 1])
         check_out(y_one, yref, a, f"row {m} one-token call")
+        y_two = run_nvfp4(w, np.stack([x[m], x[(m + 3) % M]]), torch.float32)
+        assert torch.equal(y_two[0], y_one[0]), f"row {m}: two-token call != one-token call"
+        y_b = run_nvfp4(w, x[(m + 3) % M:(m + 3) % M + 1], torch.float32)
+        assert torch.equal(y_two[1], y_b[0]), f"row {(m + 3) % M}: two-token call != one-token call"
 
 
 def test_outputs_stay_inside_their_buffer():
@@ -424,9 +429,9 @@ def _q5_call(M, N, K, seed):
 
 
 # One case per pipelined kernel: the one-token CUDA-core NVFP4 and Q5
-# kernels, the two-token Q5 variant, the tcgen05 kernel (NVFP4, 8 tokens)
+# kernels, their two-token variants, the tcgen05 kernel (NVFP4, 8 tokens)
 # and the mma.sync groupwise-int kernel (Q5, 8 tokens).
-STARVE_CASES = [("nvfp4", 1), ("nvfp4", 8), ("q5", 1), ("q5", 2), ("q5", 8)]
+STARVE_CASES = [("nvfp4", 1), ("nvfp4", 2), ("nvfp4", 8), ("q5", 1), ("q5", 2), ("q5", 8)]
 
 
 @pytest.mark.parametrize("fmt,M", STARVE_CASES)
