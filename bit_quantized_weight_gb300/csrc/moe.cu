@@ -83,8 +83,9 @@ namespace {
 constexpr int kMaxPairs = kMaxTokens * 8;
 
 struct MoeLayout {
-    size_t h, yslot, ctrl, g_gu, g_dn, u_gu, u_dn, total;
+    size_t h, yslot, ctrl, g_gu, g_dn, u_gu, u_dn, p_gu, p_dn, total;
     int r_gu, r_dn, units_gu_max, units_dn_max;
+    int rc_gu, rc_dn, passes_gu_max, passes_dn_max;  // the CUDA-core kernels' pass lists
 };
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
@@ -101,6 +102,13 @@ MoeLayout moe_layout(int M, int topk, int H, int I)
     L.r_dn = 128;
     L.units_gu_max = kMaxPairs * (I / L.r_gu);
     L.units_dn_max = kMaxPairs * (H / L.r_dn);
+    // CUDA-core passes: 32 gate/up row pairs (4 phases of 2 x 32 rows fill a
+    // 256-row stage) and 64 down rows; at most one token pair per valid (token,
+    // slot) pair, so P pairs bound the pair groups of either launch.
+    L.rc_gu = 32;
+    L.rc_dn = 64;
+    L.passes_gu_max = static_cast<int>(P) * (I / L.rc_gu);
+    L.passes_dn_max = static_cast<int>(P) * (H / L.rc_dn);
     size_t o = 0;
     L.h = o;
     o += up256(P * I * 2);
@@ -116,6 +124,10 @@ MoeLayout moe_layout(int M, int topk, int H, int I)
     o += up256(sizeof(UnitDesc) * L.units_gu_max);
     L.u_dn = o;
     o += up256(sizeof(UnitDesc) * L.units_dn_max);
+    L.p_gu = o;
+    o += up256(sizeof(CcPass) * L.passes_gu_max);
+    L.p_dn = o;
+    o += up256(sizeof(CcPass) * L.passes_dn_max);
     L.total = o;
     return L;
 }
@@ -126,9 +138,17 @@ MoeLayout moe_layout(int M, int topk, int H, int I)
 // the slot that routed token m there. Down: the pairs of an expert, at most 8
 // per group; column j reads h row x_row[j] and writes slot row out_row[j].
 // A token listing one expert twice reuses the first slot's h row.
+//
+// It also writes the CUDA-core kernels' pass lists. Gate/up: per expert, its
+// distinct tokens in pairs (x row = token, output row = that token's first
+// slot for the expert), times the expert's blocks of rc_gu row pairs. Down:
+// per expert, its (token, slot) pairs in pairs (x row = the h row the token's
+// first slot wrote, output row = the slot), times blocks of rc_dn rows. The
+// passes of one pair group's blocks are adjacent in the list; ctrl[2] and
+// ctrl[3] receive the counts.
 __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int I, int H, int r_gu, int r_dn,
-                                 GroupDesc* g_gu, GroupDesc* g_dn, UnitDesc* u_gu, UnitDesc* u_dn, int* ctrl,
-                                 int* status)
+                                 GroupDesc* g_gu, GroupDesc* g_dn, UnitDesc* u_gu, UnitDesc* u_dn, int rc_gu,
+                                 int rc_dn, CcPass* p_gu, CcPass* p_dn, int* ctrl, int* status)
 {
     __shared__ int s_pair_e[kMaxPairs];
     __shared__ int s_order[kMaxPairs];    // valid pairs sorted by (expert, pair)
@@ -286,6 +306,121 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
         ctrl[0] = n_gu;
         ctrl[1] = n_dn;
     }
+
+    // ---- pair groups of the CUDA-core passes: (expert, n, x rows, output rows),
+    // one thread per sorted position (at most 64), with 64-bit masks of the
+    // run starts and of each (expert, token)'s first position
+    __shared__ int s_pg[2][kMaxPairs][6];
+    __shared__ int s_npg[2];
+    __shared__ unsigned s_msk[2][2];           // [run start | first of token][warp]
+    __shared__ int s_cnt[2][kMaxPairs];        // per run: gate/up groups, down groups
+    __shared__ int s_base[2][kMaxPairs];       // per run: index of its first group
+    __shared__ int s_nrun;
+    const int pi = tid;
+    const bool pin = pi < nv;
+    const int pp_ = pin ? s_order[pi] : 0;
+    const int pe_ = pin ? s_pair_e[pp_] : -1;
+    const int pm_ = pp_ / topk;
+    if (tid < 64) {
+        const int pe_prev = pin && pi > 0 ? s_pair_e[s_order[pi - 1]] : -1;
+        const int pm_prev = pin && pi > 0 ? s_order[pi - 1] / topk : -1;
+        const bool rstart = pin && (pi == 0 || pe_prev != pe_);
+        const bool first = pin && (rstart || pm_prev != pm_);
+        const unsigned rb = __ballot_sync(0xffffffffu, rstart), fb = __ballot_sync(0xffffffffu, first);
+        if ((tid & 31) == 0) {
+            s_msk[0][tid >> 5] = rb;
+            s_msk[1][tid >> 5] = fb;
+        }
+    }
+    __syncthreads();
+    const unsigned long long rsm = s_msk[0][0] | (static_cast<unsigned long long>(s_msk[0][1]) << 32);
+    const unsigned long long fsm = s_msk[1][0] | (static_cast<unsigned long long>(s_msk[1][1]) << 32);
+    // bits [lo, hi) of a 64-bit mask
+    auto bits = [](int lo, int hi) -> unsigned long long {
+        const unsigned long long h = hi >= 64 ? ~0ull : ((1ull << hi) - 1ull);
+        return h & ~((1ull << lo) - 1ull);
+    };
+    int run = 0, r0 = 0, r1 = 0;
+    if (pin) {
+        run = __popcll(rsm & bits(0, pi + 1)) - 1;
+        r0 = 63 - __clzll(rsm & bits(0, pi + 1));
+        const unsigned long long above = rsm & ~bits(0, pi + 1);
+        r1 = above ? __ffsll(static_cast<long long>(above)) - 1 : nv;
+        if (r0 == pi) {
+            s_cnt[0][run] = (__popcll(fsm & bits(r0, r1)) + 1) / 2;
+            s_cnt[1][run] = (r1 - r0 + 1) / 2;
+        }
+    }
+    if (tid == 0) s_nrun = __popcll(rsm);
+    __syncthreads();
+    if (tid < 32) {
+        // exclusive prefix over the runs, two per lane
+        const int nr = s_nrun;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int a0 = 2 * tid < nr ? s_cnt[k][2 * tid] : 0;
+            const int a1 = 2 * tid + 1 < nr ? s_cnt[k][2 * tid + 1] : 0;
+            int incl = a0 + a1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (tid >= off) incl += o;
+            }
+            const int excl = incl - a0 - a1;
+            if (2 * tid < nr) s_base[k][2 * tid] = excl;
+            if (2 * tid + 1 < nr) s_base[k][2 * tid + 1] = excl + a0;
+            if (tid == 31) s_npg[k] = incl;
+        }
+    }
+    __syncthreads();
+    if (pin) {
+        // gate/up: the token's first position in the run, its rank among them
+        if (fsm & bits(pi, pi + 1)) {
+            const int dr = __popcll(fsm & bits(r0, pi + 1)) - 1;
+            const int nd = __popcll(fsm & bits(r0, r1));
+            int* g = s_pg[0][s_base[0][run] + dr / 2];
+            if (dr % 2 == 0) {
+                g[0] = pe_;
+                g[1] = min(2, nd - dr);
+            }
+            g[2 + dr % 2] = pm_;
+            g[4 + dr % 2] = pp_;
+        }
+        // down: every pair, reading the h row of its token's first position
+        const int j = pi - r0;
+        const int fpos = 63 - __clzll(fsm & bits(0, pi + 1));
+        int* d = s_pg[1][s_base[1][run] + j / 2];
+        if (j % 2 == 0) {
+            d[0] = pe_;
+            d[1] = min(2, r1 - r0 - j);
+        }
+        d[2 + j % 2] = s_order[fpos];
+        d[4 + j % 2] = pp_;
+    }
+    __syncthreads();
+    const int blk_gu = I / rc_gu, blk_dn = H / rc_dn;
+    const int np_gu = s_npg[0] * blk_gu, np_dn = s_npg[1] * blk_dn;
+    for (int u = tid; u < np_gu + np_dn; u += blockDim.x) {
+        const bool dn = u >= np_gu;
+        const int v = dn ? u - np_gu : u;
+        const int blk = dn ? blk_dn : blk_gu, rc = dn ? rc_dn : rc_gu;
+        const int* g = s_pg[dn ? 1 : 0][v / blk];
+        const int rb = v % blk;
+        CcPass ps;
+        ps.e = g[0];
+        ps.ntok = g[1];
+        ps.w_row0 = dn ? g[0] * H + rb * rc : g[0] * 2 * I + rb * rc;
+        ps.out_col0 = rb * rc;
+        ps.x_row[0] = g[2];
+        ps.x_row[1] = g[1] > 1 ? g[3] : g[2];
+        ps.out_row[0] = g[4];
+        ps.out_row[1] = g[1] > 1 ? g[5] : -1;
+        (dn ? p_dn : p_gu)[v] = ps;
+    }
+    if (tid == 0) {
+        ctrl[2] = np_gu;
+        ctrl[3] = np_dn;
+    }
 }
 
 // y[m][j] = bf16_rne( sum_{i ascending} w[m][i] * yslot[m * topk + i][j] ), fp32.
@@ -341,17 +476,27 @@ qg_status launch_moe(const uint8_t* gu_codes, const uint8_t* gu_scales, const fl
     GroupDesc* g_dn = reinterpret_cast<GroupDesc*>(w + L.g_dn);
     UnitDesc* u_gu = reinterpret_cast<UnitDesc*>(w + L.u_gu);
     UnitDesc* u_dn = reinterpret_cast<UnitDesc*>(w + L.u_dn);
+    CcPass* p_gu = reinterpret_cast<CcPass*>(w + L.p_gu);
+    CcPass* p_dn = reinterpret_cast<CcPass*>(w + L.p_dn);
     int* status = device_status_ptr();
     if (!status) return QG_ERR_CUDA;
 
     if (launch_pdl(moe_group_kernel, dim3(1), dim3(256), 0, stream, ids, M, topk, E, I, H, L.r_gu, L.r_dn, g_gu,
-                   g_dn, u_gu, u_dn, ctrl, status) != cudaSuccess)
+                   g_dn, u_gu, u_dn, L.rc_gu, L.rc_dn, p_gu, p_dn, ctrl, status) != cudaSuccess)
         return QG_ERR_CUDA;
-    qg_status s = grouped_nvfp4(gu_codes, gu_scales, E * 2 * I, H, 1, I, x, M, h, I, 0, g_gu, u_gu, ctrl + 0,
-                                       gu_g, L.r_gu, stream);
+    // the CUDA-core grouped kernels, else the tcgen05 ones
+    const int P = M * topk;
+    qg_status s = launch_cc_moe(gu_codes, gu_scales, E * 2 * I, H, 1, I, x, M, h, I, 0, p_gu, ctrl + 2,
+                                L.passes_gu_max, gu_g, L.rc_gu, stream);
+    if (s == QG_ERR_UNSUPPORTED)
+        s = grouped_nvfp4(gu_codes, gu_scales, E * 2 * I, H, 1, I, x, M, h, I, 0, g_gu, u_gu, ctrl + 0, gu_g, L.r_gu,
+                          stream);
     if (s != QG_OK) return s;
-    s = grouped_nvfp4(dn_codes, dn_scales, E * H, I, 0, 0, h, 8, yslot, H, 1, g_dn, u_dn, ctrl + 1, dn_g,
-                             L.r_dn, stream);
+    s = launch_cc_moe(dn_codes, dn_scales, E * H, I, 0, 0, h, P, yslot, H, 1, p_dn, ctrl + 3, L.passes_dn_max, dn_g,
+                      L.rc_dn, stream);
+    if (s == QG_ERR_UNSUPPORTED)
+        s = grouped_nvfp4(dn_codes, dn_scales, E * H, I, 0, 0, h, 8, yslot, H, 1, g_dn, u_dn, ctrl + 1, dn_g,
+                          L.r_dn, stream);
     if (s != QG_OK) return s;
     const int n = M * H;
     if (launch_pdl(moe_combine_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, yslot, ids, tw,

@@ -43,6 +43,17 @@ struct GroupDesc {
     int out_row[8];
 };
 
+// One pass of the grouped CUDA-core MoE kernels: a unit of rows of one expert
+// together with one or two of its tokens.
+struct CcPass {
+    int w_row0;      // first weight row (gate row for SwiGLU)
+    int out_col0;    // first output column
+    int e;           // expert id (per-expert global scale)
+    int ntok;        // 1 or 2
+    int x_row[2];    // activation rows (x_row[1] repeats x_row[0] for one token)
+    int out_row[2];  // output rows
+};
+
 struct UnitDesc {
     int grp;         // index into the group array
     int w_row0;      // first weight row (gate row for SwiGLU)
@@ -155,6 +166,9 @@ qg_status launch_tc_grouped_nvfp4(const uint8_t* codes, const uint8_t* scales, i
                                   int up_offset, const void* x, int max_cols, void* y, int out_pitch, int out_f32,
                                   const GroupDesc* groups, const UnitDesc* units, const int* n_units,
                                   const float* gscales, int rows_per_unit, cudaStream_t stream);
+qg_status launch_cc_moe(const uint8_t* codes, const uint8_t* scales, int total_rows, int K, int swiglu, int up_offset,
+                        const void* x, int n_x_rows, void* y, int out_pitch, int out_f32, const CcPass* passes,
+                        const int* n_passes, int max_passes, const float* gscales, int R, cudaStream_t stream);
 qg_status launch_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min,
                            int bits, const void* x, void* y, int out_f32, const void* residual, int M,
                            int N, int K, cudaStream_t stream);
