@@ -85,7 +85,7 @@ constexpr int kMaxPairs = kMaxTokens * 8;
 struct MoeLayout {
     size_t h, yslot, ctrl, g_gu, g_dn, u_gu, u_dn, p_gu, p_dn, total;
     int r_gu, r_dn, units_gu_max, units_dn_max;
-    int rc_gu, rc_dn, passes_gu_max, passes_dn_max;  // the CUDA-core kernels' pass lists
+    int rc_gu, rc_dn;  // the CUDA-core kernels' rows per pass
 };
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
@@ -103,12 +103,10 @@ MoeLayout moe_layout(int M, int topk, int H, int I)
     L.units_gu_max = kMaxPairs * (I / L.r_gu);
     L.units_dn_max = kMaxPairs * (H / L.r_dn);
     // CUDA-core passes: 32 gate/up row pairs (4 phases of 2 x 32 rows fill a
-    // 256-row stage) and 64 down rows; at most one token pair per valid (token,
-    // slot) pair, so P pairs bound the pair groups of either launch.
+    // 256-row stage) and 64 down rows; every pair group holds at least one
+    // valid (token, slot) pair, so P bounds the groups of either launch.
     L.rc_gu = 32;
     L.rc_dn = 64;
-    L.passes_gu_max = static_cast<int>(P) * (I / L.rc_gu);
-    L.passes_dn_max = static_cast<int>(P) * (H / L.rc_dn);
     size_t o = 0;
     L.h = o;
     o += up256(P * I * 2);
@@ -125,9 +123,9 @@ MoeLayout moe_layout(int M, int topk, int H, int I)
     L.u_dn = o;
     o += up256(sizeof(UnitDesc) * L.units_dn_max);
     L.p_gu = o;
-    o += up256(sizeof(CcPass) * L.passes_gu_max);
+    o += up256(sizeof(CcPair) * P);
     L.p_dn = o;
-    o += up256(sizeof(CcPass) * L.passes_dn_max);
+    o += up256(sizeof(CcPair) * P);
     L.total = o;
     return L;
 }
@@ -139,16 +137,14 @@ MoeLayout moe_layout(int M, int topk, int H, int I)
 // per group; column j reads h row x_row[j] and writes slot row out_row[j].
 // A token listing one expert twice reuses the first slot's h row.
 //
-// It also writes the CUDA-core kernels' pass lists. Gate/up: per expert, its
+// It also writes the CUDA-core kernels' pair groups. Gate/up: per expert, its
 // distinct tokens in pairs (x row = token, output row = that token's first
-// slot for the expert), times the expert's blocks of rc_gu row pairs. Down:
-// per expert, its (token, slot) pairs in pairs (x row = the h row the token's
-// first slot wrote, output row = the slot), times blocks of rc_dn rows. The
-// passes of one pair group's blocks are adjacent in the list; ctrl[2] and
-// ctrl[3] receive the counts.
+// slot for the expert). Down: per expert, its (token, slot) pairs in pairs (x
+// row = the h row the token's first slot wrote, output row = the slot).
+// ctrl[2] and ctrl[3] receive the counts.
 __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int I, int H, int r_gu, int r_dn,
-                                 GroupDesc* g_gu, GroupDesc* g_dn, UnitDesc* u_gu, UnitDesc* u_dn, int rc_gu,
-                                 int rc_dn, CcPass* p_gu, CcPass* p_dn, int* ctrl, int* status)
+                                 GroupDesc* g_gu, GroupDesc* g_dn, UnitDesc* u_gu, UnitDesc* u_dn, CcPair* p_gu,
+                                 CcPair* p_dn, int emit_tc, int* ctrl, int* status)
 {
     __shared__ int s_pair_e[kMaxPairs];
     __shared__ int s_order[kMaxPairs];    // valid pairs sorted by (expert, pair)
@@ -187,6 +183,10 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
         s_nv = nv;
     }
     __syncthreads();
+    const int nv = s_nv;
+    // The tcgen05 kernels' lists, only when they will run (emit_tc is the
+    // same for every thread, so the barriers inside are reached by all).
+    if (emit_tc) {
     // group boundaries along the sorted pairs (at most 64 positions: the
     // first two warps, one position per lane, ballots for the prefix counts)
     if (tid < 64) {
@@ -229,7 +229,6 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
         }
     }
     __syncthreads();
-    const int nv = s_nv;
     // one gate/up group per expert run: all M token rows of x, the first
     // slot of each token writes its h row
     for (int i = tid; i < nv; i += blockDim.x) {
@@ -305,6 +304,7 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
     if (tid == 0) {
         ctrl[0] = n_gu;
         ctrl[1] = n_dn;
+    }
     }
 
     // ---- pair groups of the CUDA-core passes: (expert, n, x rows, output rows),
@@ -398,28 +398,23 @@ __global__ void moe_group_kernel(const int32_t* ids, int M, int topk, int E, int
         d[4 + j % 2] = pp_;
     }
     __syncthreads();
-    const int blk_gu = I / rc_gu, blk_dn = H / rc_dn;
-    const int np_gu = s_npg[0] * blk_gu, np_dn = s_npg[1] * blk_dn;
-    for (int u = tid; u < np_gu + np_dn; u += blockDim.x) {
-        const bool dn = u >= np_gu;
-        const int v = dn ? u - np_gu : u;
-        const int blk = dn ? blk_dn : blk_gu, rc = dn ? rc_dn : rc_gu;
-        const int* g = s_pg[dn ? 1 : 0][v / blk];
-        const int rb = v % blk;
-        CcPass ps;
-        ps.e = g[0];
-        ps.ntok = g[1];
-        ps.w_row0 = dn ? g[0] * H + rb * rc : g[0] * 2 * I + rb * rc;
-        ps.out_col0 = rb * rc;
-        ps.x_row[0] = g[2];
-        ps.x_row[1] = g[1] > 1 ? g[3] : g[2];
-        ps.out_row[0] = g[4];
-        ps.out_row[1] = g[1] > 1 ? g[5] : -1;
-        (dn ? p_dn : p_gu)[v] = ps;
+    const int ng = s_npg[0], nd = s_npg[1];
+    for (int u = tid; u < ng + nd; u += blockDim.x) {
+        const bool dn = u >= ng;
+        const int v = dn ? u - ng : u;
+        const int* g = s_pg[dn ? 1 : 0][v];
+        CcPair pr;
+        pr.e = g[0];
+        pr.ntok = g[1];
+        pr.x_row[0] = g[2];
+        pr.x_row[1] = g[1] > 1 ? g[3] : g[2];
+        pr.out_row[0] = g[4];
+        pr.out_row[1] = g[1] > 1 ? g[5] : -1;
+        (dn ? p_dn : p_gu)[v] = pr;
     }
     if (tid == 0) {
-        ctrl[2] = np_gu;
-        ctrl[3] = np_dn;
+        ctrl[2] = ng;
+        ctrl[3] = nd;
     }
 }
 
@@ -476,27 +471,36 @@ qg_status launch_moe(const uint8_t* gu_codes, const uint8_t* gu_scales, const fl
     GroupDesc* g_dn = reinterpret_cast<GroupDesc*>(w + L.g_dn);
     UnitDesc* u_gu = reinterpret_cast<UnitDesc*>(w + L.u_gu);
     UnitDesc* u_dn = reinterpret_cast<UnitDesc*>(w + L.u_dn);
-    CcPass* p_gu = reinterpret_cast<CcPass*>(w + L.p_gu);
-    CcPass* p_dn = reinterpret_cast<CcPass*>(w + L.p_dn);
+    CcPair* p_gu = reinterpret_cast<CcPair*>(w + L.p_gu);
+    CcPair* p_dn = reinterpret_cast<CcPair*>(w + L.p_dn);
     int* status = device_status_ptr();
     if (!status) return QG_ERR_CUDA;
 
-    if (launch_pdl(moe_group_kernel, dim3(1), dim3(256), 0, stream, ids, M, topk, E, I, H, L.r_gu, L.r_dn, g_gu,
-                   g_dn, u_gu, u_dn, L.rc_gu, L.rc_dn, p_gu, p_dn, ctrl, status) != cudaSuccess)
-        return QG_ERR_CUDA;
-    // the CUDA-core grouped kernels, else the tcgen05 ones
+    // The CUDA-core grouped kernels where their plans fit, else the tcgen05
+    // ones (whose lists the grouping kernel then writes too).
     const int P = M * topk;
-    qg_status s = launch_cc_moe(gu_codes, gu_scales, E * 2 * I, H, 1, I, x, M, h, I, 0, p_gu, ctrl + 2,
-                                L.passes_gu_max, gu_g, L.rc_gu, stream);
-    if (s == QG_ERR_UNSUPPORTED)
-        s = grouped_nvfp4(gu_codes, gu_scales, E * 2 * I, H, 1, I, x, M, h, I, 0, g_gu, u_gu, ctrl + 0, gu_g, L.r_gu,
-                          stream);
+    auto cc_gu = [&](bool launch) {
+        return launch_cc_moe(gu_codes, gu_scales, E * 2 * I, H, 1, I, 2 * I, I / L.rc_gu, x, M, h, I, 0, p_gu,
+                             ctrl + 2, P, gu_g, L.rc_gu, stream, launch);
+    };
+    auto cc_dn = [&](bool launch) {
+        return launch_cc_moe(dn_codes, dn_scales, E * H, I, 0, 0, H, H / L.rc_dn, h, P, yslot, H, 1, p_dn, ctrl + 3,
+                             P, dn_g, L.rc_dn, stream, launch);
+    };
+    const qg_status fit_gu = cc_gu(false), fit_dn = cc_dn(false);
+    if (fit_gu != QG_OK && fit_gu != QG_ERR_UNSUPPORTED) return fit_gu;
+    if (fit_dn != QG_OK && fit_dn != QG_ERR_UNSUPPORTED) return fit_dn;
+    const int emit_tc = (fit_gu != QG_OK || fit_dn != QG_OK) ? 1 : 0;
+    if (launch_pdl(moe_group_kernel, dim3(1), dim3(256), 0, stream, ids, M, topk, E, I, H, L.r_gu, L.r_dn, g_gu,
+                   g_dn, u_gu, u_dn, p_gu, p_dn, emit_tc, ctrl, status) != cudaSuccess)
+        return QG_ERR_CUDA;
+    qg_status s = fit_gu == QG_OK ? cc_gu(true)
+                                  : grouped_nvfp4(gu_codes, gu_scales, E * 2 * I, H, 1, I, x, M, h, I, 0, g_gu, u_gu,
+                                                  ctrl + 0, gu_g, L.r_gu, stream);
     if (s != QG_OK) return s;
-    s = launch_cc_moe(dn_codes, dn_scales, E * H, I, 0, 0, h, P, yslot, H, 1, p_dn, ctrl + 3, L.passes_dn_max, dn_g,
-                      L.rc_dn, stream);
-    if (s == QG_ERR_UNSUPPORTED)
-        s = grouped_nvfp4(dn_codes, dn_scales, E * H, I, 0, 0, h, 8, yslot, H, 1, g_dn, u_dn, ctrl + 1, dn_g,
-                          L.r_dn, stream);
+    s = fit_dn == QG_OK ? cc_dn(true)
+                        : grouped_nvfp4(dn_codes, dn_scales, E * H, I, 0, 0, h, 8, yslot, H, 1, g_dn, u_dn, ctrl + 1,
+                                        dn_g, L.r_dn, stream);
     if (s != QG_OK) return s;
     const int n = M * H;
     if (launch_pdl(moe_combine_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, yslot, ids, tw,

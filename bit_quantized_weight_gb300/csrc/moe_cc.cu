@@ -47,10 +47,22 @@ constexpr int kMoeEpiWarp = kCcWarps + 1;
 constexpr int kMoeThreads = 32 * (kMoeEpiWarp + 1);
 constexpr uint32_t kMoeBarBytes = (2 * kCcMaxStages + 4) * 8 + 16;
 
+// One pass: a unit of R rows of one expert with one or two of its tokens.
+struct CcPass {
+    int w_row0;      // first weight row (gate row for SwiGLU)
+    int out_col0;    // first output column
+    int e;           // expert id
+    int ntok;        // 1 or 2
+    int x_row[2];    // activation rows
+    int out_row[2];  // output rows
+};
+
 struct MoeCcArgs {
     CcArgs a;                 // the unit plan (R, R8, P, Cp, C, K), ring and shared-memory offsets, waits
-    const CcPass* passes;
-    const int* n_passes;      // device count, written by the grouping kernel
+    const CcPair* pairs;      // pair groups, written by the grouping kernel
+    const int* n_pairs;       // their device count
+    int blocks;               // row blocks per expert: passes = pairs * blocks
+    int expert_rows;          // weight rows per expert (gate and up rows both)
     const float* gscales;     // per-expert global scale
     int out_pitch;            // values per output row
     int max_local;            // passes per CTA the tables were sized for
@@ -200,19 +212,28 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
     // The pass list (and the activations) come from earlier kernels.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int G = gridDim.x;
-    const int n_passes = *m.n_passes;
+    const int n_passes = *m.n_pairs * m.blocks;
     const int n_local = n_passes > static_cast<int>(blockIdx.x) ? (n_passes - blockIdx.x + G - 1) / G : 0;
     if (n_local > m.max_local) {  // more passes than the list can hold: not produced by the grouping kernel
         if (threadIdx.x == 0) set_device_status(a.status, QG_ERR_INVALID_ARG);
         return;
     }
-    // this CTA's pass descriptors, read once (their latency would otherwise
-    // stall the producer and the epilogue at every pass)
-    {
-        const int* src = reinterpret_cast<const int*>(m.passes);
-        int* dst = reinterpret_cast<int*>(sp);
-        for (int k = threadIdx.x; k < 8 * n_local; k += blockDim.x)
-            dst[k] = src[static_cast<size_t>(blockIdx.x + (k >> 3) * G) * 8 + (k & 7)];
+    // this CTA's pass descriptors, built once (reading them per pass would
+    // stall the producer and the epilogue on global latency)
+    for (int k = threadIdx.x; k < n_local; k += blockDim.x) {
+        const int v = blockIdx.x + k * G;
+        const int gi = v / m.blocks, rb = v - gi * m.blocks;
+        const CcPair pr = m.pairs[gi];
+        CcPass ps;
+        ps.w_row0 = pr.e * m.expert_rows + rb * a.R;
+        ps.out_col0 = rb * a.R;
+        ps.e = pr.e;
+        ps.ntok = pr.ntok;
+        ps.x_row[0] = pr.x_row[0];
+        ps.x_row[1] = pr.x_row[1];
+        ps.out_row[0] = pr.out_row[0];
+        ps.out_row[1] = pr.out_row[1];
+        sp[k] = ps;
     }
     __syncthreads();
 
@@ -418,14 +439,17 @@ constexpr uint32_t align_up(uint32_t v, uint32_t al) { return (v + al - 1) / al 
 
 }  // namespace
 
-// The grouped projection over a pass list of at most max_passes entries;
-// QG_ERR_UNSUPPORTED when the shapes or shared memory do not fit the plan (the
-// caller then takes the tcgen05 grouped kernel).
+// The grouped projection over at most max_pairs pair groups, each over
+// `blocks` row blocks of R rows; QG_ERR_UNSUPPORTED when the shapes or shared
+// memory do not fit the plan (the caller then takes the tcgen05 grouped
+// kernel). With launch == false it only answers whether the plan fits.
 qg_status launch_cc_moe(const uint8_t* codes, const uint8_t* scales, int total_rows, int K, int swiglu, int up_offset,
-                        const void* x, int n_x_rows, void* y, int out_pitch, int out_f32, const CcPass* passes,
-                        const int* n_passes, int max_passes, const float* gscales, int R, cudaStream_t stream)
+                        int expert_rows, int blocks, const void* x, int n_x_rows, void* y, int out_pitch, int out_f32,
+                        const CcPair* pairs, const int* n_pairs, int max_pairs, const float* gscales, int R,
+                        cudaStream_t stream, bool launch)
 {
-    if (K % kChunkK != 0 || R % 8 != 0 || R < 8 || max_passes < 0) return QG_ERR_UNSUPPORTED;
+    if (K % kChunkK != 0 || R % 8 != 0 || R < 8 || max_pairs < 0 || blocks < 1) return QG_ERR_UNSUPPORTED;
+    const int max_passes = max_pairs * blocks;
     const int sms = sm_count(-1);
     if (sms <= 0) return QG_ERR_CUDA;
     const int G = sms;
@@ -452,8 +476,10 @@ qg_status launch_cc_moe(const uint8_t* codes, const uint8_t* scales, int total_r
     const DebugState dbg = debug_state();
     a.wait_ns = dbg.wait_ns;
     a.starve = dbg.starve;
-    m.passes = passes;
-    m.n_passes = n_passes;
+    m.pairs = pairs;
+    m.n_pairs = n_pairs;
+    m.blocks = blocks;
+    m.expert_rows = expert_rows;
     m.gscales = gscales;
     m.out_pitch = out_pitch;
     m.max_local = max_local;
@@ -491,6 +517,7 @@ qg_status launch_cc_moe(const uint8_t* codes, const uint8_t* scales, int total_r
     a.smem_bar = so;
     so += bar_bytes;
     if (so > kCcSmemMax) return QG_ERR_UNSUPPORTED;
+    if (!launch) return QG_OK;
 
     CUtensorMap tmc, tms;
     memset(&tmc, 0, sizeof(tmc));

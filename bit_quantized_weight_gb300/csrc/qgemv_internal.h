@@ -43,11 +43,10 @@ struct GroupDesc {
     int out_row[8];
 };
 
-// One pass of the grouped CUDA-core MoE kernels: a unit of rows of one expert
-// together with one or two of its tokens.
-struct CcPass {
-    int w_row0;      // first weight row (gate row for SwiGLU)
-    int out_col0;    // first output column
+// A pair group of the grouped CUDA-core MoE kernels: one or two tokens of one
+// expert. Pass v of a launch is group v / blocks over the expert's row block
+// v % blocks.
+struct CcPair {
     int e;           // expert id (per-expert global scale)
     int ntok;        // 1 or 2
     int x_row[2];    // activation rows (x_row[1] repeats x_row[0] for one token)
@@ -167,8 +166,9 @@ qg_status launch_tc_grouped_nvfp4(const uint8_t* codes, const uint8_t* scales, i
                                   const GroupDesc* groups, const UnitDesc* units, const int* n_units,
                                   const float* gscales, int rows_per_unit, cudaStream_t stream);
 qg_status launch_cc_moe(const uint8_t* codes, const uint8_t* scales, int total_rows, int K, int swiglu, int up_offset,
-                        const void* x, int n_x_rows, void* y, int out_pitch, int out_f32, const CcPass* passes,
-                        const int* n_passes, int max_passes, const float* gscales, int R, cudaStream_t stream);
+                        int expert_rows, int blocks, const void* x, int n_x_rows, void* y, int out_pitch, int out_f32,
+                        const CcPair* pairs, const int* n_pairs, int max_pairs, const float* gscales, int R,
+                        cudaStream_t stream, bool launch = true);
 qg_status launch_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min,
                            int bits, const void* x, void* y, int out_f32, const void* residual, int M,
                            int N, int K, cudaStream_t stream);

@@ -146,6 +146,33 @@ def test_moe_small_shapes_with_scales(M, E, H, I, topk):
     check_moe(gu, dn, x, ids, w, y, h)
 
 
+def test_moe_tokens_sharing_experts():
+    """Every expert routed by several tokens (the CUDA-core kernels pair them
+    two per pass and repeat the expert's rows for a third and fourth), and
+    two tokens with identical routing."""
+    M, E, H, I, topk = 8, 5, 512, 512, 4
+    gu, dn, x = make_moe(14, E, H, I, M, g_range=(0.5, 2.0))
+    r = np.random.default_rng(15)
+    ids = np.stack([r.choice(E, topk, replace=False) for _ in range(M)]).astype(np.int32)
+    ids[5] = ids[2]
+    w = r.uniform(0.05, 1.0, (M, topk)).astype(np.float32).astype(np.float64)
+    y, h = run_moe(gu, dn, x, ids, w)
+    check_moe(gu, dn, x, ids, w, y, h)
+
+
+def test_moe_tcgen05_fallback_when_the_plan_does_not_fit():
+    """I = 3072: the down projection's activation rows overflow the CUDA-core
+    kernel's shared memory, so it runs on the tcgen05 grouped kernel while
+    gate/up stays on the CUDA cores."""
+    M, E, H, I, topk = 8, 16, 2048, 3072, 8
+    gu, dn, x = make_moe(16, E, H, I, M)
+    r = np.random.default_rng(17)
+    ids = np.stack([r.choice(E, topk, replace=False) for _ in range(M)]).astype(np.int32)
+    w = r.uniform(0.05, 1.0, (M, topk)).astype(np.float32).astype(np.float64)
+    y, h = run_moe(gu, dn, x, ids, w)
+    check_moe(gu, dn, x, ids, w, y, h)
+
+
 def test_moe_duplicate_and_invalid_expert_ids():
     M, E, H, I, topk = 4, 6, 256, 256, 3
     gu, dn, x = make_moe(8, E, H, I, M)
