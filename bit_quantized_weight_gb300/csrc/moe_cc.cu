@@ -195,14 +195,18 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
     uint8_t* lx = reinterpret_cast<uint8_t*>(ltab + m.max_rows);
     volatile int* n_rows_s = reinterpret_cast<volatile int*>(lx + (2 * m.max_local + 3) / 4 * 4);
 
+    // compute threads that own rows ((phase, gate/up) boxes x row groups x
+    // segments), rounded up to whole warps; the others only help convert the
+    // activations
+    const int n_act = (a.P * NGU * ((a.R + kCcRows - 1) / kCcRows) * NSEG + 31) / 32 * 32;
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.n_stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kCcThreads);
+            mbar_init(&empty[s], n_act);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&rfull[b], kCcThreads);
+            mbar_init(&rfull[b], n_act);
             mbar_init(&rempty[b], 1);
         }
         *abort_flag = 0;
@@ -355,6 +359,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
     named_barrier_sync(1, kCcThreads);
     moe_convert_rows(m, smem, ltab, *n_rows_s, warp, lane);
     named_barrier_sync(1, kCcThreads);
+    if (static_cast<int>(threadIdx.x) >= n_act) return;  // no rows: not waiting on every stage
 
     const CcGeom geom = cc_geom(a);
     const int rg_per_box = (a.R + kCcRows - 1) / kCcRows;
