@@ -108,13 +108,19 @@ using namespace qg;
 
 namespace {
 
-// NVFP4 with K a multiple of 256: one token on the CUDA-core kernel, more on
-// the tcgen05 kernel; shapes neither plan fits go to the mma.sync kernel.
+// NVFP4 with K a multiple of 256: one or two tokens on the CUDA-core kernel,
+// three to eight on the warp-MMA kernel (its cost does not grow with the
+// tokens); shapes neither plan fits go to the tcgen05 kernel, then the
+// mma.sync one.
 qg_status dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y, int f32,
                       const void* residual, int M, int N, int K, int swiglu, cudaStream_t stream)
 {
     qg_status s = launch_cc_dense_nvfp4(codes, scales, g, x, y, f32, residual, M, N, K, swiglu, stream);
     if (s != QG_ERR_UNSUPPORTED) return s;
+    if (M >= 3) {
+        s = launch_mt_dense_nvfp4(codes, scales, g, x, y, f32, residual, M, N, K, swiglu, stream);
+        if (s != QG_ERR_UNSUPPORTED) return s;
+    }
     s = launch_tc_dense_nvfp4(codes, scales, g, x, y, f32, residual, M, N, K, swiglu, stream);
     if (s != QG_ERR_UNSUPPORTED) return s;
     return launch_dense_nvfp4(codes, scales, g, x, y, f32, residual, M, N, K, swiglu, stream);

@@ -1,0 +1,519 @@
+// qgemv_mt.cu -- NVFP4 decode GEMV for 1..8 tokens: the one-token kernel's
+// weight stream and plan, with each compute warp turning a 16-row block of
+// decoded weights into mma.sync fragments for all the tokens at once.
+//
+// What is computed follows the pages' NVFP4 format (NVIDIA NVFP4 blog, "How
+// NVFP4 works": E2M1 codes, one E4M3 scale per 16 values, one FP32 tensor
+// scale) and the decode fusions (NInfer article, section 2: fused residual
+// and SwiGLU epilogues; section 1: 1..8 lanes per decode round).
+//
+// Why a warp-level MMA: the CUDA-core kernel spends one multiply-add per
+// weight and token, so its instruction count grows with the tokens and at
+// two tokens it no longer keeps pace with HBM. Here one m16n8k16 MMA takes
+// 16 rows x 16 k of exactly decoded weights against the (up to) 8 tokens, so
+// the decode -- one cvt.rn.f16x2.e2m1x2 and one exact f16 multiply by the
+// block scale per weight pair (e2m1 x e4m3 has at most 6 significant bits
+// and lies in [2^-10, 2688]) -- is the whole per-weight cost, for any M <= 8.
+//
+//   * Units, phases, ring and TMA producer are the one-token kernel's
+//     (qgemv_cc.cu); box rows are padded to 16 in
+//     shared memory (zero rows), and warp w takes 16-row block w % NRB of
+//     box w / NRB for the box's 256-k chunk of the stage.
+//   * ldmatrix.x4 reads a 16-row x 64-k tile of the 128B-swizzled codes:
+//     register j holds the 8 codes k = 32 * (j / 2) + 8 * (lane % 4) + 0..7
+//     of row lane / 4 + 8 * (j % 2). The MMA's k slots 2c, 2c+1, 2c+8, 2c+9
+//     of thread c = lane % 4 take that thread's k + 0..3 (first MMA) or
+//     k + 4..7 (second); the activations are loaded in the same order, so the
+//     permutation of k is the same on both sides and the products are the
+//     dot product's.
+//   * Activations: every token's chunk of 256 k is prescaled exactly into
+//     f16 (maximum in [2^14, 2^15)), as in the one-token kernel; a chunk
+//     that any token cannot carry exactly stays raw bf16 for all tokens and
+//     its stages run bf16 MMAs on weights converted to bf16 (also exact).
+//     Per stage the MMAs accumulate in fp32, then acc += D * 2^-prescale of
+//     each token.
+//   * At a unit's end the warps' sums meet in shared memory and are added
+//     over phases in index order; the epilogue applies g, SwiGLU or the
+//     residual and rounds once. Every sum runs in a fixed order.
+#include <algorithm>
+#include <cstring>
+
+#include "cc_core.cuh"
+
+namespace qg {
+
+namespace {
+
+constexpr int kMtTokens = 8;    // the MMA's n
+constexpr int kMtXPad = 16;     // bytes between consecutive tokens' activation rows (bank spread)
+
+struct MtArgs {
+    CcArgs a;        // plan; a.R8 is the box pitch here (R rounded up to 16)
+    int M;           // tokens
+    int NRB;         // 16-row blocks per box
+    int W;           // chunks of activations held at a time (a multiple of P; C when all fit)
+    uint32_t x_tok;  // bytes between tokens' activations in shared memory
+};
+
+__device__ __forceinline__ void mt_ldmatrix_x4(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+template <bool BF>
+__device__ __forceinline__ void mt_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    if (BF)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Every token's activations of chunks w0 .. w0 + W - 1 (a window) into shared
+// memory: chunk kc = w0 + j of token t at smem_x + t * x_tok + j * 512 (k
+// order, f16 after the exact prescale, or raw bf16 when some token's chunk
+// does not fit f16), 2^-prescale at pe[t * W + j], the chunk's bf16 flag at
+// fl[j]. One warp per chunk.
+__device__ void mt_convert(const MtArgs& m, uint8_t* smem, int warp, int lane, volatile int* any_bf, int w0)
+{
+    const CcArgs& a = m.a;
+    uint8_t* xs = smem + a.smem_x;
+    float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
+    uint8_t* fl = smem + a.smem_fl;
+    const int w1 = min(a.C, w0 + m.W);
+    for (int kc = w0 + warp; kc < w1; kc += kCcWarps) {
+        const int j = kc - w0;
+        uint4 raw[kMtTokens];
+#pragma unroll
+        for (int t = 0; t < kMtTokens; ++t)
+            raw[t] = t < m.M ? ldg_nc_128(a.x + static_cast<size_t>(t) * a.K + static_cast<size_t>(kc) * kChunkK +
+                                          lane * 8)
+                             : make_uint4(0, 0, 0, 0);
+        int e[kMtTokens];
+        bool inexact = false;
+#pragma unroll
+        for (int t = 0; t < kMtTokens; ++t) {
+            e[t] = 0;
+            if (t >= m.M) continue;
+            const uint32_t wv[4] = {raw[t].x, raw[t].y, raw[t].z, raw[t].w};
+            uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) bf16_range_acc(wv[i], mx2, mn2);
+            uint32_t emax, emin, magmax;
+            bf16_range_fin(mx2, mn2, emax, emin, magmax);
+            emax = __reduce_max_sync(0xffffffffu, emax);
+            emin = __reduce_min_sync(0xffffffffu, emin);
+            if (emax == 0u) magmax = __reduce_max_sync(0xffffffffu, magmax);
+            e[t] = min(emax != 0u ? 141 - static_cast<int>(emax) : prescale_exponent(magmax), 126);
+            inexact = inexact || (emin != 255u && static_cast<int>(emin) - 127 + e[t] < -17);
+        }
+#pragma unroll
+        for (int t = 0; t < kMtTokens; ++t) {
+            if (t >= m.M) continue;
+            const uint32_t wv[4] = {raw[t].x, raw[t].y, raw[t].z, raw[t].w};
+            uint32_t o[4];
+            if (inexact) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[i] = wv[i];
+            } else {
+                const float sc = __int_as_float((127 + e[t]) << 23);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = pack_f16x2(__uint_as_float(wv[i] << 16) * sc, __uint_as_float(wv[i] & 0xFFFF0000u) * sc);
+            }
+            *reinterpret_cast<uint4*>(xs + t * m.x_tok + j * (kChunkK * 2) + lane * 16) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+            if (lane == 0) pe[t * m.W + j] = inexact ? 1.0f : __int_as_float((127 - e[t]) << 23);
+        }
+        if (lane == 0) {
+            fl[j] = inexact ? 1 : 0;
+            if (inexact) *any_bf = 1;
+        }
+    }
+    // tokens M..7 of the MMA read zeros: their activation rows are never loaded
+}
+
+// One warp, one stage: rows 16 rb .. 16 rb + 15 of box b2 over the stage's
+// 256 k; d[] gets the MMA sums (rows g, g + 8; tokens 2c, 2c + 1), built in
+// two independent chains (the first and second MMA of each 32-k half) that
+// are added at the end.
+template <bool BF>
+__device__ __forceinline__ void mt_stage(uint32_t box, uint32_t sbox, uint32_t xc, int lane, int M, float (&d)[4])
+{
+    float d2[4] = {0.f, 0.f, 0.f, 0.f};
+    const int g = lane >> 2, c = lane & 3;
+    const int lr = (lane & 7) + 8 * ((lane >> 3) & 1);
+    const bool tok = g < M;
+#pragma unroll
+    for (int ti = 0; ti < 4; ++ti) {
+        uint32_t cr[4];
+        const int lc = 2 * ti + (lane >> 4);
+        mt_ldmatrix_x4(cr, box + static_cast<uint32_t>(lr) * 128u + ((static_cast<uint32_t>(lc ^ (lr & 7))) << 4));
+        const uint32_t sw_g = lds32(sbox + static_cast<uint32_t>(g) * 16u + 4u * ti);
+        const uint32_t sw_g8 = lds32(sbox + static_cast<uint32_t>(g + 8) * 16u + 4u * ti);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+            const uint4 bx = tok ? lds128(xc + static_cast<uint32_t>(64 * ti + 32 * ch + 8 * c) * 2u)
+                                 : make_uint4(0, 0, 0, 0);
+            // 16-k block 4 ti + 2 ch + c / 2: its E4M3 byte twice, converted,
+            // is the scale in both halves
+            const uint32_t sel = static_cast<uint32_t>((2 * ch + (c >> 1)) * 0x11);
+            const uint32_t s_g = e4m3x2_to_f16x2(__byte_perm(sw_g, 0, sel));
+            const uint32_t s_g8 = e4m3x2_to_f16x2(__byte_perm(sw_g8, 0, sel));
+            uint32_t pg[4], pg8[4];
+            e2m1x8_to_f16x2x4(cr[2 * ch], pg);
+            e2m1x8_to_f16x2x4(cr[2 * ch + 1], pg8);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                pg[b] = hmul2(pg[b], s_g);
+                pg8[b] = hmul2(pg8[b], s_g8);
+                if (BF) {
+                    pg[b] = f16x2_to_bf16x2(pg[b]);
+                    pg8[b] = f16x2_to_bf16x2(pg8[b]);
+                }
+            }
+            const uint32_t A0[4] = {pg[0], pg8[0], pg[1], pg8[1]};
+            const uint32_t A1[4] = {pg[2], pg8[2], pg[3], pg8[3]};
+            mt_mma<BF>(d, A0, bx.x, bx.y);
+            mt_mma<BF>(d2, A1, bx.z, bx.w);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] += d2[i];
+}
+
+// The compute warps' unit loop. Window w0 = 0 is converted on entry; a
+// stage in another window first converts it (all compute warps, between two
+// barriers; the weight copies keep landing in the ring meanwhile).
+template <int EPI, bool MIXED>
+__device__ __forceinline__ void mt_units(const MtArgs& m, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                         volatile int* abort_flag, volatile int* any_bf, int warp, int lane)
+{
+    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
+    const CcArgs& a = m.a;
+    const int M = m.M;
+    const int b2 = warp / m.NRB;
+    const int rb = warp % m.NRB;
+    const bool active = b2 < a.P * NGU;
+    const int p = active ? b2 / NGU : 0;
+    const int n_mine = active ? max(0, (a.C - p + a.P - 1) / a.P) : 0;
+    const int g = lane >> 2, c = lane & 3;
+    const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
+    const uint8_t* fl = smem + a.smem_fl;
+    float* red = reinterpret_cast<float*>(smem + a.smem_red);
+    const uint32_t ring = smem_u32(smem + a.smem_ring);
+    const uint32_t box_off = static_cast<uint32_t>(b2 * a.R8 + 16 * rb) * 128u;
+    const uint32_t sbox_off = a.scales_off + static_cast<uint32_t>(b2 * a.R8 + 16 * rb) * 16u;
+    const uint32_t x0 = smem_u32(smem + a.smem_x) + static_cast<uint32_t>(g) * m.x_tok;
+    const int t0 = 2 * c, t1 = 2 * c + 1;
+
+    bool aborted = false;
+    int slot = 0, lap = 0, cur_win = 0;
+    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int cc = 0; cc < a.Cp; ++cc) {
+            const int win = (cc * a.P) / m.W;  // the stage's chunks lie in one window
+            if (win != cur_win) {
+                named_barrier_sync(1, kCcThreads);
+                mt_convert(m, smem, warp, lane, any_bf, win * m.W);
+                named_barrier_sync(1, kCcThreads);
+                cur_win = win;
+            }
+            if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
+            if (!aborted && cc < n_mine) {
+                const int kc = cc * a.P + p;
+                const int j = kc - win * m.W;
+                const uint32_t stage = ring + slot * a.stage_bytes;
+                const uint32_t xc = x0 + static_cast<uint32_t>(j) * (kChunkK * 2u);
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                if (MIXED && fl[j] != 0)
+                    mt_stage<true>(stage + box_off, stage + sbox_off, xc, lane, M, d);
+                else
+                    mt_stage<false>(stage + box_off, stage + sbox_off, xc, lane, M, d);
+                const float pe0 = t0 < M ? pe_all[t0 * m.W + j] : 0.f;
+                const float pe1 = t1 < M ? pe_all[t1 * m.W + j] : 0.f;
+                acc[0] = fmaf(d[0], pe0, acc[0]);
+                acc[1] = fmaf(d[1], pe1, acc[1]);
+                acc[2] = fmaf(d[2], pe0, acc[2]);
+                acc[3] = fmaf(d[3], pe1, acc[3]);
+            }
+            mbar_arrive(&empty[slot]);
+            if (++slot == a.n_stages) {
+                slot = 0;
+                ++lap;
+            }
+        }
+
+        // the warps' sums by (box, row, token), then phases in index order
+        if (active) {
+            const int r = 16 * rb + g;
+            float* rw = red + static_cast<size_t>(b2 * a.R8 + r) * kMtTokens;
+            rw[t0] = acc[0];
+            rw[t1] = acc[1];
+            rw[8 * kMtTokens + t0] = acc[2];
+            rw[8 * kMtTokens + t1] = acc[3];
+        }
+        named_barrier_sync(1, kCcThreads);
+        if (!aborted) {
+            const int r0 = u * a.R;
+            for (int it = threadIdx.x; it < a.R * M; it += kCcThreads) {
+                const int r = it % a.R, t = it / a.R;
+                if (r0 + r >= a.n_out) continue;
+                float v[NGU];
+#pragma unroll
+                for (int gg = 0; gg < NGU; ++gg) {
+                    float s = 0.f;
+                    for (int pp = 0; pp < a.P; ++pp) s += red[static_cast<size_t>((pp * NGU + gg) * a.R8 + r) * 8 + t];
+                    v[gg] = s * a.g;
+                }
+                float val = v[0];
+                if (EPI == EPI_SWIGLU) val = (val / (1.0f + expf(-val))) * v[NGU - 1];
+                const size_t o = static_cast<size_t>(t) * a.n_out + r0 + r;
+                if (EPI == EPI_RESID) val += bf16_bits_to_f32(a.residual[o]);
+                if (a.out_f32)
+                    reinterpret_cast<float*>(a.y)[o] = val;
+                else
+                    reinterpret_cast<uint16_t*>(a.y)[o] = f32_to_bf16_bits_rn(val);
+            }
+        }
+        named_barrier_sync(1, kCcThreads);  // red is rewritten by the next unit
+    }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kCcAllThreads, 1)
+    mt_gemv_kernel(const __grid_constant__ MtArgs m, const __grid_constant__ CUtensorMap tm_codes,
+                   const __grid_constant__ CUtensorMap tm_scales)
+{
+    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
+    const CcArgs& a = m.a;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = warp_index_uniform();
+    const int lane = threadIdx.x & 31;
+
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.smem_bar);
+    uint64_t* empty = full + kCcMaxStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCcMaxStages);
+    volatile int* any_bf = abort_flag + 1;
+
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.n_stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCcThreads);
+        }
+        *abort_flag = 0;
+        *any_bf = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kCcTmaWarp) {
+        // ------------------------------------------------------------ producer (qgemv_cc.cu's)
+        if (elect_one()) {
+            prefetch_tensormap(&tm_codes);
+            prefetch_tensormap(&tm_scales);
+        }
+        __syncwarp();
+        int slot = 0, lap = 0, issued = 0;
+        bool stop = false;
+        for (int u = blockIdx.x; u < a.n_units && !stop; u += gridDim.x) {
+            const int row0 = u * a.R;
+            for (int c = 0; c < a.Cp; ++c) {
+                if (lap > 0 && !cc_wait_warp(&empty[slot], (lap - 1) & 1, a, abort_flag)) {
+                    stop = true;
+                    break;
+                }
+                if (issued == kCcLeadStages) asm volatile("griddepcontrol.wait;" ::: "memory");
+                if (*abort_flag || a.starve) {
+                    stop = true;
+                    break;
+                }
+                int live = 0;
+                for (int pp = 0; pp < a.P; ++pp) live += (c * a.P + pp < a.C) ? 1 : 0;
+                uint8_t* sb = smem + a.smem_ring + slot * a.stage_bytes;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live * NGU) * a.box_tx);
+                    for (int pp = 0; pp < a.P; ++pp) {
+                        const int kc = c * a.P + pp;
+                        if (kc >= a.C) continue;
+#pragma unroll
+                        for (int gg = 0; gg < NGU; ++gg) {
+                            const int b2 = pp * NGU + gg;
+                            const int row = row0 + gg * a.up_row_offset;
+                            tma_load_2d(sb + b2 * a.R8 * 128, &tm_codes, kc * (kChunkK / 2), row, &full[slot]);
+                            tma_load_2d(sb + a.scales_off + b2 * a.R8 * 16, &tm_scales, kc * (kChunkK / 16), row,
+                                        &full[slot]);
+                        }
+                    }
+                }
+                __syncwarp();
+                ++issued;
+                if (++slot == a.n_stages) {
+                    slot = 0;
+                    ++lap;
+                }
+            }
+        }
+        if (lane == 0)
+            for (int g = max(0, issued - a.n_stages); g < issued; ++g)
+                mbar_wait_bounded(&full[g % a.n_stages], (g / a.n_stages) & 1, a.wait_ns, a.status);
+        __syncwarp();
+        return;
+    }
+
+    // ---------------------------------------------------------------- compute warps
+    {
+        const uint32_t roff[4] = {0u, a.scales_off, 0u, 0u}, rbytes[4] = {128u, 16u, 0u, 0u};
+        cc_zero_padding(a, smem, a.P * NGU, roff, rbytes, 2);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    mt_convert(m, smem, warp, lane, any_bf, 0);
+    named_barrier_sync(1, kCcThreads);
+    // with several windows a later one may hold raw-bf16 chunks: the mixed loop
+    if (*any_bf || m.W < a.C)
+        mt_units<EPI, true>(m, smem, full, empty, abort_flag, any_bf, warp, lane);
+    else
+        mt_units<EPI, false>(m, smem, full, empty, abort_flag, any_bf, warp, lane);
+}
+
+constexpr uint32_t align_up(uint32_t v, uint32_t al) { return (v + al - 1) / al * al; }
+
+template <int EPI>
+qg_status mt_launch(MtArgs m, const CUtensorMap& tmc, const CUtensorMap& tms, int grid, cudaStream_t stream)
+{
+    constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
+    CcArgs& a = m.a;
+    a.status = device_status_ptr();
+    if (!a.status) return QG_ERR_CUDA;
+    const DebugState dbg = debug_state();
+    a.wait_ns = dbg.wait_ns;
+    a.starve = dbg.starve;
+
+    const uint32_t nbox = static_cast<uint32_t>(a.P * NGU);
+    a.scales_off = nbox * a.R8 * 128u;
+    a.stage_bytes = align_up(a.scales_off + nbox * a.R8 * 16u, 1024);
+    a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
+    const uint32_t red_bytes = align_up(nbox * a.R8 * 4u * kMtTokens, 128);
+    const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
+    // the activation window: all of K if it fits beside a ring of at least
+    // four stages, else the largest multiple of P chunks that leaves three
+    auto win_bytes = [&](int W) {
+        const uint32_t xt = static_cast<uint32_t>(W) * kChunkK * 2u + kMtXPad;
+        return align_up(static_cast<uint32_t>(m.M) * xt, 128) + align_up(static_cast<uint32_t>(m.M * W) * 4u, 16) +
+               align_up(static_cast<uint32_t>(W), 16);
+    };
+    const uint32_t other = red_bytes + bar_bytes;
+    int W = a.C;
+    if (win_bytes(W) + other + 4 * a.stage_bytes > kCcSmemMax) {
+        W = (a.C / a.P) * a.P;
+        while (W > a.P && win_bytes(W) + other + 3 * a.stage_bytes > kCcSmemMax) W -= a.P;
+    }
+    if (win_bytes(W) + other + 3 * a.stage_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
+    m.W = W;
+    m.x_tok = static_cast<uint32_t>(W) * kChunkK * 2u + kMtXPad;
+    const uint32_t x_bytes = align_up(static_cast<uint32_t>(m.M) * m.x_tok, 128);
+    const uint32_t pe_bytes = align_up(static_cast<uint32_t>(m.M * W) * 4u, 16);
+    const uint32_t fl_bytes = align_up(static_cast<uint32_t>(W), 16);
+    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + red_bytes + bar_bytes;
+    a.n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / a.stage_bytes));
+    uint32_t so = 0;
+    a.smem_ring = so;
+    so += a.n_stages * a.stage_bytes;
+    a.smem_x = so;
+    so += x_bytes;
+    a.smem_pe = so;
+    so += pe_bytes;
+    a.smem_fl = so;
+    so += fl_bytes;
+    a.smem_red = so;
+    so += red_bytes;
+    a.smem_bar = so;
+    so += bar_bytes;
+    if (so > kCcSmemMax) return QG_ERR_UNSUPPORTED;
+
+    auto kern = mt_gemv_kernel<EPI>;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCcSmemMax) != cudaSuccess)
+            return QG_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kCcAllThreads);
+    cfg.dynamicSmemBytes = so;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, m, tmc, tms) != cudaSuccess) return QG_ERR_CUDA;
+    return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+}  // namespace
+
+// 1..8 tokens, K a multiple of 256; QG_ERR_UNSUPPORTED otherwise or when the
+// plan does not fit shared memory.
+qg_status launch_mt_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
+                                int out_f32, const void* residual, int M, int N, int K, int swiglu,
+                                cudaStream_t stream)
+{
+    if (M < 1 || M > kMtTokens || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
+    const int ngu = swiglu ? 2 : 1;
+    const int n_out = swiglu ? N / 2 : N;
+    const int sms = sm_count(-1);
+    if (sms <= 0) return QG_ERR_CUDA;
+    // the one-token rule for R (equal bytes per SM), then 16-row blocks: at
+    // most 16 warps' worth of (phase, gate/up, block) per stage
+    int R = 1;
+    for (int U = 1;; ++U) {
+        R = (n_out + sms * U - 1) / (sms * U);
+        if (ngu * ((R + 15) / 16) <= kCcWarps) break;
+    }
+    R = std::max(R, 1);
+    MtArgs m{};
+    CcArgs& a = m.a;
+    a.x = static_cast<const uint16_t*>(x);
+    a.y = y;
+    a.residual = static_cast<const uint16_t*>(residual);
+    a.K = K;
+    a.C = K / kChunkK;
+    a.n_out = n_out;
+    a.R = R;
+    a.R8 = (R + 15) / 16 * 16;
+    m.NRB = a.R8 / 16;
+    a.P = std::max(1, std::min(kCcWarps / (ngu * m.NRB), a.C));
+    a.Cp = (a.C + a.P - 1) / a.P;
+    a.up_row_offset = swiglu ? n_out : 0;
+    a.out_f32 = swiglu ? 0 : out_f32;
+    a.g = g;
+    a.n_units = (n_out + R - 1) / R;
+    m.M = M;
+    const int grid = std::min(sms, a.n_units);
+    CUtensorMap tmc, tms;
+    memset(&tmc, 0, sizeof(tmc));
+    memset(&tms, 0, sizeof(tms));
+    if (!encode_tmap_2d(&tmc, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, R, true) ||
+        !encode_tmap_2d(&tms, scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 16, N, 16, R, false))
+        return QG_ERR_CUDA;
+    if (swiglu) return mt_launch<EPI_SWIGLU>(m, tmc, tms, grid, stream);
+    if (residual) return mt_launch<EPI_RESID>(m, tmc, tms, grid, stream);
+    return mt_launch<EPI_NONE>(m, tmc, tms, grid, stream);
+}
+
+}  // namespace qg

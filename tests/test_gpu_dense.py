@@ -245,6 +245,25 @@ def test_nvfp4_wide_dynamic_range_activations(M):
     check_out(run_nvfp4(w, x, torch.bfloat16), yref, a, "wide-range bf16")
 
 
+@pytest.mark.parametrize("M", [4, 8])
+def test_nvfp4_activation_windows_with_wide_range_chunks(M):
+    """K = 17408 at four and eight tokens: the warp-MMA kernel holds the
+    activations a window of chunks at a time; chunks in later windows whose
+    values f16 cannot carry exactly (for one token only) switch those stages
+    to bf16 operands."""
+    N, K = 600, 17408
+    w = synth.nvfp4_weights(24, "win", N, K)
+    x = synth.bf16_normal(25, "winx", (M, K))
+    wide = wide_range_x(1, K, 26)
+    for kc in (3, 40, 41, 66):                       # one token, chunks spread over the windows
+        x[M - 1, kc * 256:(kc + 1) * 256] = wide[0, kc * 256:(kc + 1) * 256]
+    yref, a = O.gemv_nvfp4(w, x)
+    check_out(run_nvfp4(w, x, torch.float32), yref, a, f"windows M={M}")
+    r = synth.bf16_normal(27, "winr", (M, N))
+    yref, a = O.gemv_nvfp4(w, x, residual=r)
+    check_out(run_nvfp4(w, x, torch.bfloat16, residual=r), yref, a, f"windows + residual M={M}")
+
+
 @pytest.mark.parametrize("bits", [4, 5])
 @pytest.mark.parametrize("M", [1, 2, 8])
 def test_q45_wide_dynamic_range_activations(bits, M):
