@@ -163,16 +163,18 @@ class ClockSampler:
 
 
 # Kernel sources behind each workload's launches (one or two tokens: the
-# CUDA-core kernels; NVFP4 with more tokens and the MoE: the tcgen05 kernel;
-# Q4/Q5 with more tokens: the mma.sync kernel, and the exact fallback kernel
-# for the normalised and fused groupwise-int ops); a committed traffic figure
-# is used only while these files are unchanged.
+# CUDA-core kernels; NVFP4 with three to eight tokens: the warp-MMA kernel;
+# the MoE: the grouped CUDA-core expert kernels; Q4/Q5 with more tokens: the
+# mma.sync kernel, and the exact fallback kernel for the normalised and fused
+# groupwise-int ops); a committed traffic figure is used only while these
+# files are unchanged.
 KERNEL_SOURCES = {
     "simple": ("qgemv_simple.cu", "common.cuh", "qgemv_internal.h"),
     "cc": ("qgemv_cc.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
     "tc": ("qgemv_tc.cu", "tcgen05.cuh", "common.cuh", "qgemv_internal.h"),
     "mma": ("qgemv_dense.cu", "common.cuh", "qgemv_internal.h"),
-    "moe": ("qgemv_tc.cu", "moe.cu", "tcgen05.cuh", "common.cuh", "qgemv_internal.h"),
+    "mt": ("qgemv_mt.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
+    "moe": ("moe_cc.cu", "moe.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
     "chain": ("qgemv_chain.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
 }
 
@@ -184,7 +186,7 @@ def kernel_family(workload, M):
         return "simple"
     if M <= 2:
         return "cc"
-    return "mma" if workload == "q45" else "tc"
+    return "mma" if workload == "q45" else "mt"
 
 
 def kernel_source_hash(family):
@@ -688,7 +690,9 @@ def arithmetic(workload, M):
         return "fp32 FMA on CUDA cores (exact fallback kernel for the normalised and fused ops), bf16 mma.sync for the rest"
     if workload == "q45":
         return "bf16 mma.sync, f32 accumulate (codes exact in bf16, raw bf16 activations)"
-    return "f16 tcgen05 MMA, f32 accumulate (exact decoded weights, prescaled activations)"
+    if workload == "moe":
+        return "f16 x f16 -> f32 FMA on CUDA cores (exact decoded weights, prescaled activations)"
+    return "f16 mma.sync m16n8k16, f32 accumulate (exact decoded weights, prescaled activations)"
 
 
 def measure(args, kind, M, world, rank, stream, cpu=True, e2e=True):
@@ -875,7 +879,7 @@ def measure(args, kind, M, world, rank, stream, cpu=True, e2e=True):
 
 
 # Every configuration besides the headline one, measured in the same run.
-SWEEP = [("dense", 2), ("dense", 4), ("dense", 8), ("q45", 1), ("q45", 8), ("q45ffn", 1), ("tiny", 1), ("moe", 8)]
+SWEEP = [("dense", 2), ("dense", 4), ("dense", 8), ("q45", 1), ("q45", 2), ("q45", 8), ("q45ffn", 1), ("tiny", 1), ("moe", 8)]
 
 
 def main():
