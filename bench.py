@@ -163,11 +163,11 @@ class ClockSampler:
 
 
 # Kernel sources behind each workload's launches (one or two tokens: the
-# CUDA-core kernels; NVFP4 with three to eight tokens: the warp-MMA kernel;
-# the MoE: the grouped CUDA-core expert kernels; Q4/Q5 with more tokens: the
-# mma.sync kernel, and the exact fallback kernel for the normalised and fused
-# groupwise-int ops); a committed traffic figure is used only while these
-# files are unchanged.
+# CUDA-core kernels; NVFP4 with three to eight tokens and Q4/Q5 with three to
+# six: the warp-MMA kernel; Q4/Q5 with seven or eight: the mma.sync kernel;
+# the MoE: the grouped CUDA-core expert kernels; the exact fallback kernel for
+# the normalised and fused groupwise-int ops at three or more tokens); a
+# committed traffic figure is used only while these files are unchanged.
 KERNEL_SOURCES = {
     "simple": ("qgemv_simple.cu", "common.cuh", "qgemv_internal.h"),
     "cc": ("qgemv_cc.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
@@ -186,7 +186,9 @@ def kernel_family(workload, M):
         return "simple"
     if M <= 2:
         return "cc"
-    return "mma" if workload == "q45" else "mt"
+    if workload == "q45":
+        return "mt" if M <= 6 else "mma"
+    return "mt"
 
 
 def kernel_source_hash(family):
@@ -688,6 +690,8 @@ def arithmetic(workload, M):
         return "f16 x f16 -> f32 FMA on CUDA cores (codes as exact f16, prescaled activations)"
     if workload == "q45ffn":
         return "fp32 FMA on CUDA cores (exact fallback kernel for the normalised and fused ops), bf16 mma.sync for the rest"
+    if workload == "q45" and M <= 6:
+        return "f16 mma.sync m16n8k16, f32 accumulate (codes as exact f16, prescaled activations)"
     if workload == "q45":
         return "bf16 mma.sync, f32 accumulate (codes exact in bf16, raw bf16 activations)"
     if workload == "moe":

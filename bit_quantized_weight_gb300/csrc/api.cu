@@ -126,6 +126,20 @@ qg_status dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, cons
     return launch_dense_nvfp4(codes, scales, g, x, y, f32, residual, M, N, K, swiglu, stream);
 }
 
+// Q4/Q5 with 3..8 tokens: the warp-MMA kernel up to six tokens. It converts
+// every token's activations at its start, which at seven and eight tokens
+// costs more than its faster stage saves over the groupwise mma.sync kernel
+// (raw bf16 activations brought in with each stage): measured on one box for
+// the Q4/Q5 layer, 130 vs 154 us at M = 3, 146 vs 151 us at M = 6, 161 vs
+// 150 us at M = 8.
+qg_status q45_multi_token(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min, int bits,
+                          const void* x, void* y, int f32, const void* residual, int M, int N, int K,
+                          cudaStream_t stream)
+{
+    if (M < 3 || M > 6) return QG_ERR_UNSUPPORTED;
+    return launch_mt_dense_q45(q_lo, q_hi, scale, min, bits, x, y, f32, residual, M, N, K, stream);
+}
+
 // Validation of one qg_gemv_op record (qgemv_chain, qgemv_swiglu_q45).
 qg_status check_op(const qg_gemv_op& g, int M)
 {
@@ -237,9 +251,13 @@ qg_status run_op(const qg_gemv_op& g, int M, cudaStream_t stream)
         qg_status s = launch_cc_dense_q45(g.codes, g.q_hi, g.scales, g.mins, bits, g.x, g.y, f32, g.residual, M,
                                           g.N, g.K, stream, g.norm_weight, g.norm_eps);
         if (s != QG_ERR_UNSUPPORTED) return s;
-        if (!g.norm_weight)
+        if (!g.norm_weight) {
+            s = q45_multi_token(g.codes, g.q_hi, g.scales, g.mins, bits, g.x, g.y, f32, g.residual, M, g.N, g.K,
+                                stream);
+            if (s != QG_ERR_UNSUPPORTED) return s;
             return launch_dense_q45(g.codes, g.q_hi, g.scales, g.mins, bits, g.x, g.y, f32, g.residual, M, g.N,
                                     g.K, stream);
+        }
     }
     return run_op_simple(g, M, stream);
 }
@@ -275,6 +293,8 @@ qg_status qgemv_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale,
     const int f32 = y_dtype == QG_OUT_F32;
     if (K % kChunkK == 0) {
         s = launch_cc_dense_q45(q_lo, q_hi, scale, min, bits, x, y, f32, residual, M, N, K, stream);
+        if (s != QG_ERR_UNSUPPORTED) return s;
+        s = q45_multi_token(q_lo, q_hi, scale, min, bits, x, y, f32, residual, M, N, K, stream);
         if (s != QG_ERR_UNSUPPORTED) return s;
         return launch_dense_q45(q_lo, q_hi, scale, min, bits, x, y, f32, residual, M, N, K, stream);
     }

@@ -1,6 +1,7 @@
-// qgemv_mt.cu -- NVFP4 decode GEMV for 1..8 tokens: the one-token kernel's
-// weight stream and plan, with each compute warp turning a 16-row block of
-// decoded weights into mma.sync fragments for all the tokens at once.
+// qgemv_mt.cu -- NVFP4 and groupwise-int Q4/Q5 decode GEMV for 3..8 tokens:
+// the one-token kernel's weight stream and plan, with each compute warp
+// turning a 16-row block of decoded weights into mma.sync fragments for all
+// the tokens at once.
 //
 // What is computed follows the pages' NVFP4 format (NVIDIA NVFP4 blog, "How
 // NVFP4 works": E2M1 codes, one E4M3 scale per 16 values, one FP32 tensor
@@ -32,6 +33,15 @@
 //     its stages run bf16 MMAs on weights converted to bf16 (also exact).
 //     Per stage the MMAs accumulate in fp32, then acc += D * 2^-prescale of
 //     each token.
+//   * Q4/Q5 (NInfer article, section 2: the groupwise-int recipe): a masked
+//     nibble pair of a code word is an f16 pair of subnormals (q_j, q_j+4) *
+//     2^-24 with no conversion (Q5 ORs the fifth bit from its plane), the
+//     activations are stored paired (x_j, x_j+4) to match, and the two MMAs
+//     of one 32-k half-tile are exactly one group of 32: per row and token
+//     acc += 2^24 * scale * D * 2^-prescale + min * sum(x), with sum(x) per
+//     (token, group) taken once per window from the values the projection
+//     reads. A raw-bf16 chunk runs bf16 MMAs on the codes as bf16 integers
+//     (128 + q - 128, exact).
 //   * At a unit's end the warps' sums meet in shared memory and are added
 //     over phases in index order; the epilogue applies g, SwiGLU or the
 //     residual and rounds once. Every sum runs in a fixed order.
@@ -54,6 +64,18 @@ struct MtArgs {
     int W;           // chunks of activations held at a time (a multiple of P; C when all fit)
     uint32_t x_tok;  // bytes between tokens' activations in shared memory
 };
+
+// codes, scales, then (groupwise int) mins and the Q5 plane
+struct MtMaps {
+    CUtensorMap m[4];
+};
+
+__device__ __forceinline__ uint32_t mt_bsub2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
 
 __device__ __forceinline__ void mt_ldmatrix_x4(uint32_t (&r)[4], uint32_t addr)
 {
@@ -83,13 +105,17 @@ __device__ __forceinline__ void mt_mma(float (&d)[4], const uint32_t (&a)[4], ui
 // memory: chunk kc = w0 + j of token t at smem_x + t * x_tok + j * 512 (k
 // order, f16 after the exact prescale, or raw bf16 when some token's chunk
 // does not fit f16), 2^-prescale at pe[t * W + j], the chunk's bf16 flag at
-// fl[j]. One warp per chunk.
+// fl[j]. One warp per chunk. Q45: each lane's 8 values stored paired (x0,
+// x4)(x1, x5)(x2, x6)(x3, x7), and the sum of each group of 32 values (from
+// the bf16 values) at gx[(t * W + j) * 8 + group].
+template <bool Q45>
 __device__ void mt_convert(const MtArgs& m, uint8_t* smem, int warp, int lane, volatile int* any_bf, int w0)
 {
     const CcArgs& a = m.a;
     uint8_t* xs = smem + a.smem_x;
     float* pe = reinterpret_cast<float*>(smem + a.smem_pe);
     uint8_t* fl = smem + a.smem_fl;
+    float* gx = reinterpret_cast<float*>(smem + a.smem_gx);
     const int w1 = min(a.C, w0 + m.W);
     for (int kc = w0 + warp; kc < w1; kc += kCcWarps) {
         const int j = kc - w0;
@@ -130,6 +156,21 @@ __device__ void mt_convert(const MtArgs& m, uint8_t* smem, int warp, int lane, v
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     o[i] = pack_f16x2(__uint_as_float(wv[i] << 16) * sc, __uint_as_float(wv[i] & 0xFFFF0000u) * sc);
+            }
+            if constexpr (Q45) {
+                float sx = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    sx += bf16_bits_to_f32((i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu));
+                sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+                sx += __shfl_xor_sync(0xffffffffu, sx, 2);
+                if ((lane & 3) == 0) gx[(t * m.W + j) * 8 + (lane >> 2)] = sx;
+                const uint32_t p0 = __byte_perm(o[0], o[2], 0x5410), p1 = __byte_perm(o[0], o[2], 0x7632);
+                const uint32_t p2 = __byte_perm(o[1], o[3], 0x5410), p3 = __byte_perm(o[1], o[3], 0x7632);
+                o[0] = p0;
+                o[1] = p1;
+                o[2] = p2;
+                o[3] = p3;
             }
             *reinterpret_cast<uint4*>(xs + t * m.x_tok + j * (kChunkK * 2) + lane * 16) =
                 make_uint4(o[0], o[1], o[2], o[3]);
@@ -195,7 +236,74 @@ __device__ __forceinline__ void mt_stage(uint32_t box, uint32_t sbox, uint32_t x
 // The compute warps' unit loop. Window w0 = 0 is converted on entry; a
 // stage in another window first converts it (all compute warps, between two
 // barriers; the weight copies keep landing in the ring meanwhile).
-template <int EPI, bool MIXED>
+// Q4/Q5, one warp, one stage: rows 16 rb .. 16 rb + 15 over the stage's
+// 256 k (8 groups of 32). Per group the two MMAs give D = sum(q x) (times
+// 2^-24 on the f16 path); aq collects scale * D, am collects min * sum(x),
+// per (row g or g + 8, token 2c or 2c + 1).
+template <int BITS, bool BF>
+__device__ __forceinline__ void mtq_stage(uint32_t box, uint32_t sbox, uint32_t mbox, uint32_t hbox, uint32_t xc,
+                                          const float* gxt0, const float* gxt1, int lane, int M, float (&aq)[4],
+                                          float (&am)[4])
+{
+    const int g = lane >> 2, c = lane & 3;
+    const int lr = (lane & 7) + 8 * ((lane >> 3) & 1);
+    const bool tok = g < M;
+#pragma unroll
+    for (int ti = 0; ti < 4; ++ti) {
+        uint32_t cr[4];
+        const int lc = 2 * ti + (lane >> 4);
+        mt_ldmatrix_x4(cr, box + static_cast<uint32_t>(lr) * 128u + ((static_cast<uint32_t>(lc ^ (lr & 7))) << 4));
+        // the two groups of this tile: scale and min of rows g and g + 8
+        const uint32_t sg = lds32(sbox + static_cast<uint32_t>(g) * 16u + 4u * ti);
+        const uint32_t sg8 = lds32(sbox + static_cast<uint32_t>(g + 8) * 16u + 4u * ti);
+        const uint32_t mg = lds32(mbox + static_cast<uint32_t>(g) * 16u + 4u * ti);
+        const uint32_t mg8 = lds32(mbox + static_cast<uint32_t>(g + 8) * 16u + 4u * ti);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+            const int grp = 2 * ti + ch;
+            uint32_t hs_g = 0, hs_g8 = 0;
+            if (BITS == 5) {
+                const uint32_t hb = static_cast<uint32_t>(8 * ti + 4 * ch + c);  // plane byte of k .. k + 7
+                const uint32_t h8 = lds8(hbox + static_cast<uint32_t>(g) * 32u + hb);
+                const uint32_t h88 = lds8(hbox + static_cast<uint32_t>(g + 8) * 32u + hb);
+                hs_g = ((h8 & 0x0Fu) << 4) | ((h8 & 0xF0u) << 16);
+                hs_g8 = ((h88 & 0x0Fu) << 4) | ((h88 & 0xF0u) << 16);
+            }
+            uint32_t z[4], z8[4];
+            q45_pairs<BITS>(cr[2 * ch], hs_g, z);
+            q45_pairs<BITS>(cr[2 * ch + 1], hs_g8, z8);
+            if (BF) {
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    z[b] = mt_bsub2(z[b] | 0x43004300u, 0x43004300u);
+                    z8[b] = mt_bsub2(z8[b] | 0x43004300u, 0x43004300u);
+                }
+            }
+            const uint4 bx = tok ? lds128(xc + static_cast<uint32_t>(64 * ti + 32 * ch + 8 * c) * 2u)
+                                 : make_uint4(0, 0, 0, 0);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t A0[4] = {z[0], z8[0], z[1], z8[1]};
+            const uint32_t A1[4] = {z[2], z8[2], z[3], z8[3]};
+            mt_mma<BF>(d, A0, bx.x, bx.y);
+            mt_mma<BF>(d, A1, bx.z, bx.w);
+            const float s_g = half_bits_to_f32(ch ? (sg >> 16) : (sg & 0xFFFFu));
+            const float s_g8 = half_bits_to_f32(ch ? (sg8 >> 16) : (sg8 & 0xFFFFu));
+            const float m_g = half_bits_to_f32(ch ? (mg >> 16) : (mg & 0xFFFFu));
+            const float m_g8 = half_bits_to_f32(ch ? (mg8 >> 16) : (mg8 & 0xFFFFu));
+            const float x0 = gxt0[grp], x1 = gxt1[grp];
+            aq[0] = fmaf(s_g, d[0], aq[0]);
+            aq[1] = fmaf(s_g, d[1], aq[1]);
+            aq[2] = fmaf(s_g8, d[2], aq[2]);
+            aq[3] = fmaf(s_g8, d[3], aq[3]);
+            am[0] = fmaf(m_g, x0, am[0]);
+            am[1] = fmaf(m_g, x1, am[1]);
+            am[2] = fmaf(m_g8, x0, am[2]);
+            am[3] = fmaf(m_g8, x1, am[3]);
+        }
+    }
+}
+
+template <int EPI, bool MIXED, int BITS>
 __device__ __forceinline__ void mt_units(const MtArgs& m, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                          volatile int* abort_flag, volatile int* any_bf, int warp, int lane)
 {
@@ -214,6 +322,9 @@ __device__ __forceinline__ void mt_units(const MtArgs& m, uint8_t* smem, uint64_
     const uint32_t ring = smem_u32(smem + a.smem_ring);
     const uint32_t box_off = static_cast<uint32_t>(b2 * a.R8 + 16 * rb) * 128u;
     const uint32_t sbox_off = a.scales_off + static_cast<uint32_t>(b2 * a.R8 + 16 * rb) * 16u;
+    const uint32_t mbox_off = a.mins_off + static_cast<uint32_t>(b2 * a.R8 + 16 * rb) * 16u;
+    const uint32_t hbox_off = a.hi_off + static_cast<uint32_t>(b2 * a.R8 + 16 * rb) * 32u;
+    const float* gx_all = reinterpret_cast<const float*>(smem + a.smem_gx);
     const uint32_t x0 = smem_u32(smem + a.smem_x) + static_cast<uint32_t>(g) * m.x_tok;
     const int t0 = 2 * c, t1 = 2 * c + 1;
 
@@ -225,7 +336,7 @@ __device__ __forceinline__ void mt_units(const MtArgs& m, uint8_t* smem, uint64_
             const int win = (cc * a.P) / m.W;  // the stage's chunks lie in one window
             if (win != cur_win) {
                 named_barrier_sync(1, kCcThreads);
-                mt_convert(m, smem, warp, lane, any_bf, win * m.W);
+                mt_convert<BITS != 0>(m, smem, warp, lane, any_bf, win * m.W);
                 named_barrier_sync(1, kCcThreads);
                 cur_win = win;
             }
@@ -235,17 +346,37 @@ __device__ __forceinline__ void mt_units(const MtArgs& m, uint8_t* smem, uint64_
                 const int j = kc - win * m.W;
                 const uint32_t stage = ring + slot * a.stage_bytes;
                 const uint32_t xc = x0 + static_cast<uint32_t>(j) * (kChunkK * 2u);
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                if (MIXED && fl[j] != 0)
-                    mt_stage<true>(stage + box_off, stage + sbox_off, xc, lane, M, d);
-                else
-                    mt_stage<false>(stage + box_off, stage + sbox_off, xc, lane, M, d);
                 const float pe0 = t0 < M ? pe_all[t0 * m.W + j] : 0.f;
                 const float pe1 = t1 < M ? pe_all[t1 * m.W + j] : 0.f;
-                acc[0] = fmaf(d[0], pe0, acc[0]);
-                acc[1] = fmaf(d[1], pe1, acc[1]);
-                acc[2] = fmaf(d[2], pe0, acc[2]);
-                acc[3] = fmaf(d[3], pe1, acc[3]);
+                if constexpr (BITS == 0) {
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (MIXED && fl[j] != 0)
+                        mt_stage<true>(stage + box_off, stage + sbox_off, xc, lane, M, d);
+                    else
+                        mt_stage<false>(stage + box_off, stage + sbox_off, xc, lane, M, d);
+                    acc[0] = fmaf(d[0], pe0, acc[0]);
+                    acc[1] = fmaf(d[1], pe1, acc[1]);
+                    acc[2] = fmaf(d[2], pe0, acc[2]);
+                    acc[3] = fmaf(d[3], pe1, acc[3]);
+                } else {
+                    float aq[4] = {0.f, 0.f, 0.f, 0.f}, am[4] = {0.f, 0.f, 0.f, 0.f};
+                    // tokens >= M: any row (their sums are never written)
+                    const float* g0 = gx_all + ((t0 < M ? t0 : 0) * m.W + j) * 8;
+                    const float* g1 = gx_all + ((t1 < M ? t1 : 0) * m.W + j) * 8;
+                    const bool bf = MIXED && fl[j] != 0;
+                    if (bf)
+                        mtq_stage<BITS, true>(stage + box_off, stage + sbox_off, stage + mbox_off, stage + hbox_off,
+                                              xc, g0, g1, lane, M, aq, am);
+                    else
+                        mtq_stage<BITS, false>(stage + box_off, stage + sbox_off, stage + mbox_off, stage + hbox_off,
+                                               xc, g0, g1, lane, M, aq, am);
+                    // subnormal codes carry 2^-24 (not on the bf16 path)
+                    const float f0 = bf ? 1.0f : 16777216.0f * pe0, f1 = bf ? 1.0f : 16777216.0f * pe1;
+                    acc[0] = fmaf(aq[0], f0, acc[0]) + am[0];
+                    acc[1] = fmaf(aq[1], f1, acc[1]) + am[1];
+                    acc[2] = fmaf(aq[2], f0, acc[2]) + am[2];
+                    acc[3] = fmaf(aq[3], f1, acc[3]) + am[3];
+                }
             }
             mbar_arrive(&empty[slot]);
             if (++slot == a.n_stages) {
@@ -290,10 +421,9 @@ __device__ __forceinline__ void mt_units(const MtArgs& m, uint8_t* smem, uint64_
     }
 }
 
-template <int EPI>
+template <int EPI, int BITS>
 __global__ void __launch_bounds__(kCcAllThreads, 1)
-    mt_gemv_kernel(const __grid_constant__ MtArgs m, const __grid_constant__ CUtensorMap tm_codes,
-                   const __grid_constant__ CUtensorMap tm_scales)
+    mt_gemv_kernel(const __grid_constant__ MtArgs m, const __grid_constant__ MtMaps maps)
 {
     constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
     const CcArgs& a = m.a;
@@ -320,10 +450,8 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
 
     if (warp == kCcTmaWarp) {
         // ------------------------------------------------------------ producer (qgemv_cc.cu's)
-        if (elect_one()) {
-            prefetch_tensormap(&tm_codes);
-            prefetch_tensormap(&tm_scales);
-        }
+        if (elect_one())
+            for (int i = 0; i < (BITS == 0 ? 2 : BITS == 4 ? 3 : 4); ++i) prefetch_tensormap(&maps.m[i]);
         __syncwarp();
         int slot = 0, lap = 0, issued = 0;
         bool stop = false;
@@ -351,9 +479,19 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
                         for (int gg = 0; gg < NGU; ++gg) {
                             const int b2 = pp * NGU + gg;
                             const int row = row0 + gg * a.up_row_offset;
-                            tma_load_2d(sb + b2 * a.R8 * 128, &tm_codes, kc * (kChunkK / 2), row, &full[slot]);
-                            tma_load_2d(sb + a.scales_off + b2 * a.R8 * 16, &tm_scales, kc * (kChunkK / 16), row,
-                                        &full[slot]);
+                            tma_load_2d(sb + b2 * a.R8 * 128, &maps.m[0], kc * (kChunkK / 2), row, &full[slot]);
+                            if constexpr (BITS == 0) {
+                                tma_load_2d(sb + a.scales_off + b2 * a.R8 * 16, &maps.m[1], kc * (kChunkK / 16), row,
+                                            &full[slot]);
+                            } else {
+                                tma_load_2d(sb + a.scales_off + b2 * a.R8 * 16, &maps.m[1], kc * (kChunkK / 32), row,
+                                            &full[slot]);
+                                tma_load_2d(sb + a.mins_off + b2 * a.R8 * 16, &maps.m[2], kc * (kChunkK / 32), row,
+                                            &full[slot]);
+                                if (BITS == 5)
+                                    tma_load_2d(sb + a.hi_off + b2 * a.R8 * 32, &maps.m[3], kc * (kChunkK / 8), row,
+                                                &full[slot]);
+                            }
                         }
                     }
                 }
@@ -374,23 +512,23 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
 
     // ---------------------------------------------------------------- compute warps
     {
-        const uint32_t roff[4] = {0u, a.scales_off, 0u, 0u}, rbytes[4] = {128u, 16u, 0u, 0u};
-        cc_zero_padding(a, smem, a.P * NGU, roff, rbytes, 2);
+        const uint32_t roff[4] = {0u, a.scales_off, a.mins_off, a.hi_off}, rbytes[4] = {128u, 16u, 16u, 32u};
+        cc_zero_padding(a, smem, a.P * NGU, roff, rbytes, BITS == 0 ? 2 : BITS == 4 ? 3 : 4);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    mt_convert(m, smem, warp, lane, any_bf, 0);
+    mt_convert<BITS != 0>(m, smem, warp, lane, any_bf, 0);
     named_barrier_sync(1, kCcThreads);
     // with several windows a later one may hold raw-bf16 chunks: the mixed loop
     if (*any_bf || m.W < a.C)
-        mt_units<EPI, true>(m, smem, full, empty, abort_flag, any_bf, warp, lane);
+        mt_units<EPI, true, BITS>(m, smem, full, empty, abort_flag, any_bf, warp, lane);
     else
-        mt_units<EPI, false>(m, smem, full, empty, abort_flag, any_bf, warp, lane);
+        mt_units<EPI, false, BITS>(m, smem, full, empty, abort_flag, any_bf, warp, lane);
 }
 
 constexpr uint32_t align_up(uint32_t v, uint32_t al) { return (v + al - 1) / al * al; }
 
-template <int EPI>
-qg_status mt_launch(MtArgs m, const CUtensorMap& tmc, const CUtensorMap& tms, int grid, cudaStream_t stream)
+template <int EPI, int BITS>
+qg_status mt_launch(MtArgs m, const MtMaps& maps, int grid, cudaStream_t stream)
 {
     constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
     CcArgs& a = m.a;
@@ -402,8 +540,15 @@ qg_status mt_launch(MtArgs m, const CUtensorMap& tmc, const CUtensorMap& tms, in
 
     const uint32_t nbox = static_cast<uint32_t>(a.P * NGU);
     a.scales_off = nbox * a.R8 * 128u;
-    a.stage_bytes = align_up(a.scales_off + nbox * a.R8 * 16u, 1024);
-    a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
+    if constexpr (BITS == 0) {
+        a.stage_bytes = align_up(a.scales_off + nbox * a.R8 * 16u, 1024);
+        a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
+    } else {
+        a.mins_off = a.scales_off + nbox * a.R8 * 16u;
+        a.hi_off = a.mins_off + nbox * a.R8 * 16u;
+        a.stage_bytes = align_up(a.hi_off + (BITS == 5 ? nbox * a.R8 * 32u : 0u), 1024);
+        a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (BITS == 5 ? 32u : 0u));
+    }
     const uint32_t red_bytes = align_up(nbox * a.R8 * 4u * kMtTokens, 128);
     const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
     // the activation window: all of K if it fits beside a ring of at least
@@ -411,7 +556,8 @@ qg_status mt_launch(MtArgs m, const CUtensorMap& tmc, const CUtensorMap& tms, in
     auto win_bytes = [&](int W) {
         const uint32_t xt = static_cast<uint32_t>(W) * kChunkK * 2u + kMtXPad;
         return align_up(static_cast<uint32_t>(m.M) * xt, 128) + align_up(static_cast<uint32_t>(m.M * W) * 4u, 16) +
-               align_up(static_cast<uint32_t>(W), 16);
+               align_up(static_cast<uint32_t>(W), 16) +
+               (BITS != 0 ? align_up(static_cast<uint32_t>(m.M * W) * 32u, 16) : 0u);
     };
     const uint32_t other = red_bytes + bar_bytes;
     int W = a.C;
@@ -425,7 +571,8 @@ qg_status mt_launch(MtArgs m, const CUtensorMap& tmc, const CUtensorMap& tms, in
     const uint32_t x_bytes = align_up(static_cast<uint32_t>(m.M) * m.x_tok, 128);
     const uint32_t pe_bytes = align_up(static_cast<uint32_t>(m.M * W) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(W), 16);
-    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + red_bytes + bar_bytes;
+    const uint32_t gx_bytes = BITS != 0 ? align_up(static_cast<uint32_t>(m.M * W) * 32u, 16) : 0u;
+    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + gx_bytes + red_bytes + bar_bytes;
     a.n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / a.stage_bytes));
     uint32_t so = 0;
     a.smem_ring = so;
@@ -436,13 +583,15 @@ qg_status mt_launch(MtArgs m, const CUtensorMap& tmc, const CUtensorMap& tms, in
     so += pe_bytes;
     a.smem_fl = so;
     so += fl_bytes;
+    a.smem_gx = so;
+    so += gx_bytes;
     a.smem_red = so;
     so += red_bytes;
     a.smem_bar = so;
     so += bar_bytes;
     if (so > kCcSmemMax) return QG_ERR_UNSUPPORTED;
 
-    auto kern = mt_gemv_kernel<EPI>;
+    auto kern = mt_gemv_kernel<EPI, BITS>;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
@@ -461,25 +610,20 @@ qg_status mt_launch(MtArgs m, const CUtensorMap& tmc, const CUtensorMap& tms, in
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, m, tmc, tms) != cudaSuccess) return QG_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, m, maps) != cudaSuccess) return QG_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
 }  // namespace
 
-// 1..8 tokens, K a multiple of 256; QG_ERR_UNSUPPORTED otherwise or when the
-// plan does not fit shared memory.
-qg_status launch_mt_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
-                                int out_f32, const void* residual, int M, int N, int K, int swiglu,
-                                cudaStream_t stream)
+namespace {
+
+// The plan shared by both formats: the one-token rule for R (equal bytes per
+// SM), then 16-row blocks, at most 16 warps' worth of (phase, gate/up, block)
+// per stage.
+MtArgs mt_plan(const void* x, void* y, int out_f32, const void* residual, int M, int n_out, int ngu, int K,
+               int sms)
 {
-    if (M < 1 || M > kMtTokens || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
-    const int ngu = swiglu ? 2 : 1;
-    const int n_out = swiglu ? N / 2 : N;
-    const int sms = sm_count(-1);
-    if (sms <= 0) return QG_ERR_CUDA;
-    // the one-token rule for R (equal bytes per SM), then 16-row blocks: at
-    // most 16 warps' worth of (phase, gate/up, block) per stage
     int R = 1;
     for (int U = 1;; ++U) {
         R = (n_out + sms * U - 1) / (sms * U);
@@ -499,21 +643,61 @@ qg_status launch_mt_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, flo
     m.NRB = a.R8 / 16;
     a.P = std::max(1, std::min(kCcWarps / (ngu * m.NRB), a.C));
     a.Cp = (a.C + a.P - 1) / a.P;
-    a.up_row_offset = swiglu ? n_out : 0;
-    a.out_f32 = swiglu ? 0 : out_f32;
-    a.g = g;
+    a.up_row_offset = ngu == 2 ? n_out : 0;
+    a.out_f32 = ngu == 2 ? 0 : out_f32;
+    a.g = 1.0f;
     a.n_units = (n_out + R - 1) / R;
     m.M = M;
-    const int grid = std::min(sms, a.n_units);
-    CUtensorMap tmc, tms;
-    memset(&tmc, 0, sizeof(tmc));
-    memset(&tms, 0, sizeof(tms));
-    if (!encode_tmap_2d(&tmc, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, R, true) ||
-        !encode_tmap_2d(&tms, scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 16, N, 16, R, false))
+    return m;
+}
+
+}  // namespace
+
+// 1..8 tokens, K a multiple of 256; QG_ERR_UNSUPPORTED otherwise or when the
+// plan does not fit shared memory.
+qg_status launch_mt_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
+                                int out_f32, const void* residual, int M, int N, int K, int swiglu,
+                                cudaStream_t stream)
+{
+    if (M < 1 || M > kMtTokens || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
+    const int sms = sm_count(-1);
+    if (sms <= 0) return QG_ERR_CUDA;
+    MtArgs m = mt_plan(x, y, out_f32, residual, M, swiglu ? N / 2 : N, swiglu ? 2 : 1, K, sms);
+    m.a.g = g;
+    const int grid = std::min(sms, m.a.n_units);
+    MtMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (!encode_tmap_2d(&maps.m[0], codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, m.a.R, true) ||
+        !encode_tmap_2d(&maps.m[1], scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 16, N, 16, m.a.R, false))
         return QG_ERR_CUDA;
-    if (swiglu) return mt_launch<EPI_SWIGLU>(m, tmc, tms, grid, stream);
-    if (residual) return mt_launch<EPI_RESID>(m, tmc, tms, grid, stream);
-    return mt_launch<EPI_NONE>(m, tmc, tms, grid, stream);
+    if (swiglu) return mt_launch<EPI_SWIGLU, 0>(m, maps, grid, stream);
+    if (residual) return mt_launch<EPI_RESID, 0>(m, maps, grid, stream);
+    return mt_launch<EPI_NONE, 0>(m, maps, grid, stream);
+}
+
+// Q4/Q5 with 1..8 tokens (plain or residual epilogue), K a multiple of 256.
+qg_status launch_mt_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min, int bits,
+                              const void* x, void* y, int out_f32, const void* residual, int M, int N, int K,
+                              cudaStream_t stream)
+{
+    if (M < 1 || M > kMtTokens || K % kChunkK != 0 || (bits != 4 && bits != 5)) return QG_ERR_UNSUPPORTED;
+    const int sms = sm_count(-1);
+    if (sms <= 0) return QG_ERR_CUDA;
+    MtArgs m = mt_plan(x, y, out_f32, residual, M, N, 1, K, sms);
+    const int grid = std::min(sms, m.a.n_units);
+    const int R = m.a.R;
+    MtMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (!encode_tmap_2d(&maps.m[0], q_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128, R, true) ||
+        !encode_tmap_2d(&maps.m[1], scale, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, N, 8, R, false) ||
+        !encode_tmap_2d(&maps.m[2], min, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, N, 8, R, false))
+        return QG_ERR_CUDA;
+    if (bits == 5 &&
+        !encode_tmap_2d(&maps.m[3], q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 8, N, 32, R, false))
+        return QG_ERR_CUDA;
+    if (bits == 5) return residual ? mt_launch<EPI_RESID, 5>(m, maps, grid, stream)
+                                   : mt_launch<EPI_NONE, 5>(m, maps, grid, stream);
+    return residual ? mt_launch<EPI_RESID, 4>(m, maps, grid, stream) : mt_launch<EPI_NONE, 4>(m, maps, grid, stream);
 }
 
 }  // namespace qg

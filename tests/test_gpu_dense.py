@@ -199,14 +199,16 @@ def test_q45_long_k(bits, M):
     check_out(y, yref, a, f"Q{bits} long K M={M}")
 
 
-def test_q45_deterministic_and_row_independent():
-    """Q4/Q5 with 3..8 tokens (one arithmetic for all of them): repeated
-    calls are bit-identical and a token's result does not depend on the other
-    tokens of the call. One and two tokens take the CUDA-core kernel, whose
+@pytest.mark.parametrize("big,small", [(8, 7), (6, 3)])
+def test_q45_deterministic_and_row_independent(big, small):
+    """Q4/Q5 with several tokens: repeated calls are bit-identical and a
+    token's result does not depend on the other tokens of the call, within
+    one kernel (7..8 tokens: the groupwise mma.sync kernel; 3..6: the
+    warp-MMA kernel). One and two tokens take the CUDA-core kernel, whose
     two-token results equal one-token calls (checked separately)."""
-    M, N, K = 8, 700, 2048
+    N, K = 700, 2048
     w = synth.q45_weights(33, "qdet", N, K, 5)
-    x = synth.bf16_normal(34, "qdetx", (M, K))
+    x = synth.bf16_normal(34, "qdetx", (big, K))
     d = q45_dev(w)
 
     def run(xb):
@@ -216,9 +218,12 @@ def test_q45_deterministic_and_row_independent():
         return y.cpu().numpy()
     y1, y2 = run(x), run(x)
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32)), "two runs differ"
-    for m in (0, 6):
-        ym = run(np.stack([x[m], x[(m + 5) % M], x[(m + 3) % M]]))
-        assert np.array_equal(ym[0].view(np.uint32), y1[m].view(np.uint32)), f"row {m}: M=3 call != M=8 call"
+    for m in (0, big - 2):
+        ym = run(np.stack([x[(m + i) % big] for i in range(small)]))
+        assert np.array_equal(ym[0].view(np.uint32), y1[m].view(np.uint32)), \
+            f"row {m}: M={small} call != M={big} call"
+    yref, a = O.gemv_q45(w, x)
+    check_out(torch.from_numpy(y1), yref, a, f"Q5 M={big}")
 
 
 # ---------------------------------------------------------------- activations
@@ -265,7 +270,7 @@ def test_nvfp4_activation_windows_with_wide_range_chunks(M):
 
 
 @pytest.mark.parametrize("bits", [4, 5])
-@pytest.mark.parametrize("M", [1, 2, 8])
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
 def test_q45_wide_dynamic_range_activations(bits, M):
     N, K = 200, 512
     w = synth.q45_weights(24, "qwide", N, K, bits)
@@ -328,7 +333,7 @@ def test_dense_layer_full_size(M):
     assert d27.hidden == 5120
 
 
-@pytest.mark.parametrize("M", [1, 2, 8])
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
 def test_mixed_q45_layer_full_size(M):
     for name, N, K, bits in synth.Q45_RECIPE:
         w = synth.q45_weights(3, f"q45.{name}", N, K, bits)
@@ -448,9 +453,9 @@ def _q5_call(M, N, K, seed):
 
 
 # One case per pipelined kernel: the one-token CUDA-core NVFP4 and Q5
-# kernels, their two-token variants, the tcgen05 kernel (NVFP4, 8 tokens)
-# and the mma.sync groupwise-int kernel (Q5, 8 tokens).
-STARVE_CASES = [("nvfp4", 1), ("nvfp4", 2), ("nvfp4", 8), ("q5", 1), ("q5", 2), ("q5", 8)]
+# kernels, their two-token variants, the warp-MMA kernel (NVFP4 at 8 tokens,
+# Q5 at 4) and the mma.sync groupwise-int kernel (Q5, 8 tokens).
+STARVE_CASES = [("nvfp4", 1), ("nvfp4", 2), ("nvfp4", 8), ("q5", 1), ("q5", 2), ("q5", 4), ("q5", 8)]
 
 
 @pytest.mark.parametrize("fmt,M", STARVE_CASES)
