@@ -173,10 +173,17 @@ KERNEL_SOURCES = {
     "cc": ("qgemv_cc.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
     "tc": ("qgemv_tc.cu", "tcgen05.cuh", "common.cuh", "qgemv_internal.h"),
     "mma": ("qgemv_dense.cu", "common.cuh", "qgemv_internal.h"),
-    "mt": ("qgemv_mt.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
+    "mt": ("qgemv_mt.cu", "mt_core.cuh", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
     "moe": ("moe_cc.cu", "moe.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
-    "chain": ("qgemv_chain.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
+    "chain": ("qgemv_chain.cu", "cc_core.cuh", "mt_core.cuh", "common.cuh", "qgemv_internal.h"),
 }
+
+
+def one_launch_chain(workload, M):
+    """Whether the layer's qgemv_chain call runs as one persistent launch: at
+    one or two tokens always; at three to eight unless an op carries the
+    RMSNorm prologue or the groupwise-int SwiGLU (the q45ffn layer)."""
+    return M <= 2 or (workload in ("dense", "q45") and M <= 8)
 
 
 def kernel_family(workload, M):
@@ -384,7 +391,7 @@ class Workload:
             events[-1].record()
 
     def launches_per_step(self):
-        return 1 if (self.chains and self.M <= 2) else len(self.projs)
+        return 1 if (self.chains and one_launch_chain(self.kind, self.M)) else len(self.projs)
 
     def alg_bytes(self, idx):
         """Algorithmic bytes of call idx: weights + activations in + outputs."""
@@ -683,14 +690,14 @@ def read_probe_bandwidth(torch, q, stream, peak, nbytes=2 << 30, reps=10):
             "what": "library streaming-read probe (qg_read_probe), median of 10 launches"}
 
 
-def arithmetic(workload, M):
+def arithmetic(workload, M, chained=False):
     if workload in ("dense", "tiny") and M <= 2:
         return "f16 x f16 -> f32 FMA on CUDA cores (exact decoded weights, prescaled activations)"
     if workload in ("q45", "q45ffn") and M <= 2:
         return "f16 x f16 -> f32 FMA on CUDA cores (codes as exact f16, prescaled activations)"
     if workload == "q45ffn":
         return "fp32 FMA on CUDA cores (exact fallback kernel for the normalised and fused ops), bf16 mma.sync for the rest"
-    if workload == "q45" and M <= 6:
+    if workload == "q45" and (M <= 6 or chained):
         return "f16 mma.sync m16n8k16, f32 accumulate (codes as exact f16, prescaled activations)"
     if workload == "q45":
         return "bf16 mma.sync, f32 accumulate (codes exact in bf16, raw bf16 activations)"
@@ -820,12 +827,14 @@ def measure(args, kind, M, world, rank, stream, cpu=True, e2e=True):
     alone = {"kernel": dom_name, "achieved": achieved, "frac": achieved / peak, "alg_bytes_per_launch": wl.alg_bytes(dom),
              "us_per_launch": dom_us, "traffic": traffic,
              "timing": "the projection alone, K launches in one CUDA graph, events on its stream"}
-    if chained and M <= 2:
+    if chained and one_launch_chain(kind, M):
         # the step is one launch of the chained-layer kernel: it is the
         # dominant (only) kernel, timed by the headline graph itself
         step_bytes = sum(wl.alg_bytes(i) for i in range(n_calls))
         ach = step_bytes / (ms_per_step * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "chain_kernel (whole layer, one launch)", "achieved": ach,
+        roofline = {"bound": "hbm",
+                    "kernel": ("chain_kernel" if M <= 2 else "chain_mt_kernel") + " (whole layer, one launch)",
+                    "achieved": ach,
                     "peak": peak, "unit": "GB/s", "frac": ach / peak, "peak_source": peak_src,
                     "traffic": profiled_traffic(f"{kind}.chain.M{M}", "chain"),
                     "alg_bytes_per_launch": step_bytes, "us_per_launch": ms_per_step * 1e3,
@@ -874,7 +883,7 @@ def measure(args, kind, M, world, rank, stream, cpu=True, e2e=True):
            "frac_of_measured_hbm": value / world / peak, "frac_of_8tbs": value / world / NOMINAL_HBM_GBS,
            "us_per_call": us_per_call, "roofline": roofline, "e2e": e2e_line, "cpu_baseline": cpu_line,
            "clocks": clk, "gpu_launches": wl.launches_per_step() * args.steps,
-           "dtype": arithmetic(kind, M), "l2": f"weights rotate over {wl.copies} copies "
+           "dtype": arithmetic(kind, M, chained and one_launch_chain(kind, M)), "l2": f"weights rotate over {wl.copies} copies "
            f"({wl.copies * wl.weight_bytes / 1e6:.0f} MB vs {wl.l2_bytes / 1e6:.0f} MB L2)"}
     del wl, g_warm, g_main, g_ev, g_dom
     torch.cuda.synchronize()
@@ -930,7 +939,8 @@ def main():
             "config": {"workload": head["workload"], "M": args.M,
                        "weight_bytes_per_step": head["weight_bytes_per_step"], "l2": head["l2"],
                        "parallelism": "one independent replica per GPU" if world > 1 else "single GPU",
-                       "step": "one qgemv_chain call (the layer's projections; one persistent launch at M <= 2)"
+                       "step": "one qgemv_chain call (the layer's projections; one persistent launch unless an "
+                               "op is a normalised or fused groupwise-int op at M >= 3)"
                                if head["chained"] else "one library call per projection",
                        "graph": "K steps captured in one CUDA graph (kernels only); us_per_call from a "
                                 "second graph with events between the calls (which serialise them)"},

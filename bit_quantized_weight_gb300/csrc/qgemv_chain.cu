@@ -24,7 +24,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "cc_core.cuh"
+#include "mt_core.cuh"
 
 namespace qg {
 
@@ -39,6 +39,11 @@ struct ChainOp {
     int epi;    // EPI_NONE, EPI_RESID, EPI_SWIGLU
     int dep;    // grid-wide barrier before the op reads its inputs
     int ufmt;   // groupwise-int SwiGLU: the up matrix's format
+    // 3..8 tokens (the warp-MMA stage): 16-row blocks per box, activation
+    // window in chunks, bytes between tokens' activations
+    int NRB;
+    int W;
+    uint32_t x_tok;
 };
 
 struct ChainParams {
@@ -47,6 +52,7 @@ struct ChainParams {
     CUtensorMap map[kChainMaxOps][8];
     ChainOp op[kChainMaxOps];
     int n_ops;
+    int M;                             // tokens (3..8 in the warp-MMA kernel)
     int n_stages;
     uint32_t slot_bytes;               // ring slot stride (the largest op's stage)
     uint32_t smem_bar;
@@ -365,6 +371,95 @@ __device__ __forceinline__ void chain_q45(const CcArgs& a, int epi, bool mixed, 
                                              aborted, slot, lap);
 }
 
+// The TMA warp of a chained launch: the weight stages of op after op into one
+// ring, without a stop at an op boundary (weights never depend on outputs).
+__device__ __forceinline__ void chain_producer(const ChainParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                               volatile int* abort_flag, int lane)
+{
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+        for (int o = 0; o < p.n_ops; ++o) {
+            prefetch_tensormap(&p.map[o][0]);
+            prefetch_tensormap(&p.map[o][1]);
+            if (p.op[o].fmt != FMT_NVFP4) prefetch_tensormap(&p.map[o][2]);
+            if (p.op[o].fmt == FMT_Q5) prefetch_tensormap(&p.map[o][3]);
+            if (p.op[o].fmt != FMT_NVFP4 && p.op[o].epi == EPI_SWIGLU)
+                for (int i = 4; i < 8; ++i) prefetch_tensormap(&p.map[o][i]);
+        }
+    }
+    __syncwarp();
+    int slot = 0, lap = 0, issued = 0;
+    bool stop = false;
+    for (int o = 0; o < p.n_ops && !stop; ++o) {
+        const CcArgs& a = p.op[o].a;
+        const int fmt = p.op[o].fmt;
+        const int ngu = p.op[o].epi == EPI_SWIGLU ? 2 : 1;
+        const int P = a.P, C = a.C, Cp = a.Cp, R = a.R, n_units = a.n_units, up_off = a.up_row_offset;
+        const uint32_t box_bytes = static_cast<uint32_t>(a.R8) * 128u, sbox_bytes = static_cast<uint32_t>(a.R8) * 16u;
+        const uint32_t scales_off = a.scales_off, mins_off = a.mins_off, hi_off = a.hi_off, box_tx = a.box_tx;
+        for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+            const int row0 = u * R;
+            for (int c = 0; c < Cp; ++c) {
+                if (lap > 0 && !cc_wait_warp(&empty[slot], (lap - 1) & 1, a, abort_flag)) {
+                    stop = true;
+                    break;
+                }
+                if (*abort_flag || p.starve) {
+                    stop = true;
+                    break;
+                }
+                int live = 0;
+                for (int pp = 0; pp < P; ++pp) live += (c * P + pp < C) ? 1 : 0;
+                uint8_t* sb = smem + a.smem_ring + slot * p.slot_bytes;
+                if (elect_one()) {
+                    // NVFP4: box_tx per (phase, gate/up) box; groupwise int: per phase
+                    const uint32_t phase_tx = fmt == FMT_NVFP4 ? static_cast<uint32_t>(ngu) * box_tx : box_tx;
+                    mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live) * phase_tx);
+                    for (int pp = 0; pp < P; ++pp) {
+                        const int kc = c * P + pp;
+                        if (kc >= C) continue;
+                        if (fmt == FMT_NVFP4) {
+                            for (int gg = 0; gg < ngu; ++gg) {
+                                const int b2 = pp * ngu + gg;
+                                const int row = row0 + gg * up_off;
+                                tma_load_2d(sb + b2 * box_bytes, &p.map[o][0], kc * (kChunkK / 2), row,
+                                            &full[slot]);
+                                tma_load_2d(sb + scales_off + b2 * sbox_bytes, &p.map[o][1],
+                                            kc * (kChunkK / 16), row, &full[slot]);
+                            }
+                        } else {
+                            // gate (or only) box, then a SwiGLU's up box: same rows of two matrices
+                            for (int gg = 0; gg < ngu; ++gg) {
+                                const uint32_t b2 = static_cast<uint32_t>(pp * ngu + gg);
+                                const CUtensorMap* mp = &p.map[o][4 * gg];
+                                tma_load_2d(sb + b2 * box_bytes, mp, kc * (kChunkK / 2), row0, &full[slot]);
+                                tma_load_2d(sb + scales_off + b2 * sbox_bytes, mp + 1, kc * (kChunkK / 32),
+                                            row0, &full[slot]);
+                                tma_load_2d(sb + mins_off + b2 * sbox_bytes, mp + 2, kc * (kChunkK / 32), row0,
+                                            &full[slot]);
+                                if ((gg ? p.op[o].ufmt : fmt) == FMT_Q5)
+                                    tma_load_2d(sb + hi_off + b2 * 2u * sbox_bytes, mp + 3, kc * (kChunkK / 8),
+                                                row0, &full[slot]);
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                ++issued;
+                if (++slot == p.n_stages) {
+                    slot = 0;
+                    ++lap;
+                }
+            }
+        }
+    }
+    // No copy may still be landing in shared memory when the CTA exits.
+    if (lane == 0)
+        for (int g = max(0, issued - p.n_stages); g < issued; ++g)
+            mbar_wait_bounded(&full[g % p.n_stages], (g / p.n_stages) & 1, p.wait_ns, p.status);
+    __syncwarp();
+}
+
 // MT tokens (1 or 2) per op: every op's activations, residuals and outputs
 // are MT rows (K, N or n_out apart), as in the one- and two-token kernels.
 template <int MT>
@@ -393,88 +488,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_co
     const uint32_t ring = smem_u32(smem + p.op[0].a.smem_ring);
 
     if (warp == kCcTmaWarp) {
-        // ------------------------------------------------------------ producer
-        if (elect_one()) {
-            for (int o = 0; o < p.n_ops; ++o) {
-                prefetch_tensormap(&p.map[o][0]);
-                prefetch_tensormap(&p.map[o][1]);
-                if (p.op[o].fmt != FMT_NVFP4) prefetch_tensormap(&p.map[o][2]);
-                if (p.op[o].fmt == FMT_Q5) prefetch_tensormap(&p.map[o][3]);
-                if (p.op[o].fmt != FMT_NVFP4 && p.op[o].epi == EPI_SWIGLU)
-                    for (int i = 4; i < 8; ++i) prefetch_tensormap(&p.map[o][i]);
-            }
-        }
-        __syncwarp();
-        int slot = 0, lap = 0, issued = 0;
-        bool stop = false;
-        for (int o = 0; o < p.n_ops && !stop; ++o) {
-            const CcArgs& a = p.op[o].a;
-            const int fmt = p.op[o].fmt;
-            const int ngu = p.op[o].epi == EPI_SWIGLU ? 2 : 1;
-            const int P = a.P, C = a.C, Cp = a.Cp, R = a.R, n_units = a.n_units, up_off = a.up_row_offset;
-            const uint32_t box_bytes = static_cast<uint32_t>(a.R8) * 128u, sbox_bytes = static_cast<uint32_t>(a.R8) * 16u;
-            const uint32_t scales_off = a.scales_off, mins_off = a.mins_off, hi_off = a.hi_off, box_tx = a.box_tx;
-            for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-                const int row0 = u * R;
-                for (int c = 0; c < Cp; ++c) {
-                    if (lap > 0 && !cc_wait_warp(&empty[slot], (lap - 1) & 1, a, abort_flag)) {
-                        stop = true;
-                        break;
-                    }
-                    if (*abort_flag || p.starve) {
-                        stop = true;
-                        break;
-                    }
-                    int live = 0;
-                    for (int pp = 0; pp < P; ++pp) live += (c * P + pp < C) ? 1 : 0;
-                    uint8_t* sb = smem + a.smem_ring + slot * p.slot_bytes;
-                    if (elect_one()) {
-                        // NVFP4: box_tx per (phase, gate/up) box; groupwise int: per phase
-                        const uint32_t phase_tx = fmt == FMT_NVFP4 ? static_cast<uint32_t>(ngu) * box_tx : box_tx;
-                        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live) * phase_tx);
-                        for (int pp = 0; pp < P; ++pp) {
-                            const int kc = c * P + pp;
-                            if (kc >= C) continue;
-                            if (fmt == FMT_NVFP4) {
-                                for (int gg = 0; gg < ngu; ++gg) {
-                                    const int b2 = pp * ngu + gg;
-                                    const int row = row0 + gg * up_off;
-                                    tma_load_2d(sb + b2 * box_bytes, &p.map[o][0], kc * (kChunkK / 2), row,
-                                                &full[slot]);
-                                    tma_load_2d(sb + scales_off + b2 * sbox_bytes, &p.map[o][1],
-                                                kc * (kChunkK / 16), row, &full[slot]);
-                                }
-                            } else {
-                                // gate (or only) box, then a SwiGLU's up box: same rows of two matrices
-                                for (int gg = 0; gg < ngu; ++gg) {
-                                    const uint32_t b2 = static_cast<uint32_t>(pp * ngu + gg);
-                                    const CUtensorMap* mp = &p.map[o][4 * gg];
-                                    tma_load_2d(sb + b2 * box_bytes, mp, kc * (kChunkK / 2), row0, &full[slot]);
-                                    tma_load_2d(sb + scales_off + b2 * sbox_bytes, mp + 1, kc * (kChunkK / 32),
-                                                row0, &full[slot]);
-                                    tma_load_2d(sb + mins_off + b2 * sbox_bytes, mp + 2, kc * (kChunkK / 32), row0,
-                                                &full[slot]);
-                                    if ((gg ? p.op[o].ufmt : fmt) == FMT_Q5)
-                                        tma_load_2d(sb + hi_off + b2 * 2u * sbox_bytes, mp + 3, kc * (kChunkK / 8),
-                                                    row0, &full[slot]);
-                                }
-                            }
-                        }
-                    }
-                    __syncwarp();
-                    ++issued;
-                    if (++slot == p.n_stages) {
-                        slot = 0;
-                        ++lap;
-                    }
-                }
-            }
-        }
-        // No copy may still be landing in shared memory when the CTA exits.
-        if (lane == 0)
-            for (int g = max(0, issued - p.n_stages); g < issued; ++g)
-                mbar_wait_bounded(&full[g % p.n_stages], (g / p.n_stages) & 1, p.wait_ns, p.status);
-        __syncwarp();
+        chain_producer(p, smem, full, empty, abort_flag, lane);
         return;
     }
 
@@ -523,6 +537,206 @@ __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_co
     }
 }
 
+// 3..8 tokens: the unit loop of one op on the warp-MMA stage (mt_units of
+// qgemv_mt.cu with the ring position carried across ops, the epilogue chosen
+// at run time, activations and residuals read through L2, and the op's plan
+// in registers).
+template <int BITS, bool MIXED>
+__device__ __forceinline__ void chain_units_mt(const MtArgs& m, int epi, uint8_t* smem, uint32_t ring,
+                                               uint32_t slot_bytes, int n_stages, uint64_t* full, uint64_t* empty,
+                                               volatile int* abort_flag, volatile int* any_bf, bool& aborted,
+                                               int& slot, int& lap, int warp, int lane)
+{
+    const CcArgs& a = m.a;
+    const bool swiglu = epi == EPI_SWIGLU, resid = epi == EPI_RESID;
+    const int ngu = swiglu ? 2 : 1;
+    const int M = m.M, W = m.W, NRB = m.NRB;
+    const int R = a.R, R8 = a.R8, P = a.P, C = a.C, Cp = a.Cp, n_units = a.n_units, n_out = a.n_out;
+    const float gscale = a.g;
+    const int b2 = warp / NRB;
+    const int rb = warp % NRB;
+    const bool active = b2 < P * ngu;
+    const int p = active ? b2 / ngu : 0;
+    const int n_mine = active ? max(0, (C - p + P - 1) / P) : 0;
+    const int g = lane >> 2, c = lane & 3;
+    const int t0 = 2 * c, t1 = 2 * c + 1;
+    const float* pe_all = reinterpret_cast<const float*>(smem + a.smem_pe);
+    const uint8_t* fl = smem + a.smem_fl;
+    const float* gx_all = reinterpret_cast<const float*>(smem + a.smem_gx);
+    float* red = reinterpret_cast<float*>(smem + a.smem_red);
+    const uint32_t rowb = static_cast<uint32_t>(b2 * R8 + 16 * rb);
+    const uint32_t box_off = rowb * 128u;
+    const uint32_t sbox_off = a.scales_off + rowb * 16u;
+    const uint32_t mbox_off = a.mins_off + rowb * 16u;
+    const uint32_t hbox_off = a.hi_off + rowb * 32u;
+    const uint32_t x0 = smem_u32(smem + a.smem_x) + static_cast<uint32_t>(g) * m.x_tok;
+
+    int cur_win = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int cc = 0; cc < Cp; ++cc) {
+            const int win = (cc * P) / W;
+            if (win != cur_win) {
+                named_barrier_sync(1, kCcThreads);
+                mt_convert<BITS != 0, true>(m, smem, warp, lane, any_bf, win * W);
+                named_barrier_sync(1, kCcThreads);
+                cur_win = win;
+            }
+            if (!aborted && !cc_wait_warp(&full[slot], lap & 1, a, abort_flag)) aborted = true;
+            if (!aborted && cc < n_mine) {
+                const int kc = cc * P + p;
+                const int j = kc - win * W;
+                const uint32_t stage = ring + slot * slot_bytes;
+                const uint32_t xc = x0 + static_cast<uint32_t>(j) * (kChunkK * 2u);
+                const float pe0 = t0 < M ? pe_all[t0 * W + j] : 0.f;
+                const float pe1 = t1 < M ? pe_all[t1 * W + j] : 0.f;
+                const bool bf = MIXED && fl[j] != 0;
+                if constexpr (BITS == 0) {
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (bf)
+                        mt_stage<true>(stage + box_off, stage + sbox_off, xc, lane, M, d);
+                    else
+                        mt_stage<false>(stage + box_off, stage + sbox_off, xc, lane, M, d);
+                    acc[0] = fmaf(d[0], pe0, acc[0]);
+                    acc[1] = fmaf(d[1], pe1, acc[1]);
+                    acc[2] = fmaf(d[2], pe0, acc[2]);
+                    acc[3] = fmaf(d[3], pe1, acc[3]);
+                } else {
+                    float aq[4] = {0.f, 0.f, 0.f, 0.f}, am[4] = {0.f, 0.f, 0.f, 0.f};
+                    const float* gx0 = gx_all + ((t0 < M ? t0 : 0) * W + j) * 8;
+                    const float* gx1 = gx_all + ((t1 < M ? t1 : 0) * W + j) * 8;
+                    if (bf)
+                        mtq_stage<BITS, true>(stage + box_off, stage + sbox_off, stage + mbox_off, stage + hbox_off,
+                                              xc, gx0, gx1, lane, M, aq, am);
+                    else
+                        mtq_stage<BITS, false>(stage + box_off, stage + sbox_off, stage + mbox_off,
+                                               stage + hbox_off, xc, gx0, gx1, lane, M, aq, am);
+                    const float f0 = bf ? 1.0f : 16777216.0f * pe0, f1 = bf ? 1.0f : 16777216.0f * pe1;
+                    acc[0] = fmaf(aq[0], f0, acc[0]) + am[0];
+                    acc[1] = fmaf(aq[1], f1, acc[1]) + am[1];
+                    acc[2] = fmaf(aq[2], f0, acc[2]) + am[2];
+                    acc[3] = fmaf(aq[3], f1, acc[3]) + am[3];
+                }
+            }
+            mbar_arrive(&empty[slot]);
+            if (++slot == n_stages) {
+                slot = 0;
+                ++lap;
+            }
+        }
+        if (active) {
+            float* rw = red + static_cast<size_t>(b2 * R8 + 16 * rb + g) * 8;
+            rw[t0] = acc[0];
+            rw[t1] = acc[1];
+            rw[64 + t0] = acc[2];
+            rw[64 + t1] = acc[3];
+        }
+        named_barrier_sync(1, kCcThreads);
+        if (!aborted) {
+            const int r0 = u * R;
+            for (int it = threadIdx.x; it < R * M; it += kCcThreads) {
+                const int r = it % R, t = it / R;
+                if (r0 + r >= n_out) continue;
+                float v0 = 0.f;
+                for (int pp = 0; pp < P; ++pp) v0 += red[static_cast<size_t>((pp * ngu) * R8 + r) * 8 + t];
+                v0 *= gscale;
+                float val = v0;
+                if (swiglu) {
+                    float v1 = 0.f;
+                    for (int pp = 0; pp < P; ++pp) v1 += red[static_cast<size_t>((pp * ngu + 1) * R8 + r) * 8 + t];
+                    v1 *= gscale;
+                    val = (v0 / (1.0f + expf(-v0))) * v1;
+                }
+                const int o = t * n_out + r0 + r;
+                if (resid) val += bf16_bits_to_f32(ldg_cg_u16(a.residual + o));
+                chain_store(a, o, val);
+            }
+        }
+        named_barrier_sync(1, kCcThreads);
+    }
+}
+
+// 3..8 tokens per op (the warp-MMA stage): NVFP4 ops with any epilogue,
+// Q4/Q5 ops with the plain or residual epilogue, no RMSNorm.
+__global__ void __launch_bounds__(kCcAllThreads, 1) chain_mt_kernel(const __grid_constant__ ChainParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = warp_index_uniform();
+    const int lane = threadIdx.x & 31;
+
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.smem_bar);
+    uint64_t* empty = full + kCcMaxStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCcMaxStages);
+    volatile int* any_bf = abort_flag + 1;
+
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.n_stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCcThreads);
+        }
+        *abort_flag = 0;
+        *any_bf = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const uint32_t ring = smem_u32(smem + p.op[0].a.smem_ring);
+
+    if (warp == kCcTmaWarp) {
+        chain_producer(p, smem, full, empty, abort_flag, lane);
+        return;
+    }
+
+    // ---------------------------------------------------------------- compute warps
+    // Rows past an op's R in its 16-row blocks hold whatever an earlier op's
+    // boxes left in the ring: each D row depends on its own weight row only,
+    // and those rows are never written out.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    bool aborted = false;
+    int slot = 0, lap = 0;
+    for (int o = 0; o < p.n_ops; ++o) {
+        const ChainOp& op = p.op[o];
+        MtArgs m;
+        m.a = op.a;
+        m.M = p.M;
+        m.NRB = op.NRB;
+        m.W = op.W;
+        m.x_tok = op.x_tok;
+        if (op.dep) chain_grid_barrier(p, abort_flag);
+        if (*abort_flag) aborted = true;
+        if (threadIdx.x == 0) *any_bf = 0;
+        named_barrier_sync(1, kCcThreads);
+        if (op.fmt == FMT_NVFP4)
+            mt_convert<false, true>(m, smem, warp, lane, any_bf, 0);
+        else
+            mt_convert<true, true>(m, smem, warp, lane, any_bf, 0);
+        named_barrier_sync(1, kCcThreads);
+        const bool mixed = *any_bf != 0 || m.W < m.a.C;
+        if (op.fmt == FMT_NVFP4) {
+            if (mixed)
+                chain_units_mt<0, true>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                        any_bf, aborted, slot, lap, warp, lane);
+            else
+                chain_units_mt<0, false>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                         any_bf, aborted, slot, lap, warp, lane);
+        } else if (op.fmt == FMT_Q5) {
+            if (mixed)
+                chain_units_mt<5, true>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                        any_bf, aborted, slot, lap, warp, lane);
+            else
+                chain_units_mt<5, false>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                         any_bf, aborted, slot, lap, warp, lane);
+        } else {
+            if (mixed)
+                chain_units_mt<4, true>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                        any_bf, aborted, slot, lap, warp, lane);
+            else
+                chain_units_mt<4, false>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
+                                         any_bf, aborted, slot, lap, warp, lane);
+        }
+    }
+}
+
 constexpr uint32_t align_up(uint32_t v, uint32_t al) { return (v + al - 1) / al * al; }
 
 // Units of R rows with the one-token kernels' rule: the smallest number of
@@ -551,9 +765,209 @@ void cc_plan(CcArgs& a, int n_out, int ngu, int K, int sms)
 // QG_ERR_UNSUPPORTED when the list does not fit its plan (M > 2, K not a
 // multiple of 256, too many ops, or shared memory), so that the caller runs
 // the ops one by one instead.
+namespace {
+
+// 3..8 tokens: every op on the warp-MMA stage (its plan: R for equal bytes per
+// SM, boxes padded to 16-row blocks, at most 16 blocks per stage), the
+// activations of each op held a window of chunks at a time.
+qg_status launch_chain_mt(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, cudaStream_t stream)
+{
+    const int sms = sm_count(-1);
+    if (sms <= 0) return QG_ERR_CUDA;
+    static ChainParams p;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    memset(&p, 0, sizeof(p));
+    p.n_ops = n_ops;
+    p.M = M;
+    bool any_dep = false, any_q = false;
+    uint32_t slot_bytes = 0, red_max = 0;
+    for (int o = 0; o < n_ops; ++o) {
+        const qg_gemv_op& g = ops[o];
+        if (g.K % kChunkK != 0 || g.norm_weight || g.up_codes) return QG_ERR_UNSUPPORTED;
+        ChainOp& op = p.op[o];
+        op.fmt = g.format == QG_FMT_NVFP4 ? FMT_NVFP4 : g.format == QG_FMT_Q5 ? FMT_Q5 : FMT_Q4;
+        op.epi = g.epilogue == QG_EPI_SWIGLU ? EPI_SWIGLU : g.epilogue == QG_EPI_RESIDUAL ? EPI_RESID : EPI_NONE;
+        if (op.fmt != FMT_NVFP4 && op.epi == EPI_SWIGLU) return QG_ERR_UNSUPPORTED;
+        op.dep = o > 0 && g.after_previous ? 1 : 0;
+        op.ufmt = op.fmt;
+        any_dep = any_dep || op.dep;
+        any_q = any_q || op.fmt != FMT_NVFP4;
+        const int ngu = op.epi == EPI_SWIGLU ? 2 : 1;
+        const int n_out = op.epi == EPI_SWIGLU ? g.N / 2 : g.N;
+        int R = 1;
+        for (int U = 1;; ++U) {
+            R = (n_out + sms * U - 1) / (sms * U);
+            if (ngu * ((R + 15) / 16) <= kCcWarps) break;
+        }
+        R = std::max(R, 1);
+        CcArgs& a = op.a;
+        a.x = static_cast<const uint16_t*>(g.x);
+        a.y = g.y;
+        a.residual = static_cast<const uint16_t*>(g.residual);
+        a.K = g.K;
+        a.C = g.K / kChunkK;
+        a.n_out = n_out;
+        a.R = R;
+        a.R8 = (R + 15) / 16 * 16;
+        op.NRB = a.R8 / 16;
+        a.P = std::max(1, std::min(kCcWarps / (ngu * op.NRB), a.C));
+        a.Cp = (a.C + a.P - 1) / a.P;
+        a.n_units = (n_out + R - 1) / R;
+        a.up_row_offset = op.epi == EPI_SWIGLU ? n_out : 0;
+        a.out_f32 = op.epi == EPI_SWIGLU ? 0 : (g.y_dtype == QG_OUT_F32 ? 1 : 0);
+        a.g = op.fmt == FMT_NVFP4 ? g.global_scale : 1.f;
+        const uint32_t nbox = static_cast<uint32_t>(a.P * ngu);
+        a.scales_off = nbox * a.R8 * 128u;
+        uint32_t st;
+        if (op.fmt == FMT_NVFP4) {
+            st = a.scales_off + nbox * a.R8 * 16u;
+            a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
+        } else {
+            a.mins_off = a.scales_off + nbox * a.R8 * 16u;
+            a.hi_off = a.mins_off + nbox * a.R8 * 16u;
+            st = a.hi_off + (op.fmt == FMT_Q5 ? nbox * a.R8 * 32u : 0u);
+            a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (op.fmt == FMT_Q5 ? 32u : 0u));
+        }
+        slot_bytes = std::max(slot_bytes, align_up(st, 1024));
+        red_max = std::max(red_max, nbox * a.R8 * 8u);
+        const int rows = g.N;
+        if (!encode_tmap_2d(&p.map[o][0], g.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 2, rows, 128, R, true))
+            return QG_ERR_CUDA;
+        if (op.fmt == FMT_NVFP4) {
+            if (!encode_tmap_2d(&p.map[o][1], g.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 16, rows, 16, R,
+                                false))
+                return QG_ERR_CUDA;
+        } else {
+            if (!encode_tmap_2d(&p.map[o][1], g.scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8, R,
+                                false) ||
+                !encode_tmap_2d(&p.map[o][2], g.mins, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8, R,
+                                false))
+                return QG_ERR_CUDA;
+            if (op.fmt == FMT_Q5 &&
+                !encode_tmap_2d(&p.map[o][3], g.q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 8, rows, 32, R, false))
+                return QG_ERR_CUDA;
+        }
+    }
+    if (any_dep && !sync) return QG_ERR_INVALID_ARG;
+    // shared memory: ring | activation window | 2^-prescale | flags | sums of
+    // x per group | partial sums | barriers; each op's window W (a multiple of
+    // its P chunks, all of K when it fits) leaves at least three ring slots
+    const uint32_t red_bytes = align_up(red_max * 4u, 128);
+    const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
+    auto win_bytes = [&](int W) {
+        const uint32_t xt = static_cast<uint32_t>(W) * kChunkK * 2u + 16u;
+        return align_up(static_cast<uint32_t>(M) * xt, 128) + align_up(static_cast<uint32_t>(M * W) * 4u, 16) +
+               align_up(static_cast<uint32_t>(W), 16) +
+               (any_q ? align_up(static_cast<uint32_t>(M * W) * 32u, 16) : 0u);
+    };
+    const uint32_t other = red_bytes + bar_bytes;
+    if (other + 3 * slot_bytes >= kCcSmemMax) return QG_ERR_UNSUPPORTED;
+    const uint32_t budget = kCcSmemMax - other - 4 * slot_bytes > kCcSmemMax
+                                ? 0u
+                                : kCcSmemMax - other - 4 * slot_bytes;  // all of K beside four slots
+    const uint32_t budget3 = kCcSmemMax - other - 3 * slot_bytes;
+    uint32_t win_max = 0;
+    int w_max = 1;
+    for (int o = 0; o < n_ops; ++o) {
+        CcArgs& a = p.op[o].a;
+        int W = a.C;
+        if (win_bytes(W) > budget) {
+            W = (a.C / a.P) * a.P;
+            while (W > a.P && win_bytes(W) > budget3) W -= a.P;
+        }
+        if (win_bytes(W) > budget3) return QG_ERR_UNSUPPORTED;
+        p.op[o].W = W;
+        p.op[o].x_tok = static_cast<uint32_t>(W) * kChunkK * 2u + 16u;
+        win_max = std::max(win_max, win_bytes(W));
+        w_max = std::max(w_max, W);
+    }
+    const uint32_t x_bytes = align_up(static_cast<uint32_t>(M) * (static_cast<uint32_t>(w_max) * kChunkK * 2u + 16u),
+                                      128);
+    const uint32_t pe_bytes = align_up(static_cast<uint32_t>(M * w_max) * 4u, 16);
+    const uint32_t fl_bytes = align_up(static_cast<uint32_t>(w_max), 16);
+    const uint32_t gx_bytes = any_q ? align_up(static_cast<uint32_t>(M * w_max) * 32u, 16) : 0u;
+    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + gx_bytes + red_bytes + bar_bytes;
+    if (fixed + 3 * slot_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
+    const int n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / slot_bytes));
+    uint32_t so = 0;
+    const uint32_t smem_ring = so;
+    so += n_stages * slot_bytes;
+    const uint32_t smem_x = so;
+    so += x_bytes;
+    const uint32_t smem_pe = so;
+    so += pe_bytes;
+    const uint32_t smem_fl = so;
+    so += fl_bytes;
+    const uint32_t smem_gx = so;
+    so += gx_bytes;
+    const uint32_t smem_red = so;
+    so += red_bytes;
+    const uint32_t smem_bar = so;
+    so += bar_bytes;
+    if (so > kCcSmemMax) return QG_ERR_UNSUPPORTED;
+    (void)win_max;
+
+    int* status = device_status_ptr();
+    if (!status) return QG_ERR_CUDA;
+    const DebugState dbg = debug_state();
+    p.n_stages = n_stages;
+    p.slot_bytes = slot_bytes;
+    p.smem_bar = smem_bar;
+    p.sync = sync;
+    p.wait_ns = dbg.wait_ns;
+    p.starve = dbg.starve;
+    p.status = status;
+    for (int o = 0; o < n_ops; ++o) {
+        CcArgs& a = p.op[o].a;
+        a.n_stages = n_stages;
+        a.stage_bytes = slot_bytes;
+        a.smem_ring = smem_ring;
+        a.smem_x = smem_x;
+        a.smem_pe = smem_pe;
+        a.smem_fl = smem_fl;
+        a.smem_gx = smem_gx;
+        a.smem_red = smem_red;
+        a.smem_bar = smem_bar;
+        a.wait_ns = dbg.wait_ns;
+        a.starve = dbg.starve;
+        a.status = status;
+    }
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(chain_mt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCcSmemMax) !=
+            cudaSuccess)
+            return QG_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms);
+    cfg.blockDim = dim3(kCcAllThreads);
+    cfg.dynamicSmemBytes = so;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (any_dep) {
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+    } else {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, chain_mt_kernel, p) != cudaSuccess) return QG_ERR_CUDA;
+    return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+}  // namespace
+
 qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, cudaStream_t stream)
 {
-    if (M < 1 || M > 2 || n_ops < 1 || n_ops > kChainMaxOps) return QG_ERR_UNSUPPORTED;
+    if (n_ops < 1 || n_ops > kChainMaxOps) return QG_ERR_UNSUPPORTED;
+    if (M >= 3 && M <= kMtTokens) return launch_chain_mt(ops, n_ops, M, sync, stream);
+    if (M < 1 || M > 2) return QG_ERR_UNSUPPORTED;
     const int sms = sm_count(-1);
     if (sms <= 0) return QG_ERR_CUDA;
     static ChainParams p;  // large: built here, copied into the launch's parameters

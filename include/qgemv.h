@@ -260,12 +260,13 @@ typedef struct {
  *           after_previous set; may be NULL otherwise. Calls that overlap on
  *           the GPU must use different words, and after a call that reported
  *           QG_ERR_DEVICE_TIMEOUT the words must be zeroed again.
- * With one token and K a multiple of 256 for every op, the list runs as one
- * persistent kernel (one CTA per SM, launched
- * cooperatively when an op waits for earlier ones): the weight stream runs on
- * across op boundaries. Other lists run as one launch per op, in order, on
- * `stream`; a single record is thus also the way to call any projection with
- * the RMSNorm prologue.
+ * When K is a multiple of 256 for every op, the list runs as one persistent
+ * kernel (one CTA per SM, launched cooperatively when an op waits for earlier
+ * ones): the weight stream runs on across op boundaries. That holds for one
+ * or two tokens, and for three to eight tokens when no op has the RMSNorm
+ * prologue or the groupwise-int SwiGLU. Other lists run as one launch per op,
+ * in order, on `stream`; a single record is thus also the way to call any
+ * projection with the RMSNorm prologue.
  * Every op is validated before anything is launched.
  */
 QG_API qg_status qgemv_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, cudaStream_t stream);
