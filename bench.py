@@ -180,10 +180,9 @@ KERNEL_SOURCES = {
 
 
 def one_launch_chain(workload, M):
-    """Whether the layer's qgemv_chain call runs as one persistent launch: at
-    one or two tokens always; at three to eight unless an op carries the
-    RMSNorm prologue or the groupwise-int SwiGLU (the q45ffn layer)."""
-    return M <= 2 or (workload in ("dense", "q45") and M <= 8)
+    """Whether the layer's qgemv_chain call runs as one persistent launch (it
+    does for every layer of this bench at one to eight tokens)."""
+    return M <= 8
 
 
 def kernel_family(workload, M):
@@ -939,8 +938,7 @@ def main():
             "config": {"workload": head["workload"], "M": args.M,
                        "weight_bytes_per_step": head["weight_bytes_per_step"], "l2": head["l2"],
                        "parallelism": "one independent replica per GPU" if world > 1 else "single GPU",
-                       "step": "one qgemv_chain call (the layer's projections; one persistent launch unless an "
-                               "op is a normalised or fused groupwise-int op at M >= 3)"
+                       "step": "one qgemv_chain call (the layer's projections in one persistent launch)"
                                if head["chained"] else "one library call per projection",
                        "graph": "K steps captured in one CUDA graph (kernels only); us_per_call from a "
                                 "second graph with events between the calls (which serialise them)"},

@@ -230,6 +230,11 @@ qg_status run_op(const qg_gemv_op& g, int M, cudaStream_t stream)
             qg_status s = launch_cc_dense_nvfp4(g.codes, sc, g.global_scale, g.x, g.y, swiglu ? 0 : f32, g.residual,
                                                 M, g.N, g.K, swiglu ? 1 : 0, stream, g.norm_weight, g.norm_eps);
             if (s != QG_ERR_UNSUPPORTED) return s;
+            if (M >= 3) {
+                s = launch_mt_dense_nvfp4(g.codes, sc, g.global_scale, g.x, g.y, swiglu ? 0 : f32, g.residual, M,
+                                          g.N, g.K, swiglu ? 1 : 0, stream, g.norm_weight, g.norm_eps);
+                if (s != QG_ERR_UNSUPPORTED) return s;
+            }
             s = launch_tc_dense_nvfp4(g.codes, sc, g.global_scale, g.x, g.y, swiglu ? 0 : f32, g.residual, M, g.N,
                                       g.K, swiglu ? 1 : 0, stream, g.norm_weight, g.norm_eps);
             if (s != QG_ERR_UNSUPPORTED) return s;
@@ -241,9 +246,13 @@ qg_status run_op(const qg_gemv_op& g, int M, cudaStream_t stream)
         if (full_chunks) {
             const Q45Matrix gate{g.codes, g.q_hi, g.scales, g.mins, bits};
             const Q45Matrix up{g.up_codes, g.up_q_hi, g.up_scales, g.up_mins, g.up_format == QG_FMT_Q5 ? 5 : 4};
-            const qg_status s = launch_cc_swiglu_q45(gate, up, g.x, g.y, M, g.N, g.K, stream, g.norm_weight,
-                                                     g.norm_eps);
+            qg_status s = launch_cc_swiglu_q45(gate, up, g.x, g.y, M, g.N, g.K, stream, g.norm_weight,
+                                               g.norm_eps);
             if (s != QG_ERR_UNSUPPORTED) return s;
+            if (M >= 3) {
+                s = launch_mt_swiglu_q45(gate, up, g.x, g.y, M, g.N, g.K, stream, g.norm_weight, g.norm_eps);
+                if (s != QG_ERR_UNSUPPORTED) return s;
+            }
         }
         return run_op_simple(g, M, stream);
     }
@@ -257,6 +266,13 @@ qg_status run_op(const qg_gemv_op& g, int M, cudaStream_t stream)
             if (s != QG_ERR_UNSUPPORTED) return s;
             return launch_dense_q45(g.codes, g.q_hi, g.scales, g.mins, bits, g.x, g.y, f32, g.residual, M, g.N,
                                     g.K, stream);
+        }
+        // with the RMSNorm prologue: the warp-MMA kernel at every M >= 3 (the
+        // groupwise mma.sync kernel has no prologue)
+        if (M >= 3) {
+            s = launch_mt_dense_q45(g.codes, g.q_hi, g.scales, g.mins, bits, g.x, g.y, f32, g.residual, M, g.N,
+                                    g.K, stream, g.norm_weight, g.norm_eps);
+            if (s != QG_ERR_UNSUPPORTED) return s;
         }
     }
     return run_op_simple(g, M, stream);

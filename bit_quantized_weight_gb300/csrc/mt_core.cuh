@@ -22,9 +22,10 @@ struct MtArgs {
     uint32_t x_tok;  // bytes between tokens' activations in shared memory
 };
 
-// codes, scales, then (groupwise int) mins and the Q5 plane
+// codes, scales, then (groupwise int) mins and the Q5 plane; a groupwise-int
+// SwiGLU's up matrix in m[4..7]
 struct MtMaps {
-    CUtensorMap m[4];
+    CUtensorMap m[8];
 };
 
 __device__ __forceinline__ uint32_t mt_bsub2(uint32_t a, uint32_t b)
@@ -58,6 +59,50 @@ __device__ __forceinline__ void mt_mma(float (&d)[4], const uint32_t (&a)[4], ui
             : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Converts window w0, with the RMSNorm prologue if NORM_OK and a.norm_w is
+// set (NORM_OK = false compiles the plain conversion alone: a second inlined
+// variant slowed the stage loops that hold the window conversion).
+template <bool Q45, bool CG, bool NORM_OK>
+__device__ __forceinline__ void mt_convert_any(const MtArgs& m, uint8_t* smem, int warp, int lane,
+                                               volatile int* any_bf, int w0);
+
+// RMSNorm prologue (a.norm_w set): every token's r = 1 / sqrt(sum(x^2) / K +
+// eps) over all of K, in the fixed order of rms_chunk_ss (chunk sums added in
+// k order), at a.smem_ss + 4 * (M * C + t); the chunk sums before it. Run by
+// all compute warps before the first window is converted.
+template <bool CG>
+__device__ void mt_norm_factors(const MtArgs& m, uint8_t* smem, int warp, int lane)
+{
+    const CcArgs& a = m.a;
+    float* ss = reinterpret_cast<float*>(smem + a.smem_ss);
+    const int items = m.M * a.C;
+    constexpr int B = 4;
+    for (int base = warp; base < items; base += kCcWarps * B) {
+        uint4 raw[B];
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int it = base + u * kCcWarps;
+            raw[u] = it < items ? ldg_128<CG>(a.x + static_cast<size_t>(it / a.C) * a.K +
+                                              static_cast<size_t>(it % a.C) * kChunkK + lane * 8)
+                                : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int it = base + u * kCcWarps;
+            if (it >= items) break;
+            const float v = rms_chunk_ss(raw[u]);
+            if (lane == 0) ss[it] = v;
+        }
+    }
+    named_barrier_sync(1, kCcThreads);
+    if (static_cast<int>(threadIdx.x) < m.M) {
+        float s = 0.f;
+        for (int kc = 0; kc < a.C; ++kc) s += ss[threadIdx.x * a.C + kc];
+        ss[items + threadIdx.x] = rms_factor(s, a.K, a.norm_eps);
+    }
+    named_barrier_sync(1, kCcThreads);
+}
+
 // Every token's activations of chunks w0 .. w0 + W - 1 (a window) into shared
 // memory: chunk kc = w0 + j of token t at smem_x + t * x_tok + j * 512 (k
 // order, f16 after the exact prescale, or raw bf16 when some token's chunk
@@ -65,8 +110,10 @@ __device__ __forceinline__ void mt_mma(float (&d)[4], const uint32_t (&a)[4], ui
 // fl[j]. One warp per chunk. Q45: each lane's 8 values stored paired (x0,
 // x4)(x1, x5)(x2, x6)(x3, x7), and the sum of each group of 32 values (from
 // the bf16 values) at gx[(t * W + j) * 8 + group]. CG: read x through L2
-// only (an earlier op of the same launch may have written it).
-template <bool Q45, bool CG = false>
+// only (an earlier op of the same launch may have written it). NORM (the
+// RMSNorm prologue): the values converted are h = bf16(x * r * gamma), with r
+// from mt_norm_factors.
+template <bool Q45, bool CG = false, bool NORM = false>
 __device__ void mt_convert(const MtArgs& m, uint8_t* smem, int warp, int lane, volatile int* any_bf, int w0)
 {
     const CcArgs& a = m.a;
@@ -83,6 +130,13 @@ __device__ void mt_convert(const MtArgs& m, uint8_t* smem, int warp, int lane, v
             raw[t] = t < m.M ? ldg_128<CG>(a.x + static_cast<size_t>(t) * a.K + static_cast<size_t>(kc) * kChunkK +
                                           lane * 8)
                              : make_uint4(0, 0, 0, 0);
+        if constexpr (NORM) {
+            const uint4 gam = ldg_nc_128(a.norm_w + static_cast<size_t>(kc) * kChunkK + lane * 8);
+            const float* rn = reinterpret_cast<const float*>(smem + a.smem_ss) + m.M * a.C;
+#pragma unroll
+            for (int t = 0; t < kMtTokens; ++t)
+                if (t < m.M) raw[t] = rms_apply8(raw[t], gam, rn[t]);
+        }
         int e[kMtTokens];
         bool inexact = false;
 #pragma unroll
@@ -259,6 +313,16 @@ __device__ __forceinline__ void mtq_stage(uint32_t box, uint32_t sbox, uint32_t 
             am[3] = fmaf(m_g8, x1, am[3]);
         }
     }
+}
+
+template <bool Q45, bool CG, bool NORM_OK>
+__device__ __forceinline__ void mt_convert_any(const MtArgs& m, uint8_t* smem, int warp, int lane,
+                                               volatile int* any_bf, int w0)
+{
+    if (NORM_OK && m.a.norm_w != nullptr)
+        mt_convert<Q45, CG, NORM_OK>(m, smem, warp, lane, any_bf, w0);
+    else
+        mt_convert<Q45, CG, false>(m, smem, warp, lane, any_bf, w0);
 }
 
 }  // namespace

@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1) chain_kernel(const __grid_co
 // qgemv_mt.cu with the ring position carried across ops, the epilogue chosen
 // at run time, activations and residuals read through L2, and the op's plan
 // in registers).
-template <int BITS, bool MIXED>
+template <int BITS, bool MIXED, int BITS_U, bool NORM_OK>
 __device__ __forceinline__ void chain_units_mt(const MtArgs& m, int epi, uint8_t* smem, uint32_t ring,
                                                uint32_t slot_bytes, int n_stages, uint64_t* full, uint64_t* empty,
                                                volatile int* abort_flag, volatile int* any_bf, bool& aborted,
@@ -578,7 +578,7 @@ __device__ __forceinline__ void chain_units_mt(const MtArgs& m, int epi, uint8_t
             const int win = (cc * P) / W;
             if (win != cur_win) {
                 named_barrier_sync(1, kCcThreads);
-                mt_convert<BITS != 0, true>(m, smem, warp, lane, any_bf, win * W);
+                mt_convert_any<BITS != 0, true, NORM_OK>(m, smem, warp, lane, any_bf, win * W);
                 named_barrier_sync(1, kCcThreads);
                 cur_win = win;
             }
@@ -605,12 +605,20 @@ __device__ __forceinline__ void chain_units_mt(const MtArgs& m, int epi, uint8_t
                     float aq[4] = {0.f, 0.f, 0.f, 0.f}, am[4] = {0.f, 0.f, 0.f, 0.f};
                     const float* gx0 = gx_all + ((t0 < M ? t0 : 0) * W + j) * 8;
                     const float* gx1 = gx_all + ((t1 < M ? t1 : 0) * W + j) * 8;
-                    if (bf)
+                    if (swiglu && (b2 & 1)) {  // the up matrix's box
+                        if (bf)
+                            mtq_stage<BITS_U, true>(stage + box_off, stage + sbox_off, stage + mbox_off,
+                                                    stage + hbox_off, xc, gx0, gx1, lane, M, aq, am);
+                        else
+                            mtq_stage<BITS_U, false>(stage + box_off, stage + sbox_off, stage + mbox_off,
+                                                     stage + hbox_off, xc, gx0, gx1, lane, M, aq, am);
+                    } else if (bf) {
                         mtq_stage<BITS, true>(stage + box_off, stage + sbox_off, stage + mbox_off, stage + hbox_off,
                                               xc, gx0, gx1, lane, M, aq, am);
-                    else
+                    } else {
                         mtq_stage<BITS, false>(stage + box_off, stage + sbox_off, stage + mbox_off,
                                                stage + hbox_off, xc, gx0, gx1, lane, M, aq, am);
+                    }
                     const float f0 = bf ? 1.0f : 16777216.0f * pe0, f1 = bf ? 1.0f : 16777216.0f * pe1;
                     acc[0] = fmaf(aq[0], f0, acc[0]) + am[0];
                     acc[1] = fmaf(aq[1], f1, acc[1]) + am[1];
@@ -656,8 +664,10 @@ __device__ __forceinline__ void chain_units_mt(const MtArgs& m, int epi, uint8_t
     }
 }
 
-// 3..8 tokens per op (the warp-MMA stage): NVFP4 ops with any epilogue,
-// Q4/Q5 ops with the plain or residual epilogue, no RMSNorm.
+// 3..8 tokens per op (the warp-MMA stage): every op kind (NVFP4 or Q4/Q5,
+// any epilogue, with or without the RMSNorm prologue). HAS_NORM: some op has
+// the prologue (a list without compiles the plain conversion alone).
+template <bool HAS_NORM>
 __global__ void __launch_bounds__(kCcAllThreads, 1) chain_mt_kernel(const __grid_constant__ ChainParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -706,33 +716,39 @@ __global__ void __launch_bounds__(kCcAllThreads, 1) chain_mt_kernel(const __grid
         if (*abort_flag) aborted = true;
         if (threadIdx.x == 0) *any_bf = 0;
         named_barrier_sync(1, kCcThreads);
+        if (HAS_NORM && m.a.norm_w != nullptr) mt_norm_factors<true>(m, smem, warp, lane);
         if (op.fmt == FMT_NVFP4)
-            mt_convert<false, true>(m, smem, warp, lane, any_bf, 0);
+            mt_convert_any<false, true, HAS_NORM>(m, smem, warp, lane, any_bf, 0);
         else
-            mt_convert<true, true>(m, smem, warp, lane, any_bf, 0);
+            mt_convert_any<true, true, HAS_NORM>(m, smem, warp, lane, any_bf, 0);
         named_barrier_sync(1, kCcThreads);
         const bool mixed = *any_bf != 0 || m.W < m.a.C;
         if (op.fmt == FMT_NVFP4) {
             if (mixed)
-                chain_units_mt<0, true>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                        any_bf, aborted, slot, lap, warp, lane);
+                chain_units_mt<0, true, 0, HAS_NORM>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty,
+                                                     abort_flag, any_bf, aborted, slot, lap, warp, lane);
             else
-                chain_units_mt<0, false>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                         any_bf, aborted, slot, lap, warp, lane);
-        } else if (op.fmt == FMT_Q5) {
-            if (mixed)
-                chain_units_mt<5, true>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                        any_bf, aborted, slot, lap, warp, lane);
-            else
-                chain_units_mt<5, false>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                         any_bf, aborted, slot, lap, warp, lane);
+                chain_units_mt<0, false, 0, HAS_NORM>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty,
+                                                      abort_flag, any_bf, aborted, slot, lap, warp, lane);
         } else {
-            if (mixed)
-                chain_units_mt<4, true>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                        any_bf, aborted, slot, lap, warp, lane);
+            // the gate (or only) matrix's width, and a SwiGLU's up matrix's
+            const bool b5 = op.fmt == FMT_Q5;
+            const bool u5 = op.epi == EPI_SWIGLU ? op.ufmt == FMT_Q5 : b5;
+            // one loop per width pair (the mixed one: its per-stage flag test is
+            // cheap, and fewer inlined copies keep the kernel's registers from
+            // spilling)
+#define QG_CHAIN_MT_Q(B, BU)                                                                                     \
+    chain_units_mt<B, true, BU, HAS_NORM>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag, \
+                                          any_bf, aborted, slot, lap, warp, lane)
+            if (b5 && u5)
+                QG_CHAIN_MT_Q(5, 5);
+            else if (b5)
+                QG_CHAIN_MT_Q(5, 4);
+            else if (u5)
+                QG_CHAIN_MT_Q(4, 5);
             else
-                chain_units_mt<4, false>(m, op.epi, smem, ring, p.slot_bytes, p.n_stages, full, empty, abort_flag,
-                                         any_bf, aborted, slot, lap, warp, lane);
+                QG_CHAIN_MT_Q(4, 4);
+#undef QG_CHAIN_MT_Q
         }
     }
 }
@@ -780,21 +796,22 @@ qg_status launch_chain_mt(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
     memset(&p, 0, sizeof(p));
     p.n_ops = n_ops;
     p.M = M;
-    bool any_dep = false, any_q = false;
+    bool any_dep = false, any_q = false, any_norm = false;
     uint32_t slot_bytes = 0, red_max = 0;
+    int c_max = 0;
     for (int o = 0; o < n_ops; ++o) {
         const qg_gemv_op& g = ops[o];
-        if (g.K % kChunkK != 0 || g.norm_weight || g.up_codes) return QG_ERR_UNSUPPORTED;
+        if (g.K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
         ChainOp& op = p.op[o];
         op.fmt = g.format == QG_FMT_NVFP4 ? FMT_NVFP4 : g.format == QG_FMT_Q5 ? FMT_Q5 : FMT_Q4;
         op.epi = g.epilogue == QG_EPI_SWIGLU ? EPI_SWIGLU : g.epilogue == QG_EPI_RESIDUAL ? EPI_RESID : EPI_NONE;
-        if (op.fmt != FMT_NVFP4 && op.epi == EPI_SWIGLU) return QG_ERR_UNSUPPORTED;
         op.dep = o > 0 && g.after_previous ? 1 : 0;
-        op.ufmt = op.fmt;
+        const bool sep_up = g.up_codes != nullptr;
+        op.ufmt = sep_up ? (g.up_format == QG_FMT_Q5 ? FMT_Q5 : FMT_Q4) : op.fmt;
         any_dep = any_dep || op.dep;
         any_q = any_q || op.fmt != FMT_NVFP4;
         const int ngu = op.epi == EPI_SWIGLU ? 2 : 1;
-        const int n_out = op.epi == EPI_SWIGLU ? g.N / 2 : g.N;
+        const int n_out = op.epi == EPI_SWIGLU && !sep_up ? g.N / 2 : g.N;
         int R = 1;
         for (int U = 1;; ++U) {
             R = (n_out + sms * U - 1) / (sms * U);
@@ -805,6 +822,10 @@ qg_status launch_chain_mt(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
         a.x = static_cast<const uint16_t*>(g.x);
         a.y = g.y;
         a.residual = static_cast<const uint16_t*>(g.residual);
+        a.norm_w = static_cast<const uint16_t*>(g.norm_weight);
+        a.norm_eps = g.norm_eps;
+        any_norm = any_norm || g.norm_weight != nullptr;
+        c_max = std::max(c_max, g.K / kChunkK);
         a.K = g.K;
         a.C = g.K / kChunkK;
         a.n_out = n_out;
@@ -814,7 +835,7 @@ qg_status launch_chain_mt(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
         a.P = std::max(1, std::min(kCcWarps / (ngu * op.NRB), a.C));
         a.Cp = (a.C + a.P - 1) / a.P;
         a.n_units = (n_out + R - 1) / R;
-        a.up_row_offset = op.epi == EPI_SWIGLU ? n_out : 0;
+        a.up_row_offset = op.epi == EPI_SWIGLU && !sep_up ? n_out : 0;
         a.out_f32 = op.epi == EPI_SWIGLU ? 0 : (g.y_dtype == QG_OUT_F32 ? 1 : 0);
         a.g = op.fmt == FMT_NVFP4 ? g.global_scale : 1.f;
         const uint32_t nbox = static_cast<uint32_t>(a.P * ngu);
@@ -824,10 +845,14 @@ qg_status launch_chain_mt(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
             st = a.scales_off + nbox * a.R8 * 16u;
             a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
         } else {
+            const bool any5 = op.fmt == FMT_Q5 || op.ufmt == FMT_Q5;
             a.mins_off = a.scales_off + nbox * a.R8 * 16u;
             a.hi_off = a.mins_off + nbox * a.R8 * 16u;
-            st = a.hi_off + (op.fmt == FMT_Q5 ? nbox * a.R8 * 32u : 0u);
+            st = a.hi_off + (any5 ? nbox * a.R8 * 32u : 0u);
+            // bytes one phase brings in: its gate (or only) box and a SwiGLU's up box
             a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (op.fmt == FMT_Q5 ? 32u : 0u));
+            if (ngu == 2)
+                a.box_tx += static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (op.ufmt == FMT_Q5 ? 32u : 0u));
         }
         slot_bytes = std::max(slot_bytes, align_up(st, 1024));
         red_max = std::max(red_max, nbox * a.R8 * 8u);
@@ -847,6 +872,18 @@ qg_status launch_chain_mt(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
             if (op.fmt == FMT_Q5 &&
                 !encode_tmap_2d(&p.map[o][3], g.q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 8, rows, 32, R, false))
                 return QG_ERR_CUDA;
+            if (sep_up) {
+                if (!encode_tmap_2d(&p.map[o][4], g.up_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 2, rows, 128,
+                                    R, true) ||
+                    !encode_tmap_2d(&p.map[o][5], g.up_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8,
+                                    R, false) ||
+                    !encode_tmap_2d(&p.map[o][6], g.up_mins, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8,
+                                    R, false))
+                    return QG_ERR_CUDA;
+                if (op.ufmt == FMT_Q5 && !encode_tmap_2d(&p.map[o][7], g.up_q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                                                         g.K / 8, rows, 32, R, false))
+                    return QG_ERR_CUDA;
+            }
         }
     }
     if (any_dep && !sync) return QG_ERR_INVALID_ARG;
@@ -855,13 +892,14 @@ qg_status launch_chain_mt(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
     // its P chunks, all of K when it fits) leaves at least three ring slots
     const uint32_t red_bytes = align_up(red_max * 4u, 128);
     const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
+    const uint32_t ss_bytes = any_norm ? align_up(static_cast<uint32_t>(M * (c_max + 1)) * 4u, 16) : 0u;
     auto win_bytes = [&](int W) {
         const uint32_t xt = static_cast<uint32_t>(W) * kChunkK * 2u + 16u;
         return align_up(static_cast<uint32_t>(M) * xt, 128) + align_up(static_cast<uint32_t>(M * W) * 4u, 16) +
                align_up(static_cast<uint32_t>(W), 16) +
                (any_q ? align_up(static_cast<uint32_t>(M * W) * 32u, 16) : 0u);
     };
-    const uint32_t other = red_bytes + bar_bytes;
+    const uint32_t other = red_bytes + bar_bytes + ss_bytes;
     if (other + 3 * slot_bytes >= kCcSmemMax) return QG_ERR_UNSUPPORTED;
     const uint32_t budget = kCcSmemMax - other - 4 * slot_bytes > kCcSmemMax
                                 ? 0u
@@ -887,7 +925,7 @@ qg_status launch_chain_mt(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
     const uint32_t pe_bytes = align_up(static_cast<uint32_t>(M * w_max) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(w_max), 16);
     const uint32_t gx_bytes = any_q ? align_up(static_cast<uint32_t>(M * w_max) * 32u, 16) : 0u;
-    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + gx_bytes + red_bytes + bar_bytes;
+    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + gx_bytes + ss_bytes + red_bytes + bar_bytes;
     if (fixed + 3 * slot_bytes > kCcSmemMax) return QG_ERR_UNSUPPORTED;
     const int n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / slot_bytes));
     uint32_t so = 0;
@@ -901,6 +939,8 @@ qg_status launch_chain_mt(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
     so += fl_bytes;
     const uint32_t smem_gx = so;
     so += gx_bytes;
+    const uint32_t smem_ss = so;
+    so += ss_bytes;
     const uint32_t smem_red = so;
     so += red_bytes;
     const uint32_t smem_bar = so;
@@ -927,20 +967,22 @@ qg_status launch_chain_mt(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
         a.smem_pe = smem_pe;
         a.smem_fl = smem_fl;
         a.smem_gx = smem_gx;
+        a.smem_ss = smem_ss;
         a.smem_red = smem_red;
         a.smem_bar = smem_bar;
         a.wait_ns = dbg.wait_ns;
         a.starve = dbg.starve;
         a.status = status;
     }
-    static bool attr_set[64] = {};
+    const int kv = any_norm ? 1 : 0;
+    auto kern = any_norm ? chain_mt_kernel<true> : chain_mt_kernel<false>;
+    static bool attr_set[2][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(chain_mt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCcSmemMax) !=
-            cudaSuccess)
+    if (!attr_set[kv][dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCcSmemMax) != cudaSuccess)
             return QG_ERR_CUDA;
-        attr_set[dev] = true;
+        attr_set[kv][dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sms);
@@ -957,7 +999,7 @@ qg_status launch_chain_mt(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
     }
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, chain_mt_kernel, p) != cudaSuccess) return QG_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return QG_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 

@@ -167,10 +167,12 @@ qg_status launch_tc_grouped_nvfp4(const uint8_t* codes, const uint8_t* scales, i
                                   const float* gscales, int rows_per_unit, cudaStream_t stream);
 qg_status launch_mt_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
                                 int out_f32, const void* residual, int M, int N, int K, int swiglu,
-                                cudaStream_t stream);
+                                cudaStream_t stream, const void* norm_w = nullptr, float norm_eps = 0.f);
 qg_status launch_mt_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min, int bits,
                               const void* x, void* y, int out_f32, const void* residual, int M, int N, int K,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const void* norm_w = nullptr, float norm_eps = 0.f);
+qg_status launch_mt_swiglu_q45(const Q45Matrix& gate, const Q45Matrix& up, const void* x, void* y, int M, int I, int K,
+                               cudaStream_t stream, const void* norm_w = nullptr, float norm_eps = 0.f);
 qg_status launch_cc_moe(const uint8_t* codes, const uint8_t* scales, int total_rows, int K, int swiglu, int up_offset,
                         int expert_rows, int blocks, const void* x, int n_x_rows, void* y, int out_pitch, int out_f32,
                         const CcPair* pairs, const int* n_pairs, int max_pairs, const float* gscales, int R,

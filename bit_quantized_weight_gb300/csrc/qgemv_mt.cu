@@ -54,7 +54,7 @@ namespace qg {
 
 namespace {
 
-template <int EPI, bool MIXED, int BITS>
+template <int EPI, bool MIXED, int BITS, int BITS_U, bool NORM>
 __device__ __forceinline__ void mt_units(const MtArgs& m, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                          volatile int* abort_flag, volatile int* any_bf, int warp, int lane)
 {
@@ -87,7 +87,7 @@ __device__ __forceinline__ void mt_units(const MtArgs& m, uint8_t* smem, uint64_
             const int win = (cc * a.P) / m.W;  // the stage's chunks lie in one window
             if (win != cur_win) {
                 named_barrier_sync(1, kCcThreads);
-                mt_convert<BITS != 0>(m, smem, warp, lane, any_bf, win * m.W);
+                mt_convert_any<BITS != 0, false, NORM>(m, smem, warp, lane, any_bf, win * m.W);
                 named_barrier_sync(1, kCcThreads);
                 cur_win = win;
             }
@@ -115,12 +115,21 @@ __device__ __forceinline__ void mt_units(const MtArgs& m, uint8_t* smem, uint64_
                     const float* g0 = gx_all + ((t0 < M ? t0 : 0) * m.W + j) * 8;
                     const float* g1 = gx_all + ((t1 < M ? t1 : 0) * m.W + j) * 8;
                     const bool bf = MIXED && fl[j] != 0;
-                    if (bf)
+                    // a SwiGLU's odd boxes hold the up matrix (BITS_U-bit codes)
+                    if (EPI == EPI_SWIGLU && (b2 & 1)) {
+                        if (bf)
+                            mtq_stage<BITS_U, true>(stage + box_off, stage + sbox_off, stage + mbox_off,
+                                                    stage + hbox_off, xc, g0, g1, lane, M, aq, am);
+                        else
+                            mtq_stage<BITS_U, false>(stage + box_off, stage + sbox_off, stage + mbox_off,
+                                                     stage + hbox_off, xc, g0, g1, lane, M, aq, am);
+                    } else if (bf) {
                         mtq_stage<BITS, true>(stage + box_off, stage + sbox_off, stage + mbox_off, stage + hbox_off,
                                               xc, g0, g1, lane, M, aq, am);
-                    else
+                    } else {
                         mtq_stage<BITS, false>(stage + box_off, stage + sbox_off, stage + mbox_off, stage + hbox_off,
                                                xc, g0, g1, lane, M, aq, am);
+                    }
                     // subnormal codes carry 2^-24 (not on the bf16 path)
                     const float f0 = bf ? 1.0f : 16777216.0f * pe0, f1 = bf ? 1.0f : 16777216.0f * pe1;
                     acc[0] = fmaf(aq[0], f0, acc[0]) + am[0];
@@ -172,7 +181,7 @@ __device__ __forceinline__ void mt_units(const MtArgs& m, uint8_t* smem, uint64_
     }
 }
 
-template <int EPI, int BITS>
+template <int EPI, int BITS, int BITS_U, bool NORM>
 __global__ void __launch_bounds__(kCcAllThreads, 1)
     mt_gemv_kernel(const __grid_constant__ MtArgs m, const __grid_constant__ MtMaps maps)
 {
@@ -201,8 +210,11 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
 
     if (warp == kCcTmaWarp) {
         // ------------------------------------------------------------ producer (qgemv_cc.cu's)
-        if (elect_one())
+        if (elect_one()) {
             for (int i = 0; i < (BITS == 0 ? 2 : BITS == 4 ? 3 : 4); ++i) prefetch_tensormap(&maps.m[i]);
+            if (BITS != 0 && NGU == 2)
+                for (int i = 0; i < (BITS_U == 4 ? 3 : 4); ++i) prefetch_tensormap(&maps.m[4 + i]);
+        }
         __syncwarp();
         int slot = 0, lap = 0, issued = 0;
         bool stop = false;
@@ -222,7 +234,7 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
                 for (int pp = 0; pp < a.P; ++pp) live += (c * a.P + pp < a.C) ? 1 : 0;
                 uint8_t* sb = smem + a.smem_ring + slot * a.stage_bytes;
                 if (elect_one()) {
-                    mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live * NGU) * a.box_tx);
+                    mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live) * a.box_tx);  // bytes per phase
                     for (int pp = 0; pp < a.P; ++pp) {
                         const int kc = c * a.P + pp;
                         if (kc >= a.C) continue;
@@ -230,17 +242,19 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
                         for (int gg = 0; gg < NGU; ++gg) {
                             const int b2 = pp * NGU + gg;
                             const int row = row0 + gg * a.up_row_offset;
-                            tma_load_2d(sb + b2 * a.R8 * 128, &maps.m[0], kc * (kChunkK / 2), row, &full[slot]);
+                            // a groupwise-int SwiGLU's up box comes from the up matrix's maps
+                            const CUtensorMap* mp = &maps.m[(BITS != 0 && gg == 1) ? 4 : 0];
+                            tma_load_2d(sb + b2 * a.R8 * 128, mp, kc * (kChunkK / 2), row, &full[slot]);
                             if constexpr (BITS == 0) {
-                                tma_load_2d(sb + a.scales_off + b2 * a.R8 * 16, &maps.m[1], kc * (kChunkK / 16), row,
+                                tma_load_2d(sb + a.scales_off + b2 * a.R8 * 16, mp + 1, kc * (kChunkK / 16), row,
                                             &full[slot]);
                             } else {
-                                tma_load_2d(sb + a.scales_off + b2 * a.R8 * 16, &maps.m[1], kc * (kChunkK / 32), row,
+                                tma_load_2d(sb + a.scales_off + b2 * a.R8 * 16, mp + 1, kc * (kChunkK / 32), row,
                                             &full[slot]);
-                                tma_load_2d(sb + a.mins_off + b2 * a.R8 * 16, &maps.m[2], kc * (kChunkK / 32), row,
+                                tma_load_2d(sb + a.mins_off + b2 * a.R8 * 16, mp + 2, kc * (kChunkK / 32), row,
                                             &full[slot]);
-                                if (BITS == 5)
-                                    tma_load_2d(sb + a.hi_off + b2 * a.R8 * 32, &maps.m[3], kc * (kChunkK / 8), row,
+                                if ((gg ? BITS_U : BITS) == 5)
+                                    tma_load_2d(sb + a.hi_off + b2 * a.R8 * 32, mp + 3, kc * (kChunkK / 8), row,
                                                 &full[slot]);
                             }
                         }
@@ -267,18 +281,19 @@ __global__ void __launch_bounds__(kCcAllThreads, 1)
         cc_zero_padding(a, smem, a.P * NGU, roff, rbytes, BITS == 0 ? 2 : BITS == 4 ? 3 : 4);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    mt_convert<BITS != 0>(m, smem, warp, lane, any_bf, 0);
+    if (NORM) mt_norm_factors<false>(m, smem, warp, lane);
+    mt_convert_any<BITS != 0, false, NORM>(m, smem, warp, lane, any_bf, 0);
     named_barrier_sync(1, kCcThreads);
     // with several windows a later one may hold raw-bf16 chunks: the mixed loop
     if (*any_bf || m.W < a.C)
-        mt_units<EPI, true, BITS>(m, smem, full, empty, abort_flag, any_bf, warp, lane);
+        mt_units<EPI, true, BITS, BITS_U, NORM>(m, smem, full, empty, abort_flag, any_bf, warp, lane);
     else
-        mt_units<EPI, false, BITS>(m, smem, full, empty, abort_flag, any_bf, warp, lane);
+        mt_units<EPI, false, BITS, BITS_U, NORM>(m, smem, full, empty, abort_flag, any_bf, warp, lane);
 }
 
 constexpr uint32_t align_up(uint32_t v, uint32_t al) { return (v + al - 1) / al * al; }
 
-template <int EPI, int BITS>
+template <int EPI, int BITS, int BITS_U = BITS>
 qg_status mt_launch(MtArgs m, const MtMaps& maps, int grid, cudaStream_t stream)
 {
     constexpr int NGU = EPI == EPI_SWIGLU ? 2 : 1;
@@ -293,12 +308,15 @@ qg_status mt_launch(MtArgs m, const MtMaps& maps, int grid, cudaStream_t stream)
     a.scales_off = nbox * a.R8 * 128u;
     if constexpr (BITS == 0) {
         a.stage_bytes = align_up(a.scales_off + nbox * a.R8 * 16u, 1024);
-        a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
+        a.box_tx = static_cast<uint32_t>(NGU) * static_cast<uint32_t>(a.R) * (128u + 16u);  // per phase
     } else {
+        constexpr bool any5 = BITS == 5 || (NGU == 2 && BITS_U == 5);
         a.mins_off = a.scales_off + nbox * a.R8 * 16u;
         a.hi_off = a.mins_off + nbox * a.R8 * 16u;
-        a.stage_bytes = align_up(a.hi_off + (BITS == 5 ? nbox * a.R8 * 32u : 0u), 1024);
+        a.stage_bytes = align_up(a.hi_off + (any5 ? nbox * a.R8 * 32u : 0u), 1024);
+        // bytes per phase: its gate (or only) box, and a SwiGLU's up box (Q5 gate, Q4 up may differ)
         a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (BITS == 5 ? 32u : 0u));
+        if (NGU == 2) a.box_tx += static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (BITS_U == 5 ? 32u : 0u));
     }
     const uint32_t red_bytes = align_up(nbox * a.R8 * 4u * kMtTokens, 128);
     const uint32_t bar_bytes = 2 * kCcMaxStages * 8 + 16;
@@ -310,7 +328,8 @@ qg_status mt_launch(MtArgs m, const MtMaps& maps, int grid, cudaStream_t stream)
                align_up(static_cast<uint32_t>(W), 16) +
                (BITS != 0 ? align_up(static_cast<uint32_t>(m.M * W) * 32u, 16) : 0u);
     };
-    const uint32_t other = red_bytes + bar_bytes;
+    const uint32_t other = red_bytes + bar_bytes +
+                           (a.norm_w ? align_up(static_cast<uint32_t>(m.M * (a.C + 1)) * 4u, 16) : 0u);
     int W = a.C;
     if (win_bytes(W) + other + 4 * a.stage_bytes > kCcSmemMax) {
         W = (a.C / a.P) * a.P;
@@ -323,7 +342,8 @@ qg_status mt_launch(MtArgs m, const MtMaps& maps, int grid, cudaStream_t stream)
     const uint32_t pe_bytes = align_up(static_cast<uint32_t>(m.M * W) * 4u, 16);
     const uint32_t fl_bytes = align_up(static_cast<uint32_t>(W), 16);
     const uint32_t gx_bytes = BITS != 0 ? align_up(static_cast<uint32_t>(m.M * W) * 32u, 16) : 0u;
-    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + gx_bytes + red_bytes + bar_bytes;
+    const uint32_t ss_bytes = a.norm_w ? align_up(static_cast<uint32_t>(m.M * (a.C + 1)) * 4u, 16) : 0u;
+    const uint32_t fixed = x_bytes + pe_bytes + fl_bytes + gx_bytes + ss_bytes + red_bytes + bar_bytes;
     a.n_stages = std::min<int>(kCcMaxStages, static_cast<int>((kCcSmemMax - fixed) / a.stage_bytes));
     uint32_t so = 0;
     a.smem_ring = so;
@@ -336,20 +356,22 @@ qg_status mt_launch(MtArgs m, const MtMaps& maps, int grid, cudaStream_t stream)
     so += fl_bytes;
     a.smem_gx = so;
     so += gx_bytes;
+    a.smem_ss = so;
+    so += ss_bytes;
     a.smem_red = so;
     so += red_bytes;
     a.smem_bar = so;
     so += bar_bytes;
     if (so > kCcSmemMax) return QG_ERR_UNSUPPORTED;
 
-    auto kern = mt_gemv_kernel<EPI, BITS>;
-    static bool attr_set[64] = {false};
+    auto kern = a.norm_w ? mt_gemv_kernel<EPI, BITS, BITS_U, true> : mt_gemv_kernel<EPI, BITS, BITS_U, false>;
+    static bool attr_set[2][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ERR_CUDA;
-    if (!attr_set[dev]) {
+    if (!attr_set[a.norm_w ? 1 : 0][dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCcSmemMax) != cudaSuccess)
             return QG_ERR_CUDA;
-        attr_set[dev] = true;
+        attr_set[a.norm_w ? 1 : 0][dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -408,13 +430,15 @@ MtArgs mt_plan(const void* x, void* y, int out_f32, const void* residual, int M,
 // plan does not fit shared memory.
 qg_status launch_mt_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
                                 int out_f32, const void* residual, int M, int N, int K, int swiglu,
-                                cudaStream_t stream)
+                                cudaStream_t stream, const void* norm_w, float norm_eps)
 {
     if (M < 1 || M > kMtTokens || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
     const int sms = sm_count(-1);
     if (sms <= 0) return QG_ERR_CUDA;
     MtArgs m = mt_plan(x, y, out_f32, residual, M, swiglu ? N / 2 : N, swiglu ? 2 : 1, K, sms);
     m.a.g = g;
+    m.a.norm_w = static_cast<const uint16_t*>(norm_w);
+    m.a.norm_eps = norm_eps;
     const int grid = std::min(sms, m.a.n_units);
     MtMaps maps;
     memset(&maps, 0, sizeof(maps));
@@ -429,12 +453,14 @@ qg_status launch_mt_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, flo
 // Q4/Q5 with 1..8 tokens (plain or residual epilogue), K a multiple of 256.
 qg_status launch_mt_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const void* scale, const void* min, int bits,
                               const void* x, void* y, int out_f32, const void* residual, int M, int N, int K,
-                              cudaStream_t stream)
+                              cudaStream_t stream, const void* norm_w, float norm_eps)
 {
     if (M < 1 || M > kMtTokens || K % kChunkK != 0 || (bits != 4 && bits != 5)) return QG_ERR_UNSUPPORTED;
     const int sms = sm_count(-1);
     if (sms <= 0) return QG_ERR_CUDA;
     MtArgs m = mt_plan(x, y, out_f32, residual, M, N, 1, K, sms);
+    m.a.norm_w = static_cast<const uint16_t*>(norm_w);
+    m.a.norm_eps = norm_eps;
     const int grid = std::min(sms, m.a.n_units);
     const int R = m.a.R;
     MtMaps maps;
@@ -449,6 +475,41 @@ qg_status launch_mt_dense_q45(const uint8_t* q_lo, const uint8_t* q_hi, const vo
     if (bits == 5) return residual ? mt_launch<EPI_RESID, 5>(m, maps, grid, stream)
                                    : mt_launch<EPI_NONE, 5>(m, maps, grid, stream);
     return residual ? mt_launch<EPI_RESID, 4>(m, maps, grid, stream) : mt_launch<EPI_NONE, 4>(m, maps, grid, stream);
+}
+
+// Q4/Q5 SwiGLU (separate gate and up matrices, each Q4 or Q5) with 1..8
+// tokens, K a multiple of 256, optional RMSNorm prologue.
+qg_status launch_mt_swiglu_q45(const Q45Matrix& gate, const Q45Matrix& up, const void* x, void* y, int M, int I, int K,
+                               cudaStream_t stream, const void* norm_w, float norm_eps)
+{
+    if (M < 1 || M > kMtTokens || K % kChunkK != 0) return QG_ERR_UNSUPPORTED;
+    if ((gate.bits != 4 && gate.bits != 5) || (up.bits != 4 && up.bits != 5)) return QG_ERR_UNSUPPORTED;
+    const int sms = sm_count(-1);
+    if (sms <= 0) return QG_ERR_CUDA;
+    MtArgs m = mt_plan(x, y, 0, nullptr, M, I, 2, K, sms);
+    m.a.up_row_offset = 0;  // the up rows are the same rows of the up matrix
+    m.a.norm_w = static_cast<const uint16_t*>(norm_w);
+    m.a.norm_eps = norm_eps;
+    const int grid = std::min(sms, m.a.n_units);
+    const int R = m.a.R;
+    MtMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    const Q45Matrix* mats[2] = {&gate, &up};
+    for (int gg = 0; gg < 2; ++gg) {
+        const Q45Matrix& q = *mats[gg];
+        CUtensorMap* mm = &maps.m[4 * gg];
+        if (!encode_tmap_2d(&mm[0], q.q_lo, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, I, 128, R, true) ||
+            !encode_tmap_2d(&mm[1], q.scale, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, I, 8, R, false) ||
+            !encode_tmap_2d(&mm[2], q.min, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / 32, I, 8, R, false))
+            return QG_ERR_CUDA;
+        if (q.bits == 5 &&
+            !encode_tmap_2d(&mm[3], q.q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 8, I, 32, R, false))
+            return QG_ERR_CUDA;
+    }
+    if (gate.bits == 5 && up.bits == 4) return mt_launch<EPI_SWIGLU, 5, 4>(m, maps, grid, stream);
+    if (gate.bits == 5) return mt_launch<EPI_SWIGLU, 5, 5>(m, maps, grid, stream);
+    if (up.bits == 5) return mt_launch<EPI_SWIGLU, 4, 5>(m, maps, grid, stream);
+    return mt_launch<EPI_SWIGLU, 4, 4>(m, maps, grid, stream);
 }
 
 }  // namespace qg

@@ -262,9 +262,9 @@ typedef struct {
  *           QG_ERR_DEVICE_TIMEOUT the words must be zeroed again.
  * When K is a multiple of 256 for every op, the list runs as one persistent
  * kernel (one CTA per SM, launched cooperatively when an op waits for earlier
- * ones): the weight stream runs on across op boundaries. That holds for one
- * or two tokens, and for three to eight tokens when no op has the RMSNorm
- * prologue or the groupwise-int SwiGLU. Other lists run as one launch per op,
+ * ones): the weight stream runs on across op boundaries. Other lists (an op
+ * whose K is not a multiple of 256, or one that does not fit the kernel's
+ * shared memory) run as one launch per op,
  * in order, on `stream`; a single record is thus also the way to call any
  * projection with the RMSNorm prologue.
  * Every op is validated before anything is launched.

@@ -140,7 +140,7 @@ def test_rmsnorm_changes_the_result():
 
 # ---------------------------------------------------------------- RMSNorm + Q4/Q5
 @pytest.mark.parametrize("bits", [4, 5])
-@pytest.mark.parametrize("M,N,K", [(1, 1000, 5120), (2, 300, 1024), (8, 640, 2048), (1, 200, 800)])
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 5120), (2, 300, 1024), (4, 500, 17408), (8, 640, 2048), (1, 200, 800)])
 def test_rmsnorm_q45(bits, M, N, K):
     w = synth.q45_weights(87, f"rnq{bits}.{N}", N, K, bits)
     x = synth.bf16_normal(88, f"rnqx{M}.{K}", (M, K))
@@ -175,7 +175,7 @@ def swiglu_q45_case(M, I, K, gbits, ubits, seed, norm):
 
 
 @pytest.mark.parametrize("gbits,ubits", [(5, 4), (4, 4), (5, 5), (4, 5)])
-@pytest.mark.parametrize("M", [1, 2, 8])
+@pytest.mark.parametrize("M", [1, 2, 3, 8])
 @pytest.mark.parametrize("norm", [False, True])
 def test_swiglu_q45(gbits, ubits, M, norm):
     I, K = 1000, 2048
@@ -209,44 +209,47 @@ def test_swiglu_q45_ragged_and_small():
 
 
 # ---------------------------------------------------------------- chain with the new ops
-def test_chain_with_rmsnorm_matches_single_calls():
-    """RMSNorm ops inside the persistent one-token kernel give exactly what
-    the same records give one by one."""
+@pytest.mark.parametrize("M", [1, 4])
+def test_chain_with_rmsnorm_matches_single_calls(M):
+    """RMSNorm ops inside the persistent kernel (one token: CUDA-core stage;
+    four: warp-MMA stage) give exactly what the same records give one by one."""
     K = 5120
     gamma = to_dev(gamma_bits(K, 94))
     ops, host = [], []
     for name, N, epi in [("qkv", 7168, "none"), ("gu", 2 * 4096, "swiglu")]:
         w = synth.nvfp4_weights(95, f"chn.{name}", N, K)
-        x = to_dev(synth.bf16_normal(96, f"chn.{name}.x", (1, K)))
+        x = to_dev(synth.bf16_normal(96, f"chn.{name}.x", (4, K))[:M])
         n_out = N // 2 if epi == "swiglu" else N
         d = nvfp4_dev(w)
-        ops.append(nvfp4_op(d, x, torch.empty((1, n_out), dtype=torch.bfloat16, device="cuda"), epi, norm=gamma))
+        ops.append(nvfp4_op(d, x, torch.empty((M, n_out), dtype=torch.bfloat16, device="cuda"), epi, norm=gamma))
         host.append((d, x, n_out, epi))
     q.qgemv_chain(ops)
     torch.cuda.synchronize()
     for op, (d, x, n_out, epi) in zip(ops, host):
-        y1 = torch.empty((1, n_out), dtype=torch.bfloat16, device="cuda")
+        y1 = torch.empty((M, n_out), dtype=torch.bfloat16, device="cuda")
         q.qgemv_chain([nvfp4_op(d, x, y1, epi, norm=gamma)])
         torch.cuda.synchronize()
         assert torch.equal(op["y"].view(torch.int16), y1.view(torch.int16))
 
 
-def test_q45_layer_with_fused_ffn_in_one_call():
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_q45_layer_with_fused_ffn_in_one_call(M):
     """The mixed recipe's layer as one qgemv_chain call: QK (Q4) and V (Q5)
     with the RMSNorm prologue, O (Q4), the Q5/Q4 SwiGLU FFN with its own
-    RMSNorm, down (Q4) with the residual; every output against the oracle."""
+    RMSNorm, down (Q4) with the residual; every output against the oracle.
+    (Four and eight tokens: the warp-MMA stage.)"""
     d27 = synth.DENSE27B
     H, I = d27.hidden, d27.inter
     gam1, gam2 = gamma_bits(H, 97), gamma_bits(H, 98)
     specs = {name: (N, K, bits) for name, N, K, bits in synth.Q45_RECIPE}
     W = {name: synth.q45_weights(3, f"q45.{name}", N, K, bits) for name, (N, K, bits) in specs.items()}
-    xa = synth.bf16_normal(99, "lay.xa", (1, H))
-    attn = synth.bf16_normal(99, "lay.attn", (1, d27.o_k))
-    xf = synth.bf16_normal(99, "lay.xf", (1, H))
-    hmid = synth.bf16_normal(99, "lay.hmid", (1, I))
-    res = synth.bf16_normal(99, "lay.res", (1, H))
+    xa = synth.bf16_normal(99, "lay.xa", (8, H))[:M]
+    attn = synth.bf16_normal(99, "lay.attn", (8, d27.o_k))[:M]
+    xf = synth.bf16_normal(99, "lay.xf", (8, H))[:M]
+    hmid = synth.bf16_normal(99, "lay.hmid", (8, I))[:M]
+    res = synth.bf16_normal(99, "lay.res", (8, H))[:M]
     D = {k: q45_dev(v) for k, v in W.items()}
-    ys = {"qk": (1, specs["qk"][0]), "v": (1, specs["v"][0]), "o": (1, H), "ffn": (1, I), "down": (1, H)}
+    ys = {"qk": (M, specs["qk"][0]), "v": (M, specs["v"][0]), "o": (M, H), "ffn": (M, I), "down": (M, H)}
     Y = {k: torch.empty(s, dtype=torch.bfloat16, device="cuda") for k, s in ys.items()}
     g1, g2 = to_dev(gam1), to_dev(gam2)
     ops = [q_op(D["qk"], to_dev(xa), Y["qk"], norm=g1),
