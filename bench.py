@@ -165,8 +165,8 @@ class ClockSampler:
 # Kernel sources behind each workload's launches (one or two tokens: the
 # CUDA-core kernels; NVFP4 with three to eight tokens and Q4/Q5 with three to
 # six: the warp-MMA kernel; Q4/Q5 with seven or eight: the mma.sync kernel;
-# the MoE: the grouped CUDA-core expert kernels; the exact fallback kernel for
-# the normalised and fused groupwise-int ops at three or more tokens); a
+# the MoE: the grouped CUDA-core expert kernels; the chained layer: its
+# kernel at one or two tokens, the workspace kernels at three to eight); a
 # committed traffic figure is used only while these files are unchanged.
 KERNEL_SOURCES = {
     "simple": ("qgemv_simple.cu", "common.cuh", "qgemv_internal.h"),
@@ -176,12 +176,14 @@ KERNEL_SOURCES = {
     "mt": ("qgemv_mt.cu", "mt_core.cuh", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
     "moe": ("moe_cc.cu", "moe.cu", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
     "chain": ("qgemv_chain.cu", "cc_core.cuh", "mt_core.cuh", "common.cuh", "qgemv_internal.h"),
+    "chain_ws": ("qgemv_chain_ws.cu", "mt_core.cuh", "cc_core.cuh", "common.cuh", "qgemv_internal.h"),
 }
 
 
 def one_launch_chain(workload, M):
-    """Whether the layer's qgemv_chain call runs as one persistent launch (it
-    does for every layer of this bench at one to eight tokens)."""
+    """Whether the layer's qgemv_chain call runs as one persistent layer
+    kernel (it does for every layer of this bench at one to eight tokens; at
+    three to eight a small activation conversion kernel runs before it)."""
     return M <= 8
 
 
@@ -189,7 +191,7 @@ def kernel_family(workload, M):
     if workload == "moe":
         return "moe"
     if workload == "q45ffn" and M > 2:
-        return "simple"
+        return "mt"
     if M <= 2:
         return "cc"
     if workload == "q45":
@@ -390,7 +392,11 @@ class Workload:
             events[-1].record()
 
     def launches_per_step(self):
-        return 1 if (self.chains and one_launch_chain(self.kind, self.M)) else len(self.projs)
+        # a chained layer: one launch at one or two tokens; at three to eight
+        # the activation conversion kernel and the layer kernel
+        if self.chains and one_launch_chain(self.kind, self.M):
+            return 1 if self.M <= 2 else 2
+        return len(self.projs)
 
     def alg_bytes(self, idx):
         """Algorithmic bytes of call idx: weights + activations in + outputs."""
@@ -827,15 +833,17 @@ def measure(args, kind, M, world, rank, stream, cpu=True, e2e=True):
              "us_per_launch": dom_us, "traffic": traffic,
              "timing": "the projection alone, K launches in one CUDA graph, events on its stream"}
     if chained and one_launch_chain(kind, M):
-        # the step is one launch of the chained-layer kernel: it is the
+        # the step is the chained-layer kernel (at three to eight tokens with
+        # the conversion kernel ahead of it): it is the
         # dominant (only) kernel, timed by the headline graph itself
         step_bytes = sum(wl.alg_bytes(i) for i in range(n_calls))
         ach = step_bytes / (ms_per_step * 1e-3) / 1e9
         roofline = {"bound": "hbm",
-                    "kernel": ("chain_kernel" if M <= 2 else "chain_mt_kernel") + " (whole layer, one launch)",
+                    "kernel": ("chain_kernel (whole layer, one launch)" if M <= 2 else
+                               "chain_ws_convert_kernel + chain_ws_kernel (whole layer, two launches)"),
                     "achieved": ach,
                     "peak": peak, "unit": "GB/s", "frac": ach / peak, "peak_source": peak_src,
-                    "traffic": profiled_traffic(f"{kind}.chain.M{M}", "chain"),
+                    "traffic": profiled_traffic(f"{kind}.chain.M{M}", "chain" if M <= 2 else "chain_ws"),
                     "alg_bytes_per_launch": step_bytes, "us_per_launch": ms_per_step * 1e3,
                     "timing": "K launches in one CUDA graph (the headline region), events on its stream",
                     "largest_projection_alone": alone}
@@ -938,7 +946,7 @@ def main():
             "config": {"workload": head["workload"], "M": args.M,
                        "weight_bytes_per_step": head["weight_bytes_per_step"], "l2": head["l2"],
                        "parallelism": "one independent replica per GPU" if world > 1 else "single GPU",
-                       "step": "one qgemv_chain call (the layer's projections in one persistent launch)"
+                       "step": "one qgemv_chain call (the layer's projections in one persistent kernel)"
                                if head["chained"] else "one library call per projection",
                        "graph": "K steps captured in one CUDA graph (kernels only); us_per_call from a "
                                 "second graph with events between the calls (which serialise them)"},

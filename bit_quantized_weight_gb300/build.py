@@ -23,7 +23,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]
 
-SOURCES = ["api.cu", "qgemv_dense.cu", "qgemv_tc.cu", "qgemv_cc.cu", "qgemv_simple.cu", "moe.cu", "moe_noalloc.cu", "qgemv_chain.cu", "moe_cc.cu", "qgemv_mt.cu"]
+SOURCES = ["api.cu", "qgemv_dense.cu", "qgemv_tc.cu", "qgemv_cc.cu", "qgemv_simple.cu", "moe.cu", "moe_noalloc.cu", "qgemv_chain.cu", "moe_cc.cu", "qgemv_mt.cu",
+           "qgemv_chain_ws.cu"]
 
 
 def _sources():

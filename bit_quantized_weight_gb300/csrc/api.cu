@@ -79,8 +79,7 @@ int* device_status_ptr()
     return g_status_ptr[device];
 }
 
-bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
-                    uint64_t inner_elems, uint64_t rows, uint32_t box_inner, uint32_t box_rows, bool swizzle128)
+static EncodeTiledFn tmap_encoder()
 {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
@@ -90,12 +89,38 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtyp
             q == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     });
-    if (!g_encode) return false;
+    return g_encode;
+}
+
+bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
+                    uint64_t inner_elems, uint64_t rows, uint32_t box_inner, uint32_t box_rows, bool swizzle128)
+{
+    if (!tmap_encoder()) return false;
     const cuuint64_t dims[2] = {inner_elems, rows};
     const cuuint64_t strides[1] = {inner_elems * static_cast<uint64_t>(elem_bytes)};
     const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// A row-major [rows][chunks * inner] matrix viewed as (inner, rows, chunks),
+// so that one box brings box_chunks consecutive chunks of box_rows rows,
+// laid out chunk-major in shared memory ([chunk][row][inner]).
+bool encode_tmap_chunks(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
+                        uint64_t inner_elems, uint64_t rows, uint64_t chunks, uint32_t box_rows, uint32_t box_chunks,
+                        bool swizzle128)
+{
+    if (!tmap_encoder()) return false;
+    const uint64_t inner_bytes = inner_elems * static_cast<uint64_t>(elem_bytes);
+    const cuuint64_t dims[3] = {inner_elems, rows, chunks};
+    const cuuint64_t strides[2] = {inner_bytes * chunks, inner_bytes};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(inner_elems), box_rows, box_chunks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
                                 CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -368,7 +393,22 @@ qg_status moe_qgemv_nvfp4(const uint8_t* gu_codes, const uint8_t* gu_scales, con
                       workspace, workspace_bytes, M, H, I, E, topk, stream);
 }
 
+qg_status qgemv_chain_workspace_size(const qg_gemv_op* ops, int n_ops, int M, size_t* bytes)
+{
+    if (!ops || !bytes || n_ops < 1 || n_ops > 8 || M < 1 || M > kMaxTokens) return QG_ERR_INVALID_ARG;
+    for (int o = 0; o < n_ops; ++o)
+        if (ops[o].K < 1) return QG_ERR_INVALID_ARG;
+    *bytes = chain_workspace_bytes(ops, n_ops, M);
+    return QG_OK;
+}
+
 qg_status qgemv_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, cudaStream_t stream)
+{
+    return qgemv_chain_ws(ops, n_ops, M, sync, nullptr, 0, stream);
+}
+
+qg_status qgemv_chain_ws(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream)
 {
     if (!ops || n_ops < 1 || n_ops > 8 || M < 1 || M > kMaxTokens) return QG_ERR_INVALID_ARG;
     bool any_dep = false;
@@ -379,7 +419,13 @@ qg_status qgemv_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, c
     }
     if (sync && !aligned16(sync)) return QG_ERR_MISALIGNED;
     if (any_dep && !sync) return QG_ERR_INVALID_ARG;
-    qg_status s = launch_chain(ops, n_ops, M, sync, stream);
+    qg_status s = QG_ERR_UNSUPPORTED;
+    if (workspace) {
+        if (workspace_bytes < chain_workspace_bytes(ops, n_ops, M)) return QG_ERR_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QG_ERR_MISALIGNED;
+        if (M >= 3) s = launch_chain_ws(ops, n_ops, M, sync, workspace, stream);
+    }
+    if (s == QG_ERR_UNSUPPORTED) s = launch_chain(ops, n_ops, M, sync, stream);
     if (s != QG_ERR_UNSUPPORTED) return s;
     // One launch per op, in stream order (which also orders dependent ops).
     for (int o = 0; o < n_ops; ++o) {

@@ -200,8 +200,11 @@ __device__ void mt_convert(const MtArgs& m, uint8_t* smem, int warp, int lane, v
 // 256 k; d[] gets the MMA sums (rows g, g + 8; tokens 2c, 2c + 1), built in
 // two independent chains (the first and second MMA of each 32-k half) that
 // are added at the end.
+// sw: the box's first line modulo 8 when the box does not start a 1024-byte
+// swizzle period (the 128-byte swizzle follows the line's address).
 template <bool BF>
-__device__ __forceinline__ void mt_stage(uint32_t box, uint32_t sbox, uint32_t xc, int lane, int M, float (&d)[4])
+__device__ __forceinline__ void mt_stage(uint32_t box, uint32_t sbox, uint32_t xc, int lane, int M, float (&d)[4],
+                                         uint32_t sw = 0)
 {
     float d2[4] = {0.f, 0.f, 0.f, 0.f};
     const int g = lane >> 2, c = lane & 3;
@@ -211,7 +214,8 @@ __device__ __forceinline__ void mt_stage(uint32_t box, uint32_t sbox, uint32_t x
     for (int ti = 0; ti < 4; ++ti) {
         uint32_t cr[4];
         const int lc = 2 * ti + (lane >> 4);
-        mt_ldmatrix_x4(cr, box + static_cast<uint32_t>(lr) * 128u + ((static_cast<uint32_t>(lc ^ (lr & 7))) << 4));
+        mt_ldmatrix_x4(cr, box + static_cast<uint32_t>(lr) * 128u +
+                               ((static_cast<uint32_t>(lc) ^ ((static_cast<uint32_t>(lr) + sw) & 7u)) << 4));
         const uint32_t sw_g = lds32(sbox + static_cast<uint32_t>(g) * 16u + 4u * ti);
         const uint32_t sw_g8 = lds32(sbox + static_cast<uint32_t>(g + 8) * 16u + 4u * ti);
 #pragma unroll
@@ -255,7 +259,7 @@ __device__ __forceinline__ void mt_stage(uint32_t box, uint32_t sbox, uint32_t x
 template <int BITS, bool BF>
 __device__ __forceinline__ void mtq_stage(uint32_t box, uint32_t sbox, uint32_t mbox, uint32_t hbox, uint32_t xc,
                                           const float* gxt0, const float* gxt1, int lane, int M, float (&aq)[4],
-                                          float (&am)[4])
+                                          float (&am)[4], uint32_t sw = 0)
 {
     const int g = lane >> 2, c = lane & 3;
     const int lr = (lane & 7) + 8 * ((lane >> 3) & 1);
@@ -264,7 +268,8 @@ __device__ __forceinline__ void mtq_stage(uint32_t box, uint32_t sbox, uint32_t 
     for (int ti = 0; ti < 4; ++ti) {
         uint32_t cr[4];
         const int lc = 2 * ti + (lane >> 4);
-        mt_ldmatrix_x4(cr, box + static_cast<uint32_t>(lr) * 128u + ((static_cast<uint32_t>(lc ^ (lr & 7))) << 4));
+        mt_ldmatrix_x4(cr, box + static_cast<uint32_t>(lr) * 128u +
+                               ((static_cast<uint32_t>(lc) ^ ((static_cast<uint32_t>(lr) + sw) & 7u)) << 4));
         // the two groups of this tile: scale and min of rows g and g + 8
         const uint32_t sg = lds32(sbox + static_cast<uint32_t>(g) * 16u + 4u * ti);
         const uint32_t sg8 = lds32(sbox + static_cast<uint32_t>(g + 8) * 16u + 4u * ti);

@@ -131,6 +131,9 @@ int sm_count(int device);
 bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
                     uint64_t inner_elems, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
                     bool swizzle128);
+bool encode_tmap_chunks(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
+                        uint64_t inner_elems, uint64_t rows, uint64_t chunks, uint32_t box_rows, uint32_t box_chunks,
+                        bool swizzle128);
 
 qg_status launch_dense_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, const void* x, void* y,
                              int out_f32, const void* residual, int M, int N, int K, int swiglu,
@@ -201,5 +204,10 @@ size_t moe_workspace_bytes(int M, int topk, int H, int I, int E);
 // One persistent launch for a list of one-token projections (qgemv_chain.cu);
 // QG_ERR_UNSUPPORTED when the list does not fit its plan.
 qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, cudaStream_t stream);
+// 3..8 tokens with the activations converted once into a workspace of
+// chain_workspace_bytes() (qgemv_chain_ws.cu).
+size_t chain_workspace_bytes(const qg_gemv_op* ops, int n_ops, int M);
+qg_status launch_chain_ws(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, void* workspace,
+                          cudaStream_t stream);
 
 }  // namespace qg

@@ -73,6 +73,8 @@ def lib():
                                       _I, _I, _I, _I, _I, _P]
         L.moe_qgemv_nvfp4_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]
         L.qgemv_chain.argtypes = [ctypes.POINTER(QgGemvOp), _I, _I, _P, _P]
+        L.qgemv_chain_ws.argtypes = [ctypes.POINTER(QgGemvOp), _I, _I, _P, _P, ctypes.c_size_t, _P]
+        L.qgemv_chain_workspace_size.argtypes = [ctypes.POINTER(QgGemvOp), _I, _I, ctypes.POINTER(ctypes.c_size_t)]
         L.qgemv_swiglu_q45.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _F, _P, _I, _I, _I, _P]
         L.qdequant_nvfp4.argtypes = [_P, _P, _F, _P, _I, _I, _P]
         L.qdequant_q45.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _P]
@@ -83,7 +85,8 @@ def lib():
         L.qg_debug_set_wait.argtypes = [ctypes.c_uint64, _I]
         for name in ("qgemv_nvfp4", "qgemv_q45", "qgemv_swiglu_nvfp4", "moe_route_topk",
                      "moe_qgemv_nvfp4_workspace_size", "moe_qgemv_nvfp4", "moe_qgemv_nvfp4_noalloc",
-                     "qgemv_chain", "qgemv_swiglu_q45", "qdequant_nvfp4",
+                     "qgemv_chain", "qgemv_chain_ws", "qgemv_chain_workspace_size", "qgemv_swiglu_q45",
+                     "qdequant_nvfp4",
                      "qdequant_q45", "qg_last_device_status", "qg_debug_set_wait"):
             getattr(L, name).restype = _I
         _lib = L
@@ -211,9 +214,12 @@ class GemvChain:
     format (NVFP4: codes, scales, g; Q4/Q5: q_lo, q_hi (Q5), scale, min),
     "x", "y", optionally "residual", "epilogue" ("none", "residual",
     "swiglu") and "after_previous" (bool). The tensors must stay alive and
-    unchanged in place for as long as the chain is run."""
+    unchanged in place for as long as the chain is run. By default the chain
+    owns a workspace (qgemv_chain_ws: activations converted once per call);
+    workspace=False runs qgemv_chain without one. Runs of one chain must not
+    overlap on the GPU (they share the workspace)."""
 
-    def __init__(self, ops, sync=None):
+    def __init__(self, ops, sync=None, workspace=True):
         """ops: dicts as above; optional "norm" (bf16 gamma [K] tensor) and
         "norm_eps" select the RMSNorm prologue, and for groupwise-int SwiGLU
         "up" is a dict with the up matrix's q_lo, q_hi, scale, min."""
@@ -260,15 +266,21 @@ class GemvChain:
         self.n, self.M = n, M
         self.sync = sync
         self.like = ops[0]["y"]
+        self.ws, self.ws_bytes = None, 0
+        if workspace:
+            nb = ctypes.c_size_t(0)
+            _check("qgemv_chain_workspace_size", lib().qgemv_chain_workspace_size(self.ops, n, M, ctypes.byref(nb)))
+            self.ws_bytes = max(int(nb.value), 256)
+            self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.like.device)
 
     def run(self, stream=None):
-        _check("qgemv_chain", lib().qgemv_chain(self.ops, self.n, self.M, _ptr(self.sync),
-                                                _stream(stream, self.like)))
+        _check("qgemv_chain", lib().qgemv_chain_ws(self.ops, self.n, self.M, _ptr(self.sync), _ptr(self.ws),
+                                                   self.ws_bytes, _stream(stream, self.like)))
 
 
-def qgemv_chain(ops, sync=None, stream=None):
+def qgemv_chain(ops, sync=None, stream=None, workspace=True):
     """Run a list of projections as one qgemv_chain call (see GemvChain)."""
-    GemvChain(ops, sync).run(stream)
+    GemvChain(ops, sync, workspace).run(stream)
 
 
 def qgemv_swiglu_q45(gate, up, x, y, norm=None, norm_eps=1e-6, stream=None):

@@ -67,7 +67,7 @@ typedef enum {
     QG_ERR_INVALID_ARG = 1,    /* a size, pointer or enum is out of range   */
     QG_ERR_UNSUPPORTED = 2,    /* valid request this build does not serve    */
     QG_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned           */
-    QG_ERR_WORKSPACE = 4,      /* MoE workspace missing or too small         */
+    QG_ERR_WORKSPACE = 4,      /* a workspace missing or too small           */
     QG_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed       */
     QG_ERR_DEVICE_TIMEOUT = 6  /* a bounded device-side wait ran out         */
 } qg_status;
@@ -270,6 +270,35 @@ typedef struct {
  * Every op is validated before anything is launched.
  */
 QG_API qg_status qgemv_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, cudaStream_t stream);
+
+/*
+ * qgemv_chain with a workspace: the same ops, the same results (bit for
+ * bit), and at M = 3..8 a faster plan. A small kernel first converts every
+ * op's activations once (the exact f16 prescale per 256-k chunk that each
+ * kernel otherwise repeats per CTA) into the workspace, and the layer
+ * kernel's TMA warp streams them into shared memory beside the weights; an
+ * op with after_previous is converted inside the layer kernel after its
+ * grid-wide barrier (an op with after_previous and norm_weight falls back to
+ * qgemv_chain's plan). At M = 1..2 the workspace is not used.
+ *   workspace        device memory of at least
+ *                    qgemv_chain_workspace_size() bytes, 256-byte aligned
+ *                    (else QG_ERR_MISALIGNED); NULL runs qgemv_chain. Its
+ *                    contents need no initialisation and are scratch after
+ *                    the call; calls that may overlap on the GPU need
+ *                    separate workspaces.
+ *   workspace_bytes  its size (QG_ERR_WORKSPACE if too small)
+ * Other arguments and errors as for qgemv_chain.
+ */
+QG_API qg_status qgemv_chain_ws(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Bytes of qgemv_chain_ws's workspace for these ops and M: for each op,
+ * K/256 blocks of M * 576 + 48 bytes (NVFP4) or M * 576 + 304 bytes
+ * (Q4/Q5), rounded up to 256. QG_ERR_INVALID_ARG for a null pointer, n_ops
+ * outside 1..8, M outside 1..8 or K < 1; nothing is launched.
+ */
+QG_API qg_status qgemv_chain_workspace_size(const qg_gemv_op* ops, int n_ops, int M, size_t* bytes);
 
 /*
  * SwiGLU over separate groupwise-int gate and up matrices, for the recipe

@@ -29,6 +29,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("qgemv_nvfp4", "qgemv_q45", "qgemv_swiglu_nvfp4", "moe_qgemv_nvfp4", "qgemv_chain", "qgemv_swiglu_q45",
+              "qgemv_chain_ws", "qgemv_chain_workspace_size",
               "moe_qgemv_nvfp4_workspace_size", "moe_route_topk", "qdequant_nvfp4", "qdequant_q45",
               "qg_last_device_status", "qg_status_string"):
         assert n in names
@@ -182,6 +183,36 @@ def test_chain_validation(L):
     assert _chain(L, [_op(epilogue=2, up_codes=A, up_format=1, up_scales=A, up_mins=None, **q5)]) == 1
     assert _chain(L, [_op(epilogue=2, up_codes=A + 4, up_format=1, up_scales=A, up_mins=A, **q5)]) == 3
     assert _chain(L, [_op(up_scales=A)]) == 1                                             # stray up field
+
+
+def test_chain_workspace_size(L):
+    import bit_quantized_weight_gb300 as q
+    recs = [_op(N=64, K=1024), _op(format=2, mins=A, q_hi=A, N=32, K=512), _op(K=256 * 68)]
+    arr = (q.QgGemvOp * 3)(*recs)
+    sz = ctypes.c_size_t(0)
+    for M in (1, 3, 8):
+        assert L.qgemv_chain_workspace_size(arr, 3, M, ctypes.byref(sz)) == 0
+        up = lambda v: (v + 255) // 256 * 256
+        want = up(4 * (M * 576 + 48)) + up(2 * (M * 576 + 304)) + up(68 * (M * 576 + 48))
+        assert sz.value == want
+    assert L.qgemv_chain_workspace_size(arr, 3, 9, ctypes.byref(sz)) == 1
+    assert L.qgemv_chain_workspace_size(arr, 0, 4, ctypes.byref(sz)) == 1
+    assert L.qgemv_chain_workspace_size(None, 1, 4, ctypes.byref(sz)) == 1
+    assert L.qgemv_chain_workspace_size(arr, 3, 4, None) == 1
+
+
+@fake_ptr
+def test_chain_ws_validation(L):
+    import bit_quantized_weight_gb300 as q
+    arr = (q.QgGemvOp * 2)(_op(K=1024), _op(K=512))
+    sz = ctypes.c_size_t(0)
+    assert L.qgemv_chain_workspace_size(arr, 2, 4, ctypes.byref(sz)) == 0
+    # op checks first, then the workspace's size and alignment
+    bad = (q.QgGemvOp * 1)(_op(x=A + 8))
+    assert L.qgemv_chain_ws(bad, 1, 4, None, A, 1 << 20, None) == 3
+    assert L.qgemv_chain_ws(arr, 2, 4, None, A, sz.value - 16, None) == 4
+    assert L.qgemv_chain_ws(arr, 2, 4, None, A + 16, sz.value, None) == 3
+    assert L.qgemv_chain_ws(arr, 2, 9, None, A, sz.value, None) == 1
 
 
 @fake_ptr
