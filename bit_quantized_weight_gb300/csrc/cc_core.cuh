@@ -42,6 +42,8 @@ struct CcArgs {
     int n_stages;
     uint32_t stage_bytes;
     uint32_t scales_off;
+    uint32_t code_pitch;       // chunked layout (chained kernels): bytes between a stage's matrices' code boxes
+    uint32_t sc_pitch;         // the same for scales and mins (the Q5 plane: twice)
     uint32_t box_tx;
     uint32_t smem_ring;
     uint32_t smem_x;           // activations: C chunks of 256 f16 (or raw bf16)
@@ -65,9 +67,18 @@ struct CcArgs {
 
 // Shared-memory geometry of a stage as plain values: a kernel that walks
 // several plans (the chained-layer kernel) keeps them in registers instead of
-// indexing its parameter block inside the stage loop.
+// indexing its parameter block inside the stage loop. Box b2 (phase b2 >>
+// gsh, matrix b2 & (2^gsh - 1)) starts at code line (b2 & m) * gl + (b2 >>
+// gsh) * pl and scale row (b2 & m) * gls + (b2 >> gsh) * pl: with gsh = 0
+// and pl = R8 the per-phase layout (box b2 at b2 * R8); the chunked layout
+// of the chained kernel has pl = R (one box per matrix holds a stage's
+// chunks, R rows each) and gl, gls its matrices' pitches. Code lines are 128
+// bytes, swizzled by (line & 7); scale rows 16 bytes, Q5 plane rows 32.
 struct CcGeom {
-    int R8;
+    int pl;
+    int gl;
+    int gls;
+    int gsh;
     uint32_t scales_off;
     uint32_t mins_off;
     uint32_t hi_off;
@@ -75,7 +86,24 @@ struct CcGeom {
 
 __device__ __forceinline__ CcGeom cc_geom(const CcArgs& a)
 {
-    return CcGeom{a.R8, a.scales_off, a.mins_off, a.hi_off};
+    return CcGeom{a.R8, 0, 0, 0, a.scales_off, a.mins_off, a.hi_off};
+}
+
+// The chunked layout of a chained kernel's stage (gsh: log2 of the matrices).
+__device__ __forceinline__ CcGeom cc_geom_chunked(const CcArgs& a, int gsh)
+{
+    return CcGeom{a.R, static_cast<int>(a.code_pitch / 128u), static_cast<int>(a.sc_pitch / 16u), gsh, a.scales_off,
+                  a.mins_off, a.hi_off};
+}
+
+__device__ __forceinline__ uint32_t cc_code_line(const CcGeom& g, int b2)
+{
+    return static_cast<uint32_t>((b2 & ((1 << g.gsh) - 1)) * g.gl + (b2 >> g.gsh) * g.pl);
+}
+
+__device__ __forceinline__ uint32_t cc_scale_row(const CcGeom& g, int b2)
+{
+    return static_cast<uint32_t>((b2 & ((1 << g.gsh) - 1)) * g.gls + (b2 >> g.gsh) * g.pl);
 }
 
 __device__ __forceinline__ bool cc_wait_warp(uint64_t* bar, uint32_t parity, const CcArgs& a,
@@ -315,13 +343,15 @@ __device__ __forceinline__ void cc_stage(const CcGeom& a, uint32_t stage, int b2
     constexpr int KS = kChunkK / NSEG;  // 32 or 16 k
     constexpr int NW = KS / 8;          // code words per row
     constexpr int NB = NW / 2;          // 16-k blocks per row
+    const uint32_t cl = cc_code_line(a, b2) + static_cast<uint32_t>(row0);
+    const uint32_t sr = cc_scale_row(a, b2) + static_cast<uint32_t>(row0);
     uint32_t cw[kCcRows][NW];
     float sc[kCcRows][NB];
 #pragma unroll
     for (int i = 0; i < kCcRows; ++i) {
-        const int r = row0 + i;
-        const uint32_t rowb = stage + static_cast<uint32_t>(b2 * a.R8 + r) * 128u;
-        const uint32_t chunk = static_cast<uint32_t>((NW == 4 ? seg : seg >> 1) ^ (r & 7));
+        const uint32_t line = cl + static_cast<uint32_t>(i);
+        const uint32_t rowb = stage + line * 128u;
+        const uint32_t chunk = static_cast<uint32_t>(NW == 4 ? seg : seg >> 1) ^ (line & 7u);
         if constexpr (NW == 4) {
             const uint4 v = lds128(rowb + (chunk << 4));
             cw[i][0] = v.x; cw[i][1] = v.y; cw[i][2] = v.z; cw[i][3] = v.w;
@@ -330,7 +360,7 @@ __device__ __forceinline__ void cc_stage(const CcGeom& a, uint32_t stage, int b2
             cw[i][0] = v.x; cw[i][1] = v.y;
         }
         // the NB scale bytes of this segment
-        const uint32_t sb = stage + a.scales_off + static_cast<uint32_t>((b2 * a.R8 + r) * 16 + seg * NB);
+        const uint32_t sb = stage + a.scales_off + (sr + static_cast<uint32_t>(i)) * 16u + static_cast<uint32_t>(seg * NB);
         const uint32_t two = NB == 2 ? lds16(sb) : lds8(sb);
         const uint32_t h2 = e4m3x2_to_f16x2(two);
         sc[i][0] = half_bits_to_f32(h2 & 0xFFFFu);
@@ -381,13 +411,15 @@ __device__ __forceinline__ void cc_stage_mt(const CcGeom& a, uint32_t stage, int
     constexpr int KS = kChunkK / NSEG;
     constexpr int NW = KS / 8;
     constexpr int NB = NW / 2;
+    const uint32_t cl = cc_code_line(a, b2) + static_cast<uint32_t>(row0);
+    const uint32_t sr = cc_scale_row(a, b2) + static_cast<uint32_t>(row0);
     uint32_t cw[kCcRows][NW];
     float sc[kCcRows][NB];
 #pragma unroll
     for (int i = 0; i < kCcRows; ++i) {
-        const int r = row0 + i;
-        const uint32_t rowb = stage + static_cast<uint32_t>(b2 * a.R8 + r) * 128u;
-        const uint32_t chunk = static_cast<uint32_t>((NW == 4 ? seg : seg >> 1) ^ (r & 7));
+        const uint32_t line = cl + static_cast<uint32_t>(i);
+        const uint32_t rowb = stage + line * 128u;
+        const uint32_t chunk = static_cast<uint32_t>(NW == 4 ? seg : seg >> 1) ^ (line & 7u);
         if constexpr (NW == 4) {
             const uint4 v = lds128(rowb + (chunk << 4));
             cw[i][0] = v.x; cw[i][1] = v.y; cw[i][2] = v.z; cw[i][3] = v.w;
@@ -395,7 +427,7 @@ __device__ __forceinline__ void cc_stage_mt(const CcGeom& a, uint32_t stage, int
             const uint2 v = lds64(rowb + (chunk << 4) + static_cast<uint32_t>(seg & 1) * 8u);
             cw[i][0] = v.x; cw[i][1] = v.y;
         }
-        const uint32_t sb = stage + a.scales_off + static_cast<uint32_t>((b2 * a.R8 + r) * 16 + seg * NB);
+        const uint32_t sb = stage + a.scales_off + (sr + static_cast<uint32_t>(i)) * 16u + static_cast<uint32_t>(seg * NB);
         const uint32_t two = NB == 2 ? lds16(sb) : lds8(sb);
         const uint32_t h2 = e4m3x2_to_f16x2(two);
         sc[i][0] = half_bits_to_f32(h2 & 0xFFFFu);
@@ -600,17 +632,20 @@ __device__ __forceinline__ void cc_stage_q45(const CcGeom& a, uint32_t stage, in
     constexpr int KS = kChunkK / NSEG;
     constexpr int NW = KS / 8;
     const int grp = NSEG == 8 ? seg : seg >> 1;
+    const uint32_t cl = cc_code_line(a, b2) + static_cast<uint32_t>(row0);
+    const uint32_t sr = cc_scale_row(a, b2) + static_cast<uint32_t>(row0);
 #pragma unroll
     for (int i = 0; i < kCcRows; ++i) {
-        const int r = row0 + i;  // padding rows (r >= R) read as zeros
-        const uint32_t rowi = static_cast<uint32_t>(b2 * a.R8 + r);
-        const uint32_t chunk = static_cast<uint32_t>((NW == 4 ? seg : seg >> 1) ^ (r & 7));
+        // rows at or past R: padding (zeros) or another box's rows; never stored
+        const uint32_t line = cl + static_cast<uint32_t>(i);
+        const uint32_t rowi = sr + static_cast<uint32_t>(i);
+        const uint32_t chunk = static_cast<uint32_t>(NW == 4 ? seg : seg >> 1) ^ (line & 7u);
         uint32_t cw[NW];
         if constexpr (NW == 4) {
-            const uint4 v = lds128(stage + rowi * 128u + (chunk << 4));
+            const uint4 v = lds128(stage + line * 128u + (chunk << 4));
             cw[0] = v.x; cw[1] = v.y; cw[2] = v.z; cw[3] = v.w;
         } else {
-            const uint2 v = lds64(stage + rowi * 128u + (chunk << 4) + static_cast<uint32_t>(seg & 1) * 8u);
+            const uint2 v = lds64(stage + line * 128u + (chunk << 4) + static_cast<uint32_t>(seg & 1) * 8u);
             cw[0] = v.x; cw[1] = v.y;
         }
         uint32_t hb = 0;

@@ -125,7 +125,7 @@ __device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, int epi, uint
     const bool swiglu = epi == EPI_SWIGLU, resid = epi == EPI_RESID;
     const int gsh = swiglu ? 1 : 0;   // log2 of the boxes per phase (gate and up rows)
     // the op's plan in registers (the parameter block is indexed by op)
-    const CcGeom geom = cc_geom(a);
+    const CcGeom geom = cc_geom_chunked(a, gsh);
     const int R = a.R, P = a.P, C = a.C, Cp = a.Cp, n_units = a.n_units, n_out = a.n_out;
     const float gscale = a.g;
     const int rg_per_box = (R + kCcRows - 1) / kCcRows;
@@ -198,7 +198,7 @@ __device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, int epi, uint
 #pragma unroll
             for (int i = 0; i < kCcRows; ++i)
 #pragma unroll
-                for (int t = 0; t < MT; ++t) red[(b2 * geom.R8 + row0 + i) * MT + t] = acc[i * MT + t];
+                for (int t = 0; t < MT; ++t) red[(b2 * a.R8 + row0 + i) * MT + t] = acc[i * MT + t];
         }
         named_barrier_sync(1, kCcThreads);
         if (!aborted) {
@@ -207,11 +207,11 @@ __device__ __forceinline__ void chain_units_nvfp4(const CcArgs& a, int epi, uint
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
                     float v0 = 0.f, v1 = 0.f;
-                    for (int pp = 0; pp < P; ++pp) v0 += red[((pp << gsh) * geom.R8 + r) * MT + t];
+                    for (int pp = 0; pp < P; ++pp) v0 += red[((pp << gsh) * a.R8 + r) * MT + t];
                     v0 *= gscale;
                     float val = v0;
                     if (swiglu) {
-                        for (int pp = 0; pp < P; ++pp) v1 += red[(((pp << gsh) + 1) * geom.R8 + r) * MT + t];
+                        for (int pp = 0; pp < P; ++pp) v1 += red[(((pp << gsh) + 1) * a.R8 + r) * MT + t];
                         v1 *= gscale;
                         val = (v0 / (1.0f + expf(-v0))) * v1;
                     }
@@ -239,7 +239,7 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, int epi, uint8_
     constexpr int KS = kChunkK / NSEG;
     const bool swiglu = epi == EPI_SWIGLU, resid = epi == EPI_RESID;
     const int gsh = swiglu ? 1 : 0;
-    const CcGeom geom = cc_geom(a);
+    const CcGeom geom = cc_geom_chunked(a, gsh);
     const int R = a.R, P = a.P, C = a.C, Cp = a.Cp, n_units = a.n_units, n_out = a.n_out;
     const int rg_per_box = (R + kCcRows - 1) / kCcRows;
     const int item = threadIdx.x;
@@ -318,7 +318,7 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, int epi, uint8_
 #pragma unroll
             for (int i = 0; i < kCcRows; ++i)
 #pragma unroll
-                for (int t = 0; t < MT; ++t) red[(b2 * geom.R8 + row0 + i) * MT + t] = acc[i * MT + t];
+                for (int t = 0; t < MT; ++t) red[(b2 * a.R8 + row0 + i) * MT + t] = acc[i * MT + t];
         }
         named_barrier_sync(1, kCcThreads);
         if (!aborted) {
@@ -327,10 +327,10 @@ __device__ __forceinline__ void chain_units_q45(const CcArgs& a, int epi, uint8_
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
                     float val = 0.f;
-                    for (int pp = 0; pp < P; ++pp) val += red[((pp << gsh) * geom.R8 + r) * MT + t];
+                    for (int pp = 0; pp < P; ++pp) val += red[((pp << gsh) * a.R8 + r) * MT + t];
                     if (swiglu) {
                         float v1 = 0.f;
-                        for (int pp = 0; pp < P; ++pp) v1 += red[(((pp << gsh) + 1) * geom.R8 + r) * MT + t];
+                        for (int pp = 0; pp < P; ++pp) v1 += red[(((pp << gsh) + 1) * a.R8 + r) * MT + t];
                         val = (val / (1.0f + expf(-val))) * v1;
                     }
                     const int o = t * n_out + r0 + r;
@@ -394,8 +394,8 @@ __device__ __forceinline__ void chain_producer(const ChainParams& p, uint8_t* sm
         const CcArgs& a = p.op[o].a;
         const int fmt = p.op[o].fmt;
         const int ngu = p.op[o].epi == EPI_SWIGLU ? 2 : 1;
-        const int P = a.P, C = a.C, Cp = a.Cp, R = a.R, n_units = a.n_units, up_off = a.up_row_offset;
-        const uint32_t box_bytes = static_cast<uint32_t>(a.R8) * 128u, sbox_bytes = static_cast<uint32_t>(a.R8) * 16u;
+        const int P = a.P, Cp = a.Cp, R = a.R, n_units = a.n_units, up_off = a.up_row_offset;
+        const uint32_t cpitch = a.code_pitch, spitch = a.sc_pitch;
         const uint32_t scales_off = a.scales_off, mins_off = a.mins_off, hi_off = a.hi_off, box_tx = a.box_tx;
         for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
             const int row0 = u * R;
@@ -408,39 +408,25 @@ __device__ __forceinline__ void chain_producer(const ChainParams& p, uint8_t* sm
                     stop = true;
                     break;
                 }
-                int live = 0;
-                for (int pp = 0; pp < P; ++pp) live += (c * P + pp < C) ? 1 : 0;
                 uint8_t* sb = smem + a.smem_ring + slot * p.slot_bytes;
                 if (elect_one()) {
-                    // NVFP4: box_tx per (phase, gate/up) box; groupwise int: per phase
-                    const uint32_t phase_tx = fmt == FMT_NVFP4 ? static_cast<uint32_t>(ngu) * box_tx : box_tx;
-                    mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live) * phase_tx);
-                    for (int pp = 0; pp < P; ++pp) {
-                        const int kc = c * P + pp;
-                        if (kc >= C) continue;
+                    // per matrix one box of the stage's P chunks x R rows
+                    // (chunks past K are filled with zeros and still counted)
+                    mbar_arrive_expect_tx(&full[slot], box_tx);
+                    const int kc0 = c * P;
+                    for (int gg = 0; gg < ngu; ++gg) {
                         if (fmt == FMT_NVFP4) {
-                            for (int gg = 0; gg < ngu; ++gg) {
-                                const int b2 = pp * ngu + gg;
-                                const int row = row0 + gg * up_off;
-                                tma_load_2d(sb + b2 * box_bytes, &p.map[o][0], kc * (kChunkK / 2), row,
-                                            &full[slot]);
-                                tma_load_2d(sb + scales_off + b2 * sbox_bytes, &p.map[o][1],
-                                            kc * (kChunkK / 16), row, &full[slot]);
-                            }
+                            const int row = row0 + gg * up_off;
+                            tma_load_3d(sb + gg * cpitch, &p.map[o][0], 0, row, kc0, &full[slot]);
+                            tma_load_3d(sb + scales_off + gg * spitch, &p.map[o][1], 0, row, kc0, &full[slot]);
                         } else {
                             // gate (or only) box, then a SwiGLU's up box: same rows of two matrices
-                            for (int gg = 0; gg < ngu; ++gg) {
-                                const uint32_t b2 = static_cast<uint32_t>(pp * ngu + gg);
-                                const CUtensorMap* mp = &p.map[o][4 * gg];
-                                tma_load_2d(sb + b2 * box_bytes, mp, kc * (kChunkK / 2), row0, &full[slot]);
-                                tma_load_2d(sb + scales_off + b2 * sbox_bytes, mp + 1, kc * (kChunkK / 32),
-                                            row0, &full[slot]);
-                                tma_load_2d(sb + mins_off + b2 * sbox_bytes, mp + 2, kc * (kChunkK / 32), row0,
-                                            &full[slot]);
-                                if ((gg ? p.op[o].ufmt : fmt) == FMT_Q5)
-                                    tma_load_2d(sb + hi_off + b2 * 2u * sbox_bytes, mp + 3, kc * (kChunkK / 8),
-                                                row0, &full[slot]);
-                            }
+                            const CUtensorMap* mp = &p.map[o][4 * gg];
+                            tma_load_3d(sb + gg * cpitch, mp, 0, row0, kc0, &full[slot]);
+                            tma_load_3d(sb + scales_off + gg * spitch, mp + 1, 0, row0, kc0, &full[slot]);
+                            tma_load_3d(sb + mins_off + gg * spitch, mp + 2, 0, row0, kc0, &full[slot]);
+                            if ((gg ? p.op[o].ufmt : fmt) == FMT_Q5)
+                                tma_load_3d(sb + hi_off + gg * 2u * spitch, mp + 3, 0, row0, kc0, &full[slot]);
                         }
                     }
                 }
@@ -564,11 +550,15 @@ __device__ __forceinline__ void chain_units_mt(const MtArgs& m, int epi, uint8_t
     const uint8_t* fl = smem + a.smem_fl;
     const float* gx_all = reinterpret_cast<const float*>(smem + a.smem_gx);
     float* red = reinterpret_cast<float*>(smem + a.smem_red);
-    const uint32_t rowb = static_cast<uint32_t>(b2 * R8 + 16 * rb);
-    const uint32_t box_off = rowb * 128u;
-    const uint32_t sbox_off = a.scales_off + rowb * 16u;
-    const uint32_t mbox_off = a.mins_off + rowb * 16u;
-    const uint32_t hbox_off = a.hi_off + rowb * 32u;
+    // the chunked stage layout: matrix gm's box holds [chunk][row], R rows per
+    // chunk (rows past R read the next chunk's rows or the slot's tail)
+    const uint32_t gm = active ? static_cast<uint32_t>(b2 % ngu) : 0u;
+    const uint32_t r0 = static_cast<uint32_t>(p * R + 16 * rb);
+    const uint32_t sw = r0 & 7u;
+    const uint32_t box_off = gm * a.code_pitch + r0 * 128u;
+    const uint32_t sbox_off = a.scales_off + gm * a.sc_pitch + r0 * 16u;
+    const uint32_t mbox_off = a.mins_off + gm * a.sc_pitch + r0 * 16u;
+    const uint32_t hbox_off = a.hi_off + gm * 2u * a.sc_pitch + r0 * 32u;
     const uint32_t x0 = smem_u32(smem + a.smem_x) + static_cast<uint32_t>(g) * m.x_tok;
 
     int cur_win = 0;
@@ -594,9 +584,9 @@ __device__ __forceinline__ void chain_units_mt(const MtArgs& m, int epi, uint8_t
                 if constexpr (BITS == 0) {
                     float d[4] = {0.f, 0.f, 0.f, 0.f};
                     if (bf)
-                        mt_stage<true>(stage + box_off, stage + sbox_off, xc, lane, M, d);
+                        mt_stage<true>(stage + box_off, stage + sbox_off, xc, lane, M, d, sw);
                     else
-                        mt_stage<false>(stage + box_off, stage + sbox_off, xc, lane, M, d);
+                        mt_stage<false>(stage + box_off, stage + sbox_off, xc, lane, M, d, sw);
                     acc[0] = fmaf(d[0], pe0, acc[0]);
                     acc[1] = fmaf(d[1], pe1, acc[1]);
                     acc[2] = fmaf(d[2], pe0, acc[2]);
@@ -608,16 +598,16 @@ __device__ __forceinline__ void chain_units_mt(const MtArgs& m, int epi, uint8_t
                     if (swiglu && (b2 & 1)) {  // the up matrix's box
                         if (bf)
                             mtq_stage<BITS_U, true>(stage + box_off, stage + sbox_off, stage + mbox_off,
-                                                    stage + hbox_off, xc, gx0, gx1, lane, M, aq, am);
+                                                    stage + hbox_off, xc, gx0, gx1, lane, M, aq, am, sw);
                         else
                             mtq_stage<BITS_U, false>(stage + box_off, stage + sbox_off, stage + mbox_off,
-                                                     stage + hbox_off, xc, gx0, gx1, lane, M, aq, am);
+                                                     stage + hbox_off, xc, gx0, gx1, lane, M, aq, am, sw);
                     } else if (bf) {
                         mtq_stage<BITS, true>(stage + box_off, stage + sbox_off, stage + mbox_off, stage + hbox_off,
-                                              xc, gx0, gx1, lane, M, aq, am);
+                                              xc, gx0, gx1, lane, M, aq, am, sw);
                     } else {
                         mtq_stage<BITS, false>(stage + box_off, stage + sbox_off, stage + mbox_off,
-                                               stage + hbox_off, xc, gx0, gx1, lane, M, aq, am);
+                                               stage + hbox_off, xc, gx0, gx1, lane, M, aq, am, sw);
                     }
                     const float f0 = bf ? 1.0f : 16777216.0f * pe0, f1 = bf ? 1.0f : 16777216.0f * pe1;
                     acc[0] = fmaf(aq[0], f0, acc[0]) + am[0];
@@ -783,6 +773,53 @@ void cc_plan(CcArgs& a, int n_out, int ngu, int K, int sms)
 // the ops one by one instead.
 namespace {
 
+// The chunked stage layout of op g in both chained plans: per matrix (gate,
+// up) one box of the stage's P chunks x R rows for the codes ([chunk][row],
+// 128-byte swizzled lines, 1024-aligned), then the scales (then the mins and
+// the Q5 plane), and the 3-D tensor maps that load them. box_tx is a whole
+// stage; st the bytes the layout uses.
+qg_status chain_layout(CcArgs& a, const qg_gemv_op& g, int fmt, int ufmt, int ngu, bool sep_up, CUtensorMap* maps,
+                       uint32_t& st)
+{
+    const uint32_t PR = static_cast<uint32_t>(a.P * a.R), nm = static_cast<uint32_t>(ngu);
+    a.code_pitch = align_up(PR * 128u, 1024);
+    a.sc_pitch = align_up(PR * 16u, 128);
+    a.scales_off = nm * a.code_pitch;
+    if (fmt == FMT_NVFP4) {
+        st = a.scales_off + nm * a.sc_pitch;
+        a.box_tx = nm * PR * (128u + 16u);
+    } else {
+        const bool any5 = fmt == FMT_Q5 || ufmt == FMT_Q5;
+        a.mins_off = align_up(a.scales_off + nm * a.sc_pitch, 1024);
+        a.hi_off = align_up(a.mins_off + nm * a.sc_pitch, 1024);
+        st = a.hi_off + (any5 ? nm * 2u * a.sc_pitch : 0u);
+        a.box_tx = PR * (128u + 16u + 16u + (fmt == FMT_Q5 ? 32u : 0u));
+        if (ngu == 2) a.box_tx += PR * (128u + 16u + 16u + (ufmt == FMT_Q5 ? 32u : 0u));
+    }
+    const uint64_t rows = static_cast<uint64_t>(g.N), C = static_cast<uint64_t>(a.C);
+    const uint32_t Rb = static_cast<uint32_t>(a.R), Pb = static_cast<uint32_t>(a.P);
+    if (!encode_tmap_chunks(&maps[0], g.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, rows, C, Rb, Pb, true))
+        return QG_ERR_CUDA;
+    if (fmt == FMT_NVFP4)
+        return encode_tmap_chunks(&maps[1], g.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 16, rows, C, Rb, Pb, false)
+                   ? QG_OK
+                   : QG_ERR_CUDA;
+    const void* srcs[2][4] = {{g.codes, g.scales, g.mins, g.q_hi}, {g.up_codes, g.up_scales, g.up_mins, g.up_q_hi}};
+    const int fm[2] = {fmt, ufmt};
+    for (int gg = 0; gg < (sep_up ? 2 : 1); ++gg) {
+        CUtensorMap* mm = &maps[4 * gg];
+        if ((gg == 1 &&
+             !encode_tmap_chunks(&mm[0], srcs[gg][0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, rows, C, Rb, Pb, true)) ||
+            !encode_tmap_chunks(&mm[1], srcs[gg][1], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, 8, rows, C, Rb, Pb, false) ||
+            !encode_tmap_chunks(&mm[2], srcs[gg][2], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, 8, rows, C, Rb, Pb, false))
+            return QG_ERR_CUDA;
+        if (fm[gg] == FMT_Q5 &&
+            !encode_tmap_chunks(&mm[3], srcs[gg][3], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 32, rows, C, Rb, Pb, false))
+            return QG_ERR_CUDA;
+    }
+    return QG_OK;
+}
+
 // 3..8 tokens: every op on the warp-MMA stage (its plan: R for equal bytes per
 // SM, boxes padded to 16-row blocks, at most 16 blocks per stage), the
 // activations of each op held a window of chunks at a time.
@@ -839,52 +876,13 @@ qg_status launch_chain_mt(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
         a.out_f32 = op.epi == EPI_SWIGLU ? 0 : (g.y_dtype == QG_OUT_F32 ? 1 : 0);
         a.g = op.fmt == FMT_NVFP4 ? g.global_scale : 1.f;
         const uint32_t nbox = static_cast<uint32_t>(a.P * ngu);
-        a.scales_off = nbox * a.R8 * 128u;
-        uint32_t st;
-        if (op.fmt == FMT_NVFP4) {
-            st = a.scales_off + nbox * a.R8 * 16u;
-            a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
-        } else {
-            const bool any5 = op.fmt == FMT_Q5 || op.ufmt == FMT_Q5;
-            a.mins_off = a.scales_off + nbox * a.R8 * 16u;
-            a.hi_off = a.mins_off + nbox * a.R8 * 16u;
-            st = a.hi_off + (any5 ? nbox * a.R8 * 32u : 0u);
-            // bytes one phase brings in: its gate (or only) box and a SwiGLU's up box
-            a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (op.fmt == FMT_Q5 ? 32u : 0u));
-            if (ngu == 2)
-                a.box_tx += static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (op.ufmt == FMT_Q5 ? 32u : 0u));
-        }
-        slot_bytes = std::max(slot_bytes, align_up(st, 1024));
+        (void)nbox;
+        uint32_t st = 0;
+        const qg_status ls = chain_layout(a, g, op.fmt, op.ufmt, ngu, g.up_codes != nullptr, p.map[o], st);
+        if (ls != QG_OK) return ls;
+        // + 2 KB: a thread's or warp's last rows read up to 15 lines past its box
+        slot_bytes = std::max(slot_bytes, align_up(st + 2048u, 1024));
         red_max = std::max(red_max, nbox * a.R8 * 8u);
-        const int rows = g.N;
-        if (!encode_tmap_2d(&p.map[o][0], g.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 2, rows, 128, R, true))
-            return QG_ERR_CUDA;
-        if (op.fmt == FMT_NVFP4) {
-            if (!encode_tmap_2d(&p.map[o][1], g.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 16, rows, 16, R,
-                                false))
-                return QG_ERR_CUDA;
-        } else {
-            if (!encode_tmap_2d(&p.map[o][1], g.scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8, R,
-                                false) ||
-                !encode_tmap_2d(&p.map[o][2], g.mins, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8, R,
-                                false))
-                return QG_ERR_CUDA;
-            if (op.fmt == FMT_Q5 &&
-                !encode_tmap_2d(&p.map[o][3], g.q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 8, rows, 32, R, false))
-                return QG_ERR_CUDA;
-            if (sep_up) {
-                if (!encode_tmap_2d(&p.map[o][4], g.up_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 2, rows, 128,
-                                    R, true) ||
-                    !encode_tmap_2d(&p.map[o][5], g.up_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8,
-                                    R, false) ||
-                    !encode_tmap_2d(&p.map[o][6], g.up_mins, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8,
-                                    R, false))
-                    return QG_ERR_CUDA;
-                if (op.ufmt == FMT_Q5 && !encode_tmap_2d(&p.map[o][7], g.up_q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                                                         g.K / 8, rows, 32, R, false))
-                    return QG_ERR_CUDA;
-            }
-        }
     }
     if (any_dep && !sync) return QG_ERR_INVALID_ARG;
     // shared memory: ring | activation window | 2^-prescale | flags | sums of
@@ -1043,54 +1041,14 @@ qg_status launch_chain(const qg_gemv_op* ops, int n_ops, int M, uint32_t* sync, 
         a.out_f32 = op.epi == EPI_SWIGLU ? 0 : (g.y_dtype == QG_OUT_F32 ? 1 : 0);
         a.g = op.fmt == FMT_NVFP4 ? g.global_scale : 1.f;
         const uint32_t nbox = static_cast<uint32_t>(a.P * ngu);
-        a.scales_off = nbox * a.R8 * 128u;
-        uint32_t st;
-        if (op.fmt == FMT_NVFP4) {
-            st = a.scales_off + nbox * a.R8 * 16u;
-            a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
-        } else {
-            const bool any5 = op.fmt == FMT_Q5 || op.ufmt == FMT_Q5;
-            a.mins_off = a.scales_off + nbox * a.R8 * 16u;
-            a.hi_off = a.mins_off + nbox * a.R8 * 16u;
-            st = a.hi_off + (any5 ? nbox * a.R8 * 32u : 0u);
-            // bytes one phase brings in: its gate (or only) box and a SwiGLU's up box
-            a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (op.fmt == FMT_Q5 ? 32u : 0u));
-            if (ngu == 2) a.box_tx += static_cast<uint32_t>(a.R) * (128u + 16u + 16u + (op.ufmt == FMT_Q5 ? 32u : 0u));
-        }
-        slot_bytes = std::max(slot_bytes, align_up(st, 1024));
+        (void)nbox;
+        uint32_t st = 0;
+        const qg_status ls = chain_layout(a, g, op.fmt, op.ufmt, ngu, g.up_codes != nullptr, p.map[o], st);
+        if (ls != QG_OK) return ls;
+        // + 2 KB: a thread's or warp's last rows read up to 15 lines past its box
+        slot_bytes = std::max(slot_bytes, align_up(st + 2048u, 1024));
         c_max = std::max(c_max, a.C);
         red_max = std::max(red_max, static_cast<int>(nbox) * a.R8);
-        // tensor maps: the standalone kernels' boxes
-        const int rows = g.N;
-        const int R = a.R;
-        if (!encode_tmap_2d(&p.map[o][0], g.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 2, rows, 128, R, true))
-            return QG_ERR_CUDA;
-        if (op.fmt == FMT_NVFP4) {
-            if (!encode_tmap_2d(&p.map[o][1], g.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 16, rows, 16, R,
-                                false))
-                return QG_ERR_CUDA;
-        } else {
-            if (!encode_tmap_2d(&p.map[o][1], g.scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8, R,
-                                false) ||
-                !encode_tmap_2d(&p.map[o][2], g.mins, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8, R,
-                                false))
-                return QG_ERR_CUDA;
-            if (op.fmt == FMT_Q5 &&
-                !encode_tmap_2d(&p.map[o][3], g.q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 8, rows, 32, R, false))
-                return QG_ERR_CUDA;
-            if (sep_up) {
-                if (!encode_tmap_2d(&p.map[o][4], g.up_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.K / 2, rows, 128,
-                                    R, true) ||
-                    !encode_tmap_2d(&p.map[o][5], g.up_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8,
-                                    R, false) ||
-                    !encode_tmap_2d(&p.map[o][6], g.up_mins, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, g.K / 32, rows, 8,
-                                    R, false))
-                    return QG_ERR_CUDA;
-                if (op.ufmt == FMT_Q5 && !encode_tmap_2d(&p.map[o][7], g.up_q_hi, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                                                         g.K / 8, rows, 32, R, false))
-                    return QG_ERR_CUDA;
-            }
-        }
     }
     if (any_dep && !sync) return QG_ERR_INVALID_ARG;
     // shared memory: ring | activations | 2^-prescale | flags | sums of x |
