@@ -250,38 +250,37 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
         __syncwarp();
         int slot = 0, lap = 0, issued = 0;
         bool stop = false;
+        // the plan in registers (a parameter read after each copy's memory
+        // clobber would be repeated every stage)
+        const int P = a.P, Cp = a.Cp, up_off = a.up_row_offset, n_stages = a.n_stages, starve = a.starve;
+        const uint32_t code_pitch = a.code_pitch, sc_pitch = a.sc_pitch, scales_off = a.scales_off;
+        const uint32_t box_tx = a.box_tx, stage_bytes = a.stage_bytes, smem_ring = a.smem_ring;
         for (int i = 0; i < n_local && !stop; ++i) {
             const int w_row0 = sp[i].w_row0;
-            for (int c = 0; c < a.Cp; ++c) {
+            for (int c = 0; c < Cp; ++c) {
                 if (lap > 0 && !cc_wait_warp(&empty[slot], (lap - 1) & 1, a, abort_flag)) {
                     stop = true;
                     break;
                 }
-                if (*abort_flag || a.starve) {
+                if (*abort_flag || starve) {
                     stop = true;
                     break;
                 }
-                int live = 0;
-                for (int pp = 0; pp < a.P; ++pp) live += (c * a.P + pp < a.C) ? 1 : 0;
-                uint8_t* sb = smem + a.smem_ring + slot * a.stage_bytes;
+                uint8_t* sb = smem + smem_ring + slot * stage_bytes;
                 if (elect_one()) {
-                    mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(live * NGU) * a.box_tx);
-                    for (int pp = 0; pp < a.P; ++pp) {
-                        const int kc = c * a.P + pp;
-                        if (kc >= a.C) continue;
+                    // per matrix (gate, up) one box of the stage's P chunks x R
+                    // rows (chunks past K are filled with zeros and counted)
+                    mbar_arrive_expect_tx(&full[slot], box_tx);
 #pragma unroll
-                        for (int gg = 0; gg < NGU; ++gg) {
-                            const int b2 = pp * NGU + gg;
-                            const int row = w_row0 + gg * a.up_row_offset;
-                            tma_load_2d(sb + b2 * a.R8 * 128, &tm_codes, kc * (kChunkK / 2), row, &full[slot]);
-                            tma_load_2d(sb + a.scales_off + b2 * a.R8 * 16, &tm_scales, kc * (kChunkK / 16), row,
-                                        &full[slot]);
-                        }
+                    for (int gg = 0; gg < NGU; ++gg) {
+                        const int row = w_row0 + gg * up_off;
+                        tma_load_3d(sb + gg * code_pitch, &tm_codes, 0, row, c * P, &full[slot]);
+                        tma_load_3d(sb + scales_off + gg * sc_pitch, &tm_scales, 0, row, c * P, &full[slot]);
                     }
                 }
                 __syncwarp();
                 ++issued;
-                if (++slot == a.n_stages) {
+                if (++slot == n_stages) {
                     slot = 0;
                     ++lap;
                 }
@@ -361,7 +360,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
     named_barrier_sync(1, kCcThreads);
     if (static_cast<int>(threadIdx.x) >= n_act) return;  // no rows: not waiting on every stage
 
-    const CcGeom geom = cc_geom(a);
+    const CcGeom geom = cc_geom_chunked(a, NGU == 2 ? 1 : 0);
     const int rg_per_box = (a.R + kCcRows - 1) / kCcRows;
     const int seg = threadIdx.x % NSEG;
     const int bg = threadIdx.x / NSEG;
@@ -490,10 +489,15 @@ qg_status launch_cc_moe(const uint8_t* codes, const uint8_t* scales, int total_r
     m.max_local = max_local;
     m.max_rows = max_rows;
 
+    // the chunked stage layout: per matrix one [chunk][row] box of P chunks x
+    // R rows (codes: 128-byte swizzled lines), then the scales
     const uint32_t nbox = static_cast<uint32_t>(a.P * ngu);
-    a.scales_off = nbox * a.R8 * 128u;
-    a.stage_bytes = align_up(a.scales_off + nbox * a.R8 * 16u, 1024);
-    a.box_tx = static_cast<uint32_t>(a.R) * (128u + 16u);
+    const uint32_t PR = static_cast<uint32_t>(a.P * a.R);
+    a.code_pitch = align_up(PR * 128u, 1024);
+    a.sc_pitch = align_up(PR * 16u, 128);
+    a.scales_off = static_cast<uint32_t>(ngu) * a.code_pitch;
+    a.stage_bytes = align_up(a.scales_off + static_cast<uint32_t>(ngu) * a.sc_pitch, 1024);
+    a.box_tx = static_cast<uint32_t>(ngu) * PR * (128u + 16u);
     const uint32_t items = static_cast<uint32_t>(max_rows * a.C);
     const uint32_t x_bytes = items * kChunkK * 2u;
     const uint32_t pe_bytes = align_up(items * 4u, 16);
@@ -527,8 +531,8 @@ qg_status launch_cc_moe(const uint8_t* codes, const uint8_t* scales, int total_r
     CUtensorMap tmc, tms;
     memset(&tmc, 0, sizeof(tmc));
     memset(&tms, 0, sizeof(tms));
-    if (!encode_tmap_2d(&tmc, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, total_rows, 128, R, true) ||
-        !encode_tmap_2d(&tms, scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 16, total_rows, 16, R, false))
+    if (!encode_tmap_chunks(&tmc, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, total_rows, a.C, R, a.P, true) ||
+        !encode_tmap_chunks(&tms, scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 16, total_rows, a.C, R, a.P, false))
         return QG_ERR_CUDA;
 
     auto kern = swiglu ? moe_cc_kernel<EPI_SWIGLU> : moe_cc_kernel<EPI_NONE>;
