@@ -50,7 +50,6 @@ constexpr uint32_t kWsTrailNv = 48;     // 2^-prescale x 8, bf16 flag, pad
 constexpr uint32_t kWsTrailQ = 48 + 256;  // + sums of the 8 groups of 32, x 8 tokens
 constexpr int kWsMaxXStages = 4;        // activation ring slots at most
 constexpr int kWsMaxPhases = 5;         // chunks per stage (each brings M x 576 bytes of activations)
-constexpr int kWsConvWarps = 4;          // conversion kernel: warps per CTA (fits beside a layer CTA)
 
 struct WsOp {
     CcArgs a;         // the op's plan (16-row blocks), as qgemv_chain.cu's 3..8-token path
@@ -160,48 +159,94 @@ __device__ __forceinline__ void ws_convert_chunk(const uint16_t* x, int K, int M
     if (lane == 0) *reinterpret_cast<uint32_t*>(blk + trail + 32) = inexact ? 1u : 0u;
 }
 
-// The ops without after_previous: blockIdx.y is the op, each warp one chunk.
-// With the RMSNorm prologue each CTA first takes every token's r over all of
-// K in the canonical order (chunk sums of squares, added in k order).
-__global__ void __launch_bounds__(32 * kWsConvWarps) chain_ws_convert_kernel(const __grid_constant__ WsParams p)
+// The ops without after_previous: blockIdx.y is the op, blockIdx.x the
+// chunk, warp t token t (one load round per warp, so the kernel is one
+// memory latency long). The tokens agree on the chunk's bf16 flag through
+// shared memory; every other step is ws_convert_chunk's, per token, so the
+// blocks are the same. With the RMSNorm prologue warp t first takes its
+// token's r over all of K in the canonical order (chunk sums of squares,
+// added in k order).
+__global__ void __launch_bounds__(32 * kMtTokens) chain_ws_convert_kernel(const __grid_constant__ WsParams p)
 {
-    extern __shared__ float ws_ss[];  // M x C chunk sums, then M factors
+    __shared__ int s_inexact;
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const WsOp& op = p.op[blockIdx.y];
     const CcArgs& a = op.a;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kc = blockIdx.x * kWsConvWarps + warp;
-    if (op.dep || static_cast<int>(blockIdx.x) * kWsConvWarps >= a.C) return;
-    const int M = p.M;
-    uint8_t* blk = p.ws + op.ws_off + static_cast<size_t>(kc) * op.blk;
-    const bool q = op.fmt != FMT_NVFP4;
-    if (a.norm_w != nullptr) {
-        const int items = M * a.C;
-        for (int it = warp; it < items; it += kWsConvWarps) {
-            const float v = rms_chunk_ss(ldg_nc_128(a.x + static_cast<size_t>(it / a.C) * a.K +
-                                                    static_cast<size_t>(it % a.C) * kChunkK + lane * 8));
-            if (lane == 0) ws_ss[it] = v;
+    const int t = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kc = blockIdx.x;
+    if (op.dep || kc >= a.C) return;
+    const int M = p.M, K = a.K;
+    const bool tok = t < M;
+    if (threadIdx.x == 0) s_inexact = 0;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (tok) raw = ldg_nc_128(a.x + static_cast<size_t>(t) * K + static_cast<size_t>(kc) * kChunkK + lane * 8);
+    if (tok && a.norm_w != nullptr) {
+        float ss = 0.f;
+        constexpr int U = 8;
+        for (int c0 = 0; c0 < a.C; c0 += U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                v[u] = c0 + u < a.C ? ldg_nc_128(a.x + static_cast<size_t>(t) * K +
+                                                 static_cast<size_t>(c0 + u) * kChunkK + lane * 8)
+                                    : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (c0 + u < a.C) ss += rms_chunk_ss(v[u]);
         }
-        __syncthreads();
-        if (static_cast<int>(threadIdx.x) < M) {
-            float s = 0.f;
-            for (int c = 0; c < a.C; ++c) s += ws_ss[threadIdx.x * a.C + c];
-            ws_ss[items + threadIdx.x] = rms_factor(s, a.K, a.norm_eps);
-        }
-        __syncthreads();
-        if (kc >= a.C) return;
-        if (q)
-            ws_convert_chunk<true, false, true>(a.x, a.K, M, kc, a.norm_w, ws_ss + items, blk, lane);
-        else
-            ws_convert_chunk<false, false, true>(a.x, a.K, M, kc, a.norm_w, ws_ss + items, blk, lane);
-        return;
+        const uint4 gam = ldg_nc_128(a.norm_w + static_cast<size_t>(kc) * kChunkK + lane * 8);
+        raw = rms_apply8(raw, gam, rms_factor(ss, K, a.norm_eps));
     }
-    if (kc >= a.C) return;
-    if (q)
-        ws_convert_chunk<true, false, false>(a.x, a.K, M, kc, nullptr, nullptr, blk, lane);
-    else
-        ws_convert_chunk<false, false, false>(a.x, a.K, M, kc, nullptr, nullptr, blk, lane);
+    const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+    int e = 0;
+    bool inexact = false;
+    if (tok) {
+        uint32_t mx2 = 0, mn2 = 0xFFFFFFFFu;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) bf16_range_acc(wv[i], mx2, mn2);
+        uint32_t emax, emin, magmax;
+        bf16_range_fin(mx2, mn2, emax, emin, magmax);
+        emax = __reduce_max_sync(0xffffffffu, emax);
+        emin = __reduce_min_sync(0xffffffffu, emin);
+        if (emax == 0u) magmax = __reduce_max_sync(0xffffffffu, magmax);
+        e = min(emax != 0u ? 141 - static_cast<int>(emax) : prescale_exponent(magmax), 126);
+        inexact = emin != 255u && static_cast<int>(emin) - 127 + e < -17;
+    }
+    __syncthreads();
+    if (inexact && lane == 0) atomicOr(&s_inexact, 1);
+    __syncthreads();
+    inexact = s_inexact != 0;
+    uint8_t* blk = p.ws + op.ws_off + static_cast<size_t>(kc) * op.blk;
+    const uint32_t trail = static_cast<uint32_t>(M) * kWsTokStride;
+    if (t == 0 && lane == 0) *reinterpret_cast<uint32_t*>(blk + trail + 32) = inexact ? 1u : 0u;
+    if (!tok) return;
+    uint32_t o[4];
+    if (inexact) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = wv[i];
+    } else {
+        const float sc = __int_as_float((127 + e) << 23);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = pack_f16x2(__uint_as_float(wv[i] << 16) * sc, __uint_as_float(wv[i] & 0xFFFF0000u) * sc);
+    }
+    if (op.fmt != FMT_NVFP4) {
+        float sx = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sx += bf16_bits_to_f32((i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu));
+        sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+        sx += __shfl_xor_sync(0xffffffffu, sx, 2);
+        if ((lane & 3) == 0) reinterpret_cast<float*>(blk + trail + 48)[t * 8 + (lane >> 2)] = sx;
+        const uint32_t p0 = __byte_perm(o[0], o[2], 0x5410), p1 = __byte_perm(o[0], o[2], 0x7632);
+        const uint32_t p2 = __byte_perm(o[1], o[3], 0x5410), p3 = __byte_perm(o[1], o[3], 0x7632);
+        o[0] = p0;
+        o[1] = p1;
+        o[2] = p2;
+        o[3] = p3;
+    }
+    *reinterpret_cast<uint4*>(blk + t * kWsTokStride + lane * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+    if (lane == 0) reinterpret_cast<float*>(blk + trail)[t] = inexact ? 1.0f : __int_as_float((127 - e) << 23);
 }
 
 __device__ __forceinline__ uint32_t ws_ld_acquire(const uint32_t* p)
@@ -678,7 +723,7 @@ qg_status launch_chain_ws(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
     p.M = M;
     bool any_dep = false, any_q = false, any_indep = false;
     uint32_t slot_bytes = 0, xslot_bytes = 0, red_max = 0;
-    int c_max = 0, c_norm_max = 0;
+    int c_max = 0;
     size_t ws_off = 0;
     for (int o = 0; o < n_ops; ++o) {
         const qg_gemv_op& g = ops[o];
@@ -710,7 +755,6 @@ qg_status launch_chain_ws(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
         a.K = g.K;
         a.C = g.K / kChunkK;
         c_max = std::max(c_max, a.C);
-        if (g.norm_weight) c_norm_max = std::max(c_norm_max, a.C);
         a.n_out = n_out;
         a.R = R;
         a.R8 = (R + 15) / 16 * 16;
@@ -827,23 +871,19 @@ qg_status launch_chain_ws(const qg_gemv_op* ops, int n_ops, int M, uint32_t* syn
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     // 1. the ops without after_previous: their activation blocks
     if (any_indep) {
-        const uint32_t conv_smem = static_cast<uint32_t>(M * (c_norm_max + 1)) * 4u;
         static bool conv_attr[64] = {};
         if (!conv_attr[dev]) {
             // the layer kernel's shared-memory split: an SM that runs a
             // conversion CTA then takes a layer CTA without reconfiguring
-            if (cudaFuncSetAttribute(chain_ws_convert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     48 * 1024) != cudaSuccess ||
-                cudaFuncSetAttribute(chain_ws_convert_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+            if (cudaFuncSetAttribute(chain_ws_convert_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared) != cudaSuccess)
                 return QG_ERR_CUDA;
             conv_attr[dev] = true;
         }
-        if (conv_smem > 48u * 1024u) return QG_ERR_UNSUPPORTED;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((c_max + kWsConvWarps - 1) / kWsConvWarps, n_ops);
-        cfg.blockDim = dim3(32 * kWsConvWarps);
-        cfg.dynamicSmemBytes = conv_smem;
+        cfg.gridDim = dim3(c_max, n_ops);
+        cfg.blockDim = dim3(32 * kMtTokens);
+        cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
         cfg.attrs = pdl;
         cfg.numAttrs = 1;
